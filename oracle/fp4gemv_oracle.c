@@ -1,0 +1,429 @@
+/*
+ * fp4gemv_oracle.c -- FP64 CPU oracle for the NVFP4 small-M GEMV family.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the independent reference that the
+ * CUDA library is checked against.  Only tests/, __graft_entry__.smoke() and
+ * the cpu_baseline leg of bench.py may load it.  It shares no code, header,
+ * table or constant with the CUDA path.
+ *
+ * Everything here is a plain, slow, direct transcription of what the pages
+ * define (cited per function as "page / section"):
+ *   [nvfp4_gemv]   vllm.models.flint.ops.nvfp4_gemv, module docstring and the
+ *                  nvfp4_gemv / bf16_gemv / dequantize_rows sections.
+ *   [linear]       vllm.models.flint.ops.linear, _dequant_gemm and
+ *                  _swizzled_scale_buffer sections.
+ *   [moe_gemv]     vllm.models.flint.ops.moe_gemv, module docstring and the
+ *                  gate_up / down_combine sections.
+ *
+ * Arithmetic: products and sums in double (every product of a bf16 activation
+ * and an exactly-dequantised weight has <= 14 significant bits, so products
+ * are exact; sums carry at most K * 2^-53 relative error).  The final and
+ * intermediate roundings the pages name (fp32 scale, bf16 outputs) are done
+ * explicitly, each as ONE rounding from the double value (no double rounding
+ * through float on the way to bf16).
+ *
+ * Rounding windows: where the pages round an intermediate to bf16 (the gate /
+ * up outputs before silu_mul, y_j, y_shared and the top-k sum in
+ * down_combine), an fp32-accumulating implementation may legitimately land on
+ * the other side of a bf16 rounding boundary.  Every such intermediate is
+ * carried as an interval [lo, hi] obtained by rounding (v - err) and
+ * (v + err), where err bounds the fp32 accumulation error of the exact value
+ * v.  Final outputs are reported as (nominal, lo, hi); lo == hi == nominal
+ * whenever no intermediate is ambiguous.
+ *
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared (no fast-math).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------ */
+/* Number formats                                                            */
+/* ------------------------------------------------------------------------ */
+
+/* E2M1 magnitudes indexed by the low three code bits (e1 e0 m): the FP4
+ * format of the NVFP4 weight codes [nvfp4_gemv, module docstring].  Sign is
+ * code bit 3. */
+static const double E2M1_MAG[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+
+double orc_e2m1(int code)
+{
+    double m = E2M1_MAG[code & 7];
+    return (code & 8) ? -m : m;
+}
+
+/* float8_e4m3fn from its bit fields (the dtype the pages view the block
+ * scales as [nvfp4_gemv, dequantize_rows]): 1 sign, 4 exponent (bias 7),
+ * 3 mantissa bits, no infinities, S.1111.111 is NaN. */
+double orc_e4m3(int b)
+{
+    int s = (b >> 7) & 1, E = (b >> 3) & 15, M = b & 7;
+    double v;
+    if (E == 15 && M == 7) return NAN;
+    if (E == 0) v = ldexp((double)M / 8.0, -6);
+    else        v = ldexp(1.0 + (double)M / 8.0, E - 7);
+    return s ? -v : v;
+}
+
+static double bf16_to_double(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+double orc_bf16_value(int h) { return bf16_to_double((uint16_t)h); }
+
+/* Round a double to bf16 (8 significant bits, 8-bit exponent) in ONE step,
+ * round-to-nearest-even, with gradual underflow and overflow to infinity. */
+uint16_t orc_bf16_rne(double v)
+{
+    uint16_t sign = signbit(v) ? 0x8000u : 0u;
+    double a = fabs(v), q, n, r, res;
+    int ex, lead;
+    float f;
+    uint32_t u;
+    if (isnan(v)) return (uint16_t)(sign | 0x7FC0u);
+    if (isinf(v)) return (uint16_t)(sign | 0x7F80u);
+    if (a == 0.0) return sign;
+    frexp(a, &ex);                 /* a = f * 2^ex, f in [0.5, 1) */
+    lead = ex - 1;                 /* exponent of the leading bit */
+    if (lead < -126) lead = -126;  /* subnormal binade shares the min quantum */
+    q = ldexp(1.0, lead - 7);      /* one bf16 ulp in this binade */
+    n = a / q;                     /* exact: power-of-two scaling */
+    r = nearbyint(n);              /* default mode: ties to even */
+    res = r * q;
+    if (res >= ldexp(1.0, 128)) return (uint16_t)(sign | 0x7F80u);
+    f = (float)res;                /* exact: res is a bf16 value */
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(sign | ((u >> 16) & 0x7FFFu));
+}
+
+/* Round a double to fp32 (one step, ties to even). */
+static double f32(double v) { return (double)(float)v; }
+
+/* ------------------------------------------------------------------------ */
+/* 128x4-swizzled block-scale layout                                         */
+/* ------------------------------------------------------------------------ */
+
+static int64_t roundup(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
+
+/* Bytes of the flat scale buffer for a [rows, K] weight: the size formula of
+ * _swizzled_scale_buffer [linear]. */
+int64_t orc_scale_bytes(int64_t rows, int64_t K)
+{
+    return roundup(rows, 128) * roundup(K / 16, 4);
+}
+
+/* Byte offset of the scale of (row r, 16-wide K block kb).  Reading of the
+ * "128x4" layout (the pages give only its name and size): rows are padded to
+ * 128 and K blocks to 4; each (128-row, 4-block) tile is one 512-byte chunk,
+ * chunks ordered K-block-group fastest within a 128-row group; inside a chunk
+ * the byte index is (r % 32) * 16 + ((r % 128) / 32) * 4 + kb % 4. */
+int64_t orc_swz(int64_t r, int64_t kb, int64_t K)
+{
+    int64_t kbp = roundup(K / 16, 4);
+    return ((r / 128) * (kbp / 4) + kb / 4) * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4 + kb % 4;
+}
+
+/* Inverse of orc_swz for offsets inside the used region (row < roundup(rows,
+ * 128), kb < roundup(K/16, 4)): writes r, kb. */
+void orc_unswz(int64_t off, int64_t K, int64_t* r, int64_t* kb)
+{
+    int64_t kbp = roundup(K / 16, 4);
+    int64_t chunk = off / 512, in = off % 512;
+    int64_t rg = chunk / (kbp / 4), kg = chunk % (kbp / 4);
+    *r = rg * 128 + ((in / 4) % 4) * 32 + in / 16;
+    *kb = kg * 4 + in % 4;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Dequantisation                                                            */
+/* ------------------------------------------------------------------------ */
+
+/* code(W, n, k): element 2j is the LOW nibble of byte j [nvfp4_gemv, module
+ * docstring: "two E2M1 codes per byte, low nibble first"]. */
+static int fp4_code(const uint8_t* wrow, int64_t k)
+{
+    uint8_t b = wrow[k / 2];
+    return (k & 1) ? (b >> 4) : (b & 0xF);
+}
+
+/* Wd[r, k] = e2m1(code) * e4m3(scale(r, k/16)), exact in double and in bf16
+ * [nvfp4_gemv, module docstring "dequantized exactly to BF16 (e2m1 * e4m3)"]. */
+static void dequant_row(const uint8_t* w, const uint8_t* sf, int64_t r, int64_t K, double* out)
+{
+    const uint8_t* wrow = w + r * (K / 2);
+    for (int64_t k = 0; k < K; ++k) {
+        double s = orc_e4m3(sf[orc_swz(r, k / 16, K)]);
+        out[k] = orc_e2m1(fp4_code(wrow, k)) * s;
+    }
+}
+
+/* dequantize_rows [nvfp4_gemv, dequantize_rows]: bf16 [rows, K] of the exact
+ * products, global scale not applied.  Rows r0..r1-1 are written. */
+void orc_dequant_rows(const uint8_t* w, const uint8_t* sf, int64_t K, int64_t r0, int64_t r1,
+                      double* tmp, uint16_t* out)
+{
+    for (int64_t r = r0; r < r1; ++r) {
+        dequant_row(w, sf, r, K, tmp);
+        for (int64_t k = 0; k < K; ++k) out[r * K + k] = orc_bf16_rne(tmp[k]);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Dot products                                                              */
+/* ------------------------------------------------------------------------ */
+
+/* acc = sum_k x[k] * wd[k] in double; abs = sum_k |x[k] * wd[k]|. */
+static void dot(const uint16_t* x, const double* wd, int64_t K, double* acc, double* abs_)
+{
+    double a = 0.0, b = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        double p = bf16_to_double(x[k]) * wd[k];
+        a += p;
+        b += fabs(p);
+    }
+    *acc = a;
+    *abs_ = b;
+}
+
+/* Bound on |fp32-accumulated sum - exact sum| for a K-term sum accumulated
+ * in fp32 16 terms at a time, plus a handful of extra partial-sum additions
+ * (split-K reductions).  Used only to open rounding windows. */
+static double acc_err(double abs_, int64_t K)
+{
+    return 4.0 * ((double)(K / 16) + 32.0) * ldexp(1.0, -24) * abs_;
+}
+
+/* Dense NVFP4 accumulators for rows in `rows[0..nrows)`: acc[m * nrows + i]
+ * = sum_k x[m, k] * Wd[rows[i], k] [nvfp4_gemv, nvfp4_gemv]. */
+void orc_gemv_acc(const uint16_t* x, int64_t ldx, int64_t M, const uint8_t* w, const uint8_t* sf,
+                  int64_t K, const int64_t* rows, int64_t nrows, double* tmp, double* acc,
+                  double* absacc)
+{
+    for (int64_t i = 0; i < nrows; ++i) {
+        dequant_row(w, sf, rows[i], K, tmp);
+        for (int64_t m = 0; m < M; ++m) dot(x + m * ldx, tmp, K, &acc[m * nrows + i], &absacc[m * nrows + i]);
+    }
+}
+
+/* Dense BF16-weight accumulators [nvfp4_gemv, bf16_gemv]: W is bf16 [N, K]. */
+void orc_bf16_gemv_acc(const uint16_t* x, int64_t ldx, int64_t M, const uint16_t* w, int64_t K,
+                       const int64_t* rows, int64_t nrows, double* tmp, double* acc, double* absacc)
+{
+    for (int64_t i = 0; i < nrows; ++i) {
+        for (int64_t k = 0; k < K; ++k) tmp[k] = bf16_to_double(w[rows[i] * K + k]);
+        for (int64_t m = 0; m < M; ++m) dot(x + m * ldx, tmp, K, &acc[m * nrows + i], &absacc[m * nrows + i]);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Epilogues                                                                 */
+/* ------------------------------------------------------------------------ */
+
+/* Next / previous bf16 bit pattern in value order (finite, non-NaN). */
+static uint16_t bf16_next_up(uint16_t h)
+{
+    if (h == 0x8000u) return 0x0000u;
+    return (h & 0x8000u) ? (uint16_t)(h - 1) : (uint16_t)(h + 1);
+}
+
+static int bf16_le(uint16_t a, uint16_t b) { return bf16_to_double(a) <= bf16_to_double(b); }
+
+/* y = bf16(f32(f32(acc) * s)), with its rounding window [lo, hi]
+ * [nvfp4_gemv, module docstring: "the FP32 global scale is applied to the
+ * FP32 accumulator before the single output rounding to BF16"]. */
+static void scaled_out(double acc, double abs_, int64_t K, double s, uint16_t* nom, uint16_t* lo,
+                       uint16_t* hi)
+{
+    double v = f32(f32(acc) * s);
+    double e = acc_err(abs_, K) * fabs(s) + ldexp(fabs(v), -22);
+    *nom = orc_bf16_rne(v);
+    *lo = orc_bf16_rne(v - e);
+    *hi = orc_bf16_rne(v + e);
+}
+
+/* SiLU evaluated exactly (double): x / (1 + exp(-x)). */
+static double silu(double g) { return g / (1.0 + exp(-g)); }
+
+/* silu_mul of two bf16 intervals: out = bf16(silu(G) * U) for every G in
+ * [glo, ghi], U in [ulo, uhi] (bf16 grid points), with a small fp32
+ * evaluation allowance; returns nominal (from gn, un) and the hull. */
+static void silu_mul_interval(uint16_t gn, uint16_t glo, uint16_t ghi, uint16_t un, uint16_t ulo,
+                              uint16_t uhi, uint16_t* nom, uint16_t* lo, uint16_t* hi)
+{
+    double vn = silu(bf16_to_double(gn)) * bf16_to_double(un);
+    double vmin = INFINITY, vmax = -INFINITY;
+    int ng = 0;
+    *nom = orc_bf16_rne(vn);
+    for (uint16_t g = glo;; g = bf16_next_up(g)) {
+        int nu = 0;
+        for (uint16_t u = ulo;; u = bf16_next_up(u)) {
+            double v = silu(bf16_to_double(g)) * bf16_to_double(u);
+            double e = ldexp(fabs(v), -20) + ldexp(1.0, -140);
+            if (v - e < vmin) vmin = v - e;
+            if (v + e > vmax) vmax = v + e;
+            if (u == uhi || ++nu > 64) break;
+        }
+        if (g == ghi || ++ng > 64) break;
+    }
+    *lo = orc_bf16_rne(vmin);
+    *hi = orc_bf16_rne(vmax);
+    if (!bf16_le(*lo, *nom)) *lo = *nom;
+    if (!bf16_le(*nom, *hi)) *hi = *nom;
+}
+
+/* Dense epilogue [nvfp4_gemv, nvfp4_gemv "silu_mul"]:
+ *   silu == 0: out[m, i] = bf16(f32(f32(acc) * gs)), i over nrows.
+ *   silu != 0: the accumulators hold gate rows in columns [0, half) and the
+ *   matching up rows in [half, 2 half); G, U are the bf16 outputs and
+ *   out[m, i] = bf16(silu(G) * U) ("exact SiLU, one BF16 rounding"). */
+void orc_dense_epilogue(const double* acc, const double* absacc, int64_t M, int64_t ncols, int64_t K,
+                        double gs, int silu_mul, uint16_t* nom, uint16_t* lo, uint16_t* hi)
+{
+    if (!silu_mul) {
+        for (int64_t i = 0; i < M * ncols; ++i) scaled_out(acc[i], absacc[i], K, gs, &nom[i], &lo[i], &hi[i]);
+        return;
+    }
+    int64_t half = ncols / 2;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t i = 0; i < half; ++i) {
+            uint16_t gn, gl, gh, un, ul, uh;
+            int64_t a = m * ncols + i, b = m * ncols + half + i;
+            scaled_out(acc[a], absacc[a], K, gs, &gn, &gl, &gh);
+            scaled_out(acc[b], absacc[b], K, gs, &un, &ul, &uh);
+            silu_mul_interval(gn, gl, gh, un, ul, uh, &nom[m * half + i], &lo[m * half + i], &hi[m * half + i]);
+        }
+}
+
+/* ------------------------------------------------------------------------ */
+/* MoE pair                                                                  */
+/* ------------------------------------------------------------------------ */
+
+/* Stored W1 row holding logical row (up ? up : gate) i of an expert in the
+ * "[up; gate] in 64-row groups" layout [moe_gemv, module docstring]: stored
+ * rows 128 g + [0, 64) are up rows 64 g + [0, 64), stored rows 128 g +
+ * [64, 128) the gate rows 64 g + [0, 64). */
+int64_t orc_w1_row(int64_t i, int up)
+{
+    return 128 * (i / 64) + (up ? 0 : 64) + i % 64;
+}
+
+/* gate_up [moe_gemv, gate_up], pairs p in [p0, p1) (p = t * topk + j):
+ *   e = ids[p]; g, u = f32(acc) * alpha[e] in fp32 (not rounded to bf16);
+ *   act[p, i] = bf16(silu(g) * u) (the pages use an approximate sigmoid;
+ *   the oracle uses the exact one and the tolerance covers the difference).
+ * Out-of-range expert ids leave the row untouched and return nonzero. */
+int orc_moe_gate_up_routed(const uint16_t* x, const int32_t* ids, int64_t topk, const uint8_t* w1,
+                           const uint8_t* w1_sf, const float* alpha, int64_t E, int64_t H, int64_t I,
+                           int64_t p0, int64_t p1, double* tmp_g, double* tmp_u, uint16_t* nom,
+                           uint16_t* lo, uint16_t* hi)
+{
+    int bad = 0;
+    int64_t sfe = orc_scale_bytes(2 * I, H);
+    for (int64_t p = p0; p < p1; ++p) {
+        int64_t t = p / topk, e = ids[p];
+        if (e < 0 || e >= E) { bad = 1; continue; }
+        const uint8_t* we = w1 + e * (2 * I) * (H / 2);
+        const uint8_t* se = w1_sf + e * sfe;
+        double a = (double)alpha[e];
+        for (int64_t i = 0; i < I; ++i) {
+            double ag, bg, au, bu;
+            dequant_row(we, se, orc_w1_row(i, 0), H, tmp_g);
+            dequant_row(we, se, orc_w1_row(i, 1), H, tmp_u);
+            dot(x + t * H, tmp_g, H, &ag, &bg);
+            dot(x + t * H, tmp_u, H, &au, &bu);
+            double g = f32(f32(ag) * a), u = f32(f32(au) * a);
+            double eg = acc_err(bg, H) * fabs(a) + ldexp(fabs(g), -22);
+            double eu = acc_err(bu, H) * fabs(a) + ldexp(fabs(u), -22);
+            double v = silu(g) * u;
+            /* |d silu/dg| <= 1.1; allowance for an approximate sigmoid of
+             * relative accuracy 2^-18. */
+            double e_ = 1.1 * fabs(u) * eg + fabs(silu(g)) * eu + ldexp(fabs(v), -18) + ldexp(1.0, -140);
+            int64_t o = p * I + i;
+            nom[o] = orc_bf16_rne(v);
+            lo[o] = orc_bf16_rne(v - e_);
+            hi[o] = orc_bf16_rne(v + e_);
+        }
+    }
+    return bad;
+}
+
+/* Shared expert of gate_up [moe_gemv, gate_up]: ModelOpt [gate; up] weight
+ * [2 SI, H/2] with flat 128x4 scales; sact[t, i] = bf16(silu(G) * U) with
+ * G, U = bf16(f32(acc) * gssh) (exact SiLU) -- the dense silu_mul epilogue. */
+void orc_moe_gate_up_shared(const uint16_t* x, int64_t t0, int64_t t1, const uint8_t* wsh,
+                            const uint8_t* ssh, double gssh, int64_t H, int64_t SI, double* tmp_g,
+                            double* tmp_u, uint16_t* nom, uint16_t* lo, uint16_t* hi)
+{
+    for (int64_t t = t0; t < t1; ++t)
+        for (int64_t i = 0; i < SI; ++i) {
+            double ag, bg, au, bu;
+            uint16_t gn, gl, gh, un, ul, uh;
+            dequant_row(wsh, ssh, i, H, tmp_g);
+            dequant_row(wsh, ssh, SI + i, H, tmp_u);
+            dot(x + t * H, tmp_g, H, &ag, &bg);
+            dot(x + t * H, tmp_u, H, &au, &bu);
+            scaled_out(ag, bg, H, gssh, &gn, &gl, &gh);
+            scaled_out(au, bu, H, gssh, &un, &ul, &uh);
+            silu_mul_interval(gn, gl, gh, un, ul, uh, &nom[t * SI + i], &lo[t * SI + i], &hi[t * SI + i]);
+        }
+}
+
+/* down_combine [moe_gemv, down_combine], tokens t in [t0, t1):
+ *   y_j  = bf16(f32(act[t*topk+j] @ W2[e_j]^T) * alpha2[e_j])
+ *   y_sh = bf16(f32(sact[t] @ Wsd^T) * gssd)
+ *   s    = bf16(sum_j tw[t, j] * y_j)      (fp32 sum, j = 0 .. topk-1)
+ *   out  = bf16(s + y_sh)
+ * Each bf16 intermediate is carried as [lo, hi]; tw may have any sign.
+ * Tokens with an out-of-range id are skipped; returns nonzero if any. */
+int orc_moe_down_combine(const uint16_t* act, const int32_t* ids, const float* tw, int64_t topk,
+                         const uint8_t* w2, const uint8_t* w2_sf, const float* alpha2, int64_t E,
+                         int64_t H, int64_t I, const uint16_t* sact, const uint8_t* wsd,
+                         const uint8_t* ssd, double gssd, int64_t SI, int64_t t0, int64_t t1,
+                         double* tmp, uint16_t* nom, uint16_t* lo, uint16_t* hi)
+{
+    int bad = 0;
+    int64_t sfe = orc_scale_bytes(H, I);
+    for (int64_t t = t0; t < t1; ++t) {
+        int ok = 1;
+        for (int64_t j = 0; j < topk; ++j)
+            if (ids[t * topk + j] < 0 || ids[t * topk + j] >= E) ok = 0;
+        if (!ok) { bad = 1; continue; }
+        for (int64_t h = 0; h < H; ++h) {
+            double sn = 0.0, slo = 0.0, shi = 0.0, sabs = 0.0;
+            for (int64_t j = 0; j < topk; ++j) {
+                int64_t e = ids[t * topk + j];
+                double a, b;
+                uint16_t yn, yl, yh;
+                dequant_row(w2 + e * H * (I / 2), w2_sf + e * sfe, h, I, tmp);
+                dot(act + (t * topk + j) * I, tmp, I, &a, &b);
+                scaled_out(a, b, I, (double)alpha2[e], &yn, &yl, &yh);
+                double wj = (double)tw[t * topk + j];
+                double pn = wj * bf16_to_double(yn); /* exact in double */
+                double pl = wj * bf16_to_double(yl), ph = wj * bf16_to_double(yh);
+                sn += pn;
+                slo += fmin(pl, ph);
+                shi += fmax(pl, ph);
+                sabs += fmax(fabs(pl), fabs(ph));
+            }
+            double es = (double)(topk + 2) * ldexp(1.0, -24) * sabs;
+            uint16_t s_n = orc_bf16_rne(sn), s_l = orc_bf16_rne(slo - es), s_h = orc_bf16_rne(shi + es);
+            double a, b;
+            uint16_t zn, zl, zh;
+            dequant_row(wsd, ssd, h, SI, tmp);
+            dot(sact + t * SI, tmp, SI, &a, &b);
+            scaled_out(a, b, SI, gssd, &zn, &zl, &zh);
+            double on = bf16_to_double(s_n) + bf16_to_double(zn);
+            double ol = bf16_to_double(s_l) + bf16_to_double(zl);
+            double oh = bf16_to_double(s_h) + bf16_to_double(zh);
+            double eo = ldexp(fabs(ol) + fabs(oh), -24);
+            nom[t * H + h] = orc_bf16_rne(on);
+            lo[t * H + h] = orc_bf16_rne(ol - eo);
+            hi[t * H + h] = orc_bf16_rne(oh + eo);
+        }
+    }
+    return bad;
+}
