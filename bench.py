@@ -1,0 +1,379 @@
+#!/usr/bin/env python3
+"""Benchmark: nvfp4_gemv us/call and achieved HBM GB/s on the Llama-3-8B-shaped
+decode linears (qkv 6144x4096, o_proj 4096x4096, gate_up 28672x4096 with
+silu_mul, down 4096x14336) at M = 1, 2, 4, 8, 16, 32 tokens.
+
+One step = one pass of the NVFP4 GEMV over all 4 layers x 6 token counts (24
+launches, chained with programmatic dependent launch).  Inputs are synthetic
+(seeded) and resident in HBM; the weights are rotated over 5 replicas so a
+layer's weights are re-read at a reuse distance of ~490 MB (> 3 x the 129 MB
+L2): every call streams its weights from HBM.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the FP64 CPU oracle
+on a bounded sample of the same workload instead.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from moe_nvfp4_gemv_gb300 import synth  # noqa: E402
+
+METRIC = "nvfp4_gemv µs/call and achieved HBM GB/s (% of GB300 peak) at M=1..32"
+LAYERS = synth.LLAMA8B_LAYERS
+MS = synth.LLAMA8B_M
+GS = 0.01
+REPLICAS = 5
+WORKLOAD = "llama3-8b decode linears (qkv, o_proj, gate_up+silu_mul, down), NVFP4, M=1,2,4,8,16,32"
+
+
+def nvfp4_bytes(M, N, K, silu):
+    """Algorithmic bytes of one call: codes + scales + activations + output
+    (the output of silu_mul is [M, N/2])."""
+    n_out = N // 2 if silu else N
+    return N * K // 2 + N * K // 16 + 2 * M * K + 2 * M * n_out
+
+
+def step_bytes():
+    return sum(nvfp4_bytes(M, N, K, s) for M in MS for (N, K, s) in LAYERS.values())
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "moe_nvfp4_gemv_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profile():
+    """Per-launch DRAM bytes of the dominant kernel from the committed ncu
+    summary, if it was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "nvfp4_gemv_llama8b_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling during the timed region."""
+
+    Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        return rank, local, world, dist
+    return rank, local, world, None
+
+
+def max_over_ranks(v, dist, device):
+    if dist is None:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------------------
+# CPU oracle leg (cpu_baseline and --impl reference)
+# --------------------------------------------------------------------------------------
+
+def oracle_sample(budget_s=15.0, threads=None):
+    """Time the FP64 oracle on a bounded sample of the workload: for each
+    (layer, M) a slice of output rows, until ~budget_s of work.  Returns
+    (GB/s-equivalent of the sampled algorithmic bytes, threads, description)."""
+    import numpy as np
+    import oracle
+    threads = threads or (os.cpu_count() or 1)
+    rows_per_call = 64
+    done_bytes, spent = 0.0, 0.0
+    calls = 0
+    cache = {}
+    rounds = 0
+    while spent < budget_s and rounds < 50:
+        rounds += 1
+        for name, (N, K, silu) in LAYERS.items():
+            if name not in cache:
+                w = synth.fp4_bytes(N, K, seed=1).numpy()
+                sf = synth.e4m3_bytes(oracle.scale_bytes(N, K), seed=2).numpy()
+                cache[name] = (w, sf)
+            w, sf = cache[name]
+            n_out = N // 2 if silu else N
+            for M in MS:
+                x = synth.activations(M, K, seed=3 + M).view(torch.int16).numpy().view(np.uint16)
+                rows = np.arange(rows_per_call, dtype=np.int64) + (rounds * rows_per_call) % (n_out - rows_per_call)
+                t0 = time.perf_counter()
+                oracle.nvfp4_gemv(x, w, sf, GS, silu_mul=silu, rows=rows, threads=threads)
+                spent += time.perf_counter() - t0
+                frac = rows_per_call / n_out
+                done_bytes += nvfp4_bytes(M, N, K, silu) * frac
+                calls += 1
+            if spent >= budget_s:
+                break
+    desc = (f"{calls} oracle calls of {rows_per_call} output rows each over the 24 (layer, M) cases, "
+            f"{spent:.1f} s; bytes scaled by the sampled fraction of each call")
+    return done_bytes / spent / 1e9, threads, desc
+
+
+def run_reference(args):
+    rank, local, world, dist = dist_setup(args.gpus)
+    if rank != 0:
+        return 0
+    value, threads, desc = oracle_sample(budget_s=max(5.0, 20.0 / max(1, args.steps)))
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(step_bytes() / (value * 1e9) * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "device": "host CPU (FP64 oracle)"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# --------------------------------------------------------------------------------------
+# GPU leg
+# --------------------------------------------------------------------------------------
+
+def run_gpu(args):
+    rank, local, world, dist = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from moe_nvfp4_gemv_gb300 import fp4gemv
+
+    # weights: REPLICAS copies of every layer; activations per (layer, M)
+    weights = {}
+    for name, (N, K, silu) in LAYERS.items():
+        reps = []
+        for r in range(REPLICAS):
+            w = synth.fp4_bytes(N, K, seed=1000 * r + 1, device=dev)
+            sf = synth.e4m3_bytes(fp4gemv.scale_bytes(N, K), seed=1000 * r + 2, device=dev)
+            reps.append((w, sf))
+        weights[name] = reps
+    gs = torch.tensor([GS], dtype=torch.float32, device=dev)
+    xs = {(name, M): synth.activations(M, LAYERS[name][1], seed=10 * M + 3, device=dev) for name in LAYERS for M in MS}
+    outs = {(name, M): torch.empty(M, LAYERS[name][0] // (2 if LAYERS[name][2] else 1), dtype=torch.bfloat16,
+                                   device=dev) for name in LAYERS for M in MS}
+    stream = torch.cuda.current_stream(dev)
+    counter = [0]
+
+    def one_step():
+        for M in MS:
+            r = counter[0] % REPLICAS
+            counter[0] += 1
+            for name, (N, K, silu) in LAYERS.items():
+                w, sf = weights[name][r]
+                fp4gemv.nvfp4_gemv(xs[(name, M)], w, sf, gs, silu_mul=silu, pdl=True, out=outs[(name, M)])
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+    assert fp4gemv.get_device_error() == 0, "device error during warm-up"
+
+    # ---- timed region (device-resident inputs) ----
+    barrier(dist)
+    torch.cuda.synchronize()
+    launches0 = fp4gemv.launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            one_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    barrier(dist)
+    launches = fp4gemv.launch_count() - launches0
+    ms_total = e0.elapsed_time(e1)
+    ms_total = max_over_ranks(ms_total, dist, dev)
+    ms_step = ms_total / args.steps
+    total_bytes = step_bytes() * args.steps * world
+    value = total_bytes / (ms_total * 1e-3) / 1e9
+
+    # ---- per-call us (each (layer, M) alone, back to back, replicas rotated) ----
+    per_call = {}
+    reps = 20
+    for name, (N, K, silu) in LAYERS.items():
+        per_call[name] = {}
+        for M in MS:
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            for i in range(3):
+                w, sf = weights[name][i % REPLICAS]
+                fp4gemv.nvfp4_gemv(xs[(name, M)], w, sf, gs, silu_mul=silu, pdl=True, out=outs[(name, M)])
+            a.record(stream)
+            for i in range(reps):
+                w, sf = weights[name][i % REPLICAS]
+                fp4gemv.nvfp4_gemv(xs[(name, M)], w, sf, gs, silu_mul=silu, pdl=True, out=outs[(name, M)])
+            b.record(stream)
+            torch.cuda.synchronize()
+            us = a.elapsed_time(b) * 1e3 / reps
+            per_call[name][str(M)] = {"us": round(us, 2),
+                                      "GB/s": round(nvfp4_bytes(M, N, K, silu) / (us * 1e-6) / 1e9, 1)}
+
+    # ---- end to end through the public API with host buffers ----
+    host_x = {k: v.cpu().pin_memory() for k, v in xs.items()}
+    host_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in outs.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host_x.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+
+    def e2e_step():
+        for M in MS:
+            r = counter[0] % REPLICAS
+            counter[0] += 1
+            for name, (N, K, silu) in LAYERS.items():
+                w, sf = weights[name][r]
+                xd = xs[(name, M)]
+                xd.copy_(host_x[(name, M)], non_blocking=True)
+                fp4gemv.nvfp4_gemv(xd, w, sf, gs, silu_mul=silu, pdl=True, out=outs[(name, M)])
+                host_out[(name, M)].copy_(outs[(name, M)], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(dist)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(a.elapsed_time(b), dist, dev)
+    e2e_value = total_bytes / (e2e_ms * 1e-3) / 1e9
+    assert fp4gemv.get_device_error() == 0, "device error during the timed region"
+
+    peak, peak_kind = read_peaks()
+    achieved = value / world
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, threads, desc = oracle_sample(budget_s=args.cpu_budget)
+        cpu = {"value": round(v, 4), "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "launches_per_step": len(MS) * len(LAYERS),
+                       "us_per_call_avg": round(ms_step * 1e3 / (len(MS) * len(LAYERS)), 3),
+                       "l2": f"weights rotated over {REPLICAS} replicas (reuse distance ~490 MB > 3 x L2)",
+                       "global_scale": GS, "pdl": True},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs (burst copy)",
+                         "traffic": traffic_from_profile(), "kernel": "fp4::gemv_kernel<kDenseFp4>",
+                         "bytes_per_step": step_bytes()},
+            "per_call": per_call,
+            "clocks": clk.summary(),
+            "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,445 @@
+// fp4gemv_api.cu -- the C ABI of libfp4gemv (see include/fp4gemv.h).
+//
+// Host side only: argument validation (before any launch), launch-shape
+// selection (token tile, cluster split of K, ring depth), TMA descriptor
+// encoding and the launches themselves.  All arithmetic runs in the kernels.
+#include <cuda.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+
+#include "fp4gemv.h"
+#include "launch.h"
+
+namespace fp4 {
+// Per-device error word (one copy per device context of this library image).
+__device__ uint32_t g_error_word;
+}  // namespace fp4
+
+namespace {
+
+using fp4::GemvParams;
+using fp4::KernelInfo;
+using fp4::LaunchCfg;
+
+std::atomic<uint64_t> g_launches{0};
+
+constexpr int kMaxDevices = 64;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+// 2-D row-major tensor [outer, inner] with a 128-byte-swizzled box.
+bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct DeviceState {
+  std::atomic<uint32_t*> err{nullptr};
+  std::atomic<int> sms{0};
+};
+DeviceState g_dev[kMaxDevices];
+
+fp4gemv_status device_state(uint32_t** err, int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FP4GEMV_ERR_CUDA;
+  DeviceState& d = g_dev[dev];
+  uint32_t* e = d.err.load(std::memory_order_acquire);
+  if (!e) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, fp4::g_error_word) != cudaSuccess) return FP4GEMV_ERR_CUDA;
+    e = static_cast<uint32_t*>(p);
+    d.err.store(e, std::memory_order_release);
+  }
+  int n = d.sms.load(std::memory_order_acquire);
+  if (!n) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FP4GEMV_ERR_CUDA;
+    d.sms.store(n, std::memory_order_release);
+  }
+  if (err) *err = e;
+  if (sms) *sms = n;
+  return FP4GEMV_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+fp4gemv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FP4GEMV_OK : FP4GEMV_ERR_CUDA; }
+
+int pick_nt(int m) { return m <= 16 ? 16 : m <= 32 ? 32 : m <= 64 ? 64 : 128; }
+
+cudaError_t kernel_info(int mode, int t, int nt, KernelInfo* info) {
+  GemvParams dummy;
+  LaunchCfg cfg{};
+  switch (mode) {
+    case fp4::kDenseFp4: return fp4::launch_dense_fp4(t, nt, dummy, cfg, info);
+    case fp4::kDenseBf16: return fp4::launch_dense_bf16(t, nt, dummy, cfg, info);
+    default: return fp4::launch_moe(mode, t, nt, dummy, cfg, info);
+  }
+}
+
+cudaError_t kernel_launch(int mode, int t, int nt, const GemvParams& p, const LaunchCfg& cfg) {
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  switch (mode) {
+    case fp4::kDenseFp4: return fp4::launch_dense_fp4(t, nt, p, cfg, nullptr);
+    case fp4::kDenseBf16: return fp4::launch_dense_bf16(t, nt, p, cfg, nullptr);
+    default: return fp4::launch_moe(mode, t, nt, p, cfg, nullptr);
+  }
+}
+
+// Ring depth and dynamic shared memory: two CTAs per SM when the kernel's
+// tensor-memory footprint allows it (<= 256 columns), else one.
+void size_ring(const KernelInfo& info, int* nstages, size_t* smem, int* ctas_per_sm) {
+  const int per_sm = info.tmem_cols <= 256 ? 2 : 1;
+  const int budget = per_sm == 2 ? 110 * 1024 : 220 * 1024;
+  int ns = (budget - 1024) / info.stage_bytes;
+  if (ns > fp4::kMaxStages) ns = fp4::kMaxStages;
+  if (ns < 2) ns = 2;
+  size_t bytes = 1024 + static_cast<size_t>(ns) * info.stage_bytes;
+  if (bytes < static_cast<size_t>(info.red_bytes) + 1024) bytes = info.red_bytes + 1024;
+  // one CTA per SM: ask for more than half of the SM's shared memory
+  if (per_sm == 1 && bytes < 120 * 1024) bytes = 120 * 1024;
+  *nstages = ns;
+  *smem = bytes;
+  *ctas_per_sm = per_sm;
+}
+
+// Cluster split of K: minimise (waves of CTAs) x (ring stages per CTA), ties
+// to the smaller split; every rank keeps at least one full stage.
+int pick_split(int tiles, int K, int stage_k, int slots) {
+  int best = 1;
+  long best_cost = -1;
+  for (int s = 1; s <= 8; s *= 2) {
+    if (s > 1 && K / s < stage_k) break;
+    const long ctas = static_cast<long>(tiles) * s;
+    const long waves = (ctas + slots - 1) / slots;
+    const int kslab = ((K + s - 1) / s + 63) / 64 * 64;
+    const long stages = (kslab + stage_k - 1) / stage_k;
+    const long cost = waves * stages;
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
+}
+
+fp4gemv_status dense_launch(int mode, const void* x, int64_t ldx, const void* w, const uint8_t* w_sf,
+                            const float* gs, void* out, int64_t ldo, int M, int N, int K, int silu_mul, int pdl,
+                            cudaStream_t stream) {
+  const bool fp4w = mode == fp4::kDenseFp4;
+  if (!x || !w || !out || (fp4w && (!w_sf || !gs))) return FP4GEMV_ERR_INVALID_ARG;
+  if ((silu_mul != 0 && silu_mul != 1) || (pdl != 0 && pdl != 1)) return FP4GEMV_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 1) return FP4GEMV_ERR_INVALID_ARG;
+  if (M > FP4GEMV_MAX_M || N % 16 != 0 || (silu_mul && N % 32 != 0) || K % 64 != 0) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
+  if (fp4w && K < 256) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
+  const int n_out = silu_mul ? N / 2 : N;
+  if (ldx < K || ldo < n_out) return FP4GEMV_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || (ldx * 2) % 16 != 0 || !aligned(w, 16) || !aligned(out, 16) || ldo % 8 != 0)
+    return FP4GEMV_ERR_MISALIGNED;
+  if (fp4w && !aligned(w_sf, 16)) return FP4GEMV_ERR_MISALIGNED;
+  if (gs && !aligned(gs, 4)) return FP4GEMV_ERR_MISALIGNED;
+
+  uint32_t* err = nullptr;
+  int sms = 0;
+  fp4gemv_status st = device_state(&err, &sms);
+  if (st != FP4GEMV_OK) return st;
+
+  const int T = silu_mul ? 2 : 1;
+  const int NT = pick_nt(M);
+  KernelInfo info{};
+  if (kernel_info(mode, T, NT, &info) != cudaSuccess) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
+  int nstages = 0, per_sm = 0;
+  size_t smem = 0;
+  size_ring(info, &nstages, &smem, &per_sm);
+  const int tiles = (n_out + 127) / 128;
+  const int stage_k = fp4w ? fp4::kStageK4 : fp4::kStageK16;
+  const int S = pick_split(tiles, K, stage_k, sms * per_sm);
+  const int kslab = ((K + S - 1) / S + 63) / 64 * 64;
+
+  GemvParams p;
+  std::memset(&p, 0, sizeof(p));
+  if (fp4w) {
+    if (!encode_2d(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, K / 2, N, K / 2, 128, 128)) return FP4GEMV_ERR_CUDA;
+  } else {
+    if (!encode_2d(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w, K, N, static_cast<uint64_t>(K) * 2, 64, 128))
+      return FP4GEMV_ERR_CUDA;
+    if (!encode_2d(&p.tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, M, static_cast<uint64_t>(ldx) * 2, 64, NT))
+      return FP4GEMV_ERR_CUDA;
+  }
+  p.sf = w_sf;
+  p.x = static_cast<const uint16_t*>(x);
+  p.ldx = ldx;
+  p.gs = gs;
+  p.out = static_cast<uint16_t*>(out);
+  p.ldo = ldo;
+  p.M = M;
+  p.n_out = n_out;
+  p.n_half = N / 2;
+  p.K = K;
+  p.k_split = kslab;
+  p.rows_w = N;
+  p.kbp = ((K / 16) + 3) / 4 * 4;
+  p.nstages = nstages;
+  p.err = err;
+
+  LaunchCfg cfg{};
+  cfg.grid = dim3(tiles * S, 1, 1);
+  cfg.cluster = S;
+  cfg.smem = smem;
+  cfg.pdl = pdl;
+  cfg.stream = stream;
+  return from_cuda(kernel_launch(mode, T, NT, p, cfg));
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t fp4gemv_scale_bytes(int rows, int K) {
+  if (rows < 1 || K < 16) return 0;
+  return static_cast<size_t>((rows + 127) / 128 * 128) * static_cast<size_t>((K / 16 + 3) / 4 * 4);
+}
+
+fp4gemv_status fp4gemv_nvfp4_gemv(const void* x, int64_t ldx, const uint8_t* w, const uint8_t* w_sf,
+                                  const float* global_scale, void* out, int64_t ldo, int M, int N, int K,
+                                  int silu_mul, int pdl, cudaStream_t stream) {
+  return dense_launch(fp4::kDenseFp4, x, ldx, w, w_sf, global_scale, out, ldo, M, N, K, silu_mul, pdl, stream);
+}
+
+fp4gemv_status fp4gemv_bf16_gemv(const void* x, int64_t ldx, const void* w, void* out, int64_t ldo, int M, int N,
+                                 int K, int silu_mul, int pdl, cudaStream_t stream) {
+  return dense_launch(fp4::kDenseBf16, x, ldx, w, nullptr, nullptr, out, ldo, M, N, K, silu_mul, pdl, stream);
+}
+
+fp4gemv_status fp4gemv_dequantize_rows(const uint8_t* w, const uint8_t* w_sf, void* out, int rows, int K,
+                                       cudaStream_t stream) {
+  if (!w || !w_sf || !out) return FP4GEMV_ERR_INVALID_ARG;
+  if (rows < 1 || K < 1) return FP4GEMV_ERR_INVALID_ARG;
+  if (rows % 16 != 0 || K % 256 != 0) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(w, 16) || !aligned(out, 16) || !aligned(w_sf, 4)) return FP4GEMV_ERR_MISALIGNED;
+  fp4gemv_status st = device_state(nullptr, nullptr);
+  if (st != FP4GEMV_OK) return st;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return from_cuda(fp4::launch_dequantize_rows(w, w_sf, out, rows, K, stream));
+}
+
+fp4gemv_status fp4gemv_dequant_gemm(const void* x, int64_t ldx, const uint8_t* w, const uint8_t* w_sf,
+                                    const float* global_scale, void* w_bf16, void* out, int64_t ldo, int M, int N,
+                                    int K, int pdl, cudaStream_t stream) {
+  if (!global_scale || !w_bf16) return FP4GEMV_ERR_INVALID_ARG;
+  if (pdl != 0 && pdl != 1) return FP4GEMV_ERR_INVALID_ARG;
+  if (N % 16 != 0 || K % 256 != 0) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(global_scale, 4)) return FP4GEMV_ERR_MISALIGNED;
+  // Validate the GEMM half first so nothing launches on a bad argument.
+  if (!x || !out || M < 1 || M > FP4GEMV_MAX_M || ldx < K || ldo < N) return M > FP4GEMV_MAX_M ? FP4GEMV_ERR_UNSUPPORTED_SHAPE : FP4GEMV_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || (ldx * 2) % 16 != 0 || !aligned(out, 16) || ldo % 8 != 0 || !aligned(w_bf16, 16))
+    return FP4GEMV_ERR_MISALIGNED;
+  fp4gemv_status st = fp4gemv_dequantize_rows(w, w_sf, w_bf16, N, K, stream);
+  if (st != FP4GEMV_OK) return st;
+  // The GEMM reads the weight the previous launch writes, so it is launched
+  // without early weight prefetch.
+  (void)pdl;
+  return dense_launch(fp4::kDenseBf16, x, ldx, w_bf16, nullptr, global_scale, out, ldo, M, N, K, 0, 0, stream);
+}
+
+fp4gemv_status fp4gemv_moe_gate_up(const void* x, const int32_t* ids, int M, int topk, const uint8_t* w1,
+                                   const uint8_t* w1_sf, const float* alpha, int E, int H, int I, void* act,
+                                   const uint8_t* wsh, const uint8_t* ssh, const float* gssh, int SI, void* sact,
+                                   int pdl, cudaStream_t stream) {
+  if (!x || !ids || !w1 || !w1_sf || !alpha || !act || !wsh || !ssh || !gssh || !sact) return FP4GEMV_ERR_INVALID_ARG;
+  if (pdl != 0 && pdl != 1) return FP4GEMV_ERR_INVALID_ARG;
+  if (M < 1 || topk < 1 || E < 1 || H < 1 || I < 1 || SI < 1) return FP4GEMV_ERR_INVALID_ARG;
+  if (static_cast<long>(M) * topk > 1024 || H % 64 != 0 || H < 256 || I % 64 != 0 || SI % 64 != 0)
+    return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(x, 16) || !aligned(w1, 16) || !aligned(w1_sf, 16) || !aligned(wsh, 16) || !aligned(ssh, 16) ||
+      !aligned(act, 16) || !aligned(sact, 16) || !aligned(ids, 4) || !aligned(alpha, 4) || !aligned(gssh, 4))
+    return FP4GEMV_ERR_MISALIGNED;
+  uint32_t* err = nullptr;
+  int sms = 0;
+  fp4gemv_status st = device_state(&err, &sms);
+  if (st != FP4GEMV_OK) return st;
+  const int NT = M <= 16 ? 16 : 32;
+  KernelInfo info{};
+  if (kernel_info(fp4::kMoeGateUp, 2, NT, &info) != cudaSuccess) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
+  int nstages = 0, per_sm = 0;
+  size_t smem = 0;
+  size_ring(info, &nstages, &smem, &per_sm);
+  GemvParams p;
+  std::memset(&p, 0, sizeof(p));
+  if (!encode_2d(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w1, H / 2, static_cast<uint64_t>(E) * 2 * I, H / 2, 128, 128))
+    return FP4GEMV_ERR_CUDA;
+  if (!encode_2d(&p.tm_w2, CU_TENSOR_MAP_DATA_TYPE_UINT8, wsh, H / 2, 2 * static_cast<uint64_t>(SI), H / 2, 128, 128))
+    return FP4GEMV_ERR_CUDA;
+  p.sf = w1_sf;
+  p.sf2 = ssh;
+  p.x = static_cast<const uint16_t*>(x);
+  p.x2 = p.x;
+  p.ldx = p.ldx2 = H;
+  p.gs = gssh;
+  p.alpha = alpha;
+  p.ids = ids;
+  p.out = static_cast<uint16_t*>(act);
+  p.ldo = I;
+  p.out2 = static_cast<uint16_t*>(sact);
+  p.ldo2 = SI;
+  p.M = M;
+  p.n_out = I;
+  p.n_half = SI;
+  p.K = H;
+  p.K2 = H;
+  p.E = E;
+  p.topk = topk;
+  p.P = M * topk;
+  p.rows_per_expert = 2 * I;
+  p.rows_w = 2 * SI;
+  p.shared_n_out = SI;
+  p.routed_tiles = (I + 127) / 128;
+  p.shared_tiles = (SI + 127) / 128;
+  p.kbp = p.kbp2 = ((H / 16) + 3) / 4 * 4;
+  p.sf_expert_bytes = static_cast<uint32_t>(fp4gemv_scale_bytes(2 * I, H));
+  p.nstages = nstages;
+  p.err = err;
+  const int shared_cols = (M + NT - 1) / NT;
+  LaunchCfg cfg{};
+  cfg.grid = dim3(p.routed_tiles > p.shared_tiles ? p.routed_tiles : p.shared_tiles, p.P + shared_cols, 1);
+  cfg.cluster = 1;
+  cfg.smem = smem;
+  cfg.pdl = pdl;
+  cfg.stream = stream;
+  return from_cuda(kernel_launch(fp4::kMoeGateUp, 2, NT, p, cfg));
+}
+
+size_t fp4gemv_moe_down_combine_workspace_bytes(int M, int topk, int H) {
+  if (M < 1 || topk < 1 || H < 1) return 0;
+  const size_t counters = ((static_cast<size_t>(H) + 127) / 128 * 4 + 15) / 16 * 16;
+  const size_t y = (static_cast<size_t>(M) * topk * H * 2 + 15) / 16 * 16;
+  const size_t ysh = (static_cast<size_t>(M) * H * 2 + 15) / 16 * 16;
+  return counters + y + ysh;
+}
+
+fp4gemv_status fp4gemv_moe_down_combine(const void* act, const int32_t* ids, const float* tw, int M, int topk,
+                                        const uint8_t* w2, const uint8_t* w2_sf, const float* alpha2, int E, int H,
+                                        int I, const void* sact, const uint8_t* wsd, const uint8_t* ssd,
+                                        const float* gssd, int SI, void* out, void* workspace,
+                                        size_t workspace_bytes, int pdl, cudaStream_t stream) {
+  if (!act || !ids || !tw || !w2 || !w2_sf || !alpha2 || !sact || !wsd || !ssd || !gssd || !out || !workspace)
+    return FP4GEMV_ERR_INVALID_ARG;
+  if (pdl != 0 && pdl != 1) return FP4GEMV_ERR_INVALID_ARG;
+  if (M < 1 || topk < 1 || E < 1 || H < 1 || I < 1 || SI < 1) return FP4GEMV_ERR_INVALID_ARG;
+  if (static_cast<long>(M) * topk > 1024 || H % 64 != 0 || I % 64 != 0 || I < 256 || SI % 64 != 0 || SI < 256)
+    return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
+  if (workspace_bytes < fp4gemv_moe_down_combine_workspace_bytes(M, topk, H)) return FP4GEMV_ERR_INVALID_ARG;
+  if (!aligned(act, 16) || !aligned(w2, 16) || !aligned(w2_sf, 16) || !aligned(wsd, 16) || !aligned(ssd, 16) ||
+      !aligned(sact, 16) || !aligned(out, 16) || !aligned(workspace, 16) || !aligned(ids, 4) || !aligned(tw, 4) ||
+      !aligned(alpha2, 4) || !aligned(gssd, 4))
+    return FP4GEMV_ERR_MISALIGNED;
+  uint32_t* err = nullptr;
+  int sms = 0;
+  fp4gemv_status st = device_state(&err, &sms);
+  if (st != FP4GEMV_OK) return st;
+  const int NT = M <= 16 ? 16 : 32;
+  KernelInfo info{};
+  if (kernel_info(fp4::kMoeDown, 1, NT, &info) != cudaSuccess) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
+  int nstages = 0, per_sm = 0;
+  size_t smem = 0;
+  size_ring(info, &nstages, &smem, &per_sm);
+  GemvParams p;
+  std::memset(&p, 0, sizeof(p));
+  if (!encode_2d(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w2, I / 2, static_cast<uint64_t>(E) * H, I / 2, 128, 128))
+    return FP4GEMV_ERR_CUDA;
+  if (!encode_2d(&p.tm_w2, CU_TENSOR_MAP_DATA_TYPE_UINT8, wsd, SI / 2, H, SI / 2, 128, 128)) return FP4GEMV_ERR_CUDA;
+  const size_t counters = ((static_cast<size_t>(H) + 127) / 128 * 4 + 15) / 16 * 16;
+  const size_t ybytes = (static_cast<size_t>(M) * topk * H * 2 + 15) / 16 * 16;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.counters = reinterpret_cast<uint32_t*>(ws);
+  p.out = reinterpret_cast<uint16_t*>(ws + counters);
+  p.ldo = H;
+  p.out2 = reinterpret_cast<uint16_t*>(ws + counters + ybytes);
+  p.ldo2 = H;
+  p.out3 = static_cast<uint16_t*>(out);
+  p.sf = w2_sf;
+  p.sf2 = ssd;
+  p.x = static_cast<const uint16_t*>(act);
+  p.ldx = I;
+  p.x2 = static_cast<const uint16_t*>(sact);
+  p.ldx2 = SI;
+  p.gs = gssd;
+  p.alpha = alpha2;
+  p.ids = ids;
+  p.tw = tw;
+  p.M = M;
+  p.n_out = H;
+  p.shared_n_out = H;
+  p.K = I;
+  p.K2 = SI;
+  p.E = E;
+  p.topk = topk;
+  p.P = M * topk;
+  p.rows_per_expert = H;
+  p.rows_w = H;
+  p.routed_tiles = (H + 127) / 128;
+  p.shared_tiles = p.routed_tiles;
+  p.kbp = ((I / 16) + 3) / 4 * 4;
+  p.kbp2 = ((SI / 16) + 3) / 4 * 4;
+  p.sf_expert_bytes = static_cast<uint32_t>(fp4gemv_scale_bytes(H, I));
+  p.nstages = nstages;
+  p.err = err;
+  const int shared_cols = (M + NT - 1) / NT;
+  LaunchCfg cfg{};
+  cfg.grid = dim3(p.routed_tiles, p.P + shared_cols, 1);
+  cfg.cluster = 1;
+  cfg.smem = smem;
+  cfg.pdl = pdl;
+  cfg.stream = stream;
+  return from_cuda(kernel_launch(fp4::kMoeDown, 1, NT, p, cfg));
+}
+
+fp4gemv_status fp4gemv_get_device_error(cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return FP4GEMV_ERR_CUDA;
+  uint32_t v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, fp4::g_error_word, sizeof(v)) != cudaSuccess) return FP4GEMV_ERR_CUDA;
+  if (v && cudaMemcpyToSymbol(fp4::g_error_word, &zero, sizeof(zero)) != cudaSuccess) return FP4GEMV_ERR_CUDA;
+  if (v & fp4::FP4_ERR_TIMEOUT) return FP4GEMV_ERR_TIMEOUT;
+  if (v & fp4::FP4_ERR_BADIDX) return FP4GEMV_ERR_BAD_INDEX;
+  return FP4GEMV_OK;
+}
+
+const char* fp4gemv_status_string(fp4gemv_status s) {
+  switch (s) {
+    case FP4GEMV_OK: return "FP4GEMV_OK";
+    case FP4GEMV_ERR_INVALID_ARG: return "FP4GEMV_ERR_INVALID_ARG";
+    case FP4GEMV_ERR_UNSUPPORTED_SHAPE: return "FP4GEMV_ERR_UNSUPPORTED_SHAPE";
+    case FP4GEMV_ERR_MISALIGNED: return "FP4GEMV_ERR_MISALIGNED";
+    case FP4GEMV_ERR_CUDA: return "FP4GEMV_ERR_CUDA";
+    case FP4GEMV_ERR_TIMEOUT: return "FP4GEMV_ERR_TIMEOUT";
+    case FP4GEMV_ERR_BAD_INDEX: return "FP4GEMV_ERR_BAD_INDEX";
+  }
+  return "FP4GEMV_ERR_UNKNOWN";
+}
+
+uint64_t fp4gemv_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

@@ -1,0 +1,93 @@
+// launch.h -- host-side interface between the C API translation unit and the
+// kernel translation units (each instantiates part of the kernel templates so
+// the library compiles in parallel).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "k_gemv.cuh"
+
+namespace fp4 {
+
+struct LaunchCfg {
+  dim3 grid;
+  unsigned cluster;     // CTAs per cluster along x (1: no cluster)
+  size_t smem;          // dynamic shared memory bytes
+  int pdl;              // programmatic dependent launch
+  cudaStream_t stream;
+};
+
+struct KernelInfo {
+  int threads;
+  int stage_bytes;
+  int red_bytes;
+  int tmem_cols;
+};
+
+// Per (mode, kT, kNT) kernel: static facts and a launcher.  Each returns
+// cudaErrorInvalidValue for a combination that is not instantiated.
+cudaError_t gemv_info(int mode, int t, int nt, KernelInfo* info);
+cudaError_t gemv_launch(int mode, int t, int nt, const GemvParams& p, const LaunchCfg& cfg);
+
+cudaError_t launch_dense_fp4(int t, int nt, const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info);
+cudaError_t launch_dense_bf16(int t, int nt, const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info);
+cudaError_t launch_moe(int mode, int t, int nt, const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info);
+cudaError_t launch_dequantize_rows(const uint8_t* w, const uint8_t* sf, void* out, int rows, int K,
+                                   cudaStream_t stream);
+
+// Shared launch helper for the kernel translation units.
+template <typename Kernel>
+cudaError_t launch_kernel(Kernel kernel, int threads, const GemvParams& p, const LaunchCfg& cfg) {
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = cfg.grid;
+  lc.blockDim = dim3(threads, 1, 1);
+  lc.dynamicSmemBytes = cfg.smem;
+  lc.stream = cfg.stream;
+  cudaLaunchAttribute attrs[2];
+  int na = 0;
+  if (cfg.cluster > 1) {
+    attrs[na].id = cudaLaunchAttributeClusterDimension;
+    attrs[na].val.clusterDim.x = cfg.cluster;
+    attrs[na].val.clusterDim.y = 1;
+    attrs[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  if (cfg.pdl) {
+    attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  lc.attrs = attrs;
+  lc.numAttrs = na;
+  return cudaLaunchKernelEx(&lc, kernel, p);
+}
+
+template <int kMode, int kT, int kNT>
+cudaError_t run_gemv(const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info) {
+  using C = Cfg<kMode, kT, kNT>;
+  if (info) {
+    info->threads = C::kThreads;
+    info->stage_bytes = C::kStageBytes;
+    info->red_bytes = C::kRedBytes;
+    info->tmem_cols = C::kTmemCols;
+    return cudaSuccess;
+  }
+  auto k = gemv_kernel<kMode, kT, kNT>;
+  static int configured_smem[64];  // per instantiation and device (0 = not yet)
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (configured_smem[dev] < static_cast<int>(cfg.smem)) {
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(cfg.smem));
+    if (e != cudaSuccess) return e;
+    if (cfg.cluster > 8) {
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+    }
+    configured_smem[dev] = static_cast<int>(cfg.smem);
+  }
+  return launch_kernel(k, C::kThreads, p, cfg);
+}
+
+}  // namespace fp4

@@ -1,0 +1,230 @@
+"""Thin ctypes binding of libfp4gemv (the C ABI in include/fp4gemv.h).
+
+Argument marshalling only: every call hands device pointers, sizes and the
+current CUDA stream of the tensors' device to the library; all computation
+runs in the library's kernels.  There is no fallback: importing this module
+raises if ``libfp4gemv.so`` is missing and cannot be built, and every call
+raises ``Fp4GemvError`` on a non-OK status.
+
+Names follow the pages (vllm.models.flint.ops.nvfp4_gemv: nvfp4_gemv,
+bf16_gemv, dequantize_rows; vllm.models.flint.ops.moe_gemv: gate_up,
+down_combine): ``nvfp4_gemv`` / ``bf16_gemv`` / ``dequantize_rows`` allocate
+and return their output, the MoE pair writes into caller buffers.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+OK = 0
+STATUS_NAMES = {
+    0: "FP4GEMV_OK",
+    1: "FP4GEMV_ERR_INVALID_ARG",
+    2: "FP4GEMV_ERR_UNSUPPORTED_SHAPE",
+    3: "FP4GEMV_ERR_MISALIGNED",
+    4: "FP4GEMV_ERR_CUDA",
+    5: "FP4GEMV_ERR_TIMEOUT",
+    6: "FP4GEMV_ERR_BAD_INDEX",
+}
+MAX_M = 128
+
+
+class Fp4GemvError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)}")
+
+
+def _load() -> ctypes.CDLL:
+    path = _build.LIB
+    if not os.path.exists(path) or _build._stale():
+        path = _build.build()
+    lib = ctypes.CDLL(path)
+    vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    sigs = {
+        "fp4gemv_scale_bytes": (sz, [i32, i32]),
+        "fp4gemv_nvfp4_gemv": (i32, [vp, i64, vp, vp, vp, vp, i64, i32, i32, i32, i32, i32, vp]),
+        "fp4gemv_bf16_gemv": (i32, [vp, i64, vp, vp, i64, i32, i32, i32, i32, i32, vp]),
+        "fp4gemv_dequantize_rows": (i32, [vp, vp, vp, i32, i32, vp]),
+        "fp4gemv_dequant_gemm": (i32, [vp, i64, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, vp]),
+        "fp4gemv_moe_gate_up": (i32, [vp, vp, i32, i32, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp, i32, vp, i32,
+                                      vp]),
+        "fp4gemv_moe_down_combine_workspace_bytes": (sz, [i32, i32, i32]),
+        "fp4gemv_moe_down_combine": (i32, [vp, vp, vp, i32, i32, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp, i32,
+                                           vp, vp, sz, i32, vp]),
+        "fp4gemv_get_device_error": (i32, [vp]),
+        "fp4gemv_status_string": (ctypes.c_char_p, [i32]),
+        "fp4gemv_launch_count": (ctypes.c_uint64, []),
+    }
+    for name, (res, args) in sigs.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+LIB_PATH = _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    return _lib
+
+
+def _check(status: int, what: str) -> None:
+    if status != OK:
+        raise Fp4GemvError(status, what)
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(dev: torch.device):
+    return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+
+
+def _bytes(t: torch.Tensor) -> torch.Tensor:
+    """uint8 view of a contiguous tensor (weights, float8 scales)."""
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.view(torch.uint8) if t.dtype != torch.uint8 else t
+
+
+def _rows_bf16(x: torch.Tensor, name: str) -> torch.Tensor:
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError(f"{name} must be a 2-D bf16 tensor with unit inner stride")
+    return x
+
+
+def scale_bytes(rows: int, K: int) -> int:
+    """Bytes of the flat 128x4-swizzled scale buffer of a [rows, K] weight."""
+    return int(_lib.fp4gemv_scale_bytes(rows, K))
+
+
+def nvfp4_gemv(x: torch.Tensor, weight: torch.Tensor, weight_scale: torch.Tensor, global_scale: torch.Tensor,
+               silu_mul: bool = False, pdl: bool = True, out: torch.Tensor | None = None) -> torch.Tensor:
+    """bf16 [M, N] = bf16(fp32(x @ dequant(weight).T) * global_scale); with
+    silu_mul the [M, N/2] bf16 silu(gate) * up of the [gate | up] halves."""
+    x = _rows_bf16(x, "x")
+    M, K = x.shape
+    w = _bytes(weight)
+    N = w.shape[0]
+    if w.dim() != 2 or w.shape[1] * 2 != K:
+        raise ValueError("weight must be uint8 [N, K/2]")
+    n_out = N // 2 if silu_mul else N
+    if out is None:
+        out = torch.empty(M, n_out, dtype=torch.bfloat16, device=x.device)
+    gs = global_scale.reshape(1)
+    _check(_lib.fp4gemv_nvfp4_gemv(_ptr(x), x.stride(0), _ptr(w), _ptr(_bytes(weight_scale)), _ptr(gs), _ptr(out),
+                                   out.stride(0), M, N, K, int(silu_mul), int(pdl), _stream(x.device)),
+           "fp4gemv_nvfp4_gemv")
+    return out
+
+
+def bf16_gemv(x: torch.Tensor, weight: torch.Tensor, silu_mul: bool = False, pdl: bool = True,
+              out: torch.Tensor | None = None) -> torch.Tensor:
+    """bf16 [M, N] = bf16(fp32(x @ weight.T)) for a row-major bf16 [N, K] weight."""
+    x = _rows_bf16(x, "x")
+    M, K = x.shape
+    if weight.dtype != torch.bfloat16 or not weight.is_contiguous() or weight.shape[1] != K:
+        raise ValueError("weight must be a contiguous bf16 [N, K] tensor")
+    N = weight.shape[0]
+    n_out = N // 2 if silu_mul else N
+    if out is None:
+        out = torch.empty(M, n_out, dtype=torch.bfloat16, device=x.device)
+    _check(_lib.fp4gemv_bf16_gemv(_ptr(x), x.stride(0), _ptr(weight), _ptr(out), out.stride(0), M, N, K,
+                                  int(silu_mul), int(pdl), _stream(x.device)), "fp4gemv_bf16_gemv")
+    return out
+
+
+def dequantize_rows(weight: torch.Tensor, weight_scale: torch.Tensor,
+                    out: torch.Tensor | None = None) -> torch.Tensor:
+    """Exact bf16 [rows, K] of e2m1 * e4m3 (global scale not applied)."""
+    w = _bytes(weight)
+    rows, K = w.shape[0], w.shape[1] * 2
+    if out is None:
+        out = torch.empty(rows, K, dtype=torch.bfloat16, device=w.device)
+    _check(_lib.fp4gemv_dequantize_rows(_ptr(w), _ptr(_bytes(weight_scale)), _ptr(out), rows, K,
+                                        _stream(w.device)), "fp4gemv_dequantize_rows")
+    return out
+
+
+def dequant_gemm(x: torch.Tensor, weight: torch.Tensor, weight_scale: torch.Tensor, global_scale: torch.Tensor,
+                 w_bf16: torch.Tensor | None = None, out: torch.Tensor | None = None) -> torch.Tensor:
+    """dequantize_rows into ``w_bf16`` then bf16(fp32(x @ w_bf16.T) * global_scale)."""
+    x = _rows_bf16(x, "x")
+    M, K = x.shape
+    w = _bytes(weight)
+    N = w.shape[0]
+    if w_bf16 is None:
+        w_bf16 = torch.empty(N, K, dtype=torch.bfloat16, device=x.device)
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=x.device)
+    _check(_lib.fp4gemv_dequant_gemm(_ptr(x), x.stride(0), _ptr(w), _ptr(_bytes(weight_scale)),
+                                     _ptr(global_scale.reshape(1)), _ptr(w_bf16), _ptr(out), out.stride(0), M, N, K,
+                                     1, _stream(x.device)), "fp4gemv_dequant_gemm")
+    return out
+
+
+def moe_gate_up(x, ids, w1, w1_sf, alpha, act, wsh, ssh, gssh, sact, pdl: bool = True) -> None:
+    """act[p] = bf16(silu(g) * u) of the routed experts ([up; gate] 64-row
+    groups) and sact[t] = the shared expert's silu_mul output, one launch."""
+    x = _rows_bf16(x, "x")
+    M, H = x.shape
+    topk = ids.shape[1]
+    E, I = w1.shape[0], w1.shape[1] // 2
+    SI = wsh.shape[0] // 2
+    _check(_lib.fp4gemv_moe_gate_up(_ptr(x), _ptr(ids), M, topk, _ptr(_bytes(w1)), _ptr(_bytes(w1_sf)), _ptr(alpha),
+                                    E, H, I, _ptr(act), _ptr(_bytes(wsh)), _ptr(_bytes(ssh)), _ptr(gssh.reshape(1)),
+                                    SI, _ptr(sact), int(pdl), _stream(x.device)), "fp4gemv_moe_gate_up")
+
+
+def moe_down_combine_workspace_bytes(M: int, topk: int, H: int) -> int:
+    return int(_lib.fp4gemv_moe_down_combine_workspace_bytes(M, topk, H))
+
+
+_workspaces: dict = {}
+
+
+def moe_workspace(device: torch.device, nbytes: int) -> torch.Tensor:
+    """A zero-filled workspace of at least ``nbytes`` for ``device`` (cached;
+    the kernel leaves it ready for the next call on the same stream order)."""
+    key = (device.type, device.index)
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
+
+
+def moe_down_combine(act, ids, tw, w2, w2_sf, alpha2, sact, wsd, ssd, gssd, out, pdl: bool = True,
+                     workspace: torch.Tensor | None = None) -> None:
+    """out[t] = bf16(bf16(sum_j tw[t,j] * y_j) + y_shared), one launch."""
+    M, topk = ids.shape
+    E, H, I = w2.shape[0], w2.shape[1], w2.shape[2] * 2
+    SI = wsd.shape[1] * 2
+    need = moe_down_combine_workspace_bytes(M, topk, H)
+    if workspace is None:
+        workspace = moe_workspace(act.device, need)
+    _check(_lib.fp4gemv_moe_down_combine(_ptr(act), _ptr(ids), _ptr(tw), M, topk, _ptr(_bytes(w2)),
+                                         _ptr(_bytes(w2_sf)), _ptr(alpha2), E, H, I, _ptr(sact), _ptr(_bytes(wsd)),
+                                         _ptr(_bytes(ssd)), _ptr(gssd.reshape(1)), SI, _ptr(out), _ptr(workspace),
+                                         workspace.numel() * workspace.element_size(), int(pdl),
+                                         _stream(act.device)), "fp4gemv_moe_down_combine")
+
+
+def get_device_error(device: torch.device | None = None) -> int:
+    """Synchronize the current stream, return and clear the device error word
+    (0 = FP4GEMV_OK, 5 = timeout, 6 = bad expert id)."""
+    dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    return int(_lib.fp4gemv_get_device_error(_stream(dev)))
+
+
+def launch_count() -> int:
+    """Kernel launches issued by the library in this process."""
+    return int(_lib.fp4gemv_launch_count())

@@ -1,0 +1,214 @@
+"""GPU parity of the dense ops against the FP64 oracle: dequantize_rows
+(bit-exact), nvfp4_gemv with and without silu_mul, bf16_gemv and the
+dequantize + GEMM path, on small shapes spanning several tiles and ragged
+tails, and on sampled outputs of the full-size decode layers."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from moe_nvfp4_gemv_gb300 import synth
+from gpu_util import assert_close, dense_inputs, require_gpu, sample_rows, u16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fp4():
+    require_gpu()
+    from moe_nvfp4_gemv_gb300 import fp4gemv
+    return fp4gemv
+
+
+DEV = "cuda"
+
+
+@pytest.mark.parametrize("rows,K", [(16, 256), (256, 512), (144, 1280), (384, 4096), (1024, 14336)])
+def test_dequantize_rows_bit_exact(fp4, rows, K):
+    _, w, sf = dense_inputs(1, rows, K, seed=rows + K)
+    got = fp4.dequantize_rows(w.to(DEV), sf.to(DEV))
+    torch.cuda.synchronize()
+    assert np.array_equal(u16(got), oracle.dequantize_rows(w.numpy(), sf.numpy()))
+
+
+def test_tiny_config(fp4):
+    cfg = synth.TINY
+    x, w, sf = dense_inputs(cfg["M"], cfg["N"], cfg["K"], seed=0)
+    gs = torch.tensor([cfg["gs"]], dtype=torch.float32)
+    got = fp4.nvfp4_gemv(x.to(DEV), w.to(DEV), sf.to(DEV), gs.to(DEV))
+    ref = oracle.nvfp4_gemv(u16(x), w.numpy(), sf.numpy(), cfg["gs"])
+    assert_close(u16(got), ref, "tiny config")
+
+
+SHAPES = [(256, 512), (1040, 768), (512, 320), (384, 4096), (2048, 2304)]
+
+
+@pytest.mark.parametrize("M", [1, 2, 5, 8, 16, 17, 32, 33, 64, 100, 128])
+@pytest.mark.parametrize("N,K", SHAPES)
+def test_nvfp4_gemv(fp4, M, N, K):
+    x, w, sf = dense_inputs(M, N, K, seed=7 * M + N)
+    gs = 0.01
+    got = fp4.nvfp4_gemv(x.to(DEV), w.to(DEV), sf.to(DEV), torch.tensor([gs], device=DEV))
+    ref = oracle.nvfp4_gemv(u16(x), w.numpy(), sf.numpy(), gs)
+    assert_close(u16(got), ref, f"nvfp4_gemv M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("M", [1, 3, 16, 32, 80])
+@pytest.mark.parametrize("N,K", [(256, 512), (1056, 768), (576, 320), (4096, 1024)])
+def test_nvfp4_gemv_silu_mul(fp4, M, N, K):
+    x, w, sf = dense_inputs(M, N, K, seed=11 * M + N)
+    gs = 0.02
+    got = fp4.nvfp4_gemv(x.to(DEV), w.to(DEV), sf.to(DEV), torch.tensor([gs], device=DEV), silu_mul=True)
+    assert got.shape == (M, N // 2)
+    ref = oracle.nvfp4_gemv(u16(x), w.numpy(), sf.numpy(), gs, silu_mul=True)
+    assert_close(u16(got), ref, f"silu_mul M={M} N={N} K={K}")
+
+
+def test_exact_small_integers_bit_identical(fp4):
+    # Small-integer activations, power-of-two scales, gs = 1: every partial
+    # sum is an exact fp32 integer, so GPU and oracle agree bit for bit.
+    M, N, K = 8, 384, 1024
+    rng = np.random.default_rng(5)
+    w = torch.from_numpy(rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8))
+    sf = torch.from_numpy(rng.choice(np.array([0x30, 0x38, 0x40], np.uint8), size=oracle.scale_bytes(N, K)))
+    x = torch.from_numpy(rng.integers(-3, 4, size=(M, K)).astype(np.float32)).to(torch.bfloat16)
+    got = fp4.nvfp4_gemv(x.to(DEV), w.to(DEV), sf.to(DEV), torch.ones(1, device=DEV))
+    nom, _, _ = oracle.nvfp4_gemv(u16(x), w.numpy(), sf.numpy(), 1.0)
+    assert np.array_equal(u16(got), nom)
+
+
+def test_strided_activations_and_output(fp4):
+    M, N, K = 4, 512, 1024
+    x, w, sf = dense_inputs(M, N, K, seed=3)
+    xs = torch.zeros(M, K + 64, dtype=torch.bfloat16, device=DEV)
+    xs[:, :K] = x.to(DEV)
+    out = torch.full((M, N + 8), -1.0, dtype=torch.bfloat16, device=DEV)
+    fp4.nvfp4_gemv(xs[:, :K], w.to(DEV), sf.to(DEV), torch.tensor([0.01], device=DEV), out=out[:, :N])
+    assert_close(u16(out[:, :N]), oracle.nvfp4_gemv(u16(x), w.numpy(), sf.numpy(), 0.01), "strided")
+    assert (out[:, N:] == -1).all()
+
+
+@pytest.mark.parametrize("M", [1, 8, 32, 128])
+@pytest.mark.parametrize("N,K,silu", [(256, 512, False), (1040, 768, False), (1056, 1024, True)])
+def test_bf16_gemv(fp4, M, N, K, silu):
+    x = synth.activations(M, K, seed=M + 1)
+    wb = synth.bf16_weight(N, K, seed=N + 2)
+    got = fp4.bf16_gemv(x.to(DEV), wb.to(DEV), silu_mul=silu)
+    ref = oracle.bf16_gemv(u16(x), u16(wb), silu_mul=silu)
+    assert_close(u16(got), ref, f"bf16_gemv M={M} N={N} K={K} silu={silu}")
+
+
+@pytest.mark.parametrize("M", [1, 24, 128])
+def test_dequant_gemm(fp4, M):
+    N, K = 512, 1024
+    x, w, sf = dense_inputs(M, N, K, seed=M + 40)
+    gs = 0.01
+    wb = torch.empty(N, K, dtype=torch.bfloat16, device=DEV)
+    got = fp4.dequant_gemm(x.to(DEV), w.to(DEV), sf.to(DEV), torch.tensor([gs], device=DEV), w_bf16=wb)
+    torch.cuda.synchronize()
+    assert np.array_equal(u16(wb), oracle.dequantize_rows(w.numpy(), sf.numpy()))
+    assert_close(u16(got), oracle.nvfp4_gemv(u16(x), w.numpy(), sf.numpy(), gs), f"dequant_gemm M={M}")
+
+
+def test_pdl_chain_matches_isolated_calls(fp4):
+    # Back-to-back PDL launches (weights prefetched under the previous kernel)
+    # must give the same bits as isolated launches.
+    M = 8
+    layers = [(1024, 2048), (2048, 1024), (768, 2048)]
+    ins = [dense_inputs(M, N, K, seed=N) for N, K in layers]
+    gs = torch.tensor([0.01], device=DEV)
+    dev_in = [(w.to(DEV), sf.to(DEV)) for _, w, sf in ins]
+    x0 = ins[0][0].to(DEV)
+    # chain: out_i feeds the next layer when K matches
+    outs_pdl, outs_plain = [], []
+    for pdl, outs in ((True, outs_pdl), (False, outs_plain)):
+        h = x0
+        for (N, K), (w, sf) in zip(layers, dev_in):
+            hin = h if h.shape[1] == K else ins[len(outs)][0].to(DEV)
+            h = fp4.nvfp4_gemv(hin, w, sf, gs, pdl=pdl)
+            outs.append(h)
+        torch.cuda.synchronize()
+    for a, b in zip(outs_pdl, outs_plain):
+        assert torch.equal(a, b)
+
+
+def test_deterministic(fp4):
+    x, w, sf = dense_inputs(16, 4096, 4096, seed=99)
+    xd, wd, sd = x.to(DEV), w.to(DEV), sf.to(DEV)
+    gs = torch.tensor([0.01], device=DEV)
+    a = fp4.nvfp4_gemv(xd, wd, sd, gs)
+    b = fp4.nvfp4_gemv(xd, wd, sd, gs)
+    assert torch.equal(a, b)
+
+
+# --- full-size decode layers: sampled outputs -------------------------------------------
+
+def _full_layer(fp4, N, K, silu, Ms, seed, nsample=48):
+    w = synth.fp4_bytes(N, K, seed=1)
+    sf = synth.e4m3_bytes(oracle.scale_bytes(N, K), seed=2)
+    wd, sd = w.to(DEV), sf.to(DEV)
+    gs = 0.01
+    n_out = N // 2 if silu else N
+    rows = sample_rows(n_out, nsample, seed)
+    wn, sn = w.numpy(), sf.numpy()
+    for M in Ms:
+        x = synth.activations(M, K, seed=3 + M)
+        got = fp4.nvfp4_gemv(x.to(DEV), wd, sd, torch.tensor([gs], device=DEV), silu_mul=silu)
+        g = u16(got)[:, rows]
+        ref = oracle.nvfp4_gemv(u16(x), wn, sn, gs, silu_mul=silu, rows=rows)
+        assert_close(g, ref, f"N={N} K={K} silu={silu} M={M}")
+
+
+@pytest.mark.parametrize("name", list(synth.LLAMA8B_LAYERS))
+def test_llama8b_layers_sampled(fp4, name):
+    N, K, silu = synth.LLAMA8B_LAYERS[name]
+    _full_layer(fp4, N, K, silu, synth.LLAMA8B_M, seed=len(name))
+
+
+@pytest.mark.parametrize("name", list(synth.LLAMA70B_LAYERS))
+def test_llama70b_layers_sampled(fp4, name):
+    N, K, silu = synth.LLAMA70B_LAYERS[name]
+    _full_layer(fp4, N, K, silu, synth.LLAMA70B_M, seed=len(name), nsample=24)
+
+
+@pytest.mark.parametrize("name", list(synth.LLAMA70B_LAYERS))
+def test_llama70b_dequantize_rows_sampled(fp4, name):
+    N, K, _ = synth.LLAMA70B_LAYERS[name]
+    w = synth.fp4_bytes(N, K, seed=1)
+    sf = synth.e4m3_bytes(oracle.scale_bytes(N, K), seed=2)
+    got = fp4.dequantize_rows(w.to(DEV), sf.to(DEV))
+    rows = sample_rows(N, 32, 5)
+    g = u16(got[torch.from_numpy(rows).to(DEV)])
+    # oracle on the sampled rows only (rows are independent)
+    ref = np.stack([oracle.dequantize_rows(w[r:r + 1].numpy(), _row_scales(sf.numpy(), r, N, K), threads=1)[0]
+                    for r in rows])
+    assert np.array_equal(g, ref)
+
+
+def _row_scales(sf, r, N, K):
+    """A one-row scale buffer holding row r's scales at row 0's offsets."""
+    out = np.zeros(oracle.scale_bytes(1, K), np.uint8)
+    for kb in range(K // 16):
+        out[oracle.swz(0, kb, K)] = sf[oracle.swz(r, kb, K)]
+    return out
+
+
+@pytest.mark.parametrize("M", list(synth.SWEEP_M))
+def test_sweep_shape_sampled(fp4, M):
+    N = K = synth.SWEEP_NK
+    w = synth.fp4_bytes(N, K, seed=1)
+    sf = synth.e4m3_bytes(oracle.scale_bytes(N, K), seed=2)
+    x = synth.activations(M, K, seed=3)
+    gs = 0.01
+    wd, sd, xd = w.to(DEV), sf.to(DEV), x.to(DEV)
+    rows = sample_rows(N, 16, M)
+    ref = oracle.nvfp4_gemv(u16(x), w.numpy(), sf.numpy(), gs, rows=rows)
+    got = fp4.nvfp4_gemv(xd, wd, sd, torch.tensor([gs], device=DEV))
+    assert_close(u16(got)[:, rows], ref, f"sweep nvfp4_gemv M={M}")
+    wb = torch.empty(N, K, dtype=torch.bfloat16, device=DEV)
+    got2 = fp4.dequant_gemm(xd, wd, sd, torch.tensor([gs], device=DEV), w_bf16=wb)
+    assert_close(u16(got2)[:, rows], ref, f"sweep dequant_gemm M={M}")
+
+
+def test_no_device_errors(fp4):
+    assert fp4.get_device_error() == 0

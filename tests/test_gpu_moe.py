@@ -1,0 +1,185 @@
+"""GPU parity of the MoE pair (gate_up, down_combine) against the FP64
+oracle, plus an exact-integer routing probe, duplicate experts, expert
+chunks larger than one token tile, and out-of-range ids."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from moe_nvfp4_gemv_gb300 import synth
+from gpu_util import assert_close, require_gpu, u16
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def fp4():
+    require_gpu()
+    from moe_nvfp4_gemv_gb300 import fp4gemv
+    return fp4gemv
+
+
+def make_moe(M, E, H, I, SI, topk, seed=0, ids=None):
+    if ids is None:
+        ids, tw = synth.routing(M, E, topk, seed=seed)
+    else:
+        tw = torch.softmax(torch.randn(M, topk, generator=torch.Generator().manual_seed(seed)), dim=1)
+    d = dict(M=M, E=E, H=H, I=I, SI=SI, topk=topk, ids=ids.to(torch.int32).contiguous(), tw=tw.float().contiguous())
+    d["x"] = synth.activations(M, H, seed=seed + 1)
+    d["w1"] = torch.stack([synth.fp4_bytes(2 * I, H, seed=seed + 100 + e) for e in range(E)])
+    d["w1_sf"] = torch.cat([synth.e4m3_bytes(oracle.scale_bytes(2 * I, H), seed=seed + 300 + e) for e in range(E)])
+    d["alpha"] = synth.expert_alphas(E)
+    d["wsh"] = synth.fp4_bytes(2 * SI, H, seed=seed + 2)
+    d["ssh"] = synth.e4m3_bytes(oracle.scale_bytes(2 * SI, H), seed=seed + 3)
+    d["gssh"] = torch.tensor([0.01])
+    d["act"] = synth.activations(M * topk, I, seed=seed + 4)
+    d["sact"] = synth.activations(M, SI, seed=seed + 5)
+    d["w2"] = torch.stack([synth.fp4_bytes(H, I, seed=seed + 500 + e) for e in range(E)])
+    d["w2_sf"] = torch.cat([synth.e4m3_bytes(oracle.scale_bytes(H, I), seed=seed + 700 + e) for e in range(E)])
+    d["alpha2"] = synth.expert_alphas(E)
+    d["wsd"] = synth.fp4_bytes(H, SI, seed=seed + 6)
+    d["ssd"] = synth.e4m3_bytes(oracle.scale_bytes(H, SI), seed=seed + 7)
+    d["gssd"] = torch.tensor([0.01])
+    return d
+
+
+def run_gate_up(fp4, d, pdl=True):
+    g = {k: v.to(DEV) for k, v in d.items() if isinstance(v, torch.Tensor)}
+    act = torch.full((d["M"] * d["topk"], d["I"]), 7.0, dtype=torch.bfloat16, device=DEV)
+    sact = torch.full((d["M"], d["SI"]), 7.0, dtype=torch.bfloat16, device=DEV)
+    fp4.moe_gate_up(g["x"], g["ids"], g["w1"], g["w1_sf"], g["alpha"], act, g["wsh"], g["ssh"], g["gssh"], sact, pdl=pdl)
+    return act, sact
+
+
+def run_down(fp4, d, pdl=True):
+    g = {k: v.to(DEV) for k, v in d.items() if isinstance(v, torch.Tensor)}
+    out = torch.full((d["M"], d["H"]), 7.0, dtype=torch.bfloat16, device=DEV)
+    fp4.moe_down_combine(g["act"], g["ids"], g["tw"], g["w2"], g["w2_sf"], g["alpha2"], g["sact"], g["wsd"], g["ssd"],
+                         g["gssd"], out, pdl=pdl)
+    return out
+
+
+def ref_gate_up(d, pairs=None, tokens=None):
+    return oracle.moe_gate_up(u16(d["x"]), d["ids"].numpy(), d["w1"].numpy(), d["w1_sf"].numpy(), d["alpha"].numpy(),
+                              d["wsh"].numpy(), d["ssh"].numpy(), float(d["gssh"][0]), pairs=pairs, tokens=tokens)
+
+
+def ref_down(d, tokens=None):
+    return oracle.moe_down_combine(u16(d["act"]), d["ids"].numpy(), d["tw"].numpy(), d["w2"].numpy(),
+                                   d["w2_sf"].numpy(), d["alpha2"].numpy(), u16(d["sact"]), d["wsd"].numpy(),
+                                   d["ssd"].numpy(), float(d["gssd"][0]), tokens=tokens)
+
+
+@pytest.mark.parametrize("M", [1, 3, 16, 20])
+def test_gate_up_small(fp4, M):
+    d = make_moe(M, E=8, H=512, I=256, SI=384, topk=2, seed=M)
+    act, sact = run_gate_up(fp4, d)
+    (an, al, ah), (sn, sl, sh), bad = ref_gate_up(d)
+    assert bad == 0
+    assert_close(u16(act), (an, al, ah), f"act M={M}")
+    assert_close(u16(sact), (sn, sl, sh), f"sact M={M}")
+    assert fp4.get_device_error() == 0
+
+
+@pytest.mark.parametrize("M", [1, 3, 16, 20])
+def test_down_combine_small(fp4, M):
+    d = make_moe(M, E=8, H=384, I=256, SI=512, topk=2, seed=50 + M)
+    out = run_down(fp4, d)
+    ref, bad = ref_down(d)
+    assert bad == 0
+    assert_close(u16(out), ref, f"down M={M}")
+    assert fp4.get_device_error() == 0
+
+
+def test_repeated_and_crowded_experts(fp4):
+    # every token routes both slots to expert 3 (a repeated expert within a
+    # token) and 40 tokens share it: its pair list spans several token tiles.
+    M, topk = 40, 2
+    ids = torch.full((M, topk), 3, dtype=torch.int32)
+    ids[::5, 1] = 1
+    d = make_moe(M, E=4, H=256, I=256, SI=256, topk=topk, seed=9, ids=ids)
+    act, sact = run_gate_up(fp4, d)
+    (an, al, ah), (sn, sl, sh), _ = ref_gate_up(d)
+    assert_close(u16(act), (an, al, ah), "act crowded")
+    assert_close(u16(sact), (sn, sl, sh), "sact crowded")
+    out = run_down(fp4, d)
+    ref, _ = ref_down(d)
+    assert_close(u16(out), ref, "down crowded")
+
+
+def test_routing_probe_exact(fp4):
+    # W2[e] is 1.0 in K column 0 with block-0 scale 2^e, act rows one-hot at
+    # column 0, tw = [1, 1/16], alpha2 = 1, zero shared expert:
+    # out[t, h] = 2^e0 + 2^(e1-4) exactly.
+    M, E, H, I, SI, topk = 6, 4, 256, 256, 256, 2
+    w2 = torch.zeros(E, H, I // 2, dtype=torch.uint8)
+    w2[:, :, 0] = 0x02
+    sfe = oracle.scale_bytes(H, I)
+    w2_sf = np.full(E * sfe, 0x38, np.uint8)
+    for e in range(E):
+        for h in range(H):
+            w2_sf[e * sfe + oracle.swz(h, 0, I)] = 0x38 + 8 * e
+    ids = torch.tensor([[0, 1], [3, 2], [2, 0], [1, 3], [3, 0], [2, 1]], dtype=torch.int32)
+    act = torch.zeros(M * topk, I, dtype=torch.bfloat16)
+    act[:, 0] = 1.0
+    d = dict(M=M, H=H, act=act.to(DEV), ids=ids.to(DEV), tw=torch.tensor([[1.0, 1 / 16]] * M).to(DEV),
+             w2=w2.to(DEV), w2_sf=torch.from_numpy(w2_sf).to(DEV), alpha2=torch.ones(E, device=DEV),
+             sact=torch.zeros(M, SI, dtype=torch.bfloat16, device=DEV),
+             wsd=torch.zeros(H, SI // 2, dtype=torch.uint8, device=DEV),
+             ssd=torch.zeros(oracle.scale_bytes(H, SI), dtype=torch.uint8, device=DEV),
+             gssd=torch.ones(1, device=DEV))
+    out = torch.empty(M, H, dtype=torch.bfloat16, device=DEV)
+    fp4.moe_down_combine(d["act"], d["ids"], d["tw"], d["w2"], d["w2_sf"], d["alpha2"], d["sact"], d["wsd"], d["ssd"],
+                         d["gssd"], out)
+    want = torch.tensor([2.0 ** int(a) + 2.0 ** (int(b) - 4) for a, b in ids.tolist()])
+    assert torch.equal(out.float().cpu(), want[:, None].expand(M, H))
+
+
+def test_bad_expert_id_reported(fp4):
+    d = make_moe(3, E=4, H=256, I=256, SI=256, topk=2, seed=21)
+    d["ids"][1, 1] = 17
+    act, _ = run_gate_up(fp4, d)
+    assert fp4.get_device_error() == 6
+    rows = [0, 1, 2, 4, 5]
+    (an, al, ah), _, _ = ref_gate_up(d, pairs=rows)
+    assert_close(u16(act)[rows], (an[rows], al[rows], ah[rows]), "act with a bad id elsewhere")
+    assert (act[3] == 7.0).all()  # the bad pair's row is left unwritten
+    out = run_down(fp4, d)
+    assert fp4.get_device_error() == 6
+    ref, _ = ref_down(d, tokens=[0, 2])
+    assert_close(u16(out)[[0, 2]], tuple(r[[0, 2]] for r in ref), "down with a bad id elsewhere")
+    assert (out[1] == 7.0).all()  # the token with the bad id is left unwritten
+    assert fp4.get_device_error() == 0
+
+
+@pytest.mark.parametrize("M", list(synth.MOE_M))
+def test_moe_config(fp4, M):
+    c = synth.MOE
+    d = make_moe(M, c["E"], c["H"], c["I"], c["SI"], c["topk"], seed=100)
+    act, sact = run_gate_up(fp4, d)
+    P = M * c["topk"]
+    pairs = list(range(P)) if P <= 64 else sorted(set(np.random.default_rng(M).integers(0, P, 24).tolist()) | {0, P - 1})
+    tokens = list(range(M)) if M <= 8 else [0, M // 2, M - 1]
+    (an, al, ah), (sn, sl, sh), bad = ref_gate_up(d, pairs=pairs, tokens=tokens)
+    assert bad == 0
+    assert_close(u16(act)[pairs], (an[pairs], al[pairs], ah[pairs]), f"act M={M}")
+    assert_close(u16(sact)[tokens], (sn[tokens], sl[tokens], sh[tokens]), f"sact M={M}")
+    out = run_down(fp4, d)
+    ref, bad = ref_down(d, tokens=tokens)
+    assert_close(u16(out)[tokens], tuple(r[tokens] for r in ref), f"down M={M}")
+    assert fp4.get_device_error() == 0
+
+
+def test_workspace_reuse_across_shapes(fp4):
+    # one workspace (sized for the largest call) serves calls of different M
+    c = synth.MOE
+    ws = torch.zeros(fp4.moe_down_combine_workspace_bytes(32, c["topk"], 1024), dtype=torch.uint8, device=DEV)
+    for M in (5, 32, 1, 17):
+        d = make_moe(M, 16, 1024, 512, 512, c["topk"], seed=M)
+        g = {k: v.to(DEV) for k, v in d.items() if isinstance(v, torch.Tensor)}
+        out = torch.empty(M, 1024, dtype=torch.bfloat16, device=DEV)
+        fp4.moe_down_combine(g["act"], g["ids"], g["tw"], g["w2"], g["w2_sf"], g["alpha2"], g["sact"], g["wsd"],
+                             g["ssd"], g["gssd"], out, workspace=ws)
+        ref, _ = ref_down(d)
+        assert_close(u16(out), ref, f"workspace reuse M={M}")
