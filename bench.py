@@ -354,8 +354,199 @@ def run_gpu(args):
             "cpu_baseline": cpu,
         }
         print(json.dumps(line))
+    if rank == 0 and args.extended:
+        run_extended(args.extended, dev)
     if dist is not None:
         dist.destroy_process_group()
+    return 0
+
+
+# --------------------------------------------------------------------------------------
+# Extended suite (--extended PATH): every configuration, L2-cold, one JSON file
+# --------------------------------------------------------------------------------------
+
+def time_calls(fn_list, reps, stream):
+    """Average device time (us) of one call when the calls in fn_list are
+    issued round-robin (each fn uses its own weight replica)."""
+    for f in fn_list[: min(3, len(fn_list))]:
+        f()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(reps):
+        fn_list[i % len(fn_list)]()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) * 1e3 / reps
+
+
+def replicas_for(nbytes, min_reps=2, target=400 << 20):
+    return max(min_reps, -(-target // max(1, nbytes)))
+
+
+def run_extended(path, dev):
+    from moe_nvfp4_gemv_gb300 import fp4gemv
+    stream = torch.cuda.current_stream(dev)
+    peak, peak_kind = read_peaks()
+    gs = torch.tensor([GS], dtype=torch.float32, device=dev)
+    res = {"peak_hbm_gbs": peak, "peak_kind": peak_kind, "l2_policy": "weights rotated over replicas, >= 400 MB"}
+
+    def fp4_layer(N, K, seed):
+        nb = N * K // 2 + N * K // 16
+        reps = replicas_for(nb)
+        return [(synth.fp4_bytes(N, K, seed=seed + 10 * r, device=dev),
+                 synth.e4m3_bytes(fp4gemv.scale_bytes(N, K), seed=seed + 10 * r + 1, device=dev))
+                for r in range(reps)]
+
+    # 70B layers (nvfp4_gemv) + dequantize_rows
+    t70 = {}
+    for name, (N, K, silu) in synth.LLAMA70B_LAYERS.items():
+        ws = fp4_layer(N, K, 7)
+        t70[name] = {}
+        for M in synth.LLAMA70B_M:
+            x = synth.activations(M, K, seed=M, device=dev)
+            out = torch.empty(M, N // 2 if silu else N, dtype=torch.bfloat16, device=dev)
+            fns = [lambda w=w, sf=sf: fp4gemv.nvfp4_gemv(x, w, sf, gs, silu_mul=silu, out=out) for w, sf in ws]
+            us = time_calls(fns, 20, stream)
+            gbs = nvfp4_bytes(M, N, K, silu) / (us * 1e-6) / 1e9
+            t70[name][str(M)] = {"us": round(us, 2), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 3)}
+        dq = torch.empty(N, K, dtype=torch.bfloat16, device=dev)
+        fns = [lambda w=w, sf=sf: fp4gemv.dequantize_rows(w, sf, out=dq) for w, sf in ws[:2]]
+        us = time_calls(fns, 10, stream)
+        gbs = N * K * (0.5 + 1 / 16 + 2) / (us * 1e-6) / 1e9
+        t70[name]["dequantize_rows"] = {"us": round(us, 2), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 3)}
+        del ws, dq
+    res["llama70b"] = t70
+
+    # BF16 weights on the 8B layers
+    tb = {}
+    for name, (N, K, silu) in LAYERS.items():
+        nb = 2 * N * K
+        ws = [synth.bf16_weight(N, K, seed=r, device=dev) for r in range(replicas_for(nb))]
+        tb[name] = {}
+        for M in MS:
+            x = synth.activations(M, K, seed=M, device=dev)
+            out = torch.empty(M, N // 2 if silu else N, dtype=torch.bfloat16, device=dev)
+            fns = [lambda w=w: fp4gemv.bf16_gemv(x, w, silu_mul=silu, out=out) for w in ws]
+            us = time_calls(fns, 20, stream)
+            byts = nb + 2 * M * K + 2 * M * (N // 2 if silu else N)
+            tb[name][str(M)] = {"us": round(us, 2), "GB/s": round(byts / (us * 1e-6) / 1e9, 1),
+                                "frac": round(byts / (us * 1e-6) / 1e9 / peak, 3)}
+        del ws
+    res["llama8b_bf16"] = tb
+
+    # MoE block
+    c = synth.MOE
+    E, H, I, SI, topk = c["E"], c["H"], c["I"], c["SI"], c["topk"]
+    w1 = synth.fp4_bytes(E * 2 * I, H, seed=1, device=dev).view(E, 2 * I, H // 2)
+    w1_sf = synth.e4m3_bytes(E * fp4gemv.scale_bytes(2 * I, H), seed=2, device=dev)
+    w2 = synth.fp4_bytes(E * H, I, seed=3, device=dev).view(E, H, I // 2)
+    w2_sf = synth.e4m3_bytes(E * fp4gemv.scale_bytes(H, I), seed=4, device=dev)
+    wsh = synth.fp4_bytes(2 * SI, H, seed=5, device=dev)
+    ssh = synth.e4m3_bytes(fp4gemv.scale_bytes(2 * SI, H), seed=6, device=dev)
+    wsd = synth.fp4_bytes(H, SI, seed=7, device=dev)
+    ssd = synth.e4m3_bytes(fp4gemv.scale_bytes(H, SI), seed=8, device=dev)
+    alpha = synth.expert_alphas(E, device=dev)
+    gsh = torch.tensor([0.01], device=dev)
+    tm = {}
+    ex_gu = 2 * I * H // 2 + fp4gemv.scale_bytes(2 * I, H)
+    ex_dn = H * I // 2 + fp4gemv.scale_bytes(H, I)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    for M in synth.MOE_M:
+        ids, tw = synth.routing(M, E, topk, seed=M, device=dev)
+        x = synth.activations(M, H, seed=M, device=dev)
+        act = torch.empty(M * topk, I, dtype=torch.bfloat16, device=dev)
+        sact = torch.empty(M, SI, dtype=torch.bfloat16, device=dev)
+        out = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
+        distinct = int(torch.unique(ids).numel())
+        gu_b = (distinct + 1) * ex_gu + 2 * M * H + 2 * M * topk * I + 2 * M * SI + 4 * M * topk
+        dn_b = (distinct + 1) * ex_dn + 2 * M * topk * I + 2 * M * SI + 2 * M * H + 8 * M * topk
+        t_gu, t_dn = [], []
+        for _ in range(10):
+            flush.zero_()  # evict the experts from L2 between timed calls
+            a, b, c2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            a.record(stream)
+            fp4gemv.moe_gate_up(x, ids, w1, w1_sf, alpha, act, wsh, ssh, gsh, sact)
+            b.record(stream)
+            fp4gemv.moe_down_combine(act, ids, tw, w2, w2_sf, alpha, sact, wsd, ssd, gsh, out)
+            c2.record(stream)
+            torch.cuda.synchronize()
+            t_gu.append(a.elapsed_time(b) * 1e3)
+            t_dn.append(b.elapsed_time(c2) * 1e3)
+        ug, ud = statistics.median(t_gu), statistics.median(t_dn)
+        tm[str(M)] = {"distinct_experts": distinct,
+                      "gate_up": {"us": round(ug, 2), "GB/s": round(gu_b / (ug * 1e-6) / 1e9, 1),
+                                  "frac": round(gu_b / (ug * 1e-6) / 1e9 / peak, 3)},
+                      "down_combine": {"us": round(ud, 2), "GB/s": round(dn_b / (ud * 1e-6) / 1e9, 1),
+                                       "frac": round(dn_b / (ud * 1e-6) / 1e9 / peak, 3)}}
+    res["moe"] = tm
+    del w1, w2, w1_sf, w2_sf, flush
+
+    # M sweep on N = K = 8192: nvfp4_gemv vs dequantize_rows + bf16 GEMM
+    N = K = synth.SWEEP_NK
+    ws = fp4_layer(N, K, 11)
+    wb = torch.empty(N, K, dtype=torch.bfloat16, device=dev)
+    sw = {}
+    for M in synth.SWEEP_M:
+        x = synth.activations(M, K, seed=M, device=dev)
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        fns = [lambda w=w, sf=sf: fp4gemv.nvfp4_gemv(x, w, sf, gs, out=out) for w, sf in ws]
+        us_g = time_calls(fns, 20, stream)
+        fns2 = [lambda w=w, sf=sf: fp4gemv.dequant_gemm(x, w, sf, gs, w_bf16=wb, out=out) for w, sf in ws]
+        us_d = time_calls(fns2, 10, stream)
+        b_g = nvfp4_bytes(M, N, K, False)
+        b_d = N * K * (0.5 + 1 / 16 + 2) + 2 * N * K + 2 * M * K + 2 * M * N
+        sw[str(M)] = {"gemv_us": round(us_g, 2), "gemv_GB/s": round(b_g / (us_g * 1e-6) / 1e9, 1),
+                      "gemv_TFLOP/s": round(2 * M * N * K / (us_g * 1e-6) / 1e12, 2),
+                      "dequant_gemm_us": round(us_d, 2), "dequant_gemm_GB/s": round(b_d / (us_d * 1e-6) / 1e9, 1)}
+    cross = next((m for m in synth.SWEEP_M if sw[str(m)]["dequant_gemm_us"] < sw[str(m)]["gemv_us"]), None)
+    res["sweep_8192"] = {"rows": sw, "crossover_M": cross}
+    assert fp4gemv.get_device_error() == 0
+    with open(path, "w") as f:
+        json.dump(res, f, indent=1)
+
+
+def run_profile_case(spec):
+    """A few launches of one (layer, M) case, for ncu captures:
+    LAYER:M[:bf16] with LAYER in qkv, o_proj, gate_up, down, or moe:M."""
+    from moe_nvfp4_gemv_gb300 import fp4gemv
+    dev = torch.device("cuda", 0)
+    parts = spec.split(":")
+    M = int(parts[1])
+    gs = torch.tensor([GS], dtype=torch.float32, device=dev)
+    if parts[0] == "moe":
+        c = synth.MOE
+        E, H, I, SI, topk = c["E"], c["H"], c["I"], c["SI"], c["topk"]
+        w1 = synth.fp4_bytes(E * 2 * I, H, seed=1, device=dev).view(E, 2 * I, H // 2)
+        w1_sf = synth.e4m3_bytes(E * fp4gemv.scale_bytes(2 * I, H), seed=2, device=dev)
+        w2 = synth.fp4_bytes(E * H, I, seed=3, device=dev).view(E, H, I // 2)
+        w2_sf = synth.e4m3_bytes(E * fp4gemv.scale_bytes(H, I), seed=4, device=dev)
+        wsh = synth.fp4_bytes(2 * SI, H, seed=5, device=dev)
+        ssh = synth.e4m3_bytes(fp4gemv.scale_bytes(2 * SI, H), seed=6, device=dev)
+        wsd = synth.fp4_bytes(H, SI, seed=7, device=dev)
+        ssd = synth.e4m3_bytes(fp4gemv.scale_bytes(H, SI), seed=8, device=dev)
+        alpha = synth.expert_alphas(E, device=dev)
+        ids, tw = synth.routing(M, E, topk, seed=M, device=dev)
+        x = synth.activations(M, H, seed=M, device=dev)
+        act = torch.empty(M * topk, I, dtype=torch.bfloat16, device=dev)
+        sact = torch.empty(M, SI, dtype=torch.bfloat16, device=dev)
+        out = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
+        for _ in range(4):
+            fp4gemv.moe_gate_up(x, ids, w1, w1_sf, alpha, act, wsh, ssh, gs, sact)
+            fp4gemv.moe_down_combine(act, ids, tw, w2, w2_sf, alpha, sact, wsd, ssd, gs, out)
+    else:
+        N, K, silu = LAYERS[parts[0]]
+        x = synth.activations(M, K, seed=M, device=dev)
+        if len(parts) > 2 and parts[2] == "bf16":
+            w = synth.bf16_weight(N, K, seed=1, device=dev)
+            for _ in range(4):
+                fp4gemv.bf16_gemv(x, w, silu_mul=silu)
+        else:
+            w = synth.fp4_bytes(N, K, seed=1, device=dev)
+            sf = synth.e4m3_bytes(fp4gemv.scale_bytes(N, K), seed=2, device=dev)
+            for _ in range(4):
+                fp4gemv.nvfp4_gemv(x, w, sf, gs, silu_mul=silu)
+    torch.cuda.synchronize()
+    assert fp4gemv.get_device_error() == 0
     return 0
 
 
@@ -367,9 +558,13 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--extended", metavar="PATH", help="also time every configuration into a JSON file")
+    ap.add_argument("--profile", metavar="CASE", help="run a few launches of one case (for ncu) and exit")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.profile:
+        return run_profile_case(args.profile)
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)

@@ -136,6 +136,7 @@ int pick_split(int tiles, int K, int stage_k, int slots) {
     const long ctas = static_cast<long>(tiles) * s;
     const long waves = (ctas + slots - 1) / slots;
     const int kslab = ((K + s - 1) / s + 63) / 64 * 64;
+    if (s > 1 && static_cast<long>(s - 1) * kslab >= K) break;
     const long stages = (kslab + stage_k - 1) / stage_k;
     const long cost = waves * stages;
     if (best_cost < 0 || cost < best_cost) {
@@ -176,8 +177,9 @@ fp4gemv_status dense_launch(int mode, const void* x, int64_t ldx, const void* w,
   size_ring(info, &nstages, &smem, &per_sm);
   const int tiles = (n_out + 127) / 128;
   const int stage_k = fp4w ? fp4::kStageK4 : fp4::kStageK16;
-  const int S = pick_split(tiles, K, stage_k, sms * per_sm);
-  const int kslab = ((K + S - 1) / S + 63) / 64 * 64;
+  const int S0 = pick_split(tiles, K, stage_k, sms * per_sm);
+  const int kslab = ((K + S0 - 1) / S0 + 63) / 64 * 64;
+  const int S = (K + kslab - 1) / kslab;  // every cluster rank gets a non-empty K range
 
   GemvParams p;
   std::memset(&p, 0, sizeof(p));

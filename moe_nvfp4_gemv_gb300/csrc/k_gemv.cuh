@@ -518,11 +518,12 @@ __global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, 1)
     if (active && !s_abort) {
       pdl_wait();
       if constexpr (kMode == kDenseFp4 || kMode == kDenseBf16) {
-        const int rows_per = 128 / S;
+        const int rows_per = (128 + S - 1) / S;  // this rank reduces rows [r0, r1)
         const int r0 = rank * rows_per;
+        const int r1 = min(128, r0 + rows_per);
         const float gs = p.gs ? __ldg(p.gs) : 1.0f;
-        for (int it = tid; it < rows_per * wk.ntok; it += kEpiThreads) {
-          const int n = it / rows_per, row = r0 + it % rows_per;
+        for (int it = tid; it < (r1 - r0) * wk.ntok; it += kEpiThreads) {
+          const int n = it / (r1 - r0), row = r0 + it % (r1 - r0);
           const int o = wk.out_base + row;
           if (o >= p.n_out) continue;
           uint16_t res;
