@@ -75,7 +75,7 @@ size_t fp4gemv_scale_bytes(int rows, int K);
  *   [N/2, N) up); out[m, i] = bf16(silu(G) * U) for i < N/2 with G, U the
  *   bf16 outputs of the gate and up rows (exact SiLU, one rounding).
  * Shapes: 1 <= M <= FP4GEMV_MAX_M, N % 16 == 0 (N % 32 == 0 with silu_mul),
- *   K % 64 == 0, ldx >= K, ldo >= N (N/2 with silu_mul). */
+ *   K % 64 == 0 and K >= 256, ldx >= K, ldo >= N (N/2 with silu_mul). */
 fp4gemv_status fp4gemv_nvfp4_gemv(const void* x, int64_t ldx, const uint8_t* w, const uint8_t* w_sf,
                                   const float* global_scale, void* out, int64_t ldo, int M, int N, int K,
                                   int silu_mul, int pdl, cudaStream_t stream);
@@ -118,8 +118,8 @@ fp4gemv_status fp4gemv_dequant_gemm(const void* x, int64_t ldx, const uint8_t* w
  * alpha fp32 [E]; act bf16 [M*topk, I]; wsh uint8 [2 SI, H/2] ModelOpt
  * [gate; up]; ssh flat 128x4 scales of [2 SI, H]; gssh fp32 [1];
  * sact bf16 [M, SI].
- * Shapes: 1 <= M, 1 <= topk, M * topk <= 1024, H % 64 == 0, I % 64 == 0,
- *   SI % 64 == 0, E >= 1.  Pairs whose id is outside [0, E) are left
+ * Shapes: 1 <= M, 1 <= topk, M * topk <= 1024, H % 64 == 0 and H >= 256,
+ *   I % 64 == 0, SI % 64 == 0, E >= 1.  Pairs whose id is outside [0, E) are left
  *   unwritten and raise FP4GEMV_ERR_BAD_INDEX in the device error word. */
 fp4gemv_status fp4gemv_moe_gate_up(const void* x, const int32_t* ids, int M, int topk, const uint8_t* w1,
                                    const uint8_t* w1_sf, const float* alpha, int E, int H, int I, void* act,
@@ -127,9 +127,10 @@ fp4gemv_status fp4gemv_moe_gate_up(const void* x, const int32_t* ids, int M, int
                                    int pdl, cudaStream_t stream);
 
 /* Scratch bytes fp4gemv_moe_down_combine needs for M tokens, top-k and
- * hidden size H.  The caller allocates it once, zero-fills it once (the
- * kernel leaves it ready for the next call), and must not share one
- * workspace between calls that may run concurrently. */
+ * hidden size H: per-row-tile arrival counters, then the bf16 y_j and
+ * y_shared values.  The contents need no initialisation and carry nothing
+ * between calls; one workspace serves calls of any shape that fit in it.
+ * Calls that may run concurrently on the GPU must not share a workspace. */
 size_t fp4gemv_moe_down_combine_workspace_bytes(int M, int topk, int H);
 
 /* down_combine (vllm.models.flint.ops.moe_gemv, down_combine), one launch:
@@ -141,9 +142,9 @@ size_t fp4gemv_moe_down_combine_workspace_bytes(int M, int topk, int H);
  * alpha2 fp32 [E]; sact bf16 [M, SI]; wsd uint8 [H, SI/2]; ssd flat scales
  * of [H, SI]; gssd fp32 [1]; out bf16 [M, H].
  * workspace: fp4gemv_moe_down_combine_workspace_bytes(M, topk, H) bytes,
- * zero-filled before its first use (see above), 16-byte aligned.
- * Shapes: as gate_up with the roles of H and I exchanged: H % 64 == 0,
- *   I % 64 == 0, SI % 64 == 0.  Tokens with an id outside [0, E) are left
+ * 16-byte aligned, no initialisation needed (see above).
+ * Shapes: 1 <= M, 1 <= topk, M * topk <= 1024, H % 64 == 0,
+ *   I % 64 == 0 and I >= 256, SI % 64 == 0 and SI >= 256.  Tokens with an id outside [0, E) are left
  *   unwritten and raise FP4GEMV_ERR_BAD_INDEX. */
 fp4gemv_status fp4gemv_moe_down_combine(const void* act, const int32_t* ids, const float* tw, int M, int topk,
                                         const uint8_t* w2, const uint8_t* w2_sf, const float* alpha2, int E, int H,

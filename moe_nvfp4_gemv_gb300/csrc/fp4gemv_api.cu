@@ -336,7 +336,7 @@ fp4gemv_status fp4gemv_moe_gate_up(const void* x, const int32_t* ids, int M, int
 
 size_t fp4gemv_moe_down_combine_workspace_bytes(int M, int topk, int H) {
   if (M < 1 || topk < 1 || H < 1) return 0;
-  const size_t counters = ((static_cast<size_t>(H) + 127) / 128 * 4 + 15) / 16 * 16;
+  const size_t counters = ((static_cast<size_t>(H) + 127) / 128 * 8 + 15) / 16 * 16;
   const size_t y = (static_cast<size_t>(M) * topk * H * 2 + 15) / 16 * 16;
   const size_t ysh = (static_cast<size_t>(M) * H * 2 + 15) / 16 * 16;
   return counters + y + ysh;
@@ -373,10 +373,14 @@ fp4gemv_status fp4gemv_moe_down_combine(const void* act, const int32_t* ids, con
   if (!encode_2d(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w2, I / 2, static_cast<uint64_t>(E) * H, I / 2, 128, 128))
     return FP4GEMV_ERR_CUDA;
   if (!encode_2d(&p.tm_w2, CU_TENSOR_MAP_DATA_TYPE_UINT8, wsd, SI / 2, H, SI / 2, 128, 128)) return FP4GEMV_ERR_CUDA;
-  const size_t counters = ((static_cast<size_t>(H) + 127) / 128 * 4 + 15) / 16 * 16;
+  const size_t counters = ((static_cast<size_t>(H) + 127) / 128 * 8 + 15) / 16 * 16;
   const size_t ybytes = (static_cast<size_t>(M) * topk * H * 2 + 15) / 16 * 16;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  p.counters = reinterpret_cast<uint32_t*>(ws);
+  p.counters = reinterpret_cast<unsigned long long*>(ws);
+  static std::atomic<uint32_t> epoch{0};
+  uint32_t ep = epoch.fetch_add(1, std::memory_order_relaxed) + 1;
+  if (ep == 0) ep = epoch.fetch_add(1, std::memory_order_relaxed) + 1;  // 0 is the reset value
+  p.epoch = ep;
   p.out = reinterpret_cast<uint16_t*>(ws + counters);
   p.ldo = H;
   p.out2 = reinterpret_cast<uint16_t*>(ws + counters + ybytes);

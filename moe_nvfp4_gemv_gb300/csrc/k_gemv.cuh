@@ -72,7 +72,8 @@ struct GemvParams {
   uint16_t* out2;      // gate_up sact / down y_shared scratch
   int64_t ldo2;
   uint16_t* out3;      // down: final output [M, H]
-  uint32_t* counters;  // down: per row-tile arrival counters
+  unsigned long long* counters;  // down: per row-tile arrival counters [epoch:32 | count:32]
+  uint32_t epoch;      // down: nonzero tag of this call (counters from other calls read as 0)
   int M;               // tokens
   int n_out;           // dense: output features; MoE routed: output features
   int n_half;          // dense silu: N / 2 (first up row); shared gate_up: SI
@@ -583,10 +584,22 @@ __global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, 1)
       // Every CTA of a row-tile column arrives once; the last one combines.
       epi_sync<kEpiThreads>();
       if (tid == 0) {
+        // Arrival count tagged with this call's epoch: a counter holding any
+        // other epoch (an earlier call, or never-initialised scratch) counts
+        // as zero, so the workspace needs no zero-fill.  The last arrival
+        // resets the counter.
         __threadfence();
-        const uint32_t lim = gridDim.y - 1;
-        const uint32_t old = atomicInc(p.counters + blockIdx.x, lim);
-        s_last = old == lim;
+        unsigned long long* ctr = p.counters + blockIdx.x;
+        const unsigned long long tag = static_cast<unsigned long long>(p.epoch) << 32;
+        unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(ctr), next;
+        for (;;) {
+          next = ((old & 0xFFFFFFFF00000000ull) == tag) ? old + 1 : tag + 1;
+          const unsigned long long seen = atomicCAS(ctr, old, next);
+          if (seen == old) break;
+          old = seen;
+        }
+        s_last = static_cast<uint32_t>(next) == gridDim.y;
+        if (s_last) atomicExch(ctr, 0ull);
         __threadfence();
       }
       epi_sync<kEpiThreads>();

@@ -192,12 +192,12 @@ _workspaces: dict = {}
 
 
 def moe_workspace(device: torch.device, nbytes: int) -> torch.Tensor:
-    """A zero-filled workspace of at least ``nbytes`` for ``device`` (cached;
-    the kernel leaves it ready for the next call on the same stream order)."""
+    """A cached scratch buffer of at least ``nbytes`` for ``device`` (calls
+    on one stream may share it; it needs no initialisation)."""
     key = (device.type, device.index)
     ws = _workspaces.get(key)
     if ws is None or ws.numel() < nbytes:
-        ws = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+        ws = torch.empty(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
         _workspaces[key] = ws
     return ws
 

@@ -172,13 +172,15 @@ def test_moe_config(fp4, M):
 
 
 def test_workspace_reuse_across_shapes(fp4):
-    # one workspace (sized for the largest call) serves calls of different M
+    # one uninitialised workspace (sized for the largest call) serves calls of
+    # different M and H in turn: nothing is carried between calls
     c = synth.MOE
-    ws = torch.zeros(fp4.moe_down_combine_workspace_bytes(32, c["topk"], 1024), dtype=torch.uint8, device=DEV)
-    for M in (5, 32, 1, 17):
-        d = make_moe(M, 16, 1024, 512, 512, c["topk"], seed=M)
+    ws = torch.full((fp4.moe_down_combine_workspace_bytes(32, c["topk"], 1024),), 0xA5, dtype=torch.uint8,
+                    device=DEV)
+    for M, H in ((5, 1024), (32, 256), (1, 1024), (17, 512), (32, 1024)):
+        d = make_moe(M, 16, H, 512, 512, c["topk"], seed=M)
         g = {k: v.to(DEV) for k, v in d.items() if isinstance(v, torch.Tensor)}
-        out = torch.empty(M, 1024, dtype=torch.bfloat16, device=DEV)
+        out = torch.empty(M, H, dtype=torch.bfloat16, device=DEV)
         fp4.moe_down_combine(g["act"], g["ids"], g["tw"], g["w2"], g["w2_sf"], g["alpha2"], g["sact"], g["wsd"],
                              g["ssd"], g["gssd"], out, workspace=ws)
         ref, _ = ref_down(d)
