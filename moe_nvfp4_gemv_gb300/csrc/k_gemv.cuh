@@ -48,7 +48,8 @@ enum Mode : int {
 };
 
 constexpr int kMaxStages = 8;
-constexpr int kSlots = 4;       // tensor-memory A slots
+constexpr int kSlots = 4;       // tensor-memory A slots (default)
+constexpr int kMaxSlots = 8;
 constexpr int kSubK = 64;       // K per A slot / per activation atom
 constexpr int kStageK4 = 256;   // K per ring stage, NVFP4 weights (128 B per row)
 constexpr int kStageK16 = 64;   // K per ring stage, bf16 weights (128 B per row)
@@ -117,23 +118,30 @@ __host__ __device__ constexpr int pow2_at_least(int v) {
 template <int kMode, int kT, int kNT>
 struct Cfg {
   static constexpr bool kFp4 = kMode != kDenseBf16;
-  static constexpr int kWarps = 4 * kT + 2;
+  // Dequant warpgroups per tile: the G warpgroups of a tile take turns on
+  // consecutive 64-wide K slices, so G slices of a tile are in flight.
+  static constexpr int kG = kFp4 ? 2 : 1;
+  static constexpr int kWarpgroups = kT * kG;
+  static constexpr int kWarps = 4 * kWarpgroups + 2;
   static constexpr int kThreads = kWarps * 32;
-  static constexpr int kProducerWarp = 4 * kT;
-  static constexpr int kMmaWarp = 4 * kT + 1;
+  static constexpr int kProducerWarp = 4 * kWarpgroups;
+  static constexpr int kMmaWarp = 4 * kWarpgroups + 1;
   static constexpr int kStageK = kFp4 ? kStageK4 : kStageK16;
   static constexpr int kWTileBytes = 128 * 128;
   static constexpr int kSfTileBytes = kFp4 ? 2 * 4 * 512 : 0;
   static constexpr int kXBytes = kNT * kStageK * 2;
   static constexpr int kXOff = kT * (kWTileBytes + kSfTileBytes);
   static constexpr int kStageBytes = kXOff + kXBytes;
-  static constexpr int kTmemA = kFp4 ? kSlots * kT * 32 : 0;
+  // tensor-memory A slots (64 K each): as many as fit next to the accumulators
+  static constexpr int kSlotsUsed = (kT == 2 && kNT <= 64) ? 6 : kSlots;
+  static constexpr int kTmemA = kFp4 ? kSlotsUsed * kT * 32 : 0;
   static constexpr int kTmemCols = pow2_at_least(kTmemA + kT * kNT);
   static constexpr int kRedBytes = kT * kNT * 128 * 4;
   static constexpr int kFullCount = 1 + (kFp4 ? 32 : 0);
   static_assert(kNT % 16 == 0 && kNT >= 16 && kNT <= kMaxNT, "token tile");
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
   static_assert(kTmemCols <= 512, "tensor memory");
+  static_assert(kSlotsUsed <= kMaxSlots, "slot barriers");
 };
 
 __device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) {
@@ -246,14 +254,17 @@ template <int kMode, int kT, int kNT>
 __global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, 1)
     gemv_kernel(const __grid_constant__ GemvParams p) {
   using C = Cfg<kMode, kT, kNT>;
-  constexpr int kEpiThreads = kT * 128;
+  constexpr int kEpiThreads = C::kWarpgroups * 128;
+  constexpr int kG = C::kG;
+  constexpr int kNS = C::kSlotsUsed;
 
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-aligned ring, addressed through 32-bit shared-window addresses
+  const uint32_t ring = (smem_u32(smem_raw) + 1023u) & ~1023u;
   __shared__ __align__(8) uint64_t bar_full[kMaxStages];
   __shared__ __align__(8) uint64_t bar_empty[kMaxStages];
-  __shared__ __align__(8) uint64_t bar_afull[kSlots];
-  __shared__ __align__(8) uint64_t bar_aempty[kSlots];
+  __shared__ __align__(8) uint64_t bar_afull[kMaxSlots];
+  __shared__ __align__(8) uint64_t bar_aempty[kMaxSlots];
   __shared__ __align__(8) uint64_t bar_accum;
   __shared__ __align__(8) uint64_t bar_red_ready;
   __shared__ __align__(8) uint64_t bar_red_done;
@@ -281,8 +292,8 @@ __global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, 1)
       mbar_init(smem_u32(&bar_full[i]), C::kFullCount);
       mbar_init(smem_u32(&bar_empty[i]), 1);
     }
-    for (int i = 0; i < kSlots; ++i) {
-      mbar_init(smem_u32(&bar_afull[i]), kEpiThreads);
+    for (int i = 0; i < kNS; ++i) {
+      mbar_init(smem_u32(&bar_afull[i]), kT * 128);
       mbar_init(smem_u32(&bar_aempty[i]), 1);
     }
     mbar_init(smem_u32(&bar_accum), 1);
@@ -310,10 +321,11 @@ __global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, 1)
     const uint64_t pol_w = policy_evict_first();
     const uint64_t pol_x = policy_evict_last();
     const CUtensorMap* tmw = wk.shared ? &p.tm_w2 : &p.tm_w;
-    const uint8_t* sfb = wk.shared ? p.sf2 : p.sf + (wk.expert >= 0 ? static_cast<size_t>(wk.expert) * p.sf_expert_bytes : 0);
+    const uint8_t* sfb =
+        wk.shared ? p.sf2 : p.sf + (wk.expert >= 0 ? static_cast<size_t>(wk.expert) * p.sf_expert_bytes : 0);
     auto issue_weights = [&](int s) {
       const int slot = s % nstages;
-      uint8_t* st = ring + slot * C::kStageBytes;
+      const uint32_t st = ring + slot * C::kStageBytes;
       const uint32_t fb = smem_u32(&bar_full[slot]);
       const int k0 = wk.k_begin + s * C::kStageK;
       const int kvalid = min(C::kStageK, wk.k_end - k0);
@@ -325,12 +337,12 @@ __global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, 1)
       asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(fb), "r"(bytes) : "memory");
       for (int t = 0; t < kT; ++t) {
         const int c0 = C::kFp4 ? k0 / 2 : k0;  // bytes (u8 map) or elements (bf16 map)
-        tma_load_2d(smem_u32(st + t * C::kWTileBytes), tmw, c0, wk.wrow[t], fb, pol_w);
+        tma_load_2d(st + t * C::kWTileBytes, tmw, c0, wk.wrow[t], fb, pol_w);
         if constexpr (C::kFp4) {
           for (int gi = 0; gi < wk.sgroups[t]; ++gi) {
             const size_t chunk = static_cast<size_t>(wk.srow[t] / 128 + gi) * (wk.kbp / 4) + k0 / 64;
-            bulk_load(smem_u32(st + kT * C::kWTileBytes + t * C::kSfTileBytes + gi * 2048), sfb + chunk * 512,
-                      nchunks * 512, fb, pol_w);
+            bulk_load(st + kT * C::kWTileBytes + t * C::kSfTileBytes + gi * 2048, sfb + chunk * 512, nchunks * 512,
+                      fb, pol_w);
           }
         }
       }
@@ -351,7 +363,7 @@ __global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, 1)
     for (int s = 0; s < nst && !s_abort; ++s) {
       const int slot = s % nstages;
       const uint32_t ph = (s / nstages) & 1;
-      uint8_t* st = ring + slot * C::kStageBytes;
+      const uint32_t st = ring + slot * C::kStageBytes;
       const uint32_t fb = smem_u32(&bar_full[slot]);
       if (s >= pre) {
         if (!mbar_wait(smem_u32(&bar_empty[slot]), ph ^ 1, p.err)) { s_abort = 1; break; }
@@ -362,7 +374,7 @@ __global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, 1)
       if constexpr (C::kFp4) {
         // activation rows: kNT rows x 32 chunks of 8 elements, 128-byte swizzle
         const int kvalid = min(C::kStageK, wk.k_end - k0);
-        const uint32_t xs = smem_u32(st + C::kXOff);
+        const uint32_t xs = st + C::kXOff;
         for (int it = lane; it < kNT * 32; it += 32) {
           const int n = it / 32, c = it % 32;
           const int u = c / 8, cc = c % 8;
@@ -376,7 +388,7 @@ __global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, 1)
       } else {
         if (lane == 0) {
           mbar_arrive_expect_tx(fb, C::kXBytes);
-          tma_load_2d(smem_u32(st + C::kXOff), &p.tm_x, k0, 0, fb, pol_x);
+          tma_load_2d(st + C::kXOff, &p.tm_x, k0, 0, fb, pol_x);
         }
       }
     }
@@ -387,13 +399,13 @@ __global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, 1)
       int q = 0;
       for (int s = 0; s < nst && !s_abort; ++s) {
         const int slot = s % nstages;
-        uint8_t* st = ring + slot * C::kStageBytes;
-        const uint32_t xs = smem_u32(st + C::kXOff);
+        const uint32_t st = ring + slot * C::kStageBytes;
+        const uint32_t xs = st + C::kXOff;
         if constexpr (C::kFp4) {
           const int nsub = min(C::kStageK, wk.k_end - wk.k_begin - s * C::kStageK) / kSubK;
           for (int u = 0; u < nsub; ++u, ++q) {
-            const int a = q % kSlots;
-            if (!mbar_wait(smem_u32(&bar_afull[a]), (q / kSlots) & 1, p.err)) { s_abort = 1; break; }
+            const int a = q % kNS;
+            if (!mbar_wait(smem_u32(&bar_afull[a]), (q / kNS) & 1, p.err)) { s_abort = 1; break; }
             tc_fence_after();
 #pragma unroll
             for (int t = 0; t < kT; ++t) {
@@ -412,7 +424,7 @@ __global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, 1)
 #pragma unroll
           for (int t = 0; t < kT; ++t) {
             const uint32_t d_tmem = tmem + t * kNT;
-            const uint32_t ws = smem_u32(st + t * C::kWTileBytes);
+            const uint32_t ws = st + t * C::kWTileBytes;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               mma_ss(d_tmem, sdesc_sw128(ws + kk * 32), sdesc_sw128(xs + kk * 32), idesc, (s | kk) != 0);
@@ -425,67 +437,74 @@ __global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, 1)
   } else {
     // ------------------------------------------------------------------ dequant warpgroups
     if constexpr (C::kFp4) {
-      const int g = warp / 4;           // tile
+      const int wg = warp / 4;
+      const int t = wg % kT;            // tile
+      const int g = wg / kT;            // turn: K slices q with q % kG == g
       const int i = tid % 128;          // row in tile
       const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
-      const int r = wk.srow[g] + i;     // row in the scale buffer's row space
-      const int grp = r / 128 - wk.srow[g] / 128;
-      const int sf_row_off = grp * 2048 + (r % 32) * 16 + ((r % 128) / 32) * 4;
-      const int w_row_off = (i / 8) * 1024 + (i % 8) * 128;
-      int q = 0;
+      const int r = wk.srow[t] + i;     // row in the scale buffer's row space
+      const int grp = r / 128 - wk.srow[t] / 128;
+      const uint32_t sf_row_off = grp * 2048 + (r % 32) * 16 + ((r % 128) / 32) * 4;
+      const uint32_t w_row_off = (i / 8) * 1024 + (i % 8) * 128;
+      const uint32_t i8 = i % 8;
+      int qbase = 0;  // global index of the current stage's first K slice
       for (int s = 0; s < nst && !s_abort; ++s) {
         const int slot = s % nstages;
-        uint8_t* st = ring + slot * C::kStageBytes;
-        if (!mbar_wait(smem_u32(&bar_full[slot]), (s / nstages) & 1, p.err)) { s_abort = 1; break; }
+        const uint32_t st = ring + slot * C::kStageBytes;
         const int nsub = min(C::kStageK, wk.k_end - wk.k_begin - s * C::kStageK) / kSubK;
-        const uint8_t* wt = st + g * C::kWTileBytes + w_row_off;
-        const uint8_t* sft = st + kT * C::kWTileBytes + g * C::kSfTileBytes + sf_row_off;
-        uint8_t* xs = st + C::kXOff;
-        for (int u = 0; u < nsub; ++u, ++q) {
-          const int a = q % kSlots;
-          if (!mbar_wait(smem_u32(&bar_aempty[a]), ((q / kSlots) & 1) ^ 1, p.err)) { s_abort = 1; break; }
-          tc_fence_after();
-          if (g == 0) {
-            // permute the activation atom of this K slice in place
-            uint4* xa = reinterpret_cast<uint4*>(xs + u * (kNT * 128));
+        const int first = ((g - qbase) % kG + kG) % kG;  // my first slice in this stage
+        if (first < nsub) {
+          if (!mbar_wait(smem_u32(&bar_full[slot]), (s / nstages) & 1, p.err)) { s_abort = 1; break; }
+          const uint32_t wt = st + t * C::kWTileBytes + w_row_off;
+          const uint32_t sft = st + kT * C::kWTileBytes + t * C::kSfTileBytes + sf_row_off;
+          const uint32_t xs = st + C::kXOff;
+          for (int u = first; u < nsub; u += kG) {
+            const int q = qbase + u;
+            const int a = q % kNS;
+            // this slice's codes and scales (shared memory, issued before the slot wait)
+            const uint4 q0 = lds128(wt + (((2 * u) ^ i8) * 16));
+            const uint4 q1 = lds128(wt + (((2 * u + 1) ^ i8) * 16));
+            const uint32_t sw = lds32(sft + u * 512);
+            if (!mbar_wait(smem_u32(&bar_aempty[a]), ((q / kNS) & 1) ^ 1, p.err)) { s_abort = 1; break; }
+            tc_fence_after();
+            if (t == 0) {
+              // permute the activation atom of this K slice in place
+              const uint32_t xa = xs + u * (kNT * 128);
 #pragma unroll
-            for (int j = i; j < kNT * 8; j += 128) xa[j] = perm_x8(xa[j]);
+              for (int j = i; j < kNT * 8; j += 128) sts128(xa + j * 16, perm_x8(lds128(xa + j * 16)));
+            }
+            uint32_t s0, s1, s2, s3;
+            scale_pair_to_bf16x2(sw & 0xFFFFu, s0, s1);
+            scale_pair_to_bf16x2(sw >> 16, s2, s3);
+            uint32_t o0[16], o1[16];
+            dequant32_perm(q0, s0, s1, o0);
+            dequant32_perm(q1, s2, s3, o1);
+            const uint32_t col = tmem + lane_base + (a * kT + t) * 32;
+            tmem_st16(col, o0);
+            tmem_st16(col + 16, o1);
+            tmem_wait_st();
+            if (t == 0) fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bar_afull[a]));
           }
-          const int i8 = i % 8;
-          const uint4 q0 = *reinterpret_cast<const uint4*>(wt + (((2 * u) ^ i8) * 16));
-          const uint4 q1 = *reinterpret_cast<const uint4*>(wt + (((2 * u + 1) ^ i8) * 16));
-          const uint32_t sw = *reinterpret_cast<const uint32_t*>(sft + u * 512);
-          uint32_t s0, s1, s2, s3;
-          scale_pair_to_bf16x2(sw & 0xFFFFu, s0, s1);
-          scale_pair_to_bf16x2(sw >> 16, s2, s3);
-          uint32_t o0[16], o1[16];
-          dequant32_perm(q0, s0, s1, o0);
-          dequant32_perm(q1, s2, s3, o1);
-          const uint32_t col = tmem + lane_base + (a * kT + g) * 32;
-          tmem_st16(col, o0);
-          tmem_st16(col + 16, o1);
-          tmem_wait_st();
-          if (g == 0) fence_proxy_async_smem();
-          tc_fence_before();
-          mbar_arrive(smem_u32(&bar_afull[a]));
         }
+        qbase += nsub;
       }
     }
   }
 
   // ==================================================================== epilogue
   __syncwarp();
-  if (warp < 4 * kT) {
-    const int g = warp / 4;
+  if (warp < 4 * C::kWarpgroups) {
+    const int wg = warp / 4;  // warpgroups 0 .. kT-1 read tile wg's accumulator
     const int i = tid % 128;
-    float* red = reinterpret_cast<float*>(ring);
     const bool ok_acc = active && mbar_wait(smem_u32(&bar_accum), 0, p.err);
     if (!ok_acc && active) s_abort = 1;
     tc_fence_after();
     epi_sync<kEpiThreads>();  // every ring stage is consumed: reuse it for partials
-    if (active && !s_abort) {
+    if (active && !s_abort && wg < kT) {
       const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
-      const uint32_t dcol = tmem + lane_base + C::kTmemA + g * kNT;
+      const uint32_t dcol = tmem + lane_base + C::kTmemA + wg * kNT;
       const float post = C::kFp4 ? static_cast<float>(1 << kShift) : 1.0f;
 #pragma unroll
       for (int c = 0; c < kNT; c += 8) {
@@ -493,7 +512,7 @@ __global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, 1)
         tmem_ld8(dcol + c, v);
         tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 8; ++j) red[(g * kNT + c + j) * 128 + i] = __uint_as_float(v[j]) * post;
+        for (int j = 0; j < 8; ++j) stsf(ring + ((wg * kNT + c + j) * 128 + i) * 4, __uint_as_float(v[j]) * post);
       }
     }
     tc_fence_before();
@@ -506,12 +525,12 @@ __global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, 1)
     }
     // Sum of the cluster's partials for (tile t, token n, row i), rank order.
     auto partial = [&](int t, int n, int row) -> float {
-      const int off = ((t * kNT + n) * 128 + row) * 4;
-      if (S == 1) return red[(t * kNT + n) * 128 + row];
+      const uint32_t off = ring + ((t * kNT + n) * 128 + row) * 4;
+      if (S == 1) return ldsf(off);
       float acc = 0.0f;
       for (uint32_t r2 = 0; r2 < S; ++r2) {
         float v;
-        asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(mapa(smem_u32(ring) + off, r2)) : "memory");
+        asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(mapa(off, r2)) : "memory");
         acc += v;
       }
       return acc;
