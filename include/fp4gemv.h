@@ -152,6 +152,30 @@ fp4gemv_status fp4gemv_moe_down_combine(const void* act, const int32_t* ids, con
                                         const float* gssd, int SI, void* out, void* workspace,
                                         size_t workspace_bytes, int pdl, cudaStream_t stream);
 
+/* Size of the scratch array behind fp4gemv_moe_down_combine_noalloc: 8 MiB
+ * of device memory per GPU that loads the library, held until exit. */
+#define FP4GEMV_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* down_combine for callers that cannot allocate device memory: the pages
+ * have no counterpart of this entry point.  Same arguments, layouts and
+ * result as fp4gemv_moe_down_combine, minus the workspace: the scratch is a
+ * fixed FP4GEMV_NOALLOC_SCRATCH_BYTES device array inside the library, so
+ * nothing is allocated or freed by the call.  For callers whose device
+ * memory is planned once at start-up (a serving process that must not
+ * allocate on the request path, where cudaMalloc can also synchronize the
+ * device) or that own no allocator (a plug-in that only receives tensors).
+ * Returns FP4GEMV_ERR_UNSUPPORTED_SHAPE when
+ * fp4gemv_moe_down_combine_workspace_bytes(M, topk, H) exceeds
+ * FP4GEMV_NOALLOC_SCRATCH_BYTES.  The first call on each device looks up
+ * the array's device address (cudaGetSymbolAddress, with that device
+ * current); make that first call before any stream capture.  All calls
+ * share the one array: calls that overlap on the GPU race on it. */
+fp4gemv_status fp4gemv_moe_down_combine_noalloc(const void* act, const int32_t* ids, const float* tw, int M,
+                                                int topk, const uint8_t* w2, const uint8_t* w2_sf,
+                                                const float* alpha2, int E, int H, int I, const void* sact,
+                                                const uint8_t* wsd, const uint8_t* ssd, const float* gssd, int SI,
+                                                void* out, int pdl, cudaStream_t stream);
+
 /* Synchronizes `stream`, then returns and clears the device error word of
  * the current device: FP4GEMV_OK, FP4GEMV_ERR_TIMEOUT or
  * FP4GEMV_ERR_BAD_INDEX (timeout reported first when both are set).
