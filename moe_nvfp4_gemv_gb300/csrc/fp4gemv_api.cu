@@ -57,6 +57,21 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Activations x [M, K] (bf16, row stride ldx) viewed as [K/64, M, 64]: one
+// box {64, rows, 4} holds four 64-wide K atoms of `rows` tokens, each atom a
+// [rows x 128-byte] 128B-swizzled block -- the layout the MMA reads.
+bool encode_x_atoms(CUtensorMap* m, const void* x, int K, int M, int64_t ldx, uint32_t rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(K / 64)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ldx) * 2, 128};
+  const cuuint32_t box[3] = {64, rows, 4};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(x), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 struct DeviceState {
   std::atomic<uint32_t*> err{nullptr};
   std::atomic<int> sms{0};
@@ -113,12 +128,13 @@ cudaError_t kernel_launch(int mode, int t, int nt, const GemvParams& p, const La
 // tensor-memory footprint allows it (<= 256 columns), else one.
 void size_ring(const KernelInfo& info, int* nstages, size_t* smem, int* ctas_per_sm) {
   const int per_sm = info.tmem_cols <= 256 ? 2 : 1;
-  const int budget = per_sm == 2 ? 110 * 1024 : 220 * 1024;
+  const int budget = (per_sm == 2 ? 110 * 1024 : 220 * 1024) - info.inbox_bytes;
   int ns = (budget - 1024) / info.stage_bytes;
   if (ns > fp4::kMaxStages) ns = fp4::kMaxStages;
   if (ns < 2) ns = 2;
   size_t bytes = 1024 + static_cast<size_t>(ns) * info.stage_bytes;
   if (bytes < static_cast<size_t>(info.red_bytes) + 1024) bytes = info.red_bytes + 1024;
+  bytes += info.inbox_bytes;
   // one CTA per SM: ask for more than half of the SM's shared memory
   if (per_sm == 1 && bytes < 120 * 1024) bytes = 120 * 1024;
   *nstages = ns;
@@ -188,6 +204,10 @@ fp4gemv_status dense_launch(int mode, const void* x, int64_t ldx, const void* w,
   } else {
     if (!encode_2d(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w, K, N, static_cast<uint64_t>(K) * 2, 64, 128))
       return FP4GEMV_ERR_CUDA;
+  }
+  if (fp4w) {
+    if (!encode_x_atoms(&p.tm_x, x, K, M, ldx, NT)) return FP4GEMV_ERR_CUDA;
+  } else {
     if (!encode_2d(&p.tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, M, static_cast<uint64_t>(ldx) * 2, 64, NT))
       return FP4GEMV_ERR_CUDA;
   }

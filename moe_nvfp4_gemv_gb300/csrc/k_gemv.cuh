@@ -107,6 +107,7 @@ struct CtaWork {
   float scale;     // alpha[e] or the global scale (loaded after the PDL wait)
   int tok[kMaxNT];   // B row -> activation row
   int orow[kMaxNT];  // B row -> output row (pair / token)
+  long long xoff[kMaxNT];  // B row -> element offset of its activation row
 };
 
 __host__ __device__ constexpr int pow2_at_least(int v) {
@@ -132,16 +133,32 @@ struct Cfg {
   static constexpr int kXBytes = kNT * kStageK * 2;
   static constexpr int kXOff = kT * (kWTileBytes + kSfTileBytes);
   static constexpr int kStageBytes = kXOff + kXBytes;
-  // tensor-memory A slots (64 K each): as many as fit next to the accumulators
-  static constexpr int kSlotsUsed = (kT == 2 && kNT <= 64) ? 6 : kSlots;
+  // Tensor memory: A slots (64 K each, fp4 modes) and kAcc independent fp32
+  // accumulators per tile.  Consecutive K=16 MMAs of a slice go to different
+  // accumulators so they do not serialise on one accumulator; the epilogue
+  // sums them.  Sized to 256 columns (two CTAs per SM) for one tile, 512 for
+  // two.
+  static constexpr int kSlotsUsed = (kT == 2 && kNT <= 16) ? 6 : kSlots;
   static constexpr int kTmemA = kFp4 ? kSlotsUsed * kT * 32 : 0;
-  static constexpr int kTmemCols = pow2_at_least(kTmemA + kT * kNT);
+  static constexpr int kBudget = kT == 1 ? 256 : 512;
+  static constexpr int kAcc = kTmemA + 4 * kT * kNT <= kBudget ? 4 : kTmemA + 2 * kT * kNT <= kBudget ? 2 : 1;
+  static constexpr int kTmemCols = pow2_at_least(kTmemA + kAcc * kT * kNT);
   static constexpr int kRedBytes = kT * kNT * 128 * 4;
-  static constexpr int kFullCount = 1 + (kFp4 ? 32 : 0);
+  // Dense modes read contiguous activation rows with TMA; the MoE modes
+  // gather rows by token / pair with cp.async from the producer lanes.
+  static constexpr bool kXTma = kMode == kDenseFp4 || kMode == kDenseBf16;
+  static constexpr int kFullCount = kXTma ? 1 : 33;
+  // Split-K partials are pushed to the owning cluster rank (st.async into a
+  // dedicated inbox) when the inbox is small; otherwise pulled through DSMEM
+  // from the (reused) ring.
+  static constexpr bool kPush = kT * kNT <= 64;
+  static constexpr int kInboxBytes = kPush ? kT * kNT * 136 * 4 : 0;
   static_assert(kNT % 16 == 0 && kNT >= 16 && kNT <= kMaxNT, "token tile");
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
   static_assert(kTmemCols <= 512, "tensor memory");
   static_assert(kSlotsUsed <= kMaxSlots, "slot barriers");
+  // CTAs per SM the launch aims for (tensor memory is 512 columns per SM)
+  static constexpr int kMinBlocks = kTmemCols <= 256 ? 2 : 1;
 };
 
 __device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) {
@@ -160,6 +177,24 @@ __device__ __forceinline__ void epi_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kThreadsEpi) : "memory");
 }
 
+// Eight columns [c, c+8) of a tile's accumulator: the sum of its kAcc
+// partial accumulators (kNT columns apart) in tensor memory.
+template <int kAcc, int kNT>
+__device__ __forceinline__ void load_acc(uint32_t taddr, float (&out)[8]) {
+  uint32_t v[8];
+  tmem_ld8(taddr, v);
+  tmem_wait_ld();
+#pragma unroll
+  for (int j = 0; j < 8; ++j) out[j] = __uint_as_float(v[j]);
+#pragma unroll
+  for (int a = 1; a < kAcc; ++a) {
+    tmem_ld8(taddr + a * kNT, v);
+    tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 8; ++j) out[j] += __uint_as_float(v[j]);
+  }
+}
+
 // Resolve what this CTA computes (thread 0).  Returns false if the ids could
 // not be read yet (gate_up routed: caller waits for the previous grid first).
 template <int kMode, int kT, int kNT>
@@ -172,8 +207,7 @@ __device__ void resolve_work(const GemvParams& p, CtaWork& w, uint32_t split) {
   w.wrow[1] = w.srow[1] = 0;
   const int tile = blockIdx.x / max(1u, cluster_nctarank());
   if constexpr (kMode == kDenseFp4 || kMode == kDenseBf16) {
-    w.ntok = p.M;
-    for (int n = 0; n < kNT; ++n) w.tok[n] = w.orow[n] = n < p.M ? n : 0;
+    w.ntok = p.M;  // B row n is token n (activations read by TMA)
     w.k_begin = static_cast<int>(split) * p.k_split;
     w.k_end = min(p.K, w.k_begin + p.k_split);
     w.kbp = p.kbp;
@@ -227,6 +261,7 @@ __device__ void resolve_work(const GemvParams& p, CtaWork& w, uint32_t split) {
         w.sgroups[t] = r0 < p.rows_per_expert ? 1 : 0;
       }
       w.out_base = tile * 128;
+      for (int m = 0; m < kNT; ++m) w.xoff[m] = static_cast<long long>(w.tok[m]) * p.ldx;
     } else {
       const int chunk = col - p.P;
       if (tile >= p.shared_tiles) { w.active = 0; return; }
@@ -246,12 +281,13 @@ __device__ void resolve_work(const GemvParams& p, CtaWork& w, uint32_t split) {
         w.sgroups[t] = g0 < groups_total ? g1 - g0 + 1 : 0;
       }
       w.out_base = tile * 128;
+      for (int m = 0; m < kNT; ++m) w.xoff[m] = static_cast<long long>(w.tok[m]) * p.ldx2;
     }
   }
 }
 
 template <int kMode, int kT, int kNT>
-__global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, 1)
+__global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, Cfg<kMode, kT, kNT>::kMinBlocks)
     gemv_kernel(const __grid_constant__ GemvParams p) {
   using C = Cfg<kMode, kT, kNT>;
   constexpr int kEpiThreads = C::kWarpgroups * 128;
@@ -259,13 +295,16 @@ __global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, 1)
   constexpr int kNS = C::kSlotsUsed;
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  // 1024-aligned ring, addressed through 32-bit shared-window addresses
+  // 1024-aligned ring, addressed through 32-bit shared-window addresses; the
+  // split-K inbox (push mode) follows the ring.
   const uint32_t ring = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t inbox = ring + p.nstages * C::kStageBytes;
   __shared__ __align__(8) uint64_t bar_full[kMaxStages];
   __shared__ __align__(8) uint64_t bar_empty[kMaxStages];
   __shared__ __align__(8) uint64_t bar_afull[kMaxSlots];
   __shared__ __align__(8) uint64_t bar_aempty[kMaxSlots];
   __shared__ __align__(8) uint64_t bar_accum;
+  __shared__ __align__(8) uint64_t bar_inbox;
   __shared__ __align__(8) uint64_t bar_red_ready;
   __shared__ __align__(8) uint64_t bar_red_done;
   __shared__ uint32_t s_tmem;
@@ -279,11 +318,19 @@ __global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, 1)
   const uint32_t S = cluster_nctarank();
   const uint32_t rank = S > 1 ? cluster_ctarank() : 0;
   const int nstages = p.nstages;
+  const int R = (128 + static_cast<int>(S) - 1) / static_cast<int>(S);  // rows reduced per cluster rank
+  const int r_lo = static_cast<int>(rank) * R;
+  const int r_hi = min(128, r_lo + R);
 
   // For gate_up the routed experts are only known once the router's output
   // (ids) is complete; every other mode reads ids / weights before the wait.
   constexpr bool kIdsAfterWait = kMode == kMoeGateUp;
 
+  if (warp == C::kProducerWarp && lane == 0) {
+    prefetch_tensormap(&p.tm_w);
+    if constexpr (kMode == kMoeGateUp || kMode == kMoeDown) prefetch_tensormap(&p.tm_w2);
+    if constexpr (C::kXTma) prefetch_tensormap(&p.tm_x);
+  }
   if (tid == 0) {
     s_abort = 0;
     s_last = 0;
@@ -297,15 +344,23 @@ __global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, 1)
       mbar_init(smem_u32(&bar_aempty[i]), 1);
     }
     mbar_init(smem_u32(&bar_accum), 1);
+    mbar_init(smem_u32(&bar_inbox), 1);
     mbar_init(smem_u32(&bar_red_ready), S);
     mbar_init(smem_u32(&bar_red_done), S);
     mbar_fence_init();
+    if (C::kPush && S > 1) {
+      // every rank sends its partials of my rows [r_lo, r_hi) for all tiles
+      mbar_arrive_expect_tx(smem_u32(&bar_inbox), S * kT * kNT * (r_hi - r_lo) * 4);
+    }
   }
   if (warp == C::kMmaWarp) tmem_alloc(smem_u32(&s_tmem), C::kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (S > 1) cluster_sync();  // peers' barriers are initialised before any remote arrive
+  if (S > 1) {
+    if (C::kPush) cluster_arrive();  // paired with a wait before the first remote access
+    else cluster_sync();
+  }
   // Let the next kernel in the stream start its own prologue (weight
   // prefetch) while this grid runs.  (gate_up routed CTAs have already waited
   // for the router, so a dependent kernel that reads ids early is safe.)
@@ -348,48 +403,62 @@ __global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, 1)
       }
     };
     const int pre = min(nst, nstages);
-    if (lane == 0) {
-      if (!kIdsAfterWait || wk.shared) {
-        for (int s = 0; s < pre; ++s) issue_weights(s);
-      }
+    if (lane == 0 && (!kIdsAfterWait || wk.shared)) {
+      for (int s = 0; s < pre; ++s) issue_weights(s);
     }
     pdl_wait();
     if (lane == 0 && kIdsAfterWait && !wk.shared) {
       for (int s = 0; s < pre; ++s) issue_weights(s);
     }
     __syncwarp();
-    const uint16_t* xb = wk.shared ? p.x2 : p.x;
-    const int64_t ldx = wk.shared ? p.ldx2 : p.ldx;
-    for (int s = 0; s < nst && !s_abort; ++s) {
-      const int slot = s % nstages;
-      const uint32_t ph = (s / nstages) & 1;
-      const uint32_t st = ring + slot * C::kStageBytes;
-      const uint32_t fb = smem_u32(&bar_full[slot]);
-      if (s >= pre) {
-        if (!mbar_wait(smem_u32(&bar_empty[slot]), ph ^ 1, p.err)) { s_abort = 1; break; }
-        if (lane == 0) issue_weights(s);
-        __syncwarp();
+    if constexpr (C::kXTma) {
+      // Dense activations: rows 0..M-1 of x, one TMA box {64 elements, kNT rows}
+      // per 64-wide K atom (rows beyond M read as zeros).
+      if (lane == 0) {
+        for (int s = 0; s < nst && !s_abort; ++s) {
+          const int slot = s % nstages;
+          const uint32_t st = ring + slot * C::kStageBytes;
+          const uint32_t fb = smem_u32(&bar_full[slot]);
+          if (s >= pre) {
+            if (!mbar_wait(smem_u32(&bar_empty[slot]), ((s / nstages) & 1) ^ 1, p.err)) { s_abort = 1; break; }
+            issue_weights(s);
+          }
+          const int k0 = wk.k_begin + s * C::kStageK;
+          mbar_arrive_expect_tx(fb, C::kXBytes);
+          if constexpr (C::kFp4) {
+            // one box {64 elements, kNT rows, 4 atoms} of the [K/64, M, 64] view
+            tma_load_3d(st + C::kXOff, &p.tm_x, 0, 0, k0 / kSubK, fb, pol_x);
+          } else {
+            tma_load_2d(st + C::kXOff, &p.tm_x, k0, 0, fb, pol_x);
+          }
+        }
       }
-      const int k0 = wk.k_begin + s * C::kStageK;
-      if constexpr (C::kFp4) {
-        // activation rows: kNT rows x 32 chunks of 8 elements, 128-byte swizzle
-        const int kvalid = min(C::kStageK, wk.k_end - k0);
-        const uint32_t xs = st + C::kXOff;
-        for (int it = lane; it < kNT * 32; it += 32) {
-          const int n = it / 32, c = it % 32;
-          const int u = c / 8, cc = c % 8;
-          const uint32_t dst = xs + u * (kNT * 128) + (n / 8) * 1024 + (n % 8) * 128 + ((cc ^ (n % 8)) * 16);
-          const bool valid = n < wk.ntok && c * 8 < kvalid;
-          const uint16_t* src = valid ? xb + static_cast<int64_t>(wk.tok[n]) * ldx + k0 + c * 8 : xb;
-          cp_async16(dst, src, valid ? 16u : 0u);
+    } else {
+      // Gathered activations (MoE): lane c copies 16-byte chunk c (of 32) of
+      // every B row of the stage, 128-byte swizzle.
+      const uint16_t* xb = wk.shared ? p.x2 : p.x;
+      const int u = lane / 8, cc = lane % 8;
+      for (int s = 0; s < nst && !s_abort; ++s) {
+        const int slot = s % nstages;
+        const uint32_t st = ring + slot * C::kStageBytes;
+        const uint32_t fb = smem_u32(&bar_full[slot]);
+        if (s >= pre) {
+          if (!mbar_wait(smem_u32(&bar_empty[slot]), ((s / nstages) & 1) ^ 1, p.err)) { s_abort = 1; break; }
+          if (lane == 0) issue_weights(s);
+          __syncwarp();
+        }
+        const int k0 = wk.k_begin + s * C::kStageK;
+        const bool kok = lane * 8 < min(C::kStageK, wk.k_end - k0);
+        const uint16_t* src_k = xb + k0 + lane * 8;
+        const uint32_t dst0 = st + C::kXOff + u * (kNT * 128);
+#pragma unroll 8
+        for (int n = 0; n < kNT; ++n) {
+          const bool valid = kok && n < wk.ntok;
+          const uint32_t dst = dst0 + (n / 8) * 1024 + (n % 8) * 128 + ((cc ^ (n % 8)) * 16);
+          cp_async16(dst, valid ? src_k + wk.xoff[n] : xb, valid ? 16u : 0u);
         }
         cp_async_arrive_noinc(fb);
         if (lane == 0) mbar_arrive(fb);
-      } else {
-        if (lane == 0) {
-          mbar_arrive_expect_tx(fb, C::kXBytes);
-          tma_load_2d(st + C::kXOff, &p.tm_x, k0, 0, fb, pol_x);
-        }
       }
     }
   } else if (warp == C::kMmaWarp) {
@@ -409,11 +478,13 @@ __global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, 1)
             tc_fence_after();
 #pragma unroll
             for (int t = 0; t < kT; ++t) {
-              const uint32_t d_tmem = tmem + C::kTmemA + t * kNT;
               const uint32_t a_tmem = tmem + (a * kT + t) * 32;
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_ts(d_tmem, a_tmem + kk * 8, sdesc_sw128(xs + u * (kNT * 128) + kk * 32), idesc, (q | kk) != 0);
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint32_t d_tmem = tmem + C::kTmemA + (t * C::kAcc + kk % C::kAcc) * kNT;
+                mma_ts(d_tmem, a_tmem + kk * 8, sdesc_sw128(xs + u * (kNT * 128) + kk * 32), idesc,
+                       q > 0 || kk >= C::kAcc);
+              }
             }
             mma_commit(smem_u32(&bar_aempty[a]));
             if (u == nsub - 1) mma_commit(smem_u32(&bar_empty[slot]));
@@ -423,11 +494,12 @@ __global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (int t = 0; t < kT; ++t) {
-            const uint32_t d_tmem = tmem + t * kNT;
             const uint32_t ws = st + t * C::kWTileBytes;
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_ss(d_tmem, sdesc_sw128(ws + kk * 32), sdesc_sw128(xs + kk * 32), idesc, (s | kk) != 0);
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint32_t d_tmem = tmem + (t * C::kAcc + kk % C::kAcc) * kNT;
+              mma_ss(d_tmem, sdesc_sw128(ws + kk * 32), sdesc_sw128(xs + kk * 32), idesc, s > 0 || kk >= C::kAcc);
+            }
           }
           mma_commit(smem_u32(&bar_empty[slot]));
         }
@@ -447,6 +519,32 @@ __global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, 1)
       const uint32_t sf_row_off = grp * 2048 + (r % 32) * 16 + ((r % 128) / 32) * 4;
       const uint32_t w_row_off = (i / 8) * 1024 + (i % 8) * 128;
       const uint32_t i8 = i % 8;
+      // One K slice: load codes + scales, wait for its tensor-memory slot,
+      // permute the activation atom (tile-0 warpgroups), dequantize, store.
+      auto slice = [&](uint32_t st, int u, int q) -> bool {
+        const uint32_t wt = st + t * C::kWTileBytes + w_row_off;
+        const uint4 q0 = lds128(wt + (((2 * u) ^ i8) * 16));
+        const uint4 q1 = lds128(wt + (((2 * u + 1) ^ i8) * 16));
+        const uint32_t sw = lds32(st + kT * C::kWTileBytes + t * C::kSfTileBytes + sf_row_off + u * 512);
+        const int a = q % kNS;
+        if (!mbar_wait(smem_u32(&bar_aempty[a]), ((q / kNS) & 1) ^ 1, p.err)) return false;
+        tc_fence_after();
+        if (t == 0) {
+          const uint32_t xa = st + C::kXOff + u * (kNT * 128);
+#pragma unroll
+          for (int j = i; j < kNT * 8; j += 128) sts128(xa + j * 16, perm_x8(lds128(xa + j * 16)));
+        }
+        uint32_t s0, s1, s2, s3;
+        scale_pair_to_bf16x2(sw & 0xFFFFu, s0, s1);
+        scale_pair_to_bf16x2(sw >> 16, s2, s3);
+        uint32_t o[16];
+        const uint32_t col = tmem + lane_base + (a * kT + t) * 32;
+        dequant32_perm(q0, s0, s1, o);
+        tmem_st16(col, o);
+        dequant32_perm(q1, s2, s3, o);
+        tmem_st16(col + 16, o);
+        return true;
+      };
       int qbase = 0;  // global index of the current stage's first K slice
       for (int s = 0; s < nst && !s_abort; ++s) {
         const int slot = s % nstages;
@@ -455,37 +553,16 @@ __global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, 1)
         const int first = ((g - qbase) % kG + kG) % kG;  // my first slice in this stage
         if (first < nsub) {
           if (!mbar_wait(smem_u32(&bar_full[slot]), (s / nstages) & 1, p.err)) { s_abort = 1; break; }
-          const uint32_t wt = st + t * C::kWTileBytes + w_row_off;
-          const uint32_t sft = st + kT * C::kWTileBytes + t * C::kSfTileBytes + sf_row_off;
-          const uint32_t xs = st + C::kXOff;
-          for (int u = first; u < nsub; u += kG) {
-            const int q = qbase + u;
-            const int a = q % kNS;
-            // this slice's codes and scales (shared memory, issued before the slot wait)
-            const uint4 q0 = lds128(wt + (((2 * u) ^ i8) * 16));
-            const uint4 q1 = lds128(wt + (((2 * u + 1) ^ i8) * 16));
-            const uint32_t sw = lds32(sft + u * 512);
-            if (!mbar_wait(smem_u32(&bar_aempty[a]), ((q / kNS) & 1) ^ 1, p.err)) { s_abort = 1; break; }
-            tc_fence_after();
-            if (t == 0) {
-              // permute the activation atom of this K slice in place
-              const uint32_t xa = xs + u * (kNT * 128);
-#pragma unroll
-              for (int j = i; j < kNT * 8; j += 128) sts128(xa + j * 16, perm_x8(lds128(xa + j * 16)));
-            }
-            uint32_t s0, s1, s2, s3;
-            scale_pair_to_bf16x2(sw & 0xFFFFu, s0, s1);
-            scale_pair_to_bf16x2(sw >> 16, s2, s3);
-            uint32_t o0[16], o1[16];
-            dequant32_perm(q0, s0, s1, o0);
-            dequant32_perm(q1, s2, s3, o1);
-            const uint32_t col = tmem + lane_base + (a * kT + t) * 32;
-            tmem_st16(col, o0);
-            tmem_st16(col + 16, o1);
+          // my slices two at a time: one tensor-memory store wait per pair
+          for (int u = first; u < nsub; u += 2 * kG) {
+            const int u2 = u + kG;
+            const bool two = u2 < nsub;
+            if (!slice(st, u, qbase + u) || (two && !slice(st, u2, qbase + u2))) { s_abort = 1; break; }
             tmem_wait_st();
             if (t == 0) fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(smem_u32(&bar_afull[a]));
+            mbar_arrive(smem_u32(&bar_afull[(qbase + u) % kNS]));
+            if (two) mbar_arrive(smem_u32(&bar_afull[(qbase + u2) % kNS]));
           }
         }
         qbase += nsub;
@@ -501,49 +578,90 @@ __global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, 1)
     const bool ok_acc = active && mbar_wait(smem_u32(&bar_accum), 0, p.err);
     if (!ok_acc && active) s_abort = 1;
     tc_fence_after();
-    epi_sync<kEpiThreads>();  // every ring stage is consumed: reuse it for partials
-    if (active && !s_abort && wg < kT) {
-      const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
-      const uint32_t dcol = tmem + lane_base + C::kTmemA + wg * kNT;
-      const float post = C::kFp4 ? static_cast<float>(1 << kShift) : 1.0f;
+    const float post = C::kFp4 ? static_cast<float>(1 << kShift) : 1.0f;
+    // Partials of (tile t, token n, row i).  Push mode: rank `rank` owns rows
+    // [r_lo, r_hi) and receives them from every rank into
+    // inbox[src][t][n][row - r_lo]; pull mode: each rank leaves its partials in
+    // its own ring as red[t][n][row] and the owner reads them through DSMEM.
+    if constexpr (C::kPush) {
+      if (S > 1) cluster_wait();  // all peers' inbox barriers are initialised
+      if (active && wg < kT) {
+        const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
+        const uint32_t dcol = tmem + lane_base + C::kTmemA + wg * C::kAcc * kNT;
+        const uint32_t owner = static_cast<uint32_t>(i / R);
+        const int rr = i - static_cast<int>(owner) * R;
+        const int rows_owner = min(R, 128 - static_cast<int>(owner) * R);
+        const uint32_t base = inbox + ((rank * kT + wg) * kNT * rows_owner + rr) * 4;
+        const uint32_t rbase = S > 1 ? mapa(base, owner) : base;
+        const uint32_t rbar = S > 1 ? mapa(smem_u32(&bar_inbox), owner) : 0u;
 #pragma unroll
-      for (int c = 0; c < kNT; c += 8) {
-        uint32_t v[8];
-        tmem_ld8(dcol + c, v);
-        tmem_wait_ld();
+        for (int c = 0; c < kNT; c += 8) {
+          float acc8[8];
+          load_acc<C::kAcc, kNT>(dcol + c, acc8);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) stsf(ring + ((wg * kNT + c + j) * 128 + i) * 4, __uint_as_float(v[j]) * post);
+          for (int j = 0; j < 8; ++j) {
+            const float val = acc8[j] * post;
+            const uint32_t off = (c + j) * rows_owner * 4;
+            if (S > 1) st_async_f32(rbase + off, val, rbar);
+            else stsf(rbase + off, val);
+          }
+        }
+      }
+      tc_fence_before();
+      if (S > 1) {
+        if (!mbar_wait<true>(smem_u32(&bar_inbox), 0, p.err)) s_abort = 1;
+      } else {
+        epi_sync<kEpiThreads>();
+      }
+    } else {
+      epi_sync<kEpiThreads>();  // every ring stage is consumed: reuse it for partials
+      if (active && !s_abort && wg < kT) {
+        const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
+        const uint32_t dcol = tmem + lane_base + C::kTmemA + wg * C::kAcc * kNT;
+#pragma unroll
+        for (int c = 0; c < kNT; c += 8) {
+          float acc8[8];
+          load_acc<C::kAcc, kNT>(dcol + c, acc8);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) stsf(ring + ((wg * kNT + c + j) * 128 + i) * 4, acc8[j] * post);
+        }
+      }
+      tc_fence_before();
+      epi_sync<kEpiThreads>();
+      if (S > 1) {
+        if (tid == 0) {
+          for (uint32_t r2 = 0; r2 < S; ++r2) mbar_arrive_cluster(mapa(smem_u32(&bar_red_ready), r2));
+        }
+        if (!mbar_wait<true>(smem_u32(&bar_red_ready), 0, p.err)) s_abort = 1;
       }
     }
-    tc_fence_before();
-    epi_sync<kEpiThreads>();
-    if (S > 1) {
-      if (tid == 0) {
-        for (uint32_t r2 = 0; r2 < S; ++r2) mbar_arrive_cluster(mapa(smem_u32(&bar_red_ready), r2));
-      }
-      if (!mbar_wait<true>(smem_u32(&bar_red_ready), 0, p.err)) s_abort = 1;
-    }
-    // Sum of the cluster's partials for (tile t, token n, row i), rank order.
+    // Sum over the cluster ranks, in rank order, of the partial of
+    // (tile t, token n, row) for a row this rank owns.
     auto partial = [&](int t, int n, int row) -> float {
-      const uint32_t off = ring + ((t * kNT + n) * 128 + row) * 4;
-      if (S == 1) return ldsf(off);
-      float acc = 0.0f;
-      for (uint32_t r2 = 0; r2 < S; ++r2) {
-        float v;
-        asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(mapa(off, r2)) : "memory");
-        acc += v;
+      if constexpr (C::kPush) {
+        const int rows_mine = r_hi - r_lo;
+        float acc = 0.0f;
+        for (uint32_t src = 0; src < S; ++src)
+          acc += ldsf(inbox + (((src * kT + t) * kNT + n) * rows_mine + (row - r_lo)) * 4);
+        return acc;
+      } else {
+        const uint32_t off = ring + ((t * kNT + n) * 128 + row) * 4;
+        if (S == 1) return ldsf(off);
+        float acc = 0.0f;
+        for (uint32_t r2 = 0; r2 < S; ++r2) {
+          float v;
+          asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(mapa(off, r2)) : "memory");
+          acc += v;
+        }
+        return acc;
       }
-      return acc;
     };
     if (active && !s_abort) {
       pdl_wait();
       if constexpr (kMode == kDenseFp4 || kMode == kDenseBf16) {
-        const int rows_per = (128 + S - 1) / S;  // this rank reduces rows [r0, r1)
-        const int r0 = rank * rows_per;
-        const int r1 = min(128, r0 + rows_per);
         const float gs = p.gs ? __ldg(p.gs) : 1.0f;
-        for (int it = tid; it < (r1 - r0) * wk.ntok; it += kEpiThreads) {
-          const int n = it / (r1 - r0), row = r0 + it % (r1 - r0);
+        for (int it = tid; it < (r_hi - r_lo) * wk.ntok; it += kEpiThreads) {
+          const int n = it / (r_hi - r_lo), row = r_lo + it % (r_hi - r_lo);
           const int o = wk.out_base + row;
           if (o >= p.n_out) continue;
           uint16_t res;
@@ -554,7 +672,7 @@ __global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, 1)
             const float U = bf16_to_f32(f32_to_bf16_rn(partial(1, n, row) * gs));
             res = f32_to_bf16_rn(silu_exact(G) * U);
           }
-          p.out[static_cast<int64_t>(wk.orow[n]) * p.ldo + o] = res;
+          p.out[static_cast<int64_t>(n) * p.ldo + o] = res;
         }
       } else if constexpr (kMode == kMoeGateUp) {
         if (!wk.shared) {
@@ -562,7 +680,7 @@ __global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, 1)
           for (int it = tid; it < kT * 64 * wk.ntok; it += kEpiThreads) {
             const int n = it / (kT * 64), rem = it % (kT * 64);
             const int t = rem / 64, o = rem % 64;
-            const int feat = (blockIdx.x / S) * (kT * 64) + t * 64 + o;
+            const int feat = blockIdx.x * (kT * 64) + t * 64 + o;
             if (feat >= p.n_out) continue;
             const float u = partial(t, n, o) * al;
             const float gt = partial(t, n, o + 64) * al;
@@ -592,7 +710,7 @@ __global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, 1)
         }
       }
     }
-    if (S > 1) {
+    if (!C::kPush && S > 1) {
       epi_sync<kEpiThreads>();
       if (tid == 0) {
         for (uint32_t r2 = 0; r2 < S; ++r2) mbar_arrive_cluster(mapa(smem_u32(&bar_red_done), r2));
@@ -646,6 +764,8 @@ __global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, 1)
         }
       }
     }
+  } else if (C::kPush && S > 1) {
+    cluster_wait();  // the producer and MMA warps close their cluster-barrier phase
   }
 
   // ==================================================================== teardown

@@ -21,6 +21,7 @@ struct KernelInfo {
   int threads;
   int stage_bytes;
   int red_bytes;
+  int inbox_bytes;
   int tmem_cols;
 };
 
@@ -69,6 +70,7 @@ cudaError_t run_gemv(const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info
     info->threads = C::kThreads;
     info->stage_bytes = C::kStageBytes;
     info->red_bytes = C::kRedBytes;
+    info->inbox_bytes = C::kInboxBytes;
     info->tmem_cols = C::kTmemCols;
     return cudaSuccess;
   }
