@@ -105,22 +105,27 @@ fp4gemv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FP4GEMV_OK :
 
 int pick_nt(int m) { return m <= 16 ? 16 : m <= 32 ? 32 : m <= 64 ? 64 : 128; }
 
-cudaError_t kernel_info(int mode, int t, int nt, KernelInfo* info) {
+// Pseudo-mode of the register-fed dense NVFP4 kernel (M <= 16).
+constexpr int kDenseFp4Rf = 100;
+
+cudaError_t kernel_info(int mode, int nt, KernelInfo* info) {
   GemvParams dummy;
   LaunchCfg cfg{};
   switch (mode) {
-    case fp4::kDenseFp4: return fp4::launch_dense_fp4(t, nt, dummy, cfg, info);
-    case fp4::kDenseBf16: return fp4::launch_dense_bf16(t, nt, dummy, cfg, info);
-    default: return fp4::launch_moe(mode, t, nt, dummy, cfg, info);
+    case kDenseFp4Rf: return fp4::launch_dense_rf(nt, dummy, cfg, info);
+    case fp4::kDenseFp4: return fp4::launch_dense_fp4(nt, dummy, cfg, info);
+    case fp4::kDenseBf16: return fp4::launch_dense_bf16(nt, dummy, cfg, info);
+    default: return fp4::launch_moe(mode, nt, dummy, cfg, info);
   }
 }
 
-cudaError_t kernel_launch(int mode, int t, int nt, const GemvParams& p, const LaunchCfg& cfg) {
+cudaError_t kernel_launch(int mode, int nt, const GemvParams& p, const LaunchCfg& cfg) {
   g_launches.fetch_add(1, std::memory_order_relaxed);
   switch (mode) {
-    case fp4::kDenseFp4: return fp4::launch_dense_fp4(t, nt, p, cfg, nullptr);
-    case fp4::kDenseBf16: return fp4::launch_dense_bf16(t, nt, p, cfg, nullptr);
-    default: return fp4::launch_moe(mode, t, nt, p, cfg, nullptr);
+    case kDenseFp4Rf: return fp4::launch_dense_rf(nt, p, cfg, nullptr);
+    case fp4::kDenseFp4: return fp4::launch_dense_fp4(nt, p, cfg, nullptr);
+    case fp4::kDenseBf16: return fp4::launch_dense_bf16(nt, p, cfg, nullptr);
+    default: return fp4::launch_moe(mode, nt, p, cfg, nullptr);
   }
 }
 
@@ -184,14 +189,20 @@ fp4gemv_status dense_launch(int mode, const void* x, int64_t ldx, const void* w,
   fp4gemv_status st = device_state(&err, &sms);
   if (st != FP4GEMV_OK) return st;
 
-  const int T = silu_mul ? 2 : 1;
-  const int NT = pick_nt(M);
+  // NVFP4 weights and M <= 16: the register-fed kernel (8- or 16-token tile);
+  // otherwise the tcgen05 kernel.
+  const bool rf = fp4w && M <= 16;
+  const int kmode = rf ? kDenseFp4Rf : mode;
+  const int NT = rf ? (M <= 8 ? 8 : 16) : pick_nt(M);
   KernelInfo info{};
-  if (kernel_info(mode, T, NT, &info) != cudaSuccess) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
+  if (kernel_info(kmode, NT, &info) != cudaSuccess) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
   int nstages = 0, per_sm = 0;
   size_t smem = 0;
   size_ring(info, &nstages, &smem, &per_sm);
-  const int tiles = (n_out + 127) / 128;
+  // A tile is 128 weight rows: 128 output features, or with silu_mul 64
+  // features (64 gate rows + the 64 matching up rows, two 64-row boxes).
+  const int box_rows = silu_mul ? 64 : 128;
+  const int tiles = silu_mul ? (n_out + 63) / 64 : (n_out + 127) / 128;
   const int stage_k = fp4w ? fp4::kStageK4 : fp4::kStageK16;
   const int S0 = pick_split(tiles, K, stage_k, sms * per_sm);
   const int kslab = ((K + S0 - 1) / S0 + 63) / 64 * 64;
@@ -200,9 +211,10 @@ fp4gemv_status dense_launch(int mode, const void* x, int64_t ldx, const void* w,
   GemvParams p;
   std::memset(&p, 0, sizeof(p));
   if (fp4w) {
-    if (!encode_2d(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, K / 2, N, K / 2, 128, 128)) return FP4GEMV_ERR_CUDA;
+    if (!encode_2d(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, K / 2, N, K / 2, 128, box_rows))
+      return FP4GEMV_ERR_CUDA;
   } else {
-    if (!encode_2d(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w, K, N, static_cast<uint64_t>(K) * 2, 64, 128))
+    if (!encode_2d(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w, K, N, static_cast<uint64_t>(K) * 2, 64, box_rows))
       return FP4GEMV_ERR_CUDA;
   }
   if (fp4w) {
@@ -220,6 +232,7 @@ fp4gemv_status dense_launch(int mode, const void* x, int64_t ldx, const void* w,
   p.M = M;
   p.n_out = n_out;
   p.n_half = N / 2;
+  p.silu = silu_mul;
   p.K = K;
   p.k_split = kslab;
   p.rows_w = N;
@@ -233,7 +246,7 @@ fp4gemv_status dense_launch(int mode, const void* x, int64_t ldx, const void* w,
   cfg.smem = smem;
   cfg.pdl = pdl;
   cfg.stream = stream;
-  return from_cuda(kernel_launch(mode, T, NT, p, cfg));
+  return from_cuda(kernel_launch(kmode, NT, p, cfg));
 }
 
 }  // namespace
@@ -305,7 +318,7 @@ fp4gemv_status fp4gemv_moe_gate_up(const void* x, const int32_t* ids, int M, int
   if (st != FP4GEMV_OK) return st;
   const int NT = M <= 16 ? 16 : 32;
   KernelInfo info{};
-  if (kernel_info(fp4::kMoeGateUp, 2, NT, &info) != cudaSuccess) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
+  if (kernel_info(fp4::kMoeGateUp, NT, &info) != cudaSuccess) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
   int nstages = 0, per_sm = 0;
   size_t smem = 0;
   size_ring(info, &nstages, &smem, &per_sm);
@@ -313,7 +326,8 @@ fp4gemv_status fp4gemv_moe_gate_up(const void* x, const int32_t* ids, int M, int
   std::memset(&p, 0, sizeof(p));
   if (!encode_2d(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w1, H / 2, static_cast<uint64_t>(E) * 2 * I, H / 2, 128, 128))
     return FP4GEMV_ERR_CUDA;
-  if (!encode_2d(&p.tm_w2, CU_TENSOR_MAP_DATA_TYPE_UINT8, wsh, H / 2, 2 * static_cast<uint64_t>(SI), H / 2, 128, 128))
+  // shared expert: [gate | up] halves read as paired 64-row boxes
+  if (!encode_2d(&p.tm_w2, CU_TENSOR_MAP_DATA_TYPE_UINT8, wsh, H / 2, 2 * static_cast<uint64_t>(SI), H / 2, 128, 64))
     return FP4GEMV_ERR_CUDA;
   p.sf = w1_sf;
   p.sf2 = ssh;
@@ -338,8 +352,8 @@ fp4gemv_status fp4gemv_moe_gate_up(const void* x, const int32_t* ids, int M, int
   p.rows_per_expert = 2 * I;
   p.rows_w = 2 * SI;
   p.shared_n_out = SI;
-  p.routed_tiles = (I + 127) / 128;
-  p.shared_tiles = (SI + 127) / 128;
+  p.routed_tiles = I / 64;             // one [up; gate] 128-row group (64 features) per tile
+  p.shared_tiles = (SI + 63) / 64;     // 64 features per paired tile
   p.kbp = p.kbp2 = ((H / 16) + 3) / 4 * 4;
   p.sf_expert_bytes = static_cast<uint32_t>(fp4gemv_scale_bytes(2 * I, H));
   p.nstages = nstages;
@@ -351,7 +365,7 @@ fp4gemv_status fp4gemv_moe_gate_up(const void* x, const int32_t* ids, int M, int
   cfg.smem = smem;
   cfg.pdl = pdl;
   cfg.stream = stream;
-  return from_cuda(kernel_launch(fp4::kMoeGateUp, 2, NT, p, cfg));
+  return from_cuda(kernel_launch(fp4::kMoeGateUp, NT, p, cfg));
 }
 
 size_t fp4gemv_moe_down_combine_workspace_bytes(int M, int topk, int H) {
@@ -384,7 +398,7 @@ fp4gemv_status fp4gemv_moe_down_combine(const void* act, const int32_t* ids, con
   if (st != FP4GEMV_OK) return st;
   const int NT = M <= 16 ? 16 : 32;
   KernelInfo info{};
-  if (kernel_info(fp4::kMoeDown, 1, NT, &info) != cudaSuccess) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
+  if (kernel_info(fp4::kMoeDown, NT, &info) != cudaSuccess) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
   int nstages = 0, per_sm = 0;
   size_t smem = 0;
   size_ring(info, &nstages, &smem, &per_sm);
@@ -440,7 +454,7 @@ fp4gemv_status fp4gemv_moe_down_combine(const void* act, const int32_t* ids, con
   cfg.smem = smem;
   cfg.pdl = pdl;
   cfg.stream = stream;
-  return from_cuda(kernel_launch(fp4::kMoeDown, 1, NT, p, cfg));
+  return from_cuda(kernel_launch(fp4::kMoeDown, NT, p, cfg));
 }
 
 fp4gemv_status fp4gemv_get_device_error(cudaStream_t stream) {

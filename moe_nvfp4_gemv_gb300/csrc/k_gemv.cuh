@@ -5,31 +5,36 @@
 // (vllm.models.flint.ops.nvfp4_gemv nvfp4_gemv / bf16_gemv,
 // vllm.models.flint.ops.moe_gemv gate_up / down_combine).
 //
-// Swap-AB: a CTA owns kT tiles of 128 weight rows (the MMA M dimension); the
-// tokens are the MMA N dimension (kNT = 16 .. 128).  Its K range is a slice
-// of K; the kS CTAs of a cluster split K and reduce their fp32 partials
-// through distributed shared memory in rank order (deterministic).
+// Swap-AB: a CTA owns one tile of 128 weight rows (the MMA M dimension); the
+// tokens are the MMA N dimension (kNT = 16 .. 128).  A tile is either 128
+// consecutive rows or, for the silu_mul epilogue, two 64-row boxes: 64 gate
+// rows and the 64 up rows of the same output features, so one CTA holds both
+// operands of its outputs.  Its K range is a slice of K; the S CTAs of a
+// cluster split K and reduce their fp32 partials through distributed shared
+// memory in rank order (deterministic).
 //
-// Warp roles (kT dequant warpgroups, then one producer and one MMA warp):
-//   producer  lane 0 streams weight tiles (TMA, 128-byte swizzle) and the
+// Warp roles (kW worker warpgroups, then one producer warp):
+//   producer  lane 0 streams weight boxes (TMA, 128-byte swizzle) and the
 //             matching 512-byte scale chunks (bulk copies) into a ring of
-//             shared-memory stages; with PDL these loads are issued before
-//             griddepcontrol.wait.  All 32 lanes then copy the activation
-//             rows of each stage with cp.async (after the wait).
-//   dequant   warpgroup t: thread i owns row i of tile t.  Per 64-wide K
-//             slice it reads 32 code bytes and 4 scale bytes, dequantizes
-//             them exactly to bf16 (dequant.cuh) and stores them with
-//             tcgen05.st into a tensor-memory A slot.  Warpgroup 0 also
-//             permutes the activation slice in shared memory to the weight
-//             pairs' K order.
-//   mma       one thread issues tcgen05.mma (A from tensor memory, B = the
-//             activations from shared memory, fp32 D in tensor memory) and
-//             frees A slots / ring stages with tcgen05.commit.
-//   epilogue  the dequant warpgroups read D with tcgen05.ld, exchange
+//             shared-memory stages of 256 K; with PDL these loads are issued
+//             before griddepcontrol.wait.  Activations follow after the wait
+//             (TMA for dense rows, cp.async gathers by all 32 lanes for MoE).
+//   workers   warpgroup w takes the 64-wide K slices q = w, w + kW, ...  For
+//             each slice thread i (row i) reads 32 code bytes and 4 scale
+//             bytes, dequantizes them exactly to bf16 (dequant.cuh) and
+//             stores them with tcgen05.st into one of the warpgroup's own
+//             tensor-memory A slots; the warpgroup also permutes the slice's
+//             activations in shared memory to the weight pairs' K order.
+//             After a warpgroup barrier one elected thread issues the four
+//             K=16 tcgen05.mma of the slice into the warpgroup's own fp32
+//             accumulator and frees the slot (and, once per stage, the ring
+//             stage) with tcgen05.commit.  There is no hand-off to a separate
+//             MMA thread: each warpgroup runs its own dequant -> MMA loop.
+//   epilogue  the workers sum the kW accumulators (tcgen05.ld), exchange
 //             partials through (distributed) shared memory and apply the
 //             mode's epilogue.
-// The BF16-weight mode has no dequant step: both operands come from shared
-// memory by TMA (tcgen05.mma with two smem descriptors).
+// The BF16-weight mode has no dequant step: one warpgroup, whose elected
+// thread issues tcgen05.mma with both operands in shared memory.
 #pragma once
 
 #include <cuda.h>
@@ -41,24 +46,24 @@
 namespace fp4 {
 
 enum Mode : int {
-  kDenseFp4 = 0,   // nvfp4_gemv; kT = 2 fuses silu_mul ([gate | up] halves)
+  kDenseFp4 = 0,   // nvfp4_gemv, optionally with silu_mul ([gate | up] halves)
   kDenseBf16 = 1,  // bf16_gemv and the GEMM of the dequantize + GEMM path
   kMoeGateUp = 2,  // routed experts ([up; gate] 64-row groups) + shared expert
   kMoeDown = 3,    // routed + shared experts into scratch, last CTA combines
 };
 
 constexpr int kMaxStages = 8;
-constexpr int kSlots = 4;       // tensor-memory A slots (default)
-constexpr int kMaxSlots = 8;
 constexpr int kSubK = 64;       // K per A slot / per activation atom
 constexpr int kStageK4 = 256;   // K per ring stage, NVFP4 weights (128 B per row)
 constexpr int kStageK16 = 64;   // K per ring stage, bf16 weights (128 B per row)
 constexpr int kMaxNT = 128;
+constexpr int kMaxWG = 2;
+constexpr int kMaxSlots = 4;
 
 struct GemvParams {
   CUtensorMap tm_w;    // weights read by routed / dense CTAs
   CUtensorMap tm_w2;   // shared-expert weights (MoE)
-  CUtensorMap tm_x;    // bf16 mode: activations [M, K], box {64, kNT}
+  CUtensorMap tm_x;    // dense modes: activations (TMA)
   const uint8_t* sf;   // scales of tm_w rows (MoE: E consecutive buffers)
   const uint8_t* sf2;  // scales of tm_w2 rows
   const uint16_t* x;   // activations (bf16 bits) of routed / dense CTAs
@@ -77,7 +82,8 @@ struct GemvParams {
   uint32_t epoch;      // down: nonzero tag of this call (counters from other calls read as 0)
   int M;               // tokens
   int n_out;           // dense: output features; MoE routed: output features
-  int n_half;          // dense silu: N / 2 (first up row); shared gate_up: SI
+  int n_half;          // paired tiles: first up row (dense silu: N / 2; shared gate_up: SI)
+  int silu;            // dense: 1 = silu_mul epilogue (paired tiles)
   int K;               // dense / routed K
   int K2;              // shared-expert K
   int k_split;         // dense: K elements per cluster rank (multiple of 64)
@@ -96,15 +102,17 @@ struct GemvParams {
 struct CtaWork {
   int active;      // 0: nothing to compute
   int shared;      // 1: shared-expert CTA (MoE)
+  int paired;      // 1: two 64-row boxes (gate rows, up rows); 0: one 128-row box
   int ntok;        // valid B rows
   int k_begin, k_end;
-  int wrow[2];     // tensor-map row of each tile's first row
-  int srow[2];     // first row in the scale buffer's row space
-  int sgroups[2];  // 128-row scale groups to copy per tile (0..2)
+  int wrow[2];     // tensor-map row of each box
+  int srow[2];     // scale-buffer row of each box's first row
+  int sgroup[3];   // 128-row scale groups copied per stage: box 0's, then box 1's first and
+                   // second (a 64-row box that starts off a 64-row boundary straddles two);
+                   // -1: none (beyond the buffer, or not needed)
   int kbp;
   int expert;
-  int out_base;    // first output feature of tile 0
-  float scale;     // alpha[e] or the global scale (loaded after the PDL wait)
+  int out_base;    // first output feature of the tile
   int tok[kMaxNT];   // B row -> activation row
   int orow[kMaxNT];  // B row -> output row (pair / token)
   long long xoff[kMaxNT];  // B row -> element offset of its activation row
@@ -116,34 +124,26 @@ __host__ __device__ constexpr int pow2_at_least(int v) {
   return p;
 }
 
-template <int kMode, int kT, int kNT>
+template <int kMode, int kNT>
 struct Cfg {
   static constexpr bool kFp4 = kMode != kDenseBf16;
-  // Dequant warpgroups per tile: the G warpgroups of a tile take turns on
-  // consecutive 64-wide K slices, so G slices of a tile are in flight.
-  static constexpr int kG = kFp4 ? 2 : 1;
-  static constexpr int kWarpgroups = kT * kG;
-  static constexpr int kWarps = 4 * kWarpgroups + 2;
-  static constexpr int kThreads = kWarps * 32;
-  static constexpr int kProducerWarp = 4 * kWarpgroups;
-  static constexpr int kMmaWarp = 4 * kWarpgroups + 1;
+  static constexpr int kW = kFp4 ? 2 : 1;  // worker warpgroups
+  static constexpr int kThreads = kW * 128 + 32;
+  static constexpr int kProducerWarp = 4 * kW;
   static constexpr int kStageK = kFp4 ? kStageK4 : kStageK16;
+  static constexpr int kSlicesPerStage = kStageK / kSubK;  // 4 (fp4) or 1 (bf16)
   static constexpr int kWTileBytes = 128 * 128;
-  static constexpr int kSfTileBytes = kFp4 ? 2 * 4 * 512 : 0;
+  static constexpr int kSfTileBytes = kFp4 ? 3 * 4 * 512 : 0;  // three 128-row scale groups x 4 chunks
   static constexpr int kXBytes = kNT * kStageK * 2;
-  static constexpr int kXOff = kT * (kWTileBytes + kSfTileBytes);
+  static constexpr int kXOff = kWTileBytes + kSfTileBytes;
   static constexpr int kStageBytes = kXOff + kXBytes;
-  // Tensor memory: A slots (64 K each, fp4 modes) and kAcc independent fp32
-  // accumulators per tile.  Consecutive K=16 MMAs of a slice go to different
-  // accumulators so they do not serialise on one accumulator; the epilogue
-  // sums them.  Sized to 256 columns (two CTAs per SM) for one tile, 512 for
-  // two.
-  static constexpr int kSlotsUsed = (kT == 2 && kNT <= 16) ? 6 : kSlots;
-  static constexpr int kTmemA = kFp4 ? kSlotsUsed * kT * 32 : 0;
-  static constexpr int kBudget = kT == 1 ? 256 : 512;
-  static constexpr int kAcc = kTmemA + 4 * kT * kNT <= kBudget ? 4 : kTmemA + 2 * kT * kNT <= kBudget ? 2 : 1;
-  static constexpr int kTmemCols = pow2_at_least(kTmemA + kAcc * kT * kNT);
-  static constexpr int kRedBytes = kT * kNT * 128 * 4;
+  // Tensor memory: one fp32 accumulator (kNT columns) per warpgroup, then
+  // kSlots A slots (32 columns = 64 bf16 K) per warpgroup.  Sized to 256
+  // columns (two CTAs per SM) up to kNT = 64.
+  static constexpr int kAccCols = kW * kNT;
+  static constexpr int kSlots = !kFp4 ? 0 : kNT <= 32 ? 3 : kNT <= 64 ? 2 : 4;
+  static constexpr int kTmemCols = pow2_at_least(kAccCols + kW * kSlots * 32);
+  static constexpr int kRedBytes = kNT * 128 * 4;
   // Dense modes read contiguous activation rows with TMA; the MoE modes
   // gather rows by token / pair with cp.async from the producer lanes.
   static constexpr bool kXTma = kMode == kDenseFp4 || kMode == kDenseBf16;
@@ -151,12 +151,12 @@ struct Cfg {
   // Split-K partials are pushed to the owning cluster rank (st.async into a
   // dedicated inbox) when the inbox is small; otherwise pulled through DSMEM
   // from the (reused) ring.
-  static constexpr bool kPush = kT * kNT <= 64;
-  static constexpr int kInboxBytes = kPush ? kT * kNT * 136 * 4 : 0;
+  static constexpr bool kPush = kNT <= 64;
+  static constexpr int kInboxBytes = kPush ? kNT * 136 * 4 : 0;
   static_assert(kNT % 16 == 0 && kNT >= 16 && kNT <= kMaxNT, "token tile");
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
   static_assert(kTmemCols <= 512, "tensor memory");
-  static_assert(kSlotsUsed <= kMaxSlots, "slot barriers");
+  static_assert(kSlots <= kMaxSlots && kW <= kMaxWG, "barrier arrays");
   // CTAs per SM the launch aims for (tensor memory is 512 columns per SM)
   static constexpr int kMinBlocks = kTmemCols <= 256 ? 2 : 1;
 };
@@ -171,39 +171,59 @@ __device__ __forceinline__ float silu_exact(float g) { return __fdiv_rn(g, 1.0f 
 // SiLU with the fast exponential and division (the routed experts' fast sigmoid).
 __device__ __forceinline__ float silu_fast(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
-// Named barrier over the epilogue (dequant) warpgroups only.
+// Named barriers: 1 = all worker threads; 2 + w = warpgroup w.
 template <int kThreadsEpi>
 __device__ __forceinline__ void epi_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kThreadsEpi) : "memory");
 }
+// Warpgroup barrier that also ORs a flag over the warpgroup's threads (the
+// result is the same in all 128 threads).
+template <int kId>
+__device__ __forceinline__ bool bar_red_or(bool v) {
+  uint32_t r;
+  asm volatile("{ .reg .pred p, q; setp.ne.u32 q, %1, 0; bar.red.or.pred p, %2, 128, q; selp.u32 %0, 1, 0, p; }"
+               : "=r"(r)
+               : "r"(static_cast<uint32_t>(v)), "n"(kId)
+               : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ bool wg_sync_or(int w, bool v) { return w == 0 ? bar_red_or<2>(v) : bar_red_or<3>(v); }
 
-// Eight columns [c, c+8) of a tile's accumulator: the sum of its kAcc
-// partial accumulators (kNT columns apart) in tensor memory.
-template <int kAcc, int kNT>
-__device__ __forceinline__ void load_acc(uint32_t taddr, float (&out)[8]) {
-  uint32_t v[8];
-  tmem_ld8(taddr, v);
-  tmem_wait_ld();
-#pragma unroll
-  for (int j = 0; j < 8; ++j) out[j] = __uint_as_float(v[j]);
-#pragma unroll
-  for (int a = 1; a < kAcc; ++a) {
-    tmem_ld8(taddr + a * kNT, v);
-    tmem_wait_ld();
-#pragma unroll
-    for (int j = 0; j < 8; ++j) out[j] += __uint_as_float(v[j]);
+// Rows of a tile are reduced across cluster ranks per feature unit: a tile
+// whose feature o combines rows o and o + 64 (paired gate/up boxes, routed
+// [up; gate] groups) has 64-row units, any other tile 128-row units.
+template <int kMode>
+__device__ __forceinline__ int feature_unit(const CtaWork& w) {
+  return (w.paired || (kMode == kMoeGateUp && !w.shared)) ? 64 : 128;
+}
+
+// Tensor-map row, scale row and scale groups of one box (box 0: 128 or 64
+// rows starting on a group or half-group boundary, one group; box 1: 64 rows,
+// one or two groups).
+template <typename Work>
+__device__ __forceinline__ void set_box(Work& w, int b, int wrow, int srow, int groups_total) {
+  w.wrow[b] = wrow;
+  w.srow[b] = srow;
+  const int g0 = srow / 128;
+  if (b == 0) {
+    w.sgroup[0] = g0 < groups_total ? g0 : -1;
+  } else {
+    const int g1 = (srow + 63) / 128;
+    w.sgroup[1] = g0 < groups_total ? g0 : -1;
+    w.sgroup[2] = (g1 != g0 && g1 < groups_total) ? g1 : -1;
   }
 }
 
-// Resolve what this CTA computes (thread 0).  Returns false if the ids could
-// not be read yet (gate_up routed: caller waits for the previous grid first).
-template <int kMode, int kT, int kNT>
+// Resolve what this CTA computes (producer lane 0, before the barriers are
+// initialised).  gate_up routed CTAs wait for the previous grid first: their
+// expert ids come from the router.
+template <int kMode, int kNT>
 __device__ void resolve_work(const GemvParams& p, CtaWork& w, uint32_t split) {
   w.active = 1;
   w.shared = 0;
+  w.paired = 0;
   w.expert = -1;
-  w.scale = 1.0f;
-  w.sgroups[0] = w.sgroups[1] = 0;
+  w.sgroup[1] = w.sgroup[2] = -1;
   w.wrow[1] = w.srow[1] = 0;
   const int tile = blockIdx.x / max(1u, cluster_nctarank());
   if constexpr (kMode == kDenseFp4 || kMode == kDenseBf16) {
@@ -211,15 +231,15 @@ __device__ void resolve_work(const GemvParams& p, CtaWork& w, uint32_t split) {
     w.k_begin = static_cast<int>(split) * p.k_split;
     w.k_end = min(p.K, w.k_begin + p.k_split);
     w.kbp = p.kbp;
-    w.out_base = tile * 128;
-    w.wrow[0] = tile * 128;
-    if (kT == 2) w.wrow[1] = p.n_half + tile * 128;
-    for (int t = 0; t < kT; ++t) {
-      w.srow[t] = w.wrow[t];
-      const int groups_total = (p.rows_w + 127) / 128;
-      const int g0 = w.srow[t] / 128;
-      const int g1 = min(w.srow[t] + 127, p.rows_w - 1) / 128;
-      w.sgroups[t] = g0 < groups_total ? g1 - g0 + 1 : 0;
+    const int groups_total = (p.rows_w + 127) / 128;
+    if (p.silu) {
+      w.paired = 1;
+      w.out_base = tile * 64;
+      set_box(w, 0, tile * 64, tile * 64, groups_total);                        // gate rows
+      set_box(w, 1, p.n_half + tile * 64, p.n_half + tile * 64, groups_total);  // up rows
+    } else {
+      w.out_base = tile * 128;
+      set_box(w, 0, tile * 128, tile * 128, groups_total);
     }
   } else {
     // MoE: blockIdx.y < P: routed pair column; else shared-expert token chunk.
@@ -254,13 +274,10 @@ __device__ void resolve_work(const GemvParams& p, CtaWork& w, uint32_t split) {
       w.expert = e;
       w.k_end = p.K;
       w.kbp = p.kbp;
-      for (int t = 0; t < kT; ++t) {
-        const int r0 = tile * 128 * kT + t * 128;  // row inside the expert
-        w.wrow[t] = e * p.rows_per_expert + r0;
-        w.srow[t] = r0;
-        w.sgroups[t] = r0 < p.rows_per_expert ? 1 : 0;
-      }
-      w.out_base = tile * 128;
+      // 128 consecutive rows of expert e (gate_up: one [up; gate] group)
+      const int r0 = tile * 128;
+      set_box(w, 0, e * p.rows_per_expert + r0, r0, (p.rows_per_expert + 127) / 128);
+      w.out_base = kMode == kMoeGateUp ? tile * 64 : tile * 128;
       for (int m = 0; m < kNT; ++m) w.xoff[m] = static_cast<long long>(w.tok[m]) * p.ldx;
     } else {
       const int chunk = col - p.P;
@@ -271,28 +288,29 @@ __device__ void resolve_work(const GemvParams& p, CtaWork& w, uint32_t split) {
       for (int n = 0; n < kNT; ++n) w.tok[n] = w.orow[n] = t0 + (n < w.ntok ? n : 0);
       w.k_end = p.K2;
       w.kbp = p.kbp2;
-      w.wrow[0] = tile * 128;
-      if (kT == 2) w.wrow[1] = p.n_half + tile * 128;
-      for (int t = 0; t < kT; ++t) {
-        w.srow[t] = w.wrow[t];
-        const int groups_total = (p.rows_w + 127) / 128;
-        const int g0 = w.srow[t] / 128;
-        const int g1 = min(w.srow[t] + 127, p.rows_w - 1) / 128;
-        w.sgroups[t] = g0 < groups_total ? g1 - g0 + 1 : 0;
+      const int groups_total = (p.rows_w + 127) / 128;
+      if (kMode == kMoeGateUp) {
+        w.paired = 1;
+        w.out_base = tile * 64;
+        set_box(w, 0, tile * 64, tile * 64, groups_total);                        // gate rows
+        set_box(w, 1, p.n_half + tile * 64, p.n_half + tile * 64, groups_total);  // up rows
+      } else {
+        w.out_base = tile * 128;
+        set_box(w, 0, tile * 128, tile * 128, groups_total);
       }
-      w.out_base = tile * 128;
       for (int m = 0; m < kNT; ++m) w.xoff[m] = static_cast<long long>(w.tok[m]) * p.ldx2;
     }
   }
 }
 
-template <int kMode, int kT, int kNT>
-__global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, Cfg<kMode, kT, kNT>::kMinBlocks)
+template <int kMode, int kNT>
+__global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kMinBlocks)
     gemv_kernel(const __grid_constant__ GemvParams p) {
-  using C = Cfg<kMode, kT, kNT>;
-  constexpr int kEpiThreads = C::kWarpgroups * 128;
-  constexpr int kG = C::kG;
-  constexpr int kNS = C::kSlotsUsed;
+  using C = Cfg<kMode, kNT>;
+  constexpr int kW = C::kW;
+  constexpr int kEpiThreads = kW * 128;
+  constexpr int kNS = C::kSlots;
+  constexpr int kSPS = C::kSlicesPerStage;
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-aligned ring, addressed through 32-bit shared-window addresses; the
@@ -301,8 +319,7 @@ __global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, Cfg<kMode, kT, 
   const uint32_t inbox = ring + p.nstages * C::kStageBytes;
   __shared__ __align__(8) uint64_t bar_full[kMaxStages];
   __shared__ __align__(8) uint64_t bar_empty[kMaxStages];
-  __shared__ __align__(8) uint64_t bar_afull[kMaxSlots];
-  __shared__ __align__(8) uint64_t bar_aempty[kMaxSlots];
+  __shared__ __align__(8) uint64_t bar_aempty[kMaxWG * kMaxSlots];
   __shared__ __align__(8) uint64_t bar_accum;
   __shared__ __align__(8) uint64_t bar_inbox;
   __shared__ __align__(8) uint64_t bar_red_ready;
@@ -318,42 +335,82 @@ __global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, Cfg<kMode, kT, 
   const uint32_t S = cluster_nctarank();
   const uint32_t rank = S > 1 ? cluster_ctarank() : 0;
   const int nstages = p.nstages;
-  const int R = (128 + static_cast<int>(S) - 1) / static_cast<int>(S);  // rows reduced per cluster rank
-  const int r_lo = static_cast<int>(rank) * R;
-  const int r_hi = min(128, r_lo + R);
 
   // For gate_up the routed experts are only known once the router's output
   // (ids) is complete; every other mode reads ids / weights before the wait.
   constexpr bool kIdsAfterWait = kMode == kMoeGateUp;
+  const uint64_t pol_w = policy_evict_first();
+  const uint64_t pol_x = policy_evict_last();
+
+  // ------------------------------------------------------------------ prologue
+  // The producer resolves the work, initialises every barrier and starts the
+  // weight stream before the CTA-wide barrier; warp 0 allocates tensor memory
+  // meanwhile.
+  int pre = 0;  // stages whose weights the producer has issued
+  auto stage_count = [&](const CtaWork& wk) {
+    return wk.active ? (wk.k_end - wk.k_begin + C::kStageK - 1) / C::kStageK : 0;
+  };
+  auto issue_weights = [&](const CtaWork& wk, int s) {
+    const int slot = s % nstages;
+    const uint32_t st = ring + slot * C::kStageBytes;
+    const uint32_t fb = smem_u32(&bar_full[slot]);
+    const int k0 = wk.k_begin + s * C::kStageK;
+    const int kvalid = min(C::kStageK, wk.k_end - k0);
+    const int nchunks = kvalid / kSubK;
+    const CUtensorMap* tmw = wk.shared ? &p.tm_w2 : &p.tm_w;
+    uint32_t bytes = C::kWTileBytes;
+    if constexpr (C::kFp4) {
+      for (int g = 0; g < 3; ++g) bytes += (wk.sgroup[g] >= 0 ? nchunks * 512 : 0);
+    }
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(fb), "r"(bytes) : "memory");
+    const int c0 = C::kFp4 ? k0 / 2 : k0;  // bytes (u8 map) or elements (bf16 map)
+    tma_load_2d(st, tmw, c0, wk.wrow[0], fb, pol_w);
+    if (wk.paired) tma_load_2d(st + C::kWTileBytes / 2, tmw, c0, wk.wrow[1], fb, pol_w);
+    if constexpr (C::kFp4) {
+      const uint8_t* sfb =
+          wk.shared ? p.sf2 : p.sf + (wk.expert >= 0 ? static_cast<size_t>(wk.expert) * p.sf_expert_bytes : 0);
+      for (int g = 0; g < 3; ++g) {
+        if (wk.sgroup[g] < 0) continue;
+        const size_t chunk = static_cast<size_t>(wk.sgroup[g]) * (wk.kbp / 4) + k0 / 64;
+        bulk_load(st + C::kWTileBytes + g * 2048, sfb + chunk * 512, nchunks * 512, fb, pol_w);
+      }
+    }
+  };
 
   if (warp == C::kProducerWarp && lane == 0) {
     prefetch_tensormap(&p.tm_w);
     if constexpr (kMode == kMoeGateUp || kMode == kMoeDown) prefetch_tensormap(&p.tm_w2);
     if constexpr (C::kXTma) prefetch_tensormap(&p.tm_x);
-  }
-  if (tid == 0) {
     s_abort = 0;
     s_last = 0;
-    resolve_work<kMode, kT, kNT>(p, s_work, rank);
+    CtaWork& wk = s_work;
+    resolve_work<kMode, kNT>(p, wk, rank);
+    const int nst = stage_count(wk);
+    const int nslices = wk.active ? (wk.k_end - wk.k_begin) / kSubK : 0;
     for (int i = 0; i < nstages; ++i) {
       mbar_init(smem_u32(&bar_full[i]), C::kFullCount);
-      mbar_init(smem_u32(&bar_empty[i]), 1);
+      // released by the last MMA commit of every warpgroup with a slice in the stage
+      mbar_init(smem_u32(&bar_empty[i]), kW);
     }
-    for (int i = 0; i < kNS; ++i) {
-      mbar_init(smem_u32(&bar_afull[i]), kT * 128);
-      mbar_init(smem_u32(&bar_aempty[i]), 1);
-    }
-    mbar_init(smem_u32(&bar_accum), 1);
+    for (int i = 0; i < kW * kNS; ++i) mbar_init(smem_u32(&bar_aempty[i]), 1);
+    mbar_init(smem_u32(&bar_accum), max(1, min(kW, nslices)));
     mbar_init(smem_u32(&bar_inbox), 1);
     mbar_init(smem_u32(&bar_red_ready), S);
     mbar_init(smem_u32(&bar_red_done), S);
-    mbar_fence_init();
     if (C::kPush && S > 1) {
-      // every rank sends its partials of my rows [r_lo, r_hi) for all tiles
-      mbar_arrive_expect_tx(smem_u32(&bar_inbox), S * kT * kNT * (r_hi - r_lo) * 4);
+      // every rank sends its partials of my rows for all tokens
+      const int unit = feature_unit<kMode>(wk);
+      const int R = (unit + static_cast<int>(S) - 1) / static_cast<int>(S);
+      const int mine = max(0, min(R, unit - static_cast<int>(rank) * R)) * (128 / unit);
+      mbar_arrive_expect_tx(smem_u32(&bar_inbox), S * kNT * mine * 4);
+    }
+    mbar_fence_init();
+    pre = min(nst, nstages);
+    if (!kIdsAfterWait || wk.shared) {
+      for (int s = 0; s < pre; ++s) issue_weights(wk, s);
     }
   }
-  if (warp == C::kMmaWarp) tmem_alloc(smem_u32(&s_tmem), C::kTmemCols);
+  if (warp == 0) tmem_alloc(smem_u32(&s_tmem), C::kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -369,51 +426,27 @@ __global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, Cfg<kMode, kT, 
   const CtaWork& wk = s_work;
   const bool active = wk.active != 0;
   const uint32_t tmem = s_tmem;
-  const int nst = active ? (wk.k_end - wk.k_begin + C::kStageK - 1) / C::kStageK : 0;
+  const int nst = stage_count(wk);
+  const int nslices = active ? (wk.k_end - wk.k_begin) / kSubK : 0;
+  // Output rows are reduced per feature unit: a paired tile's feature o lives
+  // in rows o and o + 64, so those rows go to the same cluster rank.
+  const int unit = feature_unit<kMode>(wk);
+  const int R = (unit + static_cast<int>(S) - 1) / static_cast<int>(S);  // features reduced per rank
+  const int f_lo = static_cast<int>(rank) * R;
+  const int f_hi = min(unit, f_lo + R);
+  const int mine = max(0, f_hi - f_lo) * (128 / unit);  // rows this rank owns
 
   if (warp == C::kProducerWarp) {
     // ------------------------------------------------------------------ producer
-    const uint64_t pol_w = policy_evict_first();
-    const uint64_t pol_x = policy_evict_last();
-    const CUtensorMap* tmw = wk.shared ? &p.tm_w2 : &p.tm_w;
-    const uint8_t* sfb =
-        wk.shared ? p.sf2 : p.sf + (wk.expert >= 0 ? static_cast<size_t>(wk.expert) * p.sf_expert_bytes : 0);
-    auto issue_weights = [&](int s) {
-      const int slot = s % nstages;
-      const uint32_t st = ring + slot * C::kStageBytes;
-      const uint32_t fb = smem_u32(&bar_full[slot]);
-      const int k0 = wk.k_begin + s * C::kStageK;
-      const int kvalid = min(C::kStageK, wk.k_end - k0);
-      const int nchunks = kvalid / kSubK;
-      uint32_t bytes = kT * C::kWTileBytes;
-      if constexpr (C::kFp4) {
-        for (int t = 0; t < kT; ++t) bytes += wk.sgroups[t] * nchunks * 512;
-      }
-      asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(fb), "r"(bytes) : "memory");
-      for (int t = 0; t < kT; ++t) {
-        const int c0 = C::kFp4 ? k0 / 2 : k0;  // bytes (u8 map) or elements (bf16 map)
-        tma_load_2d(st + t * C::kWTileBytes, tmw, c0, wk.wrow[t], fb, pol_w);
-        if constexpr (C::kFp4) {
-          for (int gi = 0; gi < wk.sgroups[t]; ++gi) {
-            const size_t chunk = static_cast<size_t>(wk.srow[t] / 128 + gi) * (wk.kbp / 4) + k0 / 64;
-            bulk_load(st + kT * C::kWTileBytes + t * C::kSfTileBytes + gi * 2048, sfb + chunk * 512, nchunks * 512,
-                      fb, pol_w);
-          }
-        }
-      }
-    };
-    const int pre = min(nst, nstages);
-    if (lane == 0 && (!kIdsAfterWait || wk.shared)) {
-      for (int s = 0; s < pre; ++s) issue_weights(s);
+    if (lane == 0 && kIdsAfterWait && !wk.shared) {
+      pre = min(nst, nstages);
+      for (int s = 0; s < pre; ++s) issue_weights(wk, s);  // resolve_work already waited
     }
     pdl_wait();
-    if (lane == 0 && kIdsAfterWait && !wk.shared) {
-      for (int s = 0; s < pre; ++s) issue_weights(s);
-    }
-    __syncwarp();
+    pre = __shfl_sync(0xFFFFFFFFu, pre, 0);
     if constexpr (C::kXTma) {
-      // Dense activations: rows 0..M-1 of x, one TMA box {64 elements, kNT rows}
-      // per 64-wide K atom (rows beyond M read as zeros).
+      // Dense activations: rows 0..M-1 of x, one TMA box {64 elements, kNT
+      // rows, 4 atoms} per stage (rows beyond M read as zeros).
       if (lane == 0) {
         for (int s = 0; s < nst && !s_abort; ++s) {
           const int slot = s % nstages;
@@ -421,12 +454,11 @@ __global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, Cfg<kMode, kT, 
           const uint32_t fb = smem_u32(&bar_full[slot]);
           if (s >= pre) {
             if (!mbar_wait(smem_u32(&bar_empty[slot]), ((s / nstages) & 1) ^ 1, p.err)) { s_abort = 1; break; }
-            issue_weights(s);
+            issue_weights(wk, s);
           }
           const int k0 = wk.k_begin + s * C::kStageK;
           mbar_arrive_expect_tx(fb, C::kXBytes);
           if constexpr (C::kFp4) {
-            // one box {64 elements, kNT rows, 4 atoms} of the [K/64, M, 64] view
             tma_load_3d(st + C::kXOff, &p.tm_x, 0, 0, k0 / kSubK, fb, pol_x);
           } else {
             tma_load_2d(st + C::kXOff, &p.tm_x, k0, 0, fb, pol_x);
@@ -444,7 +476,7 @@ __global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, Cfg<kMode, kT, 
         const uint32_t fb = smem_u32(&bar_full[slot]);
         if (s >= pre) {
           if (!mbar_wait(smem_u32(&bar_empty[slot]), ((s / nstages) & 1) ^ 1, p.err)) { s_abort = 1; break; }
-          if (lane == 0) issue_weights(s);
+          if (lane == 0) issue_weights(wk, s);
           __syncwarp();
         }
         const int k0 = wk.k_begin + s * C::kStageK;
@@ -461,151 +493,157 @@ __global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, Cfg<kMode, kT, 
         if (lane == 0) mbar_arrive(fb);
       }
     }
-  } else if (warp == C::kMmaWarp) {
-    // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0 && active) {
-      constexpr uint32_t idesc = idesc_bf16_f32(128, kNT);
-      int q = 0;
-      for (int s = 0; s < nst && !s_abort; ++s) {
+  } else if (active) {
+    // ------------------------------------------------------------------ workers
+    const int w = warp / 4;      // warpgroup
+    const int i = tid % 128;     // row in the tile
+    const bool issuer = (warp % 4) == 0 && lane == 0;
+    const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
+    const uint32_t acc = tmem + w * kNT;  // this warpgroup's accumulator
+    constexpr uint32_t idesc = idesc_bf16_f32(128, kNT);
+    if constexpr (C::kFp4) {
+      const int b = wk.paired ? i / 64 : 0;  // box of row i
+      const int r = wk.srow[b] + (wk.paired ? i % 64 : i);
+      const int gslot = b == 0 ? 0 : 1 + (r / 128 - wk.srow[1] / 128);  // smem scale group of row i
+      const uint32_t sf_row_off = C::kWTileBytes + gslot * 2048 + (r % 32) * 16 + ((r % 128) / 32) * 4;
+      const uint32_t w_row_off = (i / 8) * 1024 + (i % 8) * 128;
+      const uint32_t i8 = i % 8;
+      int cur = -1;  // ring stage whose full barrier this thread has passed
+      for (int j = 0;; ++j) {
+        const int q = w + j * kW;
+        if (q >= nslices) break;
+        const int s = q / kSPS, u = q % kSPS;
         const int slot = s % nstages;
         const uint32_t st = ring + slot * C::kStageBytes;
-        const uint32_t xs = st + C::kXOff;
-        if constexpr (C::kFp4) {
-          const int nsub = min(C::kStageK, wk.k_end - wk.k_begin - s * C::kStageK) / kSubK;
-          for (int u = 0; u < nsub; ++u, ++q) {
-            const int a = q % kNS;
-            if (!mbar_wait(smem_u32(&bar_afull[a]), (q / kNS) & 1, p.err)) { s_abort = 1; break; }
+        // Waits are bounded; a failed wait is made uniform over the warp (the
+        // tcgen05 loads / stores below are warp-collective) and then over the
+        // warpgroup at its barrier, so every thread leaves the loop together.
+        bool ok = !s_abort;
+        if (ok && s != cur) {
+          ok = mbar_wait(smem_u32(&bar_full[slot]), (s / nstages) & 1, p.err);
+          cur = s;
+        }
+        const int a = j % kNS;
+        const uint32_t xa = st + C::kXOff + u * (kNT * 128);
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        if (ok) {
+          const uint4 q0 = lds128(st + w_row_off + (((2 * u) ^ i8) * 16));
+          const uint4 q1 = lds128(st + w_row_off + (((2 * u + 1) ^ i8) * 16));
+          const uint32_t sw = lds32(st + sf_row_off + u * 512);
+          ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bar_aempty[w * kNS + a]), ((j / kNS) & 1) ^ 1, p.err));
+          if (ok) {
             tc_fence_after();
+            // activations of this slice into the weight pairs' K order
 #pragma unroll
-            for (int t = 0; t < kT; ++t) {
-              const uint32_t a_tmem = tmem + (a * kT + t) * 32;
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint32_t d_tmem = tmem + C::kTmemA + (t * C::kAcc + kk % C::kAcc) * kNT;
-                mma_ts(d_tmem, a_tmem + kk * 8, sdesc_sw128(xs + u * (kNT * 128) + kk * 32), idesc,
-                       q > 0 || kk >= C::kAcc);
-              }
-            }
-            mma_commit(smem_u32(&bar_aempty[a]));
-            if (u == nsub - 1) mma_commit(smem_u32(&bar_empty[slot]));
+            for (int c = i; c < kNT * 8; c += 128) sts128(xa + c * 16, perm_x8(lds128(xa + c * 16)));
+            uint32_t s0, s1, s2, s3;
+            scale_pair_to_bf16x2(sw & 0xFFFFu, s0, s1);
+            scale_pair_to_bf16x2(sw >> 16, s2, s3);
+            uint32_t o[16];
+            const uint32_t col = tmem + lane_base + C::kAccCols + (w * kNS + a) * 32;
+            dequant32_perm(q0, s0, s1, o);
+            tmem_st16(col, o);
+            dequant32_perm(q1, s2, s3, o);
+            tmem_st16(col + 16, o);
+            tmem_wait_st();
+            fence_proxy_async_smem();
           }
-        } else {
+        }
+        tc_fence_before();
+        if (wg_sync_or(w, !ok)) {
+          s_abort = 1;
+          break;
+        }
+        if (issuer) {
+          tc_fence_after();
+          const uint32_t a_tmem = tmem + C::kAccCols + (w * kNS + a) * 32;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts(acc, a_tmem + kk * 8, sdesc_sw128(xa + kk * 32), idesc, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(smem_u32(&bar_aempty[w * kNS + a]));
+          const int qn = q + kW;
+          if (qn >= nslices || qn / kSPS != s) mma_commit(smem_u32(&bar_empty[slot]));
+          if (qn >= nslices) mma_commit(smem_u32(&bar_accum));
+        }
+      }
+    } else {
+      // BF16 weights: warpgroup 0's elected thread issues every stage's MMAs.
+      if (issuer) {
+        for (int s = 0; s < nst && !s_abort; ++s) {
+          const int slot = s % nstages;
+          const uint32_t st = ring + slot * C::kStageBytes;
           if (!mbar_wait(smem_u32(&bar_full[slot]), (s / nstages) & 1, p.err)) { s_abort = 1; break; }
           tc_fence_after();
 #pragma unroll
-          for (int t = 0; t < kT; ++t) {
-            const uint32_t ws = st + t * C::kWTileBytes;
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint32_t d_tmem = tmem + (t * C::kAcc + kk % C::kAcc) * kNT;
-              mma_ss(d_tmem, sdesc_sw128(ws + kk * 32), sdesc_sw128(xs + kk * 32), idesc, s > 0 || kk >= C::kAcc);
-            }
-          }
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss(acc, sdesc_sw128(st + kk * 32), sdesc_sw128(st + C::kXOff + kk * 32), idesc,
+                   (s > 0 || kk > 0) ? 1u : 0u);
           mma_commit(smem_u32(&bar_empty[slot]));
         }
-      }
-      mma_commit(smem_u32(&bar_accum));
-    }
-  } else {
-    // ------------------------------------------------------------------ dequant warpgroups
-    if constexpr (C::kFp4) {
-      const int wg = warp / 4;
-      const int t = wg % kT;            // tile
-      const int g = wg / kT;            // turn: K slices q with q % kG == g
-      const int i = tid % 128;          // row in tile
-      const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
-      const int r = wk.srow[t] + i;     // row in the scale buffer's row space
-      const int grp = r / 128 - wk.srow[t] / 128;
-      const uint32_t sf_row_off = grp * 2048 + (r % 32) * 16 + ((r % 128) / 32) * 4;
-      const uint32_t w_row_off = (i / 8) * 1024 + (i % 8) * 128;
-      const uint32_t i8 = i % 8;
-      // One K slice: load codes + scales, wait for its tensor-memory slot,
-      // permute the activation atom (tile-0 warpgroups), dequantize, store.
-      auto slice = [&](uint32_t st, int u, int q) -> bool {
-        const uint32_t wt = st + t * C::kWTileBytes + w_row_off;
-        const uint4 q0 = lds128(wt + (((2 * u) ^ i8) * 16));
-        const uint4 q1 = lds128(wt + (((2 * u + 1) ^ i8) * 16));
-        const uint32_t sw = lds32(st + kT * C::kWTileBytes + t * C::kSfTileBytes + sf_row_off + u * 512);
-        const int a = q % kNS;
-        if (!mbar_wait(smem_u32(&bar_aempty[a]), ((q / kNS) & 1) ^ 1, p.err)) return false;
-        tc_fence_after();
-        if (t == 0) {
-          const uint32_t xa = st + C::kXOff + u * (kNT * 128);
-#pragma unroll
-          for (int j = i; j < kNT * 8; j += 128) sts128(xa + j * 16, perm_x8(lds128(xa + j * 16)));
-        }
-        uint32_t s0, s1, s2, s3;
-        scale_pair_to_bf16x2(sw & 0xFFFFu, s0, s1);
-        scale_pair_to_bf16x2(sw >> 16, s2, s3);
-        uint32_t o[16];
-        const uint32_t col = tmem + lane_base + (a * kT + t) * 32;
-        dequant32_perm(q0, s0, s1, o);
-        tmem_st16(col, o);
-        dequant32_perm(q1, s2, s3, o);
-        tmem_st16(col + 16, o);
-        return true;
-      };
-      int qbase = 0;  // global index of the current stage's first K slice
-      for (int s = 0; s < nst && !s_abort; ++s) {
-        const int slot = s % nstages;
-        const uint32_t st = ring + slot * C::kStageBytes;
-        const int nsub = min(C::kStageK, wk.k_end - wk.k_begin - s * C::kStageK) / kSubK;
-        const int first = ((g - qbase) % kG + kG) % kG;  // my first slice in this stage
-        if (first < nsub) {
-          if (!mbar_wait(smem_u32(&bar_full[slot]), (s / nstages) & 1, p.err)) { s_abort = 1; break; }
-          // my slices two at a time: one tensor-memory store wait per pair
-          for (int u = first; u < nsub; u += 2 * kG) {
-            const int u2 = u + kG;
-            const bool two = u2 < nsub;
-            if (!slice(st, u, qbase + u) || (two && !slice(st, u2, qbase + u2))) { s_abort = 1; break; }
-            tmem_wait_st();
-            if (t == 0) fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(smem_u32(&bar_afull[(qbase + u) % kNS]));
-            if (two) mbar_arrive(smem_u32(&bar_afull[(qbase + u2) % kNS]));
-          }
-        }
-        qbase += nsub;
+        mma_commit(smem_u32(&bar_accum));
       }
     }
   }
 
   // ==================================================================== epilogue
   __syncwarp();
-  if (warp < 4 * C::kWarpgroups) {
-    const int wg = warp / 4;  // warpgroups 0 .. kT-1 read tile wg's accumulator
+  if (warp < C::kProducerWarp) {
+    const int w = warp / 4;
     const int i = tid % 128;
     const bool ok_acc = active && mbar_wait(smem_u32(&bar_accum), 0, p.err);
     if (!ok_acc && active) s_abort = 1;
     tc_fence_after();
+    // warp-uniform: the accumulator reads below are warp-collective
+    const bool go = __all_sync(0xFFFFFFFFu, ok_acc && !s_abort);
     const float post = C::kFp4 ? static_cast<float>(1 << kShift) : 1.0f;
-    // Partials of (tile t, token n, row i).  Push mode: rank `rank` owns rows
-    // [r_lo, r_hi) and receives them from every rank into
-    // inbox[src][t][n][row - r_lo]; pull mode: each rank leaves its partials in
-    // its own ring as red[t][n][row] and the owner reads them through DSMEM.
+    const int nacc = min(kW, nslices);  // warpgroups that accumulated anything
+    constexpr int kCols = kNT / kW;     // token columns this warpgroup reduces
+    const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
+    // Row i's owner rank and its index among the owner's rows.
+    const int fi = i % unit;
+    const int owner = fi / R;
+    const int owner_feats = min(R, unit - owner * R);
+    const int rr = (i / unit) * owner_feats + (fi - owner * R);
+    const int rows_owner = owner_feats * (128 / unit);
+    // Sum of the warpgroups' accumulators for columns [c, c + 8) of row i.
+    auto load_sum = [&](int c, float (&v8)[8]) {
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) v8[jj] = 0.0f;
+      for (int a2 = 0; a2 < nacc; ++a2) {
+        uint32_t v[8];
+        tmem_ld8(tmem + lane_base + a2 * kNT + c, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) v8[jj] += __uint_as_float(v[jj]);
+      }
+    };
+    // Partials of (token n, row i).  Push mode: the owner of row i receives
+    // them from every rank into inbox[src][n][rr]; pull mode: each rank leaves
+    // its partials in its own ring as red[n][row] and the owner reads them
+    // through DSMEM.
     if constexpr (C::kPush) {
       if (S > 1) cluster_wait();  // all peers' inbox barriers are initialised
-      if (active && wg < kT) {
-        const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
-        const uint32_t dcol = tmem + lane_base + C::kTmemA + wg * C::kAcc * kNT;
-        const uint32_t owner = static_cast<uint32_t>(i / R);
-        const int rr = i - static_cast<int>(owner) * R;
-        const int rows_owner = min(R, 128 - static_cast<int>(owner) * R);
-        const uint32_t base = inbox + ((rank * kT + wg) * kNT * rows_owner + rr) * 4;
+      if (go) {
+        const uint32_t base = inbox + ((rank * kNT) * rows_owner + rr) * 4;
         const uint32_t rbase = S > 1 ? mapa(base, owner) : base;
         const uint32_t rbar = S > 1 ? mapa(smem_u32(&bar_inbox), owner) : 0u;
 #pragma unroll
-        for (int c = 0; c < kNT; c += 8) {
-          float acc8[8];
-          load_acc<C::kAcc, kNT>(dcol + c, acc8);
+        for (int c = w * kCols; c < (w + 1) * kCols; c += 8) {
+          float v8[8];
+          load_sum(c, v8);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float val = acc8[j] * post;
-            const uint32_t off = (c + j) * rows_owner * 4;
-            if (S > 1) st_async_f32(rbase + off, val, rbar);
-            else stsf(rbase + off, val);
+          for (int jj = 0; jj < 8; ++jj) {
+            const uint32_t off = (c + jj) * rows_owner * 4;
+            if (S > 1) st_async_f32(rbase + off, v8[jj] * post, rbar);
+            else stsf(rbase + off, v8[jj] * post);
           }
         }
+      } else if (active && S > 1) {
+        // keep the owners' transaction counts consistent on the abort path
+        const uint32_t base = inbox + ((rank * kNT) * rows_owner + rr) * 4;
+        const uint32_t rbase = mapa(base, owner);
+        const uint32_t rbar = mapa(smem_u32(&bar_inbox), owner);
+        for (int c = w * kCols; c < (w + 1) * kCols; ++c) st_async_f32(rbase + c * rows_owner * 4, 0.0f, rbar);
       }
       tc_fence_before();
       if (S > 1) {
@@ -615,15 +653,13 @@ __global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, Cfg<kMode, kT, 
       }
     } else {
       epi_sync<kEpiThreads>();  // every ring stage is consumed: reuse it for partials
-      if (active && !s_abort && wg < kT) {
-        const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
-        const uint32_t dcol = tmem + lane_base + C::kTmemA + wg * C::kAcc * kNT;
+      if (go) {
 #pragma unroll
-        for (int c = 0; c < kNT; c += 8) {
-          float acc8[8];
-          load_acc<C::kAcc, kNT>(dcol + c, acc8);
+        for (int c = w * kCols; c < (w + 1) * kCols; c += 8) {
+          float v8[8];
+          load_sum(c, v8);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) stsf(ring + ((wg * kNT + c + j) * 128 + i) * 4, acc8[j] * post);
+          for (int jj = 0; jj < 8; ++jj) stsf(ring + ((c + jj) * 128 + i) * 4, v8[jj] * post);
         }
       }
       tc_fence_before();
@@ -635,17 +671,15 @@ __global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, Cfg<kMode, kT, 
         if (!mbar_wait<true>(smem_u32(&bar_red_ready), 0, p.err)) s_abort = 1;
       }
     }
-    // Sum over the cluster ranks, in rank order, of the partial of
-    // (tile t, token n, row) for a row this rank owns.
-    auto partial = [&](int t, int n, int row) -> float {
+    // Sum over the cluster ranks, in rank order, of the partial of (token n,
+    // tile row) for a row this rank owns; `lr` is the row's index among mine.
+    auto partial = [&](int n, int row, int lr) -> float {
       if constexpr (C::kPush) {
-        const int rows_mine = r_hi - r_lo;
         float acc = 0.0f;
-        for (uint32_t src = 0; src < S; ++src)
-          acc += ldsf(inbox + (((src * kT + t) * kNT + n) * rows_mine + (row - r_lo)) * 4);
+        for (uint32_t src = 0; src < S; ++src) acc += ldsf(inbox + ((src * kNT + n) * mine + lr) * 4);
         return acc;
       } else {
-        const uint32_t off = ring + ((t * kNT + n) * 128 + row) * 4;
+        const uint32_t off = ring + (n * 128 + row) * 4;
         if (S == 1) return ldsf(off);
         float acc = 0.0f;
         for (uint32_t r2 = 0; r2 < S; ++r2) {
@@ -656,57 +690,49 @@ __global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, Cfg<kMode, kT, 
         return acc;
       }
     };
-    if (active && !s_abort) {
+    const int nf = f_hi - f_lo;  // features this rank owns (per unit)
+    if (active && !s_abort && nf > 0) {
       pdl_wait();
-      if constexpr (kMode == kDenseFp4 || kMode == kDenseBf16) {
-        const float gs = p.gs ? __ldg(p.gs) : 1.0f;
-        for (int it = tid; it < (r_hi - r_lo) * wk.ntok; it += kEpiThreads) {
-          const int n = it / (r_hi - r_lo), row = r_lo + it % (r_hi - r_lo);
-          const int o = wk.out_base + row;
-          if (o >= p.n_out) continue;
-          uint16_t res;
-          if (kT == 1) {
-            res = f32_to_bf16_rn(partial(0, n, row) * gs);
-          } else {
-            const float G = bf16_to_f32(f32_to_bf16_rn(partial(0, n, row) * gs));
-            const float U = bf16_to_f32(f32_to_bf16_rn(partial(1, n, row) * gs));
-            res = f32_to_bf16_rn(silu_exact(G) * U);
-          }
-          p.out[static_cast<int64_t>(n) * p.ldo + o] = res;
-        }
-      } else if constexpr (kMode == kMoeGateUp) {
-        if (!wk.shared) {
-          const float al = __ldg(p.alpha + wk.expert);
-          for (int it = tid; it < kT * 64 * wk.ntok; it += kEpiThreads) {
-            const int n = it / (kT * 64), rem = it % (kT * 64);
-            const int t = rem / 64, o = rem % 64;
-            const int feat = blockIdx.x * (kT * 64) + t * 64 + o;
-            if (feat >= p.n_out) continue;
-            const float u = partial(t, n, o) * al;
-            const float gt = partial(t, n, o + 64) * al;
-            p.out[static_cast<int64_t>(wk.orow[n]) * p.ldo + feat] = f32_to_bf16_rn(silu_fast(gt) * u);
-          }
-        } else {
-          const float gs = __ldg(p.gs);
-          for (int it = tid; it < 128 * wk.ntok; it += kEpiThreads) {
-            const int n = it / 128, row = it % 128;
-            const int o = wk.out_base + row;
-            if (o >= p.shared_n_out) continue;
-            const float G = bf16_to_f32(f32_to_bf16_rn(partial(0, n, row) * gs));
-            const float U = bf16_to_f32(f32_to_bf16_rn(partial(1, n, row) * gs));
-            p.out2[static_cast<int64_t>(wk.orow[n]) * p.ldo2 + o] = f32_to_bf16_rn(silu_exact(G) * U);
-          }
-        }
-      } else {  // kMoeDown: y values into the scratch
-        const float sc = wk.shared ? __ldg(p.gs) : __ldg(p.alpha + wk.expert);
-        uint16_t* dst = wk.shared ? p.out2 : p.out;
-        const int64_t ld = wk.shared ? p.ldo2 : p.ldo;
-        const int nfeat = wk.shared ? p.shared_n_out : p.n_out;
-        for (int it = tid; it < 128 * wk.ntok; it += kEpiThreads) {
-          const int n = it / 128, row = it % 128;
+      if (unit == 128) {
+        // plain tiles: feature = tile row
+        const float sc = (kMode == kDenseFp4 || kMode == kDenseBf16)
+                             ? (p.gs ? __ldg(p.gs) : 1.0f)
+                             : (wk.shared ? __ldg(p.gs) : __ldg(p.alpha + wk.expert));
+        uint16_t* dst = (kMode == kMoeDown && wk.shared) ? p.out2 : p.out;
+        const int64_t ld = (kMode == kMoeDown && wk.shared) ? p.ldo2 : p.ldo;
+        const int nfeat = (kMode == kMoeDown && wk.shared) ? p.shared_n_out : p.n_out;
+        for (int it = tid; it < nf * wk.ntok; it += kEpiThreads) {
+          const int n = it / nf, lr = it % nf, row = f_lo + lr;
           const int o = wk.out_base + row;
           if (o >= nfeat) continue;
-          dst[static_cast<int64_t>(wk.orow[n]) * ld + o] = f32_to_bf16_rn(partial(0, n, row) * sc);
+          const int64_t orow = (kMode == kMoeDown) ? wk.orow[n] : n;
+          dst[orow * ld + o] = f32_to_bf16_rn(partial(n, row, lr) * sc);
+        }
+      } else if (kMode == kMoeGateUp && !wk.shared) {
+        // routed [up; gate] group: feature o = up row o, gate row o + 64
+        const float al = __ldg(p.alpha + wk.expert);
+        for (int it = tid; it < nf * wk.ntok; it += kEpiThreads) {
+          const int n = it / nf, lr = it % nf, o = f_lo + lr;
+          const int feat = wk.out_base + o;
+          if (feat >= p.n_out) continue;
+          const float uu = partial(n, o, lr) * al;
+          const float gt = partial(n, o + 64, lr + nf) * al;
+          p.out[static_cast<int64_t>(wk.orow[n]) * p.ldo + feat] = f32_to_bf16_rn(silu_fast(gt) * uu);
+        }
+      } else {
+        // paired tiles: feature o = gate row o, up row o + 64
+        const float gs = p.gs ? __ldg(p.gs) : 1.0f;
+        uint16_t* dst = (kMode == kMoeGateUp) ? p.out2 : p.out;
+        const int64_t ld = (kMode == kMoeGateUp) ? p.ldo2 : p.ldo;
+        const int nfeat = (kMode == kMoeGateUp) ? p.shared_n_out : p.n_out;
+        for (int it = tid; it < nf * wk.ntok; it += kEpiThreads) {
+          const int n = it / nf, lr = it % nf, o = f_lo + lr;
+          const int feat = wk.out_base + o;
+          if (feat >= nfeat) continue;
+          const float G = bf16_to_f32(f32_to_bf16_rn(partial(n, o, lr) * gs));
+          const float U = bf16_to_f32(f32_to_bf16_rn(partial(n, o + 64, lr + nf) * gs));
+          const int64_t orow = (kMode == kMoeGateUp) ? wk.orow[n] : n;
+          dst[orow * ld + feat] = f32_to_bf16_rn(silu_exact(G) * U);
         }
       }
     }
@@ -765,13 +791,13 @@ __global__ void __launch_bounds__(Cfg<kMode, kT, kNT>::kThreads, Cfg<kMode, kT, 
       }
     }
   } else if (C::kPush && S > 1) {
-    cluster_wait();  // the producer and MMA warps close their cluster-barrier phase
+    cluster_wait();  // the producer warp closes its cluster-barrier phase
   }
 
   // ==================================================================== teardown
   tc_fence_before();
   __syncthreads();
-  if (warp == C::kMmaWarp) {
+  if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }

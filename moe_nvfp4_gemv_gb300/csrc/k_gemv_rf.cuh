@@ -1,0 +1,329 @@
+// k_gemv_rf.cuh -- the dense NVFP4 GEMV for M <= 16 with register-fed MMAs.
+//
+// Same operation as the dense mode of k_gemv.cuh (vllm.models.flint.ops.nvfp4_gemv
+// nvfp4_gemv, with or without silu_mul), built for the decode shapes where
+// the token count is tiny.  On this GPU a tcgen05 MMA with N <= 64 costs about
+// as much as N = 64 (a 128x16x16 MMA occupies the tensor core ~46 cycles,
+// plus ~44 per commit), which caps a swap-AB tcgen05 GEMV near the HBM rate
+// with no headroom.  The warp-level m16n8k16 MMA processes a 16-row x 16-K
+// weight block for 8 tokens at ~0.4 per cycle per SM (~100 weights per cycle
+// per SM), so it is not the bottleneck; the dequantization is.
+//
+// Layout of the work: a CTA owns one 128-row weight tile (plain, or 64 gate +
+// 64 up rows for silu_mul) and a K range; the S CTAs of a cluster split K and
+// reduce in rank order through distributed shared memory, exactly as the
+// tcgen05 kernel does.  A producer warp streams weights, scales and
+// activations into a ring of 256-K stages (TMA / bulk copies, weights issued
+// before griddepcontrol.wait).  Each of the 8 consumer warps owns 16 rows of
+// the tile; per stage it reads its rows' codes and scales from shared memory,
+// dequantizes them exactly to bf16 in registers (dequant.cuh) straight into
+// MMA A fragments, loads the activation B fragments (permuted in registers to
+// the weight pairs' K order) and accumulates in fp32 registers.  No warp waits
+// on another warp except through the stage ring.
+//
+// Fragment mapping.  Thread (g, c) = (lane / 4, lane % 4) of warp wp holds
+// MMA rows g and g + 8, which are tile rows 16 wp + sigma(g) and
+// 16 wp + 8 + sigma(g), sigma = (0 4 1 5 2 6 3 7): neighbouring g then sit in
+// different halves of the 128-byte swizzle, so the 16-byte code loads of a
+// quarter warp hit distinct banks.  In each 128-K half h of a stage thread c
+// reads code chunk j = 4 h + c (32 codes) of both rows; word w of the chunk
+// (8 codes) yields the bf16 pairs (c0,c4) (c2,c6) (c1,c5) (c3,c7), the A
+// registers of two MMAs, and the activation chunk of the same 8 K (token g,
+// permuted the same way) their B registers.
+#pragma once
+
+#include "k_gemv.cuh"
+
+namespace fp4 {
+
+template <int kNT>
+struct RfCfg {
+  static constexpr int kConsumerWarps = 8;
+  static constexpr int kThreads = kConsumerWarps * 32 + 32;
+  static constexpr int kProducerWarp = kConsumerWarps;
+  static constexpr int kStageK = 256;
+  static constexpr int kWTileBytes = 128 * 128;
+  static constexpr int kSfTileBytes = 3 * 4 * 512;
+  static constexpr int kXOff = kWTileBytes + kSfTileBytes;
+  static constexpr int kXBytes = kNT * kStageK * 2;
+  static constexpr int kStageBytes = kXOff + kXBytes;
+  static constexpr int kTiles = kNT / 8;  // MMA n-tiles
+  static constexpr int kInboxBytes = kNT * 136 * 4;
+  static_assert(kNT == 8 || kNT == 16, "token tile");
+  static_assert(kStageBytes % 1024 == 0, "stage alignment");
+};
+
+__device__ __forceinline__ uint32_t lds16(uint32_t a) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+  return v;
+}
+
+// D += A * B for one m16n8k16 bf16 MMA (fp32 accumulate).
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Dense CTA work: K range and the weight boxes (tensor-map rows, scale rows
+// and groups), as resolve_work computes them for the dense modes.
+struct DenseWork {
+  int paired, k_begin, k_end, kbp, out_base;
+  int wrow[2], srow[2], sgroup[3];
+};
+
+template <int kNT>
+__global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const __grid_constant__ GemvParams p) {
+  using C = RfCfg<kNT>;
+  constexpr int kEpiThreads = C::kConsumerWarps * 32;
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t ring = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t inbox = ring + p.nstages * C::kStageBytes;
+  __shared__ __align__(8) uint64_t bar_full[kMaxStages];
+  __shared__ __align__(8) uint64_t bar_empty[kMaxStages];
+  __shared__ __align__(8) uint64_t bar_inbox;
+  __shared__ volatile int s_abort;
+
+  const int tid = threadIdx.x;
+  const int warp = tid / 32;
+  const int lane = tid % 32;
+  const uint32_t S = cluster_nctarank();
+  const uint32_t rank = S > 1 ? cluster_ctarank() : 0;
+  const int nstages = p.nstages;
+
+  // ---- what this CTA computes (every thread derives it) ----
+  DenseWork wk;
+  {
+    const int tile = blockIdx.x / max(1u, S);
+    wk.k_begin = static_cast<int>(rank) * p.k_split;
+    wk.k_end = min(p.K, wk.k_begin + p.k_split);
+    wk.kbp = p.kbp;
+    wk.sgroup[1] = wk.sgroup[2] = -1;
+    wk.wrow[1] = wk.srow[1] = 0;
+    const int groups_total = (p.rows_w + 127) / 128;
+    if (p.silu) {
+      wk.paired = 1;
+      wk.out_base = tile * 64;
+      set_box(wk, 0, tile * 64, tile * 64, groups_total);
+      set_box(wk, 1, p.n_half + tile * 64, p.n_half + tile * 64, groups_total);
+    } else {
+      wk.paired = 0;
+      wk.out_base = tile * 128;
+      set_box(wk, 0, tile * 128, tile * 128, groups_total);
+    }
+  }
+  const int nst = (wk.k_end - wk.k_begin + C::kStageK - 1) / C::kStageK;
+  const int unit = wk.paired ? 64 : 128;
+  const int R = (unit + static_cast<int>(S) - 1) / static_cast<int>(S);
+  const int f_lo = static_cast<int>(rank) * R;
+  const int f_hi = min(unit, f_lo + R);
+  const int mine = max(0, f_hi - f_lo) * (128 / unit);
+
+  const uint64_t pol_w = policy_evict_first();
+  const uint64_t pol_x = policy_evict_last();
+  auto issue_weights = [&](int s) {
+    const int slot = s % nstages;
+    const uint32_t st = ring + slot * C::kStageBytes;
+    const uint32_t fb = smem_u32(&bar_full[slot]);
+    const int k0 = wk.k_begin + s * C::kStageK;
+    const int nchunks = min(C::kStageK, wk.k_end - k0) / kSubK;
+    uint32_t bytes = C::kWTileBytes;
+    for (int g = 0; g < 3; ++g) bytes += (wk.sgroup[g] >= 0 ? nchunks * 512 : 0);
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(fb), "r"(bytes) : "memory");
+    tma_load_2d(st, &p.tm_w, k0 / 2, wk.wrow[0], fb, pol_w);
+    if (wk.paired) tma_load_2d(st + C::kWTileBytes / 2, &p.tm_w, k0 / 2, wk.wrow[1], fb, pol_w);
+    for (int g = 0; g < 3; ++g) {
+      if (wk.sgroup[g] < 0) continue;
+      const size_t chunk = static_cast<size_t>(wk.sgroup[g]) * (wk.kbp / 4) + k0 / 64;
+      bulk_load(st + C::kWTileBytes + g * 2048, p.sf + chunk * 512, nchunks * 512, fb, pol_w);
+    }
+  };
+
+  // ------------------------------------------------------------------ prologue
+  const int pre = min(nst, nstages);
+  if (warp == C::kProducerWarp && lane == 0) {
+    prefetch_tensormap(&p.tm_w);
+    prefetch_tensormap(&p.tm_x);
+    s_abort = 0;
+    for (int i = 0; i < nstages; ++i) {
+      mbar_init(smem_u32(&bar_full[i]), 1);
+      mbar_init(smem_u32(&bar_empty[i]), C::kConsumerWarps);
+    }
+    mbar_init(smem_u32(&bar_inbox), 1);
+    if (S > 1) mbar_arrive_expect_tx(smem_u32(&bar_inbox), S * kNT * mine * 4);
+    mbar_fence_init();
+    for (int s = 0; s < pre; ++s) issue_weights(s);
+  }
+  __syncthreads();
+  if (S > 1) cluster_arrive();  // paired with a wait before the first remote access
+  if (tid == 0) pdl_launch_dependents();
+
+  float acc[C::kTiles][4];
+#pragma unroll
+  for (int t = 0; t < C::kTiles; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
+  const int g = lane / 4, c = lane % 4;
+  const int sg = (g % 2) * 4 + g / 2;  // sigma(g)
+  const int row0 = warp * 16 + sg;     // tile rows of MMA rows g and g + 8
+  const int row1 = row0 + 8;
+
+  if (warp == C::kProducerWarp) {
+    // ------------------------------------------------------------------ producer
+    pdl_wait();
+    if (lane == 0) {
+      for (int s = 0; s < nst && !s_abort; ++s) {
+        const int slot = s % nstages;
+        const uint32_t st = ring + slot * C::kStageBytes;
+        const uint32_t fb = smem_u32(&bar_full[slot]);
+        if (s >= pre) {
+          if (!mbar_wait(smem_u32(&bar_empty[slot]), ((s / nstages) & 1) ^ 1, p.err)) { s_abort = 1; break; }
+          issue_weights(s);
+        }
+        const int k0 = wk.k_begin + s * C::kStageK;
+        mbar_arrive_expect_tx(fb, C::kXBytes);
+        tma_load_3d(st + C::kXOff, &p.tm_x, 0, 0, k0 / kSubK, fb, pol_x);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------ consumers
+    // shared-memory offsets of this thread's two rows (128-byte swizzle key
+    // = row % 8, the same for both rows) and of their scale bytes
+    const uint32_t key = static_cast<uint32_t>(row0 % 8);
+    const uint32_t w_off0 = (row0 / 8) * 1024 + (row0 % 8) * 128;
+    const uint32_t w_off1 = (row1 / 8) * 1024 + (row1 % 8) * 128;
+    auto sf_off = [&](int row) -> uint32_t {
+      const int b = wk.paired ? row / 64 : 0;
+      const int r = wk.srow[b] + (wk.paired ? row % 64 : row);
+      const int gslot = b == 0 ? 0 : 1 + (r / 128 - wk.srow[1] / 128);
+      return C::kWTileBytes + gslot * 2048 + (r % 32) * 16 + ((r % 128) / 32) * 4;
+    };
+    const uint32_t sf0 = sf_off(row0), sf1 = sf_off(row1);
+    for (int s = 0; s < nst; ++s) {
+      const int slot = s % nstages;
+      const uint32_t st = ring + slot * C::kStageBytes;
+      const bool ok = __all_sync(0xFFFFFFFFu, !s_abort && mbar_wait(smem_u32(&bar_full[slot]), (s / nstages) & 1, p.err));
+      if (!ok) {
+        s_abort = 1;
+        break;
+      }
+      // valid K of the stage: 64 .. 256 in steps of 64; a chunk (32 K) is
+      // wholly valid or wholly past the end, where its A registers are zero
+      // (its scales were not copied and may hold anything)
+      const int kvalid = min(C::kStageK, wk.k_end - wk.k_begin - s * C::kStageK);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (128 * h < kvalid) {
+          const int j = 4 * h + c;  // code chunk (32 K) of both rows
+          const bool cvalid = 32 * j < kvalid;
+          const uint4 A0 = lds128(st + w_off0 + ((static_cast<uint32_t>(j) ^ key) * 16));
+          const uint4 A1 = lds128(st + w_off1 + ((static_cast<uint32_t>(j) ^ key) * 16));
+          const uint32_t sc_off = (j / 2) * 512 + 2 * (j % 2);
+          uint32_t s0lo, s0hi, s1lo, s1hi;
+          scale_pair_to_bf16x2(lds16(st + sf0 + sc_off), s0lo, s0hi);
+          scale_pair_to_bf16x2(lds16(st + sf1 + sc_off), s1lo, s1hi);
+          const uint32_t a0w[4] = {A0.x, A0.y, A0.z, A0.w};
+          const uint32_t a1w[4] = {A1.x, A1.y, A1.z, A1.w};
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            uint32_t r0[4], r1[4];
+            e2m1x8_raw_perm(a0w[w], r0);
+            e2m1x8_raw_perm(a1w[w], r1);
+            const uint32_t sa = w < 2 ? s0lo : s0hi, sb = w < 2 ? s1lo : s1hi;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              r0[q] = cvalid ? bf16x2_mul(r0[q], sa) : 0u;
+              r1[q] = cvalid ? bf16x2_mul(r1[q], sb) : 0u;
+            }
+            // activations of the same 8 K: atom u, 16-byte chunk ch of token n
+            const int kk = 32 * j + 8 * w;
+            const uint32_t u = kk / 64, ch = (kk % 64) / 8;
+#pragma unroll
+            for (int t = 0; t < C::kTiles; ++t) {
+              const int n = 8 * t + g;
+              const uint4 xv = perm_x8(lds128(st + C::kXOff + u * (kNT * 128) + (n / 8) * 1024 + (n % 8) * 128 +
+                                              ((ch ^ static_cast<uint32_t>(n % 8)) * 16)));
+              mma_bf16_16816(acc[t], r0[0], r1[0], r0[1], r1[1], xv.x, xv.y);
+              mma_bf16_16816(acc[t], r0[2], r1[2], r0[3], r1[3], xv.z, xv.w);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bar_empty[slot]));
+    }
+  }
+
+  // ==================================================================== epilogue
+  __syncwarp();
+  if (warp < C::kProducerWarp) {
+    const float post = static_cast<float>(1 << kShift);
+    // Push this thread's partials (rows row0 / row1, tokens 8t + 2c + {0,1})
+    // to the owners of the rows: inbox[src][n][rr].
+    if (S > 1) cluster_wait();  // all peers' inbox barriers are initialised
+    const bool go = !s_abort;
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int row = hr ? row1 : row0;
+      const int fi = row % unit;
+      const int owner = fi / R;
+      const int owner_feats = min(R, unit - owner * R);
+      const int rr = (row / unit) * owner_feats + (fi - owner * R);
+      const int rows_owner = owner_feats * (128 / unit);
+      const uint32_t base = inbox + ((rank * kNT) * rows_owner + rr) * 4;
+      const uint32_t rbase = S > 1 ? mapa(base, static_cast<uint32_t>(owner)) : base;
+      const uint32_t rbar = S > 1 ? mapa(smem_u32(&bar_inbox), static_cast<uint32_t>(owner)) : 0u;
+#pragma unroll
+      for (int t = 0; t < C::kTiles; ++t) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int n = 8 * t + 2 * c + e;
+          const float v = go ? acc[t][2 * hr + e] * post : 0.0f;
+          const uint32_t off = n * rows_owner * 4;
+          if (S > 1) st_async_f32(rbase + off, v, rbar);
+          else stsf(rbase + off, v);
+        }
+      }
+    }
+    if (S > 1) {
+      if (!mbar_wait<true>(smem_u32(&bar_inbox), 0, p.err)) s_abort = 1;
+    } else {
+      epi_sync<kEpiThreads>();
+    }
+    auto partial = [&](int n, int lr) -> float {
+      float a = 0.0f;
+      for (uint32_t src = 0; src < S; ++src) a += ldsf(inbox + ((src * kNT + n) * mine + lr) * 4);
+      return a;
+    };
+    const int nf = f_hi - f_lo;
+    if (!s_abort && nf > 0) {
+      pdl_wait();
+      const float gs = __ldg(p.gs);
+      if (!wk.paired) {
+        for (int it = tid; it < nf * p.M; it += kEpiThreads) {
+          const int n = it / nf, lr = it % nf;
+          const int o = wk.out_base + f_lo + lr;
+          if (o >= p.n_out) continue;
+          p.out[static_cast<int64_t>(n) * p.ldo + o] = f32_to_bf16_rn(partial(n, lr) * gs);
+        }
+      } else {
+        for (int it = tid; it < nf * p.M; it += kEpiThreads) {
+          const int n = it / nf, lr = it % nf;
+          const int feat = wk.out_base + f_lo + lr;
+          if (feat >= p.n_out) continue;
+          const float G = bf16_to_f32(f32_to_bf16_rn(partial(n, lr) * gs));
+          const float U = bf16_to_f32(f32_to_bf16_rn(partial(n, lr + nf) * gs));
+          p.out[static_cast<int64_t>(n) * p.ldo + feat] = f32_to_bf16_rn(silu_exact(G) * U);
+        }
+      }
+    }
+  } else if (S > 1) {
+    cluster_wait();  // the producer warp closes its cluster-barrier phase
+  }
+  __syncthreads();
+}
+
+}  // namespace fp4

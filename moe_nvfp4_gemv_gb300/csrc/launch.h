@@ -25,14 +25,13 @@ struct KernelInfo {
   int tmem_cols;
 };
 
-// Per (mode, kT, kNT) kernel: static facts and a launcher.  Each returns
-// cudaErrorInvalidValue for a combination that is not instantiated.
-cudaError_t gemv_info(int mode, int t, int nt, KernelInfo* info);
-cudaError_t gemv_launch(int mode, int t, int nt, const GemvParams& p, const LaunchCfg& cfg);
-
-cudaError_t launch_dense_fp4(int t, int nt, const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info);
-cudaError_t launch_dense_bf16(int t, int nt, const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info);
-cudaError_t launch_moe(int mode, int t, int nt, const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info);
+// Per (mode, kNT) kernel: static facts (info != nullptr) or a launch.  Each
+// returns cudaErrorInvalidValue for a combination that is not instantiated.
+cudaError_t launch_dense_fp4(int nt, const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info);
+// Register-fed dense NVFP4 GEMV for M <= 16 (k_gemv_rf.cuh), nt = 8 or 16.
+cudaError_t launch_dense_rf(int nt, const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info);
+cudaError_t launch_dense_bf16(int nt, const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info);
+cudaError_t launch_moe(int mode, int nt, const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info);
 cudaError_t launch_dequantize_rows(const uint8_t* w, const uint8_t* sf, void* out, int rows, int K,
                                    cudaStream_t stream);
 
@@ -63,9 +62,9 @@ cudaError_t launch_kernel(Kernel kernel, int threads, const GemvParams& p, const
   return cudaLaunchKernelEx(&lc, kernel, p);
 }
 
-template <int kMode, int kT, int kNT>
+template <int kMode, int kNT>
 cudaError_t run_gemv(const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info) {
-  using C = Cfg<kMode, kT, kNT>;
+  using C = Cfg<kMode, kNT>;
   if (info) {
     info->threads = C::kThreads;
     info->stage_bytes = C::kStageBytes;
@@ -74,7 +73,7 @@ cudaError_t run_gemv(const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info
     info->tmem_cols = C::kTmemCols;
     return cudaSuccess;
   }
-  auto k = gemv_kernel<kMode, kT, kNT>;
+  auto k = gemv_kernel<kMode, kNT>;
   static int configured_smem[64];  // per instantiation and device (0 = not yet)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
