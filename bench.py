@@ -221,6 +221,22 @@ def run_reference(args):
 # GPU leg
 # --------------------------------------------------------------------------------------
 
+def capture_graph(fn, dev):
+    """A CUDA graph of the launches `fn` makes (called once eagerly first, so
+    every lazily-configured attribute is set before capture)."""
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        fn()
+        side.synchronize()
+        with torch.cuda.graph(g, stream=side):
+            fn()
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize(dev)
+    return g
+
+
 def run_gpu(args):
     rank, local, world, dist = dist_setup(args.gpus)
     torch.cuda.set_device(local)
@@ -241,89 +257,109 @@ def run_gpu(args):
     outs = {(name, M): torch.empty(M, LAYERS[name][0] // (2 if LAYERS[name][2] else 1), dtype=torch.bfloat16,
                                    device=dev) for name in LAYERS for M in MS}
     stream = torch.cuda.current_stream(dev)
-    counter = [0]
 
-    def one_step():
-        for M in MS:
-            r = counter[0] % REPLICAS
-            counter[0] += 1
-            for name, (N, K, silu) in LAYERS.items():
-                w, sf = weights[name][r]
-                fp4gemv.nvfp4_gemv(xs[(name, M)], w, sf, gs, silu_mul=silu, pdl=True, out=outs[(name, M)])
+    def step_with(r):
+        """One step: the 24 (M, layer) calls on weight replica r."""
+        def fn():
+            for M in MS:
+                for name, (N, K, silu) in LAYERS.items():
+                    w, sf = weights[name][r]
+                    fp4gemv.nvfp4_gemv(xs[(name, M)], w, sf, gs, silu_mul=silu, pdl=True, out=outs[(name, M)])
+        return fn
 
-    for _ in range(args.warmup):
-        one_step()
+    # A decode server replays its step as a CUDA graph: one graph per weight
+    # replica, replayed round-robin (each layer's weights come back only after
+    # the other 4 replicas' ~600 MB have streamed through L2).
+    launches0 = fp4gemv.launch_count()
+    graphs = [capture_graph(step_with(r), dev) for r in range(REPLICAS)]
+    launches_per_step = (fp4gemv.launch_count() - launches0) // (2 * REPLICAS)
+    for i in range(args.warmup):
+        graphs[i % REPLICAS].replay()
     torch.cuda.synchronize()
     assert fp4gemv.get_device_error() == 0, "device error during warm-up"
 
     # ---- timed region (device-resident inputs) ----
     barrier(dist)
     torch.cuda.synchronize()
-    launches0 = fp4gemv.launch_count()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         e0.record(stream)
-        for _ in range(args.steps):
-            one_step()
+        for i in range(args.steps):
+            graphs[i % REPLICAS].replay()
         e1.record(stream)
         torch.cuda.synchronize()
     barrier(dist)
-    launches = fp4gemv.launch_count() - launches0
+    launches = launches_per_step * args.steps
     ms_total = e0.elapsed_time(e1)
     ms_total = max_over_ranks(ms_total, dist, dev)
     ms_step = ms_total / args.steps
     total_bytes = step_bytes() * args.steps * world
     value = total_bytes / (ms_total * 1e-3) / 1e9
+    del graphs
 
-    # ---- per-call us (each (layer, M) alone, back to back, replicas rotated) ----
+    # ---- per-call us: each (layer, M) alone, 20 calls per graph, replicas rotated ----
     per_call = {}
-    reps = 20
+    calls = 20
     for name, (N, K, silu) in LAYERS.items():
         per_call[name] = {}
         for M in MS:
+            def fn(name=name, M=M, silu=silu):
+                for i in range(calls):
+                    w, sf = weights[name][i % REPLICAS]
+                    fp4gemv.nvfp4_gemv(xs[(name, M)], w, sf, gs, silu_mul=silu, pdl=True, out=outs[(name, M)])
+            g = capture_graph(fn, dev)
+            g.replay()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            for i in range(3):
-                w, sf = weights[name][i % REPLICAS]
-                fp4gemv.nvfp4_gemv(xs[(name, M)], w, sf, gs, silu_mul=silu, pdl=True, out=outs[(name, M)])
             a.record(stream)
-            for i in range(reps):
-                w, sf = weights[name][i % REPLICAS]
-                fp4gemv.nvfp4_gemv(xs[(name, M)], w, sf, gs, silu_mul=silu, pdl=True, out=outs[(name, M)])
+            for _ in range(3):
+                g.replay()
             b.record(stream)
             torch.cuda.synchronize()
-            us = a.elapsed_time(b) * 1e3 / reps
+            us = a.elapsed_time(b) * 1e3 / (3 * calls)
             per_call[name][str(M)] = {"us": round(us, 2),
                                       "GB/s": round(nvfp4_bytes(M, N, K, silu) / (us * 1e-6) / 1e9, 1)}
+            del g
 
-    # ---- end to end through the public API with host buffers ----
+    # ---- end to end through the public API with pinned host buffers ----
     host_x = {k: v.cpu().pin_memory() for k, v in xs.items()}
     host_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in outs.items()}
     h2d = sum(v.numel() * v.element_size() for v in host_x.values())
     d2h = sum(v.numel() * v.element_size() for v in host_out.values())
 
-    def e2e_step():
-        for M in MS:
-            r = counter[0] % REPLICAS
-            counter[0] += 1
-            for name, (N, K, silu) in LAYERS.items():
-                w, sf = weights[name][r]
-                xd = xs[(name, M)]
-                xd.copy_(host_x[(name, M)], non_blocking=True)
-                fp4gemv.nvfp4_gemv(xd, w, sf, gs, silu_mul=silu, pdl=True, out=outs[(name, M)])
-                host_out[(name, M)].copy_(outs[(name, M)], non_blocking=True)
+    def e2e_with(r):
+        def fn():
+            for M in MS:
+                for name, (N, K, silu) in LAYERS.items():
+                    w, sf = weights[name][r]
+                    xd = xs[(name, M)]
+                    xd.copy_(host_x[(name, M)], non_blocking=True)
+                    fp4gemv.nvfp4_gemv(xd, w, sf, gs, silu_mul=silu, pdl=True, out=outs[(name, M)])
+                    host_out[(name, M)].copy_(outs[(name, M)], non_blocking=True)
+        return fn
 
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
-    barrier(dist)
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    b.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(a.elapsed_time(b), dist, dev)
+    def timed(step_fns, nsteps):
+        barrier(dist)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(nsteps):
+            step_fns[i % len(step_fns)]()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return max_over_ranks(a.elapsed_time(b), dist, dev)
+
+    # (a) the step graph with its copies; (b) the same calls issued eagerly
+    e2e_graphs = [capture_graph(e2e_with(r), dev) for r in range(REPLICAS)]
+    for g in e2e_graphs:
+        g.replay()
+    e2e_ms = timed([g.replay for g in e2e_graphs], args.steps)
+    del e2e_graphs
+    eager_fns = [e2e_with(r) for r in range(REPLICAS)]
+    for f in eager_fns[:2]:
+        f()
+    eager_ms = timed(eager_fns, args.steps)
     e2e_value = total_bytes / (e2e_ms * 1e-3) / 1e9
+    eager_value = total_bytes / (eager_ms * 1e-3) / 1e9
     assert fp4gemv.get_device_error() == 0, "device error during the timed region"
 
     peak, peak_kind = read_peaks()
@@ -338,18 +374,20 @@ def run_gpu(args):
             "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "launches_per_step": len(MS) * len(LAYERS),
-                       "us_per_call_avg": round(ms_step * 1e3 / (len(MS) * len(LAYERS)), 3),
+            "config": {"workload": WORKLOAD, "launches_per_step": launches_per_step,
+                       "us_per_call_avg": round(ms_step * 1e3 / launches_per_step, 3),
                        "l2": f"weights rotated over {REPLICAS} replicas (reuse distance ~490 MB > 3 x L2)",
-                       "global_scale": GS, "pdl": True},
+                       "global_scale": GS, "pdl": True,
+                       "launch": "CUDA graph per step (one per weight replica), PDL edges between the launches"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs (burst copy)",
-                         "traffic": traffic_from_profile(), "kernel": "fp4::gemv_kernel<kDenseFp4>",
+                         "traffic": traffic_from_profile(), "kernel": "fp4::gemv_rf_kernel / fp4::gemv_kernel",
                          "bytes_per_step": step_bytes()},
             "per_call": per_call,
             "clocks": clk.summary(),
             "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+                    "d2h_bytes_per_step": d2h, "launch": "CUDA graph of the step with its copies",
+                    "eager_value": round(eager_value, 1)},
             "gpu_launches": launches,
             "cpu_baseline": cpu,
         }
@@ -367,16 +405,22 @@ def run_gpu(args):
 
 def time_calls(fn_list, reps, stream):
     """Average device time (us) of one call when the calls in fn_list are
-    issued round-robin (each fn uses its own weight replica)."""
-    for f in fn_list[: min(3, len(fn_list))]:
-        f()
+    issued round-robin (each fn uses its own weight replica), replayed from a
+    CUDA graph so host launch cost does not leak into the number."""
+    dev = stream.device
+
+    def fn():
+        for i in range(reps):
+            fn_list[i % len(fn_list)]()
+    g = capture_graph(fn, dev)
+    g.replay()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    for i in range(reps):
-        fn_list[i % len(fn_list)]()
+    g.replay()
+    g.replay()
     b.record(stream)
     torch.cuda.synchronize()
-    return a.elapsed_time(b) * 1e3 / reps
+    return a.elapsed_time(b) * 1e3 / (2 * reps)
 
 
 def replicas_for(nbytes, min_reps=2, target=400 << 20):

@@ -104,4 +104,49 @@ __device__ __forceinline__ void unperm4(const uint32_t (&p)[4], uint32_t (&o)[4]
   o[3] = prmt(p[1], p[3], 0x7632u);
 }
 
+// --- f16 route --------------------------------------------------------------
+// cvt.rn.f16x2.e2m1x2 turns one code byte (two codes, K order) into an exact
+// f16 pair, and an e2m1 value times an e4m3 scale (<= 6 significant bits,
+// magnitude in [2^-10, 2688]) is again an exact normal f16.  So 8 codes cost
+// 4 conversions and 4 f16x2 multiplies, about half of the bf16 route above,
+// and the pairs stay in natural K order.  The activations then have to be
+// f16 as well (one MMA type per instruction); callers convert them and fall
+// back to the bf16 route where a value is not exactly representable.
+
+// 8 codes (natural K order) times a replicated f16x2 scale -> 4 f16x2 words
+// (k0,k1) (k2,k3) (k4,k5) (k6,k7).
+__device__ __forceinline__ void dequant8_f16(uint32_t w, uint32_t s2, uint32_t (&r)[4]) {
+  asm("{ .reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3; }"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+      : "r"(w));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r[i]) : "r"(r[i]), "r"(s2));
+}
+
+// Two e4m3 scale bytes (low byte first) -> replicated f16x2 scales.
+__device__ __forceinline__ void scale_pair_to_f16x2(uint32_t two_bytes, uint32_t& lo, uint32_t& hi) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(static_cast<unsigned short>(two_bytes & 0xFFFFu)));
+  lo = prmt(h, h, 0x1010u);
+  hi = prmt(h, h, 0x3232u);
+}
+
+// bf16 pair -> f16 pair; false if either value is not exactly representable
+// in f16 (too large, too small for its bits, or NaN).
+__device__ __forceinline__ bool bf16x2_to_f16x2_exact(uint32_t v, uint32_t& out) {
+  const float lo = __uint_as_float(v << 16);
+  const float hi = __uint_as_float(v & 0xFFFF0000u);
+  uint32_t h;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(hi), "f"(lo));
+  out = h;
+  const float blo = __half2float(__ushort_as_half(static_cast<unsigned short>(h & 0xFFFFu)));
+  const float bhi = __half2float(__ushort_as_half(static_cast<unsigned short>(h >> 16)));
+  return (blo == lo) & (bhi == hi);
+}
+
 }  // namespace fp4

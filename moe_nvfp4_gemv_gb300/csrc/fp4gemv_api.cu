@@ -43,33 +43,84 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// Encoded tensor maps are cached per host thread: decode calls re-use the
+// same weight and activation buffers, and encoding costs about as much host
+// time as the launch itself.  A map depends only on its key (base address,
+// shape, strides, box, element type); the cache holds no device state, so a
+// stale entry is impossible -- a different buffer is a different key.
+struct MapKey {
+  const void* base;
+  uint64_t dims[3];
+  uint64_t strides[2];
+  uint32_t box[3];
+  int rank, dtype;
+  bool operator==(const MapKey& o) const { return std::memcmp(this, &o, sizeof(MapKey)) == 0; }
+};
+
+bool encode_cached(CUtensorMap* m, const MapKey& key) {
+  constexpr int kEntries = 64;
+  struct Entry {
+    MapKey key;
+    CUtensorMap map;
+    bool used;
+  };
+  thread_local Entry cache[kEntries] = {};
+  thread_local int next = 0;
+  for (int i = 0; i < kEntries; ++i) {
+    if (cache[i].used && cache[i].key == key) {
+      *m = cache[i].map;
+      return true;
+    }
+  }
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint32_t estr[3] = {1, 1, 1};
+  if (fn(m, static_cast<CUtensorMapDataType>(key.dtype), key.rank, const_cast<void*>(key.base), key.dims,
+         key.strides, key.box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  Entry& e = cache[next];
+  next = (next + 1) % kEntries;
+  e.key = key;
+  e.map = *m;
+  e.used = true;
+  return true;
+}
+
 // 2-D row-major tensor [outer, inner] with a 128-byte-swizzled box.
 bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
                uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {row_bytes};
-  const cuuint32_t box[2] = {box_inner, box_outer};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  MapKey k;
+  std::memset(&k, 0, sizeof(k));
+  k.base = base;
+  k.dims[0] = inner;
+  k.dims[1] = outer;
+  k.strides[0] = row_bytes;
+  k.box[0] = box_inner;
+  k.box[1] = box_outer;
+  k.rank = 2;
+  k.dtype = static_cast<int>(dt);
+  return encode_cached(m, k);
 }
 
 // Activations x [M, K] (bf16, row stride ldx) viewed as [K/64, M, 64]: one
 // box {64, rows, 4} holds four 64-wide K atoms of `rows` tokens, each atom a
 // [rows x 128-byte] 128B-swizzled block -- the layout the MMA reads.
 bool encode_x_atoms(CUtensorMap* m, const void* x, int K, int M, int64_t ldx, uint32_t rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(K / 64)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ldx) * 2, 128};
-  const cuuint32_t box[3] = {64, rows, 4};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(x), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  MapKey k;
+  std::memset(&k, 0, sizeof(k));
+  k.base = x;
+  k.dims[0] = 64;
+  k.dims[1] = static_cast<uint64_t>(M);
+  k.dims[2] = static_cast<uint64_t>(K / 64);
+  k.strides[0] = static_cast<uint64_t>(ldx) * 2;
+  k.strides[1] = 128;
+  k.box[0] = 64;
+  k.box[1] = rows;
+  k.box[2] = 4;
+  k.rank = 3;
+  k.dtype = static_cast<int>(CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+  return encode_cached(m, k);
 }
 
 struct DeviceState {
@@ -147,8 +198,13 @@ void size_ring(const KernelInfo& info, int* nstages, size_t* smem, int* ctas_per
   *ctas_per_sm = per_sm;
 }
 
-// Cluster split of K: minimise (waves of CTAs) x (ring stages per CTA), ties
-// to the smaller split; every rank keeps at least one full stage.
+// Cluster split of K.  A CTA costs its ring stages plus a fixed overhead
+// (launch, prologue, first-load latency, cluster reduction, epilogue) of about
+// kFixedStages stages; minimise waves x (stages + fixed), ties to the smaller
+// split.  Every rank keeps a non-empty K range.
+constexpr int kFixedStages = 4;
+constexpr int kStageK4 = fp4::kStageK4;
+
 int pick_split(int tiles, int K, int stage_k, int slots) {
   int best = 1;
   long best_cost = -1;
@@ -159,7 +215,8 @@ int pick_split(int tiles, int K, int stage_k, int slots) {
     const int kslab = ((K + s - 1) / s + 63) / 64 * 64;
     if (s > 1 && static_cast<long>(s - 1) * kslab >= K) break;
     const long stages = (kslab + stage_k - 1) / stage_k;
-    const long cost = waves * stages;
+    const long fixed = kFixedStages * kStageK4 / stage_k;  // the same time in this kernel's stages
+    const long cost = waves * (stages + fixed);
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best = s;

@@ -415,7 +415,7 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
   __syncthreads();
   tc_fence_after();
   if (S > 1) {
-    if (C::kPush) cluster_arrive();  // paired with a wait before the first remote access
+    if (C::kPush) cluster_arrive_relaxed();  // paired with a wait before the first remote access
     else cluster_sync();
   }
   // Let the next kernel in the stream start its own prologue (weight

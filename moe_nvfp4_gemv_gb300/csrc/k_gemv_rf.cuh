@@ -30,6 +30,17 @@
 // (8 codes) yields the bf16 pairs (c0,c4) (c2,c6) (c1,c5) (c3,c7), the A
 // registers of two MMAs, and the activation chunk of the same 8 K (token g,
 // permuted the same way) their B registers.
+//
+// f16 route.  Per stage the consumer warps first convert the stage's
+// activation rows in shared memory to f16 in place, checking that every value
+// converts exactly; the stage then runs on f16 MMAs with the codes converted
+// by cvt.rn.f16x2.e2m1x2 (natural K order, half the ALU work of the bf16
+// route).  A stage with any value that is not exactly an f16 (|x| > 65504,
+// too many low bits for the f16 subnormal grid, NaN) runs the bf16 route with
+// the original activations from global memory instead.  Both routes compute
+// exact products into fp32, so the choice changes no result beyond fp32
+// accumulation order; they accumulate separately (the bf16 route's products
+// carry the 2^-kShift factor) and are summed at the end.
 #pragma once
 
 #include "k_gemv.cuh"
@@ -48,10 +59,24 @@ struct RfCfg {
   static constexpr int kXBytes = kNT * kStageK * 2;
   static constexpr int kStageBytes = kXOff + kXBytes;
   static constexpr int kTiles = kNT / 8;  // MMA n-tiles
+  // Independent fp32 accumulators per n-tile on the f16 route: consecutive
+  // MMAs of a thread go to different chains so they do not wait on each
+  // other's results (an MMA's latency is several times its issue interval).
+  static constexpr int kChains = kNT == 8 ? 4 : 1;  // (16 tokens: the two n-tiles already alternate)
   static constexpr int kInboxBytes = kNT * 136 * 4;
   static_assert(kNT == 8 || kNT == 16, "token tile");
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
 };
+
+// D += A * B for one m16n8k16 f16 MMA (fp32 accumulate).
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
 
 __device__ __forceinline__ uint32_t lds16(uint32_t a) {
   unsigned short v;
@@ -86,8 +111,10 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
   const uint32_t inbox = ring + p.nstages * C::kStageBytes;
   __shared__ __align__(8) uint64_t bar_full[kMaxStages];
   __shared__ __align__(8) uint64_t bar_empty[kMaxStages];
+  __shared__ __align__(8) uint64_t bar_xready[kMaxStages];
   __shared__ __align__(8) uint64_t bar_inbox;
   __shared__ volatile int s_abort;
+  __shared__ int s_xbad[kMaxStages];  // last stage (of this slot) whose activations are not all exact f16
 
   const int tid = threadIdx.x;
   const int warp = tid / 32;
@@ -133,10 +160,12 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
     const int k0 = wk.k_begin + s * C::kStageK;
     const int nchunks = min(C::kStageK, wk.k_end - k0) / kSubK;
     uint32_t bytes = C::kWTileBytes;
+#pragma unroll
     for (int g = 0; g < 3; ++g) bytes += (wk.sgroup[g] >= 0 ? nchunks * 512 : 0);
     asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(fb), "r"(bytes) : "memory");
     tma_load_2d(st, &p.tm_w, k0 / 2, wk.wrow[0], fb, pol_w);
     if (wk.paired) tma_load_2d(st + C::kWTileBytes / 2, &p.tm_w, k0 / 2, wk.wrow[1], fb, pol_w);
+#pragma unroll
     for (int g = 0; g < 3; ++g) {
       if (wk.sgroup[g] < 0) continue;
       const size_t chunk = static_cast<size_t>(wk.sgroup[g]) * (wk.kbp / 4) + k0 / 64;
@@ -153,6 +182,8 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
     for (int i = 0; i < nstages; ++i) {
       mbar_init(smem_u32(&bar_full[i]), 1);
       mbar_init(smem_u32(&bar_empty[i]), C::kConsumerWarps);
+      mbar_init(smem_u32(&bar_xready[i]), C::kConsumerWarps);
+      s_xbad[i] = -1;
     }
     mbar_init(smem_u32(&bar_inbox), 1);
     if (S > 1) mbar_arrive_expect_tx(smem_u32(&bar_inbox), S * kNT * mine * 4);
@@ -160,12 +191,20 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
     for (int s = 0; s < pre; ++s) issue_weights(s);
   }
   __syncthreads();
-  if (S > 1) cluster_arrive();  // paired with a wait before the first remote access
+  if (S > 1) cluster_arrive_relaxed();  // paired with a wait before the first remote access
   if (tid == 0) pdl_launch_dependents();
 
-  float acc[C::kTiles][4];
+  float acc[C::kChains][C::kTiles][4];  // f16-route stages (exact products)
+  float accb[C::kTiles][4];             // bf16-route stages (products times 2^-kShift)
 #pragma unroll
-  for (int t = 0; t < C::kTiles; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
+  for (int t = 0; t < C::kTiles; ++t) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      accb[t][e] = 0.0f;
+#pragma unroll
+      for (int q = 0; q < C::kChains; ++q) acc[q][t][e] = 0.0f;
+    }
+  }
   const int g = lane / 4, c = lane % 4;
   const int sg = (g % 2) * 4 + g / 2;  // sigma(g)
   const int row0 = warp * 16 + sg;     // tile rows of MMA rows g and g + 8
@@ -195,13 +234,81 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
     const uint32_t key = static_cast<uint32_t>(row0 % 8);
     const uint32_t w_off0 = (row0 / 8) * 1024 + (row0 % 8) * 128;
     const uint32_t w_off1 = (row1 / 8) * 1024 + (row1 % 8) * 128;
+    // (static indices only, so the work description stays in registers)
     auto sf_off = [&](int row) -> uint32_t {
-      const int b = wk.paired ? row / 64 : 0;
-      const int r = wk.srow[b] + (wk.paired ? row % 64 : row);
-      const int gslot = b == 0 ? 0 : 1 + (r / 128 - wk.srow[1] / 128);
+      const bool b1 = wk.paired && row >= 64;
+      const int r = (b1 ? wk.srow[1] : wk.srow[0]) + (wk.paired ? row % 64 : row);
+      const int gslot = b1 ? 1 + (r / 128 - wk.srow[1] / 128) : 0;
       return C::kWTileBytes + gslot * 2048 + (r % 32) * 16 + ((r % 128) / 32) * 4;
     };
     const uint32_t sf0 = sf_off(row0), sf1 = sf_off(row1);
+    // One 128-K half of a stage: chunk j = 4 h + c of both rows.  `cvalid`
+    // false (a chunk past the end of a ragged last stage) gives zero A
+    // registers: that chunk's scales were not copied and may hold anything.
+    auto half_f16 = [&](uint32_t st, int h, bool cvalid) {
+      const int j = 4 * h + c;
+      const uint4 A0 = lds128(st + w_off0 + ((static_cast<uint32_t>(j) ^ key) * 16));
+      const uint4 A1 = lds128(st + w_off1 + ((static_cast<uint32_t>(j) ^ key) * 16));
+      const uint32_t sc_off = (j / 2) * 512 + 2 * (j % 2);
+      uint32_t s0lo, s0hi, s1lo, s1hi;
+      scale_pair_to_f16x2(lds16(st + sf0 + sc_off), s0lo, s0hi);
+      scale_pair_to_f16x2(lds16(st + sf1 + sc_off), s1lo, s1hi);
+      if (!cvalid) s0lo = s0hi = s1lo = s1hi = 0u;
+      const uint32_t a0w[4] = {A0.x, A0.y, A0.z, A0.w};
+      const uint32_t a1w[4] = {A1.x, A1.y, A1.z, A1.w};
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        uint32_t r0[4], r1[4];
+        dequant8_f16(a0w[w], w < 2 ? s0lo : s0hi, r0);
+        dequant8_f16(a1w[w], w < 2 ? s1lo : s1hi, r1);
+        // the f16 activations of the same 8 K (natural order): atom u, chunk ch
+        const int kk = 32 * j + 8 * w;
+        const uint32_t u = kk / 64, ch = (kk % 64) / 8;
+#pragma unroll
+        for (int t = 0; t < C::kTiles; ++t) {
+          const int n = 8 * t + g;
+          const uint4 xv = lds128(st + C::kXOff + u * (kNT * 128) + (n / 8) * 1024 + (n % 8) * 128 +
+                                  ((ch ^ static_cast<uint32_t>(n % 8)) * 16));
+          mma_f16_16816(acc[(2 * w) % C::kChains][t], r0[0], r1[0], r0[1], r1[1], xv.x, xv.y);
+          mma_f16_16816(acc[(2 * w + 1) % C::kChains][t], r0[2], r1[2], r0[3], r1[3], xv.z, xv.w);
+        }
+      }
+    };
+    auto half_bf16 = [&](uint32_t st, int k0, int h, bool cvalid) {
+      const int j = 4 * h + c;
+      const uint4 A0 = lds128(st + w_off0 + ((static_cast<uint32_t>(j) ^ key) * 16));
+      const uint4 A1 = lds128(st + w_off1 + ((static_cast<uint32_t>(j) ^ key) * 16));
+      const uint32_t sc_off = (j / 2) * 512 + 2 * (j % 2);
+      uint32_t s0lo, s0hi, s1lo, s1hi;
+      scale_pair_to_bf16x2(lds16(st + sf0 + sc_off), s0lo, s0hi);
+      scale_pair_to_bf16x2(lds16(st + sf1 + sc_off), s1lo, s1hi);
+      if (!cvalid) s0lo = s0hi = s1lo = s1hi = 0u;
+      const uint32_t a0w[4] = {A0.x, A0.y, A0.z, A0.w};
+      const uint32_t a1w[4] = {A1.x, A1.y, A1.z, A1.w};
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        uint32_t r0[4], r1[4];
+        e2m1x8_raw_perm(a0w[w], r0);
+        e2m1x8_raw_perm(a1w[w], r1);
+        const uint32_t sa = w < 2 ? s0lo : s0hi, sb = w < 2 ? s1lo : s1hi;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          r0[q] = bf16x2_mul(r0[q], sa);
+          r1[q] = bf16x2_mul(r1[q], sb);
+        }
+        // the original bf16 activations of the same 8 K, from global memory
+        const int kk = 32 * j + 8 * w;
+#pragma unroll
+        for (int t = 0; t < C::kTiles; ++t) {
+          const int n = 8 * t + g;
+          uint4 xv = make_uint4(0u, 0u, 0u, 0u);
+          if (cvalid && n < p.M)
+            xv = perm_x8(__ldg(reinterpret_cast<const uint4*>(p.x + static_cast<int64_t>(n) * p.ldx + k0 + kk)));
+          mma_bf16_16816(accb[t], r0[0], r1[0], r0[1], r1[1], xv.x, xv.y);
+          mma_bf16_16816(accb[t], r0[2], r1[2], r0[3], r1[3], xv.z, xv.w);
+        }
+      }
+    };
     for (int s = 0; s < nst; ++s) {
       const int slot = s % nstages;
       const uint32_t st = ring + slot * C::kStageBytes;
@@ -214,42 +321,47 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
       // wholly valid or wholly past the end, where its A registers are zero
       // (its scales were not copied and may hold anything)
       const int kvalid = min(C::kStageK, wk.k_end - wk.k_begin - s * C::kStageK);
+      // The stage's activation rows < M to f16 in place (16-byte chunks,
+      // spread over the consumer threads); rows >= M and K past the end are
+      // zeros from the TMA fill, the same bits in f16.
+      {
+        bool exact = true;
+        for (int id = tid; id < p.M * 32; id += kEpiThreads) {
+          const int n = id / 32, q = id % 32;
+          if (8 * q >= kvalid) continue;
+          const uint32_t a = st + C::kXOff + (q / 8) * (kNT * 128) + (n / 8) * 1024 + (n % 8) * 128 +
+                             ((static_cast<uint32_t>(q % 8) ^ static_cast<uint32_t>(n % 8)) * 16);
+          const uint4 v = lds128(a);
+          uint4 o;
+          exact &= bf16x2_to_f16x2_exact(v.x, o.x);
+          exact &= bf16x2_to_f16x2_exact(v.y, o.y);
+          exact &= bf16x2_to_f16x2_exact(v.z, o.z);
+          exact &= bf16x2_to_f16x2_exact(v.w, o.w);
+          sts128(a, o);
+        }
+        if (!exact) s_xbad[slot] = s;
+        fence_proxy_async_smem();  // before the ring slot is refilled by TMA
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bar_xready[slot]));
+      }
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bar_xready[slot]), (s / nstages) & 1, p.err))) {
+        s_abort = 1;
+        break;
+      }
+      if (s_xbad[slot] != s) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        if (128 * h < kvalid) {
-          const int j = 4 * h + c;  // code chunk (32 K) of both rows
-          const bool cvalid = 32 * j < kvalid;
-          const uint4 A0 = lds128(st + w_off0 + ((static_cast<uint32_t>(j) ^ key) * 16));
-          const uint4 A1 = lds128(st + w_off1 + ((static_cast<uint32_t>(j) ^ key) * 16));
-          const uint32_t sc_off = (j / 2) * 512 + 2 * (j % 2);
-          uint32_t s0lo, s0hi, s1lo, s1hi;
-          scale_pair_to_bf16x2(lds16(st + sf0 + sc_off), s0lo, s0hi);
-          scale_pair_to_bf16x2(lds16(st + sf1 + sc_off), s1lo, s1hi);
-          const uint32_t a0w[4] = {A0.x, A0.y, A0.z, A0.w};
-          const uint32_t a1w[4] = {A1.x, A1.y, A1.z, A1.w};
-#pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            uint32_t r0[4], r1[4];
-            e2m1x8_raw_perm(a0w[w], r0);
-            e2m1x8_raw_perm(a1w[w], r1);
-            const uint32_t sa = w < 2 ? s0lo : s0hi, sb = w < 2 ? s1lo : s1hi;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              r0[q] = cvalid ? bf16x2_mul(r0[q], sa) : 0u;
-              r1[q] = cvalid ? bf16x2_mul(r1[q], sb) : 0u;
-            }
-            // activations of the same 8 K: atom u, 16-byte chunk ch of token n
-            const int kk = 32 * j + 8 * w;
-            const uint32_t u = kk / 64, ch = (kk % 64) / 8;
-#pragma unroll
-            for (int t = 0; t < C::kTiles; ++t) {
-              const int n = 8 * t + g;
-              const uint4 xv = perm_x8(lds128(st + C::kXOff + u * (kNT * 128) + (n / 8) * 1024 + (n % 8) * 128 +
-                                              ((ch ^ static_cast<uint32_t>(n % 8)) * 16)));
-              mma_bf16_16816(acc[t], r0[0], r1[0], r0[1], r1[1], xv.x, xv.y);
-              mma_bf16_16816(acc[t], r0[2], r1[2], r0[3], r1[3], xv.z, xv.w);
-            }
+        for (int h = 0; h < 2; ++h) {
+          if (128 * h < kvalid) {
+            if (128 * (h + 1) <= kvalid) half_f16(st, h, true);
+            else half_f16(st, h, 32 * (4 * h + c) < kvalid);
           }
+        }
+      } else {
+        pdl_wait();  // the activations are read from global memory directly
+        const int k0 = wk.k_begin + s * C::kStageK;
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          if (128 * h < kvalid) half_bf16(st, k0, h, 32 * (4 * h + c) < kvalid);
         }
       }
       __syncwarp();
@@ -281,7 +393,10 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int n = 8 * t + 2 * c + e;
-          const float v = go ? acc[t][2 * hr + e] * post : 0.0f;
+          float a16 = 0.0f;
+#pragma unroll
+          for (int q = 0; q < C::kChains; ++q) a16 += acc[q][t][2 * hr + e];
+          const float v = go ? a16 + accb[t][2 * hr + e] * post : 0.0f;
           const uint32_t off = n * rows_owner * 4;
           if (S > 1) st_async_f32(rbase + off, v, rbar);
           else stsf(rbase + off, v);

@@ -69,6 +69,7 @@ def _load() -> ctypes.CDLL:
 
 _lib = _load()
 LIB_PATH = _build.LIB
+_nvfp4_gemv = _lib.fp4gemv_nvfp4_gemv
 
 
 def lib() -> ctypes.CDLL:
@@ -84,8 +85,21 @@ def _ptr(t: torch.Tensor | None):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+try:  # the current stream's raw handle without building a Stream object
+    _raw_stream = torch._C._cuda_getCurrentRawStream
+except AttributeError:  # pragma: no cover - older torch
+    def _raw_stream(index):
+        return torch.cuda.current_stream(index).cuda_stream
+
+
 def _stream(dev: torch.device):
-    return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+    return ctypes.c_void_p(_raw_stream(dev.index if dev.index is not None else torch.cuda.current_device()))
+
+
+_U8 = torch.uint8
+_BF16 = torch.bfloat16
+_FP4_WEIGHT_DTYPES = (torch.uint8, torch.int8)
+_SCALE_DTYPES = (torch.uint8, torch.float8_e4m3fn)
 
 
 def _bytes(t: torch.Tensor) -> torch.Tensor:
@@ -109,20 +123,33 @@ def scale_bytes(rows: int, K: int) -> int:
 def nvfp4_gemv(x: torch.Tensor, weight: torch.Tensor, weight_scale: torch.Tensor, global_scale: torch.Tensor,
                silu_mul: bool = False, pdl: bool = True, out: torch.Tensor | None = None) -> torch.Tensor:
     """bf16 [M, N] = bf16(fp32(x @ dequant(weight).T) * global_scale); with
-    silu_mul the [M, N/2] bf16 silu(gate) * up of the [gate | up] halves."""
-    x = _rows_bf16(x, "x")
+    silu_mul the [M, N/2] bf16 silu(gate) * up of the [gate | up] halves.
+
+    The decode path: only cheap attribute checks here (the library validates
+    shapes, alignment and pointers before it launches anything)."""
+    if x.dtype is not _BF16 or x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be a 2-D bf16 tensor with unit inner stride")
     M, K = x.shape
-    w = _bytes(weight)
-    N = w.shape[0]
-    if w.dim() != 2 or w.shape[1] * 2 != K:
-        raise ValueError("weight must be uint8 [N, K/2]")
+    if weight.dtype not in _FP4_WEIGHT_DTYPES or weight.dim() != 2 or not weight.is_contiguous() \
+            or weight.shape[1] * 2 != K:
+        raise ValueError("weight must be a contiguous uint8 [N, K/2] tensor")
+    if weight_scale.dtype not in _SCALE_DTYPES or not weight_scale.is_contiguous():
+        raise ValueError("weight_scale must be a contiguous uint8 / float8_e4m3fn tensor")
+    if global_scale.dtype is not torch.float32 or global_scale.numel() != 1:
+        raise ValueError("global_scale must be one float32 value")
+    N = weight.shape[0]
     n_out = N // 2 if silu_mul else N
+    dev = x.device
     if out is None:
-        out = torch.empty(M, n_out, dtype=torch.bfloat16, device=x.device)
-    gs = global_scale.reshape(1)
-    _check(_lib.fp4gemv_nvfp4_gemv(_ptr(x), x.stride(0), _ptr(w), _ptr(_bytes(weight_scale)), _ptr(gs), _ptr(out),
-                                   out.stride(0), M, N, K, int(silu_mul), int(pdl), _stream(x.device)),
-           "fp4gemv_nvfp4_gemv")
+        out = torch.empty(M, n_out, dtype=_BF16, device=dev)
+    elif out.dtype is not _BF16 or out.dim() != 2 or out.stride(1) != 1 or out.shape[0] != M or out.shape[1] != n_out:
+        raise ValueError(f"out must be a bf16 [{M}, {n_out}] tensor with unit inner stride")
+    st = _raw_stream(dev.index)
+    status = _nvfp4_gemv(x.data_ptr(), x.stride(0), weight.data_ptr(), weight_scale.data_ptr(),
+                         global_scale.data_ptr(), out.data_ptr(), out.stride(0), M, N, K, 1 if silu_mul else 0,
+                         1 if pdl else 0, st)
+    if status:
+        raise Fp4GemvError(status, "fp4gemv_nvfp4_gemv")
     return out
 
 

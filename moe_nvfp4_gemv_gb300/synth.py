@@ -4,7 +4,8 @@ This module holds NO arithmetic of the method: no decoding, no scale layout,
 no contraction.  It only draws random numbers of the shapes and value
 distributions of the workloads:
 
-* activations ``x``: bf16 ~ N(0, 1);
+* activations ``x``: bf16 ~ N(0, 1) (and a wide-range variant with a few
+  entries of very large or very small magnitude);
 * NVFP4 weights: uint8 bytes uniform on 0..255 (two uniform 4-bit codes);
 * block scales: every byte of the flat scale buffer is float8_e4m3fn(2^U),
   U ~ Uniform[-3, 3] (round-to-nearest cast).  Because each logical scale
@@ -36,6 +37,23 @@ def activations(M: int, K: int, seed: int, device="cpu") -> torch.Tensor:
     """bf16 [M, K] ~ N(0, 1)."""
     g = _gen(seed, device)
     return torch.randn(M, K, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+
+
+def activations_wide_range(M: int, K: int, seed: int, device="cpu", frac: float = 0.01) -> torch.Tensor:
+    """bf16 [M, K] ~ N(0, 1) where a fraction `frac` of the entries in the
+    first half of K is replaced by a value of the same sign and magnitude
+    10^V, V ~ Uniform[5, 7] or Uniform[-9, -6] with equal odds (far outside
+    the f16 range, or below its subnormal grid).  The second half of K keeps
+    the plain N(0, 1) draw."""
+    g = _gen(seed, device)
+    x = torch.randn(M, K, generator=g, device=device, dtype=torch.float32)
+    pick = torch.rand(M, K, generator=g, device=device) < frac
+    pick[:, K // 2:] = False
+    big = torch.rand(M, K, generator=g, device=device) < 0.5
+    v = torch.rand(M, K, generator=g, device=device)
+    mag = torch.where(big, torch.pow(10.0, 5.0 + 2.0 * v), torch.pow(10.0, -9.0 + 3.0 * v))
+    x = torch.where(pick, torch.sign(x) * mag, x)
+    return x.to(torch.bfloat16)
 
 
 def fp4_bytes(rows: int, K: int, seed: int, device="cpu") -> torch.Tensor:

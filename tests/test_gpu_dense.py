@@ -40,7 +40,7 @@ def test_tiny_config(fp4):
     assert_close(u16(got), ref, "tiny config")
 
 
-SHAPES = [(256, 512), (1040, 768), (512, 320), (384, 4096), (2048, 2304)]
+SHAPES = [(256, 512), (1040, 768), (512, 320), (768, 448), (384, 4096), (2048, 2304)]
 
 
 @pytest.mark.parametrize("M", [1, 2, 5, 8, 16, 17, 32, 33, 64, 100, 128])
@@ -51,6 +51,21 @@ def test_nvfp4_gemv(fp4, M, N, K):
     got = fp4.nvfp4_gemv(x.to(DEV), w.to(DEV), sf.to(DEV), torch.tensor([gs], device=DEV))
     ref = oracle.nvfp4_gemv(u16(x), w.numpy(), sf.numpy(), gs)
     assert_close(u16(got), ref, f"nvfp4_gemv M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("M", [1, 6, 16, 24])
+@pytest.mark.parametrize("N,K,silu", [(512, 2304, False), (1056, 1280, True), (768, 448, False)])
+def test_nvfp4_gemv_wide_range_activations(fp4, M, N, K, silu):
+    # Activations far outside the f16 range or below its subnormal grid in the
+    # first half of K: those K stages must take the exact bf16 route, the rest
+    # the f16 route, and the result must not change.
+    x = synth.activations_wide_range(M, K, seed=5 * M + N)
+    w = synth.fp4_bytes(N, K, seed=N + 1)
+    sf = synth.e4m3_bytes(oracle.scale_bytes(N, K), seed=N + 2)
+    gs = 0.01
+    got = fp4.nvfp4_gemv(x.to(DEV), w.to(DEV), sf.to(DEV), torch.tensor([gs], device=DEV), silu_mul=silu)
+    ref = oracle.nvfp4_gemv(u16(x), w.numpy(), sf.numpy(), gs, silu_mul=silu)
+    assert_close(u16(got), ref, f"wide-range nvfp4_gemv M={M} N={N} K={K} silu={silu}")
 
 
 @pytest.mark.parametrize("M", [1, 3, 16, 32, 80])
