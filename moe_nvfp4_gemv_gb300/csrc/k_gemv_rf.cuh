@@ -31,9 +31,11 @@
 // registers of two MMAs, and the activation chunk of the same 8 K (token g,
 // permuted the same way) their B registers.
 //
-// f16 route.  Per stage the consumer warps first convert the stage's
-// activation rows in shared memory to f16 in place, checking that every value
-// converts exactly; the stage then runs on f16 MMAs with the codes converted
+// Routes.  For M > kF16MaxM every stage runs the bf16 route above.  For
+// M <= kF16MaxM the f16 route: a converter warp turns each stage's activation
+// rows in shared memory into f16 in place as soon as the stage lands (ahead of the
+// consumers, which wait for it on a per-stage barrier), checking that every
+// value converts exactly; the stage then runs on f16 MMAs with the codes converted
 // by cvt.rn.f16x2.e2m1x2 (natural K order, half the ALU work of the bf16
 // route).  A stage with any value that is not exactly an f16 (|x| > 65504,
 // too many low bits for the f16 subnormal grid, NaN) runs the bf16 route with
@@ -50,8 +52,9 @@ namespace fp4 {
 template <int kNT>
 struct RfCfg {
   static constexpr int kConsumerWarps = 8;
-  static constexpr int kThreads = kConsumerWarps * 32 + 32;
+  static constexpr int kThreads = kConsumerWarps * 32 + 64;
   static constexpr int kProducerWarp = kConsumerWarps;
+  static constexpr int kConverterWarp = kConsumerWarps + 1;
   static constexpr int kStageK = 256;
   static constexpr int kWTileBytes = 128 * 128;
   static constexpr int kSfTileBytes = 3 * 4 * 512;
@@ -63,6 +66,10 @@ struct RfCfg {
   // MMAs of a thread go to different chains so they do not wait on each
   // other's results (an MMA's latency is several times its issue interval).
   static constexpr int kChains = kNT == 8 ? 4 : 1;  // (16 tokens: the two n-tiles already alternate)
+  // Token counts up to which the f16 route is used: its per-stage activation
+  // conversion (one warp) costs ~M x 32 chunk conversions, which outweighs
+  // the cheaper dequantization beyond a few tokens.
+  static constexpr int kF16MaxM = 4;
   static constexpr int kInboxBytes = kNT * 136 * 4;
   static_assert(kNT == 8 || kNT == 16, "token tile");
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
@@ -182,7 +189,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
     for (int i = 0; i < nstages; ++i) {
       mbar_init(smem_u32(&bar_full[i]), 1);
       mbar_init(smem_u32(&bar_empty[i]), C::kConsumerWarps);
-      mbar_init(smem_u32(&bar_xready[i]), C::kConsumerWarps);
+      mbar_init(smem_u32(&bar_xready[i]), 1);
       s_xbad[i] = -1;
     }
     mbar_init(smem_u32(&bar_inbox), 1);
@@ -194,8 +201,8 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
   if (S > 1) cluster_arrive_relaxed();  // paired with a wait before the first remote access
   if (tid == 0) pdl_launch_dependents();
 
-  float acc[C::kChains][C::kTiles][4];  // f16-route stages (exact products)
-  float accb[C::kTiles][4];             // bf16-route stages (products times 2^-kShift)
+  float acc[C::kChains][C::kTiles][4];  // main route's stages
+  float accb[C::kTiles][4];             // f16 route: fallback stages (bf16, products times 2^-kShift)
 #pragma unroll
   for (int t = 0; t < C::kTiles; ++t) {
 #pragma unroll
@@ -227,6 +234,41 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
         tma_load_3d(st + C::kXOff, &p.tm_x, 0, 0, k0 / kSubK, fb, pol_x);
       }
     }
+  } else if (warp == C::kConverterWarp) {
+    // ------------------------------------------------------------------ converter
+    if (p.M <= C::kF16MaxM)
+    // Rows < M of each stage's activations to f16 in place (16-byte chunks);
+    // rows >= M and K past the end are zeros from the TMA fill, the same bits
+    // in f16.  A stage with any inexact value is flagged for the bf16 route.
+    for (int s = 0; s < nst; ++s) {
+      const int slot = s % nstages;
+      const uint32_t st = ring + slot * C::kStageBytes;
+      const bool ok =
+          __all_sync(0xFFFFFFFFu, !s_abort && mbar_wait(smem_u32(&bar_full[slot]), (s / nstages) & 1, p.err));
+      if (!ok) {
+        s_abort = 1;
+        break;
+      }
+      const int kvalid = min(C::kStageK, wk.k_end - wk.k_begin - s * C::kStageK);
+      bool exact = true;
+      for (int id = lane; id < p.M * 32; id += 32) {
+        const int n = id / 32, q = id % 32;
+        if (8 * q >= kvalid) continue;
+        const uint32_t a = st + C::kXOff + (q / 8) * (kNT * 128) + (n / 8) * 1024 + (n % 8) * 128 +
+                           ((static_cast<uint32_t>(q % 8) ^ static_cast<uint32_t>(n % 8)) * 16);
+        const uint4 v = lds128(a);
+        uint4 o;
+        exact &= bf16x2_to_f16x2_exact(v.x, o.x);
+        exact &= bf16x2_to_f16x2_exact(v.y, o.y);
+        exact &= bf16x2_to_f16x2_exact(v.z, o.z);
+        exact &= bf16x2_to_f16x2_exact(v.w, o.w);
+        sts128(a, o);
+      }
+      if (!__all_sync(0xFFFFFFFFu, exact) && lane == 0) s_xbad[slot] = s;
+      fence_proxy_async_smem();  // these writes precede the slot's next TMA fill
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bar_xready[slot]));
+    }
   } else {
     // ------------------------------------------------------------------ consumers
     // shared-memory offsets of this thread's two rows (128-byte swizzle key
@@ -242,6 +284,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
       return C::kWTileBytes + gslot * 2048 + (r % 32) * 16 + ((r % 128) / 32) * 4;
     };
     const uint32_t sf0 = sf_off(row0), sf1 = sf_off(row1);
+    const bool f16route = p.M <= C::kF16MaxM;
     // One 128-K half of a stage: chunk j = 4 h + c of both rows.  `cvalid`
     // false (a chunk past the end of a ragged last stage) gives zero A
     // registers: that chunk's scales were not copied and may hold anything.
@@ -274,6 +317,44 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
         }
       }
     };
+    // bf16 route, activations from the stage in shared memory (permuted in
+    // registers to the weight pairs' K order)
+    auto half_bf16_smem = [&](uint32_t st, int h, bool cvalid) {
+      const int j = 4 * h + c;
+      const uint4 A0 = lds128(st + w_off0 + ((static_cast<uint32_t>(j) ^ key) * 16));
+      const uint4 A1 = lds128(st + w_off1 + ((static_cast<uint32_t>(j) ^ key) * 16));
+      const uint32_t sc_off = (j / 2) * 512 + 2 * (j % 2);
+      uint32_t s0lo, s0hi, s1lo, s1hi;
+      scale_pair_to_bf16x2(lds16(st + sf0 + sc_off), s0lo, s0hi);
+      scale_pair_to_bf16x2(lds16(st + sf1 + sc_off), s1lo, s1hi);
+      if (!cvalid) s0lo = s0hi = s1lo = s1hi = 0u;
+      const uint32_t a0w[4] = {A0.x, A0.y, A0.z, A0.w};
+      const uint32_t a1w[4] = {A1.x, A1.y, A1.z, A1.w};
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        uint32_t r0[4], r1[4];
+        e2m1x8_raw_perm(a0w[w], r0);
+        e2m1x8_raw_perm(a1w[w], r1);
+        const uint32_t sa = w < 2 ? s0lo : s0hi, sb = w < 2 ? s1lo : s1hi;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          r0[q] = bf16x2_mul(r0[q], sa);
+          r1[q] = bf16x2_mul(r1[q], sb);
+        }
+        const int kk = 32 * j + 8 * w;
+        const uint32_t u = kk / 64, ch = (kk % 64) / 8;
+#pragma unroll
+        for (int t = 0; t < C::kTiles; ++t) {
+          const int n = 8 * t + g;
+          const uint4 xv = perm_x8(lds128(st + C::kXOff + u * (kNT * 128) + (n / 8) * 1024 + (n % 8) * 128 +
+                                          ((ch ^ static_cast<uint32_t>(n % 8)) * 16)));
+          mma_bf16_16816(acc[(2 * w) % C::kChains][t], r0[0], r1[0], r0[1], r1[1], xv.x, xv.y);
+          mma_bf16_16816(acc[(2 * w + 1) % C::kChains][t], r0[2], r1[2], r0[3], r1[3], xv.z, xv.w);
+        }
+      }
+    };
+    // bf16 route with the activations from global memory: the f16 route's
+    // fallback for a stage whose activations are not all exact f16
     auto half_bf16 = [&](uint32_t st, int k0, int h, bool cvalid) {
       const int j = 4 * h + c;
       const uint4 A0 = lds128(st + w_off0 + ((static_cast<uint32_t>(j) ^ key) * 16));
@@ -321,29 +402,19 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
       // wholly valid or wholly past the end, where its A registers are zero
       // (its scales were not copied and may hold anything)
       const int kvalid = min(C::kStageK, wk.k_end - wk.k_begin - s * C::kStageK);
-      // The stage's activation rows < M to f16 in place (16-byte chunks,
-      // spread over the consumer threads); rows >= M and K past the end are
-      // zeros from the TMA fill, the same bits in f16.
-      {
-        bool exact = true;
-        for (int id = tid; id < p.M * 32; id += kEpiThreads) {
-          const int n = id / 32, q = id % 32;
-          if (8 * q >= kvalid) continue;
-          const uint32_t a = st + C::kXOff + (q / 8) * (kNT * 128) + (n / 8) * 1024 + (n % 8) * 128 +
-                             ((static_cast<uint32_t>(q % 8) ^ static_cast<uint32_t>(n % 8)) * 16);
-          const uint4 v = lds128(a);
-          uint4 o;
-          exact &= bf16x2_to_f16x2_exact(v.x, o.x);
-          exact &= bf16x2_to_f16x2_exact(v.y, o.y);
-          exact &= bf16x2_to_f16x2_exact(v.z, o.z);
-          exact &= bf16x2_to_f16x2_exact(v.w, o.w);
-          sts128(a, o);
+      if (!f16route) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (128 * h < kvalid) {
+            if (128 * (h + 1) <= kvalid) half_bf16_smem(st, h, true);
+            else half_bf16_smem(st, h, 32 * (4 * h + c) < kvalid);
+          }
         }
-        if (!exact) s_xbad[slot] = s;
-        fence_proxy_async_smem();  // before the ring slot is refilled by TMA
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bar_xready[slot]));
+        if (lane == 0) mbar_arrive(smem_u32(&bar_empty[slot]));
+        continue;
       }
+      // the converter warp has turned the stage's activations into f16
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bar_xready[slot]), (s / nstages) & 1, p.err))) {
         s_abort = 1;
         break;
@@ -371,7 +442,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
 
   // ==================================================================== epilogue
   __syncwarp();
-  if (warp < C::kProducerWarp) {
+  if (warp < C::kConsumerWarps) {
     const float post = static_cast<float>(1 << kShift);
     // Push this thread's partials (rows row0 / row1, tokens 8t + 2c + {0,1})
     // to the owners of the rows: inbox[src][n][rr].
@@ -396,6 +467,9 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
           float a16 = 0.0f;
 #pragma unroll
           for (int q = 0; q < C::kChains; ++q) a16 += acc[q][t][2 * hr + e];
+          // acc holds the main route's products (exact on the f16 route,
+          // times 2^-kShift on the bf16 route); accb the f16 route's fallback
+          if (p.M > C::kF16MaxM) a16 *= post;
           const float v = go ? a16 + accb[t][2 * hr + e] * post : 0.0f;
           const uint32_t off = n * rows_owner * 4;
           if (S > 1) st_async_f32(rbase + off, v, rbar);
