@@ -247,7 +247,8 @@ fp4gemv_status dense_launch(int mode, const void* x, int64_t ldx, const void* w,
   if (st != FP4GEMV_OK) return st;
 
   // NVFP4 weights and M <= 16: the register-fed kernel (8- or 16-token tile);
-  // otherwise the tcgen05 kernel.
+  // otherwise the tcgen05 kernel (at 32 tokens the register-fed kernel is
+  // bound by its MMA count and no faster).
   const bool rf = fp4w && M <= 16;
   const int kmode = rf ? kDenseFp4Rf : mode;
   const int NT = rf ? (M <= 8 ? 8 : 16) : pick_nt(M);

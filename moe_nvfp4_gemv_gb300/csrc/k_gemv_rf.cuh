@@ -70,6 +70,7 @@ struct RfCfg {
   // conversion (one warp) costs ~M x 32 chunk conversions, which outweighs
   // the cheaper dequantization beyond a few tokens.
   static constexpr int kF16MaxM = 4;
+  static constexpr bool kHasF16 = kNT == 8;  // only the 8-token tile serves M <= kF16MaxM
   static constexpr int kInboxBytes = kNT * 136 * 4;
   static_assert(kNT == 8 || kNT == 16, "token tile");
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
@@ -202,16 +203,17 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
   if (tid == 0) pdl_launch_dependents();
 
   float acc[C::kChains][C::kTiles][4];  // main route's stages
-  float accb[C::kTiles][4];             // f16 route: fallback stages (bf16, products times 2^-kShift)
+  float accb[C::kHasF16 ? C::kTiles : 1][4];  // f16 route: fallback stages (bf16, products times 2^-kShift)
 #pragma unroll
   for (int t = 0; t < C::kTiles; ++t) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      accb[t][e] = 0.0f;
 #pragma unroll
       for (int q = 0; q < C::kChains; ++q) acc[q][t][e] = 0.0f;
     }
   }
+#pragma unroll
+  for (int t = 0; t < (C::kHasF16 ? C::kTiles : 1); ++t) accb[t][0] = accb[t][1] = accb[t][2] = accb[t][3] = 0.0f;
   const int g = lane / 4, c = lane % 4;
   const int sg = (g % 2) * 4 + g / 2;  // sigma(g)
   const int row0 = warp * 16 + sg;     // tile rows of MMA rows g and g + 8
@@ -236,7 +238,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
     }
   } else if (warp == C::kConverterWarp) {
     // ------------------------------------------------------------------ converter
-    if (p.M <= C::kF16MaxM)
+    if (C::kHasF16 && p.M <= C::kF16MaxM)
     // Rows < M of each stage's activations to f16 in place (16-byte chunks);
     // rows >= M and K past the end are zeros from the TMA fill, the same bits
     // in f16.  A stage with any inexact value is flagged for the bf16 route.
@@ -284,7 +286,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
       return C::kWTileBytes + gslot * 2048 + (r % 32) * 16 + ((r % 128) / 32) * 4;
     };
     const uint32_t sf0 = sf_off(row0), sf1 = sf_off(row1);
-    const bool f16route = p.M <= C::kF16MaxM;
+    const bool f16route = C::kHasF16 && p.M <= C::kF16MaxM;
     // One 128-K half of a stage: chunk j = 4 h + c of both rows.  `cvalid`
     // false (a chunk past the end of a ragged last stage) gives zero A
     // registers: that chunk's scales were not copied and may hold anything.
@@ -385,8 +387,8 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
           uint4 xv = make_uint4(0u, 0u, 0u, 0u);
           if (cvalid && n < p.M)
             xv = perm_x8(__ldg(reinterpret_cast<const uint4*>(p.x + static_cast<int64_t>(n) * p.ldx + k0 + kk)));
-          mma_bf16_16816(accb[t], r0[0], r1[0], r0[1], r1[1], xv.x, xv.y);
-          mma_bf16_16816(accb[t], r0[2], r1[2], r0[3], r1[3], xv.z, xv.w);
+          mma_bf16_16816(accb[C::kHasF16 ? t : 0], r0[0], r1[0], r0[1], r1[1], xv.x, xv.y);
+          mma_bf16_16816(accb[C::kHasF16 ? t : 0], r0[2], r1[2], r0[3], r1[3], xv.z, xv.w);
         }
       }
     };
@@ -414,6 +416,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
         if (lane == 0) mbar_arrive(smem_u32(&bar_empty[slot]));
         continue;
       }
+      if constexpr (C::kHasF16) {
       // the converter warp has turned the stage's activations into f16
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bar_xready[slot]), (s / nstages) & 1, p.err))) {
         s_abort = 1;
@@ -434,6 +437,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
         for (int h = 0; h < 2; ++h) {
           if (128 * h < kvalid) half_bf16(st, k0, h, 32 * (4 * h + c) < kvalid);
         }
+      }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bar_empty[slot]));
@@ -469,8 +473,9 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
           for (int q = 0; q < C::kChains; ++q) a16 += acc[q][t][2 * hr + e];
           // acc holds the main route's products (exact on the f16 route,
           // times 2^-kShift on the bf16 route); accb the f16 route's fallback
-          if (p.M > C::kF16MaxM) a16 *= post;
-          const float v = go ? a16 + accb[t][2 * hr + e] * post : 0.0f;
+          if (!C::kHasF16 || p.M > C::kF16MaxM) a16 *= post;
+          if constexpr (C::kHasF16) a16 += accb[t][2 * hr + e] * post;
+          const float v = go ? a16 : 0.0f;
           const uint32_t off = n * rows_owner * 4;
           if (S > 1) st_async_f32(rbase + off, v, rbar);
           else stsf(rbase + off, v);
