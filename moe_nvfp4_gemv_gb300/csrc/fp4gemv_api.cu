@@ -156,14 +156,19 @@ fp4gemv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FP4GEMV_OK :
 
 int pick_nt(int m) { return m <= 16 ? 16 : m <= 32 ? 32 : m <= 64 ? 64 : 128; }
 
-// Pseudo-mode of the register-fed dense NVFP4 kernel (M <= 16).
-constexpr int kDenseFp4Rf = 100;
+// Pseudo-modes of the register-fed NVFP4 kernel (chunks of <= 16 tokens).
+constexpr int kRfBase = 100;
+constexpr int kDenseFp4Rf = kRfBase + fp4::kDenseFp4;
+constexpr int kMoeGateUpRf = kRfBase + fp4::kMoeGateUp;
+constexpr int kMoeDownRf = kRfBase + fp4::kMoeDown;
 
 cudaError_t kernel_info(int mode, int nt, KernelInfo* info) {
   GemvParams dummy;
   LaunchCfg cfg{};
   switch (mode) {
-    case kDenseFp4Rf: return fp4::launch_dense_rf(nt, dummy, cfg, info);
+    case kDenseFp4Rf:
+    case kMoeGateUpRf:
+    case kMoeDownRf: return fp4::launch_rf(mode - kRfBase, nt, dummy, cfg, info);
     case fp4::kDenseFp4: return fp4::launch_dense_fp4(nt, dummy, cfg, info);
     case fp4::kDenseBf16: return fp4::launch_dense_bf16(nt, dummy, cfg, info);
     default: return fp4::launch_moe(mode, nt, dummy, cfg, info);
@@ -173,7 +178,9 @@ cudaError_t kernel_info(int mode, int nt, KernelInfo* info) {
 cudaError_t kernel_launch(int mode, int nt, const GemvParams& p, const LaunchCfg& cfg) {
   g_launches.fetch_add(1, std::memory_order_relaxed);
   switch (mode) {
-    case kDenseFp4Rf: return fp4::launch_dense_rf(nt, p, cfg, nullptr);
+    case kDenseFp4Rf:
+    case kMoeGateUpRf:
+    case kMoeDownRf: return fp4::launch_rf(mode - kRfBase, nt, p, cfg, nullptr);
     case fp4::kDenseFp4: return fp4::launch_dense_fp4(nt, p, cfg, nullptr);
     case fp4::kDenseBf16: return fp4::launch_dense_bf16(nt, p, cfg, nullptr);
     default: return fp4::launch_moe(mode, nt, p, cfg, nullptr);
@@ -374,9 +381,15 @@ fp4gemv_status fp4gemv_moe_gate_up(const void* x, const int32_t* ids, int M, int
   int sms = 0;
   fp4gemv_status st = device_state(&err, &sms);
   if (st != FP4GEMV_OK) return st;
-  const int NT = M <= 16 ? 16 : 32;
+  // chunks of <= 16 tokens / pairs: the register-fed kernel; else tcgen05
+  // Register-fed kernel for up to 64 tokens: expert chunks hold at most 16
+  // pairs (more pairs routed to one expert form further chunks) and the
+  // shared expert runs ceil(M / 16) chunks; the tcgen05 kernel beyond.
+  const bool rf = M <= 64;
+  const int kmode = rf ? kMoeGateUpRf : fp4::kMoeGateUp;
+  const int NT = rf ? (M <= 8 ? 8 : 16) : 32;
   KernelInfo info{};
-  if (kernel_info(fp4::kMoeGateUp, NT, &info) != cudaSuccess) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
+  if (kernel_info(kmode, NT, &info) != cudaSuccess) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
   int nstages = 0, per_sm = 0;
   size_t smem = 0;
   size_ring(info, &nstages, &smem, &per_sm);
@@ -423,7 +436,7 @@ fp4gemv_status fp4gemv_moe_gate_up(const void* x, const int32_t* ids, int M, int
   cfg.smem = smem;
   cfg.pdl = pdl;
   cfg.stream = stream;
-  return from_cuda(kernel_launch(fp4::kMoeGateUp, NT, p, cfg));
+  return from_cuda(kernel_launch(kmode, NT, p, cfg));
 }
 
 size_t fp4gemv_moe_down_combine_workspace_bytes(int M, int topk, int H) {
@@ -454,9 +467,14 @@ fp4gemv_status fp4gemv_moe_down_combine(const void* act, const int32_t* ids, con
   int sms = 0;
   fp4gemv_status st = device_state(&err, &sms);
   if (st != FP4GEMV_OK) return st;
-  const int NT = M <= 16 ? 16 : 32;
+  // Register-fed kernel for up to 64 tokens: expert chunks hold at most 16
+  // pairs (more pairs routed to one expert form further chunks) and the
+  // shared expert runs ceil(M / 16) chunks; the tcgen05 kernel beyond.
+  const bool rf = M <= 64;
+  const int kmode = rf ? kMoeDownRf : fp4::kMoeDown;
+  const int NT = rf ? (M <= 8 ? 8 : 16) : 32;
   KernelInfo info{};
-  if (kernel_info(fp4::kMoeDown, NT, &info) != cudaSuccess) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
+  if (kernel_info(kmode, NT, &info) != cudaSuccess) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
   int nstages = 0, per_sm = 0;
   size_t smem = 0;
   size_ring(info, &nstages, &smem, &per_sm);
@@ -512,7 +530,7 @@ fp4gemv_status fp4gemv_moe_down_combine(const void* act, const int32_t* ids, con
   cfg.smem = smem;
   cfg.pdl = pdl;
   cfg.stream = stream;
-  return from_cuda(kernel_launch(fp4::kMoeDown, NT, p, cfg));
+  return from_cuda(kernel_launch(kmode, NT, p, cfg));
 }
 
 fp4gemv_status fp4gemv_get_device_error(cudaStream_t stream) {

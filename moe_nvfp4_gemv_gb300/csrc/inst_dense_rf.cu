@@ -1,10 +1,11 @@
-// Instantiations of the register-fed dense NVFP4 GEMV (M <= 16).
+// Instantiations of the register-fed NVFP4 kernel (dense GEMV and both MoE
+// kernels, chunks of at most 16 tokens / pairs).
 #include "k_gemv_rf.cuh"
 #include "launch.h"
 
 namespace fp4 {
 
-template <int kNT>
+template <int kMode, int kNT>
 cudaError_t run_gemv_rf(const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info) {
   using C = RfCfg<kNT>;
   if (info) {
@@ -15,7 +16,7 @@ cudaError_t run_gemv_rf(const GemvParams& p, const LaunchCfg& cfg, KernelInfo* i
     info->tmem_cols = 0;
     return cudaSuccess;
   }
-  auto k = gemv_rf_kernel<kNT>;
+  auto k = gemv_rf_kernel<kMode, kNT>;
   static int configured_smem[64];  // per device (0 = not yet)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -33,11 +34,13 @@ cudaError_t run_gemv_rf(const GemvParams& p, const LaunchCfg& cfg, KernelInfo* i
   return launch_kernel(k, C::kThreads, p, cfg);
 }
 
-cudaError_t launch_dense_rf(int nt, const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info) {
-  switch (nt) {
-    case 8: return run_gemv_rf<8>(p, cfg, info);
-    case 16: return run_gemv_rf<16>(p, cfg, info);
-  }
+cudaError_t launch_rf(int mode, int nt, const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info) {
+#define FP4_CASE(M_, NT_) \
+  if (mode == M_ && nt == NT_) return run_gemv_rf<M_, NT_>(p, cfg, info);
+  FP4_CASE(kDenseFp4, 8) FP4_CASE(kDenseFp4, 16)
+  FP4_CASE(kMoeGateUp, 8) FP4_CASE(kMoeGateUp, 16)
+  FP4_CASE(kMoeDown, 8) FP4_CASE(kMoeDown, 16)
+#undef FP4_CASE
   return cudaErrorInvalidValue;
 }
 

@@ -214,82 +214,30 @@ __device__ __forceinline__ void set_box(Work& w, int b, int wrow, int srow, int 
   }
 }
 
-// Resolve what this CTA computes (producer lane 0, before the barriers are
-// initialised).  gate_up routed CTAs wait for the previous grid first: their
-// expert ids come from the router.
+// Resolve what this CTA computes (called by all 32 lanes of the producer
+// warp, before the barriers are initialised).  gate_up routed CTAs wait for
+// the previous grid first: their expert ids come from the router.  A routed
+// CTA's chunk is found with warp-wide ballots over the ids, so resolving
+// costs O(P / 32) loads per lane however many pairs there are.
 template <int kMode, int kNT>
-__device__ void resolve_work(const GemvParams& p, CtaWork& w, uint32_t split) {
-  w.active = 1;
-  w.shared = 0;
-  w.paired = 0;
-  w.expert = -1;
-  w.sgroup[1] = w.sgroup[2] = -1;
-  w.wrow[1] = w.srow[1] = 0;
+__device__ void resolve_work(const GemvParams& p, CtaWork& w, uint32_t split, int lane) {
   const int tile = blockIdx.x / max(1u, cluster_nctarank());
+  if (lane == 0) {
+    w.active = 1;
+    w.shared = 0;
+    w.paired = 0;
+    w.expert = -1;
+    w.sgroup[1] = w.sgroup[2] = -1;
+    w.wrow[1] = w.srow[1] = 0;
+  }
   if constexpr (kMode == kDenseFp4 || kMode == kDenseBf16) {
-    w.ntok = p.M;  // B row n is token n (activations read by TMA)
-    w.k_begin = static_cast<int>(split) * p.k_split;
-    w.k_end = min(p.K, w.k_begin + p.k_split);
-    w.kbp = p.kbp;
-    const int groups_total = (p.rows_w + 127) / 128;
-    if (p.silu) {
-      w.paired = 1;
-      w.out_base = tile * 64;
-      set_box(w, 0, tile * 64, tile * 64, groups_total);                        // gate rows
-      set_box(w, 1, p.n_half + tile * 64, p.n_half + tile * 64, groups_total);  // up rows
-    } else {
-      w.out_base = tile * 128;
-      set_box(w, 0, tile * 128, tile * 128, groups_total);
-    }
-  } else {
-    // MoE: blockIdx.y < P: routed pair column; else shared-expert token chunk.
-    const int col = blockIdx.y;
-    w.k_begin = 0;
-    if (col < p.P) {
-      // gate_up runs right after the router: its ids are complete only after
-      // the wait.  down_combine reads them early (they are two kernels old).
-      if (kMode == kMoeGateUp) pdl_wait();
-      const int e = __ldg(p.ids + col);
-      if (tile >= p.routed_tiles) { w.active = 0; return; }
-      if (e < 0 || e >= p.E) {
-        raise_error(p.err, FP4_ERR_BADIDX);
-        w.active = 0;
-        return;
-      }
-      // rank of this pair among the pairs routed to e; the first pair of each
-      // chunk of kNT pairs computes the whole chunk.
-      int rank = 0;
-      for (int q = 0; q < col; ++q) rank += (__ldg(p.ids + q) == e);
-      if (rank % kNT != 0) { w.active = 0; return; }
-      int n = 0;
-      for (int q = col; q < p.P && n < kNT; ++q) {
-        if (__ldg(p.ids + q) == e) {
-          w.tok[n] = kMode == kMoeGateUp ? q / p.topk : q;  // x row (token) or act row (pair)
-          w.orow[n] = q;
-          ++n;
-        }
-      }
-      w.ntok = n;
-      for (; n < kNT; ++n) w.tok[n] = w.orow[n] = w.tok[0];
-      w.expert = e;
-      w.k_end = p.K;
+    if (lane == 0) {
+      w.ntok = p.M;  // B row n is token n (activations read by TMA)
+      w.k_begin = static_cast<int>(split) * p.k_split;
+      w.k_end = min(p.K, w.k_begin + p.k_split);
       w.kbp = p.kbp;
-      // 128 consecutive rows of expert e (gate_up: one [up; gate] group)
-      const int r0 = tile * 128;
-      set_box(w, 0, e * p.rows_per_expert + r0, r0, (p.rows_per_expert + 127) / 128);
-      w.out_base = kMode == kMoeGateUp ? tile * 64 : tile * 128;
-      for (int m = 0; m < kNT; ++m) w.xoff[m] = static_cast<long long>(w.tok[m]) * p.ldx;
-    } else {
-      const int chunk = col - p.P;
-      if (tile >= p.shared_tiles) { w.active = 0; return; }
-      w.shared = 1;
-      const int t0 = chunk * kNT;
-      w.ntok = min(kNT, p.M - t0);
-      for (int n = 0; n < kNT; ++n) w.tok[n] = w.orow[n] = t0 + (n < w.ntok ? n : 0);
-      w.k_end = p.K2;
-      w.kbp = p.kbp2;
       const int groups_total = (p.rows_w + 127) / 128;
-      if (kMode == kMoeGateUp) {
+      if (p.silu) {
         w.paired = 1;
         w.out_base = tile * 64;
         set_box(w, 0, tile * 64, tile * 64, groups_total);                        // gate rows
@@ -298,9 +246,87 @@ __device__ void resolve_work(const GemvParams& p, CtaWork& w, uint32_t split) {
         w.out_base = tile * 128;
         set_box(w, 0, tile * 128, tile * 128, groups_total);
       }
-      for (int m = 0; m < kNT; ++m) w.xoff[m] = static_cast<long long>(w.tok[m]) * p.ldx2;
+    }
+  } else {
+    // MoE: blockIdx.y < P: routed pair column; else shared-expert token chunk.
+    const int col = blockIdx.y;
+    if (lane == 0) w.k_begin = 0;
+    if (col < p.P) {
+      // gate_up runs right after the router: its ids are complete only after
+      // the wait.  down_combine reads them early (they are two kernels old).
+      if (kMode == kMoeGateUp) pdl_wait();
+      const int e = __ldg(p.ids + col);
+      bool live = tile < p.routed_tiles;
+      if (live && (e < 0 || e >= p.E)) {
+        if (lane == 0) raise_error(p.err, FP4_ERR_BADIDX);
+        live = false;
+      }
+      // rank of this pair among the pairs routed to e; the first pair of each
+      // chunk of kNT pairs computes the whole chunk.
+      int cnt = 0;
+      if (live)
+        for (int q = lane; q < col; q += 32) cnt += (__ldg(p.ids + q) == e);
+      const int rank = __reduce_add_sync(0xFFFFFFFFu, cnt);
+      live = live && rank % kNT == 0;
+      if (!live) {
+        if (lane == 0) w.active = 0;
+        __syncwarp();
+        return;
+      }
+      // the chunk: the first kNT pairs q >= col routed to e, in order
+      int n = 0;
+      for (int q0 = col; q0 < p.P && n < kNT; q0 += 32) {
+        const int q = q0 + lane;
+        const bool m = q < p.P && __ldg(p.ids + q) == e;
+        const unsigned bal = __ballot_sync(0xFFFFFFFFu, m);
+        const int pos = n + __popc(bal & ((1u << lane) - 1u));
+        if (m && pos < kNT) {
+          w.tok[pos] = kMode == kMoeGateUp ? q / p.topk : q;  // x row (token) or act row (pair)
+          w.orow[pos] = q;
+        }
+        n += __popc(bal);
+      }
+      n = min(n, kNT);
+      __syncwarp();
+      if (lane == 0) {
+        w.ntok = n;
+        for (int i = n; i < kNT; ++i) w.tok[i] = w.orow[i] = w.tok[0];
+        w.expert = e;
+        w.k_end = p.K;
+        w.kbp = p.kbp;
+        // 128 consecutive rows of expert e (gate_up: one [up; gate] group)
+        const int r0 = tile * 128;
+        set_box(w, 0, e * p.rows_per_expert + r0, r0, (p.rows_per_expert + 127) / 128);
+        w.out_base = kMode == kMoeGateUp ? tile * 64 : tile * 128;
+      }
+      __syncwarp();
+      for (int m2 = lane; m2 < kNT; m2 += 32) w.xoff[m2] = static_cast<long long>(w.tok[m2]) * p.ldx;
+    } else if (lane == 0) {
+      const int chunk = col - p.P;
+      if (tile >= p.shared_tiles) {
+        w.active = 0;
+      } else {
+        w.shared = 1;
+        const int t0 = chunk * kNT;
+        w.ntok = min(kNT, p.M - t0);
+        for (int n = 0; n < kNT; ++n) w.tok[n] = w.orow[n] = t0 + (n < w.ntok ? n : 0);
+        w.k_end = p.K2;
+        w.kbp = p.kbp2;
+        const int groups_total = (p.rows_w + 127) / 128;
+        if (kMode == kMoeGateUp) {
+          w.paired = 1;
+          w.out_base = tile * 64;
+          set_box(w, 0, tile * 64, tile * 64, groups_total);                        // gate rows
+          set_box(w, 1, p.n_half + tile * 64, p.n_half + tile * 64, groups_total);  // up rows
+        } else {
+          w.out_base = tile * 128;
+          set_box(w, 0, tile * 128, tile * 128, groups_total);
+        }
+        for (int m = 0; m < kNT; ++m) w.xoff[m] = static_cast<long long>(w.tok[m]) * p.ldx2;
+      }
     }
   }
+  __syncwarp();
 }
 
 template <int kMode, int kNT>
@@ -377,6 +403,7 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
     }
   };
 
+  if (warp == C::kProducerWarp) resolve_work<kMode, kNT>(p, s_work, rank, lane);
   if (warp == C::kProducerWarp && lane == 0) {
     prefetch_tensormap(&p.tm_w);
     if constexpr (kMode == kMoeGateUp || kMode == kMoeDown) prefetch_tensormap(&p.tm_w2);
@@ -384,7 +411,6 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
     s_abort = 0;
     s_last = 0;
     CtaWork& wk = s_work;
-    resolve_work<kMode, kNT>(p, wk, rank);
     const int nst = stage_count(wk);
     const int nslices = wk.active ? (wk.k_end - wk.k_begin) / kSubK : 0;
     for (int i = 0; i < nstages; ++i) {

@@ -71,7 +71,9 @@ struct RfCfg {
   // the cheaper dequantization beyond a few tokens.
   static constexpr int kF16MaxM = 4;
   static constexpr bool kHasF16 = kNT == 8;  // only the 8-token tile serves M <= kF16MaxM
-  static constexpr int kInboxBytes = kNT * 136 * 4;
+  // The split-K inbox, then (MoE modes) the CTA's resolved work.
+  static constexpr int kInboxFloats = kNT * 136;
+  static constexpr int kInboxBytes = kInboxFloats * 4 + static_cast<int>((sizeof(CtaWork) + 15) / 16 * 16);
   static_assert(kNT == 8 || kNT == 16, "token tile");
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
 };
@@ -102,16 +104,36 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Dense CTA work: K range and the weight boxes (tensor-map rows, scale rows
-// and groups), as resolve_work computes them for the dense modes.
-struct DenseWork {
-  int paired, k_begin, k_end, kbp, out_base;
+// The per-thread copy of a CTA's work: K range and the weight boxes
+// (tensor-map rows, scale rows and groups), as resolve_work computes them.
+struct RfWork {
+  int paired, shared, expert, k_begin, k_end, kbp, out_base;
   int wrow[2], srow[2], sgroup[3];
 };
 
-template <int kNT>
+__device__ __forceinline__ void copy_work(const CtaWork& m, RfWork& w) {
+  w.paired = m.paired;
+  w.shared = m.shared;
+  w.expert = m.expert;
+  w.k_begin = m.k_begin;
+  w.k_end = m.k_end;
+  w.kbp = m.kbp;
+  w.out_base = m.out_base;
+  w.wrow[0] = m.wrow[0];
+  w.wrow[1] = m.wrow[1];
+  w.srow[0] = m.srow[0];
+  w.srow[1] = m.srow[1];
+  w.sgroup[0] = m.sgroup[0];
+  w.sgroup[1] = m.sgroup[1];
+  w.sgroup[2] = m.sgroup[2];
+}
+
+// kMode: kDenseFp4 (nvfp4_gemv), kMoeGateUp or kMoeDown (the same modes and
+// epilogues as the tcgen05 kernel, for chunks of at most 16 tokens / pairs).
+template <int kMode, int kNT>
 __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const __grid_constant__ GemvParams p) {
   using C = RfCfg<kNT>;
+  constexpr bool kDense = kMode == kDenseFp4;
   constexpr int kEpiThreads = C::kConsumerWarps * 32;
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -123,6 +145,9 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
   __shared__ __align__(8) uint64_t bar_inbox;
   __shared__ volatile int s_abort;
   __shared__ int s_xbad[kMaxStages];  // last stage (of this slot) whose activations are not all exact f16
+  __shared__ int s_last;
+  // MoE: the CTA's work, resolved by the producer before the weight stream starts
+  CtaWork* const mwork = reinterpret_cast<CtaWork*>(smem_raw + (inbox - smem_u32(smem_raw)) + C::kInboxFloats * 4);
 
   const int tid = threadIdx.x;
   const int warp = tid / 32;
@@ -131,9 +156,11 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
   const uint32_t rank = S > 1 ? cluster_ctarank() : 0;
   const int nstages = p.nstages;
 
-  // ---- what this CTA computes (every thread derives it) ----
-  DenseWork wk;
-  {
+  // ---- what this CTA computes (dense: every thread derives it) ----
+  RfWork wk;
+  wk.shared = 0;
+  wk.expert = -1;
+  if constexpr (kDense) {
     const int tile = blockIdx.x / max(1u, S);
     wk.k_begin = static_cast<int>(rank) * p.k_split;
     wk.k_end = min(p.K, wk.k_begin + p.k_split);
@@ -152,13 +179,6 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
       set_box(wk, 0, tile * 128, tile * 128, groups_total);
     }
   }
-  const int nst = (wk.k_end - wk.k_begin + C::kStageK - 1) / C::kStageK;
-  const int unit = wk.paired ? 64 : 128;
-  const int R = (unit + static_cast<int>(S) - 1) / static_cast<int>(S);
-  const int f_lo = static_cast<int>(rank) * R;
-  const int f_hi = min(unit, f_lo + R);
-  const int mine = max(0, f_hi - f_lo) * (128 / unit);
-
   const uint64_t pol_w = policy_evict_first();
   const uint64_t pol_x = policy_evict_last();
   auto issue_weights = [&](int s) {
@@ -167,40 +187,79 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
     const uint32_t fb = smem_u32(&bar_full[slot]);
     const int k0 = wk.k_begin + s * C::kStageK;
     const int nchunks = min(C::kStageK, wk.k_end - k0) / kSubK;
+    const CUtensorMap* tmw = wk.shared ? &p.tm_w2 : &p.tm_w;
+    const uint8_t* sfb =
+        wk.shared ? p.sf2 : p.sf + (wk.expert >= 0 ? static_cast<size_t>(wk.expert) * p.sf_expert_bytes : 0);
     uint32_t bytes = C::kWTileBytes;
 #pragma unroll
     for (int g = 0; g < 3; ++g) bytes += (wk.sgroup[g] >= 0 ? nchunks * 512 : 0);
     asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(fb), "r"(bytes) : "memory");
-    tma_load_2d(st, &p.tm_w, k0 / 2, wk.wrow[0], fb, pol_w);
-    if (wk.paired) tma_load_2d(st + C::kWTileBytes / 2, &p.tm_w, k0 / 2, wk.wrow[1], fb, pol_w);
+    tma_load_2d(st, tmw, k0 / 2, wk.wrow[0], fb, pol_w);
+    if (wk.paired) tma_load_2d(st + C::kWTileBytes / 2, tmw, k0 / 2, wk.wrow[1], fb, pol_w);
 #pragma unroll
     for (int g = 0; g < 3; ++g) {
       if (wk.sgroup[g] < 0) continue;
       const size_t chunk = static_cast<size_t>(wk.sgroup[g]) * (wk.kbp / 4) + k0 / 64;
-      bulk_load(st + C::kWTileBytes + g * 2048, p.sf + chunk * 512, nchunks * 512, fb, pol_w);
+      bulk_load(st + C::kWTileBytes + g * 2048, sfb + chunk * 512, nchunks * 512, fb, pol_w);
     }
   };
+  // Output rows are reduced across cluster ranks per feature unit: a tile
+  // whose feature o combines rows o and o + 64 (paired gate/up boxes, routed
+  // [up; gate] groups) has 64-row units, any other tile 128-row units.
+  auto unit_of = [&]() { return (wk.paired || (kMode == kMoeGateUp && !wk.shared)) ? 64 : 128; };
+  auto stages_of = [&](bool act) { return act ? (wk.k_end - wk.k_begin + C::kStageK - 1) / C::kStageK : 0; };
 
   // ------------------------------------------------------------------ prologue
-  const int pre = min(nst, nstages);
+  // The producer (MoE: after resolving the work -- gate_up's routed CTAs wait
+  // for the router there) initialises the barriers and starts the weights.
+  if constexpr (!kDense) {
+    if (warp == C::kProducerWarp) resolve_work<kMode, kNT>(p, *mwork, 0, lane);
+  }
   if (warp == C::kProducerWarp && lane == 0) {
     prefetch_tensormap(&p.tm_w);
-    prefetch_tensormap(&p.tm_x);
+    if constexpr (kDense) prefetch_tensormap(&p.tm_x);
+    else prefetch_tensormap(&p.tm_w2);
     s_abort = 0;
+    s_last = 0;
+    bool act = true;
+    if constexpr (!kDense) {
+      copy_work(*mwork, wk);
+      act = mwork->active != 0;
+    }
     for (int i = 0; i < nstages; ++i) {
-      mbar_init(smem_u32(&bar_full[i]), 1);
+      mbar_init(smem_u32(&bar_full[i]), kDense ? 1 : 33);
       mbar_init(smem_u32(&bar_empty[i]), C::kConsumerWarps);
       mbar_init(smem_u32(&bar_xready[i]), 1);
       s_xbad[i] = -1;
     }
     mbar_init(smem_u32(&bar_inbox), 1);
-    if (S > 1) mbar_arrive_expect_tx(smem_u32(&bar_inbox), S * kNT * mine * 4);
+    if (S > 1) {
+      const int u = unit_of(), r = (u + static_cast<int>(S) - 1) / static_cast<int>(S);
+      const int mine0 = max(0, min(r, u - static_cast<int>(rank) * r)) * (128 / u);
+      mbar_arrive_expect_tx(smem_u32(&bar_inbox), S * kNT * mine0 * 4);
+    }
     mbar_fence_init();
-    for (int s = 0; s < pre; ++s) issue_weights(s);
+    const int pre0 = min(stages_of(act), nstages);
+    for (int s = 0; s < pre0; ++s) issue_weights(s);
   }
   __syncthreads();
   if (S > 1) cluster_arrive_relaxed();  // paired with a wait before the first remote access
   if (tid == 0) pdl_launch_dependents();
+  bool active = true;
+  int ntok = p.M;  // valid B rows (tokens, or pairs of the expert chunk)
+  if constexpr (!kDense) {
+    copy_work(*mwork, wk);
+    active = mwork->active != 0;
+    ntok = active ? mwork->ntok : 0;
+  }
+  const int nst = stages_of(active);
+  const int pre = min(nst, nstages);
+  const int unit = unit_of();
+  const int R = (unit + static_cast<int>(S) - 1) / static_cast<int>(S);
+  const int f_lo = static_cast<int>(rank) * R;
+  const int f_hi = min(unit, f_lo + R);
+  const int mine = max(0, f_hi - f_lo) * (128 / unit);
+  const bool f16route = C::kHasF16 && ntok <= C::kF16MaxM;
 
   float acc[C::kChains][C::kTiles][4];  // main route's stages
   float accb[C::kHasF16 ? C::kTiles : 1][4];  // f16 route: fallback stages (bf16, products times 2^-kShift)
@@ -222,25 +281,56 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
   if (warp == C::kProducerWarp) {
     // ------------------------------------------------------------------ producer
     pdl_wait();
-    if (lane == 0) {
+    if constexpr (kDense) {
+      if (lane == 0) {
+        for (int s = 0; s < nst && !s_abort; ++s) {
+          const int slot = s % nstages;
+          const uint32_t st = ring + slot * C::kStageBytes;
+          const uint32_t fb = smem_u32(&bar_full[slot]);
+          if (s >= pre) {
+            if (!mbar_wait(smem_u32(&bar_empty[slot]), ((s / nstages) & 1) ^ 1, p.err)) { s_abort = 1; break; }
+            issue_weights(s);
+          }
+          const int k0 = wk.k_begin + s * C::kStageK;
+          mbar_arrive_expect_tx(fb, C::kXBytes);
+          tma_load_3d(st + C::kXOff, &p.tm_x, 0, 0, k0 / kSubK, fb, pol_x);
+        }
+      }
+    } else {
+      // Gathered activations: lane c copies 16-byte chunk c (of 32) of every
+      // B row of the stage into the 128-byte-swizzled atoms (rows past the
+      // chunk's pairs / tokens are zero-filled).
+      const uint16_t* xb = wk.shared ? p.x2 : p.x;
+      const int u = lane / 8, cc = lane % 8;
       for (int s = 0; s < nst && !s_abort; ++s) {
         const int slot = s % nstages;
         const uint32_t st = ring + slot * C::kStageBytes;
         const uint32_t fb = smem_u32(&bar_full[slot]);
         if (s >= pre) {
-          if (!mbar_wait(smem_u32(&bar_empty[slot]), ((s / nstages) & 1) ^ 1, p.err)) { s_abort = 1; break; }
-          issue_weights(s);
+          const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bar_empty[slot]), ((s / nstages) & 1) ^ 1, p.err));
+          if (!ok) { s_abort = 1; break; }
+          if (lane == 0) issue_weights(s);
+          __syncwarp();
         }
         const int k0 = wk.k_begin + s * C::kStageK;
-        mbar_arrive_expect_tx(fb, C::kXBytes);
-        tma_load_3d(st + C::kXOff, &p.tm_x, 0, 0, k0 / kSubK, fb, pol_x);
+        const bool kok = lane * 8 < min(C::kStageK, wk.k_end - k0);
+        const uint16_t* src_k = xb + k0 + lane * 8;
+        const uint32_t dst0 = st + C::kXOff + u * (kNT * 128);
+#pragma unroll
+        for (int n = 0; n < kNT; ++n) {
+          const bool valid = kok && n < ntok;
+          const uint32_t dst = dst0 + (n / 8) * 1024 + (n % 8) * 128 + ((cc ^ (n % 8)) * 16);
+          cp_async16(dst, valid ? src_k + mwork->xoff[n] : xb, valid ? 16u : 0u);
+        }
+        cp_async_arrive_noinc(fb);
+        if (lane == 0) mbar_arrive(fb);
       }
     }
   } else if (warp == C::kConverterWarp) {
     // ------------------------------------------------------------------ converter
-    if (C::kHasF16 && p.M <= C::kF16MaxM)
-    // Rows < M of each stage's activations to f16 in place (16-byte chunks);
-    // rows >= M and K past the end are zeros from the TMA fill, the same bits
+    if (C::kHasF16 && ntok <= C::kF16MaxM)
+    // Rows < ntok of each stage's activations to f16 in place (16-byte
+    // chunks); the other rows and K past the end are zero-filled, the same bits
     // in f16.  A stage with any inexact value is flagged for the bf16 route.
     for (int s = 0; s < nst; ++s) {
       const int slot = s % nstages;
@@ -253,7 +343,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
       }
       const int kvalid = min(C::kStageK, wk.k_end - wk.k_begin - s * C::kStageK);
       bool exact = true;
-      for (int id = lane; id < p.M * 32; id += 32) {
+      for (int id = lane; id < ntok * 32; id += 32) {
         const int n = id / 32, q = id % 32;
         if (8 * q >= kvalid) continue;
         const uint32_t a = st + C::kXOff + (q / 8) * (kNT * 128) + (n / 8) * 1024 + (n % 8) * 128 +
@@ -286,7 +376,14 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
       return C::kWTileBytes + gslot * 2048 + (r % 32) * 16 + ((r % 128) / 32) * 4;
     };
     const uint32_t sf0 = sf_off(row0), sf1 = sf_off(row1);
-    const bool f16route = C::kHasF16 && p.M <= C::kF16MaxM;
+    // global activation rows of this thread's B rows (f16 route's fallback)
+    const uint16_t* xrow[C::kTiles];
+#pragma unroll
+    for (int t = 0; t < C::kTiles; ++t) {
+      const int n = 8 * t + g;
+      if constexpr (kDense) xrow[t] = n < ntok ? p.x + static_cast<int64_t>(n) * p.ldx : nullptr;
+      else xrow[t] = n < ntok ? (wk.shared ? p.x2 : p.x) + mwork->xoff[n] : nullptr;
+    }
     // One 128-K half of a stage: chunk j = 4 h + c of both rows.  `cvalid`
     // false (a chunk past the end of a ragged last stage) gives zero A
     // registers: that chunk's scales were not copied and may hold anything.
@@ -383,10 +480,8 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
         const int kk = 32 * j + 8 * w;
 #pragma unroll
         for (int t = 0; t < C::kTiles; ++t) {
-          const int n = 8 * t + g;
           uint4 xv = make_uint4(0u, 0u, 0u, 0u);
-          if (cvalid && n < p.M)
-            xv = perm_x8(__ldg(reinterpret_cast<const uint4*>(p.x + static_cast<int64_t>(n) * p.ldx + k0 + kk)));
+          if (cvalid && xrow[t] != nullptr) xv = perm_x8(__ldg(reinterpret_cast<const uint4*>(xrow[t] + k0 + kk)));
           mma_bf16_16816(accb[C::kHasF16 ? t : 0], r0[0], r1[0], r0[1], r1[1], xv.x, xv.y);
           mma_bf16_16816(accb[C::kHasF16 ? t : 0], r0[2], r1[2], r0[3], r1[3], xv.z, xv.w);
         }
@@ -473,7 +568,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
           for (int q = 0; q < C::kChains; ++q) a16 += acc[q][t][2 * hr + e];
           // acc holds the main route's products (exact on the f16 route,
           // times 2^-kShift on the bf16 route); accb the f16 route's fallback
-          if (!C::kHasF16 || p.M > C::kF16MaxM) a16 *= post;
+          if (!f16route) a16 *= post;
           if constexpr (C::kHasF16) a16 += accb[t][2 * hr + e] * post;
           const float v = go ? a16 : 0.0f;
           const uint32_t off = n * rows_owner * 4;
@@ -493,24 +588,101 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
       return a;
     };
     const int nf = f_hi - f_lo;
-    if (!s_abort && nf > 0) {
+    if (active && !s_abort && nf > 0) {
       pdl_wait();
-      const float gs = __ldg(p.gs);
-      if (!wk.paired) {
-        for (int it = tid; it < nf * p.M; it += kEpiThreads) {
+      if (unit == 128) {
+        // plain tiles: feature = tile row (dense out, or the down y scratch)
+        float sc = 1.0f;
+        uint16_t* dst = p.out;
+        int64_t ld = p.ldo;
+        int nfeat = p.n_out;
+        if constexpr (kDense) {
+          sc = __ldg(p.gs);
+        } else {
+          sc = wk.shared ? __ldg(p.gs) : __ldg(p.alpha + wk.expert);
+          if (wk.shared) {
+            dst = p.out2;
+            ld = p.ldo2;
+            nfeat = p.shared_n_out;
+          }
+        }
+        for (int it = tid; it < nf * ntok; it += kEpiThreads) {
           const int n = it / nf, lr = it % nf;
           const int o = wk.out_base + f_lo + lr;
-          if (o >= p.n_out) continue;
-          p.out[static_cast<int64_t>(n) * p.ldo + o] = f32_to_bf16_rn(partial(n, lr) * gs);
+          if (o >= nfeat) continue;
+          const int64_t orow = kDense ? n : mwork->orow[n];
+          dst[orow * ld + o] = f32_to_bf16_rn(partial(n, lr) * sc);
         }
-      } else {
-        for (int it = tid; it < nf * p.M; it += kEpiThreads) {
+      } else if (kMode == kMoeGateUp && !wk.shared) {
+        // routed [up; gate] group: feature o = up row o, gate row o + 64
+        const float al = __ldg(p.alpha + wk.expert);
+        for (int it = tid; it < nf * ntok; it += kEpiThreads) {
           const int n = it / nf, lr = it % nf;
           const int feat = wk.out_base + f_lo + lr;
           if (feat >= p.n_out) continue;
+          const float uu = partial(n, lr) * al;
+          const float gt = partial(n, lr + nf) * al;
+          p.out[static_cast<int64_t>(mwork->orow[n]) * p.ldo + feat] = f32_to_bf16_rn(silu_fast(gt) * uu);
+        }
+      } else {
+        // paired tiles: feature o = gate row o, up row o + 64
+        const float gs = __ldg(p.gs);
+        uint16_t* dst = kDense ? p.out : p.out2;
+        const int64_t ld = kDense ? p.ldo : p.ldo2;
+        const int nfeat = kDense ? p.n_out : p.shared_n_out;
+        for (int it = tid; it < nf * ntok; it += kEpiThreads) {
+          const int n = it / nf, lr = it % nf;
+          const int feat = wk.out_base + f_lo + lr;
+          if (feat >= nfeat) continue;
           const float G = bf16_to_f32(f32_to_bf16_rn(partial(n, lr) * gs));
           const float U = bf16_to_f32(f32_to_bf16_rn(partial(n, lr + nf) * gs));
-          p.out[static_cast<int64_t>(n) * p.ldo + feat] = f32_to_bf16_rn(silu_exact(G) * U);
+          const int64_t orow = kDense ? n : mwork->orow[n];
+          dst[orow * ld + feat] = f32_to_bf16_rn(silu_exact(G) * U);
+        }
+      }
+    }
+    if constexpr (kMode == kMoeDown) {
+      // Every CTA of a row-tile column arrives once (tagged with this call's
+      // epoch, so the scratch needs no zero-fill); the last one combines:
+      // out[t] = bf16(bf16(sum_j tw[t, j] * y[t, j]) + y_shared[t]).
+      epi_sync<kEpiThreads>();
+      if (tid == 0) {
+        __threadfence();
+        unsigned long long* ctr = p.counters + blockIdx.x;
+        const unsigned long long tag = static_cast<unsigned long long>(p.epoch) << 32;
+        unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(ctr), next;
+        for (;;) {
+          next = ((old & 0xFFFFFFFF00000000ull) == tag) ? old + 1 : tag + 1;
+          const unsigned long long seen = atomicCAS(ctr, old, next);
+          if (seen == old) break;
+          old = seen;
+        }
+        s_last = static_cast<uint32_t>(next) == gridDim.y;
+        if (s_last) atomicExch(ctr, 0ull);
+        __threadfence();
+      }
+      epi_sync<kEpiThreads>();
+      if (s_last) {
+        pdl_wait();
+        const int h0 = blockIdx.x * 128;
+        for (int it = tid; it < 128 * p.M; it += kEpiThreads) {
+          const int t = it / 128, h = h0 + it % 128;
+          if (h >= p.n_out) continue;
+          bool ids_ok = true;  // a token with an out-of-range id is left unwritten
+          for (int j = 0; j < p.topk; ++j) {
+            const int e = __ldg(p.ids + t * p.topk + j);
+            ids_ok = ids_ok && e >= 0 && e < p.E;
+          }
+          if (!ids_ok) continue;
+          float a = 0.0f;
+          for (int j = 0; j < p.topk; ++j) {
+            const float wj = __ldg(p.tw + t * p.topk + j);
+            const float y = bf16_to_f32(__ldcg(p.out + static_cast<int64_t>(t * p.topk + j) * p.ldo + h));
+            a = fmaf(wj, y, a);
+          }
+          const float sb = bf16_to_f32(f32_to_bf16_rn(a));
+          const float ysh = bf16_to_f32(__ldcg(p.out2 + static_cast<int64_t>(t) * p.ldo2 + h));
+          p.out3[static_cast<int64_t>(t) * p.n_out + h] = f32_to_bf16_rn(sb + ysh);
         }
       }
     }

@@ -28,8 +28,9 @@ struct KernelInfo {
 // Per (mode, kNT) kernel: static facts (info != nullptr) or a launch.  Each
 // returns cudaErrorInvalidValue for a combination that is not instantiated.
 cudaError_t launch_dense_fp4(int nt, const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info);
-// Register-fed dense NVFP4 GEMV for M <= 16 (k_gemv_rf.cuh), nt = 8 or 16.
-cudaError_t launch_dense_rf(int nt, const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info);
+// Register-fed NVFP4 kernel (k_gemv_rf.cuh): mode kDenseFp4, kMoeGateUp or
+// kMoeDown, nt = 8 or 16.
+cudaError_t launch_rf(int mode, int nt, const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info);
 cudaError_t launch_dense_bf16(int nt, const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info);
 cudaError_t launch_moe(int mode, int nt, const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info);
 cudaError_t launch_dequantize_rows(const uint8_t* w, const uint8_t* sf, void* out, int rows, int K,
