@@ -93,6 +93,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
   }
 }
 
+// Bounded wait for roles off the critical path (the producer waiting for a
+// free slot, the converter for data): between tests the thread sleeps, so a
+// waiting warp does not take issue slots from the warps that compute.
+__device__ __forceinline__ bool mbar_wait_sleepy(uint32_t bar, uint32_t parity, uint32_t* err, uint32_t sleep_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (;;) {
+    __nanosleep(sleep_ns);
+    if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer() - t0 > FP4GEMV_WAIT_NS) {
+      raise_error(err, FP4_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Explicit shared-memory accesses (32-bit shared-window addresses)
 // ---------------------------------------------------------------------------

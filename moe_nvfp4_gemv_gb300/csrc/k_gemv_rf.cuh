@@ -288,7 +288,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
           const uint32_t st = ring + slot * C::kStageBytes;
           const uint32_t fb = smem_u32(&bar_full[slot]);
           if (s >= pre) {
-            if (!mbar_wait(smem_u32(&bar_empty[slot]), ((s / nstages) & 1) ^ 1, p.err)) { s_abort = 1; break; }
+            if (!mbar_wait_sleepy(smem_u32(&bar_empty[slot]), ((s / nstages) & 1) ^ 1, p.err, 64)) { s_abort = 1; break; }
             issue_weights(s);
           }
           const int k0 = wk.k_begin + s * C::kStageK;
@@ -307,7 +307,8 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
         const uint32_t st = ring + slot * C::kStageBytes;
         const uint32_t fb = smem_u32(&bar_full[slot]);
         if (s >= pre) {
-          const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bar_empty[slot]), ((s / nstages) & 1) ^ 1, p.err));
+          const bool ok =
+              __all_sync(0xFFFFFFFFu, mbar_wait_sleepy(smem_u32(&bar_empty[slot]), ((s / nstages) & 1) ^ 1, p.err, 64));
           if (!ok) { s_abort = 1; break; }
           if (lane == 0) issue_weights(s);
           __syncwarp();
@@ -335,8 +336,8 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
     for (int s = 0; s < nst; ++s) {
       const int slot = s % nstages;
       const uint32_t st = ring + slot * C::kStageBytes;
-      const bool ok =
-          __all_sync(0xFFFFFFFFu, !s_abort && mbar_wait(smem_u32(&bar_full[slot]), (s / nstages) & 1, p.err));
+      const bool ok = __all_sync(
+          0xFFFFFFFFu, !s_abort && mbar_wait_sleepy(smem_u32(&bar_full[slot]), (s / nstages) & 1, p.err, 32));
       if (!ok) {
         s_abort = 1;
         break;
