@@ -58,7 +58,8 @@ constexpr int kStageK4 = 256;   // K per ring stage, NVFP4 weights (128 B per ro
 constexpr int kStageK16 = 64;   // K per ring stage, bf16 weights (128 B per row)
 constexpr int kMaxNT = 128;
 constexpr int kMaxWG = 2;
-constexpr int kMaxSlots = 4;
+constexpr int kMaxSlots = 6;
+constexpr int kSliceK = 128;    // K per tensor-memory A slot (8 MMAs of K = 16 per commit)
 
 struct GemvParams {
   CUtensorMap tm_w;    // weights read by routed / dense CTAs
@@ -128,21 +129,23 @@ template <int kMode, int kNT>
 struct Cfg {
   static constexpr bool kFp4 = kMode != kDenseBf16;
   static constexpr int kW = kFp4 ? 2 : 1;  // worker warpgroups
-  static constexpr int kThreads = kW * 128 + 32;
+  static constexpr int kThreads = kW * 128 + 64;
   static constexpr int kProducerWarp = 4 * kW;
+  static constexpr int kMmaWarp = 4 * kW + 1;
   static constexpr int kStageK = kFp4 ? kStageK4 : kStageK16;
-  static constexpr int kSlicesPerStage = kStageK / kSubK;  // 4 (fp4) or 1 (bf16)
+  static constexpr int kSlicesPerStage = kFp4 ? kStageK / kSliceK : 1;  // 2 (fp4) or 1 (bf16)
   static constexpr int kWTileBytes = 128 * 128;
   static constexpr int kSfTileBytes = kFp4 ? 3 * 4 * 512 : 0;  // three 128-row scale groups x 4 chunks
   static constexpr int kXBytes = kNT * kStageK * 2;
   static constexpr int kXOff = kWTileBytes + kSfTileBytes;
   static constexpr int kStageBytes = kXOff + kXBytes;
-  // Tensor memory: one fp32 accumulator (kNT columns) per warpgroup, then
-  // kSlots A slots (32 columns = 64 bf16 K) per warpgroup.  Sized to 256
-  // columns (two CTAs per SM) up to kNT = 64.
-  static constexpr int kAccCols = kW * kNT;
-  static constexpr int kSlots = !kFp4 ? 0 : kNT <= 32 ? 3 : kNT <= 64 ? 2 : 4;
-  static constexpr int kTmemCols = pow2_at_least(kAccCols + kW * kSlots * 32);
+  // Tensor memory: one fp32 accumulator (kNT columns), then a ring of kSlots
+  // A slots (64 columns = 128 bf16 K each) shared by the warpgroups in slice
+  // order.  256 columns (two CTAs per SM) up to kNT = 64.
+  static constexpr int kAccCols = kNT;
+  static constexpr int kSlotCols = kSliceK / 2;
+  static constexpr int kSlots = !kFp4 ? 0 : kNT <= 64 ? 3 : 6;
+  static constexpr int kTmemCols = pow2_at_least(kAccCols + kSlots * kSlotCols);
   static constexpr int kRedBytes = kNT * 128 * 4;
   // Dense modes read contiguous activation rows with TMA; the MoE modes
   // gather rows by token / pair with cp.async from the producer lanes.
@@ -176,18 +179,6 @@ template <int kThreadsEpi>
 __device__ __forceinline__ void epi_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kThreadsEpi) : "memory");
 }
-// Warpgroup barrier that also ORs a flag over the warpgroup's threads (the
-// result is the same in all 128 threads).
-template <int kId>
-__device__ __forceinline__ bool bar_red_or(bool v) {
-  uint32_t r;
-  asm volatile("{ .reg .pred p, q; setp.ne.u32 q, %1, 0; bar.red.or.pred p, %2, 128, q; selp.u32 %0, 1, 0, p; }"
-               : "=r"(r)
-               : "r"(static_cast<uint32_t>(v)), "n"(kId)
-               : "memory");
-  return r != 0;
-}
-__device__ __forceinline__ bool wg_sync_or(int w, bool v) { return w == 0 ? bar_red_or<2>(v) : bar_red_or<3>(v); }
 
 // Rows of a tile are reduced across cluster ranks per feature unit: a tile
 // whose feature o combines rows o and o + 64 (paired gate/up boxes, routed
@@ -345,7 +336,8 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
   const uint32_t inbox = ring + p.nstages * C::kStageBytes;
   __shared__ __align__(8) uint64_t bar_full[kMaxStages];
   __shared__ __align__(8) uint64_t bar_empty[kMaxStages];
-  __shared__ __align__(8) uint64_t bar_aempty[kMaxWG * kMaxSlots];
+  __shared__ __align__(8) uint64_t bar_afull[kMaxSlots];   // slot dequantized (4 warps of its warpgroup)
+  __shared__ __align__(8) uint64_t bar_aempty[kMaxSlots];  // slot's MMAs done (MMA-thread commit)
   __shared__ __align__(8) uint64_t bar_accum;
   __shared__ __align__(8) uint64_t bar_inbox;
   __shared__ __align__(8) uint64_t bar_red_ready;
@@ -412,14 +404,15 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
     s_last = 0;
     CtaWork& wk = s_work;
     const int nst = stage_count(wk);
-    const int nslices = wk.active ? (wk.k_end - wk.k_begin) / kSubK : 0;
     for (int i = 0; i < nstages; ++i) {
       mbar_init(smem_u32(&bar_full[i]), C::kFullCount);
-      // released by the last MMA commit of every warpgroup with a slice in the stage
-      mbar_init(smem_u32(&bar_empty[i]), kW);
+      mbar_init(smem_u32(&bar_empty[i]), 1);  // the MMA thread's commit after the stage's last slice
     }
-    for (int i = 0; i < kW * kNS; ++i) mbar_init(smem_u32(&bar_aempty[i]), 1);
-    mbar_init(smem_u32(&bar_accum), max(1, min(kW, nslices)));
+    for (int i = 0; i < kNS; ++i) {
+      mbar_init(smem_u32(&bar_afull[i]), 4);  // one arrival per warp of the slice's warpgroup
+      mbar_init(smem_u32(&bar_aempty[i]), 1);
+    }
+    mbar_init(smem_u32(&bar_accum), 1);
     mbar_init(smem_u32(&bar_inbox), 1);
     mbar_init(smem_u32(&bar_red_ready), S);
     mbar_init(smem_u32(&bar_red_done), S);
@@ -453,7 +446,7 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
   const bool active = wk.active != 0;
   const uint32_t tmem = s_tmem;
   const int nst = stage_count(wk);
-  const int nslices = active ? (wk.k_end - wk.k_begin) / kSubK : 0;
+  const int nslices = active ? (wk.k_end - wk.k_begin + kSliceK - 1) / kSliceK : 0;  // 128-K slices (NVFP4)
   // Output rows are reduced per feature unit: a paired tile's feature o lives
   // in rows o and o + 64, so those rows go to the same cluster rank.
   const int unit = feature_unit<kMode>(wk);
@@ -479,7 +472,7 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
           const uint32_t st = ring + slot * C::kStageBytes;
           const uint32_t fb = smem_u32(&bar_full[slot]);
           if (s >= pre) {
-            if (!mbar_wait(smem_u32(&bar_empty[slot]), ((s / nstages) & 1) ^ 1, p.err)) { s_abort = 1; break; }
+            if (!mbar_wait_sleepy(smem_u32(&bar_empty[slot]), ((s / nstages) & 1) ^ 1, p.err, 64)) { s_abort = 1; break; }
             issue_weights(wk, s);
           }
           const int k0 = wk.k_begin + s * C::kStageK;
@@ -501,7 +494,7 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
         const uint32_t st = ring + slot * C::kStageBytes;
         const uint32_t fb = smem_u32(&bar_full[slot]);
         if (s >= pre) {
-          if (!mbar_wait(smem_u32(&bar_empty[slot]), ((s / nstages) & 1) ^ 1, p.err)) { s_abort = 1; break; }
+          if (!mbar_wait_sleepy(smem_u32(&bar_empty[slot]), ((s / nstages) & 1) ^ 1, p.err, 64)) { s_abort = 1; break; }
           if (lane == 0) issue_weights(wk, s);
           __syncwarp();
         }
@@ -519,82 +512,34 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
         if (lane == 0) mbar_arrive(fb);
       }
     }
-  } else if (active) {
-    // ------------------------------------------------------------------ workers
-    const int w = warp / 4;      // warpgroup
-    const int i = tid % 128;     // row in the tile
-    const bool issuer = (warp % 4) == 0 && lane == 0;
-    const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
-    const uint32_t acc = tmem + w * kNT;  // this warpgroup's accumulator
-    constexpr uint32_t idesc = idesc_bf16_f32(128, kNT);
-    if constexpr (C::kFp4) {
-      const int b = wk.paired ? i / 64 : 0;  // box of row i
-      const int r = wk.srow[b] + (wk.paired ? i % 64 : i);
-      const int gslot = b == 0 ? 0 : 1 + (r / 128 - wk.srow[1] / 128);  // smem scale group of row i
-      const uint32_t sf_row_off = C::kWTileBytes + gslot * 2048 + (r % 32) * 16 + ((r % 128) / 32) * 4;
-      const uint32_t w_row_off = (i / 8) * 1024 + (i % 8) * 128;
-      const uint32_t i8 = i % 8;
-      int cur = -1;  // ring stage whose full barrier this thread has passed
-      for (int j = 0;; ++j) {
-        const int q = w + j * kW;
-        if (q >= nslices) break;
-        const int s = q / kSPS, u = q % kSPS;
-        const int slot = s % nstages;
-        const uint32_t st = ring + slot * C::kStageBytes;
-        // Waits are bounded; a failed wait is made uniform over the warp (the
-        // tcgen05 loads / stores below are warp-collective) and then over the
-        // warpgroup at its barrier, so every thread leaves the loop together.
-        bool ok = !s_abort;
-        if (ok && s != cur) {
-          ok = mbar_wait(smem_u32(&bar_full[slot]), (s / nstages) & 1, p.err);
-          cur = s;
-        }
-        const int a = j % kNS;
-        const uint32_t xa = st + C::kXOff + u * (kNT * 128);
-        ok = __all_sync(0xFFFFFFFFu, ok);
-        if (ok) {
-          const uint4 q0 = lds128(st + w_row_off + (((2 * u) ^ i8) * 16));
-          const uint4 q1 = lds128(st + w_row_off + (((2 * u + 1) ^ i8) * 16));
-          const uint32_t sw = lds32(st + sf_row_off + u * 512);
-          ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bar_aempty[w * kNS + a]), ((j / kNS) & 1) ^ 1, p.err));
-          if (ok) {
-            tc_fence_after();
-            // activations of this slice into the weight pairs' K order
-#pragma unroll
-            for (int c = i; c < kNT * 8; c += 128) sts128(xa + c * 16, perm_x8(lds128(xa + c * 16)));
-            uint32_t s0, s1, s2, s3;
-            scale_pair_to_bf16x2(sw & 0xFFFFu, s0, s1);
-            scale_pair_to_bf16x2(sw >> 16, s2, s3);
-            uint32_t o[16];
-            const uint32_t col = tmem + lane_base + C::kAccCols + (w * kNS + a) * 32;
-            dequant32_perm(q0, s0, s1, o);
-            tmem_st16(col, o);
-            dequant32_perm(q1, s2, s3, o);
-            tmem_st16(col + 16, o);
-            tmem_wait_st();
-            fence_proxy_async_smem();
-          }
-        }
-        tc_fence_before();
-        if (wg_sync_or(w, !ok)) {
-          s_abort = 1;
-          break;
-        }
-        if (issuer) {
+  } else if (warp == C::kMmaWarp) {
+    // ------------------------------------------------------------------ MMA issuer
+    // One thread issues every MMA of the CTA into the single accumulator;
+    // the dequant warpgroups never wait on an issue.  NVFP4: per 128-K slice
+    // (a ring slot of tensor memory, filled by one warpgroup) 8 MMAs of K = 16
+    // and one commit that frees the slot; one more commit per ring stage.
+    // BF16: both operands in shared memory, 4 MMAs per 64-K stage.
+    if (lane == 0 && active) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, kNT);
+      const int klen = wk.k_end - wk.k_begin;
+      if constexpr (C::kFp4) {
+        for (int q = 0; q < nslices && !s_abort; ++q) {
+          const int a = q % kNS;
+          if (!mbar_wait(smem_u32(&bar_afull[a]), (q / kNS) & 1, p.err)) { s_abort = 1; break; }
           tc_fence_after();
-          const uint32_t a_tmem = tmem + C::kAccCols + (w * kNS + a) * 32;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_ts(acc, a_tmem + kk * 8, sdesc_sw128(xa + kk * 32), idesc, (j > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(smem_u32(&bar_aempty[w * kNS + a]));
-          const int qn = q + kW;
-          if (qn >= nslices || qn / kSPS != s) mma_commit(smem_u32(&bar_empty[slot]));
-          if (qn >= nslices) mma_commit(smem_u32(&bar_accum));
+          const int s = q / kSPS, u2 = q % kSPS;
+          const uint32_t xs = ring + (s % nstages) * C::kStageBytes + C::kXOff;
+          const int kq = min(kSliceK, klen - q * kSliceK);  // 64 or 128
+          const uint32_t a_tmem = tmem + C::kAccCols + a * C::kSlotCols;
+          for (int kk = 0; kk < kq / 16; ++kk) {
+            const int atom = 2 * u2 + kk / 4;
+            mma_ts(tmem, a_tmem + kk * 8, sdesc_sw128(xs + atom * (kNT * 128) + (kk % 4) * 32), idesc,
+                   (q > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(smem_u32(&bar_aempty[a]));
+          if (q + 1 == nslices || (q + 1) / kSPS != s) mma_commit(smem_u32(&bar_empty[s % nstages]));
         }
-      }
-    } else {
-      // BF16 weights: warpgroup 0's elected thread issues every stage's MMAs.
-      if (issuer) {
+      } else {
         for (int s = 0; s < nst && !s_abort; ++s) {
           const int slot = s % nstages;
           const uint32_t st = ring + slot * C::kStageBytes;
@@ -602,11 +547,71 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ss(acc, sdesc_sw128(st + kk * 32), sdesc_sw128(st + C::kXOff + kk * 32), idesc,
+            mma_ss(tmem, sdesc_sw128(st + kk * 32), sdesc_sw128(st + C::kXOff + kk * 32), idesc,
                    (s > 0 || kk > 0) ? 1u : 0u);
           mma_commit(smem_u32(&bar_empty[slot]));
         }
-        mma_commit(smem_u32(&bar_accum));
+      }
+      mma_commit(smem_u32(&bar_accum));
+    }
+  } else if (active) {
+    // ------------------------------------------------------------------ dequant warpgroups
+    if constexpr (C::kFp4) {
+      const int w = warp / 4;   // warpgroup: slices q = w, w + kW, ...
+      const int i = tid % 128;  // row in the tile
+      const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
+      const int b = wk.paired ? i / 64 : 0;  // box of row i
+      const int r = wk.srow[b] + (wk.paired ? i % 64 : i);
+      const int gslot = b == 0 ? 0 : 1 + (r / 128 - wk.srow[1] / 128);  // smem scale group of row i
+      const uint32_t sf_row_off = C::kWTileBytes + gslot * 2048 + (r % 32) * 16 + ((r % 128) / 32) * 4;
+      const uint32_t w_row_off = (i / 8) * 1024 + (i % 8) * 128;
+      const uint32_t i8 = i % 8;
+      const int klen = wk.k_end - wk.k_begin;
+      int cur = -1;  // ring stage whose full barrier this warp has passed
+      for (int q = w; q < nslices; q += kW) {
+        const int s = q / kSPS, u2 = q % kSPS;
+        const int slot = s % nstages;
+        const uint32_t st = ring + slot * C::kStageBytes;
+        const int a = q % kNS;
+        // Waits are bounded and made uniform over the warp (tcgen05.st is
+        // warp-collective); a warp that gives up leaves the loop, and the
+        // MMA thread's wait on its slot then times out as well.
+        bool ok = !s_abort;
+        if (ok && s != cur) {
+          ok = mbar_wait_sleepy(smem_u32(&bar_full[slot]), (s / nstages) & 1, p.err, 20);
+          cur = s;
+        }
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait_sleepy(smem_u32(&bar_aempty[a]), ((q / kNS) & 1) ^ 1, p.err, 20));
+        if (!ok) {
+          s_abort = 1;
+          break;
+        }
+        tc_fence_after();
+        const int natoms = min(kSliceK, klen - q * kSliceK) / kSubK;  // 1 or 2
+        const uint32_t col0 = tmem + lane_base + C::kAccCols + a * C::kSlotCols;
+        for (int v = 0; v < natoms; ++v) {
+          const int u = 2 * u2 + v;  // 64-K atom of the stage
+          // this warp's share of the atom's activations into the pairs' K order
+          const uint32_t xa = st + C::kXOff + u * (kNT * 128);
+          for (int c = i; c < kNT * 8; c += 128) sts128(xa + c * 16, perm_x8(lds128(xa + c * 16)));
+          const uint4 q0 = lds128(st + w_row_off + (((2 * u) ^ i8) * 16));
+          const uint4 q1 = lds128(st + w_row_off + (((2 * u + 1) ^ i8) * 16));
+          const uint32_t sw = lds32(st + sf_row_off + u * 512);
+          uint32_t s0, s1, s2, s3;
+          scale_pair_to_bf16x2(sw & 0xFFFFu, s0, s1);
+          scale_pair_to_bf16x2(sw >> 16, s2, s3);
+          uint32_t o[16];
+          dequant32_perm(q0, s0, s1, o);
+          tmem_st16(col0 + v * 32, o);
+          dequant32_perm(q1, s2, s3, o);
+          tmem_st16(col0 + v * 32 + 16, o);
+        }
+        tmem_wait_st();
+        fence_proxy_async_smem();  // the permuted activations, before the MMAs read them
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bar_afull[a]));
       }
     }
   }
@@ -622,7 +627,6 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
     // warp-uniform: the accumulator reads below are warp-collective
     const bool go = __all_sync(0xFFFFFFFFu, ok_acc && !s_abort);
     const float post = C::kFp4 ? static_cast<float>(1 << kShift) : 1.0f;
-    const int nacc = min(kW, nslices);  // warpgroups that accumulated anything
     constexpr int kCols = kNT / kW;     // token columns this warpgroup reduces
     const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
     // Row i's owner rank and its index among the owner's rows.
@@ -631,17 +635,13 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
     const int owner_feats = min(R, unit - owner * R);
     const int rr = (i / unit) * owner_feats + (fi - owner * R);
     const int rows_owner = owner_feats * (128 / unit);
-    // Sum of the warpgroups' accumulators for columns [c, c + 8) of row i.
+    // The accumulator's columns [c, c + 8) of row i.
     auto load_sum = [&](int c, float (&v8)[8]) {
+      uint32_t v[8];
+      tmem_ld8(tmem + lane_base + c, v);
+      tmem_wait_ld();
 #pragma unroll
-      for (int jj = 0; jj < 8; ++jj) v8[jj] = 0.0f;
-      for (int a2 = 0; a2 < nacc; ++a2) {
-        uint32_t v[8];
-        tmem_ld8(tmem + lane_base + a2 * kNT + c, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) v8[jj] += __uint_as_float(v[jj]);
-      }
+      for (int jj = 0; jj < 8; ++jj) v8[jj] = __uint_as_float(v[jj]);
     };
     // Partials of (token n, row i).  Push mode: the owner of row i receives
     // them from every rank into inbox[src][n][rr]; pull mode: each rank leaves
