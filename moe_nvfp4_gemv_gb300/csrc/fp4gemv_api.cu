@@ -205,6 +205,22 @@ void size_ring(const KernelInfo& info, int* nstages, size_t* smem, int* ctas_per
   *ctas_per_sm = per_sm;
 }
 
+// Ring of the register-fed kernel: a stage is the 16 KB weight tile, 2 KB per
+// scale group the call needs and the activations (info.stage_bytes); two
+// CTAs per SM, each with as many stages as its share of shared memory holds
+// (a deeper ring keeps more weight bytes in flight per SM).
+void size_ring_rf(const KernelInfo& info, int sf_groups, int* nstages, size_t* smem, int* stage_bytes,
+                  int* x_off) {
+  constexpr int kBudget = 112 * 1024;  // per CTA, two per SM
+  *x_off = 128 * 128 + sf_groups * 2048;
+  *stage_bytes = (*x_off + info.stage_bytes + 1023) / 1024 * 1024;
+  int ns = (kBudget - 1024 - info.inbox_bytes) / *stage_bytes;
+  if (ns > fp4::kMaxStages) ns = fp4::kMaxStages;
+  if (ns < 2) ns = 2;
+  *nstages = ns;
+  *smem = 1024 + static_cast<size_t>(ns) * *stage_bytes + info.inbox_bytes;
+}
+
 // Cluster split of K.  A CTA costs its ring stages plus a fixed overhead
 // (launch, prologue, first-load latency, cluster reduction, epilogue) of about
 // kFixedStages stages; minimise waves x (stages + fixed), ties to the smaller
@@ -261,9 +277,14 @@ fp4gemv_status dense_launch(int mode, const void* x, int64_t ldx, const void* w,
   const int NT = rf ? (M <= 8 ? 8 : 16) : pick_nt(M);
   KernelInfo info{};
   if (kernel_info(kmode, NT, &info) != cudaSuccess) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
-  int nstages = 0, per_sm = 0;
+  int nstages = 0, per_sm = 2, stage_bytes = 0, x_off = 0;
   size_t smem = 0;
-  size_ring(info, &nstages, &smem, &per_sm);
+  if (rf) {
+    const int sf_groups = silu_mul ? ((N / 2) % 64 == 0 ? 2 : 3) : 1;
+    size_ring_rf(info, sf_groups, &nstages, &smem, &stage_bytes, &x_off);
+  } else {
+    size_ring(info, &nstages, &smem, &per_sm);
+  }
   // A tile is 128 weight rows: 128 output features, or with silu_mul 64
   // features (64 gate rows + the 64 matching up rows, two 64-row boxes).
   const int box_rows = silu_mul ? 64 : 128;
@@ -303,6 +324,8 @@ fp4gemv_status dense_launch(int mode, const void* x, int64_t ldx, const void* w,
   p.rows_w = N;
   p.kbp = ((K / 16) + 3) / 4 * 4;
   p.nstages = nstages;
+  p.stage_bytes = stage_bytes;
+  p.x_off = x_off;
   p.err = err;
 
   LaunchCfg cfg{};
@@ -390,9 +413,10 @@ fp4gemv_status fp4gemv_moe_gate_up(const void* x, const int32_t* ids, int M, int
   const int NT = rf ? (M <= 8 ? 8 : 16) : 32;
   KernelInfo info{};
   if (kernel_info(kmode, NT, &info) != cudaSuccess) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
-  int nstages = 0, per_sm = 0;
+  int nstages = 0, per_sm = 0, stage_bytes = 0, x_off = 0;
   size_t smem = 0;
-  size_ring(info, &nstages, &smem, &per_sm);
+  if (rf) size_ring_rf(info, 2, &nstages, &smem, &stage_bytes, &x_off);  // routed: 1 group, shared: gate + up
+  else size_ring(info, &nstages, &smem, &per_sm);
   GemvParams p;
   std::memset(&p, 0, sizeof(p));
   if (!encode_2d(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w1, H / 2, static_cast<uint64_t>(E) * 2 * I, H / 2, 128, 128))
@@ -428,6 +452,8 @@ fp4gemv_status fp4gemv_moe_gate_up(const void* x, const int32_t* ids, int M, int
   p.kbp = p.kbp2 = ((H / 16) + 3) / 4 * 4;
   p.sf_expert_bytes = static_cast<uint32_t>(fp4gemv_scale_bytes(2 * I, H));
   p.nstages = nstages;
+  p.stage_bytes = stage_bytes;
+  p.x_off = x_off;
   p.err = err;
   const int shared_cols = (M + NT - 1) / NT;
   LaunchCfg cfg{};
@@ -475,9 +501,10 @@ fp4gemv_status fp4gemv_moe_down_combine(const void* act, const int32_t* ids, con
   const int NT = rf ? (M <= 8 ? 8 : 16) : 32;
   KernelInfo info{};
   if (kernel_info(kmode, NT, &info) != cudaSuccess) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
-  int nstages = 0, per_sm = 0;
+  int nstages = 0, per_sm = 0, stage_bytes = 0, x_off = 0;
   size_t smem = 0;
-  size_ring(info, &nstages, &smem, &per_sm);
+  if (rf) size_ring_rf(info, 1, &nstages, &smem, &stage_bytes, &x_off);
+  else size_ring(info, &nstages, &smem, &per_sm);
   GemvParams p;
   std::memset(&p, 0, sizeof(p));
   if (!encode_2d(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w2, I / 2, static_cast<uint64_t>(E) * H, I / 2, 128, 128))
@@ -522,6 +549,8 @@ fp4gemv_status fp4gemv_moe_down_combine(const void* act, const int32_t* ids, con
   p.kbp2 = ((SI / 16) + 3) / 4 * 4;
   p.sf_expert_bytes = static_cast<uint32_t>(fp4gemv_scale_bytes(H, I));
   p.nstages = nstages;
+  p.stage_bytes = stage_bytes;
+  p.x_off = x_off;
   p.err = err;
   const int shared_cols = (M + NT - 1) / NT;
   LaunchCfg cfg{};

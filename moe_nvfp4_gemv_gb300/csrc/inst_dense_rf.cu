@@ -10,9 +10,9 @@ cudaError_t run_gemv_rf(const GemvParams& p, const LaunchCfg& cfg, KernelInfo* i
   using C = RfCfg<kNT>;
   if (info) {
     info->threads = C::kThreads;
-    info->stage_bytes = C::kStageBytes;
+    info->stage_bytes = C::kXBytes;  // the activations' share; the host adds weights and scale groups
     info->red_bytes = 0;
-    info->inbox_bytes = C::kInboxBytes;
+    info->inbox_bytes = C::kInboxFloats * 4 + (kMode == kDenseFp4 ? 0 : C::kWorkBytes);
     info->tmem_cols = 0;
     return cudaSuccess;
   }

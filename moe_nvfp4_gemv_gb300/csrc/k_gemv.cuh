@@ -97,6 +97,8 @@ struct GemvParams {
   int kbp, kbp2;       // padded K blocks (K/16 rounded up to 4) of tm_w / tm_w2 rows
   uint32_t sf_expert_bytes;
   int nstages;
+  int stage_bytes;     // register-fed kernel: bytes per ring stage (weights, scale groups, activations)
+  int x_off;           // register-fed kernel: offset of the activations in a stage
   uint32_t* err;       // device error word
 };
 

@@ -57,10 +57,11 @@ struct RfCfg {
   static constexpr int kConverterWarp = kConsumerWarps + 1;
   static constexpr int kStageK = 256;
   static constexpr int kWTileBytes = 128 * 128;
-  static constexpr int kSfTileBytes = 3 * 4 * 512;
-  static constexpr int kXOff = kWTileBytes + kSfTileBytes;
+  // A stage: the weight tile, then 2 KB per 128-row scale group the call
+  // needs (1 plain, 2 gate/up, 3 when the up box straddles two groups), then
+  // the activations; the host sets the geometry per call (stage_bytes, x_off)
+  // so the ring is as deep as shared memory allows.
   static constexpr int kXBytes = kNT * kStageK * 2;
-  static constexpr int kStageBytes = kXOff + kXBytes;
   static constexpr int kTiles = kNT / 8;  // MMA n-tiles
   // Independent fp32 accumulators per n-tile on the f16 route: consecutive
   // MMAs of a thread go to different chains so they do not wait on each
@@ -73,9 +74,8 @@ struct RfCfg {
   static constexpr bool kHasF16 = kNT == 8;  // only the 8-token tile serves M <= kF16MaxM
   // The split-K inbox, then (MoE modes) the CTA's resolved work.
   static constexpr int kInboxFloats = kNT * 136;
-  static constexpr int kInboxBytes = kInboxFloats * 4 + static_cast<int>((sizeof(CtaWork) + 15) / 16 * 16);
+  static constexpr int kWorkBytes = static_cast<int>((sizeof(CtaWork) + 15) / 16 * 16);
   static_assert(kNT == 8 || kNT == 16, "token tile");
-  static_assert(kStageBytes % 1024 == 0, "stage alignment");
 };
 
 // D += A * B for one m16n8k16 f16 MMA (fp32 accumulate).
@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t ring = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t inbox = ring + p.nstages * C::kStageBytes;
+  const uint32_t inbox = ring + p.nstages * p.stage_bytes;
   __shared__ __align__(8) uint64_t bar_full[kMaxStages];
   __shared__ __align__(8) uint64_t bar_empty[kMaxStages];
   __shared__ __align__(8) uint64_t bar_xready[kMaxStages];
@@ -183,7 +183,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
   const uint64_t pol_x = policy_evict_last();
   auto issue_weights = [&](int s) {
     const int slot = s % nstages;
-    const uint32_t st = ring + slot * C::kStageBytes;
+    const uint32_t st = ring + slot * p.stage_bytes;
     const uint32_t fb = smem_u32(&bar_full[slot]);
     const int k0 = wk.k_begin + s * C::kStageK;
     const int nchunks = min(C::kStageK, wk.k_end - k0) / kSubK;
@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
       if (lane == 0) {
         for (int s = 0; s < nst && !s_abort; ++s) {
           const int slot = s % nstages;
-          const uint32_t st = ring + slot * C::kStageBytes;
+          const uint32_t st = ring + slot * p.stage_bytes;
           const uint32_t fb = smem_u32(&bar_full[slot]);
           if (s >= pre) {
             if (!mbar_wait_sleepy(smem_u32(&bar_empty[slot]), ((s / nstages) & 1) ^ 1, p.err, 64)) { s_abort = 1; break; }
@@ -293,7 +293,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
           }
           const int k0 = wk.k_begin + s * C::kStageK;
           mbar_arrive_expect_tx(fb, C::kXBytes);
-          tma_load_3d(st + C::kXOff, &p.tm_x, 0, 0, k0 / kSubK, fb, pol_x);
+          tma_load_3d(st + p.x_off, &p.tm_x, 0, 0, k0 / kSubK, fb, pol_x);
         }
       }
     } else {
@@ -304,7 +304,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
       const int u = lane / 8, cc = lane % 8;
       for (int s = 0; s < nst && !s_abort; ++s) {
         const int slot = s % nstages;
-        const uint32_t st = ring + slot * C::kStageBytes;
+        const uint32_t st = ring + slot * p.stage_bytes;
         const uint32_t fb = smem_u32(&bar_full[slot]);
         if (s >= pre) {
           const bool ok =
@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
         const int k0 = wk.k_begin + s * C::kStageK;
         const bool kok = lane * 8 < min(C::kStageK, wk.k_end - k0);
         const uint16_t* src_k = xb + k0 + lane * 8;
-        const uint32_t dst0 = st + C::kXOff + u * (kNT * 128);
+        const uint32_t dst0 = st + p.x_off + u * (kNT * 128);
 #pragma unroll
         for (int n = 0; n < kNT; ++n) {
           const bool valid = kok && n < ntok;
@@ -335,7 +335,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
     // in f16.  A stage with any inexact value is flagged for the bf16 route.
     for (int s = 0; s < nst; ++s) {
       const int slot = s % nstages;
-      const uint32_t st = ring + slot * C::kStageBytes;
+      const uint32_t st = ring + slot * p.stage_bytes;
       const bool ok = __all_sync(
           0xFFFFFFFFu, !s_abort && mbar_wait_sleepy(smem_u32(&bar_full[slot]), (s / nstages) & 1, p.err, 32));
       if (!ok) {
@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
       for (int id = lane; id < ntok * 32; id += 32) {
         const int n = id / 32, q = id % 32;
         if (8 * q >= kvalid) continue;
-        const uint32_t a = st + C::kXOff + (q / 8) * (kNT * 128) + (n / 8) * 1024 + (n % 8) * 128 +
+        const uint32_t a = st + p.x_off + (q / 8) * (kNT * 128) + (n / 8) * 1024 + (n % 8) * 128 +
                            ((static_cast<uint32_t>(q % 8) ^ static_cast<uint32_t>(n % 8)) * 16);
         const uint4 v = lds128(a);
         uint4 o;
@@ -410,7 +410,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
 #pragma unroll
         for (int t = 0; t < C::kTiles; ++t) {
           const int n = 8 * t + g;
-          const uint4 xv = lds128(st + C::kXOff + u * (kNT * 128) + (n / 8) * 1024 + (n % 8) * 128 +
+          const uint4 xv = lds128(st + p.x_off + u * (kNT * 128) + (n / 8) * 1024 + (n % 8) * 128 +
                                   ((ch ^ static_cast<uint32_t>(n % 8)) * 16));
           mma_f16_16816(acc[(2 * w) % C::kChains][t], r0[0], r1[0], r0[1], r1[1], xv.x, xv.y);
           mma_f16_16816(acc[(2 * w + 1) % C::kChains][t], r0[2], r1[2], r0[3], r1[3], xv.z, xv.w);
@@ -446,7 +446,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
 #pragma unroll
         for (int t = 0; t < C::kTiles; ++t) {
           const int n = 8 * t + g;
-          const uint4 xv = perm_x8(lds128(st + C::kXOff + u * (kNT * 128) + (n / 8) * 1024 + (n % 8) * 128 +
+          const uint4 xv = perm_x8(lds128(st + p.x_off + u * (kNT * 128) + (n / 8) * 1024 + (n % 8) * 128 +
                                           ((ch ^ static_cast<uint32_t>(n % 8)) * 16)));
           mma_bf16_16816(acc[(2 * w) % C::kChains][t], r0[0], r1[0], r0[1], r1[1], xv.x, xv.y);
           mma_bf16_16816(acc[(2 * w + 1) % C::kChains][t], r0[2], r1[2], r0[3], r1[3], xv.z, xv.w);
@@ -490,7 +490,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
     };
     for (int s = 0; s < nst; ++s) {
       const int slot = s % nstages;
-      const uint32_t st = ring + slot * C::kStageBytes;
+      const uint32_t st = ring + slot * p.stage_bytes;
       const bool ok = __all_sync(0xFFFFFFFFu, !s_abort && mbar_wait(smem_u32(&bar_full[slot]), (s / nstages) & 1, p.err));
       if (!ok) {
         s_abort = 1;
