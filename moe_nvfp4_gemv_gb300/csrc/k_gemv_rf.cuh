@@ -33,9 +33,9 @@
 //
 // Routes.  For M > kF16MaxM every stage runs the bf16 route above.  For
 // M <= kF16MaxM the f16 route: a converter warp turns each stage's activation
-// rows in shared memory into f16 in place as soon as the stage lands (ahead of the
-// consumers, which wait for it on a per-stage barrier), checking that every
-// value converts exactly; the stage then runs on f16 MMAs with the codes converted
+// rows in shared memory into f16 in place as soon as they land (ahead of the
+// consumers: its arrival is part of the stage's full barrier, so a consumer
+// waits on one barrier per stage), checking that every value converts exactly; the stage then runs on f16 MMAs with the codes converted
 // by cvt.rn.f16x2.e2m1x2 (natural K order, half the ALU work of the bf16
 // route).  A stage with any value that is not exactly an f16 (|x| > 65504,
 // too many low bits for the f16 subnormal grid, NaN) runs the bf16 route with
@@ -141,7 +141,10 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
   const uint32_t inbox = ring + p.nstages * p.stage_bytes;
   __shared__ __align__(8) uint64_t bar_full[kMaxStages];
   __shared__ __align__(8) uint64_t bar_empty[kMaxStages];
-  __shared__ __align__(8) uint64_t bar_xready[kMaxStages];
+  // f16 route: the activations land on bar_xfull; the converter waits there and
+  // its arrival (after the conversion) is one of the two that complete bar_full,
+  // so the consumers wait on a single barrier per stage.
+  __shared__ __align__(8) uint64_t bar_xfull[kMaxStages];
   __shared__ __align__(8) uint64_t bar_inbox;
   __shared__ volatile int s_abort;
   __shared__ int s_xbad[kMaxStages];  // last stage (of this slot) whose activations are not all exact f16
@@ -222,14 +225,20 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
     s_abort = 0;
     s_last = 0;
     bool act = true;
+    int ntok0 = p.M;
     if constexpr (!kDense) {
       copy_work(*mwork, wk);
       act = mwork->active != 0;
+      ntok0 = act ? mwork->ntok : 0;
     }
+    // arrivals: dense, the producer (+ the converter on the f16 route); MoE,
+    // the 32 gathering lanes' cp.async and lane 0 (the f16 route moves the
+    // 32 to bar_xfull and adds the converter)
+    const bool f16 = C::kHasF16 && ntok0 <= C::kF16MaxM;
     for (int i = 0; i < nstages; ++i) {
-      mbar_init(smem_u32(&bar_full[i]), kDense ? 1 : 33);
+      mbar_init(smem_u32(&bar_full[i]), f16 ? 2 : (kDense ? 1 : 33));
       mbar_init(smem_u32(&bar_empty[i]), C::kConsumerWarps);
-      mbar_init(smem_u32(&bar_xready[i]), 1);
+      mbar_init(smem_u32(&bar_xfull[i]), kDense ? 1 : 32);
       s_xbad[i] = -1;
     }
     mbar_init(smem_u32(&bar_inbox), 1);
@@ -292,8 +301,15 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
             issue_weights(s);
           }
           const int k0 = wk.k_begin + s * C::kStageK;
-          mbar_arrive_expect_tx(fb, C::kXBytes);
-          tma_load_3d(st + p.x_off, &p.tm_x, 0, 0, k0 / kSubK, fb, pol_x);
+          if (f16route) {
+            const uint32_t xb = smem_u32(&bar_xfull[slot]);
+            mbar_arrive_expect_tx(xb, C::kXBytes);
+            tma_load_3d(st + p.x_off, &p.tm_x, 0, 0, k0 / kSubK, xb, pol_x);
+            mbar_arrive(fb);
+          } else {
+            mbar_arrive_expect_tx(fb, C::kXBytes);
+            tma_load_3d(st + p.x_off, &p.tm_x, 0, 0, k0 / kSubK, fb, pol_x);
+          }
         }
       }
     } else {
@@ -323,7 +339,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
           const uint32_t dst = dst0 + (n / 8) * 1024 + (n % 8) * 128 + ((cc ^ (n % 8)) * 16);
           cp_async16(dst, valid ? src_k + mwork->xoff[n] : xb, valid ? 16u : 0u);
         }
-        cp_async_arrive_noinc(fb);
+        cp_async_arrive_noinc(f16route ? smem_u32(&bar_xfull[slot]) : fb);
         if (lane == 0) mbar_arrive(fb);
       }
     }
@@ -336,8 +352,8 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
     for (int s = 0; s < nst; ++s) {
       const int slot = s % nstages;
       const uint32_t st = ring + slot * p.stage_bytes;
-      const bool ok = __all_sync(
-          0xFFFFFFFFu, !s_abort && mbar_wait_sleepy(smem_u32(&bar_full[slot]), (s / nstages) & 1, p.err, 32));
+      const bool ok =
+          __all_sync(0xFFFFFFFFu, !s_abort && mbar_wait(smem_u32(&bar_xfull[slot]), (s / nstages) & 1, p.err));
       if (!ok) {
         s_abort = 1;
         break;
@@ -360,7 +376,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
       if (!__all_sync(0xFFFFFFFFu, exact) && lane == 0) s_xbad[slot] = s;
       fence_proxy_async_smem();  // these writes precede the slot's next TMA fill
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bar_xready[slot]));
+      if (lane == 0) mbar_arrive(smem_u32(&bar_full[slot]));
     }
   } else {
     // ------------------------------------------------------------------ consumers
@@ -513,11 +529,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
         continue;
       }
       if constexpr (C::kHasF16) {
-      // the converter warp has turned the stage's activations into f16
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bar_xready[slot]), (s / nstages) & 1, p.err))) {
-        s_abort = 1;
-        break;
-      }
+      // (bar_full included the converter's arrival: the activations are f16)
       if (s_xbad[slot] != s) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
