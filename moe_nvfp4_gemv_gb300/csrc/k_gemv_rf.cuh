@@ -88,6 +88,17 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// 16-byte shared load that only lanes with `on` perform; the others get zeros
+// (a predicated load: no branch, no shared-memory traffic for them).
+__device__ __forceinline__ uint4 lds128_if(uint32_t a, bool on) {
+  uint4 v = make_uint4(0u, 0u, 0u, 0u);
+  asm volatile(
+      "{ .reg .pred p; setp.ne.u32 p, %5, 0; @p ld.shared.v4.u32 {%0, %1, %2, %3}, [%4]; }"
+      : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w)
+      : "r"(a), "r"(static_cast<uint32_t>(on)));
+  return v;
+}
+
 __device__ __forceinline__ uint32_t lds16(uint32_t a) {
   unsigned short v;
   asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
@@ -184,8 +195,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
   }
   const uint64_t pol_w = policy_evict_first();
   const uint64_t pol_x = policy_evict_last();
-  auto issue_weights = [&](int s) {
-    const int slot = s % nstages;
+  auto issue_weights = [&](int s, int slot) {
     const uint32_t st = ring + slot * p.stage_bytes;
     const uint32_t fb = smem_u32(&bar_full[slot]);
     const int k0 = wk.k_begin + s * C::kStageK;
@@ -249,7 +259,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
     }
     mbar_fence_init();
     const int pre0 = min(stages_of(act), nstages);
-    for (int s = 0; s < pre0; ++s) issue_weights(s);
+    for (int s = 0; s < pre0; ++s) issue_weights(s, s);
   }
   __syncthreads();
   if (S > 1) cluster_arrive_relaxed();  // paired with a wait before the first remote access
@@ -292,13 +302,12 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
     pdl_wait();
     if constexpr (kDense) {
       if (lane == 0) {
-        for (int s = 0; s < nst && !s_abort; ++s) {
-          const int slot = s % nstages;
+        for (int s = 0, slot = 0, ph = 0; s < nst && !s_abort; ++s, slot = slot + 1 == nstages ? 0 : slot + 1, ph ^= slot == 0) {
           const uint32_t st = ring + slot * p.stage_bytes;
           const uint32_t fb = smem_u32(&bar_full[slot]);
           if (s >= pre) {
-            if (!mbar_wait_sleepy(smem_u32(&bar_empty[slot]), ((s / nstages) & 1) ^ 1, p.err, 64)) { s_abort = 1; break; }
-            issue_weights(s);
+            if (!mbar_wait_sleepy(smem_u32(&bar_empty[slot]), ph ^ 1, p.err, 64)) { s_abort = 1; break; }
+            issue_weights(s, slot);
           }
           const int k0 = wk.k_begin + s * C::kStageK;
           if (f16route) {
@@ -318,15 +327,14 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
       // chunk's pairs / tokens are zero-filled).
       const uint16_t* xb = wk.shared ? p.x2 : p.x;
       const int u = lane / 8, cc = lane % 8;
-      for (int s = 0; s < nst && !s_abort; ++s) {
-        const int slot = s % nstages;
+      for (int s = 0, slot = 0, ph = 0; s < nst && !s_abort; ++s, slot = slot + 1 == nstages ? 0 : slot + 1, ph ^= slot == 0) {
         const uint32_t st = ring + slot * p.stage_bytes;
         const uint32_t fb = smem_u32(&bar_full[slot]);
         if (s >= pre) {
           const bool ok =
-              __all_sync(0xFFFFFFFFu, mbar_wait_sleepy(smem_u32(&bar_empty[slot]), ((s / nstages) & 1) ^ 1, p.err, 64));
+              __all_sync(0xFFFFFFFFu, mbar_wait_sleepy(smem_u32(&bar_empty[slot]), ph ^ 1, p.err, 64));
           if (!ok) { s_abort = 1; break; }
-          if (lane == 0) issue_weights(s);
+          if (lane == 0) issue_weights(s, slot);
           __syncwarp();
         }
         const int k0 = wk.k_begin + s * C::kStageK;
@@ -349,11 +357,9 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
     // Rows < ntok of each stage's activations to f16 in place (16-byte
     // chunks); the other rows and K past the end are zero-filled, the same bits
     // in f16.  A stage with any inexact value is flagged for the bf16 route.
-    for (int s = 0; s < nst; ++s) {
-      const int slot = s % nstages;
+    for (int s = 0, slot = 0, ph = 0; s < nst; ++s, slot = slot + 1 == nstages ? 0 : slot + 1, ph ^= slot == 0) {
       const uint32_t st = ring + slot * p.stage_bytes;
-      const bool ok =
-          __all_sync(0xFFFFFFFFu, !s_abort && mbar_wait(smem_u32(&bar_xfull[slot]), (s / nstages) & 1, p.err));
+      const bool ok = __all_sync(0xFFFFFFFFu, !s_abort && mbar_wait(smem_u32(&bar_xfull[slot]), ph, p.err));
       if (!ok) {
         s_abort = 1;
         break;
@@ -401,6 +407,9 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
       if constexpr (kDense) xrow[t] = n < ntok ? p.x + static_cast<int64_t>(n) * p.ldx : nullptr;
       else xrow[t] = n < ntok ? (wk.shared ? p.x2 : p.x) + mwork->xoff[n] : nullptr;
     }
+    // B rows (tokens) past ntok are zero in the stage; lanes holding them use
+    // zero registers instead of loading (the same products, less shared-memory
+    // traffic: at M = 1 only a quarter warp loads activations).
     // One 128-K half of a stage: chunk j = 4 h + c of both rows.  `cvalid`
     // false (a chunk past the end of a ragged last stage) gives zero A
     // registers: that chunk's scales were not copied and may hold anything.
@@ -426,8 +435,9 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
 #pragma unroll
         for (int t = 0; t < C::kTiles; ++t) {
           const int n = 8 * t + g;
-          const uint4 xv = lds128(st + p.x_off + u * (kNT * 128) + (n / 8) * 1024 + (n % 8) * 128 +
-                                  ((ch ^ static_cast<uint32_t>(n % 8)) * 16));
+          const uint4 xv = lds128_if(st + p.x_off + u * (kNT * 128) + (n / 8) * 1024 + (n % 8) * 128 +
+                                         ((ch ^ static_cast<uint32_t>(n % 8)) * 16),
+                                     n < ntok);
           mma_f16_16816(acc[(2 * w) % C::kChains][t], r0[0], r1[0], r0[1], r1[1], xv.x, xv.y);
           mma_f16_16816(acc[(2 * w + 1) % C::kChains][t], r0[2], r1[2], r0[3], r1[3], xv.z, xv.w);
         }
@@ -462,8 +472,9 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
 #pragma unroll
         for (int t = 0; t < C::kTiles; ++t) {
           const int n = 8 * t + g;
-          const uint4 xv = perm_x8(lds128(st + p.x_off + u * (kNT * 128) + (n / 8) * 1024 + (n % 8) * 128 +
-                                          ((ch ^ static_cast<uint32_t>(n % 8)) * 16)));
+          const uint4 xv = perm_x8(lds128_if(st + p.x_off + u * (kNT * 128) + (n / 8) * 1024 + (n % 8) * 128 +
+                                                 ((ch ^ static_cast<uint32_t>(n % 8)) * 16),
+                                             n < ntok));
           mma_bf16_16816(acc[(2 * w) % C::kChains][t], r0[0], r1[0], r0[1], r1[1], xv.x, xv.y);
           mma_bf16_16816(acc[(2 * w + 1) % C::kChains][t], r0[2], r1[2], r0[3], r1[3], xv.z, xv.w);
         }
@@ -504,10 +515,9 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
         }
       }
     };
-    for (int s = 0; s < nst; ++s) {
-      const int slot = s % nstages;
+    for (int s = 0, slot = 0, ph = 0; s < nst; ++s, slot = slot + 1 == nstages ? 0 : slot + 1, ph ^= slot == 0) {
       const uint32_t st = ring + slot * p.stage_bytes;
-      const bool ok = __all_sync(0xFFFFFFFFu, !s_abort && mbar_wait(smem_u32(&bar_full[slot]), (s / nstages) & 1, p.err));
+      const bool ok = __all_sync(0xFFFFFFFFu, !s_abort && mbar_wait(smem_u32(&bar_full[slot]), ph, p.err));
       if (!ok) {
         s_abort = 1;
         break;
