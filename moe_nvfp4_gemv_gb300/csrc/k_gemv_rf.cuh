@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
     if (S > 1) {
       const int u = unit_of(), r = (u + static_cast<int>(S) - 1) / static_cast<int>(S);
       const int mine0 = max(0, min(r, u - static_cast<int>(rank) * r)) * (128 / u);
-      mbar_arrive_expect_tx(smem_u32(&bar_inbox), S * kNT * mine0 * 4);
+      mbar_arrive_expect_tx(smem_u32(&bar_inbox), S * ntok0 * mine0 * 4);  // tokens < ntok only
     }
     mbar_fence_init();
     const int pre0 = min(stages_of(act), nstages);
@@ -566,8 +566,8 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
   __syncwarp();
   if (warp < C::kConsumerWarps) {
     const float post = static_cast<float>(1 << kShift);
-    // Push this thread's partials (rows row0 / row1, tokens 8t + 2c + {0,1})
-    // to the owners of the rows: inbox[src][n][rr].
+    // Push this thread's partials (rows row0 / row1, tokens 8t + 2c + {0,1}
+    // below ntok) to the owners of the rows: inbox[src][n][rr].
     if (S > 1) cluster_wait();  // all peers' inbox barriers are initialised
     const bool go = !s_abort;
 #pragma unroll
@@ -595,6 +595,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
           if constexpr (C::kHasF16) a16 += accb[t][2 * hr + e] * post;
           const float v = go ? a16 : 0.0f;
           const uint32_t off = n * rows_owner * 4;
+          if (n >= ntok) continue;
           if (S > 1) st_async_f32(rbase + off, v, rbar);
           else stsf(rbase + off, v);
         }
