@@ -209,10 +209,12 @@ void size_ring(const KernelInfo& info, int* nstages, size_t* smem, int* ctas_per
 // scale group the call needs and the activations (info.stage_bytes); two
 // CTAs per SM, each with as many stages as its share of shared memory holds
 // (a deeper ring keeps more weight bytes in flight per SM).
-void size_ring_rf(const KernelInfo& info, int sf_groups, int* nstages, size_t* smem, int* stage_bytes,
-                  int* x_off) {
-  constexpr int kBudget = 112 * 1024;  // per CTA, two per SM
-  *x_off = 128 * 128 + sf_groups * 2048;
+constexpr int kRfBudget = 110 * 1024;  // shared memory per register-fed CTA, two per SM (with margin)
+
+void size_ring_rf(const KernelInfo& info, int wtile_bytes, int sf_groups, int* nstages, size_t* smem,
+                  int* stage_bytes, int* x_off) {
+  constexpr int kBudget = kRfBudget;
+  *x_off = wtile_bytes + sf_groups * 2048;
   *stage_bytes = (*x_off + info.stage_bytes + 1023) / 1024 * 1024;
   int ns = (kBudget - 1024 - info.inbox_bytes) / *stage_bytes;
   if (ns > fp4::kMaxStages) ns = fp4::kMaxStages;
@@ -227,6 +229,70 @@ void size_ring_rf(const KernelInfo& info, int sf_groups, int* nstages, size_t* s
 // split.  Every rank keeps a non-empty K range.
 constexpr int kFixedStages = 4;
 constexpr int kStageK4 = fp4::kStageK4;
+
+// Tile height and K split of the dense register-fed kernel.  A tile is 16 cw
+// rows (cw = 6 .. 8 consumer warps; with silu_mul 8 cw gate + 8 cw up rows,
+// cw even), split over S = 1, 2, 4 or 8 cluster ranks along K.  The default
+// is 128-row tiles split by pick_split; a lower tile is taken only when its
+// grid fits on the GPU at once (cap[S] CTAs in whole clusters) and its CTAs
+// are at least 8 % shorter: a stage costs a fixed part (barrier hand-offs,
+// activations) plus a part that scales with the tile height, and a CTA adds
+// kFixedStages stages (prologue, first loads, reduction, epilogue).  This
+// evens out grids such as 224 tiles of 128 rows on 304 CTA slots.
+double rf_cta_cost(int cw, int K, int s) {
+  const int kslab = ((K + s - 1) / s + 63) / 64 * 64;
+  return (static_cast<double>(kslab) / kStageK4) * (0.45 + 0.55 * cw / 8.0) + kFixedStages;
+}
+
+void pick_rf_geometry(int n_out, bool paired, int K, int s_default, const int (&cap)[9], int* cw_out, int* s_out) {
+  *cw_out = 8;
+  *s_out = s_default;
+  const long tiles8 = paired ? (n_out + 63) / 64 : (n_out + 127) / 128;
+  if (tiles8 * s_default > cap[s_default]) return;  // the default runs in waves: keep it
+  double best = rf_cta_cost(8, K, s_default) * 0.92;
+  for (int cw = 7; cw >= 6; --cw) {
+    if (paired && cw % 2 != 0) continue;
+    const int feats = paired ? 8 * cw : 16 * cw;
+    const long tiles = (n_out + feats - 1) / feats;
+    for (int s = 1; s <= 8; s *= 2) {
+      if (s > 1 && K / s < kStageK4) break;
+      const int kslab = ((K + s - 1) / s + 63) / 64 * 64;
+      if (static_cast<long>(s - 1) * kslab >= K) break;  // every rank keeps a non-empty K range
+      if (tiles * s > cap[s]) continue;
+      const double cost = rf_cta_cost(cw, K, s);
+      if (cost < best) {
+        best = cost;
+        *cw_out = cw;
+        *s_out = s;
+      }
+    }
+  }
+}
+
+// Co-resident CTAs of the dense register-fed kernel in clusters of 1 .. 8
+// (per device and token tile, queried once).
+struct RfCap {
+  std::atomic<int> v[2][9];
+};
+RfCap g_rf_cap[kMaxDevices];
+
+fp4gemv_status rf_capacity(int nt, int (&cap)[9]) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FP4GEMV_ERR_CUDA;
+  const int i = nt == 8 ? 0 : 1;
+  cap[0] = 0;
+  for (int s = 1; s <= 8; ++s) {
+    int n = g_rf_cap[dev].v[i][s].load(std::memory_order_acquire);
+    if (n == 0) {
+      // (size_ring_rf never exceeds the budget, so this is the launches' worst case)
+      if (fp4::rf_max_clusters(fp4::kDenseFp4, nt, s, kRfBudget, &n) != cudaSuccess) return FP4GEMV_ERR_CUDA;
+      if (n < 0) n = 0;
+      g_rf_cap[dev].v[i][s].store(n == 0 ? -1 : n, std::memory_order_release);
+    }
+    cap[s] = n < 0 ? 0 : n * s;  // CTAs
+  }
+  return FP4GEMV_OK;
+}
 
 int pick_split(int tiles, int K, int stage_k, int slots) {
   int best = 1;
@@ -279,18 +345,32 @@ fp4gemv_status dense_launch(int mode, const void* x, int64_t ldx, const void* w,
   if (kernel_info(kmode, NT, &info) != cudaSuccess) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
   int nstages = 0, per_sm = 2, stage_bytes = 0, x_off = 0;
   size_t smem = 0;
+  // A tile is `box_rows` weight rows per box: 128 output features (tcgen05),
+  // or with silu_mul 64 features (64 gate rows + the 64 matching up rows, two
+  // boxes); the register-fed kernel's tiles are 16 cw rows (see
+  // pick_rf_geometry).
+  int cw = 8, S0 = 1;
   if (rf) {
-    const int sf_groups = silu_mul ? ((N / 2) % 64 == 0 ? 2 : 3) : 1;
-    size_ring_rf(info, sf_groups, &nstages, &smem, &stage_bytes, &x_off);
+    int cap[9];
+    st = rf_capacity(NT, cap);
+    if (st != FP4GEMV_OK) return st;
+    const int s_default =
+        pick_split((n_out + (silu_mul ? 63 : 127)) / (silu_mul ? 64 : 128), K, fp4::kStageK4, sms * per_sm);
+    pick_rf_geometry(n_out, silu_mul != 0, K, s_default, cap, &cw, &S0);
+    // 128-row scale groups a stage holds: a box of h rows starting at an
+    // offset o (mod h) stays in one group for every tile iff h divides 128
+    // and o is a multiple of h
+    const int h = silu_mul ? 8 * cw : 16 * cw;
+    const bool even = 128 % h == 0;
+    const int sf_groups = silu_mul ? (even ? 1 : 2) + ((even && (N / 2) % h == 0) ? 1 : 2) : (even ? 1 : 2);
+    size_ring_rf(info, 16 * cw * 128, sf_groups, &nstages, &smem, &stage_bytes, &x_off);
   } else {
     size_ring(info, &nstages, &smem, &per_sm);
   }
-  // A tile is 128 weight rows: 128 output features, or with silu_mul 64
-  // features (64 gate rows + the 64 matching up rows, two 64-row boxes).
-  const int box_rows = silu_mul ? 64 : 128;
-  const int tiles = silu_mul ? (n_out + 63) / 64 : (n_out + 127) / 128;
+  const int box_rows = rf ? (silu_mul ? 8 * cw : 16 * cw) : (silu_mul ? 64 : 128);
+  const int tiles = (n_out + box_rows - 1) / box_rows;
   const int stage_k = fp4w ? fp4::kStageK4 : fp4::kStageK16;
-  const int S0 = pick_split(tiles, K, stage_k, sms * per_sm);
+  if (!rf) S0 = pick_split(tiles, K, stage_k, sms * per_sm);
   const int kslab = ((K + S0 - 1) / S0 + 63) / 64 * 64;
   const int S = (K + kslab - 1) / kslab;  // every cluster rank gets a non-empty K range
 
@@ -326,6 +406,7 @@ fp4gemv_status dense_launch(int mode, const void* x, int64_t ldx, const void* w,
   p.nstages = nstages;
   p.stage_bytes = stage_bytes;
   p.x_off = x_off;
+  p.cw = cw;
   p.err = err;
 
   LaunchCfg cfg{};
@@ -415,7 +496,7 @@ fp4gemv_status fp4gemv_moe_gate_up(const void* x, const int32_t* ids, int M, int
   if (kernel_info(kmode, NT, &info) != cudaSuccess) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
   int nstages = 0, per_sm = 0, stage_bytes = 0, x_off = 0;
   size_t smem = 0;
-  if (rf) size_ring_rf(info, 2, &nstages, &smem, &stage_bytes, &x_off);  // routed: 1 group, shared: gate + up
+  if (rf) size_ring_rf(info, 128 * 128, 2, &nstages, &smem, &stage_bytes, &x_off);  // routed: 1 group, shared: gate + up
   else size_ring(info, &nstages, &smem, &per_sm);
   GemvParams p;
   std::memset(&p, 0, sizeof(p));
@@ -503,7 +584,7 @@ fp4gemv_status fp4gemv_moe_down_combine(const void* act, const int32_t* ids, con
   if (kernel_info(kmode, NT, &info) != cudaSuccess) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
   int nstages = 0, per_sm = 0, stage_bytes = 0, x_off = 0;
   size_t smem = 0;
-  if (rf) size_ring_rf(info, 1, &nstages, &smem, &stage_bytes, &x_off);
+  if (rf) size_ring_rf(info, 128 * 128, 1, &nstages, &smem, &stage_bytes, &x_off);
   else size_ring(info, &nstages, &smem, &per_sm);
   GemvParams p;
   std::memset(&p, 0, sizeof(p));

@@ -5,6 +5,25 @@
 
 namespace fp4 {
 
+// Raise the kernel's dynamic shared-memory limit to `smem` (once per device
+// and size).
+template <int kMode, int kNT>
+cudaError_t configure_rf(size_t smem, unsigned cluster) {
+  auto k = gemv_rf_kernel<kMode, kNT>;
+  static int configured_smem[64];  // per device (0 = not yet)
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (configured_smem[dev] < static_cast<int>(smem)) {
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    configured_smem[dev] = static_cast<int>(smem);
+  }
+  if (cluster > 8) return cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return cudaSuccess;
+}
+
 template <int kMode, int kNT>
 cudaError_t run_gemv_rf(const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info) {
   using C = RfCfg<kNT>;
@@ -16,22 +35,35 @@ cudaError_t run_gemv_rf(const GemvParams& p, const LaunchCfg& cfg, KernelInfo* i
     info->tmem_cols = 0;
     return cudaSuccess;
   }
-  auto k = gemv_rf_kernel<kMode, kNT>;
-  static int configured_smem[64];  // per device (0 = not yet)
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  cudaError_t e = configure_rf<kMode, kNT>(cfg.smem, cfg.cluster);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (configured_smem[dev] < static_cast<int>(cfg.smem)) {
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(cfg.smem));
-    if (e != cudaSuccess) return e;
-    if (cfg.cluster > 8) {
-      e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-      if (e != cudaSuccess) return e;
-    }
-    configured_smem[dev] = static_cast<int>(cfg.smem);
-  }
-  return launch_kernel(k, C::kThreads, p, cfg);
+  return launch_kernel(gemv_rf_kernel<kMode, kNT>, C::kThreads, p, cfg);
+}
+
+template <int kMode, int kNT>
+cudaError_t rf_clusters(unsigned cluster, size_t smem, int* n) {
+  cudaError_t e = configure_rf<kMode, kNT>(smem, cluster);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t c = {};
+  c.gridDim = dim3(cluster, 1, 1);
+  c.blockDim = dim3(RfCfg<kNT>::kThreads, 1, 1);
+  c.dynamicSmemBytes = smem;
+  cudaLaunchAttribute a[1];
+  a[0].id = cudaLaunchAttributeClusterDimension;
+  a[0].val.clusterDim.x = cluster;
+  a[0].val.clusterDim.y = 1;
+  a[0].val.clusterDim.z = 1;
+  c.attrs = a;
+  c.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(n, gemv_rf_kernel<kMode, kNT>, &c);
+}
+
+cudaError_t rf_max_clusters(int mode, int nt, unsigned cluster, size_t smem, int* n) {
+#define FP4_CASE(M_, NT_) \
+  if (mode == M_ && nt == NT_) return rf_clusters<M_, NT_>(cluster, smem, n);
+  FP4_CASE(kDenseFp4, 8) FP4_CASE(kDenseFp4, 16)
+#undef FP4_CASE
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_rf(int mode, int nt, const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info) {

@@ -99,6 +99,7 @@ struct GemvParams {
   int nstages;
   int stage_bytes;     // register-fed kernel: bytes per ring stage (weights, scale groups, activations)
   int x_off;           // register-fed kernel: offset of the activations in a stage
+  int cw;              // register-fed dense kernel: consumer warps = tile height / 16 (4 .. 8)
   uint32_t* err;       // device error word
 };
 

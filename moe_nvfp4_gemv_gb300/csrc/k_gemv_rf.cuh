@@ -56,11 +56,10 @@ struct RfCfg {
   static constexpr int kProducerWarp = kConsumerWarps;
   static constexpr int kConverterWarp = kConsumerWarps + 1;
   static constexpr int kStageK = 256;
-  static constexpr int kWTileBytes = 128 * 128;
-  // A stage: the weight tile, then 2 KB per 128-row scale group the call
-  // needs (1 plain, 2 gate/up, 3 when the up box straddles two groups), then
-  // the activations; the host sets the geometry per call (stage_bytes, x_off)
-  // so the ring is as deep as shared memory allows.
+  // A stage: the weight tile (16 cw rows x 128 bytes), then 2 KB per 128-row
+  // scale group its boxes touch (up to 4), then the activations; the host sets
+  // the geometry per call (stage_bytes, x_off) so the ring is as deep as
+  // shared memory allows.
   static constexpr int kXBytes = kNT * kStageK * 2;
   static constexpr int kTiles = kNT / 8;  // MMA n-tiles
   // Independent fp32 accumulators per n-tile on the f16 route: consecutive
@@ -116,11 +115,22 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
 }
 
 // The per-thread copy of a CTA's work: K range and the weight boxes
-// (tensor-map rows, scale rows and groups), as resolve_work computes them.
+// (tensor-map rows, scale rows and groups).  Box b's rows lie in the 128-row
+// scale groups sgroup[2b] and (when it straddles a boundary) sgroup[2b + 1];
+// -1 marks none.  A stage holds the valid groups in this order, 2 KB each.
 struct RfWork {
   int paired, shared, expert, k_begin, k_end, kbp, out_base;
-  int wrow[2], srow[2], sgroup[3];
+  int wrow[2], srow[2], sgroup[4];
 };
+
+// Box b: weight rows [row, row + h), whose scales start at scale row `row`.
+__device__ __forceinline__ void rf_box(RfWork& w, int b, int row, int h, int groups_total) {
+  w.wrow[b] = row;
+  w.srow[b] = row;
+  const int g0 = row / 128, g1 = (row + h - 1) / 128;
+  w.sgroup[2 * b] = g0 < groups_total ? g0 : -1;
+  w.sgroup[2 * b + 1] = (g1 != g0 && g1 < groups_total) ? g1 : -1;
+}
 
 __device__ __forceinline__ void copy_work(const CtaWork& m, RfWork& w) {
   w.paired = m.paired;
@@ -134,9 +144,10 @@ __device__ __forceinline__ void copy_work(const CtaWork& m, RfWork& w) {
   w.wrow[1] = m.wrow[1];
   w.srow[0] = m.srow[0];
   w.srow[1] = m.srow[1];
-  w.sgroup[0] = m.sgroup[0];
-  w.sgroup[1] = m.sgroup[1];
-  w.sgroup[2] = m.sgroup[2];
+  w.sgroup[0] = m.sgroup[0];  // a 128-row box on a 128-row boundary: one group
+  w.sgroup[1] = -1;
+  w.sgroup[2] = m.sgroup[1];
+  w.sgroup[3] = m.sgroup[2];
 }
 
 // kMode: kDenseFp4 (nvfp4_gemv), kMoeGateUp or kMoeDown (the same modes and
@@ -170,6 +181,12 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
   const uint32_t rank = S > 1 ? cluster_ctarank() : 0;
   const int nstages = p.nstages;
 
+  // Dense tiles are 16 cw rows (cw consumer warps, chosen per call so the
+  // grid fills the GPU evenly): 16 cw features, or with silu_mul 8 cw gate
+  // rows and the 8 cw matching up rows.  MoE tiles are 128 rows.
+  const int cw = kDense ? p.cw : C::kConsumerWarps;
+  const int trows = 16 * cw;
+
   // ---- what this CTA computes (dense: every thread derives it) ----
   RfWork wk;
   wk.shared = 0;
@@ -179,18 +196,18 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
     wk.k_begin = static_cast<int>(rank) * p.k_split;
     wk.k_end = min(p.K, wk.k_begin + p.k_split);
     wk.kbp = p.kbp;
-    wk.sgroup[1] = wk.sgroup[2] = -1;
+    wk.sgroup[2] = wk.sgroup[3] = -1;
     wk.wrow[1] = wk.srow[1] = 0;
     const int groups_total = (p.rows_w + 127) / 128;
     if (p.silu) {
       wk.paired = 1;
-      wk.out_base = tile * 64;
-      set_box(wk, 0, tile * 64, tile * 64, groups_total);
-      set_box(wk, 1, p.n_half + tile * 64, p.n_half + tile * 64, groups_total);
+      wk.out_base = tile * (trows / 2);
+      rf_box(wk, 0, wk.out_base, trows / 2, groups_total);
+      rf_box(wk, 1, p.n_half + wk.out_base, trows / 2, groups_total);
     } else {
       wk.paired = 0;
-      wk.out_base = tile * 128;
-      set_box(wk, 0, tile * 128, tile * 128, groups_total);
+      wk.out_base = tile * trows;
+      rf_box(wk, 0, wk.out_base, trows, groups_total);
     }
   }
   const uint64_t pol_w = policy_evict_first();
@@ -203,23 +220,30 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
     const CUtensorMap* tmw = wk.shared ? &p.tm_w2 : &p.tm_w;
     const uint8_t* sfb =
         wk.shared ? p.sf2 : p.sf + (wk.expert >= 0 ? static_cast<size_t>(wk.expert) * p.sf_expert_bytes : 0);
-    uint32_t bytes = C::kWTileBytes;
+    uint32_t bytes = trows * 128;
 #pragma unroll
-    for (int g = 0; g < 3; ++g) bytes += (wk.sgroup[g] >= 0 ? nchunks * 512 : 0);
+    for (int g = 0; g < 4; ++g) bytes += (wk.sgroup[g] >= 0 ? nchunks * 512 : 0);
     asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(fb), "r"(bytes) : "memory");
     tma_load_2d(st, tmw, k0 / 2, wk.wrow[0], fb, pol_w);
-    if (wk.paired) tma_load_2d(st + C::kWTileBytes / 2, tmw, k0 / 2, wk.wrow[1], fb, pol_w);
+    if (wk.paired) tma_load_2d(st + trows * 64, tmw, k0 / 2, wk.wrow[1], fb, pol_w);
+    uint32_t sdst = st + trows * 128;  // the valid groups, in order
 #pragma unroll
-    for (int g = 0; g < 3; ++g) {
+    for (int g = 0; g < 4; ++g) {
       if (wk.sgroup[g] < 0) continue;
       const size_t chunk = static_cast<size_t>(wk.sgroup[g]) * (wk.kbp / 4) + k0 / 64;
-      bulk_load(st + C::kWTileBytes + g * 2048, sfb + chunk * 512, nchunks * 512, fb, pol_w);
+      bulk_load(sdst, sfb + chunk * 512, nchunks * 512, fb, pol_w);
+      sdst += 2048;
     }
   };
   // Output rows are reduced across cluster ranks per feature unit: a tile
-  // whose feature o combines rows o and o + 64 (paired gate/up boxes, routed
-  // [up; gate] groups) has 64-row units, any other tile 128-row units.
-  auto unit_of = [&]() { return (wk.paired || (kMode == kMoeGateUp && !wk.shared)) ? 64 : 128; };
+  // whose feature o combines rows o and o + unit (paired gate/up boxes, routed
+  // [up; gate] groups) has half-tile units and two rows per feature, any other
+  // tile one row per feature.
+  auto unit_of = [&]() {
+    if constexpr (kDense) return wk.paired ? trows / 2 : trows;
+    else return (wk.paired || (kMode == kMoeGateUp && !wk.shared)) ? 64 : 128;
+  };
+  auto rpf_of = [&]() { return trows / unit_of(); };
   auto stages_of = [&](bool act) { return act ? (wk.k_end - wk.k_begin + C::kStageK - 1) / C::kStageK : 0; };
 
   // ------------------------------------------------------------------ prologue
@@ -247,14 +271,14 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
     const bool f16 = C::kHasF16 && ntok0 <= C::kF16MaxM;
     for (int i = 0; i < nstages; ++i) {
       mbar_init(smem_u32(&bar_full[i]), f16 ? 2 : (kDense ? 1 : 33));
-      mbar_init(smem_u32(&bar_empty[i]), C::kConsumerWarps);
+      mbar_init(smem_u32(&bar_empty[i]), cw);
       mbar_init(smem_u32(&bar_xfull[i]), kDense ? 1 : 32);
       s_xbad[i] = -1;
     }
     mbar_init(smem_u32(&bar_inbox), 1);
     if (S > 1) {
       const int u = unit_of(), r = (u + static_cast<int>(S) - 1) / static_cast<int>(S);
-      const int mine0 = max(0, min(r, u - static_cast<int>(rank) * r)) * (128 / u);
+      const int mine0 = max(0, min(r, u - static_cast<int>(rank) * r)) * rpf_of();
       mbar_arrive_expect_tx(smem_u32(&bar_inbox), S * ntok0 * mine0 * 4);  // tokens < ntok only
     }
     mbar_fence_init();
@@ -277,7 +301,8 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
   const int R = (unit + static_cast<int>(S) - 1) / static_cast<int>(S);
   const int f_lo = static_cast<int>(rank) * R;
   const int f_hi = min(unit, f_lo + R);
-  const int mine = max(0, f_hi - f_lo) * (128 / unit);
+  const int rpf = rpf_of();  // rows per feature
+  const int mine = max(0, f_hi - f_lo) * rpf;
   const bool f16route = C::kHasF16 && ntok <= C::kF16MaxM;
 
   float acc[C::kChains][C::kTiles][4];  // main route's stages
@@ -393,10 +418,13 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
     const uint32_t w_off1 = (row1 / 8) * 1024 + (row1 % 8) * 128;
     // (static indices only, so the work description stays in registers)
     auto sf_off = [&](int row) -> uint32_t {
-      const bool b1 = wk.paired && row >= 64;
-      const int r = (b1 ? wk.srow[1] : wk.srow[0]) + (wk.paired ? row % 64 : row);
-      const int gslot = b1 ? 1 + (r / 128 - wk.srow[1] / 128) : 0;
-      return C::kWTileBytes + gslot * 2048 + (r % 32) * 16 + ((r % 128) / 32) * 4;
+      const int half = trows / 2;
+      const bool b1 = wk.paired && row >= half;
+      const int r = (b1 ? wk.srow[1] : wk.srow[0]) + (b1 ? row - half : row);
+      // stage slot of r's group: the valid groups are stored in order
+      const int g = r / 128;
+      const int gslot = b1 ? (wk.sgroup[0] >= 0) + (wk.sgroup[1] >= 0) + (g != wk.sgroup[2]) : (g != wk.sgroup[0]);
+      return trows * 128 + gslot * 2048 + (r % 32) * 16 + ((r % 128) / 32) * 4;
     };
     const uint32_t sf0 = sf_off(row0), sf1 = sf_off(row1);
     // global activation rows of this thread's B rows (f16 route's fallback)
@@ -515,7 +543,9 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
         }
       }
     };
-    for (int s = 0, slot = 0, ph = 0; s < nst; ++s, slot = slot + 1 == nstages ? 0 : slot + 1, ph ^= slot == 0) {
+    // (warps past cw own no rows of this tile: they skip the stream)
+    for (int s = 0, slot = 0, ph = 0; s < (warp < cw ? nst : 0);
+         ++s, slot = slot + 1 == nstages ? 0 : slot + 1, ph ^= slot == 0) {
       const uint32_t st = ring + slot * p.stage_bytes;
       const bool ok = __all_sync(0xFFFFFFFFu, !s_abort && mbar_wait(smem_u32(&bar_full[slot]), ph, p.err));
       if (!ok) {
@@ -572,12 +602,13 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
     const bool go = !s_abort;
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
+      if (warp >= cw) break;  // (rows past the tile)
       const int row = hr ? row1 : row0;
       const int fi = row % unit;
       const int owner = fi / R;
       const int owner_feats = min(R, unit - owner * R);
       const int rr = (row / unit) * owner_feats + (fi - owner * R);
-      const int rows_owner = owner_feats * (128 / unit);
+      const int rows_owner = owner_feats * rpf;
       const uint32_t base = inbox + ((rank * kNT) * rows_owner + rr) * 4;
       const uint32_t rbase = S > 1 ? mapa(base, static_cast<uint32_t>(owner)) : base;
       const uint32_t rbar = S > 1 ? mapa(smem_u32(&bar_inbox), static_cast<uint32_t>(owner)) : 0u;
@@ -614,7 +645,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
     const int nf = f_hi - f_lo;
     if (active && !s_abort && nf > 0) {
       pdl_wait();
-      if (unit == 128) {
+      if (rpf == 1) {
         // plain tiles: feature = tile row (dense out, or the down y scratch)
         float sc = 1.0f;
         uint16_t* dst = p.out;
