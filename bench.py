@@ -494,36 +494,34 @@ def run_extended(path, dev):
     tm = {}
     ex_gu = 2 * I * H // 2 + fp4gemv.scale_bytes(2 * I, H)
     ex_dn = H * I // 2 + fp4gemv.scale_bytes(H, I)
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    # Each kernel timed from a CUDA graph (host launch cost excluded, as for
+    # the dense layers) over R routings of the same batch size: every call
+    # touches other experts, so the ~8 experts of one call are not in L2 from
+    # the previous call.
+    R = 8
     for M in synth.MOE_M:
-        ids, tw = synth.routing(M, E, topk, seed=M, device=dev)
+        rts = [synth.routing(M, E, topk, seed=M * 1000 + r, device=dev) for r in range(R)]
         x = synth.activations(M, H, seed=M, device=dev)
         act = torch.empty(M * topk, I, dtype=torch.bfloat16, device=dev)
         sact = torch.empty(M, SI, dtype=torch.bfloat16, device=dev)
         out = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
-        distinct = int(torch.unique(ids).numel())
+        distinct = statistics.mean(int(torch.unique(ids).numel()) for ids, _ in rts)
         gu_b = (distinct + 1) * ex_gu + 2 * M * H + 2 * M * topk * I + 2 * M * SI + 4 * M * topk
         dn_b = (distinct + 1) * ex_dn + 2 * M * topk * I + 2 * M * SI + 2 * M * H + 8 * M * topk
-        t_gu, t_dn = [], []
-        for _ in range(10):
-            flush.zero_()  # evict the experts from L2 between timed calls
-            a, b, c2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
-            a.record(stream)
-            fp4gemv.moe_gate_up(x, ids, w1, w1_sf, alpha, act, wsh, ssh, gsh, sact)
-            b.record(stream)
-            fp4gemv.moe_down_combine(act, ids, tw, w2, w2_sf, alpha, sact, wsd, ssd, gsh, out)
-            c2.record(stream)
-            torch.cuda.synchronize()
-            t_gu.append(a.elapsed_time(b) * 1e3)
-            t_dn.append(b.elapsed_time(c2) * 1e3)
-        ug, ud = statistics.median(t_gu), statistics.median(t_dn)
-        tm[str(M)] = {"distinct_experts": distinct,
+        gu_fns = [lambda ids=ids: fp4gemv.moe_gate_up(x, ids, w1, w1_sf, alpha, act, wsh, ssh, gsh, sact)
+                  for ids, _ in rts]
+        dn_fns = [lambda ids=ids, tw=tw: fp4gemv.moe_down_combine(act, ids, tw, w2, w2_sf, alpha, sact, wsd, ssd,
+                                                                  gsh, out)
+                  for ids, tw in rts]
+        ug = time_calls(gu_fns, 2 * R, stream)
+        ud = time_calls(dn_fns, 2 * R, stream)
+        tm[str(M)] = {"distinct_experts": round(distinct, 1),
                       "gate_up": {"us": round(ug, 2), "GB/s": round(gu_b / (ug * 1e-6) / 1e9, 1),
                                   "frac": round(gu_b / (ug * 1e-6) / 1e9 / peak, 3)},
                       "down_combine": {"us": round(ud, 2), "GB/s": round(dn_b / (ud * 1e-6) / 1e9, 1),
                                        "frac": round(dn_b / (ud * 1e-6) / 1e9 / peak, 3)}}
     res["moe"] = tm
-    del w1, w2, w1_sf, w2_sf, flush
+    del w1, w2, w1_sf, w2_sf
 
     # M sweep on N = K = 8192: nvfp4_gemv vs dequantize_rows + bf16 GEMM
     N = K = synth.SWEEP_NK
