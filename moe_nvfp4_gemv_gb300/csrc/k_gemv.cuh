@@ -249,6 +249,10 @@ __device__ void resolve_work(const GemvParams& p, CtaWork& w, uint32_t split, in
       // gate_up runs right after the router: its ids are complete only after
       // the wait.  down_combine reads them early (they are two kernels old).
       if (kMode == kMoeGateUp) pdl_wait();
+      // ids of pairs 0 .. 63 (lane, lane + 32) load together with this
+      // column's, so resolving costs one global round trip for up to 64 pairs
+      const int id0 = lane < p.P ? __ldg(p.ids + lane) : -1;
+      const int id1 = lane + 32 < p.P ? __ldg(p.ids + lane + 32) : -1;
       const int e = __ldg(p.ids + col);
       bool live = tile < p.routed_tiles;
       if (live && (e < 0 || e >= p.E)) {
@@ -259,7 +263,7 @@ __device__ void resolve_work(const GemvParams& p, CtaWork& w, uint32_t split, in
       // chunk of kNT pairs computes the whole chunk.
       int cnt = 0;
       if (live)
-        for (int q = lane; q < col; q += 32) cnt += (__ldg(p.ids + q) == e);
+        for (int q = lane; q < col; q += 32) cnt += ((q < 32 ? id0 : q < 64 ? id1 : __ldg(p.ids + q)) == e);
       const int rank = __reduce_add_sync(0xFFFFFFFFu, cnt);
       live = live && rank % kNT == 0;
       if (!live) {
@@ -271,7 +275,10 @@ __device__ void resolve_work(const GemvParams& p, CtaWork& w, uint32_t split, in
       int n = 0;
       for (int q0 = col; q0 < p.P && n < kNT; q0 += 32) {
         const int q = q0 + lane;
-        const bool m = q < p.P && __ldg(p.ids + q) == e;
+        const int v0 = __shfl_sync(0xFFFFFFFFu, id0, q % 32);
+        const int v1 = __shfl_sync(0xFFFFFFFFu, id1, q % 32);
+        const int idq = q < 32 ? v0 : q < 64 ? v1 : (q < p.P ? __ldg(p.ids + q) : -1);
+        const bool m = q < p.P && idq == e;
         const unsigned bal = __ballot_sync(0xFFFFFFFFu, m);
         const int pos = n + __popc(bal & ((1u << lane) - 1u));
         if (m && pos < kNT) {
