@@ -485,13 +485,14 @@ fp4gemv_status fp4gemv_moe_gate_up(const void* x, const int32_t* ids, int M, int
   int sms = 0;
   fp4gemv_status st = device_state(&err, &sms);
   if (st != FP4GEMV_OK) return st;
-  // chunks of <= 16 tokens / pairs: the register-fed kernel; else tcgen05
-  // Register-fed kernel for up to 64 tokens: expert chunks hold at most 16
-  // pairs (more pairs routed to one expert form further chunks) and the
-  // shared expert runs ceil(M / 16) chunks; the tcgen05 kernel beyond.
+  // Register-fed kernel for up to 64 tokens: expert chunks hold at most 8
+  // pairs (more pairs routed to one expert form further chunks; with 8 of
+  // 128 experts per token an expert gets ~P / E pairs, a handful, so most
+  // chunks take the f16 route) and the shared expert runs ceil(M / 8)
+  // chunks; the tcgen05 kernel beyond.
   const bool rf = M <= 64;
   const int kmode = rf ? kMoeGateUpRf : fp4::kMoeGateUp;
-  const int NT = rf ? (M <= 8 ? 8 : 16) : 32;
+  const int NT = rf ? 8 : 32;
   KernelInfo info{};
   if (kernel_info(kmode, NT, &info) != cudaSuccess) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
   int nstages = 0, per_sm = 0, stage_bytes = 0, x_off = 0;
@@ -574,12 +575,11 @@ fp4gemv_status fp4gemv_moe_down_combine(const void* act, const int32_t* ids, con
   int sms = 0;
   fp4gemv_status st = device_state(&err, &sms);
   if (st != FP4GEMV_OK) return st;
-  // Register-fed kernel for up to 64 tokens: expert chunks hold at most 16
-  // pairs (more pairs routed to one expert form further chunks) and the
-  // shared expert runs ceil(M / 16) chunks; the tcgen05 kernel beyond.
+  // Register-fed kernel for up to 64 tokens, chunks of at most 8 pairs (as
+  // gate_up); the tcgen05 kernel beyond.
   const bool rf = M <= 64;
   const int kmode = rf ? kMoeDownRf : fp4::kMoeDown;
-  const int NT = rf ? (M <= 8 ? 8 : 16) : 32;
+  const int NT = rf ? 8 : 32;
   KernelInfo info{};
   if (kernel_info(kmode, NT, &info) != cudaSuccess) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
   int nstages = 0, per_sm = 0, stage_bytes = 0, x_off = 0;
