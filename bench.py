@@ -253,9 +253,21 @@ def run_gpu(args):
             reps.append((w, sf))
         weights[name] = reps
     gs = torch.tensor([GS], dtype=torch.float32, device=dev)
-    xs = {(name, M): synth.activations(M, LAYERS[name][1], seed=10 * M + 3, device=dev) for name in LAYERS for M in MS}
-    outs = {(name, M): torch.empty(M, LAYERS[name][0] // (2 if LAYERS[name][2] else 1), dtype=torch.bfloat16,
-                                   device=dev) for name in LAYERS for M in MS}
+    # The step's activations and outputs each live in one buffer (16-byte
+    # aligned views per call), so end to end a step is one host-to-device
+    # copy of its inputs and one device-to-host copy of its results.
+    def packed(shapes):
+        offs, n = {}, 0
+        for k, (r, c) in shapes.items():
+            offs[k] = n
+            n += (r * c + 7) // 8 * 8
+        flat = torch.empty(n, dtype=torch.bfloat16, device=dev)
+        return flat, {k: flat[o:o + r * c].view(r, c) for (k, (r, c)), o in zip(shapes.items(), offs.values())}
+    x_flat, xs = packed({(name, M): (M, LAYERS[name][1]) for name in LAYERS for M in MS})
+    for (name, M), v in xs.items():
+        v.copy_(synth.activations(M, LAYERS[name][1], seed=10 * M + 3, device=dev))
+    out_flat, outs = packed({(name, M): (M, LAYERS[name][0] // (2 if LAYERS[name][2] else 1))
+                             for name in LAYERS for M in MS})
     stream = torch.cuda.current_stream(dev)
 
     def step_with(r):
@@ -321,20 +333,19 @@ def run_gpu(args):
             del g
 
     # ---- end to end through the public API with pinned host buffers ----
-    host_x = {k: v.cpu().pin_memory() for k, v in xs.items()}
-    host_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in outs.items()}
-    h2d = sum(v.numel() * v.element_size() for v in host_x.values())
-    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+    host_x = x_flat.cpu().pin_memory()
+    host_out = torch.empty(out_flat.shape, dtype=out_flat.dtype).pin_memory()
+    h2d = host_x.numel() * host_x.element_size()
+    d2h = host_out.numel() * host_out.element_size()
 
     def e2e_with(r):
         def fn():
+            x_flat.copy_(host_x, non_blocking=True)  # the step's inputs
             for M in MS:
                 for name, (N, K, silu) in LAYERS.items():
                     w, sf = weights[name][r]
-                    xd = xs[(name, M)]
-                    xd.copy_(host_x[(name, M)], non_blocking=True)
-                    fp4gemv.nvfp4_gemv(xd, w, sf, gs, silu_mul=silu, pdl=True, out=outs[(name, M)])
-                    host_out[(name, M)].copy_(outs[(name, M)], non_blocking=True)
+                    fp4gemv.nvfp4_gemv(xs[(name, M)], w, sf, gs, silu_mul=silu, pdl=True, out=outs[(name, M)])
+            host_out.copy_(out_flat, non_blocking=True)  # the step's results
         return fn
 
     def timed(step_fns, nsteps):
