@@ -186,6 +186,28 @@ def test_llama70b_layers_sampled(fp4, name):
     _full_layer(fp4, N, K, silu, synth.LLAMA70B_M, seed=len(name), nsample=24)
 
 
+# Shapes whose grid uses tiles lower than 128 rows (gate_up of Llama-3-8B:
+# 48 features = 96 rows per tile; qkv of Llama-3-70B: 96-row tiles, K split
+# in two).  Every feature of the first 8 tiles (all positions of a box
+# against the 128-row scale groups, including boxes straddling two) and of
+# the ragged last tile is checked.
+@pytest.mark.parametrize("N,K,silu,feats", [(28672, 4096, 1, 48), (10240, 8192, 0, 96)])
+def test_short_tiles_all_features(fp4, N, K, silu, feats):
+    w = synth.fp4_bytes(N, K, seed=1)
+    sf = synth.e4m3_bytes(oracle.scale_bytes(N, K), seed=2)
+    wd, sd = w.to(DEV), sf.to(DEV)
+    gs = 0.01
+    n_out = N // 2 if silu else N
+    last = (n_out - 1) // feats * feats
+    rows = np.unique(np.concatenate([np.arange(8 * feats), np.arange(last, n_out)]))
+    wn, sn = w.numpy(), sf.numpy()
+    for M in (1, 3, 8, 16):
+        x = synth.activations(M, K, seed=11 + M)
+        got = fp4.nvfp4_gemv(x.to(DEV), wd, sd, torch.tensor([gs], device=DEV), silu_mul=silu)
+        ref = oracle.nvfp4_gemv(u16(x), wn, sn, gs, silu_mul=silu, rows=rows)
+        assert_close(u16(got)[:, rows], ref, f"N={N} K={K} silu={silu} M={M}")
+
+
 @pytest.mark.parametrize("name", list(synth.LLAMA70B_LAYERS))
 def test_llama70b_dequantize_rows_sampled(fp4, name):
     N, K, _ = synth.LLAMA70B_LAYERS[name]
