@@ -161,6 +161,7 @@ constexpr int kRfBase = 100;
 constexpr int kDenseFp4Rf = kRfBase + fp4::kDenseFp4;
 constexpr int kMoeGateUpRf = kRfBase + fp4::kMoeGateUp;
 constexpr int kMoeDownRf = kRfBase + fp4::kMoeDown;
+constexpr int kMoeDownRf3 = kRfBase + 10 + fp4::kMoeDown;  // budgeted for three CTAs per SM
 
 cudaError_t kernel_info(int mode, int nt, KernelInfo* info) {
   GemvParams dummy;
@@ -169,6 +170,7 @@ cudaError_t kernel_info(int mode, int nt, KernelInfo* info) {
     case kDenseFp4Rf:
     case kMoeGateUpRf:
     case kMoeDownRf: return fp4::launch_rf(mode - kRfBase, nt, dummy, cfg, info);
+    case kMoeDownRf3: return fp4::launch_rf_occ3(fp4::kMoeDown, nt, dummy, cfg, info);
     case fp4::kDenseFp4: return fp4::launch_dense_fp4(nt, dummy, cfg, info);
     case fp4::kDenseBf16: return fp4::launch_dense_bf16(nt, dummy, cfg, info);
     default: return fp4::launch_moe(mode, nt, dummy, cfg, info);
@@ -181,6 +183,7 @@ cudaError_t kernel_launch(int mode, int nt, const GemvParams& p, const LaunchCfg
     case kDenseFp4Rf:
     case kMoeGateUpRf:
     case kMoeDownRf: return fp4::launch_rf(mode - kRfBase, nt, p, cfg, nullptr);
+    case kMoeDownRf3: return fp4::launch_rf_occ3(fp4::kMoeDown, nt, p, cfg, nullptr);
     case fp4::kDenseFp4: return fp4::launch_dense_fp4(nt, p, cfg, nullptr);
     case fp4::kDenseBf16: return fp4::launch_dense_bf16(nt, p, cfg, nullptr);
     default: return fp4::launch_moe(mode, nt, p, cfg, nullptr);
@@ -212,8 +215,7 @@ void size_ring(const KernelInfo& info, int* nstages, size_t* smem, int* ctas_per
 constexpr int kRfBudget = 110 * 1024;  // shared memory per register-fed CTA, two per SM (with margin)
 
 void size_ring_rf(const KernelInfo& info, int wtile_bytes, int sf_groups, int* nstages, size_t* smem,
-                  int* stage_bytes, int* x_off) {
-  constexpr int kBudget = kRfBudget;
+                  int* stage_bytes, int* x_off, int kBudget = kRfBudget) {
   *x_off = wtile_bytes + sf_groups * 2048;
   *stage_bytes = (*x_off + info.stage_bytes + 1023) / 1024 * 1024;
   int ns = (kBudget - 1024 - info.inbox_bytes) / *stage_bytes;
@@ -576,15 +578,18 @@ fp4gemv_status fp4gemv_moe_down_combine(const void* act, const int32_t* ids, con
   fp4gemv_status st = device_state(&err, &sms);
   if (st != FP4GEMV_OK) return st;
   // Register-fed kernel for up to 64 tokens, chunks of at most 8 pairs (as
-  // gate_up); the tcgen05 kernel beyond.
+  // gate_up); the tcgen05 kernel beyond.  From 8 tokens the grid holds many
+  // short CTAs (K = I is a few stages): the variant budgeted for three CTAs
+  // per SM (72 KB ring) hides more of their fixed costs.
   const bool rf = M <= 64;
-  const int kmode = rf ? kMoeDownRf : fp4::kMoeDown;
+  const bool occ3 = rf && M >= 8;
+  const int kmode = rf ? (occ3 ? kMoeDownRf3 : kMoeDownRf) : fp4::kMoeDown;
   const int NT = rf ? 8 : 32;
   KernelInfo info{};
   if (kernel_info(kmode, NT, &info) != cudaSuccess) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
   int nstages = 0, per_sm = 0, stage_bytes = 0, x_off = 0;
   size_t smem = 0;
-  if (rf) size_ring_rf(info, 128 * 128, 1, &nstages, &smem, &stage_bytes, &x_off);
+  if (rf) size_ring_rf(info, 128 * 128, 1, &nstages, &smem, &stage_bytes, &x_off, occ3 ? 72 * 1024 : kRfBudget);
   else size_ring(info, &nstages, &smem, &per_sm);
   GemvParams p;
   std::memset(&p, 0, sizeof(p));

@@ -7,9 +7,9 @@ namespace fp4 {
 
 // Raise the kernel's dynamic shared-memory limit to `smem` (once per device
 // and size).
-template <int kMode, int kNT>
+template <int kMode, int kNT, int kOcc = 2>
 cudaError_t configure_rf(size_t smem, unsigned cluster) {
-  auto k = gemv_rf_kernel<kMode, kNT>;
+  auto k = gemv_rf_kernel<kMode, kNT, kOcc>;
   static int configured_smem[64];  // per device (0 = not yet)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -24,7 +24,7 @@ cudaError_t configure_rf(size_t smem, unsigned cluster) {
   return cudaSuccess;
 }
 
-template <int kMode, int kNT>
+template <int kMode, int kNT, int kOcc = 2>
 cudaError_t run_gemv_rf(const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info) {
   using C = RfCfg<kNT>;
   if (info) {
@@ -35,9 +35,9 @@ cudaError_t run_gemv_rf(const GemvParams& p, const LaunchCfg& cfg, KernelInfo* i
     info->tmem_cols = 0;
     return cudaSuccess;
   }
-  cudaError_t e = configure_rf<kMode, kNT>(cfg.smem, cfg.cluster);
+  cudaError_t e = configure_rf<kMode, kNT, kOcc>(cfg.smem, cfg.cluster);
   if (e != cudaSuccess) return e;
-  return launch_kernel(gemv_rf_kernel<kMode, kNT>, C::kThreads, p, cfg);
+  return launch_kernel(gemv_rf_kernel<kMode, kNT, kOcc>, C::kThreads, p, cfg);
 }
 
 template <int kMode, int kNT>
@@ -73,6 +73,11 @@ cudaError_t launch_rf(int mode, int nt, const GemvParams& p, const LaunchCfg& cf
   FP4_CASE(kMoeGateUp, 8) FP4_CASE(kMoeGateUp, 16)
   FP4_CASE(kMoeDown, 8) FP4_CASE(kMoeDown, 16)
 #undef FP4_CASE
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_rf_occ3(int mode, int nt, const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info) {
+  if (mode == kMoeDown && nt == 8) return run_gemv_rf<kMoeDown, 8, 3>(p, cfg, info);
   return cudaErrorInvalidValue;
 }
 

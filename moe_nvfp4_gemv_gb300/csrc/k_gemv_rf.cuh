@@ -152,9 +152,13 @@ __device__ __forceinline__ void copy_work(const CtaWork& m, RfWork& w) {
 
 // kMode: kDenseFp4 (nvfp4_gemv), kMoeGateUp or kMoeDown (the same modes and
 // epilogues as the tcgen05 kernel, for chunks of at most 16 tokens / pairs).
-template <int kMode, int kNT>
-__global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const __grid_constant__ GemvParams p) {
+// kOcc: CTAs per SM the registers are budgeted for.  2 by default; 3 (two
+// accumulator chains, 64 registers, the host gives it a 72 KB ring) for
+// grids of many short CTAs, whose fixed costs more co-resident CTAs hide.
+template <int kMode, int kNT, int kOcc = 2>
+__global__ void __launch_bounds__(RfCfg<kNT>::kThreads, kOcc) gemv_rf_kernel(const __grid_constant__ GemvParams p) {
   using C = RfCfg<kNT>;
+  constexpr int kChains = kOcc >= 3 && C::kChains > 2 ? 2 : C::kChains;
   constexpr bool kDense = kMode == kDenseFp4;
   constexpr int kEpiThreads = C::kConsumerWarps * 32;
 
@@ -305,14 +309,14 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
   const int mine = max(0, f_hi - f_lo) * rpf;
   const bool f16route = C::kHasF16 && ntok <= C::kF16MaxM;
 
-  float acc[C::kChains][C::kTiles][4];  // main route's stages
+  float acc[kChains][C::kTiles][4];  // main route's stages
   float accb[C::kHasF16 ? C::kTiles : 1][4];  // f16 route: fallback stages (bf16, products times 2^-kShift)
 #pragma unroll
   for (int t = 0; t < C::kTiles; ++t) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
 #pragma unroll
-      for (int q = 0; q < C::kChains; ++q) acc[q][t][e] = 0.0f;
+      for (int q = 0; q < kChains; ++q) acc[q][t][e] = 0.0f;
     }
   }
 #pragma unroll
@@ -466,8 +470,8 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
           const uint4 xv = lds128_if(st + p.x_off + u * (kNT * 128) + (n / 8) * 1024 + (n % 8) * 128 +
                                          ((ch ^ static_cast<uint32_t>(n % 8)) * 16),
                                      n < ntok);
-          mma_f16_16816(acc[(2 * w) % C::kChains][t], r0[0], r1[0], r0[1], r1[1], xv.x, xv.y);
-          mma_f16_16816(acc[(2 * w + 1) % C::kChains][t], r0[2], r1[2], r0[3], r1[3], xv.z, xv.w);
+          mma_f16_16816(acc[(2 * w) % kChains][t], r0[0], r1[0], r0[1], r1[1], xv.x, xv.y);
+          mma_f16_16816(acc[(2 * w + 1) % kChains][t], r0[2], r1[2], r0[3], r1[3], xv.z, xv.w);
         }
       }
     };
@@ -503,8 +507,8 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
           const uint4 xv = perm_x8(lds128_if(st + p.x_off + u * (kNT * 128) + (n / 8) * 1024 + (n % 8) * 128 +
                                                  ((ch ^ static_cast<uint32_t>(n % 8)) * 16),
                                              n < ntok));
-          mma_bf16_16816(acc[(2 * w) % C::kChains][t], r0[0], r1[0], r0[1], r1[1], xv.x, xv.y);
-          mma_bf16_16816(acc[(2 * w + 1) % C::kChains][t], r0[2], r1[2], r0[3], r1[3], xv.z, xv.w);
+          mma_bf16_16816(acc[(2 * w) % kChains][t], r0[0], r1[0], r0[1], r1[1], xv.x, xv.y);
+          mma_bf16_16816(acc[(2 * w + 1) % kChains][t], r0[2], r1[2], r0[3], r1[3], xv.z, xv.w);
         }
       }
     };
@@ -619,7 +623,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, 2) gemv_rf_kernel(const 
           const int n = 8 * t + 2 * c + e;
           float a16 = 0.0f;
 #pragma unroll
-          for (int q = 0; q < C::kChains; ++q) a16 += acc[q][t][2 * hr + e];
+          for (int q = 0; q < kChains; ++q) a16 += acc[q][t][2 * hr + e];
           // acc holds the main route's products (exact on the f16 route,
           // times 2^-kShift on the bf16 route); accb the f16 route's fallback
           if (!f16route) a16 *= post;
