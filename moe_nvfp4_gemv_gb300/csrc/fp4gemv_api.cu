@@ -10,6 +10,7 @@
 #include <cstring>
 
 #include "fp4gemv.h"
+#include "fp4gemv_plan.h"
 #include "launch.h"
 
 namespace fp4 {
@@ -316,6 +317,21 @@ int pick_split(int tiles, int K, int stage_k, int slots) {
   return best;
 }
 
+// The register-fed dense kernel's plan (tile height 16 cw, split, scale
+// groups per stage) for N x K on a GPU with `sms` SMs and cap[] co-resident
+// CTAs per cluster size.
+void plan_rf(int N, int K, bool silu, int sms, const int (&cap)[9], int* cw, int* s0, int* sf_groups) {
+  const int n_out = silu ? N / 2 : N;
+  const int s_default = pick_split((n_out + (silu ? 63 : 127)) / (silu ? 64 : 128), K, fp4::kStageK4, sms * 2);
+  pick_rf_geometry(n_out, silu, K, s_default, cap, cw, s0);
+  // 128-row scale groups a stage holds: a box of h rows starting at an
+  // offset o (mod h) stays in one group for every tile iff h divides 128
+  // and o is a multiple of h
+  const int h = silu ? 8 * *cw : 16 * *cw;
+  const bool even = 128 % h == 0;
+  *sf_groups = silu ? (even ? 1 : 2) + ((even && (N / 2) % h == 0) ? 1 : 2) : (even ? 1 : 2);
+}
+
 fp4gemv_status dense_launch(int mode, const void* x, int64_t ldx, const void* w, const uint8_t* w_sf,
                             const float* gs, void* out, int64_t ldo, int M, int N, int K, int silu_mul, int pdl,
                             cudaStream_t stream) {
@@ -356,15 +372,8 @@ fp4gemv_status dense_launch(int mode, const void* x, int64_t ldx, const void* w,
     int cap[9];
     st = rf_capacity(NT, cap);
     if (st != FP4GEMV_OK) return st;
-    const int s_default =
-        pick_split((n_out + (silu_mul ? 63 : 127)) / (silu_mul ? 64 : 128), K, fp4::kStageK4, sms * per_sm);
-    pick_rf_geometry(n_out, silu_mul != 0, K, s_default, cap, &cw, &S0);
-    // 128-row scale groups a stage holds: a box of h rows starting at an
-    // offset o (mod h) stays in one group for every tile iff h divides 128
-    // and o is a multiple of h
-    const int h = silu_mul ? 8 * cw : 16 * cw;
-    const bool even = 128 % h == 0;
-    const int sf_groups = silu_mul ? (even ? 1 : 2) + ((even && (N / 2) % h == 0) ? 1 : 2) : (even ? 1 : 2);
+    int sf_groups = 1;
+    plan_rf(N, K, silu_mul != 0, sms, cap, &cw, &S0, &sf_groups);
     size_ring_rf(info, 16 * cw * 128, sf_groups, &nstages, &smem, &stage_bytes, &x_off);
   } else {
     size_ring(info, &nstages, &smem, &per_sm);
@@ -423,6 +432,24 @@ fp4gemv_status dense_launch(int mode, const void* x, int64_t ldx, const void* w,
 }  // namespace
 
 extern "C" {
+
+fp4gemv_status fp4gemv_plan_rf(int N, int K, int silu_mul, int sms, const int* cap, fp4gemv_rf_plan* out) {
+  if (!cap || !out || sms < 1 || (silu_mul != 0 && silu_mul != 1) || N < 1 || K < 1) return FP4GEMV_ERR_INVALID_ARG;
+  if (N % 16 != 0 || (silu_mul && N % 32 != 0) || K % 64 != 0 || K < 256) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
+  int c[9];
+  for (int s = 0; s < 9; ++s) c[s] = s == 0 ? 0 : cap[s];
+  int cw = 8, s0 = 1, groups = 1;
+  plan_rf(N, K, silu_mul != 0, sms, c, &cw, &s0, &groups);
+  const int feats = silu_mul ? 8 * cw : 16 * cw;
+  const int n_out = silu_mul ? N / 2 : N;
+  const int kslab = ((K + s0 - 1) / s0 + 63) / 64 * 64;
+  const int split = (K + kslab - 1) / kslab;
+  out->tile_rows = 16 * cw;
+  out->split = split;
+  out->ctas = (n_out + feats - 1) / feats * split;
+  out->scale_groups = groups;
+  return FP4GEMV_OK;
+}
 
 size_t fp4gemv_scale_bytes(int rows, int K) {
   if (rows < 1 || K < 16) return 0;

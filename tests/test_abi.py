@@ -1,7 +1,8 @@
 """The C ABI without a GPU: the library builds/loads, exports every function
-include/fp4gemv.h declares, and rejects bad arguments on the host with the
-documented status before touching the device."""
+the headers in include/ declare, and rejects bad arguments on the host with
+the documented status before touching the device."""
 import ctypes
+import glob
 import os
 import re
 
@@ -10,7 +11,7 @@ import pytest
 import oracle
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "fp4gemv.h")
+HEADERS = sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
 
 
 @pytest.fixture(scope="module")
@@ -20,16 +21,18 @@ def fp4():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(fp4gemv_[a-z0-9_]+)\s*\(", text)))
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names.update(re.findall(r"\b(fp4gemv_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_the_boundary():
     names = declared_functions()
     for want in ("fp4gemv_nvfp4_gemv", "fp4gemv_bf16_gemv", "fp4gemv_dequantize_rows", "fp4gemv_moe_gate_up",
                  "fp4gemv_moe_down_combine", "fp4gemv_scale_bytes", "fp4gemv_get_device_error",
-                 "fp4gemv_status_string"):
+                 "fp4gemv_status_string", "fp4gemv_plan_rf"):
         assert want in names
 
 
