@@ -163,6 +163,7 @@ constexpr int kDenseFp4Rf = kRfBase + fp4::kDenseFp4;
 constexpr int kMoeGateUpRf = kRfBase + fp4::kMoeGateUp;
 constexpr int kMoeDownRf = kRfBase + fp4::kMoeDown;
 constexpr int kMoeDownRf3 = kRfBase + 10 + fp4::kMoeDown;  // budgeted for three CTAs per SM
+constexpr int kDenseFp4RfCoop = kRfBase + 20 + fp4::kDenseFp4;  // 5 .. 8 tokens, cooperative f16 conversion
 
 cudaError_t kernel_info(int mode, int nt, KernelInfo* info) {
   GemvParams dummy;
@@ -172,6 +173,7 @@ cudaError_t kernel_info(int mode, int nt, KernelInfo* info) {
     case kMoeGateUpRf:
     case kMoeDownRf: return fp4::launch_rf(mode - kRfBase, nt, dummy, cfg, info);
     case kMoeDownRf3: return fp4::launch_rf_occ3(fp4::kMoeDown, nt, dummy, cfg, info);
+    case kDenseFp4RfCoop: return fp4::launch_rf_coop(fp4::kDenseFp4, nt, dummy, cfg, info);
     case fp4::kDenseFp4: return fp4::launch_dense_fp4(nt, dummy, cfg, info);
     case fp4::kDenseBf16: return fp4::launch_dense_bf16(nt, dummy, cfg, info);
     default: return fp4::launch_moe(mode, nt, dummy, cfg, info);
@@ -185,6 +187,7 @@ cudaError_t kernel_launch(int mode, int nt, const GemvParams& p, const LaunchCfg
     case kMoeGateUpRf:
     case kMoeDownRf: return fp4::launch_rf(mode - kRfBase, nt, p, cfg, nullptr);
     case kMoeDownRf3: return fp4::launch_rf_occ3(fp4::kMoeDown, nt, p, cfg, nullptr);
+    case kDenseFp4RfCoop: return fp4::launch_rf_coop(fp4::kDenseFp4, nt, p, cfg, nullptr);
     case fp4::kDenseFp4: return fp4::launch_dense_fp4(nt, p, cfg, nullptr);
     case fp4::kDenseBf16: return fp4::launch_dense_bf16(nt, p, cfg, nullptr);
     default: return fp4::launch_moe(mode, nt, p, cfg, nullptr);
@@ -357,7 +360,7 @@ fp4gemv_status dense_launch(int mode, const void* x, int64_t ldx, const void* w,
   // otherwise the tcgen05 kernel (at 32 tokens the register-fed kernel is
   // bound by its MMA count and no faster).
   const bool rf = fp4w && M <= 16;
-  const int kmode = rf ? kDenseFp4Rf : mode;
+  const int kmode = rf ? (M > 4 && M <= 8 ? kDenseFp4RfCoop : kDenseFp4Rf) : mode;
   const int NT = rf ? (M <= 8 ? 8 : 16) : pick_nt(M);
   KernelInfo info{};
   if (kernel_info(kmode, NT, &info) != cudaSuccess) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;

@@ -7,9 +7,9 @@ namespace fp4 {
 
 // Raise the kernel's dynamic shared-memory limit to `smem` (once per device
 // and size).
-template <int kMode, int kNT, int kOcc = 2>
+template <int kMode, int kNT, int kOcc = 2, bool kCoop = false>
 cudaError_t configure_rf(size_t smem, unsigned cluster) {
-  auto k = gemv_rf_kernel<kMode, kNT, kOcc>;
+  auto k = gemv_rf_kernel<kMode, kNT, kOcc, kCoop>;
   static int configured_smem[64];  // per device (0 = not yet)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -24,7 +24,7 @@ cudaError_t configure_rf(size_t smem, unsigned cluster) {
   return cudaSuccess;
 }
 
-template <int kMode, int kNT, int kOcc = 2>
+template <int kMode, int kNT, int kOcc = 2, bool kCoop = false>
 cudaError_t run_gemv_rf(const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info) {
   using C = RfCfg<kNT>;
   if (info) {
@@ -35,14 +35,14 @@ cudaError_t run_gemv_rf(const GemvParams& p, const LaunchCfg& cfg, KernelInfo* i
     info->tmem_cols = 0;
     return cudaSuccess;
   }
-  cudaError_t e = configure_rf<kMode, kNT, kOcc>(cfg.smem, cfg.cluster);
+  cudaError_t e = configure_rf<kMode, kNT, kOcc, kCoop>(cfg.smem, cfg.cluster);
   if (e != cudaSuccess) return e;
-  return launch_kernel(gemv_rf_kernel<kMode, kNT, kOcc>, C::kThreads, p, cfg);
+  return launch_kernel(gemv_rf_kernel<kMode, kNT, kOcc, kCoop>, C::kThreads, p, cfg);
 }
 
-template <int kMode, int kNT>
+template <int kMode, int kNT, bool kCoop = false>
 cudaError_t rf_clusters(unsigned cluster, size_t smem, int* n) {
-  cudaError_t e = configure_rf<kMode, kNT>(smem, cluster);
+  cudaError_t e = configure_rf<kMode, kNT, 2, kCoop>(smem, cluster);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t c = {};
   c.gridDim = dim3(cluster, 1, 1);
@@ -55,7 +55,7 @@ cudaError_t rf_clusters(unsigned cluster, size_t smem, int* n) {
   a[0].val.clusterDim.z = 1;
   c.attrs = a;
   c.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(n, gemv_rf_kernel<kMode, kNT>, &c);
+  return cudaOccupancyMaxActiveClusters(n, gemv_rf_kernel<kMode, kNT, 2, kCoop>, &c);
 }
 
 cudaError_t rf_max_clusters(int mode, int nt, unsigned cluster, size_t smem, int* n) {
@@ -78,6 +78,11 @@ cudaError_t launch_rf(int mode, int nt, const GemvParams& p, const LaunchCfg& cf
 
 cudaError_t launch_rf_occ3(int mode, int nt, const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info) {
   if (mode == kMoeDown && nt == 8) return run_gemv_rf<kMoeDown, 8, 3>(p, cfg, info);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_rf_coop(int mode, int nt, const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info) {
+  if (mode == kDenseFp4 && nt == 8) return run_gemv_rf<kDenseFp4, 8, 2, true>(p, cfg, info);
   return cudaErrorInvalidValue;
 }
 

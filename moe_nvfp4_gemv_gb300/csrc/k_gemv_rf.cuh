@@ -98,6 +98,19 @@ __device__ __forceinline__ uint4 lds128_if(uint32_t a, bool on) {
   return v;
 }
 
+// Named barrier `id` over `count` threads that returns whether any of them
+// passed `pred` true (also orders their shared-memory accesses).
+template <int id>
+__device__ __forceinline__ bool bar_red_or(uint32_t count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.or.pred q, %2, %3, p; selp.u32 %0, 1, 0, q; }"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "n"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
 __device__ __forceinline__ uint32_t lds16(uint32_t a) {
   unsigned short v;
   asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
@@ -155,7 +168,10 @@ __device__ __forceinline__ void copy_work(const CtaWork& m, RfWork& w) {
 // kOcc: CTAs per SM the registers are budgeted for.  2 by default; 3 (two
 // accumulator chains, 64 registers, the host gives it a 72 KB ring) for
 // grids of many short CTAs, whose fixed costs more co-resident CTAs hide.
-template <int kMode, int kNT, int kOcc = 2>
+// kCoop: the variant for 5 .. 8 tokens whose consumer warps convert the
+// activations to f16 together (a separate instantiation, so the others'
+// code is unchanged by it).
+template <int kMode, int kNT, int kOcc = 2, bool kCoop = false>
 __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, kOcc) gemv_rf_kernel(const __grid_constant__ GemvParams p) {
   using C = RfCfg<kNT>;
   constexpr int kChains = kOcc >= 3 && C::kChains > 2 ? 2 : C::kChains;
@@ -308,6 +324,11 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, kOcc) gemv_rf_kernel(con
   const int rpf = rpf_of();  // rows per feature
   const int mine = max(0, f_hi - f_lo) * rpf;
   const bool f16route = C::kHasF16 && ntok <= C::kF16MaxM;
+  // kF16MaxM < ntok <= 8: the consumer warps convert each stage's activations
+  // to f16 together (one 16-byte chunk or two per thread) and agree on
+  // exactness at a barrier; one converter warp would not keep up with 8 rows.
+  const bool coop = kCoop && C::kHasF16 && ntok > C::kF16MaxM;
+  const bool f16acc = f16route || coop;  // acc holds exact f16-route products
 
   float acc[kChains][C::kTiles][4];  // main route's stages
   float accb[C::kHasF16 ? C::kTiles : 1][4];  // f16 route: fallback stages (bf16, products times 2^-kShift)
@@ -547,20 +568,56 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, kOcc) gemv_rf_kernel(con
         }
       }
     };
+    // Cooperative f16 conversion of a stage's activation rows < ntok (the
+    // consumer warps' threads take chunks round-robin), then a barrier that
+    // ORs "inexact or gave up" over them: 0 = every value exact (f16 route),
+    // 1 = some value inexact (bf16 fallback), 2 = a warp's wait gave up (all
+    // leave the loop).  A thread whose wait gave up still joins, so no warp is
+    // left at the barrier, and the decision to leave comes from the barrier,
+    // the same for every warp.
+    auto coop_convert = [&](uint32_t st, int kvalid, bool gave_up) -> int {
+      bool bad = gave_up;
+      if (!gave_up) {
+        for (int id = warp * 32 + lane; id < ntok * 32; id += cw * 32) {
+          const int n = id / 32, q = id % 32;
+          if (8 * q >= kvalid) continue;
+          const uint32_t a = st + p.x_off + (q / 8) * (kNT * 128) + (n / 8) * 1024 + (n % 8) * 128 +
+                             ((static_cast<uint32_t>(q % 8) ^ static_cast<uint32_t>(n % 8)) * 16);
+          const uint4 v = lds128(a);
+          uint4 o;
+          bool exact = bf16x2_to_f16x2_exact(v.x, o.x);
+          exact &= bf16x2_to_f16x2_exact(v.y, o.y);
+          exact &= bf16x2_to_f16x2_exact(v.z, o.z);
+          exact &= bf16x2_to_f16x2_exact(v.w, o.w);
+          sts128(a, o);
+          bad |= !exact;
+        }
+        fence_proxy_async_smem();  // these writes precede the slot's next TMA fill
+      }
+      if (!bar_red_or<2>(cw * 32, bad)) return 0;
+      return bar_red_or<2>(cw * 32, gave_up) ? 2 : 1;  // (every thread takes this branch or none)
+    };
     // (warps past cw own no rows of this tile: they skip the stream)
     for (int s = 0, slot = 0, ph = 0; s < (warp < cw ? nst : 0);
          ++s, slot = slot + 1 == nstages ? 0 : slot + 1, ph ^= slot == 0) {
       const uint32_t st = ring + slot * p.stage_bytes;
       const bool ok = __all_sync(0xFFFFFFFFu, !s_abort && mbar_wait(smem_u32(&bar_full[slot]), ph, p.err));
-      if (!ok) {
-        s_abort = 1;
-        break;
-      }
+      if (!ok) s_abort = 1;
       // valid K of the stage: 64 .. 256 in steps of 64; a chunk (32 K) is
       // wholly valid or wholly past the end, where its A registers are zero
       // (its scales were not copied and may hold anything)
       const int kvalid = min(C::kStageK, wk.k_end - wk.k_begin - s * C::kStageK);
-      if (!f16route) {
+      bool use_f16 = false;
+      if (coop) {
+        const int r = coop_convert(st, kvalid, !ok);
+        if (r == 2) break;
+        use_f16 = r == 0;
+      } else if (!ok) {
+        break;
+      } else if (f16route) {
+        use_f16 = s_xbad[slot] != s;  // bar_full included the converter's arrival
+      }
+      if (!f16acc) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           if (128 * h < kvalid) {
@@ -568,28 +625,23 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, kOcc) gemv_rf_kernel(con
             else half_bf16_smem(st, h, 32 * (4 * h + c) < kvalid);
           }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bar_empty[slot]));
-        continue;
-      }
-      if constexpr (C::kHasF16) {
-      // (bar_full included the converter's arrival: the activations are f16)
-      if (s_xbad[slot] != s) {
+      } else if constexpr (C::kHasF16) {
+        if (use_f16) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          if (128 * h < kvalid) {
-            if (128 * (h + 1) <= kvalid) half_f16(st, h, true);
-            else half_f16(st, h, 32 * (4 * h + c) < kvalid);
+          for (int h = 0; h < 2; ++h) {
+            if (128 * h < kvalid) {
+              if (128 * (h + 1) <= kvalid) half_f16(st, h, true);
+              else half_f16(st, h, 32 * (4 * h + c) < kvalid);
+            }
+          }
+        } else {
+          pdl_wait();  // the activations are read from global memory directly
+          const int k0 = wk.k_begin + s * C::kStageK;
+#pragma unroll 1
+          for (int h = 0; h < 2; ++h) {
+            if (128 * h < kvalid) half_bf16(st, k0, h, 32 * (4 * h + c) < kvalid);
           }
         }
-      } else {
-        pdl_wait();  // the activations are read from global memory directly
-        const int k0 = wk.k_begin + s * C::kStageK;
-#pragma unroll 1
-        for (int h = 0; h < 2; ++h) {
-          if (128 * h < kvalid) half_bf16(st, k0, h, 32 * (4 * h + c) < kvalid);
-        }
-      }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bar_empty[slot]));
@@ -626,7 +678,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, kOcc) gemv_rf_kernel(con
           for (int q = 0; q < kChains; ++q) a16 += acc[q][t][2 * hr + e];
           // acc holds the main route's products (exact on the f16 route,
           // times 2^-kShift on the bf16 route); accb the f16 route's fallback
-          if (!f16route) a16 *= post;
+          if (!f16acc) a16 *= post;
           if constexpr (C::kHasF16) a16 += accb[t][2 * hr + e] * post;
           const float v = go ? a16 : 0.0f;
           const uint32_t off = n * rows_owner * 4;
