@@ -8,7 +8,10 @@
 // 32 * (c % (K/32))): loads and stores are fully coalesced, 128-bit wide.
 // Scales are read through the read-only path from the 128x4 layout; one
 // chunk needs the scales of two consecutive 16-blocks, which are adjacent
-// bytes there.
+// bytes there.  A warp's 32 chunks are consecutive, so their outputs are one
+// contiguous 2 KB block: each thread's 64 bytes go through shared memory and
+// come back out as four warp-wide stores of 512 contiguous bytes (whole 32-byte
+// sectors), instead of 16-byte stores that each half-fill 64 sectors.
 #pragma once
 
 #include "common.cuh"
@@ -27,9 +30,14 @@ __global__ void __launch_bounds__(kDqThreads) dequantize_rows_kernel(const uint4
                                                                     const uint8_t* __restrict__ sf,
                                                                     uint4* __restrict__ out, uint64_t nchunks,
                                                                     uint32_t chunks_per_row, uint32_t kbp) {
+  __shared__ __align__(16) uint4 stage[kDqThreads / 32][128];  // 2 KB per warp
+  const int lane = threadIdx.x % 32;
+  uint4* const ws = stage[threadIdx.x / 32];
   const uint64_t stride = static_cast<uint64_t>(gridDim.x) * kDqThreads;
   uint64_t c = static_cast<uint64_t>(blockIdx.x) * kDqThreads + threadIdx.x;
-  for (; c < nchunks; c += stride * kDqUnroll) {
+  // (the warp iterates together: its __syncwarp()s need every lane; each
+  // chunk is bounds-checked)
+  for (; c - lane < nchunks; c += stride * kDqUnroll) {
     uint4 q[kDqUnroll];
     uint32_t s2[kDqUnroll];
 #pragma unroll
@@ -49,7 +57,6 @@ __global__ void __launch_bounds__(kDqThreads) dequantize_rows_kernel(const uint4
         uint32_t s_lo, s_hi;
         scale_pair_to_bf16x2(s2[u], s_lo, s_hi);
         const uint32_t words[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
-        uint4* dst = out + cc * 4;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           uint32_t r[4], p[4], o[4];
@@ -58,9 +65,22 @@ __global__ void __launch_bounds__(kDqThreads) dequantize_rows_kernel(const uint4
 #pragma unroll
           for (int j = 0; j < 4; ++j) p[j] = bf16x2_mul(bf16x2_mul(r[j], s), 0x43804380u);  // * 2^kShift
           unperm4(p, o);
-          dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+          // 16-byte piece 4 lane + i of the warp's block; the XOR spreads
+          // a store instruction's 32 pieces over all banks
+          ws[(4 * lane + i) ^ ((lane >> 1) & 3)] = make_uint4(o[0], o[1], o[2], o[3]);
         }
       }
+      __syncwarp();
+      // piece 32 i + lane of the warp's block, i.e. chunk 8 i + lane / 4 of
+      // the warp, part lane % 4 (the warp's chunks are consecutive)
+      const uint64_t wc0 = c - lane + u * stride;  // the warp's first chunk
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int piece = 32 * i + lane;
+        const int owner = piece / 4;  // lane that produced it
+        if (wc0 + owner < nchunks) out[wc0 * 4 + piece] = ws[piece ^ ((owner >> 1) & 3)];
+      }
+      __syncwarp();
     }
   }
 }
