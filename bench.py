@@ -607,14 +607,21 @@ def run_extended(path, dev):
 
 
 def run_profile_case(spec):
-    """A few launches of one (layer, M) case, for ncu captures:
-    LAYER:M[:bf16] with LAYER in qkv, o_proj, gate_up, down, or moe:M."""
+    """A few launches of one case, for ncu captures: LAYER:M[:bf16] with
+    LAYER in qkv, o_proj, gate_up, down; moe:M; dequantize_rows:N (N x N)."""
     from moe_nvfp4_gemv_gb300 import fp4gemv
     dev = torch.device("cuda", 0)
     parts = spec.split(":")
     M = int(parts[1])
     gs = torch.tensor([GS], dtype=torch.float32, device=dev)
-    if parts[0] == "moe":
+    if parts[0] == "dequantize_rows":
+        N = M
+        w = synth.fp4_bytes(N, N, seed=1, device=dev)
+        sf = synth.e4m3_bytes(fp4gemv.scale_bytes(N, N), seed=2, device=dev)
+        out = torch.empty(N, N, dtype=torch.bfloat16, device=dev)
+        for _ in range(4):
+            fp4gemv.dequantize_rows(w, sf, out=out)
+    elif parts[0] == "moe":
         c = synth.MOE
         E, H, I, SI, topk = c["E"], c["H"], c["I"], c["SI"], c["topk"]
         w1 = synth.fp4_bytes(E * 2 * I, H, seed=1, device=dev).view(E, 2 * I, H // 2)
