@@ -290,8 +290,14 @@ fp4gemv_status rf_capacity(int nt, int (&cap)[9]) {
   for (int s = 1; s <= 8; ++s) {
     int n = g_rf_cap[dev].v[i][s].load(std::memory_order_acquire);
     if (n == 0) {
-      // (size_ring_rf never exceeds the budget, so this is the launches' worst case)
-      if (fp4::rf_max_clusters(fp4::kDenseFp4, nt, s, kRfBudget, &n) != cudaSuccess) return FP4GEMV_ERR_CUDA;
+      // (size_ring_rf never exceeds the budget, so this is the launches' worst
+      // case).  A size the query cannot answer counts as fitting nothing: the
+      // plan then keeps the default tiles for it.  The error is cleared so a
+      // later launch check does not report it.
+      if (fp4::rf_max_clusters(fp4::kDenseFp4, nt, s, kRfBudget, &n) != cudaSuccess) {
+        (void)cudaGetLastError();
+        n = 0;
+      }
       if (n < 0) n = 0;
       g_rf_cap[dev].v[i][s].store(n == 0 ? -1 : n, std::memory_order_release);
     }
