@@ -13,28 +13,28 @@
 // cluster split K and reduce their fp32 partials through distributed shared
 // memory in rank order (deterministic).
 //
-// Warp roles (kW worker warpgroups, then one producer warp):
+// Warp roles (kW dequant warpgroups, then a producer warp and an MMA warp):
 //   producer  lane 0 streams weight boxes (TMA, 128-byte swizzle) and the
 //             matching 512-byte scale chunks (bulk copies) into a ring of
 //             shared-memory stages of 256 K; with PDL these loads are issued
 //             before griddepcontrol.wait.  Activations follow after the wait
 //             (TMA for dense rows, cp.async gathers by all 32 lanes for MoE).
-//   workers   warpgroup w takes the 64-wide K slices q = w, w + kW, ...  For
-//             each slice thread i (row i) reads 32 code bytes and 4 scale
+//   dequant   warpgroup w takes the 128-wide K slices q = w, w + kW, ...  For
+//             each slice thread i (row i) reads its code bytes and scale
 //             bytes, dequantizes them exactly to bf16 (dequant.cuh) and
-//             stores them with tcgen05.st into one of the warpgroup's own
-//             tensor-memory A slots; the warpgroup also permutes the slice's
-//             activations in shared memory to the weight pairs' K order.
-//             After a warpgroup barrier one elected thread issues the four
-//             K=16 tcgen05.mma of the slice into the warpgroup's own fp32
-//             accumulator and frees the slot (and, once per stage, the ring
-//             stage) with tcgen05.commit.  There is no hand-off to a separate
-//             MMA thread: each warpgroup runs its own dequant -> MMA loop.
-//   epilogue  the workers sum the kW accumulators (tcgen05.ld), exchange
+//             stores them with tcgen05.st into the slice's tensor-memory A
+//             slot (a ring of kSlots slots shared by the warpgroups); the
+//             warps also permute the slice's activations in shared memory to
+//             the weight pairs' K order, then arrive on the slot's barrier.
+//   MMA       one elected thread issues each slot's eight K=16 tcgen05.mma
+//             into the single fp32 accumulator and frees the slot (and, once
+//             per stage, the ring stage) with tcgen05.commit, so the dequant
+//             warps never wait on MMA issue.
+//   epilogue  the dequant warps read the accumulator (tcgen05.ld), exchange
 //             partials through (distributed) shared memory and apply the
 //             mode's epilogue.
-// The BF16-weight mode has no dequant step: one warpgroup, whose elected
-// thread issues tcgen05.mma with both operands in shared memory.
+// The BF16-weight mode has no dequant step: the MMA warp issues tcgen05.mma
+// with both operands in shared memory, and one warpgroup runs the epilogue.
 #pragma once
 
 #include <cuda.h>

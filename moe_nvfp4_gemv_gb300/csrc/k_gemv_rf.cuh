@@ -9,17 +9,18 @@
 // weight block for 8 tokens at ~0.4 per cycle per SM (~100 weights per cycle
 // per SM), so it is not the bottleneck; the dequantization is.
 //
-// Layout of the work: a CTA owns one 128-row weight tile (plain, or 64 gate +
-// 64 up rows for silu_mul) and a K range; the S CTAs of a cluster split K and
-// reduce in rank order through distributed shared memory, exactly as the
+// Layout of the work: a CTA owns one weight tile of 16 cw rows (plain, or 8 cw
+// gate + 8 cw up rows for silu_mul; cw = 6..8 consumer warps for the dense
+// GEMV, chosen per call, 8 for MoE) and a K range; the S CTAs of a cluster
+// split K and reduce in rank order through distributed shared memory, as the
 // tcgen05 kernel does.  A producer warp streams weights, scales and
 // activations into a ring of 256-K stages (TMA / bulk copies, weights issued
-// before griddepcontrol.wait).  Each of the 8 consumer warps owns 16 rows of
+// before griddepcontrol.wait).  Each working consumer warp owns 16 rows of
 // the tile; per stage it reads its rows' codes and scales from shared memory,
-// dequantizes them exactly to bf16 in registers (dequant.cuh) straight into
-// MMA A fragments, loads the activation B fragments (permuted in registers to
-// the weight pairs' K order) and accumulates in fp32 registers.  No warp waits
-// on another warp except through the stage ring.
+// dequantizes them exactly in registers (dequant.cuh) straight into MMA A
+// fragments, loads the activation B fragments and accumulates in fp32
+// registers.  Warps meet only through the stage ring (and, in the
+// cooperative variant, at one barrier per stage).
 //
 // Fragment mapping.  Thread (g, c) = (lane / 4, lane % 4) of warp wp holds
 // MMA rows g and g + 8, which are tile rows 16 wp + sigma(g) and
@@ -31,13 +32,15 @@
 // registers of two MMAs, and the activation chunk of the same 8 K (token g,
 // permuted the same way) their B registers.
 //
-// Routes.  For M > kF16MaxM every stage runs the bf16 route above.  For
-// M <= kF16MaxM the f16 route: a converter warp turns each stage's activation
-// rows in shared memory into f16 in place as soon as they land (ahead of the
-// consumers: its arrival is part of the stage's full barrier, so a consumer
-// waits on one barrier per stage), checking that every value converts exactly; the stage then runs on f16 MMAs with the codes converted
-// by cvt.rn.f16x2.e2m1x2 (natural K order, half the ALU work of the bf16
-// route).  A stage with any value that is not exactly an f16 (|x| > 65504,
+// Routes.  The bf16 route above serves 9-16 tokens (and MoE chunks of 5-8
+// pairs).  For M <= kF16MaxM the f16 route: a converter warp turns each
+// stage's activation rows in shared memory into f16 in place as soon as they
+// land (ahead of the consumers: its arrival is part of the stage's full
+// barrier, so a consumer waits on one barrier per stage), checking that every
+// value converts exactly; the stage then runs on f16 MMAs with the codes
+// converted by cvt.rn.f16x2.e2m1x2 (natural K order, half the ALU work of the
+// bf16 route).  The dense 5-8-token variant (kCoop) converts with all
+// consumer warps instead.  A stage with any value that is not exactly an f16 (|x| > 65504,
 // too many low bits for the f16 subnormal grid, NaN) runs the bf16 route with
 // the original activations from global memory instead.  Both routes compute
 // exact products into fp32, so the choice changes no result beyond fp32
