@@ -366,7 +366,7 @@ fp4gemv_status dense_launch(int mode, const void* x, int64_t ldx, const void* w,
   // otherwise the tcgen05 kernel (at 32 tokens the register-fed kernel is
   // bound by its MMA count and no faster).
   const bool rf = fp4w && M <= 16;
-  const int kmode = rf ? (M > 4 && M <= 8 ? kDenseFp4RfCoop : kDenseFp4Rf) : mode;
+  const int kmode = rf ? (M >= 3 && M <= 8 ? kDenseFp4RfCoop : kDenseFp4Rf) : mode;
   const int NT = rf ? (M <= 8 ? 8 : 16) : pick_nt(M);
   KernelInfo info{};
   if (kernel_info(kmode, NT, &info) != cudaSuccess) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;

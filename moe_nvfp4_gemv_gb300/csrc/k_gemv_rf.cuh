@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, kOcc) gemv_rf_kernel(con
     // arrivals: dense, the producer (+ the converter on the f16 route); MoE,
     // the 32 gathering lanes' cp.async and lane 0 (the f16 route moves the
     // 32 to bar_xfull and adds the converter)
-    const bool f16 = C::kHasF16 && ntok0 <= C::kF16MaxM;
+    const bool f16 = !kCoop && C::kHasF16 && ntok0 <= C::kF16MaxM;  // (converter warp)
     for (int i = 0; i < nstages; ++i) {
       mbar_init(smem_u32(&bar_full[i]), f16 ? 2 : (kDense ? 1 : 33));
       mbar_init(smem_u32(&bar_empty[i]), cw);
@@ -326,11 +326,11 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, kOcc) gemv_rf_kernel(con
   const int f_hi = min(unit, f_lo + R);
   const int rpf = rpf_of();  // rows per feature
   const int mine = max(0, f_hi - f_lo) * rpf;
-  const bool f16route = C::kHasF16 && ntok <= C::kF16MaxM;
+  const bool f16route = !kCoop && C::kHasF16 && ntok <= C::kF16MaxM;  // converter-warp f16 route
   // kF16MaxM < ntok <= 8: the consumer warps convert each stage's activations
   // to f16 together (one 16-byte chunk or two per thread) and agree on
   // exactness at a barrier; one converter warp would not keep up with 8 rows.
-  const bool coop = kCoop && C::kHasF16 && ntok > C::kF16MaxM;
+  const bool coop = kCoop && C::kHasF16;  // (the host launches this variant from 3 tokens)
   const bool f16acc = f16route || coop;  // acc holds exact f16-route products
 
   float acc[kChains][C::kTiles][4];  // main route's stages
@@ -406,7 +406,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, kOcc) gemv_rf_kernel(con
     }
   } else if (warp == C::kConverterWarp) {
     // ------------------------------------------------------------------ converter
-    if (C::kHasF16 && ntok <= C::kF16MaxM)
+    if (f16route)
     // Rows < ntok of each stage's activations to f16 in place (16-byte
     // chunks); the other rows and K past the end are zero-filled, the same bits
     // in f16.  A stage with any inexact value is flagged for the bf16 route.
