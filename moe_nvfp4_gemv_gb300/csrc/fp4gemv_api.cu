@@ -163,7 +163,7 @@ constexpr int kDenseFp4Rf = kRfBase + fp4::kDenseFp4;
 constexpr int kMoeGateUpRf = kRfBase + fp4::kMoeGateUp;
 constexpr int kMoeDownRf = kRfBase + fp4::kMoeDown;
 constexpr int kMoeDownRf3 = kRfBase + 10 + fp4::kMoeDown;  // budgeted for three CTAs per SM
-constexpr int kDenseFp4RfCoop = kRfBase + 20 + fp4::kDenseFp4;  // 5 .. 8 tokens, cooperative f16 conversion
+constexpr int kDenseFp4RfCoop = kRfBase + 20 + fp4::kDenseFp4;  // 3 .. 8 tokens, cooperative f16 conversion
 
 cudaError_t kernel_info(int mode, int nt, KernelInfo* info) {
   GemvParams dummy;

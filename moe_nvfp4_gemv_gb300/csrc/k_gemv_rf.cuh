@@ -39,7 +39,7 @@
 // barrier, so a consumer waits on one barrier per stage), checking that every
 // value converts exactly; the stage then runs on f16 MMAs with the codes
 // converted by cvt.rn.f16x2.e2m1x2 (natural K order, half the ALU work of the
-// bf16 route).  The dense 5-8-token variant (kCoop) converts with all
+// bf16 route).  The dense 3-8-token variant (kCoop) converts with all
 // consumer warps instead.  A stage with any value that is not exactly an f16 (|x| > 65504,
 // too many low bits for the f16 subnormal grid, NaN) runs the bf16 route with
 // the original activations from global memory instead.  Both routes compute
@@ -171,7 +171,7 @@ __device__ __forceinline__ void copy_work(const CtaWork& m, RfWork& w) {
 // kOcc: CTAs per SM the registers are budgeted for.  2 by default; 3 (two
 // accumulator chains, 64 registers, the host gives it a 72 KB ring) for
 // grids of many short CTAs, whose fixed costs more co-resident CTAs hide.
-// kCoop: the variant for 5 .. 8 tokens whose consumer warps convert the
+// kCoop: the variant for 3 .. 8 tokens whose consumer warps convert the
 // activations to f16 together (a separate instantiation, so the others'
 // code is unchanged by it).
 template <int kMode, int kNT, int kOcc = 2, bool kCoop = false>

@@ -33,7 +33,7 @@ cudaError_t launch_dense_fp4(int nt, const GemvParams& p, const LaunchCfg& cfg, 
 cudaError_t launch_rf(int mode, int nt, const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info);
 // The same kernel budgeted for three CTAs per SM (instantiated for kMoeDown, nt = 8).
 cudaError_t launch_rf_occ3(int mode, int nt, const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info);
-// The dense 8-token variant whose consumers convert the activations of 5 .. 8 tokens to f16.
+// The dense 8-token variant whose consumers convert the activations of 3 .. 8 tokens to f16.
 cudaError_t launch_rf_coop(int mode, int nt, const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info);
 // Clusters of `cluster` CTAs of the dense register-fed kernel that fit on the
 // GPU at once with `smem` bytes of dynamic shared memory each.
