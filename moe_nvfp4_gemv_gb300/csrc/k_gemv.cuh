@@ -132,9 +132,14 @@ template <int kMode, int kNT>
 struct Cfg {
   static constexpr bool kFp4 = kMode != kDenseBf16;
   static constexpr int kW = kFp4 ? 2 : 1;  // worker warpgroups
-  static constexpr int kThreads = kW * 128 + 64;
+  // MMA-issuing warps: one thread issues a slot's MMAs and each costs it
+  // ~190 cycles, so NVFP4 tiles of up to 32 tokens (whose tensor memory
+  // holds a second accumulator) get two: warp m issues slices q = m (mod 2)
+  // into accumulator m.
+  static constexpr int kMmaWarps = kFp4 && kNT <= 32 ? 2 : 1;
+  static constexpr int kThreads = kW * 128 + 32 * (1 + kMmaWarps);
   static constexpr int kProducerWarp = 4 * kW;
-  static constexpr int kMmaWarp = 4 * kW + 1;
+  static constexpr int kMmaWarp = 4 * kW + 1;  // first MMA warp
   static constexpr int kStageK = kFp4 ? kStageK4 : kStageK16;
   static constexpr int kSlicesPerStage = kFp4 ? kStageK / kSliceK : 1;  // 2 (fp4) or 1 (bf16)
   static constexpr int kWTileBytes = 128 * 128;
@@ -142,10 +147,10 @@ struct Cfg {
   static constexpr int kXBytes = kNT * kStageK * 2;
   static constexpr int kXOff = kWTileBytes + kSfTileBytes;
   static constexpr int kStageBytes = kXOff + kXBytes;
-  // Tensor memory: one fp32 accumulator (kNT columns), then a ring of kSlots
-  // A slots (64 columns = 128 bf16 K each) shared by the warpgroups in slice
-  // order.  256 columns (two CTAs per SM) up to kNT = 64.
-  static constexpr int kAccCols = kNT;
+  // Tensor memory: one fp32 accumulator (kNT columns) per MMA warp, then a
+  // ring of kSlots A slots (64 columns = 128 bf16 K each) shared by the
+  // warpgroups in slice order.  256 columns (two CTAs per SM) up to kNT = 64.
+  static constexpr int kAccCols = kNT * kMmaWarps;
   static constexpr int kSlotCols = kSliceK / 2;
   static constexpr int kSlots = !kFp4 ? 0 : kNT <= 64 ? 3 : 6;
   static constexpr int kTmemCols = pow2_at_least(kAccCols + kSlots * kSlotCols);
@@ -416,13 +421,13 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
     const int nst = stage_count(wk);
     for (int i = 0; i < nstages; ++i) {
       mbar_init(smem_u32(&bar_full[i]), C::kFullCount);
-      mbar_init(smem_u32(&bar_empty[i]), 1);  // the MMA thread's commit after the stage's last slice
+      mbar_init(smem_u32(&bar_empty[i]), C::kMmaWarps);  // each MMA thread's commit after its slice of the stage
     }
     for (int i = 0; i < kNS; ++i) {
       mbar_init(smem_u32(&bar_afull[i]), 4);  // one arrival per warp of the slice's warpgroup
       mbar_init(smem_u32(&bar_aempty[i]), 1);
     }
-    mbar_init(smem_u32(&bar_accum), 1);
+    mbar_init(smem_u32(&bar_accum), C::kMmaWarps);
     mbar_init(smem_u32(&bar_inbox), 1);
     mbar_init(smem_u32(&bar_red_ready), S);
     mbar_init(smem_u32(&bar_red_done), S);
@@ -522,18 +527,21 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
         if (lane == 0) mbar_arrive(fb);
       }
     }
-  } else if (warp == C::kMmaWarp) {
-    // ------------------------------------------------------------------ MMA issuer
-    // One thread issues every MMA of the CTA into the single accumulator;
-    // the dequant warpgroups never wait on an issue.  NVFP4: per 128-K slice
-    // (a ring slot of tensor memory, filled by one warpgroup) 8 MMAs of K = 16
-    // and one commit that frees the slot; one more commit per ring stage.
-    // BF16: both operands in shared memory, 4 MMAs per 64-K stage.
+  } else if (warp >= C::kMmaWarp && warp < C::kMmaWarp + C::kMmaWarps) {
+    // ------------------------------------------------------------------ MMA issuers
+    // One thread per MMA warp issues the MMAs (MMA warp m: slices q = m mod
+    // kMmaWarps into accumulator m); the dequant warpgroups never wait on an
+    // issue.  NVFP4: per 128-K slice (a ring slot of tensor memory, filled by
+    // one warpgroup) 8 MMAs of K = 16 and one commit that frees the slot; one
+    // more commit per ring stage by each MMA warp with a slice in it.  BF16:
+    // both operands in shared memory, 4 MMAs per 64-K stage.
+    const int m = warp - C::kMmaWarp;
     if (lane == 0 && active) {
       constexpr uint32_t idesc = idesc_bf16_f32(128, kNT);
       const int klen = wk.k_end - wk.k_begin;
+      const uint32_t acc = tmem + m * kNT;
       if constexpr (C::kFp4) {
-        for (int q = 0; q < nslices && !s_abort; ++q) {
+        for (int q = m; q < nslices && !s_abort; q += C::kMmaWarps) {
           const int a = q % kNS;
           if (!mbar_wait(smem_u32(&bar_afull[a]), (q / kNS) & 1, p.err)) { s_abort = 1; break; }
           tc_fence_after();
@@ -543,11 +551,15 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
           const uint32_t a_tmem = tmem + C::kAccCols + a * C::kSlotCols;
           for (int kk = 0; kk < kq / 16; ++kk) {
             const int atom = 2 * u2 + kk / 4;
-            mma_ts(tmem, a_tmem + kk * 8, sdesc_sw128(xs + atom * (kNT * 128) + (kk % 4) * 32), idesc,
-                   (q > 0 || kk > 0) ? 1u : 0u);
+            mma_ts(acc, a_tmem + kk * 8, sdesc_sw128(xs + atom * (kNT * 128) + (kk % 4) * 32), idesc,
+                   (q > m || kk > 0) ? 1u : 0u);
           }
           mma_commit(smem_u32(&bar_aempty[a]));
-          if (q + 1 == nslices || (q + 1) / kSPS != s) mma_commit(smem_u32(&bar_empty[s % nstages]));
+          // (two MMA warps: one slice of every stage each, so each commits
+          // every stage it has a slice of; a lone final slice's stage is
+          // never waited for)
+          if (C::kMmaWarps == 2 || q + 1 == nslices || (q + 1) / kSPS != s)
+            mma_commit(smem_u32(&bar_empty[s % nstages]));
         }
       } else {
         for (int s = 0; s < nst && !s_abort; ++s) {
@@ -557,7 +569,7 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ss(tmem, sdesc_sw128(st + kk * 32), sdesc_sw128(st + C::kXOff + kk * 32), idesc,
+            mma_ss(acc, sdesc_sw128(st + kk * 32), sdesc_sw128(st + C::kXOff + kk * 32), idesc,
                    (s > 0 || kk > 0) ? 1u : 0u);
           mma_commit(smem_u32(&bar_empty[slot]));
         }
@@ -645,13 +657,24 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
     const int owner_feats = min(R, unit - owner * R);
     const int rr = (i / unit) * owner_feats + (fi - owner * R);
     const int rows_owner = owner_feats * (128 / unit);
-    // The accumulator's columns [c, c + 8) of row i.
+    // Columns [c, c + 8) of row i, summed over the MMA warps' accumulators
+    // (accumulator 1 holds nothing when the K range is one slice: its warp
+    // issued no MMA).  CTA-uniform, so the loads stay warp-collective.
+    const bool two_acc = C::kMmaWarps == 2 && nslices > 1;
     auto load_sum = [&](int c, float (&v8)[8]) {
       uint32_t v[8];
       tmem_ld8(tmem + lane_base + c, v);
-      tmem_wait_ld();
+      if (two_acc) {
+        uint32_t v2[8];
+        tmem_ld8(tmem + lane_base + kNT + c, v2);
+        tmem_wait_ld();
 #pragma unroll
-      for (int jj = 0; jj < 8; ++jj) v8[jj] = __uint_as_float(v[jj]);
+        for (int jj = 0; jj < 8; ++jj) v8[jj] = __uint_as_float(v[jj]) + __uint_as_float(v2[jj]);
+      } else {
+        tmem_wait_ld();
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) v8[jj] = __uint_as_float(v[jj]);
+      }
     };
     // Partials of (token n, row i).  Push mode: the owner of row i receives
     // them from every rank into inbox[src][n][rr]; pull mode: each rank leaves
