@@ -26,10 +26,11 @@
 //             slot (a ring of kSlots slots shared by the warpgroups); the
 //             warps also permute the slice's activations in shared memory to
 //             the weight pairs' K order, then arrive on the slot's barrier.
-//   MMA       one elected thread issues each slot's eight K=16 tcgen05.mma
-//             into the single fp32 accumulator and frees the slot (and, once
-//             per stage, the ring stage) with tcgen05.commit, so the dequant
-//             warps never wait on MMA issue.
+//   MMA       the warp waits for each slot together and one elected lane
+//             issues the slot's eight K=16 tcgen05.mma into the fp32
+//             accumulator and frees the slot (and, once per stage, the ring
+//             stage) with tcgen05.commit, so the dequant warps never wait on
+//             MMA issue.
 //   epilogue  the dequant warps read the accumulator (tcgen05.ld), exchange
 //             partials through (distributed) shared memory and apply the
 //             mode's epilogue.
@@ -132,14 +133,9 @@ template <int kMode, int kNT>
 struct Cfg {
   static constexpr bool kFp4 = kMode != kDenseBf16;
   static constexpr int kW = kFp4 ? 2 : 1;  // worker warpgroups
-  // MMA-issuing warps: one thread issues a slot's MMAs and each costs it
-  // ~190 cycles, so NVFP4 tiles of up to 32 tokens (whose tensor memory
-  // holds a second accumulator) get two: warp m issues slices q = m (mod 2)
-  // into accumulator m.
-  static constexpr int kMmaWarps = kFp4 && kNT <= 32 ? 2 : 1;
-  static constexpr int kThreads = kW * 128 + 32 * (1 + kMmaWarps);
+  static constexpr int kThreads = kW * 128 + 64;
   static constexpr int kProducerWarp = 4 * kW;
-  static constexpr int kMmaWarp = 4 * kW + 1;  // first MMA warp
+  static constexpr int kMmaWarp = 4 * kW + 1;
   static constexpr int kStageK = kFp4 ? kStageK4 : kStageK16;
   static constexpr int kSlicesPerStage = kFp4 ? kStageK / kSliceK : 1;  // 2 (fp4) or 1 (bf16)
   static constexpr int kWTileBytes = 128 * 128;
@@ -147,10 +143,10 @@ struct Cfg {
   static constexpr int kXBytes = kNT * kStageK * 2;
   static constexpr int kXOff = kWTileBytes + kSfTileBytes;
   static constexpr int kStageBytes = kXOff + kXBytes;
-  // Tensor memory: one fp32 accumulator (kNT columns) per MMA warp, then a
-  // ring of kSlots A slots (64 columns = 128 bf16 K each) shared by the
-  // warpgroups in slice order.  256 columns (two CTAs per SM) up to kNT = 64.
-  static constexpr int kAccCols = kNT * kMmaWarps;
+  // Tensor memory: one fp32 accumulator (kNT columns), then a ring of kSlots
+  // A slots (64 columns = 128 bf16 K each) shared by the warpgroups in slice
+  // order.  256 columns (two CTAs per SM) up to kNT = 64.
+  static constexpr int kAccCols = kNT;
   static constexpr int kSlotCols = kSliceK / 2;
   static constexpr int kSlots = !kFp4 ? 0 : kNT <= 64 ? 3 : 6;
   static constexpr int kTmemCols = pow2_at_least(kAccCols + kSlots * kSlotCols);
@@ -421,13 +417,13 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
     const int nst = stage_count(wk);
     for (int i = 0; i < nstages; ++i) {
       mbar_init(smem_u32(&bar_full[i]), C::kFullCount);
-      mbar_init(smem_u32(&bar_empty[i]), C::kMmaWarps);  // each MMA thread's commit after its slice of the stage
+      mbar_init(smem_u32(&bar_empty[i]), 1);  // the MMA thread's commit after the stage's last slice
     }
     for (int i = 0; i < kNS; ++i) {
       mbar_init(smem_u32(&bar_afull[i]), 4);  // one arrival per warp of the slice's warpgroup
       mbar_init(smem_u32(&bar_aempty[i]), 1);
     }
-    mbar_init(smem_u32(&bar_accum), C::kMmaWarps);
+    mbar_init(smem_u32(&bar_accum), 1);
     mbar_init(smem_u32(&bar_inbox), 1);
     mbar_init(smem_u32(&bar_red_ready), S);
     mbar_init(smem_u32(&bar_red_done), S);
@@ -527,54 +523,67 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
         if (lane == 0) mbar_arrive(fb);
       }
     }
-  } else if (warp >= C::kMmaWarp && warp < C::kMmaWarp + C::kMmaWarps) {
-    // ------------------------------------------------------------------ MMA issuers
-    // One thread per MMA warp issues the MMAs (MMA warp m: slices q = m mod
-    // kMmaWarps into accumulator m); the dequant warpgroups never wait on an
-    // issue.  NVFP4: per 128-K slice (a ring slot of tensor memory, filled by
-    // one warpgroup) 8 MMAs of K = 16 and one commit that frees the slot; one
-    // more commit per ring stage by each MMA warp with a slice in it.  BF16:
-    // both operands in shared memory, 4 MMAs per 64-K stage.
-    const int m = warp - C::kMmaWarp;
-    if (lane == 0 && active) {
+  } else if (warp == C::kMmaWarp) {
+    // ------------------------------------------------------------------ MMA issuer
+    // One warp consumes the slots in slice order (the slot barriers' parity
+    // waits rely on a single in-order consumer); the dequant warpgroups never
+    // wait on an issue.  The whole warp runs the loop and waits; one elected
+    // lane issues a slot's MMAs, unrolled, with the shared-memory descriptors
+    // stepped by constants (issued from a loop that lane 0 runs alone,
+    // building each descriptor, an MMA costs its thread ~300 cycles instead
+    // of ~25).  NVFP4: per 128-K slice (a ring slot of tensor memory, filled
+    // by one warpgroup) 8 MMAs of K = 16 and one commit that frees the slot;
+    // one more commit per ring stage.  BF16: both operands in shared memory,
+    // 4 MMAs per 64-K stage.
+    if (active) {
       constexpr uint32_t idesc = idesc_bf16_f32(128, kNT);
       const int klen = wk.k_end - wk.k_begin;
-      const uint32_t acc = tmem + m * kNT;
+      const uint32_t acc = tmem;
       if constexpr (C::kFp4) {
-        for (int q = m; q < nslices && !s_abort; q += C::kMmaWarps) {
+        for (int q = 0; q < nslices; ++q) {
           const int a = q % kNS;
-          if (!mbar_wait(smem_u32(&bar_afull[a]), (q / kNS) & 1, p.err)) { s_abort = 1; break; }
+          if (!__all_sync(0xFFFFFFFFu, !s_abort && mbar_wait(smem_u32(&bar_afull[a]), (q / kNS) & 1, p.err))) {
+            s_abort = 1;
+            break;
+          }
           tc_fence_after();
           const int s = q / kSPS, u2 = q % kSPS;
-          const uint32_t xs = ring + (s % nstages) * C::kStageBytes + C::kXOff;
-          const int kq = min(kSliceK, klen - q * kSliceK);  // 64 or 128
+          // the slice's two 64-K activation atoms
+          const uint32_t xs = ring + (s % nstages) * C::kStageBytes + C::kXOff + 2 * u2 * (kNT * 128);
+          const uint64_t b0 = sdesc_sw128(xs), b1 = sdesc_sw128(xs + kNT * 128);
+          const bool full = klen - q * kSliceK >= kSliceK;  // else the last slice, 64 K
           const uint32_t a_tmem = tmem + C::kAccCols + a * C::kSlotCols;
-          for (int kk = 0; kk < kq / 16; ++kk) {
-            const int atom = 2 * u2 + kk / 4;
-            mma_ts(acc, a_tmem + kk * 8, sdesc_sw128(xs + atom * (kNT * 128) + (kk % 4) * 32), idesc,
-                   (q > m || kk > 0) ? 1u : 0u);
+          if (elect_one()) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              if (kk < 4 || full)  // +32 bytes of K = +2 in the descriptor's address field
+                mma_ts(acc, a_tmem + kk * 8, (kk < 4 ? b0 : b1) + 2 * (kk % 4), idesc, (q > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(smem_u32(&bar_aempty[a]));
+            if (q + 1 == nslices || (q + 1) / kSPS != s) mma_commit(smem_u32(&bar_empty[s % nstages]));
           }
-          mma_commit(smem_u32(&bar_aempty[a]));
-          // (two MMA warps: one slice of every stage each, so each commits
-          // every stage it has a slice of; a lone final slice's stage is
-          // never waited for)
-          if (C::kMmaWarps == 2 || q + 1 == nslices || (q + 1) / kSPS != s)
-            mma_commit(smem_u32(&bar_empty[s % nstages]));
+          __syncwarp();
         }
       } else {
-        for (int s = 0; s < nst && !s_abort; ++s) {
+        for (int s = 0; s < nst; ++s) {
           const int slot = s % nstages;
           const uint32_t st = ring + slot * C::kStageBytes;
-          if (!mbar_wait(smem_u32(&bar_full[slot]), (s / nstages) & 1, p.err)) { s_abort = 1; break; }
+          if (!__all_sync(0xFFFFFFFFu, !s_abort && mbar_wait(smem_u32(&bar_full[slot]), (s / nstages) & 1, p.err))) {
+            s_abort = 1;
+            break;
+          }
           tc_fence_after();
+          const uint64_t da = sdesc_sw128(st), db = sdesc_sw128(st + C::kXOff);
+          if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_ss(acc, sdesc_sw128(st + kk * 32), sdesc_sw128(st + C::kXOff + kk * 32), idesc,
-                   (s > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(smem_u32(&bar_empty[slot]));
+            for (int kk = 0; kk < 4; ++kk) mma_ss(acc, da + 2 * kk, db + 2 * kk, idesc, (s > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(smem_u32(&bar_empty[slot]));
+          }
+          __syncwarp();
         }
       }
-      mma_commit(smem_u32(&bar_accum));
+      if (elect_one()) mma_commit(smem_u32(&bar_accum));
+      __syncwarp();
     }
   } else if (active) {
     // ------------------------------------------------------------------ dequant warpgroups
@@ -657,24 +666,13 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
     const int owner_feats = min(R, unit - owner * R);
     const int rr = (i / unit) * owner_feats + (fi - owner * R);
     const int rows_owner = owner_feats * (128 / unit);
-    // Columns [c, c + 8) of row i, summed over the MMA warps' accumulators
-    // (accumulator 1 holds nothing when the K range is one slice: its warp
-    // issued no MMA).  CTA-uniform, so the loads stay warp-collective.
-    const bool two_acc = C::kMmaWarps == 2 && nslices > 1;
+    // The accumulator's columns [c, c + 8) of row i.
     auto load_sum = [&](int c, float (&v8)[8]) {
       uint32_t v[8];
       tmem_ld8(tmem + lane_base + c, v);
-      if (two_acc) {
-        uint32_t v2[8];
-        tmem_ld8(tmem + lane_base + kNT + c, v2);
-        tmem_wait_ld();
+      tmem_wait_ld();
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) v8[jj] = __uint_as_float(v[jj]) + __uint_as_float(v2[jj]);
-      } else {
-        tmem_wait_ld();
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) v8[jj] = __uint_as_float(v[jj]);
-      }
+      for (int jj = 0; jj < 8; ++jj) v8[jj] = __uint_as_float(v[jj]);
     };
     // Partials of (token n, row i).  Push mode: the owner of row i receives
     // them from every rank into inbox[src][n][rr]; pull mode: each rank leaves
