@@ -105,9 +105,11 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_
 }
 
 // Activations x [M, K] (bf16, row stride ldx) viewed as [K/64, M, 64]: one
-// box {64, rows, 4} holds four 64-wide K atoms of `rows` tokens, each atom a
-// [rows x 128-byte] 128B-swizzled block -- the layout the MMA reads.
-bool encode_x_atoms(CUtensorMap* m, const void* x, int K, int M, int64_t ldx, uint32_t rows) {
+// box {64, rows, atoms} holds `atoms` 64-wide K atoms of `rows` tokens, each
+// atom a [rows x 128-byte] 128B-swizzled block -- the layout the MMA reads.
+// The register-fed kernel loads a 256-K stage (4 atoms), the tcgen05 kernel
+// a 128-K slice (2).
+bool encode_x_atoms(CUtensorMap* m, const void* x, int K, int M, int64_t ldx, uint32_t rows, uint32_t atoms) {
   MapKey k;
   std::memset(&k, 0, sizeof(k));
   k.base = x;
@@ -118,7 +120,7 @@ bool encode_x_atoms(CUtensorMap* m, const void* x, int K, int M, int64_t ldx, ui
   k.strides[1] = 128;
   k.box[0] = 64;
   k.box[1] = rows;
-  k.box[2] = 4;
+  k.box[2] = atoms;
   k.rank = 3;
   k.dtype = static_cast<int>(CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
   return encode_cached(m, k);
@@ -196,20 +198,56 @@ cudaError_t kernel_launch(int mode, int nt, const GemvParams& p, const LaunchCfg
 
 // Ring depth and dynamic shared memory: two CTAs per SM when the kernel's
 // tensor-memory footprint allows it (<= 256 columns), else one.
-void size_ring(const KernelInfo& info, int* nstages, size_t* smem, int* ctas_per_sm) {
-  const int per_sm = info.tmem_cols <= 256 ? 2 : 1;
-  const int budget = (per_sm == 2 ? 110 * 1024 : 220 * 1024) - info.inbox_bytes;
-  int ns = (budget - 1024) / info.stage_bytes;
-  if (ns > fp4::kMaxStages) ns = fp4::kMaxStages;
-  if (ns < 2) ns = 2;
-  size_t bytes = 1024 + static_cast<size_t>(ns) * info.stage_bytes;
-  if (bytes < static_cast<size_t>(info.red_bytes) + 1024) bytes = info.red_bytes + 1024;
-  bytes += info.inbox_bytes;
+// CTAs per SM of the tcgen05 kernel: two when its tensor memory (512
+// columns per SM) allows.
+int tc_ctas_per_sm(const KernelInfo& info) { return info.tmem_cols <= 256 ? 2 : 1; }
+
+// Ring of the tcgen05 kernel for a launch of S-rank clusters, within one
+// CTA's share of shared memory.  NVFP4 (fp4w): weight stages of 16 KB codes
+// + sf_slots 2 KB scale groups (they hide HBM latency) beside nx activation
+// slots (they hide L2's): nx = 4 or 3, whichever leaves more weight stages
+// (4 on a tie), 2 if neither leaves two.  nx = 3 only with three tensor-
+// memory slots: the kernel's parity waits on an activation slot need either
+// an even nx (each warpgroup owns its slots) or nx = tensor-memory slots.
+// BF16: stages of weights and activations together.  The split-K inbox
+// (push mode) follows the ring when S > 1; with one rank it reuses the
+// ring, drained by then.
+struct TcRing {
+  int nstages = 0, nx = 0, wstage = 0, inbox_off = 0;
+  size_t smem = 0;
+};
+TcRing size_ring(const KernelInfo& info, bool fp4w, int sf_slots, int S) {
+  TcRing r;
+  const int per_sm = tc_ctas_per_sm(info);
+  const int inbox = S > 1 ? info.inbox_bytes : 0;
+  const int avail = (per_sm == 2 ? 110 * 1024 : 220 * 1024) - 1024 - inbox;
+  int bytes = 0;
+  if (fp4w) {
+    r.wstage = 16384 + 2048 * sf_slots;
+    auto stages = [&](int nx) {
+      const int n = (avail - nx * info.x_slice_bytes) / r.wstage;
+      return n > fp4::kMaxStages ? fp4::kMaxStages : n;
+    };
+    r.nx = 4;
+    if (info.tmem_slots == 3 && stages(3) > stages(4)) r.nx = 3;
+    if (stages(r.nx) < 2) r.nx = 2;
+    r.nstages = stages(r.nx);
+    if (r.nstages < 2) r.nstages = 2;
+    bytes = r.nstages * r.wstage + r.nx * info.x_slice_bytes;
+  } else {
+    r.wstage = info.stage_bytes;
+    r.nstages = avail / info.stage_bytes;
+    if (r.nstages > fp4::kMaxStages) r.nstages = fp4::kMaxStages;
+    if (r.nstages < 2) r.nstages = 2;
+    bytes = r.nstages * info.stage_bytes;
+  }
+  if (bytes < info.red_bytes) bytes = info.red_bytes;  // pull mode: partials reuse the ring
+  if (bytes < info.inbox_bytes) bytes = info.inbox_bytes;
+  r.inbox_off = S > 1 ? bytes : 0;
+  r.smem = 1024 + static_cast<size_t>(bytes) + inbox;
   // one CTA per SM: ask for more than half of the SM's shared memory
-  if (per_sm == 1 && bytes < 120 * 1024) bytes = 120 * 1024;
-  *nstages = ns;
-  *smem = bytes;
-  *ctas_per_sm = per_sm;
+  if (per_sm == 1 && r.smem < 120 * 1024) r.smem = 120 * 1024;
+  return r;
 }
 
 // Ring of the register-fed kernel: a stage is the 16 KB weight tile, 2 KB per
@@ -385,7 +423,7 @@ fp4gemv_status dense_launch(int mode, const void* x, int64_t ldx, const void* w,
     plan_rf(N, K, silu_mul != 0, sms, cap, &cw, &S0, &sf_groups);
     size_ring_rf(info, 16 * cw * 128, sf_groups, &nstages, &smem, &stage_bytes, &x_off);
   } else {
-    size_ring(info, &nstages, &smem, &per_sm);
+    per_sm = tc_ctas_per_sm(info);
   }
   const int box_rows = rf ? (silu_mul ? 8 * cw : 16 * cw) : (silu_mul ? 64 : 128);
   const int tiles = (n_out + box_rows - 1) / box_rows;
@@ -393,6 +431,15 @@ fp4gemv_status dense_launch(int mode, const void* x, int64_t ldx, const void* w,
   if (!rf) S0 = pick_split(tiles, K, stage_k, sms * per_sm);
   const int kslab = ((K + S0 - 1) / S0 + 63) / 64 * 64;
   const int S = (K + kslab - 1) / kslab;  // every cluster rank gets a non-empty K range
+  // Scale groups a weight stage holds: one 128-row group; with silu_mul the
+  // gate box's and the up box's (a third when an up box straddles two).
+  const int sf_slots = silu_mul ? ((N / 2) % 64 == 0 ? 2 : 3) : 1;
+  TcRing tr;
+  if (!rf) {
+    tr = size_ring(info, fp4w, sf_slots, S);
+    nstages = tr.nstages;
+    smem = tr.smem;
+  }
 
   GemvParams p;
   std::memset(&p, 0, sizeof(p));
@@ -404,7 +451,7 @@ fp4gemv_status dense_launch(int mode, const void* x, int64_t ldx, const void* w,
       return FP4GEMV_ERR_CUDA;
   }
   if (fp4w) {
-    if (!encode_x_atoms(&p.tm_x, x, K, M, ldx, NT)) return FP4GEMV_ERR_CUDA;
+    if (!encode_x_atoms(&p.tm_x, x, K, M, ldx, NT, rf ? 4 : 2)) return FP4GEMV_ERR_CUDA;
   } else {
     if (!encode_2d(&p.tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, M, static_cast<uint64_t>(ldx) * 2, 64, NT))
       return FP4GEMV_ERR_CUDA;
@@ -424,6 +471,10 @@ fp4gemv_status dense_launch(int mode, const void* x, int64_t ldx, const void* w,
   p.rows_w = N;
   p.kbp = ((K / 16) + 3) / 4 * 4;
   p.nstages = nstages;
+  p.nx = tr.nx;
+  p.wstage = tr.wstage;
+  p.sf_slots = sf_slots;
+  p.inbox_off = tr.inbox_off;
   p.stage_bytes = stage_bytes;
   p.x_off = x_off;
   p.cw = cw;
@@ -533,10 +584,18 @@ fp4gemv_status fp4gemv_moe_gate_up(const void* x, const int32_t* ids, int M, int
   const int NT = rf ? 8 : 32;
   KernelInfo info{};
   if (kernel_info(kmode, NT, &info) != cudaSuccess) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
-  int nstages = 0, per_sm = 0, stage_bytes = 0, x_off = 0;
+  int nstages = 0, stage_bytes = 0, x_off = 0;
   size_t smem = 0;
-  if (rf) size_ring_rf(info, 128 * 128, 2, &nstages, &smem, &stage_bytes, &x_off);  // routed: 1 group, shared: gate + up
-  else size_ring(info, &nstages, &smem, &per_sm);
+  // scale groups per stage: routed tiles one; shared-expert tiles the gate
+  // box's and the up box's (SI is a multiple of 64, so neither straddles)
+  TcRing tr;
+  if (rf) {
+    size_ring_rf(info, 128 * 128, 2, &nstages, &smem, &stage_bytes, &x_off);
+  } else {
+    tr = size_ring(info, true, 2, 1);
+    nstages = tr.nstages;
+    smem = tr.smem;
+  }
   GemvParams p;
   std::memset(&p, 0, sizeof(p));
   if (!encode_2d(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w1, H / 2, static_cast<uint64_t>(E) * 2 * I, H / 2, 128, 128))
@@ -572,6 +631,10 @@ fp4gemv_status fp4gemv_moe_gate_up(const void* x, const int32_t* ids, int M, int
   p.kbp = p.kbp2 = ((H / 16) + 3) / 4 * 4;
   p.sf_expert_bytes = static_cast<uint32_t>(fp4gemv_scale_bytes(2 * I, H));
   p.nstages = nstages;
+  p.nx = tr.nx;
+  p.wstage = tr.wstage;
+  p.sf_slots = 2;
+  p.inbox_off = tr.inbox_off;
   p.stage_bytes = stage_bytes;
   p.x_off = x_off;
   p.err = err;
@@ -623,10 +686,16 @@ fp4gemv_status fp4gemv_moe_down_combine(const void* act, const int32_t* ids, con
   const int NT = rf ? 8 : 32;
   KernelInfo info{};
   if (kernel_info(kmode, NT, &info) != cudaSuccess) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
-  int nstages = 0, per_sm = 0, stage_bytes = 0, x_off = 0;
+  int nstages = 0, stage_bytes = 0, x_off = 0;
   size_t smem = 0;
-  if (rf) size_ring_rf(info, 128 * 128, 1, &nstages, &smem, &stage_bytes, &x_off, occ3 ? 72 * 1024 : kRfBudget);
-  else size_ring(info, &nstages, &smem, &per_sm);
+  TcRing tr;  // one scale group per stage (128-row tiles)
+  if (rf) {
+    size_ring_rf(info, 128 * 128, 1, &nstages, &smem, &stage_bytes, &x_off, occ3 ? 72 * 1024 : kRfBudget);
+  } else {
+    tr = size_ring(info, true, 1, 1);
+    nstages = tr.nstages;
+    smem = tr.smem;
+  }
   GemvParams p;
   std::memset(&p, 0, sizeof(p));
   if (!encode_2d(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w2, I / 2, static_cast<uint64_t>(E) * H, I / 2, 128, 128))
@@ -671,6 +740,10 @@ fp4gemv_status fp4gemv_moe_down_combine(const void* act, const int32_t* ids, con
   p.kbp2 = ((SI / 16) + 3) / 4 * 4;
   p.sf_expert_bytes = static_cast<uint32_t>(fp4gemv_scale_bytes(H, I));
   p.nstages = nstages;
+  p.nx = tr.nx;
+  p.wstage = tr.wstage;
+  p.sf_slots = 1;
+  p.inbox_off = tr.inbox_off;
   p.stage_bytes = stage_bytes;
   p.x_off = x_off;
   p.err = err;

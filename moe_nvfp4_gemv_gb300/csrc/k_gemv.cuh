@@ -18,14 +18,18 @@
 //             matching 512-byte scale chunks (bulk copies) into a ring of
 //             shared-memory stages of 256 K; with PDL these loads are issued
 //             before griddepcontrol.wait.  Activations follow after the wait
-//             (TMA for dense rows, cp.async gathers by all 32 lanes for MoE).
+//             into a ring of their own, one 128-K slice per slot (TMA for
+//             dense rows, cp.async gathers by all 32 lanes for MoE), so the
+//             weight ring, which hides HBM latency, is not shortened by
+//             activations that come from L2.
 //   dequant   warpgroup w takes the 128-wide K slices q = w, w + kW, ...  For
 //             each slice thread i (row i) reads its code bytes and scale
 //             bytes, dequantizes them exactly to bf16 (dequant.cuh) and
 //             stores them with tcgen05.st into the slice's tensor-memory A
 //             slot (a ring of kSlots slots shared by the warpgroups); the
 //             warps also permute the slice's activations in shared memory to
-//             the weight pairs' K order, then arrive on the slot's barrier.
+//             the weight pairs' K order, then arrive on the slot's barrier
+//             and free their share of the weight stage.
 //   MMA       the warp waits for each slot together and one elected lane
 //             issues the slot's eight K=16 tcgen05.mma into the fp32
 //             accumulator and frees the slot (and, once per stage, the ring
@@ -60,6 +64,7 @@ constexpr int kStageK16 = 64;   // K per ring stage, bf16 weights (128 B per row
 constexpr int kMaxNT = 128;
 constexpr int kMaxWG = 2;
 constexpr int kMaxSlots = 6;
+constexpr int kMaxXSlots = 8;   // activation slots (NVFP4 modes)
 constexpr int kSliceK = 128;    // K per tensor-memory A slot (8 MMAs of K = 16 per commit)
 
 struct GemvParams {
@@ -97,7 +102,11 @@ struct GemvParams {
   int shared_tiles;    // MoE: column tiles of the shared expert
   int kbp, kbp2;       // padded K blocks (K/16 rounded up to 4) of tm_w / tm_w2 rows
   uint32_t sf_expert_bytes;
-  int nstages;
+  int nstages;         // weight ring stages
+  int nx;              // tcgen05 NVFP4 modes: activation slots (one 128-K slice each)
+  int wstage;          // tcgen05 NVFP4 modes: bytes per weight stage (codes + sf_slots scale groups)
+  int sf_slots;        // tcgen05 NVFP4 modes: 2 KB scale-group slots per weight stage (1 .. 3)
+  int inbox_off;       // tcgen05 push mode: offset of the split-K inbox from the ring (0: the drained ring)
   int stage_bytes;     // register-fed kernel: bytes per ring stage (weights, scale groups, activations)
   int x_off;           // register-fed kernel: offset of the activations in a stage
   int cw;              // register-fed dense kernel: consumer warps = tile height / 16 (4 .. 8)
@@ -133,16 +142,21 @@ template <int kMode, int kNT>
 struct Cfg {
   static constexpr bool kFp4 = kMode != kDenseBf16;
   static constexpr int kW = kFp4 ? 2 : 1;  // worker warpgroups
-  static constexpr int kThreads = kW * 128 + 64;
+  // NVFP4: a third warp streams the activation ring
+  static constexpr int kThreads = kW * 128 + (kFp4 ? 96 : 64);
   static constexpr int kProducerWarp = 4 * kW;
   static constexpr int kMmaWarp = 4 * kW + 1;
+  static constexpr int kXWarp = 4 * kW + 2;
   static constexpr int kStageK = kFp4 ? kStageK4 : kStageK16;
   static constexpr int kSlicesPerStage = kFp4 ? kStageK / kSliceK : 1;  // 2 (fp4) or 1 (bf16)
   static constexpr int kWTileBytes = 128 * 128;
   static constexpr int kSfTileBytes = kFp4 ? 3 * 4 * 512 : 0;  // three 128-row scale groups x 4 chunks
   static constexpr int kXBytes = kNT * kStageK * 2;
   static constexpr int kXOff = kWTileBytes + kSfTileBytes;
-  static constexpr int kStageBytes = kXOff + kXBytes;
+  static constexpr int kStageBytes = kXOff + kXBytes;  // BF16: weights and activations of a stage
+  // NVFP4: activations have a ring of their own, one 128-K slice per slot
+  // (two 64-K atoms of kNT rows x 128 bytes).
+  static constexpr int kXSliceBytes = kNT * kSliceK * 2;
   // Tensor memory: one fp32 accumulator (kNT columns), then a ring of kSlots
   // A slots (64 columns = 128 bf16 K each) shared by the warpgroups in slice
   // order.  256 columns (two CTAs per SM) up to kNT = 64.
@@ -158,10 +172,10 @@ struct Cfg {
   // Split-K partials are pushed to the owning cluster rank (st.async into a
   // dedicated inbox) when the inbox is small; otherwise pulled through DSMEM
   // from the (reused) ring.
-  static constexpr bool kPush = kNT <= 64;
+  static constexpr bool kPush = kNT <= 32;
   static constexpr int kInboxBytes = kPush ? kNT * 136 * 4 : 0;
   static_assert(kNT % 16 == 0 && kNT >= 16 && kNT <= kMaxNT, "token tile");
-  static_assert(kStageBytes % 1024 == 0, "stage alignment");
+  static_assert(kStageBytes % 1024 == 0 && kXSliceBytes % 1024 == 0, "stage alignment");
   static_assert(kTmemCols <= 512, "tensor memory");
   static_assert(kSlots <= kMaxSlots && kW <= kMaxWG, "barrier arrays");
   // CTAs per SM the launch aims for (tensor memory is 512 columns per SM)
@@ -341,12 +355,18 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
   constexpr int kSPS = C::kSlicesPerStage;
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  // 1024-aligned ring, addressed through 32-bit shared-window addresses; the
-  // split-K inbox (push mode) follows the ring.
+  // 1024-aligned ring, addressed through 32-bit shared-window addresses:
+  // the weight stages, then (NVFP4) the activation slots; the split-K inbox
+  // (push mode) follows, or with one rank reuses the drained ring.
   const uint32_t ring = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t inbox = ring + p.nstages * C::kStageBytes;
+  const int wstage = C::kFp4 ? p.wstage : C::kStageBytes;
+  const uint32_t xring = ring + p.nstages * wstage;
+  const int nx = p.nx;
+  const uint32_t inbox = ring + p.inbox_off;
   __shared__ __align__(8) uint64_t bar_full[kMaxStages];
-  __shared__ __align__(8) uint64_t bar_empty[kMaxStages];
+  __shared__ __align__(8) uint64_t bar_empty[kMaxStages];   // NVFP4: stage dequantized; BF16: its MMAs done
+  __shared__ __align__(8) uint64_t bar_xfull[kMaxXSlots];   // activation slice landed
+  __shared__ __align__(8) uint64_t bar_xempty[kMaxXSlots];  // activation slice's MMAs done (MMA-thread commit)
   __shared__ __align__(8) uint64_t bar_afull[kMaxSlots];   // slot dequantized (4 warps of its warpgroup)
   __shared__ __align__(8) uint64_t bar_aempty[kMaxSlots];  // slot's MMAs done (MMA-thread commit)
   __shared__ __align__(8) uint64_t bar_accum;
@@ -379,9 +399,14 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
   auto stage_count = [&](const CtaWork& wk) {
     return wk.active ? (wk.k_end - wk.k_begin + C::kStageK - 1) / C::kStageK : 0;
   };
+  // Weights of stage s into its ring slot.  NVFP4: the stage's full barrier
+  // counts this arrival and the code and scale bytes; BF16: only the bytes
+  // (the activations' load arrives).  A stage holds p.sf_slots scale groups;
+  // a group beyond them (which the host's sizing rules out) is reported and
+  // not copied.
   auto issue_weights = [&](const CtaWork& wk, int s) {
     const int slot = s % nstages;
-    const uint32_t st = ring + slot * C::kStageBytes;
+    const uint32_t st = ring + slot * wstage;
     const uint32_t fb = smem_u32(&bar_full[slot]);
     const int k0 = wk.k_begin + s * C::kStageK;
     const int kvalid = min(C::kStageK, wk.k_end - k0);
@@ -389,16 +414,25 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
     const CUtensorMap* tmw = wk.shared ? &p.tm_w2 : &p.tm_w;
     uint32_t bytes = C::kWTileBytes;
     if constexpr (C::kFp4) {
-      for (int g = 0; g < 3; ++g) bytes += (wk.sgroup[g] >= 0 ? nchunks * 512 : 0);
+      for (int g = 0; g < 3; ++g) {
+        if (wk.sgroup[g] < 0) continue;
+        if (g >= p.sf_slots) {
+          raise_error(p.err, FP4_ERR_BADIDX);
+          continue;
+        }
+        bytes += nchunks * 512;
+      }
+      mbar_arrive_expect_tx(fb, bytes);
+    } else {
+      asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(fb), "r"(bytes) : "memory");
     }
-    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(fb), "r"(bytes) : "memory");
     const int c0 = C::kFp4 ? k0 / 2 : k0;  // bytes (u8 map) or elements (bf16 map)
     tma_load_2d(st, tmw, c0, wk.wrow[0], fb, pol_w);
     if (wk.paired) tma_load_2d(st + C::kWTileBytes / 2, tmw, c0, wk.wrow[1], fb, pol_w);
     if constexpr (C::kFp4) {
       const uint8_t* sfb =
           wk.shared ? p.sf2 : p.sf + (wk.expert >= 0 ? static_cast<size_t>(wk.expert) * p.sf_expert_bytes : 0);
-      for (int g = 0; g < 3; ++g) {
+      for (int g = 0; g < 3 && g < p.sf_slots; ++g) {
         if (wk.sgroup[g] < 0) continue;
         const size_t chunk = static_cast<size_t>(wk.sgroup[g]) * (wk.kbp / 4) + k0 / 64;
         bulk_load(st + C::kWTileBytes + g * 2048, sfb + chunk * 512, nchunks * 512, fb, pol_w);
@@ -416,8 +450,15 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
     CtaWork& wk = s_work;
     const int nst = stage_count(wk);
     for (int i = 0; i < nstages; ++i) {
-      mbar_init(smem_u32(&bar_full[i]), C::kFullCount);
-      mbar_init(smem_u32(&bar_empty[i]), 1);  // the MMA thread's commit after the stage's last slice
+      // NVFP4: the weights' arrival; a stage is free once every warp of the
+      // warpgroups that dequantize its slices has read it.  BF16: the
+      // activations' arrival; freed by the MMA thread's commit.
+      mbar_init(smem_u32(&bar_full[i]), C::kFp4 ? 1 : C::kFullCount);
+      mbar_init(smem_u32(&bar_empty[i]), C::kFp4 ? 4 * kSPS : 1);
+    }
+    for (int i = 0; i < nx; ++i) {
+      mbar_init(smem_u32(&bar_xfull[i]), C::kFullCount);  // TMA: one arrival; gathers: 32 lanes + lane 0
+      mbar_init(smem_u32(&bar_xempty[i]), 1);
     }
     for (int i = 0; i < kNS; ++i) {
       mbar_init(smem_u32(&bar_afull[i]), 4);  // one arrival per warp of the slice's warpgroup
@@ -474,9 +515,22 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
     }
     pdl_wait();
     pre = __shfl_sync(0xFFFFFFFFu, pre, 0);
-    if constexpr (C::kXTma) {
-      // Dense activations: rows 0..M-1 of x, one TMA box {64 elements, kNT
-      // rows, 4 atoms} per stage (rows beyond M read as zeros).
+    if constexpr (C::kFp4) {
+      // Weight stages as their slots free up: a stage's slot once the
+      // dequant warps have read the stage that held it.
+      if (lane == 0) {
+        for (int s = pre; s < nst && !s_abort; ++s) {
+          if (s >= nstages &&
+              !mbar_wait_sleepy(smem_u32(&bar_empty[s % nstages]), ((s / nstages) & 1) ^ 1, p.err, 64)) {
+            s_abort = 1;
+            break;
+          }
+          issue_weights(wk, s);
+        }
+      }
+    } else {
+      // BF16 (dense): weights and activations of a stage share its slot;
+      // rows 0..M-1 of x, one TMA box {64 elements, kNT rows} per stage.
       if (lane == 0) {
         for (int s = 0; s < nst && !s_abort; ++s) {
           const int slot = s % nstages;
@@ -488,39 +542,52 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
           }
           const int k0 = wk.k_begin + s * C::kStageK;
           mbar_arrive_expect_tx(fb, C::kXBytes);
-          if constexpr (C::kFp4) {
-            tma_load_3d(st + C::kXOff, &p.tm_x, 0, 0, k0 / kSubK, fb, pol_x);
-          } else {
-            tma_load_2d(st + C::kXOff, &p.tm_x, k0, 0, fb, pol_x);
-          }
+          tma_load_2d(st + C::kXOff, &p.tm_x, k0, 0, fb, pol_x);
         }
       }
-    } else {
-      // Gathered activations (MoE): lane c copies 16-byte chunk c (of 32) of
-      // every B row of the stage, 128-byte swizzle.
+    }
+  } else if (warp == C::kXWarp) {
+    // ------------------------------------------------------------------ activation producer
+    // NVFP4: one 128-K slice per slot, issued once the MMAs of the slice
+    // that held the slot are done (dense: TMA by lane 0; MoE: cp.async
+    // gathers by all lanes).  Activations are read only after the wait for
+    // the previous grid.
+    if constexpr (C::kFp4) {
+      pdl_wait();
       const uint16_t* xb = wk.shared ? p.x2 : p.x;
-      const int u = lane / 8, cc = lane % 8;
-      for (int s = 0; s < nst && !s_abort; ++s) {
-        const int slot = s % nstages;
-        const uint32_t st = ring + slot * C::kStageBytes;
-        const uint32_t fb = smem_u32(&bar_full[slot]);
-        if (s >= pre) {
-          if (!mbar_wait_sleepy(smem_u32(&bar_empty[slot]), ((s / nstages) & 1) ^ 1, p.err, 64)) { s_abort = 1; break; }
-          if (lane == 0) issue_weights(wk, s);
-          __syncwarp();
+      for (int q = 0; q < nslices; ++q) {
+        const int xs = q % nx;
+        if (!__all_sync(0xFFFFFFFFu, !s_abort && (q < nx || mbar_wait_sleepy(smem_u32(&bar_xempty[xs]),
+                                                                               ((q / nx) & 1) ^ 1, p.err, 64)))) {
+          s_abort = 1;
+          break;
         }
-        const int k0 = wk.k_begin + s * C::kStageK;
-        const bool kok = lane * 8 < min(C::kStageK, wk.k_end - k0);
-        const uint16_t* src_k = xb + k0 + lane * 8;
-        const uint32_t dst0 = st + C::kXOff + u * (kNT * 128);
-#pragma unroll 8
-        for (int n = 0; n < kNT; ++n) {
-          const bool valid = kok && n < wk.ntok;
-          const uint32_t dst = dst0 + (n / 8) * 1024 + (n % 8) * 128 + ((cc ^ (n % 8)) * 16);
-          cp_async16(dst, valid ? src_k + wk.xoff[n] : xb, valid ? 16u : 0u);
+        const uint32_t dst0 = xring + xs * C::kXSliceBytes;
+        const uint32_t fb = smem_u32(&bar_xfull[xs]);
+        const int k0 = wk.k_begin + q * kSliceK;
+        if constexpr (C::kXTma) {
+          // rows 0..M-1 of x, one TMA box {64 elements, kNT rows, 2 atoms}
+          // (rows beyond M and K beyond the slab's end read as zeros)
+          if (lane == 0) {
+            mbar_arrive_expect_tx(fb, C::kXSliceBytes);
+            tma_load_3d(dst0, &p.tm_x, 0, 0, k0 / kSubK, fb, pol_x);
+          }
+        } else {
+          // gathered rows: lane = 16-byte chunk (of 16 per row slice) +
+          // 16 x row parity; 128-byte swizzle within each 64-K atom
+          const int cc = lane % 16, rh = lane / 16;
+          const bool kok = cc * 8 < min(kSliceK, wk.k_end - k0);
+          const uint16_t* src_k = xb + k0 + cc * 8;
+          const uint32_t dsta = dst0 + (cc / 8) * (kNT * 128);
+#pragma unroll 4
+          for (int n = rh; n < kNT; n += 2) {
+            const bool valid = kok && n < wk.ntok;
+            const uint32_t dst = dsta + (n / 8) * 1024 + (n % 8) * 128 + (((cc % 8) ^ (n % 8)) * 16);
+            cp_async16(dst, valid ? src_k + wk.xoff[n] : xb, valid ? 16u : 0u);
+          }
+          cp_async_arrive_noinc(fb);
+          if (lane == 0) mbar_arrive(fb);
         }
-        cp_async_arrive_noinc(fb);
-        if (lane == 0) mbar_arrive(fb);
       }
     }
   } else if (warp == C::kMmaWarp) {
@@ -532,9 +599,10 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
     // stepped by constants (issued from a loop that lane 0 runs alone,
     // building each descriptor, an MMA costs its thread ~300 cycles instead
     // of ~25).  NVFP4: per 128-K slice (a ring slot of tensor memory, filled
-    // by one warpgroup) 8 MMAs of K = 16 and one commit that frees the slot;
-    // one more commit per ring stage.  BF16: both operands in shared memory,
-    // 4 MMAs per 64-K stage.
+    // by one warpgroup) 8 MMAs of K = 16, one commit that frees the tensor
+    // memory slot and one that frees the slice's activation slot.  BF16: both
+    // operands in shared memory, 4 MMAs per 64-K stage and a commit that
+    // frees the stage.
     if (active) {
       constexpr uint32_t idesc = idesc_bf16_f32(128, kNT);
       const int klen = wk.k_end - wk.k_begin;
@@ -547,9 +615,8 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
             break;
           }
           tc_fence_after();
-          const int s = q / kSPS, u2 = q % kSPS;
           // the slice's two 64-K activation atoms
-          const uint32_t xs = ring + (s % nstages) * C::kStageBytes + C::kXOff + 2 * u2 * (kNT * 128);
+          const uint32_t xs = xring + (q % nx) * C::kXSliceBytes;
           const uint64_t b0 = sdesc_sw128(xs), b1 = sdesc_sw128(xs + kNT * 128);
           const bool full = klen - q * kSliceK >= kSliceK;  // else the last slice, 64 K
           const uint32_t a_tmem = tmem + C::kAccCols + a * C::kSlotCols;
@@ -560,7 +627,7 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
                 mma_ts(acc, a_tmem + kk * 8, (kk < 4 ? b0 : b1) + 2 * (kk % 4), idesc, (q > 0 || kk > 0) ? 1u : 0u);
             }
             mma_commit(smem_u32(&bar_aempty[a]));
-            if (q + 1 == nslices || (q + 1) / kSPS != s) mma_commit(smem_u32(&bar_empty[s % nstages]));
+            mma_commit(smem_u32(&bar_xempty[q % nx]));
           }
           __syncwarp();
         }
@@ -602,41 +669,83 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
       for (int q = w; q < nslices; q += kW) {
         const int s = q / kSPS, u2 = q % kSPS;
         const int slot = s % nstages;
-        const uint32_t st = ring + slot * C::kStageBytes;
+        const uint32_t st = ring + slot * wstage;
+        const uint32_t xs = xring + (q % nx) * C::kXSliceBytes;
         const int a = q % kNS;
         // Waits are bounded and made uniform over the warp (tcgen05.st is
         // warp-collective); a warp that gives up leaves the loop, and the
-        // MMA thread's wait on its slot then times out as well.
+        // MMA thread's wait on its slot then times out as well.  Each wait
+        // comes as late as the work allows: codes and scales are loaded and
+        // the stage released first, the first 32 weights dequantized before
+        // the tensor-memory slot is waited for, and the activations waited
+        // for only when they are permuted.  The activation slot's wait comes
+        // after the tensor-memory slot's: a parity wait is sound only once
+        // the slot's previous fill (slice q - nx) is known to have landed,
+        // which this warpgroup saw itself when nx is even (the slot holds
+        // only its slices) and which the tensor-memory slot's wait implies
+        // when nx = kSlots = 3 (slice q - 3 consumed).
         bool ok = !s_abort;
         if (ok && s != cur) {
           ok = mbar_wait_sleepy(smem_u32(&bar_full[slot]), (s / nstages) & 1, p.err, 20);
           cur = s;
         }
-        ok = __all_sync(0xFFFFFFFFu, ok);
-        if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait_sleepy(smem_u32(&bar_aempty[a]), ((q / kNS) & 1) ^ 1, p.err, 20));
-        if (!ok) {
+        if (!__all_sync(0xFFFFFFFFu, ok)) {
+          s_abort = 1;
+          break;
+        }
+        const int natoms = min(kSliceK, klen - q * kSliceK) / kSubK;  // 1 or 2
+        uint4 qc[2][2];
+        uint32_t sw[2] = {0u, 0u};
+        uint32_t dep = 0;
+#pragma unroll
+        for (int v = 0; v < 2; ++v) {
+          if (v < natoms) {
+            const int u = 2 * u2 + v;  // 64-K atom of the stage
+            qc[v][0] = lds128(st + w_row_off + (((2 * u) ^ i8) * 16));
+            qc[v][1] = lds128(st + w_row_off + (((2 * u + 1) ^ i8) * 16));
+            sw[v] = lds32(st + sf_row_off + u * 512);
+            dep ^= qc[v][0].x ^ qc[v][0].y ^ qc[v][0].z ^ qc[v][0].w ^ qc[v][1].x ^ qc[v][1].y ^ qc[v][1].z ^
+                   qc[v][1].w ^ sw[v];
+          }
+        }
+        // every lane's loads have returned (dep consumes them) before lane 0
+        // releases this warp's share of the stage
+        asm volatile("" ::"r"(dep) : "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bar_empty[slot]));
+        uint32_t sc[2][4];
+#pragma unroll
+        for (int v = 0; v < 2; ++v) {
+          scale_pair_to_bf16x2(sw[v] & 0xFFFFu, sc[v][0], sc[v][1]);
+          scale_pair_to_bf16x2(sw[v] >> 16, sc[v][2], sc[v][3]);
+        }
+        uint32_t o[16];
+        dequant32_perm(qc[0][0], sc[0][0], sc[0][1], o);
+        if (!__all_sync(0xFFFFFFFFu,
+                        !s_abort && mbar_wait_sleepy(smem_u32(&bar_aempty[a]), ((q / kNS) & 1) ^ 1, p.err, 20))) {
           s_abort = 1;
           break;
         }
         tc_fence_after();
-        const int natoms = min(kSliceK, klen - q * kSliceK) / kSubK;  // 1 or 2
         const uint32_t col0 = tmem + lane_base + C::kAccCols + a * C::kSlotCols;
+        tmem_st16(col0, o);
+        dequant32_perm(qc[0][1], sc[0][2], sc[0][3], o);
+        tmem_st16(col0 + 16, o);
+        if (natoms > 1) {
+          dequant32_perm(qc[1][0], sc[1][0], sc[1][1], o);
+          tmem_st16(col0 + 32, o);
+          dequant32_perm(qc[1][1], sc[1][2], sc[1][3], o);
+          tmem_st16(col0 + 48, o);
+        }
+        if (!__all_sync(0xFFFFFFFFu,
+                        !s_abort && mbar_wait_sleepy(smem_u32(&bar_xfull[q % nx]), (q / nx) & 1, p.err, 20))) {
+          s_abort = 1;
+          break;
+        }
+        // this warp's share of the slice's activations into the pairs' K order
         for (int v = 0; v < natoms; ++v) {
-          const int u = 2 * u2 + v;  // 64-K atom of the stage
-          // this warp's share of the atom's activations into the pairs' K order
-          const uint32_t xa = st + C::kXOff + u * (kNT * 128);
+          const uint32_t xa = xs + v * (kNT * 128);
           for (int c = i; c < kNT * 8; c += 128) sts128(xa + c * 16, perm_x8(lds128(xa + c * 16)));
-          const uint4 q0 = lds128(st + w_row_off + (((2 * u) ^ i8) * 16));
-          const uint4 q1 = lds128(st + w_row_off + (((2 * u + 1) ^ i8) * 16));
-          const uint32_t sw = lds32(st + sf_row_off + u * 512);
-          uint32_t s0, s1, s2, s3;
-          scale_pair_to_bf16x2(sw & 0xFFFFu, s0, s1);
-          scale_pair_to_bf16x2(sw >> 16, s2, s3);
-          uint32_t o[16];
-          dequant32_perm(q0, s0, s1, o);
-          tmem_st16(col0 + v * 32, o);
-          dequant32_perm(q1, s2, s3, o);
-          tmem_st16(col0 + v * 32 + 16, o);
         }
         tmem_wait_st();
         fence_proxy_async_smem();  // the permuted activations, before the MMAs read them

@@ -19,7 +19,9 @@ struct LaunchCfg {
 
 struct KernelInfo {
   int threads;
-  int stage_bytes;
+  int stage_bytes;    // tcgen05 BF16 / register-fed: ring stage; tcgen05 NVFP4: unused
+  int x_slice_bytes;  // tcgen05 NVFP4: one activation slot
+  int tmem_slots;     // tcgen05 NVFP4: tensor-memory A slots
   int red_bytes;
   int inbox_bytes;
   int tmem_cols;
@@ -76,6 +78,8 @@ cudaError_t run_gemv(const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info
   if (info) {
     info->threads = C::kThreads;
     info->stage_bytes = C::kStageBytes;
+    info->x_slice_bytes = C::kXSliceBytes;
+    info->tmem_slots = C::kSlots;
     info->red_bytes = C::kRedBytes;
     info->inbox_bytes = C::kInboxBytes;
     info->tmem_cols = C::kTmemCols;
