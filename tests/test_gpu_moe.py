@@ -92,6 +92,30 @@ def test_down_combine_small(fp4, M):
     assert fp4.get_device_error() == 0
 
 
+# Above 64 tokens both MoE kernels run on the tcgen05 path (chunks of up to
+# 32 pairs per expert); with 4 experts and top-2 each expert gets several
+# chunks and a ragged last one.
+@pytest.mark.parametrize("M", [72, 130])
+def test_gate_up_tcgen05_path(fp4, M):
+    d = make_moe(M, E=4, H=512, I=256, SI=384, topk=2, seed=300 + M)
+    act, sact = run_gate_up(fp4, d)
+    (an, al, ah), (sn, sl, sh), bad = ref_gate_up(d)
+    assert bad == 0
+    assert_close(u16(act), (an, al, ah), f"act M={M}")
+    assert_close(u16(sact), (sn, sl, sh), f"sact M={M}")
+    assert fp4.get_device_error() == 0
+
+
+@pytest.mark.parametrize("M", [72, 130])
+def test_down_combine_tcgen05_path(fp4, M):
+    d = make_moe(M, E=4, H=384, I=512, SI=256, topk=2, seed=400 + M)
+    out = run_down(fp4, d)
+    ref, bad = ref_down(d)
+    assert bad == 0
+    assert_close(u16(out), ref, f"down M={M}")
+    assert fp4.get_device_error() == 0
+
+
 def test_repeated_and_crowded_experts(fp4):
     # every token routes both slots to expert 3 (a repeated expert within a
     # token) and 40 tokens share it: its pair list spans several token tiles.
