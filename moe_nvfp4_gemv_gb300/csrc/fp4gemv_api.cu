@@ -228,7 +228,7 @@ TcRing size_ring(const KernelInfo& info, bool fp4w, int sf_slots, int S) {
       const int n = (avail - nx * info.x_slice_bytes) / r.wstage;
       return n > fp4::kMaxStages ? fp4::kMaxStages : n;
     };
-    r.nx = 4;
+    r.nx = fp4::kMaxXSlots;  // 4
     if (info.tmem_slots == 3 && stages(3) > stages(4)) r.nx = 3;
     if (stages(r.nx) < 2) r.nx = 2;
     r.nstages = stages(r.nx);

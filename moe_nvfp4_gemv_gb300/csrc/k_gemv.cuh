@@ -64,7 +64,7 @@ constexpr int kStageK16 = 64;   // K per ring stage, bf16 weights (128 B per row
 constexpr int kMaxNT = 128;
 constexpr int kMaxWG = 2;
 constexpr int kMaxSlots = 6;
-constexpr int kMaxXSlots = 8;   // activation slots (NVFP4 modes)
+constexpr int kMaxXSlots = 4;   // activation slots (NVFP4 modes; the host picks 2, 3 or 4)
 constexpr int kSliceK = 128;    // K per tensor-memory A slot (8 MMAs of K = 16 per commit)
 
 struct GemvParams {
