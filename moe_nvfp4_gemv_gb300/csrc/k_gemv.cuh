@@ -13,28 +13,32 @@
 // cluster split K and reduce their fp32 partials through distributed shared
 // memory in rank order (deterministic).
 //
-// Warp roles (kW dequant warpgroups, then a producer warp and an MMA warp):
-//   producer  lane 0 streams weight boxes (TMA, 128-byte swizzle) and the
+// Warp roles (kW dequant warpgroups, then a weight producer warp, an MMA
+// warp and, NVFP4 only, an activation producer warp):
+//   weights   lane 0 streams weight boxes (TMA, 128-byte swizzle) and the
 //             matching 512-byte scale chunks (bulk copies) into a ring of
-//             shared-memory stages of 256 K; with PDL these loads are issued
-//             before griddepcontrol.wait.  Activations follow after the wait
-//             into a ring of their own, one 128-K slice per slot (TMA for
-//             dense rows, cp.async gathers by all 32 lanes for MoE), so the
-//             weight ring, which hides HBM latency, is not shortened by
-//             activations that come from L2.
+//             shared-memory stages of 256 K; with PDL the first stages are
+//             issued before griddepcontrol.wait.  A stage is refilled once
+//             the dequant warps have read the stage that held its slot.
+//   activations  (NVFP4) after the wait, into a ring of their own, one 128-K
+//             slice per slot (TMA for dense rows, cp.async gathers by all 32
+//             lanes for MoE), refilled once the slice's MMAs are done, so
+//             the weight ring, which hides HBM latency, is not shortened by
+//             activations that come from L2.  BF16: a stage's activations
+//             travel in the weight stage, loaded by the weight producer.
 //   dequant   warpgroup w takes the 128-wide K slices q = w, w + kW, ...  For
 //             each slice thread i (row i) reads its code bytes and scale
-//             bytes, dequantizes them exactly to bf16 (dequant.cuh) and
-//             stores them with tcgen05.st into the slice's tensor-memory A
-//             slot (a ring of kSlots slots shared by the warpgroups); the
-//             warps also permute the slice's activations in shared memory to
-//             the weight pairs' K order, then arrive on the slot's barrier
-//             and free their share of the weight stage.
+//             bytes (then frees its warp's share of the weight stage),
+//             dequantizes them exactly to bf16 (dequant.cuh) and stores them
+//             with tcgen05.st into the slice's tensor-memory A slot (a ring
+//             of kSlots slots shared by the warpgroups); the warps also
+//             permute the slice's activations in shared memory to the weight
+//             pairs' K order, then arrive on the slot's barrier.
 //   MMA       the warp waits for each slot together and one elected lane
 //             issues the slot's eight K=16 tcgen05.mma into the fp32
-//             accumulator and frees the slot (and, once per stage, the ring
-//             stage) with tcgen05.commit, so the dequant warps never wait on
-//             MMA issue.
+//             accumulator and frees the tensor-memory slot and the slice's
+//             activation slot with tcgen05.commit, so the dequant warps never
+//             wait on MMA issue.
 //   epilogue  the dequant warps read the accumulator (tcgen05.ld), exchange
 //             partials through (distributed) shared memory and apply the
 //             mode's epilogue.
