@@ -247,5 +247,29 @@ def test_sweep_shape_sampled(fp4, M):
     assert_close(u16(got2)[:, rows], ref, f"sweep dequant_gemm M={M}")
 
 
+def _random_cases(n=20, seed=2024):
+    """Seeded random shapes over both kernels (M drawn from 1..16, 17..32
+    twice, 33..64 and 65..128 in turn):
+    N from 32 to 2048 (multiples of 32), K from 256 to 2048 (multiples of
+    64) -- small K runs unsplit, larger K in clusters of 2..8 ranks, and the
+    ring sizes, slot counts and reduction modes vary with them."""
+    rng = np.random.RandomState(seed)
+    cases = []
+    for i in range(n):
+        lo, hi = ((1, 17), (17, 33), (17, 33), (33, 65), (65, 129))[i % 5]
+        M = int(rng.randint(lo, hi))
+        cases.append((M, 32 * int(rng.randint(1, 65)), 64 * int(rng.randint(4, 33)), int(rng.randint(0, 2))))
+    return cases
+
+
+@pytest.mark.parametrize("M,N,K,silu", _random_cases())
+def test_random_shapes(fp4, M, N, K, silu):
+    x, w, sf = dense_inputs(M, N, K, seed=M + N + K)
+    gs = 0.01
+    got = fp4.nvfp4_gemv(x.to(DEV), w.to(DEV), sf.to(DEV), torch.tensor([gs], device=DEV), silu_mul=bool(silu))
+    ref = oracle.nvfp4_gemv(u16(x), w.numpy(), sf.numpy(), gs, silu_mul=bool(silu))
+    assert_close(u16(got), ref, f"M={M} N={N} K={K} silu={silu}")
+
+
 def test_no_device_errors(fp4):
     assert fp4.get_device_error() == 0
