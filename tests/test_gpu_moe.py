@@ -116,6 +116,36 @@ def test_down_combine_tcgen05_path(fp4, M):
     assert fp4.get_device_error() == 0
 
 
+def _random_moe_cases(n=8, seed=77):
+    """Seeded random MoE layers: tokens alternate between the register-fed
+    range (<= 64) and the tcgen05 range (> 64); E, top-k and the widths vary
+    (multiples of 64, at least 256 where the kernels require it)."""
+    rng = np.random.RandomState(seed)
+    cases = []
+    for i in range(n):
+        M = int(rng.randint(1, 65)) if i % 2 == 0 else int(rng.randint(65, 161))
+        E = int(rng.randint(2, 17))
+        topk = int(rng.randint(1, min(E, 4) + 1))
+        H, I, SI = (64 * int(rng.randint(4, 13)) for _ in range(3))
+        cases.append((M, E, topk, H, I, SI))
+    return cases
+
+
+@pytest.mark.parametrize("M,E,topk,H,I,SI", _random_moe_cases())
+def test_moe_random_shapes(fp4, M, E, topk, H, I, SI):
+    d = make_moe(M, E=E, H=H, I=I, SI=SI, topk=topk, seed=M * 31 + E)
+    act, sact = run_gate_up(fp4, d)
+    (an, al, ah), (sn, sl, sh), bad = ref_gate_up(d)
+    assert bad == 0
+    assert_close(u16(act), (an, al, ah), f"act M={M} E={E} topk={topk} H={H} I={I} SI={SI}")
+    assert_close(u16(sact), (sn, sl, sh), f"sact M={M} E={E} topk={topk} H={H} I={I} SI={SI}")
+    out = run_down(fp4, d)
+    ref, bad = ref_down(d)
+    assert bad == 0
+    assert_close(u16(out), ref, f"down M={M} E={E} topk={topk} H={H} I={I} SI={SI}")
+    assert fp4.get_device_error() == 0
+
+
 def test_repeated_and_crowded_experts(fp4):
     # every token routes both slots to expert 3 (a repeated expert within a
     # token) and 40 tokens share it: its pair list spans several token tiles.
