@@ -1,6 +1,7 @@
 /*
- * fp4gemv_plan.h -- the launch plan libfp4gemv's dense NVFP4 GEMV uses for
- * M <= 16 (the register-fed kernel), as a host-only function.
+ * fp4gemv_plan.h -- the launch plans libfp4gemv's dense GEMVs use, as
+ * host-only functions: the register-fed kernel's (NVFP4, M <= 16) and the
+ * tcgen05 kernel's (NVFP4 M > 16, BF16 weights).
  *
  * Operation: the grid decomposition of nvfp4_gemv (vllm.models.flint.ops.
  * nvfp4_gemv, nvfp4_gemv): which tile height and K split the library
@@ -35,6 +36,32 @@ typedef struct {
  * Returns FP4GEMV_ERR_INVALID_ARG for null pointers or sms < 1,
  * FP4GEMV_ERR_UNSUPPORTED_SHAPE for shapes fp4gemv_nvfp4_gemv rejects. */
 fp4gemv_status fp4gemv_plan_rf(int N, int K, int silu_mul, int sms, const int* cap, fp4gemv_rf_plan* out);
+
+typedef struct {
+  int tokens_tile;    /* MMA N of the tcgen05 kernel: 16, 32, 64 or 128 (covers M) */
+  int ctas_per_sm;    /* 2, or 1 when the tile's tensor memory needs more than 256 columns */
+  int tiles;          /* CTA tiles along N: 128 features, or 64 with silu_mul */
+  int split;          /* CTAs per cluster along K (1 .. 8) */
+  int k_slab;         /* K elements per cluster rank, a multiple of 64 */
+  int weight_stages;  /* weight ring stages of 256 K (2 .. 8) */
+  int act_slots;      /* NVFP4: activation slots of one 128-K slice (2 .. 4); BF16: 0 */
+  int scale_slots;    /* NVFP4: 2 KB scale groups per weight stage (1 .. 3) */
+  int inbox_in_ring;  /* 1: the split-K inbox reuses the drained ring (one rank) */
+  size_t smem_bytes;  /* dynamic shared memory per CTA */
+} fp4gemv_tc_plan;
+
+/* Plan of the tcgen05 kernel: fp4gemv_nvfp4_gemv for M > 16, and
+ * fp4gemv_bf16_gemv (bf16_weights = 1) for any M.  The launch uses exactly
+ * this plan; no GPU is needed to compute it.
+ *   M, N, K, silu_mul: as the GEMV call (same shape rules).
+ *   bf16_weights: 0 = NVFP4 weights, 1 = BF16 weights.
+ *   sms:  streaming multiprocessors of the GPU (152 on GB300).
+ *   out:  HOST pointer, filled on success.
+ * Returns FP4GEMV_ERR_INVALID_ARG for a null out, sms < 1 or flags outside
+ * {0, 1}, FP4GEMV_ERR_UNSUPPORTED_SHAPE for shapes the GEMV rejects and
+ * for NVFP4 weights with M <= 16 (the register-fed kernel; see
+ * fp4gemv_plan_rf). */
+fp4gemv_status fp4gemv_plan_tc(int M, int N, int K, int silu_mul, int bf16_weights, int sms, fp4gemv_tc_plan* out);
 
 #ifdef __cplusplus
 }

@@ -379,6 +379,31 @@ int balance_split(int S, int tiles, int K, int stage_k, int sms, int per_sm) {
   return c2 < c1 ? 2 : 1;
 }
 
+// The tcgen05 kernel's plan for an N x K weight (NVFP4 or BF16): tiles of
+// 128 features (64 with silu_mul), the K split, the scale groups a weight
+// stage holds (one 128-row group; with silu_mul the gate box's and the up
+// box's, a third when an up box straddles two) and the ring.
+struct TcPlan {
+  KernelInfo info{};
+  int per_sm = 2, tiles = 0, S = 1, kslab = 0, sf_slots = 1;
+  TcRing ring;
+};
+bool plan_tc(int kmode, int NT, bool fp4w, int N, int K, bool silu, int sms, TcPlan* tp) {
+  if (kernel_info(kmode, NT, &tp->info) != cudaSuccess) return false;
+  tp->per_sm = tc_ctas_per_sm(tp->info);
+  const int n_out = silu ? N / 2 : N;
+  const int box_rows = silu ? 64 : 128;
+  tp->tiles = (n_out + box_rows - 1) / box_rows;
+  const int stage_k = fp4w ? fp4::kStageK4 : fp4::kStageK16;
+  int S0 = pick_split(tp->tiles, K, stage_k, sms * tp->per_sm);
+  if (fp4w) S0 = balance_split(S0, tp->tiles, K, stage_k, sms, tp->per_sm);
+  tp->kslab = ((K + S0 - 1) / S0 + 63) / 64 * 64;
+  tp->S = (K + tp->kslab - 1) / tp->kslab;  // every cluster rank gets a non-empty K range
+  tp->sf_slots = silu ? ((N / 2) % 64 == 0 ? 2 : 3) : 1;
+  tp->ring = size_ring(tp->info, fp4w, tp->sf_slots, tp->S);
+  return true;
+}
+
 // The register-fed dense kernel's plan (tile height 16 cw, split, scale
 // groups per stage) for N x K on a GPU with `sms` SMs and cap[] co-resident
 // CTAs per cluster size.
@@ -421,43 +446,35 @@ fp4gemv_status dense_launch(int mode, const void* x, int64_t ldx, const void* w,
   const bool rf = fp4w && M <= 16;
   const int kmode = rf ? (M >= 3 && M <= 8 ? kDenseFp4RfCoop : kDenseFp4Rf) : mode;
   const int NT = rf ? (M <= 8 ? 8 : 16) : pick_nt(M);
-  KernelInfo info{};
-  if (kernel_info(kmode, NT, &info) != cudaSuccess) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
-  int nstages = 0, per_sm = 2, stage_bytes = 0, x_off = 0;
+  int nstages = 0, stage_bytes = 0, x_off = 0;
   size_t smem = 0;
   // A tile is `box_rows` weight rows per box: 128 output features (tcgen05),
   // or with silu_mul 64 features (64 gate rows + the 64 matching up rows, two
   // boxes); the register-fed kernel's tiles are 16 cw rows (see
   // pick_rf_geometry).
-  int cw = 8, S0 = 1;
+  int cw = 8, S0 = 1, kslab = 0;
+  TcPlan tp;  // tcgen05 kernel
+  TcRing& tr = tp.ring;
   if (rf) {
+    KernelInfo info{};
+    if (kernel_info(kmode, NT, &info) != cudaSuccess) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
     int cap[9];
     st = rf_capacity(NT, cap);
     if (st != FP4GEMV_OK) return st;
     int sf_groups = 1;
     plan_rf(N, K, silu_mul != 0, sms, cap, &cw, &S0, &sf_groups);
     size_ring_rf(info, 16 * cw * 128, sf_groups, &nstages, &smem, &stage_bytes, &x_off);
+    kslab = ((K + S0 - 1) / S0 + 63) / 64 * 64;
   } else {
-    per_sm = tc_ctas_per_sm(info);
+    if (!plan_tc(kmode, NT, fp4w, N, K, silu_mul != 0, sms, &tp)) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
+    nstages = tr.nstages;
+    smem = tr.smem;
+    kslab = tp.kslab;
   }
   const int box_rows = rf ? (silu_mul ? 8 * cw : 16 * cw) : (silu_mul ? 64 : 128);
   const int tiles = (n_out + box_rows - 1) / box_rows;
-  const int stage_k = fp4w ? fp4::kStageK4 : fp4::kStageK16;
-  if (!rf) {
-    S0 = pick_split(tiles, K, stage_k, sms * per_sm);
-    if (fp4w) S0 = balance_split(S0, tiles, K, stage_k, sms, per_sm);
-  }
-  const int kslab = ((K + S0 - 1) / S0 + 63) / 64 * 64;
   const int S = (K + kslab - 1) / kslab;  // every cluster rank gets a non-empty K range
-  // Scale groups a weight stage holds: one 128-row group; with silu_mul the
-  // gate box's and the up box's (a third when an up box straddles two).
-  const int sf_slots = silu_mul ? ((N / 2) % 64 == 0 ? 2 : 3) : 1;
-  TcRing tr;
-  if (!rf) {
-    tr = size_ring(info, fp4w, sf_slots, S);
-    nstages = tr.nstages;
-    smem = tr.smem;
-  }
+  const int sf_slots = tp.sf_slots;
 
   GemvParams p;
   std::memset(&p, 0, sizeof(p));
@@ -526,6 +543,31 @@ fp4gemv_status fp4gemv_plan_rf(int N, int K, int silu_mul, int sms, const int* c
   out->split = split;
   out->ctas = (n_out + feats - 1) / feats * split;
   out->scale_groups = groups;
+  return FP4GEMV_OK;
+}
+
+fp4gemv_status fp4gemv_plan_tc(int M, int N, int K, int silu_mul, int bf16_weights, int sms, fp4gemv_tc_plan* out) {
+  if (!out || sms < 1 || (silu_mul != 0 && silu_mul != 1) || (bf16_weights != 0 && bf16_weights != 1) || M < 1 ||
+      N < 1 || K < 1)
+    return FP4GEMV_ERR_INVALID_ARG;
+  const bool fp4w = bf16_weights == 0;
+  if (M > FP4GEMV_MAX_M || N % 16 != 0 || (silu_mul && N % 32 != 0) || K % 64 != 0 || (fp4w && K < 256) ||
+      (fp4w && M <= 16))
+    return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
+  const int NT = pick_nt(M);
+  TcPlan tp;
+  if (!plan_tc(fp4w ? fp4::kDenseFp4 : fp4::kDenseBf16, NT, fp4w, N, K, silu_mul != 0, sms, &tp))
+    return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
+  out->tokens_tile = NT;
+  out->ctas_per_sm = tp.per_sm;
+  out->tiles = tp.tiles;
+  out->split = tp.S;
+  out->k_slab = tp.kslab;
+  out->weight_stages = tp.ring.nstages;
+  out->act_slots = tp.ring.nx;
+  out->scale_slots = fp4w ? tp.sf_slots : 0;
+  out->inbox_in_ring = tp.S == 1 ? 1 : 0;
+  out->smem_bytes = tp.ring.smem;
   return FP4GEMV_OK;
 }
 

@@ -32,7 +32,7 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for want in ("fp4gemv_nvfp4_gemv", "fp4gemv_bf16_gemv", "fp4gemv_dequantize_rows", "fp4gemv_moe_gate_up",
                  "fp4gemv_moe_down_combine", "fp4gemv_scale_bytes", "fp4gemv_get_device_error",
-                 "fp4gemv_status_string", "fp4gemv_plan_rf"):
+                 "fp4gemv_status_string", "fp4gemv_plan_rf", "fp4gemv_plan_tc"):
         assert want in names
 
 

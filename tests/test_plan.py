@@ -94,3 +94,89 @@ def test_plan_invariants(plan_fn, silu):
             # room for every scale group any tile's boxes touch
             assert 1 <= p.scale_groups <= 4
             assert max(_groups_touched(N, silu, p.tile_rows, t) for t in range(tiles)) <= p.scale_groups
+
+
+# ---------------------------------------------------------------------------
+# The tcgen05 kernel's plan (fp4gemv_plan_tc): NVFP4 M > 16 and BF16 weights.
+
+class TcPlan(ctypes.Structure):
+    _fields_ = [("tokens_tile", ctypes.c_int), ("ctas_per_sm", ctypes.c_int), ("tiles", ctypes.c_int),
+                ("split", ctypes.c_int), ("k_slab", ctypes.c_int), ("weight_stages", ctypes.c_int),
+                ("act_slots", ctypes.c_int), ("scale_slots", ctypes.c_int), ("inbox_in_ring", ctypes.c_int),
+                ("smem_bytes", ctypes.c_size_t)]
+
+
+@pytest.fixture(scope="module")
+def tc_plan_fn():
+    from moe_nvfp4_gemv_gb300 import fp4gemv
+    f = fp4gemv.lib().fp4gemv_plan_tc
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_int] * 6 + [ctypes.POINTER(TcPlan)]
+
+    def plan(M, N, K, silu, bf16=0, sms=SMS):
+        out = TcPlan()
+        st = f(M, N, K, silu, bf16, sms, ctypes.byref(out))
+        return st, out
+    return plan
+
+
+@pytest.mark.parametrize("name,N,K,silu,split", [
+    ("8B gate_up", 28672, 4096, 1, 2),    # 224 tiles > 152 SMs: a split of two evens the load
+    ("8B qkv", 6144, 4096, 0, 4),
+    ("8B o_proj", 4096, 4096, 0, 8),
+    ("8B down", 4096, 14336, 0, 8),
+    ("70B gate_up", 57344, 8192, 1, 2),
+    ("70B qkv", 10240, 8192, 0, 2),
+])
+def test_tc_decode_layer_splits(tc_plan_fn, name, N, K, silu, split):
+    st, p = tc_plan_fn(32, N, K, silu)
+    assert st == 0 and p.split == split, name
+
+
+def _tc_cases():
+    rng = np.random.RandomState(5)
+    cases = [(M, N, K, s, b) for M in (17, 32, 33, 64, 65, 128) for (N, K) in
+             ((28672, 4096), (6144, 4096), (4096, 14336), (1056, 320), (96, 2304)) for s in (0, 1) for b in (0, 1)]
+    for _ in range(60):
+        cases.append((int(rng.randint(17, 129)), 32 * int(rng.randint(1, 1800)), 64 * int(rng.randint(4, 400)),
+                      int(rng.randint(0, 2)), int(rng.randint(0, 2))))
+    return cases
+
+
+@pytest.mark.parametrize("M,N,K,silu,bf16", _tc_cases())
+def test_tc_plan_invariants(tc_plan_fn, M, N, K, silu, bf16):
+    st, p = tc_plan_fn(M, N, K, silu, bf16)
+    assert st == 0
+    nt = 16 if M <= 16 else 32 if M <= 32 else 64 if M <= 64 else 128
+    assert p.tokens_tile == nt
+    # tensor memory: accumulator + A slots (3 up to 64 tokens, 6 above)
+    assert p.ctas_per_sm == (1 if (not bf16 and nt == 128) else 2)
+    n_out = N // 2 if silu else N
+    assert p.tiles == -(-n_out // (64 if silu else 128))
+    # the K split: ranks 1 .. 8, each with a non-empty range of whole atoms
+    assert 1 <= p.split <= 8 and p.k_slab % 64 == 0
+    assert (p.split - 1) * p.k_slab < K <= p.split * p.k_slab
+    assert 2 <= p.weight_stages <= 8
+    assert p.inbox_in_ring == (p.split == 1)
+    # shared memory: within one CTA's share (two CTAs per SM leave room for
+    # the kernel's static shared memory and the per-CTA reserve)
+    assert p.smem_bytes <= (110 * 1024 + 1024 if p.ctas_per_sm == 2 else 227 * 1024)
+    if bf16:
+        assert p.act_slots == 0 and p.scale_slots == 0
+    else:
+        assert p.scale_slots == ((2 if (N // 2) % 64 == 0 else 3) if silu else 1)
+        # activation slots: even (each warpgroup owns its slots) or 3 only
+        # with three tensor-memory slots (up to 64 tokens)
+        assert p.act_slots in (2, 3, 4) and (p.act_slots != 3 or nt <= 64)
+        ring = p.weight_stages * (16384 + 2048 * p.scale_slots) + p.act_slots * nt * 256
+        assert ring + 1024 <= p.smem_bytes
+
+
+def test_tc_plan_rejects(tc_plan_fn):
+    assert tc_plan_fn(16, 4096, 4096, 0)[0] == 2      # NVFP4 M <= 16: the register-fed kernel
+    assert tc_plan_fn(16, 4096, 4096, 0, bf16=1)[0] == 0
+    assert tc_plan_fn(129, 4096, 4096, 0)[0] == 2     # M > 128
+    assert tc_plan_fn(32, 4104, 4096, 0)[0] == 2      # N % 16
+    assert tc_plan_fn(32, 4096, 4096, 2)[0] == 1
+    assert tc_plan_fn(32, 4096, 4096, 0, bf16=2)[0] == 1
+    assert tc_plan_fn(32, 4096, 4096, 0, sms=0)[0] == 1
