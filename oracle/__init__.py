@@ -10,9 +10,14 @@ releases the GIL during each foreign call).
 Conventions: bf16 tensors are numpy ``uint16`` bit patterns; weights, scales
 are ``uint8``; every result is a triple ``(nominal, lo, hi)`` of bf16 bit
 arrays -- ``nominal`` is the pages' formula with exact arithmetic and
-round-to-nearest-even at each rounding the pages name, ``[lo, hi]`` the
-values an fp32-accumulating implementation may legally produce when an
-intermediate bf16 rounding sits inside the accumulation-error window.
+round-to-nearest-even at each rounding the pages name; ``[lo, hi]`` is the
+hull of the outputs reached when an INTERMEDIATE bf16 rounding the pages
+name (G / U before silu_mul; y_j, y_shared and the top-k sum in
+down_combine) takes its other neighbour because the exact value lies next to
+a rounding midpoint (within 2^-16 relative for the dot products, within the
+rigorous fp32 bound for the top-k sum).  Outputs without such an
+intermediate (the plain dense GEMV, bf16_gemv, the routed gate_up) always
+have lo == hi == nominal.
 
 Sources (title / section): vllm.models.flint.ops.nvfp4_gemv (module docstring,
 nvfp4_gemv, bf16_gemv, dequantize_rows), vllm.models.flint.ops.linear
@@ -73,9 +78,11 @@ def _load():
                 "orc_unswz": (None, [_i64, _i64, ctypes.POINTER(_i64), ctypes.POINTER(_i64)]),
                 "orc_w1_row": (_i64, [_i64, ctypes.c_int]),
                 "orc_dequant_rows": (None, [_vp, _vp, _i64, _i64, _i64, _vp, _vp]),
-                "orc_gemv_acc": (None, [_vp, _i64, _i64, _vp, _vp, _i64, _vp, _i64, _vp, _vp, _vp]),
-                "orc_bf16_gemv_acc": (None, [_vp, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _vp]),
-                "orc_dense_epilogue": (None, [_vp, _vp, _i64, _i64, _i64, _dbl, ctypes.c_int, _vp, _vp, _vp]),
+                "orc_round_intermediate": (None, [_dbl, _dbl, ctypes.POINTER(ctypes.c_uint16),
+                                                  ctypes.POINTER(ctypes.c_uint16)]),
+                "orc_gemv_acc": (None, [_vp, _i64, _i64, _vp, _vp, _i64, _vp, _i64, _vp, _vp]),
+                "orc_bf16_gemv_acc": (None, [_vp, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _vp]),
+                "orc_dense_epilogue": (None, [_vp, _i64, _i64, _dbl, ctypes.c_int, _vp, _vp, _vp]),
                 "orc_moe_gate_up_routed": (ctypes.c_int, [_vp, _vp, _i64, _vp, _vp, _vp, _i64, _i64, _i64,
                                                           _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
                 "orc_moe_gate_up_shared": (None, [_vp, _i64, _i64, _vp, _vp, _dbl, _i64, _i64, _vp, _vp,
@@ -148,6 +155,18 @@ def unswz(off: int, K: int) -> tuple[int, int]:
     return r.value, kb.value
 
 
+def round_intermediate(v: float, eps: float) -> tuple[int, int]:
+    """(nominal, alternative) bf16 bits of an intermediate value v: the
+    alternative is the other neighbour when a rounding midpoint lies within
+    eps of v, else the nominal rounding again."""
+    n, a = ctypes.c_uint16(), ctypes.c_uint16()
+    _load().orc_round_intermediate(float(v), float(eps), ctypes.byref(n), ctypes.byref(a))
+    return int(n.value), int(a.value)
+
+
+INTERMEDIATE_REL_WINDOW = 2.0 ** -16
+
+
 def w1_row(i: int, up: bool) -> int:
     return int(_load().orc_w1_row(i, 1 if up else 0))
 
@@ -194,24 +213,36 @@ def _dense(acc_fn, x, K, N, gs, silu_mul, rows, threads):
         wrows = outs
     nr = wrows.size
     acc = np.empty((M, nr), np.float64)
-    absacc = np.empty((M, nr), np.float64)
     t = _threads(threads)
 
     def work(a, b):
         sub = np.ascontiguousarray(wrows[a:b])
         tmp = np.empty(K, np.float64)
         pa = np.empty((M, b - a), np.float64)
-        pb = np.empty((M, b - a), np.float64)
-        acc_fn(x, sub, tmp, pa, pb)
+        acc_fn(x, sub, tmp, pa)
         acc[:, a:b] = pa
-        absacc[:, a:b] = pb
 
     _run(work, _chunks(nr, 4 * t), t)
     nc = outs.size
     nom, lo, hi = (np.empty((M, nc), np.uint16) for _ in range(3))
-    lib.orc_dense_epilogue(_p(acc), _p(absacc), M, nr, K, float(gs), 1 if silu_mul else 0,
-                           _p(nom), _p(lo), _p(hi))
+    lib.orc_dense_epilogue(_p(acc), M, nr, float(gs), 1 if silu_mul else 0, _p(nom), _p(lo), _p(hi))
     return nom, lo, hi
+
+
+def dense_acc(x, w, sf, rows=None, threads=None) -> np.ndarray:
+    """The exact float64 accumulators acc[m, i] = x[m] . dequant(W)[rows[i]]
+    (all rows when ``rows`` is None), before any scale or rounding."""
+    lib = _load()
+    w = np.ascontiguousarray(w, np.uint8)
+    sf = np.ascontiguousarray(sf, np.uint8).reshape(-1)
+    x = np.ascontiguousarray(x, np.uint16)
+    N, K = w.shape[0], w.shape[1] * 2
+    M = x.shape[0]
+    wrows = np.arange(N, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, np.int64)
+    acc = np.empty((M, wrows.size), np.float64)
+    tmp = np.empty(K, np.float64)
+    lib.orc_gemv_acc(_p(x), K, M, _p(w), _p(sf), K, _p(wrows), wrows.size, _p(tmp), _p(acc))
+    return acc
 
 
 def nvfp4_gemv(x, w, sf, global_scale: float, silu_mul: bool = False, rows=None, threads=None):
@@ -222,8 +253,8 @@ def nvfp4_gemv(x, w, sf, global_scale: float, silu_mul: bool = False, rows=None,
     sf = np.ascontiguousarray(sf, np.uint8).reshape(-1)
     N, K = w.shape[0], w.shape[1] * 2
 
-    def acc_fn(xx, sub, tmp, pa, pb):
-        lib.orc_gemv_acc(_p(xx), K, xx.shape[0], _p(w), _p(sf), K, _p(sub), sub.size, _p(tmp), _p(pa), _p(pb))
+    def acc_fn(xx, sub, tmp, pa):
+        lib.orc_gemv_acc(_p(xx), K, xx.shape[0], _p(w), _p(sf), K, _p(sub), sub.size, _p(tmp), _p(pa))
 
     return _dense(acc_fn, x, K, N, global_scale, silu_mul, rows, threads)
 
@@ -235,8 +266,8 @@ def bf16_gemv(x, w, silu_mul: bool = False, rows=None, threads=None, global_scal
     w = np.ascontiguousarray(w, np.uint16)
     N, K = w.shape
 
-    def acc_fn(xx, sub, tmp, pa, pb):
-        lib.orc_bf16_gemv_acc(_p(xx), K, xx.shape[0], _p(w), K, _p(sub), sub.size, _p(tmp), _p(pa), _p(pb))
+    def acc_fn(xx, sub, tmp, pa):
+        lib.orc_bf16_gemv_acc(_p(xx), K, xx.shape[0], _p(w), K, _p(sub), sub.size, _p(tmp), _p(pa))
 
     return _dense(acc_fn, x, K, N, global_scale, silu_mul, rows, threads)
 
@@ -340,9 +371,12 @@ def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
 
 
 def check(gpu_bits: np.ndarray, ref, rel: float = 2.0 ** -7, rms_frac: float = 2.0 ** -10):
-    """Acceptance rule: |gpu - [lo, hi]| <= rel * |nominal| + rms_frac * rms(nominal)
-    element-wise, where the distance to the interval is 0 inside it.
-    Returns (ok, worst_excess, n_bad, first_bad_index)."""
+    """Acceptance rule, per element: |gpu - [lo, hi]| <= rel * |nominal| +
+    rms_frac * rms(nominal), the distance to the interval being 0 inside it.
+    For an output without an intermediate rounding lo == hi == nominal, so
+    this is exactly |gpu - nominal| <= 2^-7 |nominal| + 2^-10 rms(nominal);
+    otherwise [lo, hi] holds only the outputs of the intermediates'
+    alternative roundings.  Returns (ok, worst_excess, n_bad, first_bad_index)."""
     nom, lo, hi = (bf16_to_f64(r) for r in ref)
     g = bf16_to_f64(gpu_bits)
     lo_, hi_ = np.minimum(lo, hi), np.maximum(lo, hi)

@@ -22,14 +22,19 @@
  * explicitly, each as ONE rounding from the double value (no double rounding
  * through float on the way to bf16).
  *
- * Rounding windows: where the pages round an intermediate to bf16 (the gate /
- * up outputs before silu_mul, y_j, y_shared and the top-k sum in
- * down_combine), an fp32-accumulating implementation may legitimately land on
- * the other side of a bf16 rounding boundary.  Every such intermediate is
- * carried as an interval [lo, hi] obtained by rounding (v - err) and
- * (v + err), where err bounds the fp32 accumulation error of the exact value
- * v.  Final outputs are reported as (nominal, lo, hi); lo == hi == nominal
- * whenever no intermediate is ambiguous.
+ * Alternatives at intermediate roundings: the pages round some intermediate
+ * values to bf16 before the output is formed (the gate / up outputs before
+ * silu_mul, y_j, y_shared and the top-k sum in down_combine).  An
+ * fp32-accumulating implementation computes such a value with a tiny
+ * relative error, so where the exact value lies next to a bf16 rounding
+ * midpoint both neighbours are correct.  Each such intermediate carries the
+ * other neighbour as an alternative (relative window 2^-16 for the long dot
+ * products; the rigorous fp32 bound for the top-k sum), and each output
+ * reports (nominal, lo, hi): nominal takes every intermediate at its own
+ * rounding, [lo, hi] is the hull of the outputs over the alternatives.
+ * Final roundings get no window: an output with no intermediate rounding
+ * has lo == hi == nominal, and the acceptance rule compares it with the
+ * nominal value under the stated per-element tolerance.
  *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared (no fast-math).
  */
@@ -143,7 +148,8 @@ void orc_unswz(int64_t off, int64_t K, int64_t* r, int64_t* kb)
 /* ------------------------------------------------------------------------ */
 
 /* code(W, n, k): element 2j is the LOW nibble of byte j [nvfp4_gemv, module
- * docstring: "two E2M1 codes per byte, low nibble first"]. */
+ * docstring: each byte packs two E2M1 codes, the lower-indexed one in the low
+ * nibble]. */
 static int fp4_code(const uint8_t* wrow, int64_t k)
 {
     uint8_t b = wrow[k / 2];
@@ -151,7 +157,8 @@ static int fp4_code(const uint8_t* wrow, int64_t k)
 }
 
 /* Wd[r, k] = e2m1(code) * e4m3(scale(r, k/16)), exact in double and in bf16
- * [nvfp4_gemv, module docstring "dequantized exactly to BF16 (e2m1 * e4m3)"]. */
+ * [nvfp4_gemv, module docstring: the product of the two is the weight, with
+ * no rounding]. */
 static void dequant_row(const uint8_t* w, const uint8_t* sf, int64_t r, int64_t K, double* out)
 {
     const uint8_t* wrow = w + r * (K / 2);
@@ -172,129 +179,124 @@ void orc_dequant_rows(const uint8_t* w, const uint8_t* sf, int64_t K, int64_t r0
     }
 }
 
-/* ------------------------------------------------------------------------ */
 /* Dot products                                                              */
 /* ------------------------------------------------------------------------ */
 
-/* acc = sum_k x[k] * wd[k] in double; abs = sum_k |x[k] * wd[k]|. */
-static void dot(const uint16_t* x, const double* wd, int64_t K, double* acc, double* abs_)
+/* sum_k x[k] * wd[k] in double. */
+static double dot(const uint16_t* x, const double* wd, int64_t K)
 {
-    double a = 0.0, b = 0.0;
-    for (int64_t k = 0; k < K; ++k) {
-        double p = bf16_to_double(x[k]) * wd[k];
-        a += p;
-        b += fabs(p);
-    }
-    *acc = a;
-    *abs_ = b;
-}
-
-/* Bound on |fp32-accumulated sum - exact sum| for a K-term sum accumulated
- * in fp32 16 terms at a time, plus a handful of extra partial-sum additions
- * (split-K reductions).  Used only to open rounding windows. */
-static double acc_err(double abs_, int64_t K)
-{
-    return 4.0 * ((double)(K / 16) + 32.0) * ldexp(1.0, -24) * abs_;
+    double a = 0.0;
+    for (int64_t k = 0; k < K; ++k) a += bf16_to_double(x[k]) * wd[k];
+    return a;
 }
 
 /* Dense NVFP4 accumulators for rows in `rows[0..nrows)`: acc[m * nrows + i]
  * = sum_k x[m, k] * Wd[rows[i], k] [nvfp4_gemv, nvfp4_gemv]. */
 void orc_gemv_acc(const uint16_t* x, int64_t ldx, int64_t M, const uint8_t* w, const uint8_t* sf,
-                  int64_t K, const int64_t* rows, int64_t nrows, double* tmp, double* acc,
-                  double* absacc)
+                  int64_t K, const int64_t* rows, int64_t nrows, double* tmp, double* acc)
 {
     for (int64_t i = 0; i < nrows; ++i) {
         dequant_row(w, sf, rows[i], K, tmp);
-        for (int64_t m = 0; m < M; ++m) dot(x + m * ldx, tmp, K, &acc[m * nrows + i], &absacc[m * nrows + i]);
+        for (int64_t m = 0; m < M; ++m) acc[m * nrows + i] = dot(x + m * ldx, tmp, K);
     }
 }
 
 /* Dense BF16-weight accumulators [nvfp4_gemv, bf16_gemv]: W is bf16 [N, K]. */
 void orc_bf16_gemv_acc(const uint16_t* x, int64_t ldx, int64_t M, const uint16_t* w, int64_t K,
-                       const int64_t* rows, int64_t nrows, double* tmp, double* acc, double* absacc)
+                       const int64_t* rows, int64_t nrows, double* tmp, double* acc)
 {
     for (int64_t i = 0; i < nrows; ++i) {
         for (int64_t k = 0; k < K; ++k) tmp[k] = bf16_to_double(w[rows[i] * K + k]);
-        for (int64_t m = 0; m < M; ++m) dot(x + m * ldx, tmp, K, &acc[m * nrows + i], &absacc[m * nrows + i]);
+        for (int64_t m = 0; m < M; ++m) acc[m * nrows + i] = dot(x + m * ldx, tmp, K);
     }
 }
 
 /* ------------------------------------------------------------------------ */
-/* Epilogues                                                                 */
+/* Roundings                                                                 */
 /* ------------------------------------------------------------------------ */
 
-/* Next / previous bf16 bit pattern in value order (finite, non-NaN). */
+/* Next bf16 bit pattern in value order (finite, non-NaN). */
 static uint16_t bf16_next_up(uint16_t h)
 {
     if (h == 0x8000u) return 0x0000u;
     return (h & 0x8000u) ? (uint16_t)(h - 1) : (uint16_t)(h + 1);
 }
 
-static int bf16_le(uint16_t a, uint16_t b) { return bf16_to_double(a) <= bf16_to_double(b); }
+/* Relative half-width of the window around an intermediate bf16 rounding of
+ * a long fp32 dot product (G and U before silu_mul, y_j and y_shared in
+ * down_combine).  An fp32-accumulating implementation reaches such a value
+ * with a small relative error; when the exact value lies within this
+ * distance of a bf16 rounding midpoint, both neighbours are correct roundings
+ * of a correct fp32 result. */
+#define INTERMEDIATE_REL_WINDOW 0x1p-16
 
-/* y = bf16(f32(f32(acc) * s)), with its rounding window [lo, hi]
- * [nvfp4_gemv, module docstring: "the FP32 global scale is applied to the
- * FP32 accumulator before the single output rounding to BF16"]. */
-static void scaled_out(double acc, double abs_, int64_t K, double s, uint16_t* nom, uint16_t* lo,
-                       uint16_t* hi)
+/* Round an intermediate v to bf16: *nom is the rounding of v itself, *alt
+ * the other neighbour when a rounding midpoint lies within eps of v (else
+ * *alt = *nom).  eps must be well below half a bf16 ulp. */
+void orc_round_intermediate(double v, double eps, uint16_t* nom, uint16_t* alt)
+{
+    uint16_t n = orc_bf16_rne(v), a = orc_bf16_rne(v - eps), b = orc_bf16_rne(v + eps);
+    *nom = n;
+    *alt = (a != n) ? a : b;
+}
+
+/* y = bf16(f32(f32(acc) * s)) as an intermediate: nominal and alternative. */
+static void scaled_intermediate(double acc, double s, uint16_t* nom, uint16_t* alt)
 {
     double v = f32(f32(acc) * s);
-    double e = acc_err(abs_, K) * fabs(s) + ldexp(fabs(v), -22);
-    *nom = orc_bf16_rne(v);
-    *lo = orc_bf16_rne(v - e);
-    *hi = orc_bf16_rne(v + e);
+    orc_round_intermediate(v, INTERMEDIATE_REL_WINDOW * fabs(v), nom, alt);
 }
 
 /* SiLU evaluated exactly (double): x / (1 + exp(-x)). */
 static double silu(double g) { return g / (1.0 + exp(-g)); }
 
-/* silu_mul of two bf16 intervals: out = bf16(silu(G) * U) for every G in
- * [glo, ghi], U in [ulo, uhi] (bf16 grid points), with a small fp32
- * evaluation allowance; returns nominal (from gn, un) and the hull. */
-static void silu_mul_interval(uint16_t gn, uint16_t glo, uint16_t ghi, uint16_t un, uint16_t ulo,
-                              uint16_t uhi, uint16_t* nom, uint16_t* lo, uint16_t* hi)
+static void hull_add(uint16_t v, uint16_t* lo, uint16_t* hi)
 {
-    double vn = silu(bf16_to_double(gn)) * bf16_to_double(un);
-    double vmin = INFINITY, vmax = -INFINITY;
-    int ng = 0;
-    *nom = orc_bf16_rne(vn);
-    for (uint16_t g = glo;; g = bf16_next_up(g)) {
-        int nu = 0;
-        for (uint16_t u = ulo;; u = bf16_next_up(u)) {
-            double v = silu(bf16_to_double(g)) * bf16_to_double(u);
-            double e = ldexp(fabs(v), -20) + ldexp(1.0, -140);
-            if (v - e < vmin) vmin = v - e;
-            if (v + e > vmax) vmax = v + e;
-            if (u == uhi || ++nu > 64) break;
-        }
-        if (g == ghi || ++ng > 64) break;
-    }
-    *lo = orc_bf16_rne(vmin);
-    *hi = orc_bf16_rne(vmax);
-    if (!bf16_le(*lo, *nom)) *lo = *nom;
-    if (!bf16_le(*nom, *hi)) *hi = *nom;
+    if (bf16_to_double(v) < bf16_to_double(*lo)) *lo = v;
+    if (bf16_to_double(v) > bf16_to_double(*hi)) *hi = v;
 }
 
-/* Dense epilogue [nvfp4_gemv, nvfp4_gemv "silu_mul"]:
- *   silu == 0: out[m, i] = bf16(f32(f32(acc) * gs)), i over nrows.
+/* out = bf16(silu(G) * U) for G in {gn, ga}, U in {un, ua} (the bf16 outputs
+ * of the gate and up rows, each with its alternative rounding): the nominal
+ * value from (gn, un) and the hull of all four. */
+static void silu_mul_out(uint16_t gn, uint16_t ga, uint16_t un, uint16_t ua, uint16_t* nom, uint16_t* lo,
+                         uint16_t* hi)
+{
+    const uint16_t gs_[2] = {gn, ga}, us_[2] = {un, ua};
+    *nom = orc_bf16_rne(silu(bf16_to_double(gn)) * bf16_to_double(un));
+    *lo = *hi = *nom;
+    for (int i = 0; i < 2; ++i)
+        for (int j = 0; j < 2; ++j)
+            hull_add(orc_bf16_rne(silu(bf16_to_double(gs_[i])) * bf16_to_double(us_[j])), lo, hi);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Epilogues                                                                 */
+/* ------------------------------------------------------------------------ */
+
+/* Dense epilogue [nvfp4_gemv, module docstring: the fp32 accumulator is
+ * multiplied by the fp32 global scale and rounded to bf16 once; nvfp4_gemv,
+ * the silu_mul flag]:
+ *   silu == 0: out[m, i] = bf16(f32(f32(acc) * gs)), one rounding, no
+ *   alternative (lo == hi == nom).
  *   silu != 0: the accumulators hold gate rows in columns [0, half) and the
  *   matching up rows in [half, 2 half); G, U are the bf16 outputs and
- *   out[m, i] = bf16(silu(G) * U) ("exact SiLU, one BF16 rounding"). */
-void orc_dense_epilogue(const double* acc, const double* absacc, int64_t M, int64_t ncols, int64_t K,
-                        double gs, int silu_mul, uint16_t* nom, uint16_t* lo, uint16_t* hi)
+ *   out[m, i] = bf16(silu(G) * U) (exact SiLU, rounded once); [lo, hi]
+ *   is the hull over the alternative roundings of G and U. */
+void orc_dense_epilogue(const double* acc, int64_t M, int64_t ncols, double gs, int silu_mul, uint16_t* nom,
+                        uint16_t* lo, uint16_t* hi)
 {
     if (!silu_mul) {
-        for (int64_t i = 0; i < M * ncols; ++i) scaled_out(acc[i], absacc[i], K, gs, &nom[i], &lo[i], &hi[i]);
+        for (int64_t i = 0; i < M * ncols; ++i) nom[i] = lo[i] = hi[i] = orc_bf16_rne(f32(f32(acc[i]) * gs));
         return;
     }
     int64_t half = ncols / 2;
     for (int64_t m = 0; m < M; ++m)
         for (int64_t i = 0; i < half; ++i) {
-            uint16_t gn, gl, gh, un, ul, uh;
-            int64_t a = m * ncols + i, b = m * ncols + half + i;
-            scaled_out(acc[a], absacc[a], K, gs, &gn, &gl, &gh);
-            scaled_out(acc[b], absacc[b], K, gs, &un, &ul, &uh);
-            silu_mul_interval(gn, gl, gh, un, ul, uh, &nom[m * half + i], &lo[m * half + i], &hi[m * half + i]);
+            uint16_t gn, ga, un, ua;
+            scaled_intermediate(acc[m * ncols + i], gs, &gn, &ga);
+            scaled_intermediate(acc[m * ncols + half + i], gs, &un, &ua);
+            silu_mul_out(gn, ga, un, ua, &nom[m * half + i], &lo[m * half + i], &hi[m * half + i]);
         }
 }
 
@@ -313,8 +315,9 @@ int64_t orc_w1_row(int64_t i, int up)
 
 /* gate_up [moe_gemv, gate_up], pairs p in [p0, p1) (p = t * topk + j):
  *   e = ids[p]; g, u = f32(acc) * alpha[e] in fp32 (not rounded to bf16);
- *   act[p, i] = bf16(silu(g) * u) (the pages use an approximate sigmoid;
- *   the oracle uses the exact one and the tolerance covers the difference).
+ *   act[p, i] = bf16(silu(g) * u), one rounding, no alternative (the pages
+ *   use an approximate sigmoid; the oracle uses the exact one and the
+ *   output tolerance covers the difference).
  * Out-of-range expert ids leave the row untouched and return nonzero. */
 int orc_moe_gate_up_routed(const uint16_t* x, const int32_t* ids, int64_t topk, const uint8_t* w1,
                            const uint8_t* w1_sf, const float* alpha, int64_t E, int64_t H, int64_t I,
@@ -330,22 +333,12 @@ int orc_moe_gate_up_routed(const uint16_t* x, const int32_t* ids, int64_t topk, 
         const uint8_t* se = w1_sf + e * sfe;
         double a = (double)alpha[e];
         for (int64_t i = 0; i < I; ++i) {
-            double ag, bg, au, bu;
             dequant_row(we, se, orc_w1_row(i, 0), H, tmp_g);
             dequant_row(we, se, orc_w1_row(i, 1), H, tmp_u);
-            dot(x + t * H, tmp_g, H, &ag, &bg);
-            dot(x + t * H, tmp_u, H, &au, &bu);
-            double g = f32(f32(ag) * a), u = f32(f32(au) * a);
-            double eg = acc_err(bg, H) * fabs(a) + ldexp(fabs(g), -22);
-            double eu = acc_err(bu, H) * fabs(a) + ldexp(fabs(u), -22);
-            double v = silu(g) * u;
-            /* |d silu/dg| <= 1.1; allowance for an approximate sigmoid of
-             * relative accuracy 2^-18. */
-            double e_ = 1.1 * fabs(u) * eg + fabs(silu(g)) * eu + ldexp(fabs(v), -18) + ldexp(1.0, -140);
+            double g = f32(f32(dot(x + t * H, tmp_g, H)) * a);
+            double u = f32(f32(dot(x + t * H, tmp_u, H)) * a);
             int64_t o = p * I + i;
-            nom[o] = orc_bf16_rne(v);
-            lo[o] = orc_bf16_rne(v - e_);
-            hi[o] = orc_bf16_rne(v + e_);
+            nom[o] = lo[o] = hi[o] = orc_bf16_rne(silu(g) * u);
         }
     }
     return bad;
@@ -360,25 +353,27 @@ void orc_moe_gate_up_shared(const uint16_t* x, int64_t t0, int64_t t1, const uin
 {
     for (int64_t t = t0; t < t1; ++t)
         for (int64_t i = 0; i < SI; ++i) {
-            double ag, bg, au, bu;
-            uint16_t gn, gl, gh, un, ul, uh;
+            uint16_t gn, ga, un, ua;
             dequant_row(wsh, ssh, i, H, tmp_g);
             dequant_row(wsh, ssh, SI + i, H, tmp_u);
-            dot(x + t * H, tmp_g, H, &ag, &bg);
-            dot(x + t * H, tmp_u, H, &au, &bu);
-            scaled_out(ag, bg, H, gssh, &gn, &gl, &gh);
-            scaled_out(au, bu, H, gssh, &un, &ul, &uh);
-            silu_mul_interval(gn, gl, gh, un, ul, uh, &nom[t * SI + i], &lo[t * SI + i], &hi[t * SI + i]);
+            scaled_intermediate(dot(x + t * H, tmp_g, H), gssh, &gn, &ga);
+            scaled_intermediate(dot(x + t * H, tmp_u, H), gssh, &un, &ua);
+            silu_mul_out(gn, ga, un, ua, &nom[t * SI + i], &lo[t * SI + i], &hi[t * SI + i]);
         }
 }
 
-/* down_combine [moe_gemv, down_combine], tokens t in [t0, t1):
+/* down_combine [moe_gemv, module docstring and down_combine], tokens t in
+ * [t0, t1):
  *   y_j  = bf16(f32(act[t*topk+j] @ W2[e_j]^T) * alpha2[e_j])
  *   y_sh = bf16(f32(sact[t] @ Wsd^T) * gssd)
  *   s    = bf16(sum_j tw[t, j] * y_j)      (fp32 sum, j = 0 .. topk-1)
  *   out  = bf16(s + y_sh)
- * Each bf16 intermediate is carried as [lo, hi]; tw may have any sign.
- * Tokens with an out-of-range id are skipped; returns nonzero if any. */
+ * The nominal output takes every intermediate at its own rounding.  [lo, hi]
+ * is the hull of the outputs over the alternatives: y_j and y_sh at their
+ * alternative roundings, and every bf16 rounding of an fp32 sum of the
+ * chosen tw_j * y_j (topk fused multiply-adds, each within 2^-24 of the
+ * running sum).  tw may have any sign.  Tokens with an out-of-range id are
+ * skipped; returns nonzero if any. */
 int orc_moe_down_combine(const uint16_t* act, const int32_t* ids, const float* tw, int64_t topk,
                          const uint8_t* w2, const uint8_t* w2_sf, const float* alpha2, int64_t E,
                          int64_t H, int64_t I, const uint16_t* sact, const uint8_t* wsd,
@@ -396,33 +391,32 @@ int orc_moe_down_combine(const uint16_t* act, const int32_t* ids, const float* t
             double sn = 0.0, slo = 0.0, shi = 0.0, sabs = 0.0;
             for (int64_t j = 0; j < topk; ++j) {
                 int64_t e = ids[t * topk + j];
-                double a, b;
-                uint16_t yn, yl, yh;
+                uint16_t yn, ya;
                 dequant_row(w2 + e * H * (I / 2), w2_sf + e * sfe, h, I, tmp);
-                dot(act + (t * topk + j) * I, tmp, I, &a, &b);
-                scaled_out(a, b, I, (double)alpha2[e], &yn, &yl, &yh);
+                scaled_intermediate(dot(act + (t * topk + j) * I, tmp, I), (double)alpha2[e], &yn, &ya);
                 double wj = (double)tw[t * topk + j];
                 double pn = wj * bf16_to_double(yn); /* exact in double */
-                double pl = wj * bf16_to_double(yl), ph = wj * bf16_to_double(yh);
+                double pa = wj * bf16_to_double(ya);
                 sn += pn;
-                slo += fmin(pl, ph);
-                shi += fmax(pl, ph);
-                sabs += fmax(fabs(pl), fabs(ph));
+                slo += fmin(pn, pa);
+                shi += fmax(pn, pa);
+                sabs += fmax(fabs(pn), fabs(pa));
             }
-            double es = (double)(topk + 2) * ldexp(1.0, -24) * sabs;
-            uint16_t s_n = orc_bf16_rne(sn), s_l = orc_bf16_rne(slo - es), s_h = orc_bf16_rne(shi + es);
-            double a, b;
-            uint16_t zn, zl, zh;
+            double es = (double)(topk + 1) * ldexp(1.0, -24) * sabs;
+            uint16_t s_n = orc_bf16_rne(sn), s_lo = orc_bf16_rne(slo - es), s_hi = orc_bf16_rne(shi + es);
+            uint16_t zn, za;
             dequant_row(wsd, ssd, h, SI, tmp);
-            dot(sact + t * SI, tmp, SI, &a, &b);
-            scaled_out(a, b, SI, gssd, &zn, &zl, &zh);
-            double on = bf16_to_double(s_n) + bf16_to_double(zn);
-            double ol = bf16_to_double(s_l) + bf16_to_double(zl);
-            double oh = bf16_to_double(s_h) + bf16_to_double(zh);
-            double eo = ldexp(fabs(ol) + fabs(oh), -24);
-            nom[t * H + h] = orc_bf16_rne(on);
-            lo[t * H + h] = orc_bf16_rne(ol - eo);
-            hi[t * H + h] = orc_bf16_rne(oh + eo);
+            scaled_intermediate(dot(sact + t * SI, tmp, SI), gssd, &zn, &za);
+            uint16_t o_n = orc_bf16_rne(bf16_to_double(s_n) + bf16_to_double(zn)), o_lo = o_n, o_hi = o_n;
+            int steps = 0;
+            for (uint16_t b = s_lo;; b = bf16_next_up(b)) {
+                hull_add(orc_bf16_rne(bf16_to_double(b) + bf16_to_double(zn)), &o_lo, &o_hi);
+                hull_add(orc_bf16_rne(bf16_to_double(b) + bf16_to_double(za)), &o_lo, &o_hi);
+                if (b == s_hi || ++steps > 64) break;
+            }
+            nom[t * H + h] = o_n;
+            lo[t * H + h] = o_lo;
+            hi[t * H + h] = o_hi;
         }
     }
     return bad;
