@@ -37,7 +37,7 @@ METRIC = "nvfp4_gemv µs/call and achieved HBM GB/s (% of GB300 peak) at M=1..32
 LAYERS = synth.LLAMA8B_LAYERS
 MS = synth.LLAMA8B_M
 GS = 0.01
-REPLICAS = 5
+PHASES = 7  # replica rotation of the step (see run_gpu)
 WORKLOAD = "llama3-8b decode linears (qkv, o_proj, gate_up+silu_mul, down), NVFP4, M=1,2,4,8,16,32"
 
 
@@ -207,7 +207,9 @@ def run_reference(args):
     value, threads, desc = oracle_sample(budget_s=max(5.0, 20.0 / max(1, args.steps)))
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(step_bytes() / (value * 1e9) * 1e3, 3), "higher_is_better": True,
+            "ms_per_step": round(step_bytes() / (value * 1e9) * 1e3, 3),
+            "ms_per_step_kind": "extrapolated: one step's algorithmic bytes / the sampled oracle throughput",
+            "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD, "device": "host CPU (FP64 oracle)"},
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
@@ -243,15 +245,16 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     from moe_nvfp4_gemv_gb300 import fp4gemv
 
-    # weights: REPLICAS copies of every layer; activations per (layer, M)
+    # Weights: every layer has a pool of replicas, at least PHASES and at
+    # least 400 MB.  In the step, call c of a layer (c = step * 6 + m_index)
+    # reads replica c % PHASES, so a replica comes back only after 6 other
+    # calls of each of the 4 layers (~740 MB of other weights, > 5 x L2).
     weights = {}
     for name, (N, K, silu) in LAYERS.items():
-        reps = []
-        for r in range(REPLICAS):
-            w = synth.fp4_bytes(N, K, seed=1000 * r + 1, device=dev)
-            sf = synth.e4m3_bytes(fp4gemv.scale_bytes(N, K), seed=1000 * r + 2, device=dev)
-            reps.append((w, sf))
-        weights[name] = reps
+        nb = N * K // 2 + fp4gemv.scale_bytes(N, K)
+        weights[name] = [(synth.fp4_bytes(N, K, seed=1000 * r + 1, device=dev),
+                          synth.e4m3_bytes(fp4gemv.scale_bytes(N, K), seed=1000 * r + 2, device=dev))
+                         for r in range(max(PHASES, replicas_for(nb)))]
     gs = torch.tensor([GS], dtype=torch.float32, device=dev)
     # The step's activations and outputs each live in one buffer (16-byte
     # aligned views per call), so end to end a step is one host-to-device
@@ -270,23 +273,28 @@ def run_gpu(args):
                              for name in LAYERS for M in MS})
     stream = torch.cuda.current_stream(dev)
 
-    def step_with(r):
-        """One step: the 24 (M, layer) calls on weight replica r."""
+    def step_with(phase, xv=None, ov=None, keep=lambda M: True):
+        """The step's calls in phase `phase` of the replica rotation (all 24,
+        or those whose token count passes `keep`)."""
+        xv = xs if xv is None else xv
+        ov = outs if ov is None else ov
+
         def fn():
-            for M in MS:
+            for mi, M in enumerate(MS):
+                if not keep(M):
+                    continue
                 for name, (N, K, silu) in LAYERS.items():
-                    w, sf = weights[name][r]
-                    fp4gemv.nvfp4_gemv(xs[(name, M)], w, sf, gs, silu_mul=silu, pdl=True, out=outs[(name, M)])
+                    w, sf = weights[name][(phase * len(MS) + mi) % PHASES]
+                    fp4gemv.nvfp4_gemv(xv[(name, M)], w, sf, gs, silu_mul=silu, pdl=True, out=ov[(name, M)])
         return fn
 
-    # A decode server replays its step as a CUDA graph: one graph per weight
-    # replica, replayed round-robin (each layer's weights come back only after
-    # the other 4 replicas' ~600 MB have streamed through L2).
+    # A decode server replays its step as a CUDA graph: one graph per phase
+    # of the replica rotation, replayed in turn.
     launches0 = fp4gemv.launch_count()
-    graphs = [capture_graph(step_with(r), dev) for r in range(REPLICAS)]
-    launches_per_step = (fp4gemv.launch_count() - launches0) // (2 * REPLICAS)
-    for i in range(args.warmup):
-        graphs[i % REPLICAS].replay()
+    graphs = [capture_graph(step_with(ph), dev) for ph in range(PHASES)]
+    launches_per_step = (fp4gemv.launch_count() - launches0) // (2 * PHASES)
+    for i in range(max(args.warmup, PHASES)):
+        graphs[i % PHASES].replay()
     torch.cuda.synchronize()
     assert fp4gemv.get_device_error() == 0, "device error during warm-up"
 
@@ -297,7 +305,7 @@ def run_gpu(args):
     with ClockSampler(local) as clk:
         e0.record(stream)
         for i in range(args.steps):
-            graphs[i % REPLICAS].replay()
+            graphs[i % PHASES].replay()
         e1.record(stream)
         torch.cuda.synchronize()
     barrier(dist)
@@ -309,15 +317,38 @@ def run_gpu(args):
     value = total_bytes / (ms_total * 1e-3) / 1e9
     del graphs
 
-    # ---- per-call us: each (layer, M) alone, 20 calls per graph, replicas rotated ----
+    # ---- each kernel alone: the step's calls of one kernel, same rotation ----
+    # (register-fed kernel: the 16 calls with M <= 16; tcgen05 kernel: M = 32)
+    kernels = {}
+    for kname, keep in (("gemv_rf_kernel", lambda M: M <= 16), ("gemv_kernel", lambda M: M > 16)):
+        gk = [capture_graph(step_with(ph, keep=keep), dev) for ph in range(PHASES)]
+        for i in range(PHASES):
+            gk[i % PHASES].replay()
+        reps = max(args.steps, PHASES)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(reps):
+            gk[i % PHASES].replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        n_calls = sum(1 for M in MS if keep(M)) * len(LAYERS)
+        kb = sum(nvfp4_bytes(M, N, K, s) for M in MS if keep(M) for (N, K, s) in LAYERS.values())
+        us = a.elapsed_time(b) * 1e3 / (reps * n_calls)
+        kernels[kname] = {"launches_per_step": n_calls, "bytes_per_launch": round(kb / n_calls),
+                          "us_per_launch": round(us, 3), "GB/s": round(kb / n_calls / (us * 1e-6) / 1e9, 1)}
+        del gk
+
+    # ---- per-call us: each (layer, M) alone, every replica of the layer's
+    # pool (>= 400 MB) in turn within one graph ----
     per_call = {}
-    calls = 20
     for name, (N, K, silu) in LAYERS.items():
         per_call[name] = {}
+        pool = weights[name]
+        calls = max(20, len(pool))
         for M in MS:
-            def fn(name=name, M=M, silu=silu):
+            def fn(name=name, M=M, silu=silu, pool=pool, calls=calls):
                 for i in range(calls):
-                    w, sf = weights[name][i % REPLICAS]
+                    w, sf = pool[i % len(pool)]
                     fp4gemv.nvfp4_gemv(xs[(name, M)], w, sf, gs, silu_mul=silu, pdl=True, out=outs[(name, M)])
             g = capture_graph(fn, dev)
             g.replay()
@@ -349,18 +380,9 @@ def run_gpu(args):
     bufs = [(x_flat, xs, out_flat, outs), (x_flat2, xs2, out_flat2, outs2)]
     copy_stream = torch.cuda.Stream(dev)
 
-    def gemvs_with(r, b):
-        _, xv, _, ov = bufs[b]
-
-        def fn():
-            for M in MS:
-                for name, (N, K, silu) in LAYERS.items():
-                    w, sf = weights[name][r]
-                    fp4gemv.nvfp4_gemv(xv[(name, M)], w, sf, gs, silu_mul=silu, pdl=True, out=ov[(name, M)])
-        return fn
-
     def e2e_pipelined(nsteps):
-        graphs_b = [[capture_graph(gemvs_with(r, b), dev) for b in range(2)] for r in range(REPLICAS)]
+        graphs_b = [[capture_graph(step_with(ph, bufs[b][1], bufs[b][3]), dev) for b in range(2)]
+                    for ph in range(PHASES)]
         h2d_done = [torch.cuda.Event(), torch.cuda.Event()]
         comp_done = [torch.cuda.Event(), torch.cuda.Event()]
 
@@ -372,7 +394,7 @@ def run_gpu(args):
             for i in range(n):
                 b = i % 2
                 stream.wait_event(h2d_done[b])
-                graphs_b[i % REPLICAS][b].replay()
+                graphs_b[i % PHASES][b].replay()
                 comp_done[b].record(stream)
                 with torch.cuda.stream(copy_stream):
                     if i + 1 < n:  # (buffer 1-b: step i-1 is done with it, in this stream's order)
@@ -381,7 +403,7 @@ def run_gpu(args):
                     copy_stream.wait_event(comp_done[b])
                     host_out.copy_(bufs[b][2], non_blocking=True)
             stream.wait_stream(copy_stream)
-        run(2 * REPLICAS)  # warm-up
+        run(2 * PHASES)  # warm-up
         torch.cuda.synchronize()
         barrier(dist)
         a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -392,10 +414,10 @@ def run_gpu(args):
         del graphs_b
         return max_over_ranks(a.elapsed_time(b2), dist, dev)
 
-    def e2e_with(r):
+    def e2e_with(ph):
         def fn():
             x_flat.copy_(host_x, non_blocking=True)  # the step's inputs
-            gemvs_with(r, 0)()
+            step_with(ph)()
             host_out.copy_(out_flat, non_blocking=True)  # the step's results
         return fn
 
@@ -413,20 +435,24 @@ def run_gpu(args):
     # (a) graph-replayed GEMVs with pipelined copies; (b) the same calls and
     # copies issued eagerly, one stream
     e2e_ms = e2e_pipelined(args.steps)
-    eager_fns = [e2e_with(r) for r in range(REPLICAS)]
+    eager_fns = [e2e_with(ph) for ph in range(PHASES)]
     for f in eager_fns[:2]:
         f()
     eager_ms = timed(eager_fns, args.steps)
     e2e_value = total_bytes / (e2e_ms * 1e-3) / 1e9
     eager_value = total_bytes / (eager_ms * 1e-3) / 1e9
     assert fp4gemv.get_device_error() == 0, "device error during the timed region"
+    del weights
 
     peak, peak_kind = read_peaks()
-    achieved = value / world
+    dom = kernels["gemv_rf_kernel"]
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, threads, desc = oracle_sample(budget_s=args.cpu_budget)
         cpu = {"value": round(v, 4), "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc}
+    extra = None
+    if rank == 0 and not args.no_configs:
+        extra = config_results(dev, compact=True)
 
     if rank == 0:
         line = {
@@ -435,13 +461,19 @@ def run_gpu(args):
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": WORKLOAD, "launches_per_step": launches_per_step,
                        "us_per_call_avg": round(ms_step * 1e3 / launches_per_step, 3),
-                       "l2": f"weights rotated over {REPLICAS} replicas (reuse distance ~490 MB > 3 x L2)",
+                       "l2": (f"inputs larger than L2 instead of a flush: call c of a layer (c = step * 6 + "
+                              f"m_index) reads weight replica c % {PHASES}, so each replica comes back after 6 "
+                              f"calls of each of the 4 layers (~740 MB > 5 x the 129 MB L2); per-call timing "
+                              f"rotates >= 400 MB of replicas of the one layer"),
                        "global_scale": GS, "pdl": True,
-                       "launch": "CUDA graph per step (one per weight replica), PDL edges between the launches"},
-            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs (burst copy)",
-                         "traffic": traffic_from_profile(), "kernel": "fp4::gemv_rf_kernel / fp4::gemv_kernel",
-                         "bytes_per_step": step_bytes()},
+                       "launch": f"one CUDA graph per rotation phase ({PHASES}), PDL edges between the launches"},
+            "roofline": {"bound": "hbm", "achieved": dom["GB/s"], "peak": peak, "unit": "GB/s",
+                         "frac": round(dom["GB/s"] / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs (burst copy)",
+                         "traffic": traffic_from_profile(), "kernel": "fp4::gemv_rf_kernel (M <= 16 calls)",
+                         "bytes_per_launch": dom["bytes_per_launch"], "us_per_launch": dom["us_per_launch"],
+                         "timing": "CUDA events around graph replays of the step's 16 M <= 16 calls, same rotation"},
+            "kernels": kernels,
+            "step_frac": round(value / world / peak, 4),
             "per_call": per_call,
             "clocks": clk.summary(),
             "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
@@ -449,10 +481,12 @@ def run_gpu(args):
                     "eager_value": round(eager_value, 1)},
             "gpu_launches": launches,
             "cpu_baseline": cpu,
+            "configs": extra,
         }
         print(json.dumps(line))
     if rank == 0 and args.extended:
-        run_extended(args.extended, dev)
+        with open(args.extended, "w") as f:
+            json.dump(config_results(dev, compact=False), f, indent=1)
     if dist is not None:
         dist.destroy_process_group()
     return 0
@@ -486,12 +520,27 @@ def replicas_for(nbytes, min_reps=2, target=400 << 20):
     return max(min_reps, -(-target // max(1, nbytes)))
 
 
-def run_extended(path, dev):
+def read_tflops():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
+def config_results(dev, compact=True):
+    """Every configuration besides the default step, L2-cold (weights rotated
+    over >= 400 MB of replicas, MoE over 8 routings): the 70B layers and
+    their dequantize_rows, the 8B layers with BF16 weights, the MoE block,
+    and the N = K = 8192 sweep of the GEMV against dequantize + GEMM (with
+    `compact`, the sweep at M = 1, 8, 32, 128 only)."""
     from moe_nvfp4_gemv_gb300 import fp4gemv
     stream = torch.cuda.current_stream(dev)
     peak, peak_kind = read_peaks()
+    tpeak, tpeak_kind = read_tflops()
     gs = torch.tensor([GS], dtype=torch.float32, device=dev)
-    res = {"peak_hbm_gbs": peak, "peak_kind": peak_kind, "l2_policy": "weights rotated over replicas, >= 400 MB"}
+    res = {"peak_hbm_gbs": peak, "peak_kind": peak_kind, "peak_bf16_tflops": tpeak, "tflops_kind": tpeak_kind,
+           "l2_policy": "weights rotated over replicas, >= 400 MB"}
 
     def fp4_layer(N, K, seed):
         nb = N * K // 2 + N * K // 16
@@ -586,8 +635,11 @@ def run_extended(path, dev):
     N = K = synth.SWEEP_NK
     ws = fp4_layer(N, K, 11)
     wb = torch.empty(N, K, dtype=torch.bfloat16, device=dev)
+    wbs = [torch.empty(N, K, dtype=torch.bfloat16, device=dev) for _ in range(replicas_for(2 * N * K))]
+    for (w, sf), b in zip(ws * len(wbs), wbs):
+        fp4gemv.dequantize_rows(w, sf, out=b)
     sw = {}
-    for M in synth.SWEEP_M:
+    for M in ((1, 8, 32, 128) if compact else synth.SWEEP_M):
         x = synth.activations(M, K, seed=M, device=dev)
         out = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
         fns = [lambda w=w, sf=sf: fp4gemv.nvfp4_gemv(x, w, sf, gs, out=out) for w, sf in ws]
@@ -596,14 +648,22 @@ def run_extended(path, dev):
         us_d = time_calls(fns2, 10, stream)
         b_g = nvfp4_bytes(M, N, K, False)
         b_d = N * K * (0.5 + 1 / 16 + 2) + 2 * N * K + 2 * M * K + 2 * M * N
+        # the GEMM half alone (bf16 weights already dequantized, rotated)
+        fns3 = [lambda b=b: fp4gemv.bf16_gemv(x, b, out=out) for b in wbs]
+        us_m = time_calls(fns3, 10, stream)
+        tf = 2 * M * N * K / (us_m * 1e-6) / 1e12
         sw[str(M)] = {"gemv_us": round(us_g, 2), "gemv_GB/s": round(b_g / (us_g * 1e-6) / 1e9, 1),
+                      "gemv_frac": round(b_g / (us_g * 1e-6) / 1e9 / peak, 3),
                       "gemv_TFLOP/s": round(2 * M * N * K / (us_g * 1e-6) / 1e12, 2),
-                      "dequant_gemm_us": round(us_d, 2), "dequant_gemm_GB/s": round(b_d / (us_d * 1e-6) / 1e9, 1)}
-    cross = next((m for m in synth.SWEEP_M if sw[str(m)]["dequant_gemm_us"] < sw[str(m)]["gemv_us"]), None)
+                      "dequant_gemm_us": round(us_d, 2), "dequant_gemm_GB/s": round(b_d / (us_d * 1e-6) / 1e9, 1),
+                      "dequant_gemm_frac": round(b_d / (us_d * 1e-6) / 1e9 / peak, 3),
+                      "gemm_us": round(us_m, 2), "gemm_TFLOP/s": round(tf, 1), "gemm_tflops_frac": round(tf / tpeak, 4)}
+    rows_m = [int(m) for m in sw]
+    cross = next((m for m in rows_m if sw[str(m)]["dequant_gemm_us"] < sw[str(m)]["gemv_us"]), None)
     res["sweep_8192"] = {"rows": sw, "crossover_M": cross}
+    del ws, wbs, wb
     assert fp4gemv.get_device_error() == 0
-    with open(path, "w") as f:
-        json.dump(res, f, indent=1)
+    return res
 
 
 def run_profile_case(spec):
@@ -667,6 +727,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--extended", metavar="PATH", help="also time every configuration into a JSON file")
+    ap.add_argument("--no-configs", action="store_true", help="leave the other configurations out of the line")
     ap.add_argument("--profile", metavar="CASE", help="run a few launches of one case (for ncu) and exit")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -423,7 +423,9 @@ fp4gemv_status dense_launch(int mode, const void* x, int64_t ldx, const void* w,
                             const float* gs, void* out, int64_t ldo, int M, int N, int K, int silu_mul, int pdl,
                             cudaStream_t stream) {
   const bool fp4w = mode == fp4::kDenseFp4;
-  if (!x || !w || !out || (fp4w && (!w_sf || !gs))) return FP4GEMV_ERR_INVALID_ARG;
+  // Order of the checks: flags and sizes, then alignment, then null
+  // pointers (a null pointer passes the alignment test), so a call with
+  // null pointers and a bad size reports the size.
   if ((silu_mul != 0 && silu_mul != 1) || (pdl != 0 && pdl != 1)) return FP4GEMV_ERR_INVALID_ARG;
   if (M < 1 || N < 1 || K < 1) return FP4GEMV_ERR_INVALID_ARG;
   if (M > FP4GEMV_MAX_M || N % 16 != 0 || (silu_mul && N % 32 != 0) || K % 64 != 0) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
@@ -434,6 +436,7 @@ fp4gemv_status dense_launch(int mode, const void* x, int64_t ldx, const void* w,
     return FP4GEMV_ERR_MISALIGNED;
   if (fp4w && !aligned(w_sf, 16)) return FP4GEMV_ERR_MISALIGNED;
   if (gs && !aligned(gs, 4)) return FP4GEMV_ERR_MISALIGNED;
+  if (!x || !w || !out || (fp4w && (!w_sf || !gs))) return FP4GEMV_ERR_INVALID_ARG;
 
   uint32_t* err = nullptr;
   int sms = 0;
@@ -589,10 +592,10 @@ fp4gemv_status fp4gemv_bf16_gemv(const void* x, int64_t ldx, const void* w, void
 
 fp4gemv_status fp4gemv_dequantize_rows(const uint8_t* w, const uint8_t* w_sf, void* out, int rows, int K,
                                        cudaStream_t stream) {
-  if (!w || !w_sf || !out) return FP4GEMV_ERR_INVALID_ARG;
   if (rows < 1 || K < 1) return FP4GEMV_ERR_INVALID_ARG;
   if (rows % 16 != 0 || K % 256 != 0) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
   if (!aligned(w, 16) || !aligned(out, 16) || !aligned(w_sf, 4)) return FP4GEMV_ERR_MISALIGNED;
+  if (!w || !w_sf || !out) return FP4GEMV_ERR_INVALID_ARG;
   fp4gemv_status st = device_state(nullptr, nullptr);
   if (st != FP4GEMV_OK) return st;
   g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -602,14 +605,14 @@ fp4gemv_status fp4gemv_dequantize_rows(const uint8_t* w, const uint8_t* w_sf, vo
 fp4gemv_status fp4gemv_dequant_gemm(const void* x, int64_t ldx, const uint8_t* w, const uint8_t* w_sf,
                                     const float* global_scale, void* w_bf16, void* out, int64_t ldo, int M, int N,
                                     int K, int pdl, cudaStream_t stream) {
-  if (!global_scale || !w_bf16) return FP4GEMV_ERR_INVALID_ARG;
   if (pdl != 0 && pdl != 1) return FP4GEMV_ERR_INVALID_ARG;
-  if (N % 16 != 0 || K % 256 != 0) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
-  if (!aligned(global_scale, 4)) return FP4GEMV_ERR_MISALIGNED;
+  if (M > FP4GEMV_MAX_M || N % 16 != 0 || K % 256 != 0) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
   // Validate the GEMM half first so nothing launches on a bad argument.
-  if (!x || !out || M < 1 || M > FP4GEMV_MAX_M || ldx < K || ldo < N) return M > FP4GEMV_MAX_M ? FP4GEMV_ERR_UNSUPPORTED_SHAPE : FP4GEMV_ERR_INVALID_ARG;
-  if (!aligned(x, 16) || (ldx * 2) % 16 != 0 || !aligned(out, 16) || ldo % 8 != 0 || !aligned(w_bf16, 16))
+  if (M < 1 || ldx < K || ldo < N) return FP4GEMV_ERR_INVALID_ARG;
+  if (!aligned(global_scale, 4) || !aligned(x, 16) || (ldx * 2) % 16 != 0 || !aligned(out, 16) || ldo % 8 != 0 ||
+      !aligned(w_bf16, 16))
     return FP4GEMV_ERR_MISALIGNED;
+  if (!global_scale || !w_bf16 || !x || !out) return FP4GEMV_ERR_INVALID_ARG;
   fp4gemv_status st = fp4gemv_dequantize_rows(w, w_sf, w_bf16, N, K, stream);
   if (st != FP4GEMV_OK) return st;
   // The GEMM reads the weight the previous launch writes, so it is launched
@@ -622,7 +625,6 @@ fp4gemv_status fp4gemv_moe_gate_up(const void* x, const int32_t* ids, int M, int
                                    const uint8_t* w1_sf, const float* alpha, int E, int H, int I, void* act,
                                    const uint8_t* wsh, const uint8_t* ssh, const float* gssh, int SI, void* sact,
                                    int pdl, cudaStream_t stream) {
-  if (!x || !ids || !w1 || !w1_sf || !alpha || !act || !wsh || !ssh || !gssh || !sact) return FP4GEMV_ERR_INVALID_ARG;
   if (pdl != 0 && pdl != 1) return FP4GEMV_ERR_INVALID_ARG;
   if (M < 1 || topk < 1 || E < 1 || H < 1 || I < 1 || SI < 1) return FP4GEMV_ERR_INVALID_ARG;
   if (static_cast<long>(M) * topk > 1024 || H % 64 != 0 || H < 256 || I % 64 != 0 || SI % 64 != 0)
@@ -630,6 +632,7 @@ fp4gemv_status fp4gemv_moe_gate_up(const void* x, const int32_t* ids, int M, int
   if (!aligned(x, 16) || !aligned(w1, 16) || !aligned(w1_sf, 16) || !aligned(wsh, 16) || !aligned(ssh, 16) ||
       !aligned(act, 16) || !aligned(sact, 16) || !aligned(ids, 4) || !aligned(alpha, 4) || !aligned(gssh, 4))
     return FP4GEMV_ERR_MISALIGNED;
+  if (!x || !ids || !w1 || !w1_sf || !alpha || !act || !wsh || !ssh || !gssh || !sact) return FP4GEMV_ERR_INVALID_ARG;
   uint32_t* err = nullptr;
   int sms = 0;
   fp4gemv_status st = device_state(&err, &sms);
@@ -721,8 +724,6 @@ fp4gemv_status fp4gemv_moe_down_combine(const void* act, const int32_t* ids, con
                                         int I, const void* sact, const uint8_t* wsd, const uint8_t* ssd,
                                         const float* gssd, int SI, void* out, void* workspace,
                                         size_t workspace_bytes, int pdl, cudaStream_t stream) {
-  if (!act || !ids || !tw || !w2 || !w2_sf || !alpha2 || !sact || !wsd || !ssd || !gssd || !out || !workspace)
-    return FP4GEMV_ERR_INVALID_ARG;
   if (pdl != 0 && pdl != 1) return FP4GEMV_ERR_INVALID_ARG;
   if (M < 1 || topk < 1 || E < 1 || H < 1 || I < 1 || SI < 1) return FP4GEMV_ERR_INVALID_ARG;
   if (static_cast<long>(M) * topk > 1024 || H % 64 != 0 || I % 64 != 0 || I < 256 || SI % 64 != 0 || SI < 256)
@@ -732,6 +733,8 @@ fp4gemv_status fp4gemv_moe_down_combine(const void* act, const int32_t* ids, con
       !aligned(sact, 16) || !aligned(out, 16) || !aligned(workspace, 16) || !aligned(ids, 4) || !aligned(tw, 4) ||
       !aligned(alpha2, 4) || !aligned(gssd, 4))
     return FP4GEMV_ERR_MISALIGNED;
+  if (!act || !ids || !tw || !w2 || !w2_sf || !alpha2 || !sact || !wsd || !ssd || !gssd || !out || !workspace)
+    return FP4GEMV_ERR_INVALID_ARG;
   uint32_t* err = nullptr;
   int sms = 0;
   fp4gemv_status st = device_state(&err, &sms);

@@ -920,7 +920,11 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
         // Arrival count tagged with this call's epoch: a counter holding any
         // other epoch (an earlier call, or never-initialised scratch) counts
         // as zero, so the workspace needs no zero-fill.  The last arrival
-        // resets the counter.
+        // resets the counter.  The previous grid in the stream may be a
+        // down_combine on the same workspace (PDL lets this grid start
+        // early): its counting must be over before this call's first
+        // arrival, which retags the counter.
+        pdl_wait();
         __threadfence();
         unsigned long long* ctr = p.counters + blockIdx.x;
         const unsigned long long tag = static_cast<unsigned long long>(p.epoch) << 32;

@@ -761,6 +761,10 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, kOcc) gemv_rf_kernel(con
       // out[t] = bf16(bf16(sum_j tw[t, j] * y[t, j]) + y_shared[t]).
       epi_sync<kEpiThreads>();
       if (tid == 0) {
+        // The previous grid in the stream may be a down_combine on the same
+        // workspace (PDL lets this grid start early): its counting must be
+        // over before this call's first arrival, which retags the counter.
+        pdl_wait();
         __threadfence();
         unsigned long long* ctr = p.counters + blockIdx.x;
         const unsigned long long tag = static_cast<unsigned long long>(p.epoch) << 32;

@@ -218,10 +218,16 @@ def moe_down_combine_workspace_bytes(M: int, topk: int, H: int) -> int:
 _workspaces: dict = {}
 
 
-def moe_workspace(device: torch.device, nbytes: int) -> torch.Tensor:
-    """A cached scratch buffer of at least ``nbytes`` for ``device`` (calls
-    on one stream may share it; it needs no initialisation)."""
-    key = (device.type, device.index)
+def moe_workspace(device: torch.device, nbytes: int, stream: int | None = None) -> torch.Tensor:
+    """A cached scratch buffer of at least ``nbytes`` for ``device`` and one
+    CUDA stream (the current one when ``stream`` is None).  Calls on the same
+    stream run one after another and may share it; calls on different
+    streams may overlap on the GPU, so each stream gets its own buffer.  It
+    needs no initialisation."""
+    index = device.index if device.index is not None else torch.cuda.current_device()
+    if stream is None:
+        stream = _raw_stream(index)
+    key = (device.type, index, int(stream))
     ws = _workspaces.get(key)
     if ws is None or ws.numel() < nbytes:
         ws = torch.empty(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
@@ -237,7 +243,7 @@ def moe_down_combine(act, ids, tw, w2, w2_sf, alpha2, sact, wsd, ssd, gssd, out,
     SI = wsd.shape[1] * 2
     need = moe_down_combine_workspace_bytes(M, topk, H)
     if workspace is None:
-        workspace = moe_workspace(act.device, need)
+        workspace = moe_workspace(act.device, need)  # this stream's own buffer
     _check(_lib.fp4gemv_moe_down_combine(_ptr(act), _ptr(ids), _ptr(tw), M, topk, _ptr(_bytes(w2)),
                                          _ptr(_bytes(w2_sf)), _ptr(alpha2), E, H, I, _ptr(sact), _ptr(_bytes(wsd)),
                                          _ptr(_bytes(ssd)), _ptr(gssd.reshape(1)), SI, _ptr(out), _ptr(workspace),

@@ -273,3 +273,49 @@ def test_random_shapes(fp4, M, N, K, silu):
 
 def test_no_device_errors(fp4):
     assert fp4.get_device_error() == 0
+
+
+# --- every finite E4M3 scale byte, every E2M1 code -------------------------------------
+
+def _all_e4m3_bytes():
+    """The 254 finite float8_e4m3fn bytes: +-0, the subnormals (2^-9 .. 7 x
+    2^-9), the normals up to 448, both signs (0x7F / 0xFF are NaN)."""
+    return np.array([b for b in range(256) if b & 0x7F != 0x7F], np.uint8)
+
+
+def _full_range_weight(rows, K, seed):
+    """Weight bytes uniform (all 16 codes in both nibbles) and a scale buffer
+    where block kb of row r holds finite byte (7 r + kb) mod 254."""
+    vals = _all_e4m3_bytes()
+    w = synth.fp4_bytes(rows, K, seed=seed)
+    sf = np.zeros(oracle.scale_bytes(rows, K), np.uint8)
+    for r in range(rows):
+        for kb in range(K // 16):
+            sf[oracle.swz(r, kb, K)] = vals[(7 * r + kb) % vals.size]
+    return w, torch.from_numpy(sf)
+
+
+def test_full_e4m3_range_dequantize_rows_bit_exact(fp4):
+    rows, K = 256, 4096
+    w, sf = _full_range_weight(rows, K, seed=77)
+    wn = w.numpy()
+    lo, hi = wn & 0xF, wn >> 4
+    assert len(np.unique(lo)) == 16 and len(np.unique(hi)) == 16
+    got = fp4.dequantize_rows(w.to(DEV), sf.to(DEV))
+    torch.cuda.synchronize()
+    assert np.array_equal(u16(got), oracle.dequantize_rows(wn, sf.numpy()))
+
+
+@pytest.mark.parametrize("M", [1, 2, 5, 8, 12, 16, 24])
+@pytest.mark.parametrize("silu", [False, True])
+def test_full_e4m3_range_gemv(fp4, M, silu):
+    # 1..2 tokens: f16 route (converter warp); 3..8: f16 route (cooperative);
+    # 9..16: bf16 bit-placement route; 17+: the tcgen05 kernel.  The scales
+    # span zero, subnormals, negatives and 448.
+    N, K = 256, 4096
+    w, sf = _full_range_weight(N, K, seed=78 + M)
+    x = synth.activations(M, K, seed=79 + M)
+    gs = 0.01
+    got = fp4.nvfp4_gemv(x.to(DEV), w.to(DEV), sf.to(DEV), torch.tensor([gs], device=DEV), silu_mul=silu)
+    ref = oracle.nvfp4_gemv(u16(x), w.numpy(), sf.numpy(), gs, silu_mul=silu)
+    assert_close(u16(got), ref, f"full E4M3 range M={M} silu={silu}")
