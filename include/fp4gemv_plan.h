@@ -1,7 +1,8 @@
 /*
  * fp4gemv_plan.h -- the launch plans libfp4gemv's dense GEMVs use, as
- * host-only functions: the register-fed kernel's (NVFP4, M <= 16) and the
- * tcgen05 kernel's (NVFP4 M > 16, BF16 weights).
+ * host-only functions: the slab kernel's (NVFP4, large weights at M <= 4),
+ * the register-fed kernel's (NVFP4, M <= 16 otherwise) and the tcgen05
+ * kernel's (NVFP4 M > 16, BF16 weights).
  *
  * Operation: the grid decomposition of nvfp4_gemv (vllm.models.flint.ops.
  * nvfp4_gemv, nvfp4_gemv): which tile height and K split the library
@@ -26,7 +27,8 @@ typedef struct {
   int scale_groups;  /* 128-row scale groups a ring stage reserves room for (1 .. 4) */
 } fp4gemv_rf_plan;
 
-/* Plan of fp4gemv_nvfp4_gemv for M <= 16.
+/* Plan of fp4gemv_nvfp4_gemv for M <= 16 when fp4gemv_plan_slab has no
+ * plan.
  *   N, K, silu_mul: as fp4gemv_nvfp4_gemv (same shape rules).
  *   sms:  streaming multiprocessors of the GPU (152 on GB300).
  *   cap:  HOST array of 9 ints; cap[s] (s = 1 .. 8) is the number of CTAs
@@ -36,6 +38,35 @@ typedef struct {
  * Returns FP4GEMV_ERR_INVALID_ARG for null pointers or sms < 1,
  * FP4GEMV_ERR_UNSUPPORTED_SHAPE for shapes fp4gemv_nvfp4_gemv rejects. */
 fp4gemv_status fp4gemv_plan_rf(int N, int K, int silu_mul, int sms, const int* cap, fp4gemv_rf_plan* out);
+
+typedef struct {
+  int row_blocks;     /* 16-row blocks per consumer warp: 1 or 2 */
+  int warps;          /* consumer warps per CTA: 2 or 4 (the CTA adds one producer warp) */
+  int tile_rows;      /* weight rows per CTA tile: 16 x row_blocks x warps (silu_mul: half gate, half up) */
+  int split;          /* CTAs per cluster along K (1 .. 16) */
+  int ctas;           /* grid size: tiles x split */
+  int k_slab;         /* K elements per cluster rank, a multiple of 64 */
+  int stages;         /* weight ring stages of 256 K */
+  int slab_bytes;     /* shared memory holding the CTA's activations */
+  int ctas_per_sm;    /* CTAs an SM runs at once with this shared memory, threads and registers */
+  size_t smem_bytes;  /* dynamic shared memory per CTA */
+} fp4gemv_slab_plan;
+
+/* Plan of fp4gemv_nvfp4_gemv on the slab kernel (the kernel that keeps each
+ * CTA's activations in shared memory).  No GPU is needed.
+ *   M, N, K, silu_mul: as fp4gemv_nvfp4_gemv (same shape rules).
+ *   sms:  streaming multiprocessors of the GPU (152 on GB300).
+ *   regs: HOST array of 2 ints, registers per thread of the kernel with 1
+ *         and with 2 row blocks per warp (they bound the CTAs per SM).
+ *   out:  HOST pointer, filled on success.
+ * Applies to 1 <= M <= 4 and weights of at least 1.2 x sms tiles of 128
+ * rows (e.g. the gate_up projections of Llama-3-8B / 70B): on smaller grids
+ * and more tokens the register-fed kernel was as fast or faster.
+ * Returns FP4GEMV_ERR_INVALID_ARG for null pointers, sms < 1 or a flag
+ * outside {0, 1}; FP4GEMV_ERR_UNSUPPORTED_SHAPE for shapes the GEMV rejects
+ * and for calls the slab kernel does not serve (they run on the kernel
+ * fp4gemv_plan_rf describes). */
+fp4gemv_status fp4gemv_plan_slab(int M, int N, int K, int silu_mul, int sms, const int* regs, fp4gemv_slab_plan* out);
 
 typedef struct {
   int tokens_tile;    /* MMA N of the tcgen05 kernel: 16, 32, 64 or 128 (covers M) */

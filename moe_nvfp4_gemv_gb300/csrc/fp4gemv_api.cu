@@ -166,6 +166,7 @@ constexpr int kMoeGateUpRf = kRfBase + fp4::kMoeGateUp;
 constexpr int kMoeDownRf = kRfBase + fp4::kMoeDown;
 constexpr int kMoeDownRf3 = kRfBase + 10 + fp4::kMoeDown;  // budgeted for three CTAs per SM
 constexpr int kDenseFp4RfCoop = kRfBase + 20 + fp4::kDenseFp4;  // 3 .. 8 tokens, cooperative f16 conversion
+constexpr int kDenseFp4Slab = kRfBase + 30 + fp4::kDenseFp4;    // 1 .. 8 tokens, activations resident in smem
 
 cudaError_t kernel_info(int mode, int nt, KernelInfo* info) {
   GemvParams dummy;
@@ -176,6 +177,7 @@ cudaError_t kernel_info(int mode, int nt, KernelInfo* info) {
     case kMoeDownRf: return fp4::launch_rf(mode - kRfBase, nt, dummy, cfg, info);
     case kMoeDownRf3: return fp4::launch_rf_occ3(fp4::kMoeDown, nt, dummy, cfg, info);
     case kDenseFp4RfCoop: return fp4::launch_rf_coop(fp4::kDenseFp4, nt, dummy, cfg, info);
+    case kDenseFp4Slab: return fp4::launch_slab(2, dummy, cfg, info);
     case fp4::kDenseFp4: return fp4::launch_dense_fp4(nt, dummy, cfg, info);
     case fp4::kDenseBf16: return fp4::launch_dense_bf16(nt, dummy, cfg, info);
     default: return fp4::launch_moe(mode, nt, dummy, cfg, info);
@@ -190,6 +192,7 @@ cudaError_t kernel_launch(int mode, int nt, const GemvParams& p, const LaunchCfg
     case kMoeDownRf: return fp4::launch_rf(mode - kRfBase, nt, p, cfg, nullptr);
     case kMoeDownRf3: return fp4::launch_rf_occ3(fp4::kMoeDown, nt, p, cfg, nullptr);
     case kDenseFp4RfCoop: return fp4::launch_rf_coop(fp4::kDenseFp4, nt, p, cfg, nullptr);
+    case kDenseFp4Slab: return fp4::launch_slab(p.slab_r, p, cfg, nullptr);
     case fp4::kDenseFp4: return fp4::launch_dense_fp4(nt, p, cfg, nullptr);
     case fp4::kDenseBf16: return fp4::launch_dense_bf16(nt, p, cfg, nullptr);
     default: return fp4::launch_moe(mode, nt, p, cfg, nullptr);
@@ -419,6 +422,92 @@ void plan_rf(int N, int K, bool silu, int sms, const int (&cap)[9], int* cw, int
   *sf_groups = silu ? (even ? 1 : 2) + ((even && (N / 2) % h == 0) ? 1 : 2) : (even ? 1 : 2);
 }
 
+// The slab kernel's plan (M <= 8): tiles of 128 rows (two 16-row blocks per
+// consumer warp, four consumer warps; with silu_mul 64 gate + 64 up rows),
+// three CTAs per SM, and the largest K split S in 1, 2, 4, 8 whose grid still
+// runs in one wave (tiles x S <= 3 x SMs) -- for 1 .. kSlabMaxM tokens and
+// weights of at least kSlabMinTiles tiles per SM, provided the grid then
+// holds at least kSlabMinFill CTAs per SM and the CTA's activation slab and
+// two 256-K weight stages fit a third of the SM's shared memory.  Measured on
+// the Llama-3-8B layers: gate_up at 1 .. 4 tokens 9-11 % faster than the
+// register-fed kernel alone and ~1 % on a whole decode step; qkv (48 tiles,
+// split 8) 5 % faster alone but slower inside a step next to the register-
+// fed kernels (their 110 KB CTAs and these 70 KB ones pack badly at the
+// hand-over); at 8 tokens the larger slab made it slower; on grids of fewer
+// CTAs (o_proj, down: 32 tiles) the register-fed kernel's 8-warp CTAs are as
+// fast or faster, and more splits (clusters of 16) or several waves were
+// slower.  False: the register-fed kernel serves the call.
+constexpr int kSlabOcc = 3;
+constexpr double kSlabMinFill = 2.4;
+constexpr double kSlabMinTiles = 1.2;  // tiles per SM before the split
+constexpr int kSlabMaxM = 4;
+constexpr int kSmemPerSm = 228 * 1024;   // shared memory per SM
+constexpr int kSmemPerCta = 2048;        // per-CTA reservation + the kernel's static shared memory
+
+struct SlabPlan {
+  int r = 2, cw = 4, S = 1, kslab = 0, sf_groups = 1, nstages = 0, stage_bytes = 0, slab_bytes = 0, occ = 0;
+  size_t smem = 0;
+};
+
+// regs[r - 1]: registers per thread of the kernel with r row blocks per warp
+// (with the threads and the shared memory they bound the CTAs per SM).
+bool plan_slab(int M, int N, int K, bool silu, int sms, int inbox_bytes, const int (&regs)[2], SlabPlan* sp) {
+  if (M < 1 || M > kSlabMaxM || sms < 1) return false;
+  const int r = 2, cw = 4, occ = kSlabOcc;
+  const int warp_regs = (regs[r - 1] * 32 + 255) / 256 * 256;  // registers allocated per warp
+  if (static_cast<long>(occ) * (cw + 1) * warp_regs > 65536) return false;
+  const int trows = 16 * r * cw;
+  const int h = silu ? trows / 2 : trows;  // rows per box, h | 128, boxes start on multiples of h
+  const long tiles = ((silu ? N / 2 : N) + h - 1) / h;
+  const int groups = silu ? 1 + ((N / 2) % h == 0 ? 1 : 2) : 1;
+  const int stage = (trows * 128 + groups * 2048 + 1023) / 1024 * 1024;
+  const int dyn = kSmemPerSm / occ - kSmemPerCta;
+  if (tiles < kSlabMinTiles * sms) return false;
+  for (int S = 8; S >= 1; S /= 2) {
+    if (tiles * S > static_cast<long>(occ) * sms) continue;         // more than one wave
+    if (tiles * S < kSlabMinFill * sms) return false;                // too few CTAs to fill the SMs
+    const int kslab = ((K + S - 1) / S + 63) / 64 * 64;
+    if (S > 1 && (kslab < 256 || static_cast<long>(S - 1) * kslab >= K)) continue;
+    const int nst = (kslab + 255) / 256;
+    if (nst > fp4::kSlabMaxStages) return false;
+    const int slab = (M * nst * 512 + 1023) / 1024 * 1024;
+    // Two stages: with three CTAs per SM that is 6 stages (~110 KB) in
+    // flight per SM; deeper rings measured slower (gate_up 15.4 -> 16.0 us at
+    // M = 1), their burst of first loads delaying the previous grid's end.
+    const int ns = 2;
+    if (1024 + slab + ns * stage + inbox_bytes > dyn) return false;
+    sp->r = r;
+    sp->cw = cw;
+    sp->kslab = kslab;
+    sp->S = (K + kslab - 1) / kslab;  // every cluster rank gets a non-empty K range
+    sp->sf_groups = groups;
+    sp->nstages = ns;
+    sp->stage_bytes = stage;
+    sp->slab_bytes = slab;
+    sp->occ = occ;
+    sp->smem = 1024 + static_cast<size_t>(slab) + static_cast<size_t>(ns) * stage + inbox_bytes;
+    return true;
+  }
+  return false;
+}
+
+// Registers per thread of both slab-kernel variants (queried once per device).
+std::atomic<int> g_slab_regs[kMaxDevices][2];
+
+fp4gemv_status slab_registers(int (&regs)[2]) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FP4GEMV_ERR_CUDA;
+  for (int r = 1; r <= 2; ++r) {
+    int v = g_slab_regs[dev][r - 1].load(std::memory_order_acquire);
+    if (v == 0) {
+      if (fp4::slab_regs(r, &v) != cudaSuccess || v <= 0) return FP4GEMV_ERR_CUDA;
+      g_slab_regs[dev][r - 1].store(v, std::memory_order_release);
+    }
+    regs[r - 1] = v;
+  }
+  return FP4GEMV_OK;
+}
+
 fp4gemv_status dense_launch(int mode, const void* x, int64_t ldx, const void* w, const uint8_t* w_sf,
                             const float* gs, void* out, int64_t ldo, int M, int N, int K, int silu_mul, int pdl,
                             cudaStream_t stream) {
@@ -447,10 +536,21 @@ fp4gemv_status dense_launch(int mode, const void* x, int64_t ldx, const void* w,
   // otherwise the tcgen05 kernel (at 32 tokens the register-fed kernel is
   // bound by its MMA count and no faster).
   const bool rf = fp4w && M <= 16;
-  const int kmode = rf ? (M >= 3 && M <= 8 ? kDenseFp4RfCoop : kDenseFp4Rf) : mode;
+  int kmode = rf ? (M >= 3 && M <= 8 ? kDenseFp4RfCoop : kDenseFp4Rf) : mode;
   const int NT = rf ? (M <= 8 ? 8 : 16) : pick_nt(M);
   int nstages = 0, stage_bytes = 0, x_off = 0;
   size_t smem = 0;
+  // 1 .. 8 tokens: the slab kernel when the CTA's activations fit in shared
+  // memory, else the register-fed kernel.
+  bool slab = false;
+  SlabPlan sp;
+  if (rf && M <= 8) {
+    int regs[2];
+    st = slab_registers(regs);
+    if (st != FP4GEMV_OK) return st;
+    slab = plan_slab(M, N, K, silu_mul != 0, sms, fp4::SlabInboxBytes, regs, &sp);
+    if (slab) kmode = kDenseFp4Slab;
+  }
   // A tile is `box_rows` weight rows per box: 128 output features (tcgen05),
   // or with silu_mul 64 features (64 gate rows + the 64 matching up rows, two
   // boxes); the register-fed kernel's tiles are 16 cw rows (see
@@ -458,7 +558,14 @@ fp4gemv_status dense_launch(int mode, const void* x, int64_t ldx, const void* w,
   int cw = 8, S0 = 1, kslab = 0;
   TcPlan tp;  // tcgen05 kernel
   TcRing& tr = tp.ring;
-  if (rf) {
+  if (slab) {
+    cw = sp.cw;
+    nstages = sp.nstages;
+    smem = sp.smem;
+    stage_bytes = sp.stage_bytes;
+    x_off = sp.slab_bytes;
+    kslab = sp.kslab;
+  } else if (rf) {
     KernelInfo info{};
     if (kernel_info(kmode, NT, &info) != cudaSuccess) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
     int cap[9];
@@ -474,7 +581,8 @@ fp4gemv_status dense_launch(int mode, const void* x, int64_t ldx, const void* w,
     smem = tr.smem;
     kslab = tp.kslab;
   }
-  const int box_rows = rf ? (silu_mul ? 8 * cw : 16 * cw) : (silu_mul ? 64 : 128);
+  const int tile_rows = slab ? 16 * sp.r * cw : 16 * cw;
+  const int box_rows = rf ? (silu_mul ? tile_rows / 2 : tile_rows) : (silu_mul ? 64 : 128);
   const int tiles = (n_out + box_rows - 1) / box_rows;
   const int S = (K + kslab - 1) / kslab;  // every cluster rank gets a non-empty K range
   const int sf_slots = tp.sf_slots;
@@ -488,7 +596,9 @@ fp4gemv_status dense_launch(int mode, const void* x, int64_t ldx, const void* w,
     if (!encode_2d(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w, K, N, static_cast<uint64_t>(K) * 2, 64, box_rows))
       return FP4GEMV_ERR_CUDA;
   }
-  if (fp4w) {
+  if (slab) {
+    // (activations read with plain loads)
+  } else if (fp4w) {
     if (!encode_x_atoms(&p.tm_x, x, K, M, ldx, NT, rf ? 4 : 2)) return FP4GEMV_ERR_CUDA;
   } else {
     if (!encode_2d(&p.tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, M, static_cast<uint64_t>(ldx) * 2, 64, NT))
@@ -516,6 +626,7 @@ fp4gemv_status dense_launch(int mode, const void* x, int64_t ldx, const void* w,
   p.stage_bytes = stage_bytes;
   p.x_off = x_off;
   p.cw = cw;
+  p.slab_r = slab ? sp.r : 0;
   p.err = err;
 
   LaunchCfg cfg{};
@@ -546,6 +657,30 @@ fp4gemv_status fp4gemv_plan_rf(int N, int K, int silu_mul, int sms, const int* c
   out->split = split;
   out->ctas = (n_out + feats - 1) / feats * split;
   out->scale_groups = groups;
+  return FP4GEMV_OK;
+}
+
+fp4gemv_status fp4gemv_plan_slab(int M, int N, int K, int silu_mul, int sms, const int* regs, fp4gemv_slab_plan* out) {
+  if (!regs || !out || sms < 1 || (silu_mul != 0 && silu_mul != 1) || M < 1 || N < 1 || K < 1)
+    return FP4GEMV_ERR_INVALID_ARG;
+  if (M > 8 || N % 16 != 0 || (silu_mul && N % 32 != 0) || K % 64 != 0 || K < 256) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
+  const int rg[2] = {regs[0], regs[1]};
+  if (rg[0] < 1 || rg[1] < 1) return FP4GEMV_ERR_INVALID_ARG;
+  SlabPlan sp;
+  if (!plan_slab(M, N, K, silu_mul != 0, sms, fp4::SlabInboxBytes, rg, &sp)) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
+  const int trows = 16 * sp.r * sp.cw;
+  const int feats = silu_mul ? trows / 2 : trows;
+  const int n_out = silu_mul ? N / 2 : N;
+  out->row_blocks = sp.r;
+  out->warps = sp.cw;
+  out->tile_rows = trows;
+  out->split = sp.S;
+  out->ctas = (n_out + feats - 1) / feats * sp.S;
+  out->k_slab = sp.kslab;
+  out->stages = sp.nstages;
+  out->slab_bytes = sp.slab_bytes;
+  out->ctas_per_sm = sp.occ;
+  out->smem_bytes = sp.smem;
   return FP4GEMV_OK;
 }
 

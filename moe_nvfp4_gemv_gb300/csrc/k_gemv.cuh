@@ -70,6 +70,8 @@ constexpr int kMaxWG = 2;
 constexpr int kMaxSlots = 6;
 constexpr int kMaxXSlots = 4;   // activation slots (NVFP4 modes; the host picks 2, 3 or 4)
 constexpr int kSliceK = 128;    // K per tensor-memory A slot (8 MMAs of K = 16 per commit)
+constexpr int kSlabMaxStages = 64;  // slab kernel: K per CTA <= 64 stages of 256
+constexpr int SlabInboxBytes = 8 * (128 + 16) * 4;  // slab kernel: split-K inbox (8 tokens x 144 rows, fp32)
 
 struct GemvParams {
   CUtensorMap tm_w;    // weights read by routed / dense CTAs
@@ -111,9 +113,13 @@ struct GemvParams {
   int wstage;          // tcgen05 NVFP4 modes: bytes per weight stage (codes + sf_slots scale groups)
   int sf_slots;        // tcgen05 NVFP4 modes: 2 KB scale-group slots per weight stage (1 .. 3)
   int inbox_off;       // tcgen05 push mode: offset of the split-K inbox from the ring (0: the drained ring)
-  int stage_bytes;     // register-fed kernel: bytes per ring stage (weights, scale groups, activations)
-  int x_off;           // register-fed kernel: offset of the activations in a stage
-  int cw;              // register-fed dense kernel: consumer warps = tile height / 16 (4 .. 8)
+  int stage_bytes;     // register-fed kernel: bytes per ring stage (weights, scale groups, activations);
+                       // slab kernel: bytes per ring stage (weights, scale groups)
+  int x_off;           // register-fed kernel: offset of the activations in a stage; slab kernel:
+                       // bytes of the activation slab (the ring starts there)
+  int cw;              // register-fed dense kernel: consumer warps = tile height / 16 (4 .. 8);
+                       // slab kernel: consumer warps (2 or 4), tile height 16 slab_r cw
+  int slab_r;          // slab kernel: 16-row blocks per consumer warp (1 or 2)
   uint32_t* err;       // device error word
 };
 

@@ -1,0 +1,431 @@
+// k_gemv_slab.cuh -- the dense NVFP4 GEMV for 1 .. 8 tokens with the CTA's
+// activations resident in shared memory.
+//
+// Same operation as the dense mode of k_gemv_rf.cuh (vllm.models.flint.ops.
+// nvfp4_gemv, nvfp4_gemv, with or without silu_mul), organised so that the
+// only per-stage traffic is the weight stream:
+//
+//   * The CTA's activation slab, x[0 .. M)[k_begin .. k_end), is read from
+//     global memory once, after griddepcontrol.wait, by all consumer threads
+//     and kept in shared memory for the whole launch (64-K atoms of M rows x
+//     128 bytes, 16-byte chunks XOR-swizzled by token).  A 256-K stage whose
+//     activations are all exactly representable in f16 is converted to f16
+//     in place (the f16 route: cvt.rn.f16x2.e2m1x2 on the weights, f16
+//     MMAs); any other stage keeps its bf16 values and runs the bf16
+//     bit-placement route (dequant.cuh).  Both routes form exact products
+//     and accumulate in fp32, separately, summed at the end.
+//   * The ring holds only weights and their scale groups (TMA boxes and
+//     bulk copies).  The producer warp never waits for the previous grid:
+//     weights are not written by it, so the ring fills completely under PDL.
+//   * No converter warp and no per-stage CTA barrier: a consumer warp waits
+//     on one full barrier per stage and releases the stage with one arrival.
+//   * The block has exactly cw consumer warps and the producer warp (the
+//     host launches (cw + 1) x 32 threads), so no warp sits idle.
+//
+// Fragment mapping as in k_gemv_rf.cuh: thread (g, c) of consumer warp w
+// holds, for each of its kR 16-row blocks b, MMA rows g and g + 8 = tile rows
+// 16 (kR w + b) + sigma(g) and + 8, sigma = (0 4 1 5 2 6 3 7); in 128-K half h
+// of a stage it reads code chunk 4 h + c of both rows.  The K split over the
+// S CTAs of a cluster and its reduction through distributed shared memory
+// are those of the register-fed kernel.
+#pragma once
+
+#include "k_gemv_rf.cuh"
+
+namespace fp4 {
+
+constexpr int kSlabNT = 8;            // MMA N: tokens 0 .. 7
+constexpr int kSlabR = 2;             // 16-row blocks per consumer warp
+constexpr int kSlabMaxCW = 4;         // consumer warps (tiles of 16 kSlabR cw rows: 64 or 128)
+constexpr int kSlabThreads = kSlabMaxCW * 32 + 32;
+constexpr int kSlabMinBlocks = 3;     // CTAs per SM the registers are budgeted for
+
+template <int kR>
+struct SlabCfg {
+  static constexpr int kChains = kR == 1 ? 4 : 2;  // independent fp32 accumulators per row block
+  static constexpr int kInboxFloats = kSlabNT * (16 * kSlabMaxCW * kR + 16);
+  static_assert(kInboxFloats * 4 <= SlabInboxBytes, "inbox");
+};
+
+// Named barrier 1 over the first n threads (the consumer warps).
+__device__ __forceinline__ void cons_sync(int n) { asm volatile("bar.sync 1, %0;" ::"r"(n) : "memory"); }
+
+// Eight bf16 values -> eight f16 values; false if any is not exact in f16.
+__device__ __forceinline__ bool bf16x8_to_f16x8_exact(const uint4& v, uint4& o) {
+  bool e = bf16x2_to_f16x2_exact(v.x, o.x);
+  e &= bf16x2_to_f16x2_exact(v.y, o.y);
+  e &= bf16x2_to_f16x2_exact(v.z, o.z);
+  e &= bf16x2_to_f16x2_exact(v.w, o.w);
+  return e;
+}
+
+template <int kR>
+__global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel(const __grid_constant__ GemvParams p) {
+  using C = SlabCfg<kR>;
+  constexpr int kChains = C::kChains;
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t slab = base;                    // activations
+  const uint32_t ring = base + p.x_off;          // weight stages (x_off: the slab's bytes, 1024-aligned)
+  const uint32_t inbox = ring + p.nstages * p.stage_bytes;
+  __shared__ __align__(8) uint64_t bar_full[kMaxStages];
+  __shared__ __align__(8) uint64_t bar_empty[kMaxStages];
+  __shared__ __align__(8) uint64_t bar_inbox;
+  __shared__ volatile int s_abort;
+  __shared__ int s_xbad[kSlabMaxStages];  // 1: the stage's activations are not all exact in f16
+
+  const int tid = threadIdx.x;
+  const int warp = tid / 32;
+  const int lane = tid % 32;
+  const int cw = p.cw;                 // consumer warps; warp cw is the producer
+  const int ncons = cw * 32;
+  const uint32_t S = cluster_nctarank();
+  const uint32_t rank = S > 1 ? cluster_ctarank() : 0;
+  const int nstages = p.nstages;
+  const int M = p.M;
+  const int trows = 16 * kR * cw;
+
+  // ---- what this CTA computes (every thread derives it) ----
+  RfWork wk;
+  wk.shared = 0;
+  wk.expert = -1;
+  {
+    const int tile = blockIdx.x / max(1u, S);
+    wk.k_begin = static_cast<int>(rank) * p.k_split;
+    wk.k_end = min(p.K, wk.k_begin + p.k_split);
+    wk.kbp = p.kbp;
+    wk.sgroup[2] = wk.sgroup[3] = -1;
+    wk.wrow[1] = wk.srow[1] = 0;
+    const int groups_total = (p.rows_w + 127) / 128;
+    if (p.silu) {
+      wk.paired = 1;
+      wk.out_base = tile * (trows / 2);
+      rf_box(wk, 0, wk.out_base, trows / 2, groups_total);
+      rf_box(wk, 1, p.n_half + wk.out_base, trows / 2, groups_total);
+    } else {
+      wk.paired = 0;
+      wk.out_base = tile * trows;
+      rf_box(wk, 0, wk.out_base, trows, groups_total);
+    }
+  }
+  const int klen = wk.k_end - wk.k_begin;
+  const int nst = (klen + 255) / 256;
+  const uint32_t slab_stage = static_cast<uint32_t>(M) * 512u;  // bytes of one stage's activations
+  const uint64_t pol_w = policy_evict_first();
+  auto issue_weights = [&](int s, int slot) {
+    const uint32_t st = ring + slot * p.stage_bytes;
+    const uint32_t fb = smem_u32(&bar_full[slot]);
+    const int k0 = wk.k_begin + s * 256;
+    const int nchunks = min(256, wk.k_end - k0) / kSubK;
+    uint32_t bytes = trows * 128;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) bytes += (wk.sgroup[g] >= 0 ? nchunks * 512 : 0);
+    mbar_arrive_expect_tx(fb, bytes);
+    tma_load_2d(st, &p.tm_w, k0 / 2, wk.wrow[0], fb, pol_w);
+    if (wk.paired) tma_load_2d(st + trows * 64, &p.tm_w, k0 / 2, wk.wrow[1], fb, pol_w);
+    uint32_t sdst = st + trows * 128;  // the valid groups, in order
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      if (wk.sgroup[g] < 0) continue;
+      const size_t chunk = static_cast<size_t>(wk.sgroup[g]) * (wk.kbp / 4) + k0 / 64;
+      bulk_load(sdst, p.sf + chunk * 512, nchunks * 512, fb, pol_w);
+      sdst += 2048;
+    }
+  };
+  // Output rows are reduced across cluster ranks per feature unit: paired
+  // tiles combine rows o and o + trows / 2 (two rows per feature).
+  const int unit = wk.paired ? trows / 2 : trows;
+  const int rpf = trows / unit;
+
+  // ------------------------------------------------------------------ prologue
+  if (warp == cw && lane == 0) {
+    prefetch_tensormap(&p.tm_w);
+    s_abort = 0;
+    for (int i = 0; i < nstages; ++i) {
+      mbar_init(smem_u32(&bar_full[i]), 1);
+      mbar_init(smem_u32(&bar_empty[i]), cw);
+    }
+    mbar_init(smem_u32(&bar_inbox), 1);
+    if (S > 1) {
+      const int r = (unit + static_cast<int>(S) - 1) / static_cast<int>(S);
+      const int mine0 = max(0, min(r, unit - static_cast<int>(rank) * r)) * rpf;
+      mbar_arrive_expect_tx(smem_u32(&bar_inbox), S * M * mine0 * 4);  // tokens < M only
+    }
+    mbar_fence_init();
+    const int pre = min(nst, nstages);
+    for (int s = 0; s < pre; ++s) issue_weights(s, s);
+  }
+  for (int i = tid; i < nst; i += blockDim.x) s_xbad[i] = 0;
+  __syncthreads();
+  if (S > 1) cluster_arrive_relaxed();  // paired with a wait before the first remote access
+  if (tid == 0) pdl_launch_dependents();
+  const int R = (unit + static_cast<int>(S) - 1) / static_cast<int>(S);
+  const int f_lo = static_cast<int>(rank) * R;
+  const int f_hi = min(unit, f_lo + R);
+  const int mine = max(0, f_hi - f_lo) * rpf;
+
+  float acc[kChains][kR][4];   // f16-route stages (exact products)
+  float accb[kR][4];           // bf16-route stages (products times 2^-kShift)
+#pragma unroll
+  for (int b = 0; b < kR; ++b) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      accb[b][e] = 0.0f;
+#pragma unroll
+      for (int q = 0; q < kChains; ++q) acc[q][b][e] = 0.0f;
+    }
+  }
+  const int g = lane / 4, c = lane % 4;
+  const int sg = (g % 2) * 4 + g / 2;  // sigma(g)
+
+  if (warp == cw) {
+    // ------------------------------------------------------------------ producer
+    // Weights only; they do not depend on the previous grid, so no wait.
+    if (lane == 0) {
+      const int pre = min(nst, nstages);
+      int issued = pre;
+      for (int s = pre, slot = pre % nstages, ph = (pre / nstages) & 1; s < nst && !s_abort;
+           ++s, slot = slot + 1 == nstages ? 0 : slot + 1, ph ^= slot == 0) {
+        if (!mbar_wait_sleepy(smem_u32(&bar_empty[slot]), ph ^ 1, p.err, 64)) {
+          s_abort = 1;
+          break;
+        }
+        issue_weights(s, slot);
+        issued = s + 1;
+      }
+      // After an abort, let every copy still in flight land before the CTA
+      // (and its shared memory) goes away: the latest fill of each slot.
+      if (s_abort) {
+        for (int s = max(0, issued - nstages); s < issued; ++s)
+          (void)mbar_wait(smem_u32(&bar_full[s % nstages]), (s / nstages) & 1, p.err);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------ consumers
+    // The activation slab: bf16 chunks in (pass 1, with an exactness check
+    // per stage), then the exact stages to f16 in place (pass 2).
+    // K past the end of a ragged last stage is zero-filled (the same bits in
+    // bf16 and f16), so the zero weights there meet zero activations.
+    pdl_wait();
+    const int nchk = klen / 8;  // 16-byte chunks per token holding data
+    const int nslot = nst * 32;  // 16-byte chunks per token in the slab
+    for (int q = tid; q < M * nslot; q += ncons) {
+      const int n = q / nslot, kq = q % nslot;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (kq < nchk) v = __ldg(reinterpret_cast<const uint4*>(p.x + static_cast<int64_t>(n) * p.ldx + wk.k_begin + 8 * kq));
+      const int s = kq / 32, u = (kq % 32) / 8, ch = kq % 8;
+      const uint32_t a = slab + s * slab_stage + (u * M + n) * 128 + ((ch ^ (n & 7)) * 16);
+      sts128(a, v);
+      uint4 o;
+      if (!bf16x8_to_f16x8_exact(v, o)) atomicOr(&s_xbad[s], 1);
+    }
+    cons_sync(ncons);
+    for (int q = tid; q < M * nchk; q += ncons) {
+      const int n = q / nchk, kq = q % nchk;
+      const int s = kq / 32, u = (kq % 32) / 8, ch = kq % 8;
+      if (s_xbad[s]) continue;
+      const uint32_t a = slab + s * slab_stage + (u * M + n) * 128 + ((ch ^ (n & 7)) * 16);
+      uint4 o;
+      bf16x8_to_f16x8_exact(lds128(a), o);
+      sts128(a, o);
+    }
+    cons_sync(ncons);
+
+    // shared-memory offsets of this thread's rows (128-byte swizzle key
+    // = row % 8, the same for every row of the thread) and of their scales
+    uint32_t w_off[kR][2], sf_off[kR][2];
+    const uint32_t key = static_cast<uint32_t>(sg);
+#pragma unroll
+    for (int b = 0; b < kR; ++b) {
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int row = (warp * kR + b) * 16 + sg + 8 * hr;
+        w_off[b][hr] = (row / 8) * 1024 + (row % 8) * 128;
+        const int half = trows / 2;
+        const bool b1 = wk.paired && row >= half;
+        const int r = (b1 ? wk.srow[1] : wk.srow[0]) + (b1 ? row - half : row);
+        const int gr = r / 128;
+        const int gslot = b1 ? (wk.sgroup[0] >= 0) + (wk.sgroup[1] >= 0) + (gr != wk.sgroup[2]) : (gr != wk.sgroup[0]);
+        sf_off[b][hr] = trows * 128 + gslot * 2048 + (r % 32) * 16 + ((r % 128) / 32) * 4;
+      }
+    }
+    // One 128-K half of a stage, f16 route.  `cvalid` false (a chunk past
+    // the end of a ragged last stage) gives zero A registers: that chunk's
+    // scales were not copied and may hold anything.
+    auto half_f16 = [&](uint32_t st, uint32_t xs, int h, bool cvalid) {
+      const int j = 4 * h + c;
+      uint4 A[kR][2];
+      uint32_t slo[kR][2], shi[kR][2];
+      const uint32_t sc_off = (j / 2) * 512 + 2 * (j % 2);
+#pragma unroll
+      for (int b = 0; b < kR; ++b) {
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          A[b][hr] = lds128(st + w_off[b][hr] + ((static_cast<uint32_t>(j) ^ key) * 16));
+          scale_pair_to_f16x2(lds16(st + sf_off[b][hr] + sc_off), slo[b][hr], shi[b][hr]);
+          if (!cvalid) slo[b][hr] = shi[b][hr] = 0u;
+        }
+      }
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const int kk = 32 * j + 8 * w;
+        const uint32_t u = kk / 64, ch = (kk % 64) / 8;
+        const uint4 xv = lds128_if(xs + (u * M + g) * 128 + ((ch ^ static_cast<uint32_t>(g)) * 16), g < M);
+#pragma unroll
+        for (int b = 0; b < kR; ++b) {
+          const uint32_t w0 = w == 0 ? A[b][0].x : w == 1 ? A[b][0].y : w == 2 ? A[b][0].z : A[b][0].w;
+          const uint32_t w1 = w == 0 ? A[b][1].x : w == 1 ? A[b][1].y : w == 2 ? A[b][1].z : A[b][1].w;
+          uint32_t r0[4], r1[4];
+          dequant8_f16(w0, w < 2 ? slo[b][0] : shi[b][0], r0);
+          dequant8_f16(w1, w < 2 ? slo[b][1] : shi[b][1], r1);
+          mma_f16_16816(acc[(2 * w) % kChains][b], r0[0], r1[0], r0[1], r1[1], xv.x, xv.y);
+          mma_f16_16816(acc[(2 * w + 1) % kChains][b], r0[2], r1[2], r0[3], r1[3], xv.z, xv.w);
+        }
+      }
+    };
+    // The same half on the bf16 route (the stage's activations stayed bf16;
+    // they are permuted in registers to the weight pairs' K order).
+    auto half_bf16 = [&](uint32_t st, uint32_t xs, int h, bool cvalid) {
+      const int j = 4 * h + c;
+      uint4 A[kR][2];
+      uint32_t slo[kR][2], shi[kR][2];
+      const uint32_t sc_off = (j / 2) * 512 + 2 * (j % 2);
+#pragma unroll
+      for (int b = 0; b < kR; ++b) {
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          A[b][hr] = lds128(st + w_off[b][hr] + ((static_cast<uint32_t>(j) ^ key) * 16));
+          scale_pair_to_bf16x2(lds16(st + sf_off[b][hr] + sc_off), slo[b][hr], shi[b][hr]);
+          if (!cvalid) slo[b][hr] = shi[b][hr] = 0u;
+        }
+      }
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const int kk = 32 * j + 8 * w;
+        const uint32_t u = kk / 64, ch = (kk % 64) / 8;
+        const uint4 xv =
+            perm_x8(lds128_if(xs + (u * M + g) * 128 + ((ch ^ static_cast<uint32_t>(g)) * 16), g < M));
+#pragma unroll
+        for (int b = 0; b < kR; ++b) {
+          const uint32_t w0 = w == 0 ? A[b][0].x : w == 1 ? A[b][0].y : w == 2 ? A[b][0].z : A[b][0].w;
+          const uint32_t w1 = w == 0 ? A[b][1].x : w == 1 ? A[b][1].y : w == 2 ? A[b][1].z : A[b][1].w;
+          uint32_t r0[4], r1[4];
+          e2m1x8_raw_perm(w0, r0);
+          e2m1x8_raw_perm(w1, r1);
+          const uint32_t sa = w < 2 ? slo[b][0] : shi[b][0], sb = w < 2 ? slo[b][1] : shi[b][1];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            r0[q] = bf16x2_mul(r0[q], sa);
+            r1[q] = bf16x2_mul(r1[q], sb);
+          }
+          mma_bf16_16816(accb[b], r0[0], r1[0], r0[1], r1[1], xv.x, xv.y);
+          mma_bf16_16816(accb[b], r0[2], r1[2], r0[3], r1[3], xv.z, xv.w);
+        }
+      }
+    };
+    for (int s = 0, slot = 0, ph = 0; s < nst; ++s, slot = slot + 1 == nstages ? 0 : slot + 1, ph ^= slot == 0) {
+      const uint32_t st = ring + slot * p.stage_bytes;
+      const uint32_t xs = slab + s * slab_stage;
+      const bool ok = __all_sync(0xFFFFFFFFu, !s_abort && mbar_wait(smem_u32(&bar_full[slot]), ph, p.err));
+      if (!ok) {
+        s_abort = 1;
+        break;
+      }
+      // valid K of the stage: 64 .. 256 in steps of 64; a chunk (32 K) is
+      // wholly valid or wholly past the end
+      const int kvalid = min(256, klen - s * 256);
+      if (!s_xbad[s]) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (128 * h < kvalid) {
+            if (128 * (h + 1) <= kvalid) half_f16(st, xs, h, true);
+            else half_f16(st, xs, h, 32 * (4 * h + c) < kvalid);
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          if (128 * h < kvalid) half_bf16(st, xs, h, 32 * (4 * h + c) < kvalid);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bar_empty[slot]));
+    }
+  }
+
+  // ==================================================================== epilogue
+  __syncwarp();
+  if (warp < cw) {
+    const float post = static_cast<float>(1 << kShift);
+    // Push this thread's partials (its rows, tokens 2c + {0,1} below M) to
+    // the owners of the rows: inbox[src][n][rr].
+    if (S > 1) cluster_wait();  // all peers' inbox barriers are initialised
+    const bool go = !s_abort;
+#pragma unroll
+    for (int b = 0; b < kR; ++b) {
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int row = (warp * kR + b) * 16 + sg + 8 * hr;
+        const int fi = row % unit;
+        const int owner = fi / R;
+        const int owner_feats = min(R, unit - owner * R);
+        const int rr = (row / unit) * owner_feats + (fi - owner * R);
+        const int rows_owner = owner_feats * rpf;
+        const uint32_t bse = inbox + ((rank * M) * rows_owner + rr) * 4;
+        const uint32_t rbase = S > 1 ? mapa(bse, static_cast<uint32_t>(owner)) : bse;
+        const uint32_t rbar = S > 1 ? mapa(smem_u32(&bar_inbox), static_cast<uint32_t>(owner)) : 0u;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int n = 2 * c + e;
+          float a16 = 0.0f;
+#pragma unroll
+          for (int q = 0; q < kChains; ++q) a16 += acc[q][b][2 * hr + e];
+          a16 += accb[b][2 * hr + e] * post;
+          const float v = go ? a16 : 0.0f;
+          if (n >= M) continue;
+          const uint32_t off = n * rows_owner * 4;
+          if (S > 1) st_async_f32(rbase + off, v, rbar);
+          else stsf(rbase + off, v);
+        }
+      }
+    }
+    if (S > 1) {
+      if (!mbar_wait<true>(smem_u32(&bar_inbox), 0, p.err)) s_abort = 1;
+    } else {
+      cons_sync(ncons);
+    }
+    auto partial = [&](int n, int lr) -> float {
+      float a = 0.0f;
+      for (uint32_t src = 0; src < S; ++src) a += ldsf(inbox + ((src * M + n) * mine + lr) * 4);
+      return a;
+    };
+    const int nf = f_hi - f_lo;
+    if (!s_abort && nf > 0) {
+      const float gs = __ldg(p.gs);
+      if (rpf == 1) {
+        for (int it = tid; it < nf * M; it += ncons) {
+          const int n = it / nf, lr = it % nf;
+          const int o = wk.out_base + f_lo + lr;
+          if (o >= p.n_out) continue;
+          p.out[static_cast<int64_t>(n) * p.ldo + o] = f32_to_bf16_rn(partial(n, lr) * gs);
+        }
+      } else {
+        // paired tiles: feature o = gate row o, up row o + unit
+        for (int it = tid; it < nf * M; it += ncons) {
+          const int n = it / nf, lr = it % nf;
+          const int feat = wk.out_base + f_lo + lr;
+          if (feat >= p.n_out) continue;
+          const float G = bf16_to_f32(f32_to_bf16_rn(partial(n, lr) * gs));
+          const float U = bf16_to_f32(f32_to_bf16_rn(partial(n, lr + nf) * gs));
+          p.out[static_cast<int64_t>(n) * p.ldo + feat] = f32_to_bf16_rn(silu_exact(G) * U);
+        }
+      }
+    }
+  } else if (S > 1) {
+    cluster_wait();  // the producer warp closes its cluster-barrier phase
+  }
+  __syncthreads();
+}
+
+}  // namespace fp4

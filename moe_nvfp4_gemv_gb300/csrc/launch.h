@@ -40,6 +40,14 @@ cudaError_t launch_rf_coop(int mode, int nt, const GemvParams& p, const LaunchCf
 // Clusters of `cluster` CTAs of the dense register-fed kernel that fit on the
 // GPU at once with `smem` bytes of dynamic shared memory each.
 cudaError_t rf_max_clusters(int mode, int nt, unsigned cluster, size_t smem, int* n);
+// Slab kernel (k_gemv_slab.cuh): dense NVFP4, 1 .. 8 tokens, r = 16-row
+// blocks per consumer warp (1 or 2); the block is (p.cw + 1) warps.
+cudaError_t launch_slab(int r, const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info);
+// Clusters of `cluster` slab-kernel CTAs (cw consumer warps, `smem` bytes of
+// dynamic shared memory) that fit on the GPU at once.
+cudaError_t slab_max_clusters(int r, int cw, unsigned cluster, size_t smem, int* n);
+// Registers per thread of the slab kernel with r row blocks per warp.
+cudaError_t slab_regs(int r, int* regs);
 cudaError_t launch_dense_bf16(int nt, const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info);
 cudaError_t launch_moe(int mode, int nt, const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info);
 cudaError_t launch_dequantize_rows(const uint8_t* w, const uint8_t* sf, void* out, int rows, int K,

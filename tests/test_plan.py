@@ -1,4 +1,5 @@
-"""The dense GEMV's launch plan for M <= 16 (fp4gemv_plan_rf, host only): the
+"""The dense GEMV's launch plans (host only): fp4gemv_plan_slab for M <= 8,
+fp4gemv_plan_rf for M <= 16 otherwise.  For plan_rf: the
 tile heights and K splits the library launches for the decode layers on
 GB300's co-resident CTA counts, and the invariants the kernel relies on for
 any shape (grid size, room for every scale group a tile's boxes touch)."""
@@ -180,3 +181,104 @@ def test_tc_plan_rejects(tc_plan_fn):
     assert tc_plan_fn(32, 4096, 4096, 2)[0] == 1
     assert tc_plan_fn(32, 4096, 4096, 0, bf16=2)[0] == 1
     assert tc_plan_fn(32, 4096, 4096, 0, sms=0)[0] == 1
+
+
+# --- the slab kernel's plan (M <= 8), host only ------------------------------------------
+
+class SlabPlan(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("row_blocks", "warps", "tile_rows", "split", "ctas", "k_slab", "stages",
+                                            "slab_bytes", "ctas_per_sm")] + [("smem_bytes", ctypes.c_size_t)]
+
+
+REGS = (107, 125)  # registers per thread of the two builds (only their CTA-per-SM bound matters here)
+
+
+@pytest.fixture(scope="module")
+def slab_fn():
+    from moe_nvfp4_gemv_gb300 import fp4gemv
+    f = fp4gemv.lib().fp4gemv_plan_slab
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_int] * 5 + [ctypes.POINTER(ctypes.c_int), ctypes.POINTER(SlabPlan)]
+
+    def plan(M, N, K, silu, regs=REGS, sms=SMS):
+        r = (ctypes.c_int * 2)(*regs)
+        out = SlabPlan()
+        return f(M, N, K, silu, sms, r, ctypes.byref(out)), out
+    return plan
+
+
+def slab_rule(M, N, K, silu, sms=SMS):
+    """The rule written out: M <= 4 and >= 1.2 tiles per SM; 128-row tiles,
+    three CTAs per SM, the largest split of one wave that fills >= 2.4 CTAs
+    per SM, two 256-K stages, the activation slab M x K-slab bf16 -- all
+    within a third of 228 KB."""
+    trows, occ = 128, 3
+    h = trows // 2 if silu else trows
+    tiles = -(-(N // 2 if silu else N) // h)
+    if M > 4 or tiles < 1.2 * sms:
+        return None
+    groups = 1 + (1 if (N // 2) % h == 0 else 2) if silu else 1
+    stage = -(-(trows * 128 + groups * 2048) // 1024) * 1024
+    dyn = 228 * 1024 // occ - 2048
+    inbox = 8 * 144 * 4
+    for S in (8, 4, 2, 1):
+        if tiles * S > occ * sms:
+            continue
+        if tiles * S < 2.4 * sms:
+            return None
+        kslab = -(-(-(-K // S)) // 64) * 64
+        if S > 1 and (kslab < 256 or (S - 1) * kslab >= K):
+            continue
+        nst = -(-kslab // 256)
+        slab = -(-(M * nst * 512) // 1024) * 1024
+        smem = 1024 + slab + 2 * stage + inbox
+        if smem > dyn:
+            return None
+        return dict(split=-(-K // kslab), ctas=tiles * -(-K // kslab), k_slab=kslab, stages=2, slab_bytes=slab,
+                    smem_bytes=smem)
+    return None
+
+
+@pytest.mark.parametrize("M", [1, 2, 4, 8])
+@pytest.mark.parametrize("N,K,silu", [(6144, 4096, 0), (4096, 4096, 0), (28672, 4096, 1), (4096, 14336, 0),
+                                      (57344, 8192, 1), (8192, 28672, 0), (10240, 8192, 0), (8192, 8192, 0),
+                                      (2048, 2304, 0), (1056, 1280, 1)])
+def test_slab_plan_matches_rule(slab_fn, M, N, K, silu):
+    st, p = slab_fn(M, N, K, silu)
+    want = slab_rule(M, N, K, silu)
+    if want is None:
+        assert st == 2
+        return
+    assert st == 0
+    got = dict(split=p.split, ctas=p.ctas, k_slab=p.k_slab, stages=p.stages, slab_bytes=p.slab_bytes,
+               smem_bytes=p.smem_bytes)
+    assert got == want
+    assert (p.row_blocks, p.warps, p.tile_rows, p.ctas_per_sm) == (2, 4, 128, 3)
+    # every rank has a non-empty K range and the slab holds the rank's K
+    assert (p.split - 1) * p.k_slab < K and p.slab_bytes >= M * p.k_slab * 2
+
+
+@pytest.mark.parametrize("M,N,K,silu,split,ctas", [
+    (1, 28672, 4096, 1, 2, 448),    # Llama-3-8B gate_up
+    (4, 28672, 4096, 1, 2, 448),    # gate_up at 4 tokens
+    (1, 57344, 8192, 1, 1, 448),    # Llama-3-70B gate_up
+])
+def test_slab_plan_decode_layers(slab_fn, M, N, K, silu, split, ctas):
+    st, p = slab_fn(M, N, K, silu)
+    assert st == 0 and (p.split, p.ctas) == (split, ctas)
+
+
+@pytest.mark.parametrize("M,N,K,silu", [(1, 4096, 4096, 0), (1, 4096, 14336, 0), (1, 6144, 4096, 0),
+                                        (8, 28672, 4096, 1), (2, 57344, 8192, 1)])
+def test_slab_plan_declines(slab_fn, M, N, K, silu):
+    # o_proj, down, qkv: too few tiles; 8 tokens: beyond the slab kernel's
+    # range; 70B gate_up at 2 tokens: the 32 KB slab does not fit beside two
+    # stages at three CTAs per SM
+    assert slab_fn(M, N, K, silu)[0] == 2
+
+
+def test_slab_plan_rejects_bad_arguments(slab_fn):
+    assert slab_fn(9, 4096, 4096, 0)[0] == 2
+    assert slab_fn(0, 4096, 4096, 0)[0] == 1
+    assert slab_fn(1, 4096, 4096, 2)[0] == 1
+    assert slab_fn(1, 4096, 4096, 0, sms=0)[0] == 1
