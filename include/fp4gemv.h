@@ -182,6 +182,23 @@ fp4gemv_status fp4gemv_moe_down_combine_noalloc(const void* act, const int32_t* 
  * Returns FP4GEMV_ERR_CUDA if the synchronization itself fails. */
 fp4gemv_status fp4gemv_get_device_error(cudaStream_t stream);
 
+/* Wait limit of the kernels' bounded waits on the current device, in ns
+ * (0 restores the built-in 2 s).  A wait that runs out records
+ * FP4GEMV_ERR_TIMEOUT in the device error word and the kernel winds down,
+ * leaving its outputs unwritten.  Synchronous; affects launches made after
+ * it returns.  FP4GEMV_ERR_CUDA if the device copy fails. */
+fp4gemv_status fp4gemv_set_wait_limit_ns(uint64_t ns);
+
+/* Test hook for the timeout path (no counterpart on the pages): from now on
+ * the producers of the dense NVFP4 GEMV for 1 .. 16 tokens issue nothing at
+ * all -- no copy, no arrival -- for the 256-K ring stage with this index of
+ * every CTA, so the
+ * consumers' bounded wait for it runs out with no copy in flight; -1 (the
+ * default) turns it off.  A process-wide host setting read at each
+ * fp4gemv_nvfp4_gemv launch; for tests only.
+ * FP4GEMV_ERR_INVALID_ARG for stage < -1. */
+fp4gemv_status fp4gemv_debug_skip_stage(int stage);
+
 /* Static, human-readable name of a status code. */
 const char* fp4gemv_status_string(fp4gemv_status status);
 

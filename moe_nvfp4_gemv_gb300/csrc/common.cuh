@@ -2,9 +2,10 @@
 //
 // Inline-PTX wrappers for mbarriers, TMA / bulk copies, cp.async, tcgen05
 // (tensor memory, MMA), programmatic dependent launch and cluster shared
-// memory, plus the per-device error word.  Every wait is bounded: after
-// kWaitNs of wall-clock time it records FP4_ERR_TIMEOUT in the error word and
-// returns false so the caller can wind down instead of hanging.
+// memory, plus the per-device error word.  Every wait is bounded: after the
+// wait limit (2 s unless the host sets another) it records FP4_ERR_TIMEOUT in
+// the error word and returns false so the caller can wind down instead of
+// hanging.
 #pragma once
 
 #include <cstdint>
@@ -19,10 +20,18 @@ namespace fp4 {
 constexpr uint32_t FP4_ERR_TIMEOUT = 1u;
 constexpr uint32_t FP4_ERR_BADIDX = 2u;
 
-// The per-device error word lives in the API translation unit; kernels get its
-// device address as a parameter.
+// The per-device error state lives in the API translation unit; kernels get
+// the address of its error word as a parameter.  The state is
+//   { uint32 error word, uint32 unused, uint64 wait limit in ns }
+// so a wait that has to wait reads its limit 8 bytes past the word (the host
+// sets it with fp4gemv_set_wait_limit_ns; FP4GEMV_WAIT_NS without a state).
 __device__ __forceinline__ void raise_error(uint32_t* err, uint32_t bits) {
   if (err) atomicOr(err, bits);
+}
+__device__ __forceinline__ uint64_t wait_limit_ns(const uint32_t* err) {
+  if (!err) return FP4GEMV_WAIT_NS;
+  const uint64_t v = *reinterpret_cast<const volatile unsigned long long*>(err + 2);
+  return v ? v : FP4GEMV_WAIT_NS;
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -79,14 +88,15 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
   return ok != 0;
 }
 // Bounded wait for phase `parity`.  Returns false (and records a timeout) if
-// the phase did not complete within FP4GEMV_WAIT_NS.
+// the phase did not complete within the wait limit (wait_limit_ns).
 template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* err) {
   if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
+  const uint64_t limit = wait_limit_ns(err);
   for (uint32_t i = 1;; ++i) {
     if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
-    if ((i & 7u) == 0 && globaltimer() - t0 > FP4GEMV_WAIT_NS) {
+    if ((i & 7u) == 0 && globaltimer() - t0 > limit) {
       raise_error(err, FP4_ERR_TIMEOUT);
       return false;
     }
@@ -99,10 +109,11 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
 __device__ __forceinline__ bool mbar_wait_sleepy(uint32_t bar, uint32_t parity, uint32_t* err, uint32_t sleep_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
+  const uint64_t limit = wait_limit_ns(err);
   for (;;) {
     __nanosleep(sleep_ns);
     if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer() - t0 > FP4GEMV_WAIT_NS) {
+    if (globaltimer() - t0 > limit) {
       raise_error(err, FP4_ERR_TIMEOUT);
       return false;
     }

@@ -7,6 +7,7 @@
 
 #include <atomic>
 #include <cstdint>
+#include <cstddef>
 #include <cstring>
 
 #include "fp4gemv.h"
@@ -14,8 +15,16 @@
 #include "launch.h"
 
 namespace fp4 {
-// Per-device error word (one copy per device context of this library image).
-__device__ uint32_t g_error_word;
+// Per-device error state (one copy per device context of this library image):
+// the error word, then the wait limit the kernels' bounded waits use (see
+// common.cuh; 0 = the built-in 2 s).
+struct DeviceErrorState {
+  uint32_t word;
+  uint32_t unused;
+  unsigned long long wait_limit_ns;
+};
+__device__ DeviceErrorState g_dev_state = {0u, 0u, 0ull};
+static_assert(offsetof(DeviceErrorState, wait_limit_ns) == 8, "the kernels read the limit 8 bytes past the word");
 }  // namespace fp4
 
 namespace {
@@ -25,6 +34,7 @@ using fp4::KernelInfo;
 using fp4::LaunchCfg;
 
 std::atomic<uint64_t> g_launches{0};
+std::atomic<int> g_skip_stage{-1};  // test hook (fp4gemv_debug_skip_stage)
 
 constexpr int kMaxDevices = 64;
 
@@ -139,8 +149,8 @@ fp4gemv_status device_state(uint32_t** err, int* sms) {
   uint32_t* e = d.err.load(std::memory_order_acquire);
   if (!e) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, fp4::g_error_word) != cudaSuccess) return FP4GEMV_ERR_CUDA;
-    e = static_cast<uint32_t*>(p);
+    if (cudaGetSymbolAddress(&p, fp4::g_dev_state) != cudaSuccess) return FP4GEMV_ERR_CUDA;
+    e = &static_cast<fp4::DeviceErrorState*>(p)->word;
     d.err.store(e, std::memory_order_release);
   }
   int n = d.sms.load(std::memory_order_acquire);
@@ -627,6 +637,7 @@ fp4gemv_status dense_launch(int mode, const void* x, int64_t ldx, const void* w,
   p.x_off = x_off;
   p.cw = cw;
   p.slab_r = slab ? sp.r : 0;
+  p.skip_stage = g_skip_stage.load(std::memory_order_relaxed);
   p.err = err;
 
   LaunchCfg cfg{};
@@ -835,6 +846,7 @@ fp4gemv_status fp4gemv_moe_gate_up(const void* x, const int32_t* ids, int M, int
   p.inbox_off = tr.inbox_off;
   p.stage_bytes = stage_bytes;
   p.x_off = x_off;
+  p.skip_stage = -1;
   p.err = err;
   const int shared_cols = (M + NT - 1) / NT;
   LaunchCfg cfg{};
@@ -944,6 +956,7 @@ fp4gemv_status fp4gemv_moe_down_combine(const void* act, const int32_t* ids, con
   p.inbox_off = tr.inbox_off;
   p.stage_bytes = stage_bytes;
   p.x_off = x_off;
+  p.skip_stage = -1;
   p.err = err;
   const int shared_cols = (M + NT - 1) / NT;
   LaunchCfg cfg{};
@@ -958,10 +971,24 @@ fp4gemv_status fp4gemv_moe_down_combine(const void* act, const int32_t* ids, con
 fp4gemv_status fp4gemv_get_device_error(cudaStream_t stream) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return FP4GEMV_ERR_CUDA;
   uint32_t v = 0, zero = 0;
-  if (cudaMemcpyFromSymbol(&v, fp4::g_error_word, sizeof(v)) != cudaSuccess) return FP4GEMV_ERR_CUDA;
-  if (v && cudaMemcpyToSymbol(fp4::g_error_word, &zero, sizeof(zero)) != cudaSuccess) return FP4GEMV_ERR_CUDA;
+  if (cudaMemcpyFromSymbol(&v, fp4::g_dev_state, sizeof(v)) != cudaSuccess) return FP4GEMV_ERR_CUDA;
+  if (v && cudaMemcpyToSymbol(fp4::g_dev_state, &zero, sizeof(zero)) != cudaSuccess) return FP4GEMV_ERR_CUDA;
   if (v & fp4::FP4_ERR_TIMEOUT) return FP4GEMV_ERR_TIMEOUT;
   if (v & fp4::FP4_ERR_BADIDX) return FP4GEMV_ERR_BAD_INDEX;
+  return FP4GEMV_OK;
+}
+
+fp4gemv_status fp4gemv_set_wait_limit_ns(uint64_t ns) {
+  const unsigned long long v = ns;
+  if (cudaMemcpyToSymbol(fp4::g_dev_state, &v, sizeof(v), offsetof(fp4::DeviceErrorState, wait_limit_ns)) !=
+      cudaSuccess)
+    return FP4GEMV_ERR_CUDA;
+  return FP4GEMV_OK;
+}
+
+fp4gemv_status fp4gemv_debug_skip_stage(int stage) {
+  if (stage < -1) return FP4GEMV_ERR_INVALID_ARG;
+  g_skip_stage.store(stage, std::memory_order_relaxed);
   return FP4GEMV_OK;
 }
 

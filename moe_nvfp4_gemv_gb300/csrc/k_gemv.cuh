@@ -120,7 +120,8 @@ struct GemvParams {
   int cw;              // register-fed dense kernel: consumer warps = tile height / 16 (4 .. 8);
                        // slab kernel: consumer warps (2 or 4), tile height 16 slab_r cw
   int slab_r;          // slab kernel: 16-row blocks per consumer warp (1 or 2)
-  uint32_t* err;       // device error word
+  int skip_stage;      // test hook: the dense producers issue nothing for this 256-K stage (-1: none)
+  uint32_t* err;       // device error word (the wait limit follows it, see common.cuh)
 };
 
 struct CtaWork {

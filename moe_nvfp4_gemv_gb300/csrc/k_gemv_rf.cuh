@@ -306,7 +306,8 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, kOcc) gemv_rf_kernel(con
     }
     mbar_fence_init();
     const int pre0 = min(stages_of(act), nstages);
-    for (int s = 0; s < pre0; ++s) issue_weights(s, s);
+    for (int s = 0; s < pre0; ++s)
+      if (!kDense || s != p.skip_stage) issue_weights(s, s);
   }
   __syncthreads();
   if (S > 1) cluster_arrive_relaxed();  // paired with a wait before the first remote access
@@ -358,10 +359,11 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, kOcc) gemv_rf_kernel(con
         for (int s = 0, slot = 0, ph = 0; s < nst && !s_abort; ++s, slot = slot + 1 == nstages ? 0 : slot + 1, ph ^= slot == 0) {
           const uint32_t st = ring + slot * p.stage_bytes;
           const uint32_t fb = smem_u32(&bar_full[slot]);
-          if (s >= pre) {
-            if (!mbar_wait_sleepy(smem_u32(&bar_empty[slot]), ph ^ 1, p.err, 64)) { s_abort = 1; break; }
-            issue_weights(s, slot);
-          }
+          if (s >= pre && !mbar_wait_sleepy(smem_u32(&bar_empty[slot]), ph ^ 1, p.err, 64)) { s_abort = 1; break; }
+          // (test hook: nothing at all for the skipped stage -- no copy and no
+          // arrival, so the consumers' wait for it runs out with nothing in flight)
+          if (s == p.skip_stage) continue;
+          if (s >= pre) issue_weights(s, slot);
           const int k0 = wk.k_begin + s * C::kStageK;
           if (f16route) {
             const uint32_t xb = smem_u32(&bar_xfull[slot]);

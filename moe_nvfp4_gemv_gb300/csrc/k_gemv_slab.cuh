@@ -154,7 +154,8 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
     }
     mbar_fence_init();
     const int pre = min(nst, nstages);
-    for (int s = 0; s < pre; ++s) issue_weights(s, s);
+    for (int s = 0; s < pre; ++s)
+      if (s != p.skip_stage) issue_weights(s, s);  // (test hook: the skipped stage is never issued)
   }
   for (int i = tid; i < nst; i += blockDim.x) s_xbad[i] = 0;
   __syncthreads();
@@ -191,14 +192,14 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
           s_abort = 1;
           break;
         }
-        issue_weights(s, slot);
+        if (s != p.skip_stage) issue_weights(s, slot);
         issued = s + 1;
       }
       // After an abort, let every copy still in flight land before the CTA
       // (and its shared memory) goes away: the latest fill of each slot.
       if (s_abort) {
         for (int s = max(0, issued - nstages); s < issued; ++s)
-          (void)mbar_wait(smem_u32(&bar_full[s % nstages]), (s / nstages) & 1, p.err);
+          if (s != p.skip_stage) (void)mbar_wait(smem_u32(&bar_full[s % nstages]), (s / nstages) & 1, p.err);
       }
     }
   } else {

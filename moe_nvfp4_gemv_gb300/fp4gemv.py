@@ -58,6 +58,8 @@ def _load() -> ctypes.CDLL:
                                            vp, vp, sz, i32, vp]),
         "fp4gemv_get_device_error": (i32, [vp]),
         "fp4gemv_status_string": (ctypes.c_char_p, [i32]),
+        "fp4gemv_set_wait_limit_ns": (i32, [ctypes.c_uint64]),
+        "fp4gemv_debug_skip_stage": (i32, [i32]),
         "fp4gemv_launch_count": (ctypes.c_uint64, []),
     }
     for name, (res, args) in sigs.items():
@@ -256,6 +258,18 @@ def get_device_error(device: torch.device | None = None) -> int:
     (0 = FP4GEMV_OK, 5 = timeout, 6 = bad expert id)."""
     dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
     return int(_lib.fp4gemv_get_device_error(_stream(dev)))
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    """Wait limit of the kernels' bounded waits on the current device (0: the
+    built-in 2 s)."""
+    _check(_lib.fp4gemv_set_wait_limit_ns(int(ns)), "fp4gemv_set_wait_limit_ns")
+
+
+def debug_skip_stage(stage: int) -> None:
+    """Test hook: the dense GEMV (1 .. 16 tokens) issues nothing for ring stage
+    ``stage`` of every CTA, so its wait runs out (-1: off)."""
+    _check(_lib.fp4gemv_debug_skip_stage(int(stage)), "fp4gemv_debug_skip_stage")
 
 
 def launch_count() -> int:
