@@ -586,6 +586,22 @@ def config_results(dev, compact=True):
         del ws
     res["llama8b_bf16"] = tb
 
+    res["decode_chain"] = decode_chain(dev, gs, peak, Ms=(1, 4, 8) if compact else (1, 2, 4, 8, 16, 32))
+
+    # BF16 GEMV against cuBLAS (torch.nn.functional.linear) on the 8B layers
+    bc = {}
+    for name, (N, K, silu) in LAYERS.items():
+        ws = [synth.bf16_weight(N, K, seed=r, device=dev) for r in range(replicas_for(2 * N * K))]
+        bc[name] = {}
+        for M in ((1, 8, 32, 128) if compact else (1, 2, 4, 8, 16, 32, 64, 128)):
+            x = synth.activations(M, K, seed=M, device=dev)
+            out = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+            us_g = time_calls([lambda w=w: fp4gemv.bf16_gemv(x, w, out=out) for w in ws], 20, stream)
+            us_c = time_calls([lambda w=w: torch.matmul(x, w.t(), out=out) for w in ws], 20, stream)
+            bc[name][str(M)] = {"gemv_us": round(us_g, 2), "cublas_us": round(us_c, 2)}
+        del ws
+    res["bf16_gemv_vs_cublas"] = bc
+
     # MoE block
     c = synth.MOE
     E, H, I, SI, topk = c["E"], c["H"], c["I"], c["SI"], c["topk"]
@@ -663,6 +679,53 @@ def config_results(dev, compact=True):
     res["sweep_8192"] = {"rows": sw, "crossover_M": cross}
     del ws, wbs, wb
     assert fp4gemv.get_device_error() == 0
+    return res
+
+
+def decode_chain(dev, gs, peak, Ms=(1, 4, 8)):
+    """The four decode linears of a Llama-3-8B layer chained with their real
+    data dependencies -- x -> qkv; o_proj on the first 4096 columns of the
+    qkv output (a strided view standing in for attention's output);
+    gate_up + silu_mul on o_proj's output; down on that; down's output is the
+    next layer's x -- over 7 layers of distinct weights (L2-cold), replayed as
+    one CUDA graph.  Reported per layer: with PDL on every launch; with PDL
+    off on o_proj (the launch after attention, a kernel that needs the whole
+    GPU); with PDL off everywhere; and the sum of the four calls timed alone
+    (per_call), whose difference to the chain is the overlap PDL buys."""
+    from moe_nvfp4_gemv_gb300 import fp4gemv
+    stream = torch.cuda.current_stream(dev)
+    nl = 7
+    ws = {name: [(synth.fp4_bytes(N, K, seed=100 * l + 1, device=dev),
+                  synth.e4m3_bytes(fp4gemv.scale_bytes(N, K), seed=100 * l + 2, device=dev)) for l in range(nl)]
+          for name, (N, K, silu) in LAYERS.items()}
+    layer_bytes = {M: sum(nvfp4_bytes(M, N, K, s) for (N, K, s) in LAYERS.values()) for M in Ms}
+    res = {}
+    for M in Ms:
+        H = LAYERS["o_proj"][1]
+        x0 = synth.activations(M, H, seed=M, device=dev)
+        bufs = {"x": [x0] + [torch.empty(M, H, dtype=torch.bfloat16, device=dev) for _ in range(nl)],
+                "qkv": torch.empty(M, LAYERS["qkv"][0], dtype=torch.bfloat16, device=dev),
+                "o": torch.empty(M, H, dtype=torch.bfloat16, device=dev),
+                "gu": torch.empty(M, LAYERS["gate_up"][0] // 2, dtype=torch.bfloat16, device=dev)}
+
+        def chain(pdl_o, pdl_rest):
+            def fn():
+                for l in range(nl):
+                    x = bufs["x"][l]
+                    fp4gemv.nvfp4_gemv(x, *ws["qkv"][l], gs, pdl=pdl_rest, out=bufs["qkv"])
+                    fp4gemv.nvfp4_gemv(bufs["qkv"][:, :H], *ws["o_proj"][l], gs, pdl=pdl_o, out=bufs["o"])
+                    fp4gemv.nvfp4_gemv(bufs["o"], *ws["gate_up"][l], gs, silu_mul=True, pdl=pdl_rest, out=bufs["gu"])
+                    fp4gemv.nvfp4_gemv(bufs["gu"], *ws["down"][l], gs, pdl=pdl_rest, out=bufs["x"][l + 1])
+            return fn
+
+        row = {}
+        for key, (po, pr) in (("pdl", (True, True)), ("pdl_off_after_attention", (False, True)),
+                              ("no_pdl", (False, False))):
+            us = time_calls([chain(po, pr)], 1, stream) / nl
+            row[key] = {"us_per_layer": round(us, 2), "GB/s": round(layer_bytes[M] / (us * 1e-6) / 1e9, 1),
+                        "frac": round(layer_bytes[M] / (us * 1e-6) / 1e9 / peak, 3)}
+        res[str(M)] = row
+    del ws
     return res
 
 

@@ -80,6 +80,17 @@ fp4gemv_status fp4gemv_nvfp4_gemv(const void* x, int64_t ldx, const uint8_t* w, 
                                   const float* global_scale, void* out, int64_t ldo, int M, int N, int K,
                                   int silu_mul, int pdl, cudaStream_t stream);
 
+/* fp4gemv_nvfp4_gemv on a scale buffer padded along K (the zero-copy reuse of
+ * another library's scale tensor, vllm.models.flint.ops.linear,
+ * _swizzled_scale_buffer): each 128-row group of w_sf holds sf_k_blocks
+ * 16-wide K blocks (sf_k_blocks / 4 chunks of 512 bytes) instead of
+ * roundup(K / 16, 4); the chunks past roundup(K / 16, 4) are never read.
+ * sf_k_blocks: 0 (the exact layout) or a multiple of 4 >= roundup(K/16, 4),
+ * else FP4GEMV_ERR_INVALID_ARG.  Everything else as fp4gemv_nvfp4_gemv. */
+fp4gemv_status fp4gemv_nvfp4_gemv_padded(const void* x, int64_t ldx, const uint8_t* w, const uint8_t* w_sf,
+                                         int sf_k_blocks, const float* global_scale, void* out, int64_t ldo, int M,
+                                         int N, int K, int silu_mul, int pdl, cudaStream_t stream);
+
 /* bf16_gemv (vllm.models.flint.ops.nvfp4_gemv, bf16_gemv): same contract
  * with a row-major bf16 weight w [N, K] and global scale 1.
  * Shapes: 1 <= M <= FP4GEMV_MAX_M, N % 16 == 0 (N % 32 with silu_mul),
@@ -93,6 +104,11 @@ fp4gemv_status fp4gemv_bf16_gemv(const void* x, int64_t ldx, const void* w, void
  * Shapes: rows % 16 == 0, K % 256 == 0 (the pages' assertion). */
 fp4gemv_status fp4gemv_dequantize_rows(const uint8_t* w, const uint8_t* w_sf, void* out, int rows, int K,
                                        cudaStream_t stream);
+
+/* fp4gemv_dequantize_rows on a scale buffer padded along K: sf_k_blocks as
+ * for fp4gemv_nvfp4_gemv_padded (0 or a multiple of 4 >= K / 16). */
+fp4gemv_status fp4gemv_dequantize_rows_padded(const uint8_t* w, const uint8_t* w_sf, int sf_k_blocks, void* out,
+                                              int rows, int K, cudaStream_t stream);
 
 /* Dequantize + GEMM path (vllm.models.flint.ops.linear, _dequant_gemm):
  *   w_bf16 = dequantize_rows(w, w_sf);  out = bf16(fp32(x @ w_bf16^T) * gs)

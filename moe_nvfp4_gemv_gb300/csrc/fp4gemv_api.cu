@@ -518,10 +518,14 @@ fp4gemv_status slab_registers(int (&regs)[2]) {
   return FP4GEMV_OK;
 }
 
+// sf_kbp: 16-wide K blocks per 128-row group of the scale buffer (0: the
+// exact roundup(K / 16, 4); more for buffers padded along K).
 fp4gemv_status dense_launch(int mode, const void* x, int64_t ldx, const void* w, const uint8_t* w_sf,
                             const float* gs, void* out, int64_t ldo, int M, int N, int K, int silu_mul, int pdl,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, int sf_kbp = 0) {
   const bool fp4w = mode == fp4::kDenseFp4;
+  const int kbp_exact = ((K / 16) + 3) / 4 * 4;
+  if (sf_kbp != 0 && (sf_kbp < kbp_exact || sf_kbp % 4 != 0)) return FP4GEMV_ERR_INVALID_ARG;
   // Order of the checks: flags and sizes, then alignment, then null
   // pointers (a null pointer passes the alignment test), so a call with
   // null pointers and a bad size reports the size.
@@ -627,7 +631,7 @@ fp4gemv_status dense_launch(int mode, const void* x, int64_t ldx, const void* w,
   p.K = K;
   p.k_split = kslab;
   p.rows_w = N;
-  p.kbp = ((K / 16) + 3) / 4 * 4;
+  p.kbp = sf_kbp ? sf_kbp : kbp_exact;
   p.nstages = nstages;
   p.nx = tr.nx;
   p.wstage = tr.wstage;
@@ -731,21 +735,34 @@ fp4gemv_status fp4gemv_nvfp4_gemv(const void* x, int64_t ldx, const uint8_t* w, 
   return dense_launch(fp4::kDenseFp4, x, ldx, w, w_sf, global_scale, out, ldo, M, N, K, silu_mul, pdl, stream);
 }
 
+fp4gemv_status fp4gemv_nvfp4_gemv_padded(const void* x, int64_t ldx, const uint8_t* w, const uint8_t* w_sf,
+                                         int sf_k_blocks, const float* global_scale, void* out, int64_t ldo, int M,
+                                         int N, int K, int silu_mul, int pdl, cudaStream_t stream) {
+  return dense_launch(fp4::kDenseFp4, x, ldx, w, w_sf, global_scale, out, ldo, M, N, K, silu_mul, pdl, stream,
+                      sf_k_blocks);
+}
+
 fp4gemv_status fp4gemv_bf16_gemv(const void* x, int64_t ldx, const void* w, void* out, int64_t ldo, int M, int N,
                                  int K, int silu_mul, int pdl, cudaStream_t stream) {
   return dense_launch(fp4::kDenseBf16, x, ldx, w, nullptr, nullptr, out, ldo, M, N, K, silu_mul, pdl, stream);
 }
 
-fp4gemv_status fp4gemv_dequantize_rows(const uint8_t* w, const uint8_t* w_sf, void* out, int rows, int K,
-                                       cudaStream_t stream) {
+fp4gemv_status fp4gemv_dequantize_rows_padded(const uint8_t* w, const uint8_t* w_sf, int sf_k_blocks, void* out,
+                                              int rows, int K, cudaStream_t stream) {
   if (rows < 1 || K < 1) return FP4GEMV_ERR_INVALID_ARG;
   if (rows % 16 != 0 || K % 256 != 0) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
+  if (sf_k_blocks != 0 && (sf_k_blocks < K / 16 || sf_k_blocks % 4 != 0)) return FP4GEMV_ERR_INVALID_ARG;
   if (!aligned(w, 16) || !aligned(out, 16) || !aligned(w_sf, 4)) return FP4GEMV_ERR_MISALIGNED;
   if (!w || !w_sf || !out) return FP4GEMV_ERR_INVALID_ARG;
   fp4gemv_status st = device_state(nullptr, nullptr);
   if (st != FP4GEMV_OK) return st;
   g_launches.fetch_add(1, std::memory_order_relaxed);
-  return from_cuda(fp4::launch_dequantize_rows(w, w_sf, out, rows, K, stream));
+  return from_cuda(fp4::launch_dequantize_rows(w, w_sf, out, rows, K, sf_k_blocks, stream));
+}
+
+fp4gemv_status fp4gemv_dequantize_rows(const uint8_t* w, const uint8_t* w_sf, void* out, int rows, int K,
+                                       cudaStream_t stream) {
+  return fp4gemv_dequantize_rows_padded(w, w_sf, 0, out, rows, K, stream);
 }
 
 fp4gemv_status fp4gemv_dequant_gemm(const void* x, int64_t ldx, const uint8_t* w, const uint8_t* w_sf,

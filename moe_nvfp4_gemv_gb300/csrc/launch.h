@@ -50,7 +50,8 @@ cudaError_t slab_max_clusters(int r, int cw, unsigned cluster, size_t smem, int*
 cudaError_t slab_regs(int r, int* regs);
 cudaError_t launch_dense_bf16(int nt, const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info);
 cudaError_t launch_moe(int mode, int nt, const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info);
-cudaError_t launch_dequantize_rows(const uint8_t* w, const uint8_t* sf, void* out, int rows, int K,
+// kbp: 16-wide K blocks per 128-row scale group in sf (0: roundup(K / 16, 4)).
+cudaError_t launch_dequantize_rows(const uint8_t* w, const uint8_t* sf, void* out, int rows, int K, int kbp,
                                    cudaStream_t stream);
 
 // Shared launch helper for the kernel translation units.

@@ -50,6 +50,8 @@ def _load() -> ctypes.CDLL:
         "fp4gemv_nvfp4_gemv": (i32, [vp, i64, vp, vp, vp, vp, i64, i32, i32, i32, i32, i32, vp]),
         "fp4gemv_bf16_gemv": (i32, [vp, i64, vp, vp, i64, i32, i32, i32, i32, i32, vp]),
         "fp4gemv_dequantize_rows": (i32, [vp, vp, vp, i32, i32, vp]),
+        "fp4gemv_dequantize_rows_padded": (i32, [vp, vp, i32, vp, i32, i32, vp]),
+        "fp4gemv_nvfp4_gemv_padded": (i32, [vp, i64, vp, vp, i32, vp, vp, i64, i32, i32, i32, i32, i32, vp]),
         "fp4gemv_dequant_gemm": (i32, [vp, i64, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, vp]),
         "fp4gemv_moe_gate_up": (i32, [vp, vp, i32, i32, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp, i32, vp, i32,
                                       vp]),
@@ -117,26 +119,51 @@ def _rows_bf16(x: torch.Tensor, name: str) -> torch.Tensor:
     return x
 
 
+def flat_scale_buffer(weight_scale: torch.Tensor) -> torch.Tensor:
+    """uint8 flat view (no copy) of the storage behind a block-scale tensor.
+
+    A contiguous tensor is its own flat buffer.  A strided view -- the way
+    another library may index the same 128x4-swizzled bytes (for instance as
+    [rows / 128, K-blocks / 4, 32, 4, 4]) -- must start at offset 0 of its
+    storage; the whole storage is then the flat buffer."""
+    if weight_scale.element_size() != 1:
+        raise ValueError("block scales are one byte each (uint8 / float8_e4m3fn)")
+    t = weight_scale if weight_scale.dtype == torch.uint8 else weight_scale.view(torch.uint8)
+    if t.is_contiguous():
+        return t.reshape(-1)
+    if t.storage_offset() != 0:
+        raise ValueError("a strided scale view must start at offset 0 of its storage")
+    nbytes = t.untyped_storage().nbytes()
+    return t.as_strided((nbytes,), (1,), 0)
+
+
 def scale_bytes(rows: int, K: int) -> int:
     """Bytes of the flat 128x4-swizzled scale buffer of a [rows, K] weight."""
     return int(_lib.fp4gemv_scale_bytes(rows, K))
 
 
 def nvfp4_gemv(x: torch.Tensor, weight: torch.Tensor, weight_scale: torch.Tensor, global_scale: torch.Tensor,
-               silu_mul: bool = False, pdl: bool = True, out: torch.Tensor | None = None) -> torch.Tensor:
+               silu_mul: bool = False, pdl: bool = True, out: torch.Tensor | None = None,
+               sf_k_blocks: int = 0) -> torch.Tensor:
     """bf16 [M, N] = bf16(fp32(x @ dequant(weight).T) * global_scale); with
     silu_mul the [M, N/2] bf16 silu(gate) * up of the [gate | up] halves.
 
-    The decode path: only cheap attribute checks here (the library validates
-    shapes, alignment and pointers before it launches anything)."""
+    ``weight_scale``: the flat 128x4-swizzled buffer, or a strided view of one
+    (see ``flat_scale_buffer``); ``sf_k_blocks`` > 0 for a buffer whose
+    128-row groups hold that many 16-wide K blocks (padded past
+    roundup(K / 16, 4)).  The decode path: only cheap attribute checks here
+    (the library validates shapes, alignment and pointers before it launches
+    anything)."""
     if x.dtype is not _BF16 or x.dim() != 2 or x.stride(1) != 1:
         raise ValueError("x must be a 2-D bf16 tensor with unit inner stride")
     M, K = x.shape
     if weight.dtype not in _FP4_WEIGHT_DTYPES or weight.dim() != 2 or not weight.is_contiguous() \
             or weight.shape[1] * 2 != K:
         raise ValueError("weight must be a contiguous uint8 [N, K/2] tensor")
-    if weight_scale.dtype not in _SCALE_DTYPES or not weight_scale.is_contiguous():
-        raise ValueError("weight_scale must be a contiguous uint8 / float8_e4m3fn tensor")
+    if weight_scale.dtype not in _SCALE_DTYPES:
+        raise ValueError("weight_scale must be a uint8 / float8_e4m3fn tensor")
+    if not weight_scale.is_contiguous():
+        weight_scale = flat_scale_buffer(weight_scale)
     if global_scale.dtype is not torch.float32 or global_scale.numel() != 1:
         raise ValueError("global_scale must be one float32 value")
     N = weight.shape[0]
@@ -147,6 +174,13 @@ def nvfp4_gemv(x: torch.Tensor, weight: torch.Tensor, weight_scale: torch.Tensor
     elif out.dtype is not _BF16 or out.dim() != 2 or out.stride(1) != 1 or out.shape[0] != M or out.shape[1] != n_out:
         raise ValueError(f"out must be a bf16 [{M}, {n_out}] tensor with unit inner stride")
     st = _raw_stream(dev.index)
+    if sf_k_blocks:
+        status = _lib.fp4gemv_nvfp4_gemv_padded(x.data_ptr(), x.stride(0), weight.data_ptr(), weight_scale.data_ptr(),
+                                                int(sf_k_blocks), global_scale.data_ptr(), out.data_ptr(),
+                                                out.stride(0), M, N, K, 1 if silu_mul else 0, 1 if pdl else 0, st)
+        if status:
+            raise Fp4GemvError(status, "fp4gemv_nvfp4_gemv_padded")
+        return out
     status = _nvfp4_gemv(x.data_ptr(), x.stride(0), weight.data_ptr(), weight_scale.data_ptr(),
                          global_scale.data_ptr(), out.data_ptr(), out.stride(0), M, N, K, 1 if silu_mul else 0,
                          1 if pdl else 0, st)
@@ -172,14 +206,16 @@ def bf16_gemv(x: torch.Tensor, weight: torch.Tensor, silu_mul: bool = False, pdl
 
 
 def dequantize_rows(weight: torch.Tensor, weight_scale: torch.Tensor,
-                    out: torch.Tensor | None = None) -> torch.Tensor:
-    """Exact bf16 [rows, K] of e2m1 * e4m3 (global scale not applied)."""
+                    out: torch.Tensor | None = None, sf_k_blocks: int = 0) -> torch.Tensor:
+    """Exact bf16 [rows, K] of e2m1 * e4m3 (global scale not applied);
+    ``weight_scale`` and ``sf_k_blocks`` as for ``nvfp4_gemv``."""
     w = _bytes(weight)
     rows, K = w.shape[0], w.shape[1] * 2
     if out is None:
         out = torch.empty(rows, K, dtype=torch.bfloat16, device=w.device)
-    _check(_lib.fp4gemv_dequantize_rows(_ptr(w), _ptr(_bytes(weight_scale)), _ptr(out), rows, K,
-                                        _stream(w.device)), "fp4gemv_dequantize_rows")
+    sf = flat_scale_buffer(weight_scale)
+    _check(_lib.fp4gemv_dequantize_rows_padded(_ptr(w), _ptr(sf), int(sf_k_blocks), _ptr(out), rows, K,
+                                               _stream(w.device)), "fp4gemv_dequantize_rows")
     return out
 
 

@@ -1,0 +1,171 @@
+"""Dense linear layers that route each call by its token count.
+
+The dispatch of vllm.models.flint.ops.linear (FlintNvFp4LinearKernel.
+apply_weights, FlintBf16LinearMethod.apply, _use_gemv, _dequant_gemm,
+gate_up_silu_mul) over this library's kernels:
+
+* NVFP4 weights (``NvFp4Linear``): a call of M tokens (the input flattened
+  to [M, K]) runs the small-M GEMV (``fp4gemv.nvfp4_gemv``) while
+  ``M < dequant_min_m``; from ``dequant_min_m`` tokens it dequantizes the
+  weight to BF16 and runs a GEMM with the global scale as alpha on the fp32
+  accumulator -- this library's tensor-core GEMM up to ``MAX_M`` tokens
+  (``fp4gemv.dequant_gemm``), cuBLAS beyond or on a scale buffer padded along
+  K (``torch.addmm`` with BF16 reduced-precision reductions off, alpha the
+  host copy of the global scale, as the page does).
+* BF16 weights (``Bf16Linear``): ``fp4gemv.bf16_gemv`` up to
+  ``gemv_max_m`` tokens, cuBLAS (``torch.nn.functional.linear``) beyond.
+* Fused gate/up projections (``[gate | up]`` halves of N): ``gate_up_silu_mul``
+  returns ``bf16(silu(G) * U)`` from one GEMV for small M, else None (the
+  caller runs the linear and its own silu_and_mul).
+
+The pages route by tuned tables (``pick_nt`` / ``tuned``, contents not
+printed).  Here the library accepts every valid shape and picks its launch
+shape itself, so ``gemv_tile`` answers only which token tile a call uses and
+``DEQUANT_MIN_M`` is the measured crossover: on GB300, N = K = 8192, the GEMV
+was faster than dequantize + GEMM at every M up to 128 (43.5 vs 64.6 us at
+M = 128), so the GEMV serves every M it supports and the dequantize + GEMM
+path starts past it.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import fp4gemv
+
+MAX_M = fp4gemv.MAX_M
+# First token count routed to dequantize + GEMM (the GEMV is faster up to MAX_M).
+DEQUANT_MIN_M = MAX_M + 1
+# Largest token count the BF16 GEMV takes by default (cuBLAS beyond).
+BF16_GEMV_MAX_M = MAX_M
+
+
+def gemv_tile(m: int) -> int | None:
+    """Token tile the GEMV uses for ``m`` tokens (the MMA N it covers): 8 or
+    16 for the register-fed kernels, 16 .. 128 for the tensor-core kernel;
+    None when the GEMV does not take ``m`` (the analogue of ``pick_nt``)."""
+    if m < 1 or m > MAX_M:
+        return None
+    if m <= 8:
+        return 8
+    if m <= 16:
+        return 16
+    t = 32
+    while t < m:
+        t *= 2
+    return t
+
+
+class NvFp4Linear(torch.nn.Module):
+    """y = bf16(fp32(x @ dequant(W)^T) * global_scale), routed by token count.
+
+    weight: uint8 [N, K/2] (two E2M1 codes per byte, low nibble first);
+    weight_scale: the 128x4-swizzled E4M3 block scales of [N, K] (uint8 or
+    float8_e4m3fn), as the flat buffer or as another library's strided view
+    of it (used without a copy, vllm.models.flint.ops.linear,
+    _swizzled_scale_buffer); ``sf_k_blocks``: 16-wide K blocks per 128-row
+    group when the buffer is padded along K (0: roundup(K / 16, 4));
+    global_scale: fp32 [1] on the weight's device.  ``pdl``: launch the GEMV
+    with programmatic dependent launch (pass False after kernels that need
+    the whole GPU).  ``dequant_min_m``: first token count routed to
+    dequantize + GEMM."""
+
+    def __init__(self, weight: torch.Tensor, weight_scale: torch.Tensor, global_scale: torch.Tensor,
+                 pdl: bool = True, dequant_min_m: int = DEQUANT_MIN_M, sf_k_blocks: int = 0):
+        super().__init__()
+        if weight.dtype != torch.uint8 or weight.dim() != 2 or not weight.is_contiguous():
+            raise ValueError("weight must be a contiguous uint8 [N, K/2] tensor")
+        N, K = weight.shape[0], weight.shape[1] * 2
+        sf = fp4gemv.flat_scale_buffer(weight_scale)
+        kbp = sf_k_blocks or (K // 16 + 3) // 4 * 4
+        need = (N + 127) // 128 * 128 * kbp
+        if sf.numel() < need:
+            raise ValueError(f"weight_scale must hold at least {need} bytes (128x4-swizzled [N, {kbp}] blocks)")
+        if global_scale.dtype != torch.float32 or global_scale.numel() != 1:
+            raise ValueError("global_scale must be one float32 value")
+        self.register_buffer("weight", weight, persistent=False)
+        self.register_buffer("weight_scale", sf, persistent=False)
+        self.register_buffer("global_scale", global_scale.reshape(1), persistent=False)
+        self.global_scale_host = float(global_scale.reshape(()).item())  # alpha of the cuBLAS path
+        self.out_features, self.in_features = N, K
+        self.pdl = bool(pdl)
+        self.dequant_min_m = int(dequant_min_m)
+        self.sf_k_blocks = int(sf_k_blocks)
+
+    def route(self, m: int) -> str:
+        """'empty', 'gemv' or 'dequant_gemm' for a call of ``m`` tokens."""
+        if m == 0:
+            return "empty"
+        if m >= self.dequant_min_m or gemv_tile(m) is None:
+            return "dequant_gemm"
+        return "gemv"
+
+    def forward(self, x: torch.Tensor) -> torch.Tensor:
+        x2 = x.reshape(-1, x.shape[-1])
+        m = x2.shape[0]
+        route = self.route(m)
+        if route == "empty":
+            return x2.new_empty(*x.shape[:-1], self.out_features)
+        if route == "gemv":
+            out = fp4gemv.nvfp4_gemv(x2, self.weight, self.weight_scale, self.global_scale, pdl=self.pdl,
+                                     sf_k_blocks=self.sf_k_blocks)
+        else:
+            out = self._dequant_gemm(x2)
+        return out.view(*x.shape[:-1], self.out_features)
+
+    def _dequant_gemm(self, x2: torch.Tensor) -> torch.Tensor:
+        if x2.shape[0] <= MAX_M and not self.sf_k_blocks:
+            return fp4gemv.dequant_gemm(x2, self.weight, self.weight_scale, self.global_scale)
+        # past MAX_M tokens (or on a padded scale buffer): dequantize, then cuBLAS
+        w = fp4gemv.dequantize_rows(self.weight, self.weight_scale, sf_k_blocks=self.sf_k_blocks)
+        out = torch.empty(x2.shape[0], self.out_features, dtype=torch.bfloat16, device=x2.device)
+        matmul = torch.backends.cuda.matmul
+        prev = matmul.allow_bf16_reduced_precision_reduction
+        matmul.allow_bf16_reduced_precision_reduction = False  # fp32 split-K sums
+        try:
+            torch.addmm(out, x2, w.t(), beta=0, alpha=self.global_scale_host, out=out)
+        finally:
+            matmul.allow_bf16_reduced_precision_reduction = prev
+        return out
+
+    def gate_up_silu_mul(self, x: torch.Tensor) -> torch.Tensor | None:
+        """bf16(silu(G) * U) of the [gate | up] halves in one GEMV when the
+        GEMV takes this call, else None."""
+        if x.dim() != 2 or self.out_features % 32 != 0 or self.route(x.shape[0]) != "gemv":
+            return None
+        return fp4gemv.nvfp4_gemv(x, self.weight, self.weight_scale, self.global_scale, silu_mul=True, pdl=self.pdl,
+                                  sf_k_blocks=self.sf_k_blocks)
+
+
+class Bf16Linear(torch.nn.Module):
+    """y = bf16(fp32(x @ W^T)) for a row-major bf16 [N, K] weight: the GEMV up
+    to ``gemv_max_m`` tokens, cuBLAS beyond."""
+
+    def __init__(self, weight: torch.Tensor, pdl: bool = True, gemv_max_m: int = BF16_GEMV_MAX_M):
+        super().__init__()
+        if weight.dtype != torch.bfloat16 or weight.dim() != 2 or not weight.is_contiguous():
+            raise ValueError("weight must be a contiguous bf16 [N, K] tensor")
+        self.register_buffer("weight", weight, persistent=False)
+        self.out_features, self.in_features = weight.shape
+        self.pdl = bool(pdl)
+        self.gemv_max_m = min(int(gemv_max_m), MAX_M)
+
+    def route(self, m: int) -> str:
+        if m == 0:
+            return "empty"
+        return "gemv" if m <= self.gemv_max_m else "cublas"
+
+    def forward(self, x: torch.Tensor) -> torch.Tensor:
+        x2 = x.reshape(-1, x.shape[-1])
+        route = self.route(x2.shape[0])
+        if route == "empty":
+            return x2.new_empty(*x.shape[:-1], self.out_features)
+        if route == "gemv":
+            out = fp4gemv.bf16_gemv(x2, self.weight, pdl=self.pdl)
+        else:
+            out = torch.nn.functional.linear(x2, self.weight)
+        return out.view(*x.shape[:-1], self.out_features)
+
+    def gate_up_silu_mul(self, x: torch.Tensor) -> torch.Tensor | None:
+        if x.dim() != 2 or self.out_features % 32 != 0 or self.route(x.shape[0]) != "gemv":
+            return None
+        return fp4gemv.bf16_gemv(x, self.weight, silu_mul=True, pdl=self.pdl)

@@ -319,3 +319,45 @@ def test_full_e4m3_range_gemv(fp4, M, silu):
     got = fp4.nvfp4_gemv(x.to(DEV), w.to(DEV), sf.to(DEV), torch.tensor([gs], device=DEV), silu_mul=silu)
     ref = oracle.nvfp4_gemv(u16(x), w.numpy(), sf.numpy(), gs, silu_mul=silu)
     assert_close(u16(got), ref, f"full E4M3 range M={M} silu={silu}")
+
+
+def test_decode_chain_real_dependencies(fp4):
+    # qkv -> o_proj (on the first H columns of qkv's output, a strided view)
+    # -> gate_up + silu_mul -> down -> next layer, two layers, every launch
+    # reading its predecessor's output: with PDL on, off after the o_proj
+    # stand-in for attention, and off everywhere the bits are the same, and
+    # each launch matches the oracle on its own (GPU-produced) input.
+    H, Q, I2 = 512, 768, 2048
+    M, gs_v = 4, 0.01
+    gs = torch.tensor([gs_v], device=DEV)
+    layers = []
+    for l in range(2):
+        mk = lambda N, K, s: (synth.fp4_bytes(N, K, seed=s), synth.e4m3_bytes(oracle.scale_bytes(N, K), seed=s + 1))  # noqa: E731
+        layers.append({"qkv": mk(Q, H, 10 * l + 1), "o": mk(H, H, 10 * l + 3), "gu": mk(I2, H, 10 * l + 5),
+                       "down": mk(H, I2 // 2, 10 * l + 7)})
+    dl = [{k: (w.to(DEV), s.to(DEV)) for k, (w, s) in L.items()} for L in layers]
+    x0 = synth.activations(M, H, seed=1).to(DEV)
+
+    def run(pdl_o, pdl_rest):
+        trace = []
+        x = x0
+        for L in dl:
+            q = fp4.nvfp4_gemv(x, *L["qkv"], gs, pdl=pdl_rest)
+            o = fp4.nvfp4_gemv(q[:, :H], *L["o"], gs, pdl=pdl_o)
+            g = fp4.nvfp4_gemv(o, *L["gu"], gs, silu_mul=True, pdl=pdl_rest)
+            x = fp4.nvfp4_gemv(g, *L["down"], gs, pdl=pdl_rest)
+            trace.append((x if not trace else trace[-1][-1], q, o, g, x))
+        torch.cuda.synchronize()
+        return trace
+
+    a, b, c = run(True, True), run(False, True), run(False, False)
+    for ta, tb, tc in zip(a, b, c):
+        for u, v, w in zip(ta[1:], tb[1:], tc[1:]):
+            assert torch.equal(u, v) and torch.equal(u, w)
+    xin = x0
+    for L, (_, q, o, g, x) in zip(layers, a):
+        for inp, out, (w, s), silu in ((xin, q, L["qkv"], False), (q[:, :H], o, L["o"], False),
+                                       (o, g, L["gu"], True), (g, x, L["down"], False)):
+            ref = oracle.nvfp4_gemv(u16(inp), w.numpy(), s.numpy(), gs_v, silu_mul=silu)
+            assert_close(u16(out), ref, "decode chain")
+        xin = x
