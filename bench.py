@@ -318,7 +318,7 @@ def run_gpu(args):
     del graphs
 
     # ---- each kernel alone: the step's calls of one kernel, same rotation ----
-    # (register-fed kernel: the 16 calls with M <= 16; tcgen05 kernel: M = 32)
+    # (register-fed kernels: the 20 calls with M <= 16; tcgen05 kernel: M = 32)
     kernels = {}
     for kname, keep in (("gemv_rf_kernel", lambda M: M <= 16), ("gemv_kernel", lambda M: M > 16)):
         gk = [capture_graph(step_with(ph, keep=keep), dev) for ph in range(PHASES)]
@@ -469,9 +469,10 @@ def run_gpu(args):
                        "launch": f"one CUDA graph per rotation phase ({PHASES}), PDL edges between the launches"},
             "roofline": {"bound": "hbm", "achieved": dom["GB/s"], "peak": peak, "unit": "GB/s",
                          "frac": round(dom["GB/s"] / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs (burst copy)",
-                         "traffic": traffic_from_profile(), "kernel": "fp4::gemv_rf_kernel (M <= 16 calls)",
+                         "traffic": traffic_from_profile(),
+                         "kernel": "fp4::gemv_rf_kernel / fp4::gemv_slab_kernel (the register-fed kernels: M <= 16)",
                          "bytes_per_launch": dom["bytes_per_launch"], "us_per_launch": dom["us_per_launch"],
-                         "timing": "CUDA events around graph replays of the step's 16 M <= 16 calls, same rotation"},
+                         "timing": "CUDA events around graph replays of the step's 20 M <= 16 calls, same rotation"},
             "kernels": kernels,
             "step_frac": round(value / world / peak, 4),
             "per_call": per_call,
@@ -731,13 +732,24 @@ def decode_chain(dev, gs, peak, Ms=(1, 4, 8)):
 
 def run_profile_case(spec):
     """A few launches of one case, for ncu captures: LAYER:M[:bf16] with
-    LAYER in qkv, o_proj, gate_up, down; moe:M; dequantize_rows:N (N x N)."""
+    LAYER in qkv, o_proj, gate_up, down; moe:M; dequantize_rows:N (N x N);
+    sweep_gemm:M (dequantize + GEMM, N = K = 8192)."""
     from moe_nvfp4_gemv_gb300 import fp4gemv
     dev = torch.device("cuda", 0)
     parts = spec.split(":")
     M = int(parts[1])
     gs = torch.tensor([GS], dtype=torch.float32, device=dev)
-    if parts[0] == "dequantize_rows":
+    if parts[0] == "sweep_gemm":
+        # the dequantize + GEMM path on N = K = 8192 (dequantize_rows, then the
+        # tcgen05 GEMM on the bf16 weight)
+        N = K = synth.SWEEP_NK
+        w = synth.fp4_bytes(N, K, seed=1, device=dev)
+        sf = synth.e4m3_bytes(fp4gemv.scale_bytes(N, K), seed=2, device=dev)
+        x = synth.activations(M, K, seed=M, device=dev)
+        wb = torch.empty(N, K, dtype=torch.bfloat16, device=dev)
+        for _ in range(4):
+            fp4gemv.dequant_gemm(x, w, sf, gs, w_bf16=wb)
+    elif parts[0] == "dequantize_rows":
         N = M
         w = synth.fp4_bytes(N, N, seed=1, device=dev)
         sf = synth.e4m3_bytes(fp4gemv.scale_bytes(N, N), seed=2, device=dev)

@@ -36,7 +36,13 @@ MAX_M = fp4gemv.MAX_M
 # First token count routed to dequantize + GEMM (the GEMV is faster up to MAX_M).
 DEQUANT_MIN_M = MAX_M + 1
 # Largest token count the BF16 GEMV takes by default (cuBLAS beyond).
-BF16_GEMV_MAX_M = MAX_M
+# Measured on GB300 against torch.matmul (L2-cold, CUDA-graph replay), us at
+# M = 1 / 8 / 32 / 128: o_proj 4096x4096 GEMV 7.6 / 7.6 / 9.1 / 20.0 vs cuBLAS
+# 8.6 / 8.7 / 9.1 / 8.2; down 4096x14336 18.9 / 19.8 / 20.9 / 31.7 vs
+# 21.4 / 21.2 / 22.1 / 25.1; gate_up 28672x4096 35.3 / 37.2 / 42.1 / 58.9 vs
+# 36.1 / 35.9 / 36.5 / 41.6; qkv 6144x4096 11.0 / 11.3 / 13.2 / 25.6 vs
+# 9.7 / 9.6 / 9.7 / 10.0.  The GEMV wins mostly up to 8 tokens.
+BF16_GEMV_MAX_M = 8
 
 
 def gemv_tile(m: int) -> int | None:

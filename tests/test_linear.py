@@ -99,7 +99,7 @@ def test_gate_up_silu_mul(M):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("M", [1, 64, 200])
+@pytest.mark.parametrize("M", [1, 8, 64, 200])
 def test_bf16_linear(M):
     if not torch.cuda.is_available():
         pytest.fail("GPU test run without a CUDA device")
