@@ -37,6 +37,13 @@
  *   - Alignment: bf16 tensors and row strides 16-byte aligned, uint8 weights
  *     16-byte aligned, scale buffers 4-byte aligned (16-byte for the dense
  *     GEMV), fp32 scalars 4-byte aligned.
+ *   - Lifetime: the first call on a device looks up the addresses of the
+ *     library's own device-side state (the error word and wait limit, the
+ *     scratch of fp4gemv_moe_down_combine_noalloc) and keeps them per device
+ *     ordinal for the life of the process; encoded tensor maps are cached
+ *     per host thread and buffer.  Do not call the library after
+ *     cudaDeviceReset() on a device it has used: the new context would make
+ *     those addresses stale.
  */
 #ifndef FP4GEMV_H
 #define FP4GEMV_H
