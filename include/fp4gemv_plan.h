@@ -69,6 +69,36 @@ typedef struct {
 fp4gemv_status fp4gemv_plan_slab(int M, int N, int K, int silu_mul, int sms, const int* regs, fp4gemv_slab_plan* out);
 
 typedef struct {
+  int split;          /* CTAs per cluster along H (1, 2, 4 or 8) */
+  int k_slab;         /* H elements per cluster rank, a multiple of 64 */
+  int chunk_pairs;    /* most (token, expert) pairs one routed CTA computes */
+  int columns;        /* grid columns: M * topk routed pair columns + the shared expert's token chunks */
+  int tiles;          /* 128-row tiles per column: max(I / 64, ceil(SI / 64)) */
+  int slab_bytes;     /* shared memory holding a CTA's activations */
+  int stage_bytes;    /* one weight stage (codes of 128 rows x 256 K, two scale groups) */
+  size_t smem_bytes;  /* dynamic shared memory per CTA */
+} fp4gemv_moe_slab_plan;
+
+/* Plan of fp4gemv_moe_gate_up on the slab kernel (vllm.models.flint.ops.
+ * moe_gemv, gate_up: routed chunks of up to chunk_pairs pairs of one expert
+ * and the shared expert, the CTA's activations in shared memory, three
+ * CTAs per SM, H split over a cluster).  No GPU is needed.
+ *   M, topk, E, H, I, SI: as fp4gemv_moe_gate_up (same shape rules).
+ *   sms:  streaming multiprocessors of the GPU (152 on GB300).
+ *   regs: registers per thread of the kernel.
+ *   out:  HOST pointer, filled on success.
+ * It applies when the CTAs of every expert the call can touch (at most
+ * min(M * topk, E) routed chunks plus the shared expert's) fit on the GPU in
+ * one wave with a split that leaves each rank at least 256 of H (one token
+ * on the E = 128, top-8, H = 4096, I = SI = 1536 block: a split of two).
+ * Returns FP4GEMV_ERR_INVALID_ARG for a null out, sms < 1 or regs < 1;
+ * FP4GEMV_ERR_UNSUPPORTED_SHAPE for shapes fp4gemv_moe_gate_up rejects and
+ * for calls the slab kernel does not serve (they run on the register-fed
+ * kernel, chunks of 8 pairs, or beyond 64 tokens on the tcgen05 kernel). */
+fp4gemv_status fp4gemv_plan_moe_slab(int M, int topk, int E, int H, int I, int SI, int sms, int regs,
+                                     fp4gemv_moe_slab_plan* out);
+
+typedef struct {
   int tokens_tile;    /* MMA N of the tcgen05 kernel: 16, 32, 64 or 128 (covers M) */
   int ctas_per_sm;    /* 2, or 1 when the tile's tensor memory needs more than 256 columns */
   int tiles;          /* CTA tiles along N: 128 features, or 64 with silu_mul */

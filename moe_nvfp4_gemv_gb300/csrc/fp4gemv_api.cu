@@ -501,6 +501,53 @@ bool plan_slab(int M, int N, int K, bool silu, int sms, int inbox_bytes, const i
   return false;
 }
 
+// The slab kernel for MoE gate_up: 128-row tiles (a routed [up; gate] group
+// or a shared-expert pair of 64-row gate and up boxes), routed chunks of up
+// to fp4::kSlabChunk pairs, K split so that the CTAs of the experts a call
+// can touch (at most min(P, E) routed chunks of one expert each when no
+// expert gets more than kSlabChunk pairs, plus the shared expert's chunks)
+// run in one wave at three CTAs per SM; the CTA's activations (kSlabChunk
+// rows at most) and two weight stages must fit a third of the SM's shared
+// memory.  At one token of the E = 128, top-8, H = 4096, I = SI = 1536
+// block (8 experts + the shared one: 216 tiles) that is a split of two; the
+// register-fed kernel ran those 216 whole-K CTAs in one uneven wave.
+struct SlabMoePlan {
+  int S = 1, kslab = 0, slab_bytes = 0, stage_bytes = 0;
+  size_t smem = 0;
+};
+
+bool plan_slab_moe(int M, int topk, int E, int H, int I, int SI, int sms, int regs, SlabMoePlan* sp) {
+  const int cw = fp4::kSlabMaxCW, occ = kSlabOcc;
+  const int warp_regs = (regs * 32 + 255) / 256 * 256;
+  if (static_cast<long>(occ) * (cw + 1) * warp_regs > 65536 || sms < 1) return false;
+  const long P = static_cast<long>(M) * topk;
+  const long routed_cols = P < E ? P : E;
+  const long shared_cols = (M + fp4::kSlabChunk - 1) / fp4::kSlabChunk;
+  const long tiles = routed_cols * (I / 64) + shared_cols * ((SI + 63) / 64);
+  const int rows = static_cast<int>(P < fp4::kSlabChunk ? P : fp4::kSlabChunk);  // B rows of a chunk, at most
+  const int stage = 128 * 128 + 2 * 2048;  // codes + two scale groups (shared-expert gate and up boxes)
+  const int dyn = kSmemPerSm / occ - kSmemPerCta;
+  for (int S = 8; S >= 1; S /= 2) {
+    if (tiles * S > static_cast<long>(occ) * sms) continue;  // more than one wave
+    const int kslab = ((H + S - 1) / S + 63) / 64 * 64;
+    if (S > 1 && (kslab < 256 || static_cast<long>(S - 1) * kslab >= H)) continue;
+    const int nst = (kslab + 255) / 256;
+    if (nst > fp4::kSlabMaxStages) return false;
+    const int slab = (rows * nst * 512 + 1023) / 1024 * 1024;
+    const size_t smem = 1024 + static_cast<size_t>(slab) + 2 * static_cast<size_t>(stage) + fp4::SlabInboxBytes;
+    if (smem > static_cast<size_t>(dyn)) return false;  // a smaller split only needs more
+    sp->S = (H + kslab - 1) / kslab;
+    sp->kslab = kslab;
+    sp->slab_bytes = slab;
+    sp->stage_bytes = stage;
+    sp->smem = smem;
+    return true;
+  }
+  return false;
+}
+
+std::atomic<int> g_slab_moe_regs[kMaxDevices];
+
 // Registers per thread of both slab-kernel variants (queried once per device).
 std::atomic<int> g_slab_regs[kMaxDevices][2];
 
@@ -699,6 +746,25 @@ fp4gemv_status fp4gemv_plan_slab(int M, int N, int K, int silu_mul, int sms, con
   return FP4GEMV_OK;
 }
 
+fp4gemv_status fp4gemv_plan_moe_slab(int M, int topk, int E, int H, int I, int SI, int sms, int regs,
+                                     fp4gemv_moe_slab_plan* out) {
+  if (!out || sms < 1 || regs < 1 || M < 1 || topk < 1 || E < 1 || H < 1 || I < 1 || SI < 1)
+    return FP4GEMV_ERR_INVALID_ARG;
+  if (static_cast<long>(M) * topk > 1024 || H % 64 != 0 || H < 256 || I % 64 != 0 || SI % 64 != 0)
+    return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
+  SlabMoePlan sp;
+  if (!plan_slab_moe(M, topk, E, H, I, SI, sms, regs, &sp)) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
+  out->split = sp.S;
+  out->k_slab = sp.kslab;
+  out->chunk_pairs = fp4::kSlabChunk;
+  out->columns = M * topk + (M + fp4::kSlabChunk - 1) / fp4::kSlabChunk;
+  out->tiles = I / 64 > (SI + 63) / 64 ? I / 64 : (SI + 63) / 64;
+  out->slab_bytes = sp.slab_bytes;
+  out->stage_bytes = sp.stage_bytes;
+  out->smem_bytes = sp.smem;
+  return FP4GEMV_OK;
+}
+
 fp4gemv_status fp4gemv_plan_tc(int M, int N, int K, int silu_mul, int bf16_weights, int sms, fp4gemv_tc_plan* out) {
   if (!out || sms < 1 || (silu_mul != 0 && silu_mul != 1) || (bf16_weights != 0 && bf16_weights != 1) || M < 1 ||
       N < 1 || K < 1)
@@ -800,11 +866,76 @@ fp4gemv_status fp4gemv_moe_gate_up(const void* x, const int32_t* ids, int M, int
   int sms = 0;
   fp4gemv_status st = device_state(&err, &sms);
   if (st != FP4GEMV_OK) return st;
-  // Register-fed kernel for up to 64 tokens: expert chunks hold at most 8
-  // pairs (more pairs routed to one expert form further chunks; with 8 of
-  // 128 experts per token an expert gets ~P / E pairs, a handful, so most
-  // chunks take the f16 route) and the shared expert runs ceil(M / 8)
-  // chunks; the tcgen05 kernel beyond.
+  // The slab kernel when its plan fits one wave (plan_slab_moe: one token
+  // on the E = 128, H = 4096 block); else the register-fed kernel for up to 64
+  // tokens: expert chunks hold at most 8 pairs (more pairs routed to one
+  // expert form further chunks; with 8 of 128 experts per token an expert
+  // gets ~P / E pairs, a handful, so most chunks take the f16 route) and the
+  // shared expert runs ceil(M / 8) chunks; the tcgen05 kernel beyond.
+  {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FP4GEMV_ERR_CUDA;
+    int regs = g_slab_moe_regs[dev].load(std::memory_order_acquire);
+    if (regs == 0) {
+      if (fp4::slab_moe_regs(&regs) != cudaSuccess || regs <= 0) return FP4GEMV_ERR_CUDA;
+      g_slab_moe_regs[dev].store(regs, std::memory_order_release);
+    }
+    SlabMoePlan sp;
+    if (plan_slab_moe(M, topk, E, H, I, SI, sms, regs, &sp)) {
+      GemvParams p;
+      std::memset(&p, 0, sizeof(p));
+      if (!encode_2d(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w1, H / 2, static_cast<uint64_t>(E) * 2 * I, H / 2, 128,
+                     128))
+        return FP4GEMV_ERR_CUDA;
+      if (!encode_2d(&p.tm_w2, CU_TENSOR_MAP_DATA_TYPE_UINT8, wsh, H / 2, 2 * static_cast<uint64_t>(SI), H / 2, 128,
+                     64))
+        return FP4GEMV_ERR_CUDA;
+      p.sf = w1_sf;
+      p.sf2 = ssh;
+      p.x = static_cast<const uint16_t*>(x);
+      p.x2 = p.x;
+      p.ldx = p.ldx2 = H;
+      p.gs = gssh;
+      p.alpha = alpha;
+      p.ids = ids;
+      p.out = static_cast<uint16_t*>(act);
+      p.ldo = I;
+      p.out2 = static_cast<uint16_t*>(sact);
+      p.ldo2 = SI;
+      p.M = M;
+      p.n_out = I;
+      p.n_half = SI;
+      p.K = H;
+      p.K2 = H;
+      p.k_split = sp.kslab;
+      p.E = E;
+      p.topk = topk;
+      p.P = M * topk;
+      p.rows_per_expert = 2 * I;
+      p.rows_w = 2 * SI;
+      p.shared_n_out = SI;
+      p.routed_tiles = I / 64;
+      p.shared_tiles = (SI + 63) / 64;
+      p.kbp = p.kbp2 = ((H / 16) + 3) / 4 * 4;
+      p.sf_expert_bytes = static_cast<uint32_t>(fp4gemv_scale_bytes(2 * I, H));
+      p.nstages = 2;
+      p.stage_bytes = sp.stage_bytes;
+      p.x_off = sp.slab_bytes;
+      p.cw = fp4::kSlabMaxCW;
+      p.slab_r = 2;
+      p.skip_stage = -1;
+      p.err = err;
+      LaunchCfg cfg{};
+      const int tiles = p.routed_tiles > p.shared_tiles ? p.routed_tiles : p.shared_tiles;
+      cfg.grid = dim3(tiles * sp.S, p.P + (M + fp4::kSlabChunk - 1) / fp4::kSlabChunk, 1);
+      cfg.cluster = sp.S;
+      cfg.smem = sp.smem;
+      cfg.pdl = pdl;
+      cfg.stream = stream;
+      g_launches.fetch_add(1, std::memory_order_relaxed);
+      return from_cuda(fp4::launch_slab_moe(p, cfg));
+    }
+  }
   const bool rf = M <= 64;
   const int kmode = rf ? kMoeGateUpRf : fp4::kMoeGateUp;
   const int NT = rf ? 8 : 32;

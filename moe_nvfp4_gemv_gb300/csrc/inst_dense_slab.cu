@@ -7,19 +7,8 @@ namespace fp4 {
 
 template <int kR>
 cudaError_t configure_slab(size_t smem, unsigned cluster) {
-  auto k = gemv_slab_kernel<kR>;
   static int configured_smem[64];  // per device (0 = not yet)
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (configured_smem[dev] < static_cast<int>(smem)) {
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    configured_smem[dev] = static_cast<int>(smem);
-  }
-  if (cluster > 8) return cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  return cudaSuccess;
+  return configure_kernel(gemv_slab_kernel<kR>, configured_smem, smem, cluster);
 }
 
 cudaError_t launch_slab(int r, const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info) {

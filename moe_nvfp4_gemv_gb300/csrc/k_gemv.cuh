@@ -71,6 +71,8 @@ constexpr int kMaxSlots = 6;
 constexpr int kMaxXSlots = 4;   // activation slots (NVFP4 modes; the host picks 2, 3 or 4)
 constexpr int kSliceK = 128;    // K per tensor-memory A slot (8 MMAs of K = 16 per commit)
 constexpr int kSlabMaxStages = 64;  // slab kernel: K per CTA <= 64 stages of 256
+constexpr int kSlabMaxCW = 4;       // slab kernel: consumer warps (tiles of 16 kSlabR cw rows: 64 or 128)
+constexpr int kSlabChunk = 4;       // slab kernel, MoE: pairs of one expert per CTA (B rows)
 constexpr int SlabInboxBytes = 8 * (128 + 16) * 4;  // slab kernel: split-K inbox (8 tokens x 144 rows, fp32)
 
 struct GemvParams {
@@ -124,7 +126,10 @@ struct GemvParams {
   uint32_t* err;       // device error word (the wait limit follows it, see common.cuh)
 };
 
-struct CtaWork {
+// kN: the most B rows a CTA holds (the token tile, or the slab kernel's
+// expert chunk).
+template <int kN>
+struct CtaWorkN {
   int active;      // 0: nothing to compute
   int shared;      // 1: shared-expert CTA (MoE)
   int paired;      // 1: two 64-row boxes (gate rows, up rows); 0: one 128-row box
@@ -138,10 +143,11 @@ struct CtaWork {
   int kbp;
   int expert;
   int out_base;    // first output feature of the tile
-  int tok[kMaxNT];   // B row -> activation row
-  int orow[kMaxNT];  // B row -> output row (pair / token)
-  long long xoff[kMaxNT];  // B row -> element offset of its activation row
+  int tok[kN];   // B row -> activation row
+  int orow[kN];  // B row -> output row (pair / token)
+  long long xoff[kN];  // B row -> element offset of its activation row
 };
+using CtaWork = CtaWorkN<kMaxNT>;
 
 __host__ __device__ constexpr int pow2_at_least(int v) {
   int p = 32;
@@ -239,8 +245,8 @@ __device__ __forceinline__ void set_box(Work& w, int b, int wrow, int srow, int 
 // the previous grid first: their expert ids come from the router.  A routed
 // CTA's chunk is found with warp-wide ballots over the ids, so resolving
 // costs O(P / 32) loads per lane however many pairs there are.
-template <int kMode, int kNT>
-__device__ void resolve_work(const GemvParams& p, CtaWork& w, uint32_t split, int lane) {
+template <int kMode, int kNT, typename Work = CtaWork>
+__device__ void resolve_work(const GemvParams& p, Work& w, uint32_t split, int lane) {
   const int tile = blockIdx.x / max(1u, cluster_nctarank());
   if (lane == 0) {
     w.active = 1;

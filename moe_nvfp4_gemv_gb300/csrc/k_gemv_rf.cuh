@@ -148,7 +148,8 @@ __device__ __forceinline__ void rf_box(RfWork& w, int b, int row, int h, int gro
   w.sgroup[2 * b + 1] = (g1 != g0 && g1 < groups_total) ? g1 : -1;
 }
 
-__device__ __forceinline__ void copy_work(const CtaWork& m, RfWork& w) {
+template <typename Work>
+__device__ __forceinline__ void copy_work(const Work& m, RfWork& w) {
   w.paired = m.paired;
   w.shared = m.shared;
   w.expert = m.expert;

@@ -36,9 +36,9 @@ namespace fp4 {
 
 constexpr int kSlabNT = 8;            // MMA N: tokens 0 .. 7
 constexpr int kSlabR = 2;             // 16-row blocks per consumer warp
-constexpr int kSlabMaxCW = 4;         // consumer warps (tiles of 16 kSlabR cw rows: 64 or 128)
 constexpr int kSlabThreads = kSlabMaxCW * 32 + 32;
 constexpr int kSlabMinBlocks = 3;     // CTAs per SM the registers are budgeted for
+using SlabWork = CtaWorkN<kSlabChunk>;
 
 template <int kR>
 struct SlabCfg {
@@ -59,10 +59,16 @@ __device__ __forceinline__ bool bf16x8_to_f16x8_exact(const uint4& v, uint4& o) 
   return e;
 }
 
-template <int kR>
+// kMode: kDenseFp4 (nvfp4_gemv) or kMoeGateUp (the gate_up launch of
+// vllm.models.flint.ops.moe_gemv: routed chunks of up to kSlabChunk pairs of
+// one expert, and the shared expert's token chunks, with the epilogues of
+// the register-fed kernel).
+template <int kR, int kMode = kDenseFp4>
 __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel(const __grid_constant__ GemvParams p) {
   using C = SlabCfg<kR>;
   constexpr int kChains = C::kChains;
+  constexpr bool kDense = kMode == kDenseFp4;
+  static_assert(kDense || kMode == kMoeGateUp, "slab kernel modes");
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -74,6 +80,7 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
   __shared__ __align__(8) uint64_t bar_inbox;
   __shared__ volatile int s_abort;
   __shared__ int s_xbad[kSlabMaxStages];  // 1: the stage's activations are not all exact in f16
+  __shared__ SlabWork s_mwork;            // MoE: the CTA's work, resolved by the producer warp
 
   const int tid = threadIdx.x;
   const int warp = tid / 32;
@@ -83,14 +90,21 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
   const uint32_t S = cluster_nctarank();
   const uint32_t rank = S > 1 ? cluster_ctarank() : 0;
   const int nstages = p.nstages;
-  const int M = p.M;
   const int trows = 16 * kR * cw;
 
-  // ---- what this CTA computes (every thread derives it) ----
+  // ---- what this CTA computes (dense: every thread derives it; MoE: the
+  // producer warp resolves it -- routed CTAs after the router's ids are
+  // complete -- and every thread copies it) ----
   RfWork wk;
   wk.shared = 0;
   wk.expert = -1;
-  {
+  if constexpr (!kDense) {
+    if (warp == cw) resolve_work<kMode, kSlabChunk, SlabWork>(p, s_mwork, 0, lane);
+    __syncthreads();
+    copy_work(s_mwork, wk);
+    wk.k_begin = static_cast<int>(rank) * p.k_split;  // routed and shared K are both H
+    wk.k_end = min(p.K, wk.k_begin + p.k_split);
+  } else {
     const int tile = blockIdx.x / max(1u, S);
     wk.k_begin = static_cast<int>(rank) * p.k_split;
     wk.k_end = min(p.K, wk.k_begin + p.k_split);
@@ -109,8 +123,11 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
       rf_box(wk, 0, wk.out_base, trows, groups_total);
     }
   }
+  // B rows: tokens (dense) or the pairs of the expert chunk / the shared
+  // expert's tokens (MoE; 0 for an inactive CTA, which streams nothing)
+  const int M = kDense ? p.M : (s_mwork.active ? s_mwork.ntok : 0);
   const int klen = wk.k_end - wk.k_begin;
-  const int nst = (klen + 255) / 256;
+  const int nst = M > 0 ? (klen + 255) / 256 : 0;
   const uint32_t slab_stage = static_cast<uint32_t>(M) * 512u;  // bytes of one stage's activations
   const uint64_t pol_w = policy_evict_first();
   auto issue_weights = [&](int s, int slot) {
@@ -118,29 +135,34 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
     const uint32_t fb = smem_u32(&bar_full[slot]);
     const int k0 = wk.k_begin + s * 256;
     const int nchunks = min(256, wk.k_end - k0) / kSubK;
+    const CUtensorMap* tmw = wk.shared ? &p.tm_w2 : &p.tm_w;
+    const uint8_t* sfb =
+        wk.shared ? p.sf2 : p.sf + (wk.expert >= 0 ? static_cast<size_t>(wk.expert) * p.sf_expert_bytes : 0);
     uint32_t bytes = trows * 128;
 #pragma unroll
     for (int g = 0; g < 4; ++g) bytes += (wk.sgroup[g] >= 0 ? nchunks * 512 : 0);
     mbar_arrive_expect_tx(fb, bytes);
-    tma_load_2d(st, &p.tm_w, k0 / 2, wk.wrow[0], fb, pol_w);
-    if (wk.paired) tma_load_2d(st + trows * 64, &p.tm_w, k0 / 2, wk.wrow[1], fb, pol_w);
+    tma_load_2d(st, tmw, k0 / 2, wk.wrow[0], fb, pol_w);
+    if (wk.paired) tma_load_2d(st + trows * 64, tmw, k0 / 2, wk.wrow[1], fb, pol_w);
     uint32_t sdst = st + trows * 128;  // the valid groups, in order
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
       if (wk.sgroup[g] < 0) continue;
       const size_t chunk = static_cast<size_t>(wk.sgroup[g]) * (wk.kbp / 4) + k0 / 64;
-      bulk_load(sdst, p.sf + chunk * 512, nchunks * 512, fb, pol_w);
+      bulk_load(sdst, sfb + chunk * 512, nchunks * 512, fb, pol_w);
       sdst += 2048;
     }
   };
   // Output rows are reduced across cluster ranks per feature unit: paired
-  // tiles combine rows o and o + trows / 2 (two rows per feature).
-  const int unit = wk.paired ? trows / 2 : trows;
+  // tiles and routed [up; gate] groups combine rows o and o + trows / 2 (two
+  // rows per feature).
+  const int unit = (wk.paired || !kDense) ? trows / 2 : trows;
   const int rpf = trows / unit;
 
   // ------------------------------------------------------------------ prologue
   if (warp == cw && lane == 0) {
     prefetch_tensormap(&p.tm_w);
+    if constexpr (!kDense) prefetch_tensormap(&p.tm_w2);
     s_abort = 0;
     for (int i = 0; i < nstages; ++i) {
       mbar_init(smem_u32(&bar_full[i]), 1);
@@ -214,7 +236,11 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
     for (int q = tid; q < M * nslot; q += ncons) {
       const int n = q / nslot, kq = q % nslot;
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (kq < nchk) v = __ldg(reinterpret_cast<const uint4*>(p.x + static_cast<int64_t>(n) * p.ldx + wk.k_begin + 8 * kq));
+      if (kq < nchk) {
+        const uint16_t* xr = kDense ? p.x + static_cast<int64_t>(n) * p.ldx
+                                    : (wk.shared ? p.x2 : p.x) + s_mwork.xoff[n];
+        v = __ldg(reinterpret_cast<const uint4*>(xr + wk.k_begin + 8 * kq));
+      }
       const int s = kq / 32, u = (kq % 32) / 8, ch = kq % 8;
       const uint32_t a = slab + s * slab_stage + (u * M + n) * 128 + ((ch ^ (n & 7)) * 16);
       sts128(a, v);
@@ -402,7 +428,31 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
       return a;
     };
     const int nf = f_hi - f_lo;
-    if (!s_abort && nf > 0) {
+    if (!s_abort && nf > 0 && !kDense) {
+      if (!wk.shared) {
+        // routed [up; gate] group: feature o = up row o, gate row o + 64
+        const float al = __ldg(p.alpha + wk.expert);
+        for (int it = tid; it < nf * M; it += ncons) {
+          const int n = it / nf, lr = it % nf;
+          const int feat = wk.out_base + f_lo + lr;
+          if (feat >= p.n_out) continue;
+          const float uu = partial(n, lr) * al;
+          const float gt = partial(n, lr + nf) * al;
+          p.out[static_cast<int64_t>(s_mwork.orow[n]) * p.ldo + feat] = f32_to_bf16_rn(silu_fast(gt) * uu);
+        }
+      } else {
+        // shared expert, paired tiles: feature o = gate row o, up row o + 64
+        const float gs = __ldg(p.gs);
+        for (int it = tid; it < nf * M; it += ncons) {
+          const int n = it / nf, lr = it % nf;
+          const int feat = wk.out_base + f_lo + lr;
+          if (feat >= p.shared_n_out) continue;
+          const float G = bf16_to_f32(f32_to_bf16_rn(partial(n, lr) * gs));
+          const float U = bf16_to_f32(f32_to_bf16_rn(partial(n, lr + nf) * gs));
+          p.out2[static_cast<int64_t>(s_mwork.orow[n]) * p.ldo2 + feat] = f32_to_bf16_rn(silu_exact(G) * U);
+        }
+      }
+    } else if (!s_abort && nf > 0) {
       const float gs = __ldg(p.gs);
       if (rpf == 1) {
         for (int it = tid; it < nf * M; it += ncons) {

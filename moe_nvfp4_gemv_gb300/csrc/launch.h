@@ -43,6 +43,9 @@ cudaError_t rf_max_clusters(int mode, int nt, unsigned cluster, size_t smem, int
 // Slab kernel (k_gemv_slab.cuh): dense NVFP4, 1 .. 8 tokens, r = 16-row
 // blocks per consumer warp (1 or 2); the block is (p.cw + 1) warps.
 cudaError_t launch_slab(int r, const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info);
+// The slab kernel's MoE gate_up mode (r = 2, four consumer warps).
+cudaError_t launch_slab_moe(const GemvParams& p, const LaunchCfg& cfg);
+cudaError_t slab_moe_regs(int* regs);
 // Clusters of `cluster` slab-kernel CTAs (cw consumer warps, `smem` bytes of
 // dynamic shared memory) that fit on the GPU at once.
 cudaError_t slab_max_clusters(int r, int cw, unsigned cluster, size_t smem, int* n);
@@ -53,6 +56,24 @@ cudaError_t launch_moe(int mode, int nt, const GemvParams& p, const LaunchCfg& c
 // kbp: 16-wide K blocks per 128-row scale group in sf (0: roundup(K / 16, 4)).
 cudaError_t launch_dequantize_rows(const uint8_t* w, const uint8_t* sf, void* out, int rows, int K, int kbp,
                                    cudaStream_t stream);
+
+// Raises a kernel's dynamic shared-memory limit to `smem` (once per device
+// and size; `configured` holds the size set per device) and allows
+// clusters of more than 8 CTAs when asked for.
+template <typename Kernel>
+cudaError_t configure_kernel(Kernel k, int (&configured)[64], size_t smem, unsigned cluster) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (configured[dev] < static_cast<int>(smem)) {
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    configured[dev] = static_cast<int>(smem);
+  }
+  if (cluster > 8) return cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return cudaSuccess;
+}
 
 // Shared launch helper for the kernel translation units.
 template <typename Kernel>

@@ -239,3 +239,69 @@ def test_workspace_reuse_across_shapes(fp4):
                              g["ssd"], g["gssd"], out, workspace=ws)
         ref, _ = ref_down(d)
         assert_close(u16(out), ref, f"workspace reuse M={M}")
+
+
+def _moe_slab_split(fp4, M, topk, E, H, I, SI):
+    """Split of the slab kernel's plan for this gate_up call on this GPU
+    (None: the call runs on the register-fed kernel)."""
+    import ctypes
+
+    class Plan(ctypes.Structure):
+        _fields_ = [(n, ctypes.c_int) for n in ("split", "k_slab", "chunk_pairs", "columns", "tiles", "slab_bytes",
+                                                "stage_bytes")] + [("smem_bytes", ctypes.c_size_t)]
+    f = fp4.lib().fp4gemv_plan_moe_slab
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_int] * 8 + [ctypes.POINTER(Plan)]
+    out = Plan()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return out.split if f(M, topk, E, H, I, SI, sms, 125, ctypes.byref(out)) == 0 else None
+
+
+# gate_up on the slab kernel (routed chunks of up to 4 pairs of one expert,
+# H split over clusters of 1, 2, 4 and 8 CTAs): both outputs element by
+# element against the oracle.
+@pytest.mark.parametrize("M,topk,E,H,split", [(1, 2, 8, 256, 1), (1, 4, 8, 512, 2), (2, 2, 8, 1024, 4),
+                                              (3, 2, 8, 2048, 8), (1, 8, 16, 4096, 8)])
+def test_gate_up_slab_splits(fp4, M, topk, E, H, split):
+    I, SI = 192, 320
+    assert _moe_slab_split(fp4, M, topk, E, H, I, SI) == split
+    d = make_moe(M, E=E, H=H, I=I, SI=SI, topk=topk, seed=600 + H + M)
+    act, sact = run_gate_up(fp4, d)
+    (an, al, ah), (sn, sl, sh), bad = ref_gate_up(d)
+    assert bad == 0
+    assert_close(u16(act), (an, al, ah), f"act slab M={M} H={H}")
+    assert_close(u16(sact), (sn, sl, sh), f"sact slab M={M} H={H}")
+    assert fp4.get_device_error() == 0
+
+
+# Repeated experts on the slab kernel: 8 pairs of one expert (two full
+# chunks), and a token that sends 5 of its 8 slots to one expert (a full
+# chunk and a ragged one) and 3 to another.
+@pytest.mark.parametrize("M,topk,ids", [(2, 4, [[2, 2, 2, 2], [2, 2, 2, 2]]),
+                                        (1, 8, [[5, 1, 5, 1, 1, 5, 1, 1]])])
+def test_gate_up_slab_repeated_experts(fp4, M, topk, ids):
+    E, H, I, SI = 8, 1024, 256, 256
+    assert _moe_slab_split(fp4, M, topk, E, H, I, SI) is not None
+    d = make_moe(M, E=E, H=H, I=I, SI=SI, topk=topk, seed=31, ids=torch.tensor(ids, dtype=torch.int32))
+    act, sact = run_gate_up(fp4, d)
+    (an, al, ah), (sn, sl, sh), _ = ref_gate_up(d)
+    assert_close(u16(act), (an, al, ah), "act slab repeated")
+    assert_close(u16(sact), (sn, sl, sh), "sact slab repeated")
+    assert fp4.get_device_error() == 0
+
+
+def test_gate_up_slab_decode_block(fp4):
+    # one token of the E = 128, top-8, H = 4096, I = SI = 1536 block takes the
+    # slab kernel with a split of two; every output against the oracle, and
+    # two calls in a row agree bit for bit
+    c = synth.MOE
+    assert _moe_slab_split(fp4, 1, c["topk"], c["E"], c["H"], c["I"], c["SI"]) == 2
+    d = make_moe(1, c["E"], c["H"], c["I"], c["SI"], c["topk"], seed=7)
+    act, sact = run_gate_up(fp4, d)
+    act2, sact2 = run_gate_up(fp4, d)
+    assert torch.equal(act, act2) and torch.equal(sact, sact2)
+    (an, al, ah), (sn, sl, sh), bad = ref_gate_up(d)
+    assert bad == 0
+    assert_close(u16(act), (an, al, ah), "act decode block M=1")
+    assert_close(u16(sact), (sn, sl, sh), "sact decode block M=1")
+    assert fp4.get_device_error() == 0

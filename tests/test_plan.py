@@ -282,3 +282,82 @@ def test_slab_plan_rejects_bad_arguments(slab_fn):
     assert slab_fn(0, 4096, 4096, 0)[0] == 1
     assert slab_fn(1, 4096, 4096, 2)[0] == 1
     assert slab_fn(1, 4096, 4096, 0, sms=0)[0] == 1
+
+
+# --- the slab kernel's MoE gate_up plan, host only ----------------------------------------
+
+class MoeSlabPlan(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("split", "k_slab", "chunk_pairs", "columns", "tiles", "slab_bytes",
+                                            "stage_bytes")] + [("smem_bytes", ctypes.c_size_t)]
+
+
+@pytest.fixture(scope="module")
+def moe_slab_fn():
+    from moe_nvfp4_gemv_gb300 import fp4gemv
+    f = fp4gemv.lib().fp4gemv_plan_moe_slab
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_int] * 8 + [ctypes.POINTER(MoeSlabPlan)]
+
+    def plan(M, topk, E, H, I, SI, regs=125, sms=SMS):
+        out = MoeSlabPlan()
+        return f(M, topk, E, H, I, SI, sms, regs, ctypes.byref(out)), out
+    return plan
+
+
+def moe_slab_rule(M, topk, E, H, I, SI, sms=SMS):
+    """The rule written out: chunks of <= 4 pairs; the routed columns that
+    can be active (min(P, E)) and the shared expert's ceil(M / 4) chunks, in
+    128-row tiles, fit one wave at three CTAs per SM with the largest split
+    whose ranks keep >= 256 of H; a CTA's slab (min(P, 4) rows of its H range,
+    bf16) and two 20 KB stages fit a third of 228 KB."""
+    P = M * topk
+    tiles = min(P, E) * (I // 64) + -(-M // 4) * -(-SI // 64)
+    rows = min(P, 4)
+    dyn = 228 * 1024 // 3 - 2048
+    for S in (8, 4, 2, 1):
+        if tiles * S > 3 * sms:
+            continue
+        kslab = -(-(-(-H // S)) // 64) * 64
+        if S > 1 and (kslab < 256 or (S - 1) * kslab >= H):
+            continue
+        slab = -(-(rows * -(-kslab // 256) * 512) // 1024) * 1024
+        smem = 1024 + slab + 2 * 20480 + 8 * 144 * 4
+        if smem > dyn:
+            return None
+        return dict(split=-(-H // kslab), k_slab=kslab, slab_bytes=slab, smem_bytes=smem)
+    return None
+
+
+@pytest.mark.parametrize("M,topk,E,H,I,SI", [(1, 8, 128, 4096, 1536, 1536), (2, 8, 128, 4096, 1536, 1536),
+                                             (8, 8, 128, 4096, 1536, 1536), (1, 2, 8, 512, 256, 384),
+                                             (3, 2, 8, 1024, 256, 384), (2, 4, 4, 2048, 256, 256),
+                                             (1, 1, 2, 256, 64, 64), (4, 8, 16, 8192, 512, 512)])
+def test_moe_slab_plan_matches_rule(moe_slab_fn, M, topk, E, H, I, SI):
+    st, p = moe_slab_fn(M, topk, E, H, I, SI)
+    want = moe_slab_rule(M, topk, E, H, I, SI)
+    if want is None:
+        assert st == 2
+        return
+    assert st == 0
+    got = dict(split=p.split, k_slab=p.k_slab, slab_bytes=p.slab_bytes, smem_bytes=p.smem_bytes)
+    assert got == want
+    assert (p.chunk_pairs, p.stage_bytes) == (4, 20480)
+    assert p.columns == M * topk + -(-M // 4) and p.tiles == max(I // 64, -(-SI // 64))
+    assert (p.split - 1) * p.k_slab < H and p.slab_bytes >= min(M * topk, 4) * p.k_slab * 2
+
+
+def test_moe_slab_plan_decode_block(moe_slab_fn):
+    # one token of the E = 128, top-8, H = 4096, I = SI = 1536 block: 9 columns
+    # x 24 tiles split in two (432 CTAs, one wave at three per SM); two tokens
+    # (17 x 24 = 408 tiles) would need the whole H per CTA, whose slab does not fit
+    st, p = moe_slab_fn(1, 8, 128, 4096, 1536, 1536)
+    assert st == 0 and (p.split, p.k_slab, p.columns, p.tiles) == (2, 2048, 9, 24)
+    assert moe_slab_fn(2, 8, 128, 4096, 1536, 1536)[0] == 2
+
+
+def test_moe_slab_plan_rejects_bad_arguments(moe_slab_fn):
+    assert moe_slab_fn(0, 8, 128, 4096, 1536, 1536)[0] == 1
+    assert moe_slab_fn(1, 8, 128, 4096, 1536, 1536, regs=0)[0] == 1
+    assert moe_slab_fn(1, 8, 128, 4096, 1536, 1536, sms=0)[0] == 1
+    assert moe_slab_fn(1, 8, 128, 4000, 1536, 1536)[0] == 2   # H % 64
+    assert moe_slab_fn(200, 8, 128, 4096, 1536, 1536)[0] == 2  # M * topk > 1024
