@@ -99,6 +99,41 @@ fp4gemv_status fp4gemv_plan_moe_slab(int M, int topk, int E, int H, int I, int S
                                      fp4gemv_moe_slab_plan* out);
 
 typedef struct {
+  int tiles_per_cta;  /* most 128-row tiles of H one CTA streams in turn: ceil(tiles / groups) */
+  int groups;         /* grid columns along H; group g takes tiles [g tiles / groups, (g + 1) tiles / groups) */
+  int columns;        /* grid rows: M * topk routed pair columns + the shared expert's token chunks */
+  int chunk_pairs;    /* most (token, expert) pairs one routed CTA computes (1, 2, 4 or 8) */
+  int slab_bytes;     /* shared memory holding a CTA's activation rows (the whole K) */
+  int stage_bytes;    /* one weight stage (codes of 128 rows x 256 K, one scale group) */
+  int stages;         /* weight ring stages (2 .. 8) */
+  int ctas_per_sm;    /* CTAs per SM the ring is sized for (2 or 3) */
+  size_t smem_bytes;  /* dynamic shared memory per CTA */
+} fp4gemv_moe_down_slab_plan;
+
+/* Plan of fp4gemv_moe_down_combine on the slab kernel (vllm.models.flint.ops.
+ * moe_gemv, down_combine: chunks of up to 8 pairs of one expert, each CTA
+ * streaming T row tiles of its expert over its resident activation rows,
+ * writing each tile's y rows and arriving on the tile's counter; the CTA
+ * that arrives last combines the tile).  No GPU is needed.
+ *   M, topk, E, H, I, SI: as fp4gemv_moe_down_combine (same shape rules).
+ *   sms:  streaming multiprocessors of the GPU (152 on GB300).
+ *   regs: registers per thread of the kernel.
+ *   out:  HOST pointer, filled on success.
+ * Applies to M <= 64 and E <= 256 when the activation rows and two weight
+ * stages fit.  The sizes follow the expected routing, E (1 - (1 - topk /
+ * E)^M) distinct experts for distinct top-k picks (at most M * topk): the
+ * chunk is the power of two (<= 8) that holds an expert's expected pairs; T
+ * makes the expected CTAs (distinct experts + ceil(M / chunk) shared-expert
+ * chunks, times the tile groups) fill 80 % of three CTAs per SM; the ring takes as
+ * many stages as fit (at most 8), sized for two CTAs per SM when the
+ * expected CTAs fit two per SM, else three.
+ * Returns FP4GEMV_ERR_INVALID_ARG for a null out, sms < 1 or regs < 1;
+ * FP4GEMV_ERR_UNSUPPORTED_SHAPE for shapes fp4gemv_moe_down_combine rejects
+ * and for calls the slab kernel does not serve. */
+fp4gemv_status fp4gemv_plan_moe_down_slab(int M, int topk, int E, int H, int I, int SI, int sms, int regs,
+                                          fp4gemv_moe_down_slab_plan* out);
+
+typedef struct {
   int tokens_tile;    /* MMA N of the tcgen05 kernel: 16, 32, 64 or 128 (covers M) */
   int ctas_per_sm;    /* 2, or 1 when the tile's tensor memory needs more than 256 columns */
   int tiles;          /* CTA tiles along N: 128 features, or 64 with silu_mul */

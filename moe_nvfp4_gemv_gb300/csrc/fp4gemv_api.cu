@@ -6,6 +6,7 @@
 #include <cuda.h>
 
 #include <atomic>
+#include <cmath>
 #include <cstdint>
 #include <cstddef>
 #include <cstring>
@@ -548,6 +549,75 @@ bool plan_slab_moe(int M, int topk, int E, int H, int I, int SI, int sms, int re
 
 std::atomic<int> g_slab_moe_regs[kMaxDevices];
 
+// The slab kernel for down_combine: the whole K per CTA (its activation
+// rows resident), T row tiles per CTA streamed in turn over the same rows (one
+// CTA's fixed costs -- its activation load, the ramp of its ring -- serve T
+// tiles), one scale group per 128-row weight stage.  Sizes come from the
+// expected routing: E (1 - (1 - topk / E)^M) distinct experts for distinct
+// top-k picks (at most M * topk), P / distinct pairs per expert.
+//   chunk: pairs per CTA, the power of two (<= 8) that holds the expected
+//          pairs of an expert (an expert with more forms more chunks); it
+//          bounds the resident rows, and a smaller slab leaves room for a
+//          deeper ring.
+//   groups: the tiles split evenly into groups (T = ceil(tiles / groups)
+//          tiles at most per CTA) so that the expected CTAs (distinct
+//          experts + ceil(M / chunk) shared chunks, times the groups) fill
+//          80 % of three CTAs per SM.
+//   ring:  as many 18 KB stages as fit (at most 8) beside the slab, at two
+//          CTAs per SM when the expected CTAs fit two per SM, else three.
+// One token: chunk 1, T = 1, 288 CTAs of 6 stages with 5 in the ring; 8
+// tokens (~53 experts): chunk 2, 6 groups of 5 or 6 tiles.
+struct SlabDownPlan {
+  int T = 1, groups = 1, chunk = 8, slab_bytes = 0, stage_bytes = 0, nstages = 2, occ = 3;
+  size_t smem = 0;
+};
+
+constexpr int kSmemPerCtaDown = 4096;  // reservation + static shared memory (incl. the expert counts)
+
+bool plan_slab_down(int M, int topk, int E, int H, int I, int SI, int sms, int regs, SlabDownPlan* sp) {
+  const int cw = fp4::kSlabMaxCW;
+  const int warp_regs = (regs * 32 + 255) / 256 * 256;
+  if (3L * (cw + 1) * warp_regs > 65536 || sms < 1 || E > fp4::kSlabMaxExperts) return false;
+  const long P = static_cast<long>(M) * topk;
+  const double pick = topk < E ? static_cast<double>(topk) / E : 1.0;
+  double distinct = E * (1.0 - std::pow(1.0 - pick, M));
+  if (distinct > P) distinct = static_cast<double>(P);
+  if (distinct < 1.0) distinct = 1.0;
+  int chunk = 1;
+  while (chunk < fp4::kSlabNT && chunk < static_cast<double>(P) / distinct) chunk *= 2;
+  const int rows = static_cast<int>(P < chunk ? P : chunk);
+  const int kmax = I > SI ? I : SI;
+  const int nst = (kmax + 255) / 256;
+  if (nst > fp4::kSlabMaxStages) return false;
+  const int slab = (rows * nst * 512 + 1023) / 1024 * 1024;
+  const int stage = 128 * 128 + 2048;
+  const int tiles = (H + 127) / 128;
+  const double cols = distinct + (M + chunk - 1) / chunk;
+  // (80 % of the slots: the estimate misses experts with more than one
+  // chunk and routings with more distinct experts, and a CTA past one wave
+  // would double the call)
+  int groups = static_cast<int>(0.8 * 3 * sms / cols);
+  if (groups < 1) groups = 1;
+  if (groups > tiles) groups = tiles;
+  const int T = (tiles + groups - 1) / groups;  // (groups take floor or ceil of tiles / groups tiles)
+  const int occ = cols * groups <= 2.0 * sms ? 2 : 3;
+  const long room = static_cast<long>(kSmemPerSm / occ - kSmemPerCtaDown) - 1024 - slab;
+  int ns = static_cast<int>(room / stage);
+  if (ns > fp4::kMaxStages) ns = fp4::kMaxStages;
+  if (ns > T * ((I + 255) / 256)) ns = T * ((I + 255) / 256);  // (no deeper than a routed CTA's stream)
+  if (ns < 2) return false;
+  sp->T = T;
+  sp->groups = groups;
+  sp->chunk = chunk;
+  sp->slab_bytes = slab;
+  sp->stage_bytes = stage;
+  sp->nstages = ns;
+  sp->occ = occ;
+  sp->smem = 1024 + static_cast<size_t>(slab) + static_cast<size_t>(ns) * stage;
+  return true;
+}
+std::atomic<int> g_slab_down_regs[kMaxDevices];
+
 // Registers per thread of both slab-kernel variants (queried once per device).
 std::atomic<int> g_slab_regs[kMaxDevices][2];
 
@@ -765,6 +835,26 @@ fp4gemv_status fp4gemv_plan_moe_slab(int M, int topk, int E, int H, int I, int S
   return FP4GEMV_OK;
 }
 
+fp4gemv_status fp4gemv_plan_moe_down_slab(int M, int topk, int E, int H, int I, int SI, int sms, int regs,
+                                          fp4gemv_moe_down_slab_plan* out) {
+  if (!out || sms < 1 || regs < 1 || M < 1 || topk < 1 || E < 1 || H < 1 || I < 1 || SI < 1)
+    return FP4GEMV_ERR_INVALID_ARG;
+  if (static_cast<long>(M) * topk > 1024 || H % 64 != 0 || I % 64 != 0 || I < 256 || SI % 64 != 0 || SI < 256)
+    return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
+  SlabDownPlan sp;
+  if (M > 64 || !plan_slab_down(M, topk, E, H, I, SI, sms, regs, &sp)) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
+  out->tiles_per_cta = sp.T;
+  out->groups = sp.groups;
+  out->columns = M * topk + (M + sp.chunk - 1) / sp.chunk;
+  out->chunk_pairs = sp.chunk;
+  out->slab_bytes = sp.slab_bytes;
+  out->stage_bytes = sp.stage_bytes;
+  out->stages = sp.nstages;
+  out->ctas_per_sm = sp.occ;
+  out->smem_bytes = sp.smem;
+  return FP4GEMV_OK;
+}
+
 fp4gemv_status fp4gemv_plan_tc(int M, int N, int K, int silu_mul, int bf16_weights, int sms, fp4gemv_tc_plan* out) {
   if (!out || sms < 1 || (silu_mul != 0 && silu_mul != 1) || (bf16_weights != 0 && bf16_weights != 1) || M < 1 ||
       N < 1 || K < 1)
@@ -877,7 +967,7 @@ fp4gemv_status fp4gemv_moe_gate_up(const void* x, const int32_t* ids, int M, int
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FP4GEMV_ERR_CUDA;
     int regs = g_slab_moe_regs[dev].load(std::memory_order_acquire);
     if (regs == 0) {
-      if (fp4::slab_moe_regs(&regs) != cudaSuccess || regs <= 0) return FP4GEMV_ERR_CUDA;
+      if (fp4::slab_moe_regs(fp4::kMoeGateUp, &regs) != cudaSuccess || regs <= 0) return FP4GEMV_ERR_CUDA;
       g_slab_moe_regs[dev].store(regs, std::memory_order_release);
     }
     SlabMoePlan sp;
@@ -933,7 +1023,7 @@ fp4gemv_status fp4gemv_moe_gate_up(const void* x, const int32_t* ids, int M, int
       cfg.pdl = pdl;
       cfg.stream = stream;
       g_launches.fetch_add(1, std::memory_order_relaxed);
-      return from_cuda(fp4::launch_slab_moe(p, cfg));
+      return from_cuda(fp4::launch_slab_moe(fp4::kMoeGateUp, p, cfg));
     }
   }
   const bool rf = M <= 64;
@@ -1034,10 +1124,24 @@ fp4gemv_status fp4gemv_moe_down_combine(const void* act, const int32_t* ids, con
   int sms = 0;
   fp4gemv_status st = device_state(&err, &sms);
   if (st != FP4GEMV_OK) return st;
-  // Register-fed kernel for up to 64 tokens, chunks of at most 8 pairs (as
-  // gate_up); the tcgen05 kernel beyond.  From 8 tokens the grid holds many
-  // short CTAs (K = I is a few stages): the variant budgeted for three CTAs
-  // per SM (72 KB ring) hides more of their fixed costs.
+  // Up to 64 tokens the slab kernel when its plan fits (plan_slab_down);
+  // otherwise the register-fed kernel for up to 64 tokens, chunks of at most
+  // 8 pairs (as gate_up), the tcgen05 kernel beyond.  From 8 tokens the
+  // register-fed grid holds many short CTAs (K = I is a few stages): the
+  // variant budgeted for three CTAs per SM (72 KB ring) hides more of their
+  // fixed costs.
+  SlabDownPlan sdp;
+  bool slab = false;
+  if (M <= 64) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FP4GEMV_ERR_CUDA;
+    int regs = g_slab_down_regs[dev].load(std::memory_order_acquire);
+    if (regs == 0) {
+      if (fp4::slab_moe_regs(fp4::kMoeDown, &regs) != cudaSuccess || regs <= 0) return FP4GEMV_ERR_CUDA;
+      g_slab_down_regs[dev].store(regs, std::memory_order_release);
+    }
+    slab = plan_slab_down(M, topk, E, H, I, SI, sms, regs, &sdp);
+  }
   const bool rf = M <= 64;
   const bool occ3 = rf && M >= 8;
   const int kmode = rf ? (occ3 ? kMoeDownRf3 : kMoeDownRf) : fp4::kMoeDown;
@@ -1106,6 +1210,24 @@ fp4gemv_status fp4gemv_moe_down_combine(const void* act, const int32_t* ids, con
   p.x_off = x_off;
   p.skip_stage = -1;
   p.err = err;
+  if (slab) {
+    p.nstages = sdp.nstages;
+    p.stage_bytes = sdp.stage_bytes;
+    p.x_off = sdp.slab_bytes;
+    p.cw = fp4::kSlabMaxCW;
+    p.slab_r = 2;
+    p.tiles_per_cta = sdp.T;
+    p.chunk = sdp.chunk;
+    p.routed_tiles = p.shared_tiles = sdp.groups;  // (a CTA's first tile is blockIdx.x * T)
+    LaunchCfg cfg{};
+    cfg.grid = dim3(sdp.groups, p.P + (M + sdp.chunk - 1) / sdp.chunk, 1);
+    cfg.cluster = 1;
+    cfg.smem = sdp.smem;
+    cfg.pdl = pdl;
+    cfg.stream = stream;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return from_cuda(fp4::launch_slab_moe(fp4::kMoeDown, p, cfg));
+  }
   const int shared_cols = (M + NT - 1) / NT;
   LaunchCfg cfg{};
   cfg.grid = dim3(p.routed_tiles, p.P + shared_cols, 1);

@@ -73,6 +73,8 @@ constexpr int kSliceK = 128;    // K per tensor-memory A slot (8 MMAs of K = 16 
 constexpr int kSlabMaxStages = 64;  // slab kernel: K per CTA <= 64 stages of 256
 constexpr int kSlabMaxCW = 4;       // slab kernel: consumer warps (tiles of 16 kSlabR cw rows: 64 or 128)
 constexpr int kSlabChunk = 4;       // slab kernel, MoE: pairs of one expert per CTA (B rows)
+constexpr int kSlabNT = 8;          // slab kernel: MMA N (tokens / pairs 0 .. 7)
+constexpr int kSlabMaxExperts = 256;  // slab kernel, down_combine: experts counted in shared memory
 constexpr int SlabInboxBytes = 8 * (128 + 16) * 4;  // slab kernel: split-K inbox (8 tokens x 144 rows, fp32)
 
 struct GemvParams {
@@ -122,6 +124,8 @@ struct GemvParams {
   int cw;              // register-fed dense kernel: consumer warps = tile height / 16 (4 .. 8);
                        // slab kernel: consumer warps (2 or 4), tile height 16 slab_r cw
   int slab_r;          // slab kernel: 16-row blocks per consumer warp (1 or 2)
+  int tiles_per_cta;   // slab kernel, down_combine: 128-row tiles one CTA streams in turn
+  int chunk;           // MoE: pairs (shared expert: tokens) per CTA column chunk, 1 .. kNT (0: kNT)
   int skip_stage;      // test hook: the dense producers issue nothing for this 256-K stage (-1: none)
   uint32_t* err;       // device error word (the wait limit follows it, see common.cuh)
 };
@@ -204,6 +208,51 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) {
 }
 __device__ __forceinline__ float bf16_to_f32(uint16_t h) { return __uint_as_float(static_cast<uint32_t>(h) << 16); }
 
+// down_combine of one 128-row tile of H (rows h0 .. h0 + 127) by `nthr`
+// threads (this one is `ti`): out[t, h] = bf16(bf16(sum_j tw[t, j] *
+// y[t, j, h]) + y_shared[t, h]), the sum in fp32 over j = 0 .. topk - 1 with
+// fused multiply-adds.  A work item is 8 consecutive h of one token (16-byte
+// loads of y and y_shared, one 16-byte store; H is a multiple of 64, so an
+// item is wholly inside or outside H).  A token with an out-of-range id is
+// left unwritten.
+__device__ __forceinline__ void moe_combine_tile(const GemvParams& p, int h0, int ti, int nthr) {
+  for (int it = ti; it < 16 * p.M; it += nthr) {
+    const int t = it / 16, h = h0 + 8 * (it % 16);
+    if (h >= p.n_out) continue;
+    bool ids_ok = true;
+    for (int j = 0; j < p.topk; ++j) {
+      const int e = __ldg(p.ids + t * p.topk + j);
+      ids_ok = ids_ok && e >= 0 && e < p.E;
+    }
+    if (!ids_ok) continue;
+    float a[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = 0.0f;
+    for (int j = 0; j < p.topk; ++j) {
+      const float wj = __ldg(p.tw + t * p.topk + j);
+      const uint4 yv = __ldcg(reinterpret_cast<const uint4*>(p.out + static_cast<int64_t>(t * p.topk + j) * p.ldo + h));
+      const uint32_t yw[4] = {yv.x, yv.y, yv.z, yv.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        a[2 * q] = fmaf(wj, __uint_as_float(yw[q] << 16), a[2 * q]);
+        a[2 * q + 1] = fmaf(wj, __uint_as_float(yw[q] & 0xFFFF0000u), a[2 * q + 1]);
+      }
+    }
+    const uint4 sv = __ldcg(reinterpret_cast<const uint4*>(p.out2 + static_cast<int64_t>(t) * p.ldo2 + h));
+    const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float lo = __uint_as_float(static_cast<uint32_t>(f32_to_bf16_rn(a[2 * q])) << 16) +
+                       __uint_as_float(sw[q] << 16);
+      const float hi = __uint_as_float(static_cast<uint32_t>(f32_to_bf16_rn(a[2 * q + 1])) << 16) +
+                       __uint_as_float(sw[q] & 0xFFFF0000u);
+      o[q] = static_cast<uint32_t>(f32_to_bf16_rn(lo)) | (static_cast<uint32_t>(f32_to_bf16_rn(hi)) << 16);
+    }
+    *reinterpret_cast<uint4*>(p.out3 + static_cast<int64_t>(t) * p.n_out + h) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
 // SiLU with IEEE exp and division (the "exact" SiLU of the dense path).
 __device__ __forceinline__ float silu_exact(float g) { return __fdiv_rn(g, 1.0f + expf(-g)); }
 // SiLU with the fast exponential and division (the routed experts' fast sigmoid).
@@ -248,6 +297,8 @@ __device__ __forceinline__ void set_box(Work& w, int b, int wrow, int srow, int 
 template <int kMode, int kNT, typename Work = CtaWork>
 __device__ void resolve_work(const GemvParams& p, Work& w, uint32_t split, int lane) {
   const int tile = blockIdx.x / max(1u, cluster_nctarank());
+  // pairs (tokens) per MoE chunk: p.chunk when the host set one (1 .. kNT), else kNT
+  const int cn = p.chunk > 0 && p.chunk < kNT ? p.chunk : kNT;
   if (lane == 0) {
     w.active = 1;
     w.shared = 0;
@@ -292,20 +343,20 @@ __device__ void resolve_work(const GemvParams& p, Work& w, uint32_t split, int l
         live = false;
       }
       // rank of this pair among the pairs routed to e; the first pair of each
-      // chunk of kNT pairs computes the whole chunk.
+      // chunk of `cn` pairs computes the whole chunk.
       int cnt = 0;
       if (live)
         for (int q = lane; q < col; q += 32) cnt += ((q < 32 ? id0 : q < 64 ? id1 : __ldg(p.ids + q)) == e);
       const int rank = __reduce_add_sync(0xFFFFFFFFu, cnt);
-      live = live && rank % kNT == 0;
+      live = live && rank % cn == 0;
       if (!live) {
         if (lane == 0) w.active = 0;
         __syncwarp();
         return;
       }
-      // the chunk: the first kNT pairs q >= col routed to e, in order
+      // the chunk: the first cn pairs q >= col routed to e, in order
       int n = 0;
-      for (int q0 = col; q0 < p.P && n < kNT; q0 += 32) {
+      for (int q0 = col; q0 < p.P && n < cn; q0 += 32) {
         const int q = q0 + lane;
         const int v0 = __shfl_sync(0xFFFFFFFFu, id0, q % 32);
         const int v1 = __shfl_sync(0xFFFFFFFFu, id1, q % 32);
@@ -313,13 +364,13 @@ __device__ void resolve_work(const GemvParams& p, Work& w, uint32_t split, int l
         const bool m = q < p.P && idq == e;
         const unsigned bal = __ballot_sync(0xFFFFFFFFu, m);
         const int pos = n + __popc(bal & ((1u << lane) - 1u));
-        if (m && pos < kNT) {
+        if (m && pos < cn) {
           w.tok[pos] = kMode == kMoeGateUp ? q / p.topk : q;  // x row (token) or act row (pair)
           w.orow[pos] = q;
         }
         n += __popc(bal);
       }
-      n = min(n, kNT);
+      n = min(n, cn);
       __syncwarp();
       if (lane == 0) {
         w.ntok = n;
@@ -340,8 +391,8 @@ __device__ void resolve_work(const GemvParams& p, Work& w, uint32_t split, int l
         w.active = 0;
       } else {
         w.shared = 1;
-        const int t0 = chunk * kNT;
-        w.ntok = min(kNT, p.M - t0);
+        const int t0 = chunk * cn;
+        w.ntok = min(cn, p.M - t0);
         for (int n = 0; n < kNT; ++n) w.tok[n] = w.orow[n] = t0 + (n < w.ntok ? n : 0);
         w.k_end = p.K2;
         w.kbp = p.kbp2;
@@ -955,26 +1006,7 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
       epi_sync<kEpiThreads>();
       if (s_last) {
         pdl_wait();
-        const int h0 = blockIdx.x * 128;
-        for (int it = tid; it < 128 * p.M; it += kEpiThreads) {
-          const int t = it / 128, h = h0 + it % 128;
-          if (h >= p.n_out) continue;
-          bool ids_ok = true;  // a token with an out-of-range id is left unwritten
-          for (int j = 0; j < p.topk; ++j) {
-            const int e = __ldg(p.ids + t * p.topk + j);
-            ids_ok = ids_ok && e >= 0 && e < p.E;
-          }
-          if (!ids_ok) continue;
-          float acc = 0.0f;
-          for (int j = 0; j < p.topk; ++j) {
-            const float wj = __ldg(p.tw + t * p.topk + j);
-            const float y = bf16_to_f32(__ldcg(p.out + static_cast<int64_t>(t * p.topk + j) * p.ldo + h));
-            acc = fmaf(wj, y, acc);
-          }
-          const float sb = bf16_to_f32(f32_to_bf16_rn(acc));
-          const float ysh = bf16_to_f32(__ldcg(p.out2 + static_cast<int64_t>(t) * p.ldo2 + h));
-          p.out3[static_cast<int64_t>(t) * p.n_out + h] = f32_to_bf16_rn(sb + ysh);
-        }
+        moe_combine_tile(p, blockIdx.x * 128, tid, kEpiThreads);
       }
     }
   } else if (C::kPush && S > 1) {

@@ -785,26 +785,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, kOcc) gemv_rf_kernel(con
       epi_sync<kEpiThreads>();
       if (s_last) {
         pdl_wait();
-        const int h0 = blockIdx.x * 128;
-        for (int it = tid; it < 128 * p.M; it += kEpiThreads) {
-          const int t = it / 128, h = h0 + it % 128;
-          if (h >= p.n_out) continue;
-          bool ids_ok = true;  // a token with an out-of-range id is left unwritten
-          for (int j = 0; j < p.topk; ++j) {
-            const int e = __ldg(p.ids + t * p.topk + j);
-            ids_ok = ids_ok && e >= 0 && e < p.E;
-          }
-          if (!ids_ok) continue;
-          float a = 0.0f;
-          for (int j = 0; j < p.topk; ++j) {
-            const float wj = __ldg(p.tw + t * p.topk + j);
-            const float y = bf16_to_f32(__ldcg(p.out + static_cast<int64_t>(t * p.topk + j) * p.ldo + h));
-            a = fmaf(wj, y, a);
-          }
-          const float sb = bf16_to_f32(f32_to_bf16_rn(a));
-          const float ysh = bf16_to_f32(__ldcg(p.out2 + static_cast<int64_t>(t) * p.ldo2 + h));
-          p.out3[static_cast<int64_t>(t) * p.n_out + h] = f32_to_bf16_rn(sb + ysh);
-        }
+        moe_combine_tile(p, blockIdx.x * 128, tid, kEpiThreads);
       }
     }
   } else if (S > 1) {

@@ -34,11 +34,9 @@
 
 namespace fp4 {
 
-constexpr int kSlabNT = 8;            // MMA N: tokens 0 .. 7
 constexpr int kSlabR = 2;             // 16-row blocks per consumer warp
 constexpr int kSlabThreads = kSlabMaxCW * 32 + 32;
 constexpr int kSlabMinBlocks = 3;     // CTAs per SM the registers are budgeted for
-using SlabWork = CtaWorkN<kSlabChunk>;
 
 template <int kR>
 struct SlabCfg {
@@ -59,16 +57,24 @@ __device__ __forceinline__ bool bf16x8_to_f16x8_exact(const uint4& v, uint4& o) 
   return e;
 }
 
-// kMode: kDenseFp4 (nvfp4_gemv) or kMoeGateUp (the gate_up launch of
+// kMode: kDenseFp4 (nvfp4_gemv); kMoeGateUp (the gate_up launch of
 // vllm.models.flint.ops.moe_gemv: routed chunks of up to kSlabChunk pairs of
 // one expert, and the shared expert's token chunks, with the epilogues of
-// the register-fed kernel).
+// the register-fed kernel); kMoeDown (down_combine: chunks of up to 8 pairs;
+// CTA column x streams its share of the row tiles (the tiles split evenly
+// over gridDim.x groups) in turn over one resident activation slab, the
+// whole K, and after each tile writes the
+// tile's y rows, arrives on the tile's counter and, when it arrives last,
+// combines the tile's outputs).
 template <int kR, int kMode = kDenseFp4>
 __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel(const __grid_constant__ GemvParams p) {
   using C = SlabCfg<kR>;
   constexpr int kChains = C::kChains;
   constexpr bool kDense = kMode == kDenseFp4;
-  static_assert(kDense || kMode == kMoeGateUp, "slab kernel modes");
+  constexpr bool kDown = kMode == kMoeDown;
+  static_assert(kDense || kMode == kMoeGateUp || kDown, "slab kernel modes");
+  constexpr int kChunk = kDown ? kSlabNT : kSlabChunk;  // B rows of a MoE CTA, at most
+  using Work = CtaWorkN<kChunk>;
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -80,7 +86,10 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
   __shared__ __align__(8) uint64_t bar_inbox;
   __shared__ volatile int s_abort;
   __shared__ int s_xbad[kSlabMaxStages];  // 1: the stage's activations are not all exact in f16
-  __shared__ SlabWork s_mwork;            // MoE: the CTA's work, resolved by the producer warp
+  __shared__ Work s_mwork;                // MoE: the CTA's work, resolved by the producer warp
+  __shared__ int s_last;                  // down_combine: this CTA arrived last on the tile's counter
+  __shared__ int s_target;                // down_combine: arrivals that complete a tile (active CTAs per tile)
+  __shared__ int s_hist[kDown ? kSlabMaxExperts : 1];  // down_combine: pairs per expert
 
   const int tid = threadIdx.x;
   const int warp = tid / 32;
@@ -99,11 +108,37 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
   wk.shared = 0;
   wk.expert = -1;
   if constexpr (!kDense) {
-    if (warp == cw) resolve_work<kMode, kSlabChunk, SlabWork>(p, s_mwork, 0, lane);
+    if (warp == cw) resolve_work<kMode, kChunk, Work>(p, s_mwork, 0, lane);
     __syncthreads();
     copy_work(s_mwork, wk);
-    wk.k_begin = static_cast<int>(rank) * p.k_split;  // routed and shared K are both H
-    wk.k_end = min(p.K, wk.k_begin + p.k_split);
+    if constexpr (!kDown) {
+      wk.k_begin = static_cast<int>(rank) * p.k_split;  // routed and shared K are both H
+      wk.k_end = min(p.K, wk.k_begin + p.k_split);
+    }
+    // (down_combine: the whole K; the host sets routed_tiles = shared_tiles
+    // = the tile groups, and the box is moved to the group's tiles below)
+    if constexpr (kDown) {
+      // The CTAs that compute something for a tile group -- one per chunk of
+      // up to p.chunk pairs of an expert (valid ids only) and one per shared-
+      // expert token chunk -- are the arrivals a tile's combine waits for,
+      // so the CTAs of the other columns leave at once.  The ids are two
+      // kernels old (the router's, read by gate_up after its wait), so they
+      // are read before this grid's wait.
+      for (int i = tid; i < p.E; i += blockDim.x) s_hist[i] = 0;
+      __syncthreads();
+      for (int q = tid; q < p.P; q += blockDim.x) {
+        const int e = __ldg(p.ids + q);
+        if (e >= 0 && e < p.E) atomicAdd(&s_hist[e], 1);
+      }
+      __syncthreads();
+      if (warp == 0) {
+        const int cn = p.chunk > 0 && p.chunk < kChunk ? p.chunk : kChunk;  // (as resolve_work)
+        int t = 0;
+        for (int i = lane; i < p.E; i += 32) t += (s_hist[i] + cn - 1) / cn;
+        t = __reduce_add_sync(0xFFFFFFFFu, t);
+        if (lane == 0) s_target = t + (p.M + cn - 1) / cn;
+      }
+    }
   } else {
     const int tile = blockIdx.x / max(1u, S);
     wk.k_begin = static_cast<int>(rank) * p.k_split;
@@ -127,13 +162,36 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
   // expert's tokens (MoE; 0 for an inactive CTA, which streams nothing)
   const int M = kDense ? p.M : (s_mwork.active ? s_mwork.ntok : 0);
   const int klen = wk.k_end - wk.k_begin;
-  const int nst = M > 0 ? (klen + 255) / 256 : 0;
+  const int nst_tile = (klen + 255) / 256;  // stages per row tile (and activation stages in the slab)
+  // down_combine: the CTA's row tiles tile0 .. tile0 + ntl - 1
+  const int tiles_h = (p.n_out + 127) / 128;
+  const int tile0 = kDown ? static_cast<int>(blockIdx.x * tiles_h / gridDim.x) : 0;
+  const int ntl = kDown ? static_cast<int>((blockIdx.x + 1) * tiles_h / gridDim.x) - tile0 : 1;
+  // The CTAs of a tile group take its tiles in rotated orders (column y
+  // starts at tile y mod ntl), so their arrivals on one tile's counter are
+  // spread over the group's run instead of meeting at once.
+  const int rot = kDown ? static_cast<int>(blockIdx.y % static_cast<unsigned>(ntl)) : 0;
+  auto tile_of = [&](int tt) { return tt + rot < ntl ? tt + rot : tt + rot - ntl; };  // CTA-relative tile
+  if constexpr (kDown) {
+    wk.wrow[0] = (wk.shared ? 0 : wk.expert * p.rows_per_expert) + tile0 * 128;
+    wk.srow[0] = tile0 * 128;
+    wk.sgroup[0] = tile0;
+  }
+  const int nst = M > 0 ? ntl * nst_tile : 0;
+  if constexpr (kDown) {
+    if (M == 0) return;  // (uniform: no barrier, copy or arrival of this CTA is pending)
+  }
   const uint32_t slab_stage = static_cast<uint32_t>(M) * 512u;  // bytes of one stage's activations
   const uint64_t pol_w = policy_evict_first();
   auto issue_weights = [&](int s, int slot) {
     const uint32_t st = ring + slot * p.stage_bytes;
     const uint32_t fb = smem_u32(&bar_full[slot]);
-    const int k0 = wk.k_begin + s * 256;
+    int tt = 0, ks = s;  // row tile (down_combine) and K stage
+    if constexpr (kDown) {
+      tt = s / nst_tile;
+      ks = s - tt * nst_tile;
+    }
+    const int k0 = wk.k_begin + ks * 256;
     const int nchunks = min(256, wk.k_end - k0) / kSubK;
     const CUtensorMap* tmw = wk.shared ? &p.tm_w2 : &p.tm_w;
     const uint8_t* sfb =
@@ -142,13 +200,13 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
 #pragma unroll
     for (int g = 0; g < 4; ++g) bytes += (wk.sgroup[g] >= 0 ? nchunks * 512 : 0);
     mbar_arrive_expect_tx(fb, bytes);
-    tma_load_2d(st, tmw, k0 / 2, wk.wrow[0], fb, pol_w);
+    tma_load_2d(st, tmw, k0 / 2, wk.wrow[0] + tile_of(tt) * 128, fb, pol_w);
     if (wk.paired) tma_load_2d(st + trows * 64, tmw, k0 / 2, wk.wrow[1], fb, pol_w);
     uint32_t sdst = st + trows * 128;  // the valid groups, in order
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
       if (wk.sgroup[g] < 0) continue;
-      const size_t chunk = static_cast<size_t>(wk.sgroup[g]) * (wk.kbp / 4) + k0 / 64;
+      const size_t chunk = static_cast<size_t>(wk.sgroup[g] + tile_of(tt)) * (wk.kbp / 4) + k0 / 64;
       bulk_load(sdst, sfb + chunk * 512, nchunks * 512, fb, pol_w);
       sdst += 2048;
     }
@@ -179,7 +237,7 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
     for (int s = 0; s < pre; ++s)
       if (s != p.skip_stage) issue_weights(s, s);  // (test hook: the skipped stage is never issued)
   }
-  for (int i = tid; i < nst; i += blockDim.x) s_xbad[i] = 0;
+  for (int i = tid; i < nst_tile; i += blockDim.x) s_xbad[i] = 0;
   __syncthreads();
   if (S > 1) cluster_arrive_relaxed();  // paired with a wait before the first remote access
   if (tid == 0) pdl_launch_dependents();
@@ -232,7 +290,7 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
     // bf16 and f16), so the zero weights there meet zero activations.
     pdl_wait();
     const int nchk = klen / 8;  // 16-byte chunks per token holding data
-    const int nslot = nst * 32;  // 16-byte chunks per token in the slab
+    const int nslot = (M > 0 ? nst_tile : 0) * 32;  // 16-byte chunks per token in the slab
     for (int q = tid; q < M * nslot; q += ncons) {
       const int n = q / nslot, kq = q % nslot;
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
@@ -351,18 +409,85 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
         }
       }
     };
+    // down_combine, after a row tile's last stage: the tile's y rows (y_j =
+    // bf16(acc * alpha2[e]) into the workspace, or y_shared = bf16(acc *
+    // gssd)), then one arrival on the tile's counter, tagged with this
+    // call's epoch; the CTA that arrives last combines the tile:
+    // out[t] = bf16(bf16(sum_j tw[t, j] * y[t, j]) + y_shared[t]).
+    // Every consumer warp calls it for the same tiles, also after a wait ran
+    // out (the first barrier agrees on the abort, which skips the tile's
+    // writes and arrival: its outputs stay unwritten); returns the abort.
+    auto tile_done = [&](int tt) -> bool {
+      const bool ab = bar_red_or<1>(ncons, s_abort != 0);
+      const int h0 = (tile0 + tile_of(tt)) * 128;
+      if (!ab) {
+        const float post = static_cast<float>(1 << kShift);
+        const float sc = wk.shared ? __ldg(p.gs) : __ldg(p.alpha + wk.expert);
+        uint16_t* dst = wk.shared ? p.out2 : p.out;
+        const int64_t ld = wk.shared ? p.ldo2 : p.ldo;
+#pragma unroll
+        for (int b = 0; b < kR; ++b) {
+#pragma unroll
+          for (int hr = 0; hr < 2; ++hr) {
+            const int h = h0 + (warp * kR + b) * 16 + sg + 8 * hr;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int n = 2 * c + e;
+              float v = accb[b][2 * hr + e] * post;
+              accb[b][2 * hr + e] = 0.0f;
+#pragma unroll
+              for (int q = 0; q < kChains; ++q) {
+                v += acc[q][b][2 * hr + e];
+                acc[q][b][2 * hr + e] = 0.0f;
+              }
+              if (n < M && h < p.n_out) dst[static_cast<int64_t>(s_mwork.orow[n]) * ld + h] = f32_to_bf16_rn(v * sc);
+            }
+          }
+        }
+      }
+      cons_sync(ncons);  // this CTA's y rows of the tile are written
+      if (tid == 0 && ab) s_last = 0;
+      if (tid == 0 && !ab) {
+        __threadfence();
+        unsigned long long* ctr = p.counters + tile0 + tile_of(tt);
+        const unsigned long long tag = static_cast<unsigned long long>(p.epoch) << 32;
+        unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(ctr), next;
+        for (;;) {
+          next = ((old & 0xFFFFFFFF00000000ull) == tag) ? old + 1 : tag + 1;
+          const unsigned long long seen = atomicCAS(ctr, old, next);
+          if (seen == old) break;
+          old = seen;
+        }
+        s_last = static_cast<int>(static_cast<uint32_t>(next)) == s_target;
+        if (s_last) atomicExch(ctr, 0ull);
+        __threadfence();
+      }
+      cons_sync(ncons);
+      if (s_last) {
+        moe_combine_tile(p, h0, tid, ncons);
+      }
+      return ab;
+    };
     for (int s = 0, slot = 0, ph = 0; s < nst; ++s, slot = slot + 1 == nstages ? 0 : slot + 1, ph ^= slot == 0) {
       const uint32_t st = ring + slot * p.stage_bytes;
-      const uint32_t xs = slab + s * slab_stage;
+      const int tt = kDown ? s / nst_tile : 0;  // row tile (down_combine)
+      const int ks = s - tt * nst_tile;         // K stage
+      const uint32_t xs = slab + ks * slab_stage;
       const bool ok = __all_sync(0xFFFFFFFFu, !s_abort && mbar_wait(smem_u32(&bar_full[slot]), ph, p.err));
       if (!ok) {
         s_abort = 1;
-        break;
+        if constexpr (kDown) {
+          // (the slot is not released: its copy may still land)
+          if (ks == nst_tile - 1 && tile_done(tt)) break;
+          continue;
+        } else {
+          break;
+        }
       }
       // valid K of the stage: 64 .. 256 in steps of 64; a chunk (32 K) is
       // wholly valid or wholly past the end
-      const int kvalid = min(256, klen - s * 256);
-      if (!s_xbad[s]) {
+      const int kvalid = min(256, klen - ks * 256);
+      if (!s_xbad[ks]) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           if (128 * h < kvalid) {
@@ -378,12 +503,17 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bar_empty[slot]));
+      if constexpr (kDown) {
+        if (ks == nst_tile - 1 && tile_done(tt)) break;
+      }
     }
   }
 
   // ==================================================================== epilogue
   __syncwarp();
-  if (warp < cw) {
+  if (kDown) {
+    // (down_combine finished each tile inside the loop)
+  } else if (warp < cw) {
     const float post = static_cast<float>(1 << kShift);
     // Push this thread's partials (its rows, tokens 2c + {0,1} below M) to
     // the owners of the rows: inbox[src][n][rr].

@@ -43,9 +43,10 @@ cudaError_t rf_max_clusters(int mode, int nt, unsigned cluster, size_t smem, int
 // Slab kernel (k_gemv_slab.cuh): dense NVFP4, 1 .. 8 tokens, r = 16-row
 // blocks per consumer warp (1 or 2); the block is (p.cw + 1) warps.
 cudaError_t launch_slab(int r, const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info);
-// The slab kernel's MoE gate_up mode (r = 2, four consumer warps).
-cudaError_t launch_slab_moe(const GemvParams& p, const LaunchCfg& cfg);
-cudaError_t slab_moe_regs(int* regs);
+// The slab kernel's MoE modes, kMoeGateUp or kMoeDown (r = 2, four consumer
+// warps; down_combine without a cluster).
+cudaError_t launch_slab_moe(int mode, const GemvParams& p, const LaunchCfg& cfg);
+cudaError_t slab_moe_regs(int mode, int* regs);
 // Clusters of `cluster` slab-kernel CTAs (cw consumer warps, `smem` bytes of
 // dynamic shared memory) that fit on the GPU at once.
 cudaError_t slab_max_clusters(int r, int cw, unsigned cluster, size_t smem, int* n);

@@ -305,3 +305,51 @@ def test_gate_up_slab_decode_block(fp4):
     assert_close(u16(act), (an, al, ah), "act decode block M=1")
     assert_close(u16(sact), (sn, sl, sh), "sact decode block M=1")
     assert fp4.get_device_error() == 0
+
+
+def _down_slab_tiles(fp4, M, topk, E, H, I, SI):
+    """Row tiles per CTA of the slab kernel's plan for this down_combine call
+    on this GPU (None: another kernel serves it)."""
+    import ctypes
+
+    class Plan(ctypes.Structure):
+        _fields_ = [(n, ctypes.c_int) for n in ("tiles_per_cta", "groups", "columns", "chunk_pairs", "slab_bytes",
+                                                "stage_bytes", "stages", "ctas_per_sm")] + \
+            [("smem_bytes", ctypes.c_size_t)]
+    f = fp4.lib().fp4gemv_plan_moe_down_slab
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_int] * 8 + [ctypes.POINTER(Plan)]
+    out = Plan()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return out.tiles_per_cta if f(M, topk, E, H, I, SI, sms, 128, ctypes.byref(out)) == 0 else None
+
+
+# down_combine on the slab kernel with several row tiles per CTA: H = 832 is
+# 6.5 tiles (a partial last tile) in groups of one or two tiles;
+# many experts, so most columns are inactive duplicates that leave at once
+# and the combine waits only for the CTAs that compute.
+@pytest.mark.parametrize("M,topk,E,H,I,SI,T", [(16, 8, 128, 832, 256, 256, 2), (12, 8, 96, 1024, 320, 448, 2)])
+def test_down_combine_slab_tiles(fp4, M, topk, E, H, I, SI, T):
+    assert _down_slab_tiles(fp4, M, topk, E, H, I, SI) == T
+    d = make_moe(M, E=E, H=H, I=I, SI=SI, topk=topk, seed=800 + M)
+    out = run_down(fp4, d)
+    ref, bad = ref_down(d)
+    assert bad == 0
+    assert_close(u16(out), ref, f"down slab M={M} H={H}")
+    assert fp4.get_device_error() == 0
+    out2 = run_down(fp4, d)
+    assert torch.equal(out, out2)
+
+
+def test_down_combine_slab_decode_block(fp4):
+    # 8 tokens of the E = 128, top-8, H = 4096, I = SI = 1536 block: five or
+    # six row tiles per CTA; sampled tokens against the oracle
+    c = synth.MOE
+    assert _down_slab_tiles(fp4, 8, c["topk"], c["E"], c["H"], c["I"], c["SI"]) == 6
+    d = make_moe(8, c["E"], c["H"], c["I"], c["SI"], c["topk"], seed=101)
+    out = run_down(fp4, d)
+    tokens = [0, 3, 7]
+    ref, bad = ref_down(d, tokens=tokens)
+    assert bad == 0
+    assert_close(u16(out)[tokens], tuple(r[tokens] for r in ref), "down slab decode block M=8")
+    assert fp4.get_device_error() == 0

@@ -361,3 +361,93 @@ def test_moe_slab_plan_rejects_bad_arguments(moe_slab_fn):
     assert moe_slab_fn(1, 8, 128, 4096, 1536, 1536, sms=0)[0] == 1
     assert moe_slab_fn(1, 8, 128, 4000, 1536, 1536)[0] == 2   # H % 64
     assert moe_slab_fn(200, 8, 128, 4096, 1536, 1536)[0] == 2  # M * topk > 1024
+
+
+# --- the slab kernel's MoE down_combine plan, host only -----------------------------------
+
+class MoeDownSlabPlan(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("tiles_per_cta", "groups", "columns", "chunk_pairs", "slab_bytes",
+                                            "stage_bytes", "stages", "ctas_per_sm")] + [("smem_bytes", ctypes.c_size_t)]
+
+
+@pytest.fixture(scope="module")
+def down_slab_fn():
+    from moe_nvfp4_gemv_gb300 import fp4gemv
+    f = fp4gemv.lib().fp4gemv_plan_moe_down_slab
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_int] * 8 + [ctypes.POINTER(MoeDownSlabPlan)]
+
+    def plan(M, topk, E, H, I, SI, regs=128, sms=SMS):
+        out = MoeDownSlabPlan()
+        return f(M, topk, E, H, I, SI, sms, regs, ctypes.byref(out)), out
+    return plan
+
+
+def down_slab_rule(M, topk, E, H, I, SI, sms=SMS):
+    """The rule written out: M <= 64, E <= 256; from the expected distinct
+    experts E (1 - (1 - topk / E)^M) (at most P, at least 1): the chunk, the
+    power of two <= 8 covering P / distinct pairs; rows min(P, chunk) of
+    max(I, SI) bf16; T so the expected CTAs fill 80 % of three per SM; as many 18 KB
+    stages as fit beside the slab (2 .. 8, at most T routed tiles' stages), at
+    two CTAs per SM when the expected CTAs fit two per SM."""
+    if M > 64 or E > 256:
+        return None
+    P = M * topk
+    pick = topk / E if topk < E else 1.0
+    distinct = max(min(E * (1.0 - (1.0 - pick) ** M), P), 1.0)
+    chunk = 1
+    while chunk < 8 and chunk < P / distinct:
+        chunk *= 2
+    rows = min(P, chunk)
+    nst = -(-max(I, SI) // 256)
+    slab = -(-(rows * nst * 512) // 1024) * 1024
+    tiles = -(-H // 128)
+    cols = distinct + -(-M // chunk)
+    groups = min(max(1, int(0.8 * 3 * sms / cols)), tiles)
+    T = -(-tiles // groups)
+    occ = 2 if cols * groups <= 2.0 * sms else 3
+    ns = min(8, (228 * 1024 // occ - 4096 - 1024 - slab) // 18432, T * -(-I // 256))
+    if ns < 2:
+        return None
+    return dict(tiles_per_cta=T, groups=groups, chunk_pairs=chunk, slab_bytes=slab, stages=ns, ctas_per_sm=occ,
+                smem_bytes=1024 + slab + ns * 18432)
+
+
+@pytest.mark.parametrize("M,topk,E,H,I,SI", [(1, 8, 128, 4096, 1536, 1536), (8, 8, 128, 4096, 1536, 1536),
+                                             (32, 8, 128, 4096, 1536, 1536), (64, 8, 128, 4096, 1536, 1536),
+                                             (16, 8, 128, 832, 256, 256), (3, 2, 8, 384, 256, 512),
+                                             (20, 2, 8, 384, 256, 512), (1, 8, 300, 4096, 1536, 1536),
+                                             (4, 8, 128, 4096, 8192, 1536), (65, 8, 128, 4096, 1536, 1536),
+                                             (64, 8, 16, 4096, 16384, 1536)])
+def test_down_slab_plan_matches_rule(down_slab_fn, M, topk, E, H, I, SI):
+    st, p = down_slab_fn(M, topk, E, H, I, SI)
+    want = down_slab_rule(M, topk, E, H, I, SI)
+    if want is None:
+        assert st == 2
+        return
+    assert st == 0
+    got = dict(tiles_per_cta=p.tiles_per_cta, groups=p.groups, chunk_pairs=p.chunk_pairs, slab_bytes=p.slab_bytes,
+               stages=p.stages, ctas_per_sm=p.ctas_per_sm, smem_bytes=p.smem_bytes)
+    assert got == want
+    assert p.stage_bytes == 18432 and p.columns == M * topk + -(-M // p.chunk_pairs)
+    # the groups split the tiles evenly: floor or ceil of tiles / groups each
+    tiles = -(-H // 128)
+    sizes = [(g + 1) * tiles // p.groups - g * tiles // p.groups for g in range(p.groups)]
+    assert sum(sizes) == tiles and max(sizes) == p.tiles_per_cta and max(sizes) - min(sizes) <= 1
+
+
+def test_down_slab_plan_decode_block(down_slab_fn):
+    # E = 128, top-8, H = 4096, I = SI = 1536: one token, one tile and one
+    # pair per CTA (9 columns x 32 tiles, two CTAs per SM, 5 of its 6 stages
+    # in the ring); 8 tokens (~53 experts), two pairs and six tiles per CTA
+    st, p = down_slab_fn(1, 8, 128, 4096, 1536, 1536)
+    assert st == 0 and (p.tiles_per_cta, p.chunk_pairs, p.ctas_per_sm, p.stages) == (1, 1, 2, 5)
+    st, p = down_slab_fn(8, 8, 128, 4096, 1536, 1536)
+    assert st == 0 and (p.tiles_per_cta, p.groups, p.chunk_pairs) == (6, 6, 2)  # 5 or 6 tiles each
+
+
+def test_down_slab_plan_rejects_bad_arguments(down_slab_fn):
+    assert down_slab_fn(0, 8, 128, 4096, 1536, 1536)[0] == 1
+    assert down_slab_fn(1, 8, 128, 4096, 1536, 1536, regs=0)[0] == 1
+    assert down_slab_fn(1, 8, 128, 4096, 1536, 1536, sms=0)[0] == 1
+    assert down_slab_fn(1, 8, 128, 4096, 192, 1536)[0] == 2   # I < 256
