@@ -69,28 +69,37 @@ typedef struct {
 fp4gemv_status fp4gemv_plan_slab(int M, int N, int K, int silu_mul, int sms, const int* regs, fp4gemv_slab_plan* out);
 
 typedef struct {
-  int split;          /* CTAs per cluster along H (1, 2, 4 or 8) */
-  int k_slab;         /* H elements per cluster rank, a multiple of 64 */
-  int chunk_pairs;    /* most (token, expert) pairs one routed CTA computes */
-  int columns;        /* grid columns: M * topk routed pair columns + the shared expert's token chunks */
+  int split;          /* split form: CTAs per cluster along H (1, 2, 4 or 8); grouped form: 1 */
+  int k_slab;         /* H elements per cluster rank, a multiple of 64 (grouped form: H) */
+  int tiles_per_cta;  /* 0: split form, one tile per CTA; else grouped form, the most tiles one CTA takes */
+  int groups;         /* grid columns: tiles x split (split form) or tile groups (grouped form) */
+  int chunk_pairs;    /* most (token, expert) pairs one routed CTA computes (1, 2 or 4) */
+  int columns;        /* grid rows: M * topk routed pair columns + the shared expert's token chunks */
   int tiles;          /* 128-row tiles per column: max(I / 64, ceil(SI / 64)) */
   int slab_bytes;     /* shared memory holding a CTA's activations */
   int stage_bytes;    /* one weight stage (codes of 128 rows x 256 K, two scale groups) */
+  int stages;         /* weight ring stages (2 .. 8) */
+  int ctas_per_sm;    /* CTAs per SM the shared memory is sized for (2 or 3) */
   size_t smem_bytes;  /* dynamic shared memory per CTA */
 } fp4gemv_moe_slab_plan;
 
 /* Plan of fp4gemv_moe_gate_up on the slab kernel (vllm.models.flint.ops.
- * moe_gemv, gate_up: routed chunks of up to chunk_pairs pairs of one expert
- * and the shared expert, the CTA's activations in shared memory, three
- * CTAs per SM, H split over a cluster).  No GPU is needed.
+ * moe_gemv, gate_up: routed chunks of pairs of one expert and the shared
+ * expert's token chunks, the CTA's activations in shared memory).  No GPU
+ * is needed.
  *   M, topk, E, H, I, SI: as fp4gemv_moe_gate_up (same shape rules).
  *   sms:  streaming multiprocessors of the GPU (152 on GB300).
  *   regs: registers per thread of the kernel.
  *   out:  HOST pointer, filled on success.
- * It applies when the CTAs of every expert the call can touch (at most
- * min(M * topk, E) routed chunks plus the shared expert's) fit on the GPU in
- * one wave with a split that leaves each rank at least 256 of H (one token
- * on the E = 128, top-8, H = 4096, I = SI = 1536 block: a split of two).
+ * Split form, when the CTAs of every expert the call can touch (at most
+ * min(M * topk, E) routed chunks of 4 pairs plus the shared expert's) fit
+ * one wave at three CTAs per SM with a split of H that leaves each rank at
+ * least 256 (one token on the E = 128, top-8, H = 4096, I = SI = 1536 block:
+ * a split of two).  Otherwise, up to 64 tokens, the grouped form: the whole
+ * H per CTA and T of its column's tiles in turn (T = 1 up to 2 tokens, else
+ * 2), many waves of CTAs; chunks of 1 pair up to 2 tokens, 2 up to 16, 4
+ * from 32 (halved while fewer than two stages fit); three CTAs per SM, two
+ * from 32 tokens; as many weight stages as fit (2 .. 8).
  * Returns FP4GEMV_ERR_INVALID_ARG for a null out, sms < 1 or regs < 1;
  * FP4GEMV_ERR_UNSUPPORTED_SHAPE for shapes fp4gemv_moe_gate_up rejects and
  * for calls the slab kernel does not serve (they run on the register-fed
@@ -102,11 +111,11 @@ typedef struct {
   int tiles_per_cta;  /* most 128-row tiles of H one CTA streams in turn: ceil(tiles / groups) */
   int groups;         /* grid columns along H; group g takes tiles [g tiles / groups, (g + 1) tiles / groups) */
   int columns;        /* grid rows: M * topk routed pair columns + the shared expert's token chunks */
-  int chunk_pairs;    /* most (token, expert) pairs one routed CTA computes (1, 2, 4 or 8) */
+  int chunk_pairs;    /* most (token, expert) pairs one routed CTA computes (8) */
   int slab_bytes;     /* shared memory holding a CTA's activation rows (the whole K) */
   int stage_bytes;    /* one weight stage (codes of 128 rows x 256 K, one scale group) */
   int stages;         /* weight ring stages (2 .. 8) */
-  int ctas_per_sm;    /* CTAs per SM the ring is sized for (2 or 3) */
+  int ctas_per_sm;    /* CTAs per SM the ring is sized for (3) */
   size_t smem_bytes;  /* dynamic shared memory per CTA */
 } fp4gemv_moe_down_slab_plan;
 
@@ -119,14 +128,10 @@ typedef struct {
  *   sms:  streaming multiprocessors of the GPU (152 on GB300).
  *   regs: registers per thread of the kernel.
  *   out:  HOST pointer, filled on success.
- * Applies to M <= 64 and E <= 256 when the activation rows and two weight
- * stages fit.  The sizes follow the expected routing, E (1 - (1 - topk /
- * E)^M) distinct experts for distinct top-k picks (at most M * topk): the
- * chunk is the power of two (<= 8) that holds an expert's expected pairs; T
- * makes the expected CTAs (distinct experts + ceil(M / chunk) shared-expert
- * chunks, times the tile groups) fill 80 % of three CTAs per SM; the ring takes as
- * many stages as fit (at most 8), sized for two CTAs per SM when the
- * expected CTAs fit two per SM, else three.
+ * Applies to 2 <= M <= 64 and E <= 256 when 8 activation rows of
+ * max(I, SI) and two weight stages fit a third of the SM's shared memory
+ * (one token runs on the register-fed kernel): chunks of 8 pairs, T = 2 tiles
+ * per CTA, three CTAs per SM, as many weight stages as fit (2 .. 8).
  * Returns FP4GEMV_ERR_INVALID_ARG for a null out, sms < 1 or regs < 1;
  * FP4GEMV_ERR_UNSUPPORTED_SHAPE for shapes fp4gemv_moe_down_combine rejects
  * and for calls the slab kernel does not serve. */

@@ -6,7 +6,6 @@
 #include <cuda.h>
 
 #include <atomic>
-#include <cmath>
 #include <cstdint>
 #include <cstddef>
 #include <cstring>
@@ -503,45 +502,93 @@ bool plan_slab(int M, int N, int K, bool silu, int sms, int inbox_bytes, const i
 }
 
 // The slab kernel for MoE gate_up: 128-row tiles (a routed [up; gate] group
-// or a shared-expert pair of 64-row gate and up boxes), routed chunks of up
-// to fp4::kSlabChunk pairs, K split so that the CTAs of the experts a call
-// can touch (at most min(P, E) routed chunks of one expert each when no
-// expert gets more than kSlabChunk pairs, plus the shared expert's chunks)
-// run in one wave at three CTAs per SM; the CTA's activations (kSlabChunk
-// rows at most) and two weight stages must fit a third of the SM's shared
-// memory.  At one token of the E = 128, top-8, H = 4096, I = SI = 1536
-// block (8 experts + the shared one: 216 tiles) that is a split of two; the
-// register-fed kernel ran those 216 whole-K CTAs in one uneven wave.
+// of 64 features, or a shared-expert pair of 64-row gate and up boxes), the
+// CTA's activation rows resident, two scale groups per weight stage.  Two
+// forms:
+//   split:   one tile per CTA, routed chunks of up to fp4::kSlabChunk pairs,
+//            H split over a cluster so that the CTAs of every expert the
+//            call can touch (at most min(P, E) routed chunks plus the shared
+//            expert's) run in one wave at three CTAs per SM.  One token of
+//            the E = 128, top-8, H = 4096, I = SI = 1536 block (216 tiles):
+//            a split of two; the register-fed kernel ran those 216 whole-H
+//            CTAs in one uneven wave.
+//   grouped: the whole H per CTA, T = 1 or 2 of its column's tiles in turn
+//            over the same activation rows, many waves of CTAs.  Measured
+//            on that block (us per call, L2-cold, 8 routings; against the
+//            register-fed kernel's chunks of 8): a sweep of chunk, tiles per
+//            CTA and CTAs per SM put the best at one tile per CTA for 2
+//            tokens (32.2 vs 39.7), two tiles per CTA from 4 tokens (4: 56.6
+//            vs 64.4; 8: 102.3 vs 115.3; 16: 164.6 vs 176.6), pairs of 2 at
+//            three CTAs per SM up to 16 tokens and pairs of 4 at two CTAs
+//            per SM (a deeper ring) from 32 (255 vs 265); fewer, longer
+//            CTAs were slower at every size (each CTA's stream is bounded
+//            by its ring, so the GPU needs many of them).  The ring takes
+//            as many stages as fit (2 .. 8); a chunk that leaves room for
+//            fewer than two is halved.
 struct SlabMoePlan {
-  int S = 1, kslab = 0, slab_bytes = 0, stage_bytes = 0;
+  int S = 1, kslab = 0, T = 0, groups = 0, chunk = fp4::kSlabChunk, slab_bytes = 0, stage_bytes = 0, nstages = 2,
+      occ = kSlabOcc;
   size_t smem = 0;
 };
 
 bool plan_slab_moe(int M, int topk, int E, int H, int I, int SI, int sms, int regs, SlabMoePlan* sp) {
-  const int cw = fp4::kSlabMaxCW, occ = kSlabOcc;
+  const int cw = fp4::kSlabMaxCW, occ3 = kSlabOcc;
   const int warp_regs = (regs * 32 + 255) / 256 * 256;
-  if (static_cast<long>(occ) * (cw + 1) * warp_regs > 65536 || sms < 1) return false;
+  if (static_cast<long>(occ3) * (cw + 1) * warp_regs > 65536 || sms < 1 || M > 64) return false;
   const long P = static_cast<long>(M) * topk;
-  const long routed_cols = P < E ? P : E;
-  const long shared_cols = (M + fp4::kSlabChunk - 1) / fp4::kSlabChunk;
-  const long tiles = routed_cols * (I / 64) + shared_cols * ((SI + 63) / 64);
-  const int rows = static_cast<int>(P < fp4::kSlabChunk ? P : fp4::kSlabChunk);  // B rows of a chunk, at most
   const int stage = 128 * 128 + 2 * 2048;  // codes + two scale groups (shared-expert gate and up boxes)
-  const int dyn = kSmemPerSm / occ - kSmemPerCta;
-  for (int S = 8; S >= 1; S /= 2) {
-    if (tiles * S > static_cast<long>(occ) * sms) continue;  // more than one wave
-    const int kslab = ((H + S - 1) / S + 63) / 64 * 64;
-    if (S > 1 && (kslab < 256 || static_cast<long>(S - 1) * kslab >= H)) continue;
-    const int nst = (kslab + 255) / 256;
-    if (nst > fp4::kSlabMaxStages) return false;
+  const int tiles = I / 64 > (SI + 63) / 64 ? I / 64 : (SI + 63) / 64;
+  {  // split form
+    const long routed_cols = P < E ? P : E;
+    const long shared_cols = (M + fp4::kSlabChunk - 1) / fp4::kSlabChunk;
+    const long ctas1 = routed_cols * (I / 64) + shared_cols * ((SI + 63) / 64);
+    const int rows = static_cast<int>(P < fp4::kSlabChunk ? P : fp4::kSlabChunk);  // B rows of a chunk, at most
+    const int dyn = kSmemPerSm / occ3 - kSmemPerCta;
+    for (int S = 8; S >= 1; S /= 2) {
+      if (ctas1 * S > static_cast<long>(occ3) * sms) continue;  // more than one wave
+      const int kslab = ((H + S - 1) / S + 63) / 64 * 64;
+      if (S > 1 && (kslab < 256 || static_cast<long>(S - 1) * kslab >= H)) continue;
+      const int nst = (kslab + 255) / 256;
+      if (nst > fp4::kSlabMaxStages) break;
+      const int slab = (rows * nst * 512 + 1023) / 1024 * 1024;
+      const size_t smem = 1024 + static_cast<size_t>(slab) + 2 * static_cast<size_t>(stage) + fp4::SlabInboxBytes;
+      if (smem > static_cast<size_t>(dyn)) break;  // a smaller split only needs more
+      sp->S = (H + kslab - 1) / kslab;
+      sp->kslab = kslab;
+      sp->T = 0;
+      sp->groups = static_cast<int>(tiles) * sp->S;
+      sp->chunk = fp4::kSlabChunk;
+      sp->slab_bytes = slab;
+      sp->stage_bytes = stage;
+      sp->nstages = 2;
+      sp->occ = occ3;
+      sp->smem = smem;
+      return true;
+    }
+  }
+  // grouped form
+  const int nst = (H + 255) / 256;
+  if (nst > fp4::kSlabMaxStages) return false;
+  const int occ = M >= 32 ? 2 : 3;
+  const int T = M <= 2 ? 1 : 2;
+  for (int chunk = M >= 32 ? 4 : M <= 2 ? 1 : 2; chunk >= 1; chunk /= 2) {
+    const int rows = static_cast<int>(P < chunk ? P : chunk);
     const int slab = (rows * nst * 512 + 1023) / 1024 * 1024;
-    const size_t smem = 1024 + static_cast<size_t>(slab) + 2 * static_cast<size_t>(stage) + fp4::SlabInboxBytes;
-    if (smem > static_cast<size_t>(dyn)) return false;  // a smaller split only needs more
-    sp->S = (H + kslab - 1) / kslab;
-    sp->kslab = kslab;
+    const long room = static_cast<long>(kSmemPerSm / occ - kSmemPerCta) - 1024 - slab - fp4::SlabInboxBytes;
+    long ns = room / stage;
+    if (ns > fp4::kMaxStages) ns = fp4::kMaxStages;
+    if (ns > static_cast<long>(T) * nst) ns = static_cast<long>(T) * nst;
+    if (ns < 2) continue;
+    sp->S = 1;
+    sp->kslab = H;
+    sp->T = T;
+    sp->groups = (tiles + T - 1) / T;
+    sp->chunk = chunk;
     sp->slab_bytes = slab;
     sp->stage_bytes = stage;
-    sp->smem = smem;
+    sp->nstages = static_cast<int>(ns);
+    sp->occ = occ;
+    sp->smem = 1024 + static_cast<size_t>(slab) + static_cast<size_t>(ns) * stage + fp4::SlabInboxBytes;
     return true;
   }
   return false;
@@ -550,41 +597,28 @@ bool plan_slab_moe(int M, int topk, int E, int H, int I, int SI, int sms, int re
 std::atomic<int> g_slab_moe_regs[kMaxDevices];
 
 // The slab kernel for down_combine: the whole K per CTA (its activation
-// rows resident), T row tiles per CTA streamed in turn over the same rows (one
-// CTA's fixed costs -- its activation load, the ramp of its ring -- serve T
-// tiles), one scale group per 128-row weight stage.  Sizes come from the
-// expected routing: E (1 - (1 - topk / E)^M) distinct experts for distinct
-// top-k picks (at most M * topk), P / distinct pairs per expert.
-//   chunk: pairs per CTA, the power of two (<= 8) that holds the expected
-//          pairs of an expert (an expert with more forms more chunks); it
-//          bounds the resident rows, and a smaller slab leaves room for a
-//          deeper ring.
-//   groups: the tiles split evenly into groups (T = ceil(tiles / groups)
-//          tiles at most per CTA) so that the expected CTAs (distinct
-//          experts + ceil(M / chunk) shared chunks, times the groups) fill
-//          80 % of three CTAs per SM.
-//   ring:  as many 18 KB stages as fit (at most 8) beside the slab, at two
-//          CTAs per SM when the expected CTAs fit two per SM, else three.
-// One token: chunk 1, T = 1, 288 CTAs of 6 stages with 5 in the ring; 8
-// tokens (~53 experts): chunk 2, 6 groups of 5 or 6 tiles.
+// rows resident), chunks of up to 8 pairs of one expert, T = 2 row tiles per
+// CTA streamed in turn over the same rows, three CTAs per SM, many waves;
+// one scale group per 128-row weight stage, as many stages as fit (2 .. 8).
+// Measured on the E = 128, top-8, H = 4096, I = SI = 1536 block (us per
+// call, L2-cold, 8 routings), a sweep of chunk, tiles per CTA and CTAs per
+// SM: 8 tokens 80.4 (register-fed kernel 92.2), 32 tokens 159.8 (216.3);
+// fewer, longer CTAs were slower.  One token stays on the register-fed
+// kernel (17.3 against 17.8 at best here).
 struct SlabDownPlan {
-  int T = 1, groups = 1, chunk = 8, slab_bytes = 0, stage_bytes = 0, nstages = 2, occ = 3;
+  int T = 2, groups = 1, chunk = 8, slab_bytes = 0, stage_bytes = 0, nstages = 2, occ = 3;
   size_t smem = 0;
 };
 
 constexpr int kSmemPerCtaDown = 4096;  // reservation + static shared memory (incl. the expert counts)
 
 bool plan_slab_down(int M, int topk, int E, int H, int I, int SI, int sms, int regs, SlabDownPlan* sp) {
-  const int cw = fp4::kSlabMaxCW;
+  const int cw = fp4::kSlabMaxCW, occ = 3, T = 2;
   const int warp_regs = (regs * 32 + 255) / 256 * 256;
-  if (3L * (cw + 1) * warp_regs > 65536 || sms < 1 || E > fp4::kSlabMaxExperts) return false;
+  if (static_cast<long>(occ) * (cw + 1) * warp_regs > 65536 || sms < 1 || E > fp4::kSlabMaxExperts) return false;
+  if (M < 2 || M > 64) return false;
   const long P = static_cast<long>(M) * topk;
-  const double pick = topk < E ? static_cast<double>(topk) / E : 1.0;
-  double distinct = E * (1.0 - std::pow(1.0 - pick, M));
-  if (distinct > P) distinct = static_cast<double>(P);
-  if (distinct < 1.0) distinct = 1.0;
-  int chunk = 1;
-  while (chunk < fp4::kSlabNT && chunk < static_cast<double>(P) / distinct) chunk *= 2;
+  const int chunk = fp4::kSlabNT;
   const int rows = static_cast<int>(P < chunk ? P : chunk);
   const int kmax = I > SI ? I : SI;
   const int nst = (kmax + 255) / 256;
@@ -592,22 +626,13 @@ bool plan_slab_down(int M, int topk, int E, int H, int I, int SI, int sms, int r
   const int slab = (rows * nst * 512 + 1023) / 1024 * 1024;
   const int stage = 128 * 128 + 2048;
   const int tiles = (H + 127) / 128;
-  const double cols = distinct + (M + chunk - 1) / chunk;
-  // (80 % of the slots: the estimate misses experts with more than one
-  // chunk and routings with more distinct experts, and a CTA past one wave
-  // would double the call)
-  int groups = static_cast<int>(0.8 * 3 * sms / cols);
-  if (groups < 1) groups = 1;
-  if (groups > tiles) groups = tiles;
-  const int T = (tiles + groups - 1) / groups;  // (groups take floor or ceil of tiles / groups tiles)
-  const int occ = cols * groups <= 2.0 * sms ? 2 : 3;
   const long room = static_cast<long>(kSmemPerSm / occ - kSmemPerCtaDown) - 1024 - slab;
   int ns = static_cast<int>(room / stage);
   if (ns > fp4::kMaxStages) ns = fp4::kMaxStages;
   if (ns > T * ((I + 255) / 256)) ns = T * ((I + 255) / 256);  // (no deeper than a routed CTA's stream)
   if (ns < 2) return false;
   sp->T = T;
-  sp->groups = groups;
+  sp->groups = (tiles + T - 1) / T;
   sp->chunk = chunk;
   sp->slab_bytes = slab;
   sp->stage_bytes = stage;
@@ -826,11 +851,15 @@ fp4gemv_status fp4gemv_plan_moe_slab(int M, int topk, int E, int H, int I, int S
   if (!plan_slab_moe(M, topk, E, H, I, SI, sms, regs, &sp)) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
   out->split = sp.S;
   out->k_slab = sp.kslab;
-  out->chunk_pairs = fp4::kSlabChunk;
-  out->columns = M * topk + (M + fp4::kSlabChunk - 1) / fp4::kSlabChunk;
+  out->tiles_per_cta = sp.T;
+  out->groups = sp.groups;
+  out->chunk_pairs = sp.chunk;
+  out->columns = M * topk + (M + sp.chunk - 1) / sp.chunk;
   out->tiles = I / 64 > (SI + 63) / 64 ? I / 64 : (SI + 63) / 64;
   out->slab_bytes = sp.slab_bytes;
   out->stage_bytes = sp.stage_bytes;
+  out->stages = sp.nstages;
+  out->ctas_per_sm = sp.occ;
   out->smem_bytes = sp.smem;
   return FP4GEMV_OK;
 }
@@ -956,12 +985,11 @@ fp4gemv_status fp4gemv_moe_gate_up(const void* x, const int32_t* ids, int M, int
   int sms = 0;
   fp4gemv_status st = device_state(&err, &sms);
   if (st != FP4GEMV_OK) return st;
-  // The slab kernel when its plan fits one wave (plan_slab_moe: one token
-  // on the E = 128, H = 4096 block); else the register-fed kernel for up to 64
+  // The slab kernel when it has a plan (plan_slab_moe: up to 64 tokens,
+  // split or grouped form); else the register-fed kernel for up to 64
   // tokens: expert chunks hold at most 8 pairs (more pairs routed to one
-  // expert form further chunks; with 8 of 128 experts per token an expert
-  // gets ~P / E pairs, a handful, so most chunks take the f16 route) and the
-  // shared expert runs ceil(M / 8) chunks; the tcgen05 kernel beyond.
+  // expert form further chunks) and the shared expert runs ceil(M / 8)
+  // chunks; the tcgen05 kernel beyond.
   {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FP4GEMV_ERR_CUDA;
@@ -1008,16 +1036,18 @@ fp4gemv_status fp4gemv_moe_gate_up(const void* x, const int32_t* ids, int M, int
       p.shared_tiles = (SI + 63) / 64;
       p.kbp = p.kbp2 = ((H / 16) + 3) / 4 * 4;
       p.sf_expert_bytes = static_cast<uint32_t>(fp4gemv_scale_bytes(2 * I, H));
-      p.nstages = 2;
+      p.nstages = sp.nstages;
       p.stage_bytes = sp.stage_bytes;
       p.x_off = sp.slab_bytes;
       p.cw = fp4::kSlabMaxCW;
       p.slab_r = 2;
+      p.chunk = sp.chunk;
+      p.tiles_per_cta = sp.T;  // 0: the split form
+      if (sp.T > 0) p.routed_tiles = p.shared_tiles = sp.groups;  // (grouped: resolve_work's tile is the group)
       p.skip_stage = -1;
       p.err = err;
       LaunchCfg cfg{};
-      const int tiles = p.routed_tiles > p.shared_tiles ? p.routed_tiles : p.shared_tiles;
-      cfg.grid = dim3(tiles * sp.S, p.P + (M + fp4::kSlabChunk - 1) / fp4::kSlabChunk, 1);
+      cfg.grid = dim3(sp.groups, p.P + (M + sp.chunk - 1) / sp.chunk, 1);
       cfg.cluster = sp.S;
       cfg.smem = sp.smem;
       cfg.pdl = pdl;

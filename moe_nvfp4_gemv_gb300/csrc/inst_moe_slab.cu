@@ -1,7 +1,7 @@
-// Instantiations of the slab kernel's MoE modes: gate_up (routed chunks of up
-// to kSlabChunk pairs of one expert and the shared expert's token chunks, H
-// split over a cluster) and down_combine (chunks of up to 8 pairs, several
-// row tiles per CTA over one resident activation slab).
+// Instantiations of the slab kernel's MoE modes: gate_up (routed chunks of
+// pairs of one expert and the shared expert's token chunks; split form: H
+// split over a cluster; grouped form: several tiles per CTA over one
+// resident activation slab) and down_combine (grouped).
 #include "k_gemv_slab.cuh"
 #include "launch.h"
 
@@ -9,7 +9,13 @@ namespace fp4 {
 
 cudaError_t launch_slab_moe(int mode, const GemvParams& p, const LaunchCfg& cfg) {
   if (p.cw != kSlabMaxCW) return cudaErrorInvalidValue;  // 128-row tiles
-  static int configured_up[64], configured_down[64];     // per device (0 = not yet)
+  static int configured_up[64], configured_grouped[64], configured_down[64];  // per device (0 = not yet)
+  if (mode == kMoeGateUp && p.tiles_per_cta > 0) {  // the grouped form
+    if (cfg.cluster != 1) return cudaErrorInvalidValue;
+    cudaError_t e = configure_kernel(gemv_slab_kernel<2, kMoeGateUp, true>, configured_grouped, cfg.smem, 1);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(gemv_slab_kernel<2, kMoeGateUp, true>, (p.cw + 1) * 32, p, cfg);
+  }
   if (mode == kMoeGateUp) {
     cudaError_t e = configure_kernel(gemv_slab_kernel<2, kMoeGateUp>, configured_up, cfg.smem, cfg.cluster);
     if (e != cudaSuccess) return e;
@@ -24,11 +30,17 @@ cudaError_t launch_slab_moe(int mode, const GemvParams& p, const LaunchCfg& cfg)
   return cudaErrorInvalidValue;
 }
 
+// (gate_up: the larger of its two forms)
 cudaError_t slab_moe_regs(int mode, int* regs) {
-  cudaFuncAttributes a;
-  cudaError_t e = mode == kMoeGateUp   ? cudaFuncGetAttributes(&a, gemv_slab_kernel<2, kMoeGateUp>)
-                  : mode == kMoeDown ? cudaFuncGetAttributes(&a, gemv_slab_kernel<2, kMoeDown>)
-                                     : cudaErrorInvalidValue;
+  cudaFuncAttributes a, b;
+  cudaError_t e = cudaErrorInvalidValue;
+  if (mode == kMoeGateUp) {
+    e = cudaFuncGetAttributes(&a, gemv_slab_kernel<2, kMoeGateUp>);
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&b, gemv_slab_kernel<2, kMoeGateUp, true>);
+    if (e == cudaSuccess && b.numRegs > a.numRegs) a.numRegs = b.numRegs;
+  } else if (mode == kMoeDown) {
+    e = cudaFuncGetAttributes(&a, gemv_slab_kernel<2, kMoeDown>);
+  }
   if (e == cudaSuccess) *regs = a.numRegs;
   return e;
 }

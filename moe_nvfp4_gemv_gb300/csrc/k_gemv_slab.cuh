@@ -66,7 +66,8 @@ __device__ __forceinline__ bool bf16x8_to_f16x8_exact(const uint4& v, uint4& o) 
 // whole K, and after each tile writes the
 // tile's y rows, arrives on the tile's counter and, when it arrives last,
 // combines the tile's outputs).
-template <int kR, int kMode = kDenseFp4>
+// kGroupedUp: gate_up in the grouped form (see below; down_combine always).
+template <int kR, int kMode = kDenseFp4, bool kGroupedUp = false>
 __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel(const __grid_constant__ GemvParams p) {
   using C = SlabCfg<kR>;
   constexpr int kChains = C::kChains;
@@ -163,33 +164,48 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
   const int M = kDense ? p.M : (s_mwork.active ? s_mwork.ntok : 0);
   const int klen = wk.k_end - wk.k_begin;
   const int nst_tile = (klen + 255) / 256;  // stages per row tile (and activation stages in the slab)
-  // down_combine: the CTA's row tiles tile0 .. tile0 + ntl - 1
-  const int tiles_h = (p.n_out + 127) / 128;
-  const int tile0 = kDown ? static_cast<int>(blockIdx.x * tiles_h / gridDim.x) : 0;
-  const int ntl = kDown ? static_cast<int>((blockIdx.x + 1) * tiles_h / gridDim.x) - tile0 : 1;
-  // The CTAs of a tile group take its tiles in rotated orders (column y
-  // starts at tile y mod ntl), so their arrivals on one tile's counter are
-  // spread over the group's run instead of meeting at once.
-  const int rot = kDown ? static_cast<int>(blockIdx.y % static_cast<unsigned>(ntl)) : 0;
-  auto tile_of = [&](int tt) { return tt + rot < ntl ? tt + rot : tt + rot - ntl; };  // CTA-relative tile
-  if constexpr (kDown) {
-    wk.wrow[0] = (wk.shared ? 0 : wk.expert * p.rows_per_expert) + tile0 * 128;
-    wk.srow[0] = tile0 * 128;
-    wk.sgroup[0] = tile0;
-  }
-  const int nst = M > 0 ? ntl * nst_tile : 0;
-  if constexpr (kDown) {
-    if (M == 0) return;  // (uniform: no barrier, copy or arrival of this CTA is pending)
-  }
+  // Tile groups (down_combine always; gate_up in the grouped form, with the
+  // whole H per CTA): CTA column x takes the
+  // tiles [x tiles / gridDim.x, (x + 1) tiles / gridDim.x) of its column's
+  // weight in turn over one resident activation slab: 128-row tiles of H
+  // (down_combine), [up; gate] groups of 64 features (routed gate_up) or
+  // pairs of 64-row gate and up boxes (shared gate_up).
+  constexpr bool grouped = kDown || (kMode == kMoeGateUp && kGroupedUp);
+  const int tiles_h = kDown ? (p.n_out + 127) / 128
+                            : (wk.shared ? (p.shared_n_out + 63) / 64 : p.n_out / 64);
+  const int tile0 = grouped ? static_cast<int>(blockIdx.x * tiles_h / gridDim.x) : 0;
+  const int ntl = grouped ? static_cast<int>((blockIdx.x + 1) * tiles_h / gridDim.x) - tile0 : 1;
+  // down_combine: the CTAs of a tile group take its tiles in rotated orders
+  // (column y starts at tile y mod ntl), so their arrivals on one tile's
+  // counter are spread over the group's run instead of meeting at once.
+  const int rot = kDown && ntl > 0 ? static_cast<int>(blockIdx.y % static_cast<unsigned>(ntl)) : 0;
+  auto tile_of = [&](int tt) { return tile0 + (tt + rot < ntl ? tt + rot : tt + rot - ntl); };  // tile index
+  // The weight boxes of tile t (grouped modes).
+  auto box_for_tile = [&](RfWork& w, int t) {
+    if (kDown || !w.shared) {
+      w.wrow[0] = (w.shared ? 0 : w.expert * p.rows_per_expert) + t * 128;
+      w.srow[0] = t * 128;
+      w.sgroup[0] = t;
+    } else {
+      const int groups_total = (p.rows_w + 127) / 128;
+      rf_box(w, 0, t * 64, 64, groups_total);                 // gate rows
+      rf_box(w, 1, p.n_half + t * 64, 64, groups_total);      // up rows
+    }
+  };
+  if (grouped && ntl > 0) box_for_tile(wk, tile_of(0));
+  const int nst = M > 0 && ntl > 0 ? ntl * nst_tile : 0;
+  if (grouped && nst == 0) return;  // (uniform: no barrier, copy or arrival of this CTA is pending)
   const uint32_t slab_stage = static_cast<uint32_t>(M) * 512u;  // bytes of one stage's activations
   const uint64_t pol_w = policy_evict_first();
   auto issue_weights = [&](int s, int slot) {
     const uint32_t st = ring + slot * p.stage_bytes;
     const uint32_t fb = smem_u32(&bar_full[slot]);
-    int tt = 0, ks = s;  // row tile (down_combine) and K stage
-    if constexpr (kDown) {
+    int tt = 0, ks = s;  // row tile (grouped modes) and K stage
+    RfWork bw = wk;
+    if constexpr (grouped) {
       tt = s / nst_tile;
       ks = s - tt * nst_tile;
+      box_for_tile(bw, tile_of(tt));
     }
     const int k0 = wk.k_begin + ks * 256;
     const int nchunks = min(256, wk.k_end - k0) / kSubK;
@@ -198,15 +214,15 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
         wk.shared ? p.sf2 : p.sf + (wk.expert >= 0 ? static_cast<size_t>(wk.expert) * p.sf_expert_bytes : 0);
     uint32_t bytes = trows * 128;
 #pragma unroll
-    for (int g = 0; g < 4; ++g) bytes += (wk.sgroup[g] >= 0 ? nchunks * 512 : 0);
+    for (int g = 0; g < 4; ++g) bytes += (bw.sgroup[g] >= 0 ? nchunks * 512 : 0);
     mbar_arrive_expect_tx(fb, bytes);
-    tma_load_2d(st, tmw, k0 / 2, wk.wrow[0] + tile_of(tt) * 128, fb, pol_w);
-    if (wk.paired) tma_load_2d(st + trows * 64, tmw, k0 / 2, wk.wrow[1], fb, pol_w);
+    tma_load_2d(st, tmw, k0 / 2, bw.wrow[0], fb, pol_w);
+    if (bw.paired) tma_load_2d(st + trows * 64, tmw, k0 / 2, bw.wrow[1], fb, pol_w);
     uint32_t sdst = st + trows * 128;  // the valid groups, in order
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
-      if (wk.sgroup[g] < 0) continue;
-      const size_t chunk = static_cast<size_t>(wk.sgroup[g] + tile_of(tt)) * (wk.kbp / 4) + k0 / 64;
+      if (bw.sgroup[g] < 0) continue;
+      const size_t chunk = static_cast<size_t>(bw.sgroup[g]) * (wk.kbp / 4) + k0 / 64;
       bulk_load(sdst, sfb + chunk * 512, nchunks * 512, fb, pol_w);
       sdst += 2048;
     }
@@ -321,20 +337,23 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
     // = row % 8, the same for every row of the thread) and of their scales
     uint32_t w_off[kR][2], sf_off[kR][2];
     const uint32_t key = static_cast<uint32_t>(sg);
+    auto set_offsets = [&](const RfWork& w) {
 #pragma unroll
-    for (int b = 0; b < kR; ++b) {
+      for (int b = 0; b < kR; ++b) {
 #pragma unroll
-      for (int hr = 0; hr < 2; ++hr) {
-        const int row = (warp * kR + b) * 16 + sg + 8 * hr;
-        w_off[b][hr] = (row / 8) * 1024 + (row % 8) * 128;
-        const int half = trows / 2;
-        const bool b1 = wk.paired && row >= half;
-        const int r = (b1 ? wk.srow[1] : wk.srow[0]) + (b1 ? row - half : row);
-        const int gr = r / 128;
-        const int gslot = b1 ? (wk.sgroup[0] >= 0) + (wk.sgroup[1] >= 0) + (gr != wk.sgroup[2]) : (gr != wk.sgroup[0]);
-        sf_off[b][hr] = trows * 128 + gslot * 2048 + (r % 32) * 16 + ((r % 128) / 32) * 4;
+        for (int hr = 0; hr < 2; ++hr) {
+          const int row = (warp * kR + b) * 16 + sg + 8 * hr;
+          w_off[b][hr] = (row / 8) * 1024 + (row % 8) * 128;
+          const int half = trows / 2;
+          const bool b1 = w.paired && row >= half;
+          const int r = (b1 ? w.srow[1] : w.srow[0]) + (b1 ? row - half : row);
+          const int gr = r / 128;
+          const int gslot = b1 ? (w.sgroup[0] >= 0) + (w.sgroup[1] >= 0) + (gr != w.sgroup[2]) : (gr != w.sgroup[0]);
+          sf_off[b][hr] = trows * 128 + gslot * 2048 + (r % 32) * 16 + ((r % 128) / 32) * 4;
+        }
       }
-    }
+    };
+    set_offsets(wk);
     // One 128-K half of a stage, f16 route.  `cvalid` false (a chunk past
     // the end of a ragged last stage) gives zero A registers: that chunk's
     // scales were not copied and may hold anything.
@@ -409,80 +428,142 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
         }
       }
     };
-    // down_combine, after a row tile's last stage: the tile's y rows (y_j =
-    // bf16(acc * alpha2[e]) into the workspace, or y_shared = bf16(acc *
-    // gssd)), then one arrival on the tile's counter, tagged with this
-    // call's epoch; the CTA that arrives last combines the tile:
-    // out[t] = bf16(bf16(sum_j tw[t, j] * y[t, j]) + y_shared[t]).
-    // Every consumer warp calls it for the same tiles, also after a wait ran
-    // out (the first barrier agrees on the abort, which skips the tile's
-    // writes and arrival: its outputs stay unwritten); returns the abort.
+    // After a tile's last stage (grouped modes).  Every consumer warp calls
+    // it for the same tiles, also after a wait ran out (the first barrier
+    // agrees on the abort, which skips the tile's writes and arrival: its
+    // outputs stay unwritten); returns the abort.  The accumulators restart.
+    //   down_combine: the tile's y rows (y_j = bf16(acc * alpha2[e]) into
+    //     the workspace, or y_shared = bf16(acc * gssd)), then one arrival on
+    //     the tile's counter, tagged with this call's epoch; the CTA that
+    //     arrives last combines the tile:
+    //     out[t] = bf16(bf16(sum_j tw[t, j] * y[t, j]) + y_shared[t]).
+    //   gate_up: the tile's sums staged in shared memory (row-major per B
+    //     row), then the 64 features' outputs as in the split epilogue.
     auto tile_done = [&](int tt) -> bool {
       const bool ab = bar_red_or<1>(ncons, s_abort != 0);
-      const int h0 = (tile0 + tile_of(tt)) * 128;
-      if (!ab) {
-        const float post = static_cast<float>(1 << kShift);
-        const float sc = wk.shared ? __ldg(p.gs) : __ldg(p.alpha + wk.expert);
-        uint16_t* dst = wk.shared ? p.out2 : p.out;
-        const int64_t ld = wk.shared ? p.ldo2 : p.ldo;
+      const int t = tile_of(tt);
+      const float post = static_cast<float>(1 << kShift);
+      float v[kR][2][2];  // this thread's sums: row block, row half, token
 #pragma unroll
-        for (int b = 0; b < kR; ++b) {
+      for (int b = 0; b < kR; ++b) {
 #pragma unroll
-          for (int hr = 0; hr < 2; ++hr) {
-            const int h = h0 + (warp * kR + b) * 16 + sg + 8 * hr;
+        for (int hr = 0; hr < 2; ++hr) {
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int n = 2 * c + e;
-              float v = accb[b][2 * hr + e] * post;
-              accb[b][2 * hr + e] = 0.0f;
+          for (int e = 0; e < 2; ++e) {
+            float a = accb[b][2 * hr + e] * post;
+            accb[b][2 * hr + e] = 0.0f;
 #pragma unroll
-              for (int q = 0; q < kChains; ++q) {
-                v += acc[q][b][2 * hr + e];
-                acc[q][b][2 * hr + e] = 0.0f;
-              }
-              if (n < M && h < p.n_out) dst[static_cast<int64_t>(s_mwork.orow[n]) * ld + h] = f32_to_bf16_rn(v * sc);
+            for (int q = 0; q < kChains; ++q) {
+              a += acc[q][b][2 * hr + e];
+              acc[q][b][2 * hr + e] = 0.0f;
             }
+            v[b][hr][e] = a;
           }
         }
       }
-      cons_sync(ncons);  // this CTA's y rows of the tile are written
-      if (tid == 0 && ab) s_last = 0;
-      if (tid == 0 && !ab) {
-        __threadfence();
-        unsigned long long* ctr = p.counters + tile0 + tile_of(tt);
-        const unsigned long long tag = static_cast<unsigned long long>(p.epoch) << 32;
-        unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(ctr), next;
-        for (;;) {
-          next = ((old & 0xFFFFFFFF00000000ull) == tag) ? old + 1 : tag + 1;
-          const unsigned long long seen = atomicCAS(ctr, old, next);
-          if (seen == old) break;
-          old = seen;
+      if constexpr (kDown) {
+        const int h0 = t * 128;
+        if (!ab) {
+          const float sc = wk.shared ? __ldg(p.gs) : __ldg(p.alpha + wk.expert);
+          uint16_t* dst = wk.shared ? p.out2 : p.out;
+          const int64_t ld = wk.shared ? p.ldo2 : p.ldo;
+#pragma unroll
+          for (int b = 0; b < kR; ++b) {
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+              const int h = h0 + (warp * kR + b) * 16 + sg + 8 * hr;
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int n = 2 * c + e;
+                if (n < M && h < p.n_out)
+                  dst[static_cast<int64_t>(s_mwork.orow[n]) * ld + h] = f32_to_bf16_rn(v[b][hr][e] * sc);
+              }
+            }
+          }
         }
-        s_last = static_cast<int>(static_cast<uint32_t>(next)) == s_target;
-        if (s_last) atomicExch(ctr, 0ull);
-        __threadfence();
-      }
-      cons_sync(ncons);
-      if (s_last) {
-        moe_combine_tile(p, h0, tid, ncons);
+        cons_sync(ncons);  // this CTA's y rows of the tile are written
+        if (tid == 0 && ab) s_last = 0;
+        if (tid == 0 && !ab) {
+          __threadfence();
+          unsigned long long* ctr = p.counters + t;
+          const unsigned long long tag = static_cast<unsigned long long>(p.epoch) << 32;
+          unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(ctr), next;
+          for (;;) {
+            next = ((old & 0xFFFFFFFF00000000ull) == tag) ? old + 1 : tag + 1;
+            const unsigned long long seen = atomicCAS(ctr, old, next);
+            if (seen == old) break;
+            old = seen;
+          }
+          s_last = static_cast<int>(static_cast<uint32_t>(next)) == s_target;
+          if (s_last) atomicExch(ctr, 0ull);
+          __threadfence();
+        }
+        cons_sync(ncons);
+        if (s_last) moe_combine_tile(p, h0, tid, ncons);
+      } else {
+        if (!ab) {
+#pragma unroll
+          for (int b = 0; b < kR; ++b) {
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+              const int row = (warp * kR + b) * 16 + sg + 8 * hr;
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int n = 2 * c + e;
+                if (n < M) stsf(inbox + (n * 128 + row) * 4, v[b][hr][e]);
+              }
+            }
+          }
+        }
+        cons_sync(ncons);
+        if (!ab) {
+          if (!wk.shared) {
+            // routed [up; gate] group: feature o = up row o, gate row o + 64
+            const float al = __ldg(p.alpha + wk.expert);
+            for (int it = tid; it < 64 * M; it += ncons) {
+              const int n = it / 64, lr = it % 64;
+              const int feat = t * 64 + lr;
+              if (feat >= p.n_out) continue;
+              const float uu = ldsf(inbox + (n * 128 + lr) * 4) * al;
+              const float gt = ldsf(inbox + (n * 128 + 64 + lr) * 4) * al;
+              p.out[static_cast<int64_t>(s_mwork.orow[n]) * p.ldo + feat] = f32_to_bf16_rn(silu_fast(gt) * uu);
+            }
+          } else {
+            // shared expert: feature o = gate row o, up row o + 64
+            const float gs = __ldg(p.gs);
+            for (int it = tid; it < 64 * M; it += ncons) {
+              const int n = it / 64, lr = it % 64;
+              const int feat = t * 64 + lr;
+              if (feat >= p.shared_n_out) continue;
+              const float G = bf16_to_f32(f32_to_bf16_rn(ldsf(inbox + (n * 128 + lr) * 4) * gs));
+              const float U = bf16_to_f32(f32_to_bf16_rn(ldsf(inbox + (n * 128 + 64 + lr) * 4) * gs));
+              p.out2[static_cast<int64_t>(s_mwork.orow[n]) * p.ldo2 + feat] = f32_to_bf16_rn(silu_exact(G) * U);
+            }
+          }
+        }
       }
       return ab;
     };
     for (int s = 0, slot = 0, ph = 0; s < nst; ++s, slot = slot + 1 == nstages ? 0 : slot + 1, ph ^= slot == 0) {
       const uint32_t st = ring + slot * p.stage_bytes;
-      const int tt = kDown ? s / nst_tile : 0;  // row tile (down_combine)
-      const int ks = s - tt * nst_tile;         // K stage
+      const int tt = grouped ? s / nst_tile : 0;  // tile (grouped modes)
+      const int ks = s - tt * nst_tile;           // K stage
       const uint32_t xs = slab + ks * slab_stage;
+      if (grouped && ks == 0 && tt > 0) {
+        // (the scale offsets of shared gate_up boxes move with the tile)
+        RfWork tw = wk;
+        box_for_tile(tw, tile_of(tt));
+        set_offsets(tw);
+      }
       const bool ok = __all_sync(0xFFFFFFFFu, !s_abort && mbar_wait(smem_u32(&bar_full[slot]), ph, p.err));
       if (!ok) {
         s_abort = 1;
-        if constexpr (kDown) {
+        if constexpr (grouped) {
           // (the slot is not released: its copy may still land)
           if (ks == nst_tile - 1 && tile_done(tt)) break;
           continue;
-        } else {
-          break;
         }
+        break;
       }
       // valid K of the stage: 64 .. 256 in steps of 64; a chunk (32 K) is
       // wholly valid or wholly past the end
@@ -503,16 +584,14 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bar_empty[slot]));
-      if constexpr (kDown) {
-        if (ks == nst_tile - 1 && tile_done(tt)) break;
-      }
+      if (grouped && ks == nst_tile - 1 && tile_done(tt)) break;
     }
   }
 
   // ==================================================================== epilogue
   __syncwarp();
-  if (kDown) {
-    // (down_combine finished each tile inside the loop)
+  if constexpr (grouped) {
+    // (grouped modes finished each tile inside the loop)
   } else if (warp < cw) {
     const float post = static_cast<float>(1 << kShift);
     // Push this thread's partials (its rows, tokens 2c + {0,1} below M) to

@@ -241,20 +241,28 @@ def test_workspace_reuse_across_shapes(fp4):
         assert_close(u16(out), ref, f"workspace reuse M={M}")
 
 
-def _moe_slab_split(fp4, M, topk, E, H, I, SI):
-    """Split of the slab kernel's plan for this gate_up call on this GPU
-    (None: the call runs on the register-fed kernel)."""
+def _moe_slab_plan(fp4, M, topk, E, H, I, SI):
+    """The slab kernel's gate_up plan for this call on this GPU as (split,
+    tiles per CTA; 0 in the split form), or None when the call runs on
+    another kernel."""
     import ctypes
 
     class Plan(ctypes.Structure):
-        _fields_ = [(n, ctypes.c_int) for n in ("split", "k_slab", "chunk_pairs", "columns", "tiles", "slab_bytes",
-                                                "stage_bytes")] + [("smem_bytes", ctypes.c_size_t)]
+        _fields_ = [(n, ctypes.c_int) for n in ("split", "k_slab", "tiles_per_cta", "groups", "chunk_pairs",
+                                                "columns", "tiles", "slab_bytes", "stage_bytes", "stages",
+                                                "ctas_per_sm")] + [("smem_bytes", ctypes.c_size_t)]
     f = fp4.lib().fp4gemv_plan_moe_slab
     f.restype = ctypes.c_int
     f.argtypes = [ctypes.c_int] * 8 + [ctypes.POINTER(Plan)]
     out = Plan()
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    return out.split if f(M, topk, E, H, I, SI, sms, 125, ctypes.byref(out)) == 0 else None
+    return (out.split, out.tiles_per_cta) if f(M, topk, E, H, I, SI, sms, 125, ctypes.byref(out)) == 0 else None
+
+
+def _moe_slab_split(fp4, M, topk, E, H, I, SI):
+    """Split of the slab kernel's split-form plan (None otherwise)."""
+    plan = _moe_slab_plan(fp4, M, topk, E, H, I, SI)
+    return plan[0] if plan is not None and plan[1] == 0 else None
 
 
 # gate_up on the slab kernel (routed chunks of up to 4 pairs of one expert,
@@ -324,10 +332,10 @@ def _down_slab_tiles(fp4, M, topk, E, H, I, SI):
     return out.tiles_per_cta if f(M, topk, E, H, I, SI, sms, 128, ctypes.byref(out)) == 0 else None
 
 
-# down_combine on the slab kernel with several row tiles per CTA: H = 832 is
-# 6.5 tiles (a partial last tile) in groups of one or two tiles;
-# many experts, so most columns are inactive duplicates that leave at once
-# and the combine waits only for the CTAs that compute.
+# down_combine on the slab kernel with two row tiles per CTA: H = 832 is
+# 6.5 tiles (a partial last tile, and a last group of one tile); many
+# experts, so many columns are inactive duplicates that leave at once and
+# the combine waits only for the CTAs that compute.
 @pytest.mark.parametrize("M,topk,E,H,I,SI,T", [(16, 8, 128, 832, 256, 256, 2), (12, 8, 96, 1024, 320, 448, 2)])
 def test_down_combine_slab_tiles(fp4, M, topk, E, H, I, SI, T):
     assert _down_slab_tiles(fp4, M, topk, E, H, I, SI) == T
@@ -342,14 +350,35 @@ def test_down_combine_slab_tiles(fp4, M, topk, E, H, I, SI, T):
 
 
 def test_down_combine_slab_decode_block(fp4):
-    # 8 tokens of the E = 128, top-8, H = 4096, I = SI = 1536 block: five or
-    # six row tiles per CTA; sampled tokens against the oracle
+    # 8 tokens of the E = 128, top-8, H = 4096, I = SI = 1536 block: two row
+    # tiles per CTA; sampled tokens against the oracle
     c = synth.MOE
-    assert _down_slab_tiles(fp4, 8, c["topk"], c["E"], c["H"], c["I"], c["SI"]) == 6
+    assert _down_slab_tiles(fp4, 8, c["topk"], c["E"], c["H"], c["I"], c["SI"]) == 2
     d = make_moe(8, c["E"], c["H"], c["I"], c["SI"], c["topk"], seed=101)
     out = run_down(fp4, d)
     tokens = [0, 3, 7]
     ref, bad = ref_down(d, tokens=tokens)
     assert bad == 0
     assert_close(u16(out)[tokens], tuple(r[tokens] for r in ref), "down slab decode block M=8")
+    assert fp4.get_device_error() == 0
+
+
+# gate_up in the grouped form (the whole H per CTA, several tiles per CTA in
+# turn): routed and shared tiles split unevenly over the groups, shared-
+# expert boxes that alternate between the halves of their 128-row scale
+# groups; then crowded experts (8 experts x 4 pairs: chunks of 4).
+@pytest.mark.parametrize("M,topk,E,H,I,SI,ids", [
+    (6, 8, 64, 512, 1024, 960, None),
+    (4, 8, 16, 1024, 2048, 448, [[0, 1, 2, 3, 4, 5, 6, 7]] * 4),
+])
+def test_gate_up_slab_grouped(fp4, M, topk, E, H, I, SI, ids):
+    plan = _moe_slab_plan(fp4, M, topk, E, H, I, SI)
+    assert plan is not None and plan[0] == 1 and plan[1] >= 2
+    d = make_moe(M, E=E, H=H, I=I, SI=SI, topk=topk, seed=900 + M,
+                 ids=None if ids is None else torch.tensor(ids, dtype=torch.int32))
+    act, sact = run_gate_up(fp4, d)
+    (an, al, ah), (sn, sl, sh), bad = ref_gate_up(d)
+    assert bad == 0
+    assert_close(u16(act), (an, al, ah), f"act grouped M={M}")
+    assert_close(u16(sact), (sn, sl, sh), f"sact grouped M={M}")
     assert fp4.get_device_error() == 0

@@ -287,8 +287,9 @@ def test_slab_plan_rejects_bad_arguments(slab_fn):
 # --- the slab kernel's MoE gate_up plan, host only ----------------------------------------
 
 class MoeSlabPlan(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_int) for n in ("split", "k_slab", "chunk_pairs", "columns", "tiles", "slab_bytes",
-                                            "stage_bytes")] + [("smem_bytes", ctypes.c_size_t)]
+    _fields_ = [(n, ctypes.c_int) for n in ("split", "k_slab", "tiles_per_cta", "groups", "chunk_pairs", "columns",
+                                            "tiles", "slab_bytes", "stage_bytes", "stages", "ctas_per_sm")] + \
+        [("smem_bytes", ctypes.c_size_t)]
 
 
 @pytest.fixture(scope="module")
@@ -305,17 +306,24 @@ def moe_slab_fn():
 
 
 def moe_slab_rule(M, topk, E, H, I, SI, sms=SMS):
-    """The rule written out: chunks of <= 4 pairs; the routed columns that
-    can be active (min(P, E)) and the shared expert's ceil(M / 4) chunks, in
-    128-row tiles, fit one wave at three CTAs per SM with the largest split
-    whose ranks keep >= 256 of H; a CTA's slab (min(P, 4) rows of its H range,
-    bf16) and two 20 KB stages fit a third of 228 KB."""
+    """The rule written out.  Split form: chunks of <= 4 pairs; the routed
+    columns that can be active (min(P, E)) and the shared expert's ceil(M / 4)
+    chunks, in 128-row tiles, fit one wave at three CTAs per SM with the
+    largest split whose ranks keep >= 256 of H; a CTA's slab (min(P, 4) rows of
+    its H range, bf16) and two 20 KB stages fit a third of 228 KB.  Grouped
+    form (M <= 64): the whole H, T = 1 tile per CTA up to 2 tokens else 2;
+    chunks of 1 (M <= 2), 2 (M < 32) or 4 pairs, halved while fewer than two
+    20 KB stages fit; three CTAs per SM, two from 32 tokens; as many stages
+    as fit (<= 8, <= T stages of H)."""
+    if M > 64:
+        return None
     P = M * topk
-    tiles = min(P, E) * (I // 64) + -(-M // 4) * -(-SI // 64)
+    tiles = max(I // 64, -(-SI // 64))
+    ctas1 = min(P, E) * (I // 64) + -(-M // 4) * -(-SI // 64)
     rows = min(P, 4)
     dyn = 228 * 1024 // 3 - 2048
     for S in (8, 4, 2, 1):
-        if tiles * S > 3 * sms:
+        if ctas1 * S > 3 * sms:
             continue
         kslab = -(-(-(-H // S)) // 64) * 64
         if S > 1 and (kslab < 256 or (S - 1) * kslab >= H):
@@ -323,15 +331,30 @@ def moe_slab_rule(M, topk, E, H, I, SI, sms=SMS):
         slab = -(-(rows * -(-kslab // 256) * 512) // 1024) * 1024
         smem = 1024 + slab + 2 * 20480 + 8 * 144 * 4
         if smem > dyn:
-            return None
-        return dict(split=-(-H // kslab), k_slab=kslab, slab_bytes=slab, smem_bytes=smem)
+            break
+        return dict(split=-(-H // kslab), k_slab=kslab, tiles_per_cta=0, groups=tiles * -(-H // kslab),
+                    chunk_pairs=4, slab_bytes=slab, stages=2, ctas_per_sm=3, smem_bytes=smem)
+    nst = -(-H // 256)
+    occ = 2 if M >= 32 else 3
+    T = 1 if M <= 2 else 2
+    chunk = 4 if M >= 32 else 1 if M <= 2 else 2
+    while chunk >= 1:
+        rows = min(P, chunk)
+        slab = -(-(rows * nst * 512) // 1024) * 1024
+        ns = min(8, (228 * 1024 // occ - 2048 - 1024 - slab - 8 * 144 * 4) // 20480, T * nst)
+        if ns >= 2:
+            return dict(split=1, k_slab=H, tiles_per_cta=T, groups=-(-tiles // T), chunk_pairs=chunk, slab_bytes=slab,
+                        stages=ns, ctas_per_sm=occ, smem_bytes=1024 + slab + ns * 20480 + 8 * 144 * 4)
+        chunk //= 2
     return None
 
 
 @pytest.mark.parametrize("M,topk,E,H,I,SI", [(1, 8, 128, 4096, 1536, 1536), (2, 8, 128, 4096, 1536, 1536),
-                                             (8, 8, 128, 4096, 1536, 1536), (1, 2, 8, 512, 256, 384),
-                                             (3, 2, 8, 1024, 256, 384), (2, 4, 4, 2048, 256, 256),
-                                             (1, 1, 2, 256, 64, 64), (4, 8, 16, 8192, 512, 512)])
+                                             (8, 8, 128, 4096, 1536, 1536), (32, 8, 128, 4096, 1536, 1536),
+                                             (64, 8, 128, 4096, 1536, 1536), (65, 8, 128, 4096, 1536, 1536),
+                                             (1, 2, 8, 512, 256, 384), (3, 2, 8, 1024, 256, 384),
+                                             (2, 4, 4, 2048, 256, 256), (1, 1, 2, 256, 64, 64),
+                                             (4, 8, 16, 8192, 512, 512), (16, 8, 64, 16384, 512, 512)])
 def test_moe_slab_plan_matches_rule(moe_slab_fn, M, topk, E, H, I, SI):
     st, p = moe_slab_fn(M, topk, E, H, I, SI)
     want = moe_slab_rule(M, topk, E, H, I, SI)
@@ -339,20 +362,23 @@ def test_moe_slab_plan_matches_rule(moe_slab_fn, M, topk, E, H, I, SI):
         assert st == 2
         return
     assert st == 0
-    got = dict(split=p.split, k_slab=p.k_slab, slab_bytes=p.slab_bytes, smem_bytes=p.smem_bytes)
+    got = dict(split=p.split, k_slab=p.k_slab, tiles_per_cta=p.tiles_per_cta, groups=p.groups,
+               chunk_pairs=p.chunk_pairs, slab_bytes=p.slab_bytes, stages=p.stages, ctas_per_sm=p.ctas_per_sm,
+               smem_bytes=p.smem_bytes)
     assert got == want
-    assert (p.chunk_pairs, p.stage_bytes) == (4, 20480)
-    assert p.columns == M * topk + -(-M // 4) and p.tiles == max(I // 64, -(-SI // 64))
-    assert (p.split - 1) * p.k_slab < H and p.slab_bytes >= min(M * topk, 4) * p.k_slab * 2
+    assert p.stage_bytes == 20480 and p.columns == M * topk + -(-M // p.chunk_pairs)
+    assert p.tiles == max(I // 64, -(-SI // 64))
+    assert (p.split - 1) * p.k_slab < H and p.slab_bytes >= min(M * topk, p.chunk_pairs) * p.k_slab * 2
 
 
 def test_moe_slab_plan_decode_block(moe_slab_fn):
     # one token of the E = 128, top-8, H = 4096, I = SI = 1536 block: 9 columns
-    # x 24 tiles split in two (432 CTAs, one wave at three per SM); two tokens
-    # (17 x 24 = 408 tiles) would need the whole H per CTA, whose slab does not fit
+    # x 24 tiles split in two (432 CTAs, one wave at three per SM); 8 tokens
+    # (~53 experts): the grouped form, pairs of 2, 12 groups of 2 tiles
     st, p = moe_slab_fn(1, 8, 128, 4096, 1536, 1536)
-    assert st == 0 and (p.split, p.k_slab, p.columns, p.tiles) == (2, 2048, 9, 24)
-    assert moe_slab_fn(2, 8, 128, 4096, 1536, 1536)[0] == 2
+    assert st == 0 and (p.split, p.k_slab, p.tiles_per_cta, p.columns, p.tiles) == (2, 2048, 0, 9, 24)
+    st, p = moe_slab_fn(8, 8, 128, 4096, 1536, 1536)
+    assert st == 0 and (p.split, p.tiles_per_cta, p.groups, p.chunk_pairs) == (1, 2, 12, 2)
 
 
 def test_moe_slab_plan_rejects_bad_arguments(moe_slab_fn):
@@ -361,6 +387,7 @@ def test_moe_slab_plan_rejects_bad_arguments(moe_slab_fn):
     assert moe_slab_fn(1, 8, 128, 4096, 1536, 1536, sms=0)[0] == 1
     assert moe_slab_fn(1, 8, 128, 4000, 1536, 1536)[0] == 2   # H % 64
     assert moe_slab_fn(200, 8, 128, 4096, 1536, 1536)[0] == 2  # M * topk > 1024
+    assert moe_slab_fn(65, 8, 128, 4096, 1536, 1536)[0] == 2   # beyond 64 tokens: the tcgen05 kernel
 
 
 # --- the slab kernel's MoE down_combine plan, host only -----------------------------------
@@ -384,32 +411,20 @@ def down_slab_fn():
 
 
 def down_slab_rule(M, topk, E, H, I, SI, sms=SMS):
-    """The rule written out: M <= 64, E <= 256; from the expected distinct
-    experts E (1 - (1 - topk / E)^M) (at most P, at least 1): the chunk, the
-    power of two <= 8 covering P / distinct pairs; rows min(P, chunk) of
-    max(I, SI) bf16; T so the expected CTAs fill 80 % of three per SM; as many 18 KB
-    stages as fit beside the slab (2 .. 8, at most T routed tiles' stages), at
-    two CTAs per SM when the expected CTAs fit two per SM."""
-    if M > 64 or E > 256:
+    """The rule written out: 2 <= M <= 64, E <= 256; chunks of 8 pairs (rows
+    min(P, 8) of max(I, SI) bf16), two tiles per CTA, three CTAs per SM, as
+    many 18 KB stages as fit beside the slab within a third of 228 KB less
+    4 KB (2 .. 8, at most two tiles' stages of I)."""
+    if M < 2 or M > 64 or E > 256:
         return None
-    P = M * topk
-    pick = topk / E if topk < E else 1.0
-    distinct = max(min(E * (1.0 - (1.0 - pick) ** M), P), 1.0)
-    chunk = 1
-    while chunk < 8 and chunk < P / distinct:
-        chunk *= 2
-    rows = min(P, chunk)
+    rows = min(M * topk, 8)
     nst = -(-max(I, SI) // 256)
     slab = -(-(rows * nst * 512) // 1024) * 1024
-    tiles = -(-H // 128)
-    cols = distinct + -(-M // chunk)
-    groups = min(max(1, int(0.8 * 3 * sms / cols)), tiles)
-    T = -(-tiles // groups)
-    occ = 2 if cols * groups <= 2.0 * sms else 3
-    ns = min(8, (228 * 1024 // occ - 4096 - 1024 - slab) // 18432, T * -(-I // 256))
+    ns = min(8, (228 * 1024 // 3 - 4096 - 1024 - slab) // 18432, 2 * -(-I // 256))
     if ns < 2:
         return None
-    return dict(tiles_per_cta=T, groups=groups, chunk_pairs=chunk, slab_bytes=slab, stages=ns, ctas_per_sm=occ,
+    tiles = -(-H // 128)
+    return dict(tiles_per_cta=2, groups=-(-tiles // 2), chunk_pairs=8, slab_bytes=slab, stages=ns, ctas_per_sm=3,
                 smem_bytes=1024 + slab + ns * 18432)
 
 
@@ -437,13 +452,11 @@ def test_down_slab_plan_matches_rule(down_slab_fn, M, topk, E, H, I, SI):
 
 
 def test_down_slab_plan_decode_block(down_slab_fn):
-    # E = 128, top-8, H = 4096, I = SI = 1536: one token, one tile and one
-    # pair per CTA (9 columns x 32 tiles, two CTAs per SM, 5 of its 6 stages
-    # in the ring); 8 tokens (~53 experts), two pairs and six tiles per CTA
-    st, p = down_slab_fn(1, 8, 128, 4096, 1536, 1536)
-    assert st == 0 and (p.tiles_per_cta, p.chunk_pairs, p.ctas_per_sm, p.stages) == (1, 1, 2, 5)
+    # E = 128, top-8, H = 4096, I = SI = 1536: one token stays on the
+    # register-fed kernel; 8 tokens, chunks of 8 pairs and two tiles per CTA
+    assert down_slab_fn(1, 8, 128, 4096, 1536, 1536)[0] == 2
     st, p = down_slab_fn(8, 8, 128, 4096, 1536, 1536)
-    assert st == 0 and (p.tiles_per_cta, p.groups, p.chunk_pairs) == (6, 6, 2)  # 5 or 6 tiles each
+    assert st == 0 and (p.tiles_per_cta, p.groups, p.chunk_pairs, p.ctas_per_sm) == (2, 16, 8, 3)
 
 
 def test_down_slab_plan_rejects_bad_arguments(down_slab_fn):
