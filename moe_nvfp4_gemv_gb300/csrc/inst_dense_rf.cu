@@ -83,6 +83,7 @@ cudaError_t launch_rf_occ3(int mode, int nt, const GemvParams& p, const LaunchCf
 
 cudaError_t launch_rf_coop(int mode, int nt, const GemvParams& p, const LaunchCfg& cfg, KernelInfo* info) {
   if (mode == kDenseFp4 && nt == 8) return run_gemv_rf<kDenseFp4, 8, 2, true>(p, cfg, info);
+  if (mode == kDenseFp4 && nt == 16) return run_gemv_rf<kDenseFp4, 16, 2, true>(p, cfg, info);
   return cudaErrorInvalidValue;
 }
 

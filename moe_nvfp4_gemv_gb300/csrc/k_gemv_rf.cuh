@@ -39,8 +39,8 @@
 // barrier, so a consumer waits on one barrier per stage), checking that every
 // value converts exactly; the stage then runs on f16 MMAs with the codes
 // converted by cvt.rn.f16x2.e2m1x2 (natural K order, half the ALU work of the
-// bf16 route).  The dense 3-8-token variant (kCoop) converts with all
-// consumer warps instead.  A stage with any value that is not exactly an f16 (|x| > 65504,
+// bf16 route).  The dense variant for 3-12 tokens (kCoop, 8- and 16-token
+// tiles) converts with all consumer warps instead.  A stage with any value that is not exactly an f16 (|x| > 65504,
 // too many low bits for the f16 subnormal grid, NaN) runs the bf16 route with
 // the original activations from global memory instead.  Both routes compute
 // exact products into fp32, so the choice changes no result beyond fp32
@@ -172,13 +172,16 @@ __device__ __forceinline__ void copy_work(const Work& m, RfWork& w) {
 // kOcc: CTAs per SM the registers are budgeted for.  2 by default; 3 (two
 // accumulator chains, 64 registers, the host gives it a 72 KB ring) for
 // grids of many short CTAs, whose fixed costs more co-resident CTAs hide.
-// kCoop: the variant for 3 .. 8 tokens whose consumer warps convert the
-// activations to f16 together (a separate instantiation, so the others'
+// kCoop: the dense variant for 3 .. 12 tokens whose consumer warps convert
+// the activations to f16 together (a separate instantiation, so the others'
 // code is unchanged by it).
 template <int kMode, int kNT, int kOcc = 2, bool kCoop = false>
 __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, kOcc) gemv_rf_kernel(const __grid_constant__ GemvParams p) {
   using C = RfCfg<kNT>;
   constexpr int kChains = kOcc >= 3 && C::kChains > 2 ? 2 : C::kChains;
+  // f16-route code: the 8-token tile (converter warp or cooperative) and the
+  // cooperative variants of larger tiles
+  constexpr bool kF16 = C::kHasF16 || kCoop;
   constexpr bool kDense = kMode == kDenseFp4;
   constexpr int kEpiThreads = C::kConsumerWarps * 32;
 
@@ -329,14 +332,14 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, kOcc) gemv_rf_kernel(con
   const int rpf = rpf_of();  // rows per feature
   const int mine = max(0, f_hi - f_lo) * rpf;
   const bool f16route = !kCoop && C::kHasF16 && ntok <= C::kF16MaxM;  // converter-warp f16 route
-  // kF16MaxM < ntok <= 8: the consumer warps convert each stage's activations
-  // to f16 together (one 16-byte chunk or two per thread) and agree on
-  // exactness at a barrier; one converter warp would not keep up with 8 rows.
-  const bool coop = kCoop && C::kHasF16;  // (the host launches this variant from 3 tokens)
+  // kF16MaxM < ntok <= 12: the consumer warps convert each stage's
+  // activations to f16 together (one to three 16-byte chunks per thread) and
+  // agree on exactness at a barrier; one converter warp would not keep up.
+  const bool coop = kCoop;  // (the host launches this variant from 3 tokens)
   const bool f16acc = f16route || coop;  // acc holds exact f16-route products
 
   float acc[kChains][C::kTiles][4];  // main route's stages
-  float accb[C::kHasF16 ? C::kTiles : 1][4];  // f16 route: fallback stages (bf16, products times 2^-kShift)
+  float accb[kF16 ? C::kTiles : 1][4];  // f16 route: fallback stages (bf16, products times 2^-kShift)
 #pragma unroll
   for (int t = 0; t < C::kTiles; ++t) {
 #pragma unroll
@@ -346,7 +349,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, kOcc) gemv_rf_kernel(con
     }
   }
 #pragma unroll
-  for (int t = 0; t < (C::kHasF16 ? C::kTiles : 1); ++t) accb[t][0] = accb[t][1] = accb[t][2] = accb[t][3] = 0.0f;
+  for (int t = 0; t < (kF16 ? C::kTiles : 1); ++t) accb[t][0] = accb[t][1] = accb[t][2] = accb[t][3] = 0.0f;
   const int g = lane / 4, c = lane % 4;
   const int sg = (g % 2) * 4 + g / 2;  // sigma(g)
   const int row0 = warp * 16 + sg;     // tile rows of MMA rows g and g + 8
@@ -569,8 +572,8 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, kOcc) gemv_rf_kernel(con
         for (int t = 0; t < C::kTiles; ++t) {
           uint4 xv = make_uint4(0u, 0u, 0u, 0u);
           if (cvalid && xrow[t] != nullptr) xv = perm_x8(__ldg(reinterpret_cast<const uint4*>(xrow[t] + k0 + kk)));
-          mma_bf16_16816(accb[C::kHasF16 ? t : 0], r0[0], r1[0], r0[1], r1[1], xv.x, xv.y);
-          mma_bf16_16816(accb[C::kHasF16 ? t : 0], r0[2], r1[2], r0[3], r1[3], xv.z, xv.w);
+          mma_bf16_16816(accb[kF16 ? t : 0], r0[0], r1[0], r0[1], r1[1], xv.x, xv.y);
+          mma_bf16_16816(accb[kF16 ? t : 0], r0[2], r1[2], r0[3], r1[3], xv.z, xv.w);
         }
       }
     };
@@ -631,7 +634,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, kOcc) gemv_rf_kernel(con
             else half_bf16_smem(st, h, 32 * (4 * h + c) < kvalid);
           }
         }
-      } else if constexpr (C::kHasF16) {
+      } else if constexpr (kF16) {
         if (use_f16) {
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
@@ -685,7 +688,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, kOcc) gemv_rf_kernel(con
           // acc holds the main route's products (exact on the f16 route,
           // times 2^-kShift on the bf16 route); accb the f16 route's fallback
           if (!f16acc) a16 *= post;
-          if constexpr (C::kHasF16) a16 += accb[t][2 * hr + e] * post;
+          if constexpr (kF16) a16 += accb[t][2 * hr + e] * post;
           const float v = go ? a16 : 0.0f;
           const uint32_t off = n * rows_owner * 4;
           if (n >= ntok) continue;

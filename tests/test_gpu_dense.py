@@ -43,7 +43,7 @@ def test_tiny_config(fp4):
 SHAPES = [(256, 512), (1040, 768), (512, 320), (768, 448), (384, 4096), (2048, 2304)]
 
 
-@pytest.mark.parametrize("M", [1, 2, 5, 8, 16, 17, 32, 33, 64, 100, 128])
+@pytest.mark.parametrize("M", [1, 2, 5, 8, 11, 16, 17, 32, 33, 64, 100, 128])
 @pytest.mark.parametrize("N,K", SHAPES)
 def test_nvfp4_gemv(fp4, M, N, K):
     x, w, sf = dense_inputs(M, N, K, seed=7 * M + N)
@@ -53,7 +53,7 @@ def test_nvfp4_gemv(fp4, M, N, K):
     assert_close(u16(got), ref, f"nvfp4_gemv M={M} N={N} K={K}")
 
 
-@pytest.mark.parametrize("M", [1, 6, 16, 24])
+@pytest.mark.parametrize("M", [1, 6, 12, 16, 24])
 @pytest.mark.parametrize("N,K,silu", [(512, 2304, False), (1056, 1280, True), (768, 448, False)])
 def test_nvfp4_gemv_wide_range_activations(fp4, M, N, K, silu):
     # Activations far outside the f16 range or below its subnormal grid in the
@@ -309,9 +309,9 @@ def test_full_e4m3_range_dequantize_rows_bit_exact(fp4):
 @pytest.mark.parametrize("M", [1, 2, 5, 8, 12, 16, 24])
 @pytest.mark.parametrize("silu", [False, True])
 def test_full_e4m3_range_gemv(fp4, M, silu):
-    # 1..2 tokens: f16 route (converter warp); 3..8: f16 route (cooperative);
-    # 9..16: bf16 bit-placement route; 17+: the tcgen05 kernel.  The scales
-    # span zero, subnormals, negatives and 448.
+    # 1..2 tokens: f16 route (converter warp); 3..12: f16 route (cooperative,
+    # 8- and 16-token tiles); 13..16: bf16 bit-placement route; 17+: the
+    # tcgen05 kernel.  The scales span zero, subnormals, negatives and 448.
     N, K = 256, 4096
     w, sf = _full_range_weight(N, K, seed=78 + M)
     x = synth.activations(M, K, seed=79 + M)
