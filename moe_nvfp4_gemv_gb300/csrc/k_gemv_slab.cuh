@@ -307,19 +307,33 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
     pdl_wait();
     const int nchk = klen / 8;  // 16-byte chunks per token holding data
     const int nslot = (M > 0 ? nst_tile : 0) * 32;  // 16-byte chunks per token in the slab
-    for (int q = tid; q < M * nslot; q += ncons) {
-      const int n = q / nslot, kq = q % nslot;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (kq < nchk) {
-        const uint16_t* xr = kDense ? p.x + static_cast<int64_t>(n) * p.ldx
-                                    : (wk.shared ? p.x2 : p.x) + s_mwork.xoff[n];
-        v = __ldg(reinterpret_cast<const uint4*>(xr + wk.k_begin + 8 * kq));
+    // (loads in batches of kFillBatch per thread, all issued before their
+    // stores, so a thread waits for one round trip per batch, not per chunk)
+    constexpr int kFillBatch = 4;
+    for (int q0 = tid; q0 < M * nslot; q0 += kFillBatch * ncons) {
+      uint4 v[kFillBatch];
+#pragma unroll
+      for (int i = 0; i < kFillBatch; ++i) {
+        const int q = q0 + i * ncons;
+        const int n = q / nslot, kq = q % nslot;
+        v[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (q < M * nslot && kq < nchk) {
+          const uint16_t* xr = kDense ? p.x + static_cast<int64_t>(n) * p.ldx
+                                      : (wk.shared ? p.x2 : p.x) + s_mwork.xoff[n];
+          v[i] = __ldg(reinterpret_cast<const uint4*>(xr + wk.k_begin + 8 * kq));
+        }
       }
-      const int s = kq / 32, u = (kq % 32) / 8, ch = kq % 8;
-      const uint32_t a = slab + s * slab_stage + (u * M + n) * 128 + ((ch ^ (n & 7)) * 16);
-      sts128(a, v);
-      uint4 o;
-      if (!bf16x8_to_f16x8_exact(v, o)) atomicOr(&s_xbad[s], 1);
+#pragma unroll
+      for (int i = 0; i < kFillBatch; ++i) {
+        const int q = q0 + i * ncons;
+        if (q >= M * nslot) break;
+        const int n = q / nslot, kq = q % nslot;
+        const int s = kq / 32, u = (kq % 32) / 8, ch = kq % 8;
+        const uint32_t a = slab + s * slab_stage + (u * M + n) * 128 + ((ch ^ (n & 7)) * 16);
+        sts128(a, v[i]);
+        uint4 o;
+        if (!bf16x8_to_f16x8_exact(v[i], o)) atomicOr(&s_xbad[s], 1);
+      }
     }
     cons_sync(ncons);
     for (int q = tid; q < M * nchk; q += ncons) {
