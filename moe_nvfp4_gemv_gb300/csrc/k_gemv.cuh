@@ -14,7 +14,7 @@
 // memory in rank order (deterministic).
 //
 // Warp roles (kW dequant warpgroups, then a weight producer warp, an MMA
-// warp and, NVFP4 only, an activation producer warp):
+// warp and, NVFP4 only, an activation producer warp and a permute warp):
 //   weights   lane 0 streams weight boxes (TMA, 128-byte swizzle) and the
 //             matching 512-byte scale chunks (bulk copies) into a ring of
 //             shared-memory stages of 256 K; with PDL the first stages are
@@ -26,15 +26,20 @@
 //             the weight ring, which hides HBM latency, is not shortened by
 //             activations that come from L2.  BF16: a stage's activations
 //             travel in the weight stage, loaded by the weight producer.
+//   permute   (NVFP4) as each slice lands, its activations in place into
+//             the weight pairs' K order (dequant.cuh), then an arrival the
+//             MMA warp waits for, so the dequant warps never wait for
+//             activations (measured at 32 tokens: ~0.6 us of waiting and
+//             ~0.3 us of permuting per slice when they did).
 //   dequant   warpgroup w takes the 128-wide K slices q = w, w + kW, ...  For
 //             each slice thread i (row i) reads its code bytes and scale
 //             bytes (then frees its warp's share of the weight stage),
 //             dequantizes them exactly to bf16 (dequant.cuh) and stores them
 //             with tcgen05.st into the slice's tensor-memory A slot (a ring
-//             of kSlots slots shared by the warpgroups); the warps also
-//             permute the slice's activations in shared memory to the weight
-//             pairs' K order, then arrive on the slot's barrier.
-//   MMA       the warp waits for each slot together and one elected lane
+//             of kSlots slots shared by the warpgroups), then arrive on the
+//             slot's barrier.
+//   MMA       the warp waits for each slot (and its permuted activation
+//             slice) together and one elected lane
 //             issues the slot's eight K=16 tcgen05.mma into the fp32
 //             accumulator and frees the tensor-memory slot and the slice's
 //             activation slot with tcgen05.commit, so the dequant warps never
@@ -163,11 +168,15 @@ template <int kMode, int kNT>
 struct Cfg {
   static constexpr bool kFp4 = kMode != kDenseBf16;
   static constexpr int kW = kFp4 ? 2 : 1;  // worker warpgroups
-  // NVFP4: a third warp streams the activation ring
-  static constexpr int kThreads = kW * 128 + (kFp4 ? 96 : 64);
+  // NVFP4: a third warp streams the activation ring; up to 32 tokens a
+  // fourth permutes each landed activation slice for the MMAs (larger tiles:
+  // the dequant warps permute it, a slice being too much for one warp)
+  static constexpr bool kPermSep = kFp4 && kNT <= 32;
+  static constexpr int kThreads = kW * 128 + (kFp4 ? (kPermSep ? 128 : 96) : 64);
   static constexpr int kProducerWarp = 4 * kW;
   static constexpr int kMmaWarp = 4 * kW + 1;
   static constexpr int kXWarp = 4 * kW + 2;
+  static constexpr int kPermWarp = kPermSep ? 4 * kW + 3 : -1;
   static constexpr int kStageK = kFp4 ? kStageK4 : kStageK16;
   static constexpr int kSlicesPerStage = kFp4 ? kStageK / kSliceK : 1;  // 2 (fp4) or 1 (bf16)
   static constexpr int kWTileBytes = 128 * 128;
@@ -435,6 +444,7 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
   __shared__ __align__(8) uint64_t bar_empty[kMaxStages];   // NVFP4: stage dequantized; BF16: its MMAs done
   __shared__ __align__(8) uint64_t bar_xfull[kMaxXSlots];   // activation slice landed
   __shared__ __align__(8) uint64_t bar_xempty[kMaxXSlots];  // activation slice's MMAs done (MMA-thread commit)
+  __shared__ __align__(8) uint64_t bar_xready[kMaxXSlots];  // activation slice permuted (permute warp)
   __shared__ __align__(8) uint64_t bar_afull[kMaxSlots];   // slot dequantized (4 warps of its warpgroup)
   __shared__ __align__(8) uint64_t bar_aempty[kMaxSlots];  // slot's MMAs done (MMA-thread commit)
   __shared__ __align__(8) uint64_t bar_accum;
@@ -453,16 +463,14 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
   const uint32_t rank = S > 1 ? cluster_ctarank() : 0;
   const int nstages = p.nstages;
 
-  // For gate_up the routed experts are only known once the router's output
-  // (ids) is complete; every other mode reads ids / weights before the wait.
-  constexpr bool kIdsAfterWait = kMode == kMoeGateUp;
   const uint64_t pol_w = policy_evict_first();
   const uint64_t pol_x = policy_evict_last();
 
   // ------------------------------------------------------------------ prologue
-  // The producer resolves the work, initialises every barrier and starts the
-  // weight stream before the CTA-wide barrier; warp 0 allocates tensor memory
-  // meanwhile.
+  // The producer resolves the work (gate_up routed CTAs: after the wait for
+  // the router's ids) and initialises every barrier before the CTA-wide
+  // barrier; warp 0 allocates tensor memory meanwhile.  The weight stream
+  // starts right after it.
   int pre = 0;  // stages whose weights the producer has issued
   auto stage_count = [&](const CtaWork& wk) {
     return wk.active ? (wk.k_end - wk.k_begin + C::kStageK - 1) / C::kStageK : 0;
@@ -527,6 +535,7 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
     for (int i = 0; i < nx; ++i) {
       mbar_init(smem_u32(&bar_xfull[i]), C::kFullCount);  // TMA: one arrival; gathers: 32 lanes + lane 0
       mbar_init(smem_u32(&bar_xempty[i]), 1);
+      mbar_init(smem_u32(&bar_xready[i]), 1);
     }
     for (int i = 0; i < kNS; ++i) {
       mbar_init(smem_u32(&bar_afull[i]), 4);  // one arrival per warp of the slice's warpgroup
@@ -544,10 +553,6 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
       mbar_arrive_expect_tx(smem_u32(&bar_inbox), S * kNT * mine * 4);
     }
     mbar_fence_init();
-    pre = min(nst, nstages);
-    if (!kIdsAfterWait || wk.shared) {
-      for (int s = 0; s < pre; ++s) issue_weights(wk, s);
-    }
   }
   if (warp == 0) tmem_alloc(smem_u32(&s_tmem), C::kTmemCols);
   tc_fence_before();
@@ -577,9 +582,14 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
 
   if (warp == C::kProducerWarp) {
     // ------------------------------------------------------------------ producer
-    if (lane == 0 && kIdsAfterWait && !wk.shared) {
+    // The first stages, issued after the CTA barrier so the other warps need
+    // not wait for the copies' issue (~2.4 us for three stages of 128-row
+    // tiles, measured at a CTA's start; the block barrier held every warp
+    // for it when they were issued before).  Still before the wait for the
+    // previous grid (gate_up routed CTAs: resolve_work already waited).
+    if (lane == 0) {
       pre = min(nst, nstages);
-      for (int s = 0; s < pre; ++s) issue_weights(wk, s);  // resolve_work already waited
+      for (int s = 0; s < pre; ++s) issue_weights(wk, s);
     }
     pdl_wait();
     pre = __shfl_sync(0xFFFFFFFFu, pre, 0);
@@ -658,6 +668,33 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
         }
       }
     }
+  } else if (warp == C::kPermWarp) {
+    // ------------------------------------------------------------------ activation permute
+    // NVFP4, tiles of up to 32 tokens: each landed slice in place into the
+    // weight pairs' K order (dequant.cuh), then a proxy fence (the MMAs read
+    // it through the async proxy) and one arrival; the MMA warp waits for
+    // it.  The single in-order consumer of the slots' landing barriers
+    // (parity waits).
+    if constexpr (C::kPermSep) {
+      const int klen = wk.k_end - wk.k_begin;
+      for (int q = 0; q < nslices; ++q) {
+        const int xs = q % nx;
+        if (!__all_sync(0xFFFFFFFFu,
+                        !s_abort && mbar_wait_sleepy(smem_u32(&bar_xfull[xs]), (q / nx) & 1, p.err, 20))) {
+          s_abort = 1;
+          break;
+        }
+        const int natoms = min(kSliceK, klen - q * kSliceK) / kSubK;  // 1 or 2
+        for (int v = 0; v < natoms; ++v) {
+          const uint32_t xa = xring + xs * C::kXSliceBytes + v * (kNT * 128);
+#pragma unroll 4
+          for (int c = lane; c < kNT * 8; c += 32) sts128(xa + c * 16, perm_x8(lds128(xa + c * 16)));
+        }
+        fence_proxy_async_smem();  // the permuted activations, before the MMAs read them
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bar_xready[xs]));
+      }
+    }
   } else if (warp == C::kMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
     // One warp consumes the slots in slice order (the slot barriers' parity
@@ -678,7 +715,9 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
       if constexpr (C::kFp4) {
         for (int q = 0; q < nslices; ++q) {
           const int a = q % kNS;
-          if (!__all_sync(0xFFFFFFFFu, !s_abort && mbar_wait(smem_u32(&bar_afull[a]), (q / kNS) & 1, p.err))) {
+          if (!__all_sync(0xFFFFFFFFu, !s_abort && mbar_wait(smem_u32(&bar_afull[a]), (q / kNS) & 1, p.err) &&
+                                           (!C::kPermSep ||
+                                            mbar_wait(smem_u32(&bar_xready[q % nx]), (q / nx) & 1, p.err)))) {
             s_abort = 1;
             break;
           }
@@ -745,13 +784,15 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
         // MMA thread's wait on its slot then times out as well.  Each wait
         // comes as late as the work allows: codes and scales are loaded and
         // the stage released first, the first 32 weights dequantized before
-        // the tensor-memory slot is waited for, and the activations waited
-        // for only when they are permuted.  The activation slot's wait comes
-        // after the tensor-memory slot's: a parity wait is sound only once
-        // the slot's previous fill (slice q - nx) is known to have landed,
-        // which this warpgroup saw itself when nx is even (the slot holds
-        // only its slices) and which the tensor-memory slot's wait implies
-        // when nx = kSlots = 3 (slice q - 3 consumed).
+        // the tensor-memory slot is waited for.  Tiles of up to 32 tokens:
+        // the activations are the permute warp's, these warps never wait
+        // for them.  Larger tiles: the warps permute the slice's activations
+        // after the tensor-memory slot's wait -- a parity wait on the
+        // activation slot is sound only once its previous fill (slice q - nx)
+        // is known to have landed, which this warpgroup saw itself when nx
+        // is even (the slot holds only its slices) and which the tensor-
+        // memory slot's wait implies when nx = kSlots = 3 (slice q - 3
+        // consumed).
         bool ok = !s_abort;
         if (ok && s != cur) {
           ok = mbar_wait_sleepy(smem_u32(&bar_full[slot]), (s / nstages) & 1, p.err, 20);
@@ -805,18 +846,20 @@ __global__ void __launch_bounds__(Cfg<kMode, kNT>::kThreads, Cfg<kMode, kNT>::kM
           dequant32_perm(qc[1][1], sc[1][2], sc[1][3], o);
           tmem_st16(col0 + 48, o);
         }
-        if (!__all_sync(0xFFFFFFFFu,
-                        !s_abort && mbar_wait_sleepy(smem_u32(&bar_xfull[q % nx]), (q / nx) & 1, p.err, 20))) {
-          s_abort = 1;
-          break;
-        }
-        // this warp's share of the slice's activations into the pairs' K order
-        for (int v = 0; v < natoms; ++v) {
-          const uint32_t xa = xs + v * (kNT * 128);
-          for (int c = i; c < kNT * 8; c += 128) sts128(xa + c * 16, perm_x8(lds128(xa + c * 16)));
+        if constexpr (!C::kPermSep) {
+          if (!__all_sync(0xFFFFFFFFu,
+                          !s_abort && mbar_wait_sleepy(smem_u32(&bar_xfull[q % nx]), (q / nx) & 1, p.err, 20))) {
+            s_abort = 1;
+            break;
+          }
+          // this warp's share of the slice's activations into the pairs' K order
+          for (int v = 0; v < natoms; ++v) {
+            const uint32_t xa = xs + v * (kNT * 128);
+            for (int c = i; c < kNT * 8; c += 128) sts128(xa + c * 16, perm_x8(lds128(xa + c * 16)));
+          }
+          fence_proxy_async_smem();  // the permuted activations, before the MMAs read them
         }
         tmem_wait_st();
-        fence_proxy_async_smem();  // the permuted activations, before the MMAs read them
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bar_afull[a]));
