@@ -57,6 +57,93 @@ __device__ __forceinline__ bool bf16x8_to_f16x8_exact(const uint4& v, uint4& o) 
   return e;
 }
 
+// One 128-K half h of a 256-K stage for a consumer warp of the slab
+// kernels (f16 route): thread (g, c) of the warp, its kR row blocks' code
+// rows at w_off and scale bytes at sf_off in the stage at `st`, the stage's
+// activations at `xs` (64-K atoms of M rows x 128 bytes, 16-byte chunks
+// XOR-swizzled by row % 8, f16).  `cvalid` false (a chunk past the end of a
+// ragged last stage) gives zero A registers: that chunk's scales were not
+// copied and may hold anything.
+template <int kR, int kChains>
+__device__ __forceinline__ void slab_half_f16(float (&acc)[kChains][kR][4], uint32_t st, uint32_t xs, int h,
+                                              bool cvalid, int M, const uint32_t (&w_off)[kR][2],
+                                              const uint32_t (&sf_off)[kR][2], uint32_t key, int g, int c) {
+  const int j = 4 * h + c;
+  uint4 A[kR][2];
+  uint32_t slo[kR][2], shi[kR][2];
+  const uint32_t sc_off = (j / 2) * 512 + 2 * (j % 2);
+#pragma unroll
+  for (int b = 0; b < kR; ++b) {
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      A[b][hr] = lds128(st + w_off[b][hr] + ((static_cast<uint32_t>(j) ^ key) * 16));
+      scale_pair_to_f16x2(lds16(st + sf_off[b][hr] + sc_off), slo[b][hr], shi[b][hr]);
+      if (!cvalid) slo[b][hr] = shi[b][hr] = 0u;
+    }
+  }
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const int kk = 32 * j + 8 * w;
+    const uint32_t u = kk / 64, ch = (kk % 64) / 8;
+    const uint4 xv = lds128_if(xs + (u * M + g) * 128 + ((ch ^ static_cast<uint32_t>(g)) * 16), g < M);
+#pragma unroll
+    for (int b = 0; b < kR; ++b) {
+      const uint32_t w0 = w == 0 ? A[b][0].x : w == 1 ? A[b][0].y : w == 2 ? A[b][0].z : A[b][0].w;
+      const uint32_t w1 = w == 0 ? A[b][1].x : w == 1 ? A[b][1].y : w == 2 ? A[b][1].z : A[b][1].w;
+      uint32_t r0[4], r1[4];
+      dequant8_f16(w0, w < 2 ? slo[b][0] : shi[b][0], r0);
+      dequant8_f16(w1, w < 2 ? slo[b][1] : shi[b][1], r1);
+      mma_f16_16816(acc[(2 * w) % kChains][b], r0[0], r1[0], r0[1], r1[1], xv.x, xv.y);
+      mma_f16_16816(acc[(2 * w + 1) % kChains][b], r0[2], r1[2], r0[3], r1[3], xv.z, xv.w);
+    }
+  }
+}
+
+// The same half on the bf16 route (the stage's activations are bf16; they
+// are permuted in registers to the weight pairs' K order); products times
+// 2^-kShift into accb.
+template <int kR>
+__device__ __forceinline__ void slab_half_bf16(float (&accb)[kR][4], uint32_t st, uint32_t xs, int h, bool cvalid,
+                                               int M, const uint32_t (&w_off)[kR][2], const uint32_t (&sf_off)[kR][2],
+                                               uint32_t key, int g, int c) {
+  const int j = 4 * h + c;
+  uint4 A[kR][2];
+  uint32_t slo[kR][2], shi[kR][2];
+  const uint32_t sc_off = (j / 2) * 512 + 2 * (j % 2);
+#pragma unroll
+  for (int b = 0; b < kR; ++b) {
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      A[b][hr] = lds128(st + w_off[b][hr] + ((static_cast<uint32_t>(j) ^ key) * 16));
+      scale_pair_to_bf16x2(lds16(st + sf_off[b][hr] + sc_off), slo[b][hr], shi[b][hr]);
+      if (!cvalid) slo[b][hr] = shi[b][hr] = 0u;
+    }
+  }
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const int kk = 32 * j + 8 * w;
+    const uint32_t u = kk / 64, ch = (kk % 64) / 8;
+    const uint4 xv =
+        perm_x8(lds128_if(xs + (u * M + g) * 128 + ((ch ^ static_cast<uint32_t>(g)) * 16), g < M));
+#pragma unroll
+    for (int b = 0; b < kR; ++b) {
+      const uint32_t w0 = w == 0 ? A[b][0].x : w == 1 ? A[b][0].y : w == 2 ? A[b][0].z : A[b][0].w;
+      const uint32_t w1 = w == 0 ? A[b][1].x : w == 1 ? A[b][1].y : w == 2 ? A[b][1].z : A[b][1].w;
+      uint32_t r0[4], r1[4];
+      e2m1x8_raw_perm(w0, r0);
+      e2m1x8_raw_perm(w1, r1);
+      const uint32_t sa = w < 2 ? slo[b][0] : shi[b][0], sb = w < 2 ? slo[b][1] : shi[b][1];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        r0[q] = bf16x2_mul(r0[q], sa);
+        r1[q] = bf16x2_mul(r1[q], sb);
+      }
+      mma_bf16_16816(accb[b], r0[0], r1[0], r0[1], r1[1], xv.x, xv.y);
+      mma_bf16_16816(accb[b], r0[2], r1[2], r0[3], r1[3], xv.z, xv.w);
+    }
+  }
+}
+
 // kMode: kDenseFp4 (nvfp4_gemv); kMoeGateUp (the gate_up launch of
 // vllm.models.flint.ops.moe_gemv: routed chunks of up to kSlabChunk pairs of
 // one expert, and the shared expert's token chunks, with the epilogues of
@@ -368,80 +455,6 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
       }
     };
     set_offsets(wk);
-    // One 128-K half of a stage, f16 route.  `cvalid` false (a chunk past
-    // the end of a ragged last stage) gives zero A registers: that chunk's
-    // scales were not copied and may hold anything.
-    auto half_f16 = [&](uint32_t st, uint32_t xs, int h, bool cvalid) {
-      const int j = 4 * h + c;
-      uint4 A[kR][2];
-      uint32_t slo[kR][2], shi[kR][2];
-      const uint32_t sc_off = (j / 2) * 512 + 2 * (j % 2);
-#pragma unroll
-      for (int b = 0; b < kR; ++b) {
-#pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-          A[b][hr] = lds128(st + w_off[b][hr] + ((static_cast<uint32_t>(j) ^ key) * 16));
-          scale_pair_to_f16x2(lds16(st + sf_off[b][hr] + sc_off), slo[b][hr], shi[b][hr]);
-          if (!cvalid) slo[b][hr] = shi[b][hr] = 0u;
-        }
-      }
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const int kk = 32 * j + 8 * w;
-        const uint32_t u = kk / 64, ch = (kk % 64) / 8;
-        const uint4 xv = lds128_if(xs + (u * M + g) * 128 + ((ch ^ static_cast<uint32_t>(g)) * 16), g < M);
-#pragma unroll
-        for (int b = 0; b < kR; ++b) {
-          const uint32_t w0 = w == 0 ? A[b][0].x : w == 1 ? A[b][0].y : w == 2 ? A[b][0].z : A[b][0].w;
-          const uint32_t w1 = w == 0 ? A[b][1].x : w == 1 ? A[b][1].y : w == 2 ? A[b][1].z : A[b][1].w;
-          uint32_t r0[4], r1[4];
-          dequant8_f16(w0, w < 2 ? slo[b][0] : shi[b][0], r0);
-          dequant8_f16(w1, w < 2 ? slo[b][1] : shi[b][1], r1);
-          mma_f16_16816(acc[(2 * w) % kChains][b], r0[0], r1[0], r0[1], r1[1], xv.x, xv.y);
-          mma_f16_16816(acc[(2 * w + 1) % kChains][b], r0[2], r1[2], r0[3], r1[3], xv.z, xv.w);
-        }
-      }
-    };
-    // The same half on the bf16 route (the stage's activations stayed bf16;
-    // they are permuted in registers to the weight pairs' K order).
-    auto half_bf16 = [&](uint32_t st, uint32_t xs, int h, bool cvalid) {
-      const int j = 4 * h + c;
-      uint4 A[kR][2];
-      uint32_t slo[kR][2], shi[kR][2];
-      const uint32_t sc_off = (j / 2) * 512 + 2 * (j % 2);
-#pragma unroll
-      for (int b = 0; b < kR; ++b) {
-#pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-          A[b][hr] = lds128(st + w_off[b][hr] + ((static_cast<uint32_t>(j) ^ key) * 16));
-          scale_pair_to_bf16x2(lds16(st + sf_off[b][hr] + sc_off), slo[b][hr], shi[b][hr]);
-          if (!cvalid) slo[b][hr] = shi[b][hr] = 0u;
-        }
-      }
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const int kk = 32 * j + 8 * w;
-        const uint32_t u = kk / 64, ch = (kk % 64) / 8;
-        const uint4 xv =
-            perm_x8(lds128_if(xs + (u * M + g) * 128 + ((ch ^ static_cast<uint32_t>(g)) * 16), g < M));
-#pragma unroll
-        for (int b = 0; b < kR; ++b) {
-          const uint32_t w0 = w == 0 ? A[b][0].x : w == 1 ? A[b][0].y : w == 2 ? A[b][0].z : A[b][0].w;
-          const uint32_t w1 = w == 0 ? A[b][1].x : w == 1 ? A[b][1].y : w == 2 ? A[b][1].z : A[b][1].w;
-          uint32_t r0[4], r1[4];
-          e2m1x8_raw_perm(w0, r0);
-          e2m1x8_raw_perm(w1, r1);
-          const uint32_t sa = w < 2 ? slo[b][0] : shi[b][0], sb = w < 2 ? slo[b][1] : shi[b][1];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            r0[q] = bf16x2_mul(r0[q], sa);
-            r1[q] = bf16x2_mul(r1[q], sb);
-          }
-          mma_bf16_16816(accb[b], r0[0], r1[0], r0[1], r1[1], xv.x, xv.y);
-          mma_bf16_16816(accb[b], r0[2], r1[2], r0[3], r1[3], xv.z, xv.w);
-        }
-      }
-    };
     // After a tile's last stage (grouped modes).  Every consumer warp calls
     // it for the same tiles, also after a wait ran out (the first barrier
     // agrees on the abort, which skips the tile's writes and arrival: its
@@ -586,14 +599,14 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           if (128 * h < kvalid) {
-            if (128 * (h + 1) <= kvalid) half_f16(st, xs, h, true);
-            else half_f16(st, xs, h, 32 * (4 * h + c) < kvalid);
+            if (128 * (h + 1) <= kvalid) slab_half_f16<kR, kChains>(acc, st, xs, h, true, M, w_off, sf_off, key, g, c);
+            else slab_half_f16<kR, kChains>(acc, st, xs, h, 32 * (4 * h + c) < kvalid, M, w_off, sf_off, key, g, c);
           }
         }
       } else {
 #pragma unroll 1
         for (int h = 0; h < 2; ++h) {
-          if (128 * h < kvalid) half_bf16(st, xs, h, 32 * (4 * h + c) < kvalid);
+          if (128 * h < kvalid) slab_half_bf16<kR>(accb, st, xs, h, 32 * (4 * h + c) < kvalid, M, w_off, sf_off, key, g, c);
         }
       }
       __syncwarp();
