@@ -213,12 +213,13 @@ fp4gemv_status fp4gemv_get_device_error(cudaStream_t stream);
 fp4gemv_status fp4gemv_set_wait_limit_ns(uint64_t ns);
 
 /* Test hook for the timeout path (no counterpart on the pages): from now on
- * the producers of the dense NVFP4 GEMV for 1 .. 16 tokens issue nothing at
- * all -- no copy, no arrival -- for the 256-K ring stage with this index of
- * every CTA, so the
- * consumers' bounded wait for it runs out with no copy in flight; -1 (the
- * default) turns it off.  A process-wide host setting read at each
- * fp4gemv_nvfp4_gemv launch; for tests only.
+ * the producers of the dense NVFP4 GEMV for 1 .. 16 tokens, and of
+ * fp4gemv_moe_down_combine on the slab kernel (1 .. 64 tokens, E <= 256),
+ * issue nothing at all -- no copy, no arrival -- for the 256-K ring stage
+ * with this index of every CTA (down_combine: counted over the CTA's row
+ * tiles in turn), so the consumers' bounded wait for it runs out with no
+ * copy in flight; -1 (the default) turns it off.  A process-wide host
+ * setting read at each of those launches; for tests only.
  * FP4GEMV_ERR_INVALID_ARG for stage < -1. */
 fp4gemv_status fp4gemv_debug_skip_stage(int stage);
 

@@ -115,23 +115,28 @@ typedef struct {
   int slab_bytes;     /* shared memory holding a CTA's activation rows (the whole K) */
   int stage_bytes;    /* one weight stage (codes of 128 rows x 256 K, one scale group) */
   int stages;         /* weight ring stages (2 .. 8) */
-  int ctas_per_sm;    /* CTAs per SM the ring is sized for (3) */
+  int ctas_per_sm;    /* CTAs per SM the ring is sized for (2 or 3) */
   size_t smem_bytes;  /* dynamic shared memory per CTA */
 } fp4gemv_moe_down_slab_plan;
 
 /* Plan of fp4gemv_moe_down_combine on the slab kernel (vllm.models.flint.ops.
  * moe_gemv, down_combine: chunks of up to 8 pairs of one expert, each CTA
- * streaming T row tiles of its expert over its resident activation rows,
- * writing each tile's y rows and arriving on the tile's counter; the CTA
- * that arrives last combines the tile).  No GPU is needed.
+ * streaming T row tiles of its expert over its resident activation rows and
+ * writing each tile's y rows; a second, small kernel then combines them).
+ * No GPU is needed.
  *   M, topk, E, H, I, SI: as fp4gemv_moe_down_combine (same shape rules).
  *   sms:  streaming multiprocessors of the GPU (152 on GB300).
  *   regs: registers per thread of the kernel.
  *   out:  HOST pointer, filled on success.
- * Applies to 2 <= M <= 64 and E <= 256 when 8 activation rows of
- * max(I, SI) and two weight stages fit a third of the SM's shared memory
- * (one token runs on the register-fed kernel): chunks of 8 pairs, T = 2 tiles
- * per CTA, three CTAs per SM, as many weight stages as fit (2 .. 8).
+ * Applies to 1 <= M <= 64 and E <= 256 when up to 8 activation rows of
+ * max(I, SI) and two weight stages fit the CTA's share of the SM's shared
+ * memory.  Chunks of 8 pairs.  With C = (E (1 - (1 - 1/E)^(M topk)), at
+ * least ceil(M topk / 8)) + ceil(M / 8) expected streaming columns and
+ * n(T) = C ceil(ceil(H / 128) / T) CTAs: T = 1 at two CTAs per SM if
+ * n(1) <= 2 sms, else T = 2 at two per SM if n(2) <= 2 sms, else T = 2 at
+ * three per SM if n(2) <= 3 sms, else T = 1 at three per SM if
+ * n(2) <= 3.3 sms, else T = 2 at three per SM; as many weight stages as fit
+ * (2 .. 8, at most T stage streams of I).
  * Returns FP4GEMV_ERR_INVALID_ARG for a null out, sms < 1 or regs < 1;
  * FP4GEMV_ERR_UNSUPPORTED_SHAPE for shapes fp4gemv_moe_down_combine rejects
  * and for calls the slab kernel does not serve. */

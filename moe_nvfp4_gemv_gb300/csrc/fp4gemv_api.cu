@@ -5,6 +5,8 @@
 // encoding and the launches themselves.  All arithmetic runs in the kernels.
 #include <cuda.h>
 
+#include <algorithm>
+#include <cmath>
 #include <atomic>
 #include <cstdint>
 #include <cstddef>
@@ -597,35 +599,52 @@ bool plan_slab_moe(int M, int topk, int E, int H, int I, int SI, int sms, int re
 std::atomic<int> g_slab_moe_regs[kMaxDevices];
 
 // The slab kernel for down_combine: the whole K per CTA (its activation
-// rows resident), chunks of up to 8 pairs of one expert, T = 2 row tiles per
-// CTA streamed in turn over the same rows, three CTAs per SM, many waves;
-// one scale group per 128-row weight stage, as many stages as fit (2 .. 8).
+// rows resident), chunks of up to 8 pairs of one expert, T row tiles per CTA
+// streamed in turn over the same rows; one scale group per 128-row weight
+// stage, as many stages as fit (2 .. 8).  The combine is a kernel of its own
+// after it.  T and the CTAs per SM follow the number of CTAs that stream:
+// the host does not see the ids, so it takes the expected number of distinct
+// experts of P = M topk uniform draws (at least P / 8 chunks) plus the shared
+// expert's token chunks as the columns, times ceil(tiles / T):
+//   one tile per CTA at two CTAs per SM if those fit in one wave (deeper
+//   rings), else two tiles at two per SM if they fit, else two tiles at
+//   three per SM, except when that overflows one wave by at most 10 % (then
+//   one tile at three per SM: twice as many CTAs of half the length).
 // Measured on the E = 128, top-8, H = 4096, I = SI = 1536 block (us per
-// call, L2-cold, 8 routings), a sweep of chunk, tiles per CTA and CTAs per
-// SM: 8 tokens 80.4 (register-fed kernel 92.2), 32 tokens 159.8 (216.3);
-// fewer, longer CTAs were slower.  One token stays on the register-fed
-// kernel (17.3 against 17.8 at best here).
+// call, L2-cold, 8 routings; a sweep of T = 1, 2, 3, 4, chunks of 2, 4, 8
+// and two or three CTAs per SM): 1 token 15.7 (register-fed kernel 17.9),
+// 2 tokens 25.6 (two tiles at three per SM: 32.8), 3: 33.4, 4: 44.8 (two
+// tiles: 50.0), 8: 68.8, 16: 107.7, 32: 153.1, 64: 196.8 (T = 3 or 4 within
+// 2 %).
 struct SlabDownPlan {
   int T = 2, groups = 1, chunk = 8, slab_bytes = 0, stage_bytes = 0, nstages = 2, occ = 3;
   size_t smem = 0;
 };
 
-constexpr int kSmemPerCtaDown = 4096;  // reservation + static shared memory (incl. the expert counts)
+constexpr int kSmemPerCtaDown = 4096;  // reservation + static shared memory
 
 bool plan_slab_down(int M, int topk, int E, int H, int I, int SI, int sms, int regs, SlabDownPlan* sp) {
-  const int cw = fp4::kSlabMaxCW, occ = 3, T = 2;
+  const int cw = fp4::kSlabMaxCW;
   const int warp_regs = (regs * 32 + 255) / 256 * 256;
-  if (static_cast<long>(occ) * (cw + 1) * warp_regs > 65536 || sms < 1 || E > fp4::kSlabMaxExperts) return false;
-  if (M < 2 || M > 64) return false;
+  if (sms < 1 || E > fp4::kSlabMaxExperts || M < 1 || M > 64) return false;
   const long P = static_cast<long>(M) * topk;
   const int chunk = fp4::kSlabNT;
+  const int tiles = (H + 127) / 128;
+  const double distinct = E * (1.0 - std::pow(1.0 - 1.0 / E, static_cast<double>(P)));
+  const double cols = std::max(distinct, static_cast<double>((P + chunk - 1) / chunk)) + (M + chunk - 1) / chunk;
+  auto ctas = [&](int T) { return cols * ((tiles + T - 1) / T); };
+  int T = 2, occ = 3;
+  if (ctas(1) <= 2.0 * sms) T = 1, occ = 2;
+  else if (ctas(2) <= 2.0 * sms) T = 2, occ = 2;
+  else if (ctas(2) <= 3.0 * sms) T = 2, occ = 3;
+  else if (ctas(2) <= 3.3 * sms) T = 1, occ = 3;
+  if (static_cast<long>(occ) * (cw + 1) * warp_regs > 65536) return false;
   const int rows = static_cast<int>(P < chunk ? P : chunk);
   const int kmax = I > SI ? I : SI;
   const int nst = (kmax + 255) / 256;
   if (nst > fp4::kSlabMaxStages) return false;
   const int slab = (rows * nst * 512 + 1023) / 1024 * 1024;
   const int stage = 128 * 128 + 2048;
-  const int tiles = (H + 127) / 128;
   const long room = static_cast<long>(kSmemPerSm / occ - kSmemPerCtaDown) - 1024 - slab;
   int ns = static_cast<int>(room / stage);
   if (ns > fp4::kMaxStages) ns = fp4::kMaxStages;
@@ -1158,12 +1177,13 @@ fp4gemv_status fp4gemv_moe_down_combine(const void* act, const int32_t* ids, con
   int sms = 0;
   fp4gemv_status st = device_state(&err, &sms);
   if (st != FP4GEMV_OK) return st;
-  // Up to 64 tokens the slab kernel when its plan fits (plan_slab_down);
-  // otherwise the register-fed kernel for up to 64 tokens, chunks of at most
-  // 8 pairs (as gate_up), the tcgen05 kernel beyond.  From 8 tokens the
-  // register-fed grid holds many short CTAs (K = I is a few stages): the
-  // variant budgeted for three CTAs per SM (72 KB ring) hides more of their
-  // fixed costs.
+  // Up to 64 tokens the slab kernel when its plan fits (plan_slab_down),
+  // then the combine kernel; otherwise (more than 256 experts, or activation
+  // rows too long for the slab) the register-fed kernel for up to 64 tokens,
+  // chunks of at most 8 pairs (as gate_up), the tcgen05 kernel beyond.  From
+  // 8 tokens the register-fed grid holds many short CTAs (K = I is a few
+  // stages): the variant budgeted for three CTAs per SM (72 KB ring) hides
+  // more of their fixed costs.
   SlabDownPlan sdp;
   bool slab = false;
   if (M <= 64) {
@@ -1245,6 +1265,7 @@ fp4gemv_status fp4gemv_moe_down_combine(const void* act, const int32_t* ids, con
   p.skip_stage = -1;
   p.err = err;
   if (slab) {
+    p.skip_stage = g_skip_stage.load(std::memory_order_relaxed);  // (test hook)
     p.nstages = sdp.nstages;
     p.stage_bytes = sdp.stage_bytes;
     p.x_off = sdp.slab_bytes;
@@ -1260,7 +1281,20 @@ fp4gemv_status fp4gemv_moe_down_combine(const void* act, const int32_t* ids, con
     cfg.pdl = pdl;
     cfg.stream = stream;
     g_launches.fetch_add(1, std::memory_order_relaxed);
-    return from_cuda(fp4::launch_slab_moe(fp4::kMoeDown, p, cfg));
+    st = from_cuda(fp4::launch_slab_moe(fp4::kMoeDown, p, cfg));
+    if (st != FP4GEMV_OK) return st;
+    // The combine runs as a kernel of its own, launched early (PDL) and
+    // waiting for the slab grid: measured, the slab CTAs' per-tile arrival
+    // (fence, counter, the last CTA's combine) cost 20 % of the call.
+    const long items = static_cast<long>(M) * (H / 8);
+    LaunchCfg ccfg{};
+    ccfg.grid = dim3(static_cast<unsigned>(std::min<long>((items + 127) / 128, 4L * sms)), 1, 1);
+    ccfg.cluster = 1;
+    ccfg.smem = 0;
+    ccfg.pdl = 1;
+    ccfg.stream = stream;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return from_cuda(fp4::launch_moe_combine(p, ccfg));
   }
   const int shared_cols = (M + NT - 1) / NT;
   LaunchCfg cfg{};

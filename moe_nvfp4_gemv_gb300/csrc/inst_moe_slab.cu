@@ -1,11 +1,32 @@
 // Instantiations of the slab kernel's MoE modes: gate_up (routed chunks of
 // pairs of one expert and the shared expert's token chunks; split form: H
 // split over a cluster; grouped form: several tiles per CTA over one
-// resident activation slab) and down_combine (grouped).
+// resident activation slab) and down_combine (grouped), and the combine
+// kernel that follows the slab kernel's down_combine.
 #include "k_gemv_slab.cuh"
 #include "launch.h"
 
 namespace fp4 {
+
+// down_combine after the slab kernel: one thread per 8 consecutive h of one
+// token, grid-strided; waits for the previous grid (the slab kernel, whose y
+// rows it reads) and skips the tiles a CTA of that grid tagged as given up.
+__global__ void __launch_bounds__(128) moe_combine_kernel(const __grid_constant__ GemvParams p) {
+  if (threadIdx.x == 0) pdl_launch_dependents();
+  pdl_wait();
+  const int per_token = p.n_out / 8;
+  const unsigned long long tag = abort_tag(p.epoch);
+  for (int it = blockIdx.x * blockDim.x + threadIdx.x; it < p.M * per_token; it += gridDim.x * blockDim.x) {
+    const int t = it / per_token, h = 8 * (it % per_token);
+    if (__ldcg(p.counters + h / 128) == tag) continue;
+    moe_combine_item(p, t, h);
+  }
+}
+
+
+cudaError_t launch_moe_combine(const GemvParams& p, const LaunchCfg& cfg) {
+  return launch_kernel(moe_combine_kernel, 128, p, cfg);
+}
 
 cudaError_t launch_slab_moe(int mode, const GemvParams& p, const LaunchCfg& cfg) {
   if (p.cw != kSlabMaxCW) return cudaErrorInvalidValue;  // 128-row tiles

@@ -217,49 +217,60 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) {
 }
 __device__ __forceinline__ float bf16_to_f32(uint16_t h) { return __uint_as_float(static_cast<uint32_t>(h) << 16); }
 
+// down_combine of 8 consecutive h of token t: out[t, h .. h + 7] =
+// bf16(bf16(sum_j tw[t, j] * y[t, j, h]) + y_shared[t, h]), the sum in fp32
+// over j = 0 .. topk - 1 with fused multiply-adds (16-byte loads of y and
+// y_shared, one 16-byte store).  A token with an out-of-range id is left
+// unwritten.
+__device__ __forceinline__ void moe_combine_item(const GemvParams& p, int t, int h) {
+  bool ids_ok = true;
+  for (int j = 0; j < p.topk; ++j) {
+    const int e = __ldg(p.ids + t * p.topk + j);
+    ids_ok = ids_ok && e >= 0 && e < p.E;
+  }
+  if (!ids_ok) return;
+  float a[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) a[i] = 0.0f;
+  for (int j = 0; j < p.topk; ++j) {
+    const float wj = __ldg(p.tw + t * p.topk + j);
+    const uint4 yv = __ldcg(reinterpret_cast<const uint4*>(p.out + static_cast<int64_t>(t * p.topk + j) * p.ldo + h));
+    const uint32_t yw[4] = {yv.x, yv.y, yv.z, yv.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      a[2 * q] = fmaf(wj, __uint_as_float(yw[q] << 16), a[2 * q]);
+      a[2 * q + 1] = fmaf(wj, __uint_as_float(yw[q] & 0xFFFF0000u), a[2 * q + 1]);
+    }
+  }
+  const uint4 sv = __ldcg(reinterpret_cast<const uint4*>(p.out2 + static_cast<int64_t>(t) * p.ldo2 + h));
+  const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float lo = __uint_as_float(static_cast<uint32_t>(f32_to_bf16_rn(a[2 * q])) << 16) +
+                     __uint_as_float(sw[q] << 16);
+    const float hi = __uint_as_float(static_cast<uint32_t>(f32_to_bf16_rn(a[2 * q + 1])) << 16) +
+                     __uint_as_float(sw[q] & 0xFFFF0000u);
+    o[q] = static_cast<uint32_t>(f32_to_bf16_rn(lo)) | (static_cast<uint32_t>(f32_to_bf16_rn(hi)) << 16);
+  }
+  *reinterpret_cast<uint4*>(p.out3 + static_cast<int64_t>(t) * p.n_out + h) = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // down_combine of one 128-row tile of H (rows h0 .. h0 + 127) by `nthr`
-// threads (this one is `ti`): out[t, h] = bf16(bf16(sum_j tw[t, j] *
-// y[t, j, h]) + y_shared[t, h]), the sum in fp32 over j = 0 .. topk - 1 with
-// fused multiply-adds.  A work item is 8 consecutive h of one token (16-byte
-// loads of y and y_shared, one 16-byte store; H is a multiple of 64, so an
-// item is wholly inside or outside H).  A token with an out-of-range id is
-// left unwritten.
+// threads (this one is `ti`); a work item is 8 consecutive h of one token
+// (H is a multiple of 64, so an item is wholly inside or outside H).
 __device__ __forceinline__ void moe_combine_tile(const GemvParams& p, int h0, int ti, int nthr) {
   for (int it = ti; it < 16 * p.M; it += nthr) {
     const int t = it / 16, h = h0 + 8 * (it % 16);
-    if (h >= p.n_out) continue;
-    bool ids_ok = true;
-    for (int j = 0; j < p.topk; ++j) {
-      const int e = __ldg(p.ids + t * p.topk + j);
-      ids_ok = ids_ok && e >= 0 && e < p.E;
-    }
-    if (!ids_ok) continue;
-    float a[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) a[i] = 0.0f;
-    for (int j = 0; j < p.topk; ++j) {
-      const float wj = __ldg(p.tw + t * p.topk + j);
-      const uint4 yv = __ldcg(reinterpret_cast<const uint4*>(p.out + static_cast<int64_t>(t * p.topk + j) * p.ldo + h));
-      const uint32_t yw[4] = {yv.x, yv.y, yv.z, yv.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        a[2 * q] = fmaf(wj, __uint_as_float(yw[q] << 16), a[2 * q]);
-        a[2 * q + 1] = fmaf(wj, __uint_as_float(yw[q] & 0xFFFF0000u), a[2 * q + 1]);
-      }
-    }
-    const uint4 sv = __ldcg(reinterpret_cast<const uint4*>(p.out2 + static_cast<int64_t>(t) * p.ldo2 + h));
-    const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float lo = __uint_as_float(static_cast<uint32_t>(f32_to_bf16_rn(a[2 * q])) << 16) +
-                       __uint_as_float(sw[q] << 16);
-      const float hi = __uint_as_float(static_cast<uint32_t>(f32_to_bf16_rn(a[2 * q + 1])) << 16) +
-                       __uint_as_float(sw[q] & 0xFFFF0000u);
-      o[q] = static_cast<uint32_t>(f32_to_bf16_rn(lo)) | (static_cast<uint32_t>(f32_to_bf16_rn(hi)) << 16);
-    }
-    *reinterpret_cast<uint4*>(p.out3 + static_cast<int64_t>(t) * p.n_out + h) = make_uint4(o[0], o[1], o[2], o[3]);
+    if (h < p.n_out) moe_combine_item(p, t, h);
   }
+}
+
+// Tag a down_combine CTA leaves in a tile's counter when it gave up (a wait
+// ran out): the slab kernel's calls combine in a kernel of their own, which
+// skips tiles tagged with its call's epoch, so their outputs stay unwritten.
+__host__ __device__ constexpr unsigned long long abort_tag(uint32_t epoch) {
+  return (static_cast<unsigned long long>(epoch) << 32) | 0xFFFFFFFFull;
 }
 
 // SiLU with IEEE exp and division (the "exact" SiLU of the dense path).

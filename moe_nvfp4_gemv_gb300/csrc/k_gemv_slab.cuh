@@ -175,9 +175,6 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
   __shared__ volatile int s_abort;
   __shared__ int s_xbad[kSlabMaxStages];  // 1: the stage's activations are not all exact in f16
   __shared__ Work s_mwork;                // MoE: the CTA's work, resolved by the producer warp
-  __shared__ int s_last;                  // down_combine: this CTA arrived last on the tile's counter
-  __shared__ int s_target;                // down_combine: arrivals that complete a tile (active CTAs per tile)
-  __shared__ int s_hist[kDown ? kSlabMaxExperts : 1];  // down_combine: pairs per expert
 
   const int tid = threadIdx.x;
   const int warp = tid / 32;
@@ -205,28 +202,6 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
     }
     // (down_combine: the whole K; the host sets routed_tiles = shared_tiles
     // = the tile groups, and the box is moved to the group's tiles below)
-    if constexpr (kDown) {
-      // The CTAs that compute something for a tile group -- one per chunk of
-      // up to p.chunk pairs of an expert (valid ids only) and one per shared-
-      // expert token chunk -- are the arrivals a tile's combine waits for,
-      // so the CTAs of the other columns leave at once.  The ids are two
-      // kernels old (the router's, read by gate_up after its wait), so they
-      // are read before this grid's wait.
-      for (int i = tid; i < p.E; i += blockDim.x) s_hist[i] = 0;
-      __syncthreads();
-      for (int q = tid; q < p.P; q += blockDim.x) {
-        const int e = __ldg(p.ids + q);
-        if (e >= 0 && e < p.E) atomicAdd(&s_hist[e], 1);
-      }
-      __syncthreads();
-      if (warp == 0) {
-        const int cn = p.chunk > 0 && p.chunk < kChunk ? p.chunk : kChunk;  // (as resolve_work)
-        int t = 0;
-        for (int i = lane; i < p.E; i += 32) t += (s_hist[i] + cn - 1) / cn;
-        t = __reduce_add_sync(0xFFFFFFFFu, t);
-        if (lane == 0) s_target = t + (p.M + cn - 1) / cn;
-      }
-    }
   } else {
     const int tile = blockIdx.x / max(1u, S);
     wk.k_begin = static_cast<int>(rank) * p.k_split;
@@ -262,11 +237,7 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
                             : (wk.shared ? (p.shared_n_out + 63) / 64 : p.n_out / 64);
   const int tile0 = grouped ? static_cast<int>(blockIdx.x * tiles_h / gridDim.x) : 0;
   const int ntl = grouped ? static_cast<int>((blockIdx.x + 1) * tiles_h / gridDim.x) - tile0 : 1;
-  // down_combine: the CTAs of a tile group take its tiles in rotated orders
-  // (column y starts at tile y mod ntl), so their arrivals on one tile's
-  // counter are spread over the group's run instead of meeting at once.
-  const int rot = kDown && ntl > 0 ? static_cast<int>(blockIdx.y % static_cast<unsigned>(ntl)) : 0;
-  auto tile_of = [&](int tt) { return tile0 + (tt + rot < ntl ? tt + rot : tt + rot - ntl); };  // tile index
+  auto tile_of = [&](int tt) { return tile0 + tt; };  // tile index
   // The weight boxes of tile t (grouped modes).
   auto box_for_tile = [&](RfWork& w, int t) {
     if (kDown || !w.shared) {
@@ -456,18 +427,18 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
     };
     set_offsets(wk);
     // After a tile's last stage (grouped modes).  Every consumer warp calls
-    // it for the same tiles, also after a wait ran out (the first barrier
-    // agrees on the abort, which skips the tile's writes and arrival: its
-    // outputs stay unwritten); returns the abort.  The accumulators restart.
+    // it for the same tiles, also after a wait ran out; returns the abort.
+    // The accumulators restart.
     //   down_combine: the tile's y rows (y_j = bf16(acc * alpha2[e]) into
-    //     the workspace, or y_shared = bf16(acc * gssd)), then one arrival on
-    //     the tile's counter, tagged with this call's epoch; the CTA that
-    //     arrives last combines the tile:
-    //     out[t] = bf16(bf16(sum_j tw[t, j] * y[t, j]) + y_shared[t]).
+    //     the workspace, or y_shared = bf16(acc * gssd)), each warp its own
+    //     rows with no barrier: the combine is a kernel of its own, after
+    //     this grid.  A CTA that gave up tags its tiles instead (below).
     //   gate_up: the tile's sums staged in shared memory (row-major per B
-    //     row), then the 64 features' outputs as in the split epilogue.
+    //     row), then the 64 features' outputs as in the split epilogue; the
+    //     first barrier agrees on the abort, which skips the tile's writes
+    //     (its outputs stay unwritten).
     auto tile_done = [&](int tt) -> bool {
-      const bool ab = bar_red_or<1>(ncons, s_abort != 0);
+      const bool ab = kDown ? s_abort != 0 : bar_red_or<1>(ncons, s_abort != 0);
       const int t = tile_of(tt);
       const float post = static_cast<float>(1 << kShift);
       float v[kR][2][2];  // this thread's sums: row block, row half, token
@@ -508,25 +479,6 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
             }
           }
         }
-        cons_sync(ncons);  // this CTA's y rows of the tile are written
-        if (tid == 0 && ab) s_last = 0;
-        if (tid == 0 && !ab) {
-          __threadfence();
-          unsigned long long* ctr = p.counters + t;
-          const unsigned long long tag = static_cast<unsigned long long>(p.epoch) << 32;
-          unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(ctr), next;
-          for (;;) {
-            next = ((old & 0xFFFFFFFF00000000ull) == tag) ? old + 1 : tag + 1;
-            const unsigned long long seen = atomicCAS(ctr, old, next);
-            if (seen == old) break;
-            old = seen;
-          }
-          s_last = static_cast<int>(static_cast<uint32_t>(next)) == s_target;
-          if (s_last) atomicExch(ctr, 0ull);
-          __threadfence();
-        }
-        cons_sync(ncons);
-        if (s_last) moe_combine_tile(p, h0, tid, ncons);
       } else {
         if (!ab) {
 #pragma unroll
@@ -713,6 +665,10 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
     cluster_wait();  // the producer warp closes its cluster-barrier phase
   }
   __syncthreads();
+  // down_combine: a CTA that gave up tags each of its tiles with this call's
+  // epoch, and the combine kernel leaves those tiles' outputs unwritten.
+  if (kDown && tid == 0 && s_abort)
+    for (int tt = 0; tt < ntl; ++tt) p.counters[tile_of(tt)] = abort_tag(p.epoch);
 }
 
 }  // namespace fp4

@@ -4,7 +4,9 @@ stage -- no copy and no arrival, so nothing is in flight when a wait gives
 up -- and the wait limit is lowered to a few milliseconds.  The call must
 come back, the device error word must read FP4GEMV_ERR_TIMEOUT, the outputs
 must be left unwritten, and the next normal call must be correct.  Unsplit
-(one CTA per cluster) launches on both kernels that serve 1 .. 16 tokens."""
+(one CTA per cluster) launches on both kernels that serve 1 .. 16 tokens,
+and down_combine on the slab kernel, whose CTAs that gave up tag their row
+tiles so that the combine kernel after them leaves those outputs unwritten."""
 import numpy as np
 import pytest
 import torch
@@ -73,3 +75,29 @@ def test_timeout_path_then_recovery(fp4, M, N, K, kernel, skip):
 def test_skip_hook_rejects_bad_stage(fp4):
     with pytest.raises(Exception):
         fp4.debug_skip_stage(-2)
+
+
+# (I = 512: two 256-K stages per row tile; SI = 256: the shared expert's
+# CTAs have one, so skipping stage 1 stops only the routed CTAs.  The last
+# case streams two tiles per CTA and stops in the second: the CTA has
+# written the first tile's y rows, and both of its tiles are tagged.)
+@pytest.mark.parametrize("M,E,H,topk,T,skip", [(1, 16, 512, 2, 1, 1), (8, 16, 512, 2, 1, 0), (8, 128, 1024, 8, 2, 3)])
+def test_down_combine_timeout_then_recovery(fp4, M, E, H, topk, T, skip):
+    from test_gpu_moe import _down_slab_tiles, make_moe, ref_down, run_down
+    I, SI = 512, 256
+    assert _down_slab_tiles(fp4, M, topk, E, H, I, SI) == T
+    d = make_moe(M, E=E, H=H, I=I, SI=SI, topk=topk, seed=77 + M)
+    assert fp4.get_device_error() == 0
+    fp4.set_wait_limit_ns(5_000_000)  # 5 ms
+    fp4.debug_skip_stage(skip)
+    out = run_down(fp4, d)  # (filled with 7.0 before the call)
+    assert fp4.get_device_error() == TIMEOUT
+    assert (out == 7.0).all(), "outputs of a call that timed out must be left unwritten"
+    fp4.debug_skip_stage(-1)
+    fp4.set_wait_limit_ns(0)
+    out = run_down(fp4, d)
+    torch.cuda.synchronize()
+    assert fp4.get_device_error() == 0
+    ref, bad = ref_down(d)
+    assert bad == 0
+    assert_close(u16(out), ref, f"down_combine after the timeout M={M}")

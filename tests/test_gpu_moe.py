@@ -363,6 +363,36 @@ def test_down_combine_slab_decode_block(fp4):
     assert fp4.get_device_error() == 0
 
 
+def test_down_combine_slab_decode_block_one_token(fp4):
+    # one token of the E = 128, top-8, H = 4096, I = SI = 1536 block: one row
+    # tile per CTA at two CTAs per SM (288 CTAs, one wave), then the combine
+    # kernel; the whole output against the oracle
+    c = synth.MOE
+    assert _down_slab_tiles(fp4, 1, c["topk"], c["E"], c["H"], c["I"], c["SI"]) == 1
+    d = make_moe(1, c["E"], c["H"], c["I"], c["SI"], c["topk"], seed=102)
+    out = run_down(fp4, d)
+    ref, bad = ref_down(d)
+    assert bad == 0
+    assert_close(u16(out), ref, "down slab decode block M=1")
+    assert fp4.get_device_error() == 0
+
+
+# More than 256 experts: the slab kernel has no plan (its per-CTA expert
+# table holds 256), so down_combine runs on the register-fed kernel with its
+# in-kernel arrival counters and combine (one token: the converter-warp
+# variant; 8 tokens: the variant budgeted for three CTAs per SM).
+@pytest.mark.parametrize("M", [1, 8])
+def test_down_combine_register_fed_path(fp4, M):
+    E = 300
+    assert _down_slab_tiles(fp4, M, 2, E, 256, 256, 256) is None
+    d = make_moe(M, E=E, H=256, I=256, SI=256, topk=2, seed=1000 + M)
+    out = run_down(fp4, d)
+    ref, bad = ref_down(d)
+    assert bad == 0
+    assert_close(u16(out), ref, f"down register-fed M={M} E={E}")
+    assert fp4.get_device_error() == 0
+
+
 # gate_up in the grouped form (the whole H per CTA, several tiles per CTA in
 # turn): routed and shared tiles split unevenly over the groups, shared-
 # expert boxes that alternate between the halves of their 128-row scale

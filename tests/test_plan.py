@@ -411,21 +411,48 @@ def down_slab_fn():
 
 
 def down_slab_rule(M, topk, E, H, I, SI, sms=SMS):
-    """The rule written out: 2 <= M <= 64, E <= 256; chunks of 8 pairs (rows
-    min(P, 8) of max(I, SI) bf16), two tiles per CTA, three CTAs per SM, as
-    many 18 KB stages as fit beside the slab within a third of 228 KB less
-    4 KB (2 .. 8, at most two tiles' stages of I)."""
-    if M < 2 or M > 64 or E > 256:
+    """The rule written out: 1 <= M <= 64, E <= 256; chunks of 8 pairs (rows
+    min(P, 8) of max(I, SI) bf16).  Expected streaming columns C: the
+    expected distinct experts of P uniform draws (at least ceil(P / 8)
+    chunks) plus ceil(M / 8) shared-expert chunks; n(T) = C ceil(tiles / T).
+    One tile at two CTAs per SM when n(1) fits one wave of two per SM, two
+    tiles at two per SM when n(2) does, two tiles at three per SM when n(2)
+    fits one wave of three, one tile at three per SM when n(2) overflows that
+    wave by at most 10 %, else two tiles at three per SM.  As many 18 KB
+    stages as fit beside the slab within 228 KB / occ less 4 KB (2 .. 8, at
+    most T stage streams of I)."""
+    if M < 1 or M > 64 or E > 256:
         return None
-    rows = min(M * topk, 8)
+    P = M * topk
+    tiles = -(-H // 128)
+    cols = max(E * (1.0 - (1.0 - 1.0 / E) ** P), float(-(-P // 8))) + -(-M // 8)
+    n = lambda T: cols * -(-tiles // T)  # noqa: E731
+    if n(1) <= 2.0 * sms:
+        T, occ = 1, 2
+    elif n(2) <= 2.0 * sms:
+        T, occ = 2, 2
+    elif n(2) <= 3.0 * sms:
+        T, occ = 2, 3
+    elif n(2) <= 3.3 * sms:
+        T, occ = 1, 3
+    else:
+        T, occ = 2, 3
+    rows = min(P, 8)
     nst = -(-max(I, SI) // 256)
     slab = -(-(rows * nst * 512) // 1024) * 1024
-    ns = min(8, (228 * 1024 // 3 - 4096 - 1024 - slab) // 18432, 2 * -(-I // 256))
+    ns = min(8, (228 * 1024 // occ - 4096 - 1024 - slab) // 18432, T * -(-I // 256))
     if ns < 2:
         return None
-    tiles = -(-H // 128)
-    return dict(tiles_per_cta=2, groups=-(-tiles // 2), chunk_pairs=8, slab_bytes=slab, stages=ns, ctas_per_sm=3,
+    return dict(tiles_per_cta=T, groups=-(-tiles // T), chunk_pairs=8, slab_bytes=slab, stages=ns, ctas_per_sm=occ,
                 smem_bytes=1024 + slab + ns * 18432)
+
+
+def test_down_slab_rule_decode_block():
+    # the E = 128, top-8, H = 4096, I = SI = 1536 block on 152 SMs: the
+    # shapes the sweep found best at 1, 2, 4 and 8 tokens
+    c = (8, 128, 4096, 1536, 1536)
+    got = {M: (down_slab_rule(M, *c)["tiles_per_cta"], down_slab_rule(M, *c)["ctas_per_sm"]) for M in (1, 2, 3, 4, 8, 64)}
+    assert got == {1: (1, 2), 2: (2, 2), 3: (2, 3), 4: (1, 3), 8: (2, 3), 64: (2, 3)}
 
 
 @pytest.mark.parametrize("M,topk,E,H,I,SI", [(1, 8, 128, 4096, 1536, 1536), (8, 8, 128, 4096, 1536, 1536),
@@ -452,9 +479,11 @@ def test_down_slab_plan_matches_rule(down_slab_fn, M, topk, E, H, I, SI):
 
 
 def test_down_slab_plan_decode_block(down_slab_fn):
-    # E = 128, top-8, H = 4096, I = SI = 1536: one token stays on the
-    # register-fed kernel; 8 tokens, chunks of 8 pairs and two tiles per CTA
-    assert down_slab_fn(1, 8, 128, 4096, 1536, 1536)[0] == 2
+    # E = 128, top-8, H = 4096, I = SI = 1536: one token, one tile per CTA at
+    # two CTAs per SM (its 288 CTAs in one wave); 8 tokens, chunks of 8 pairs
+    # and two tiles per CTA at three per SM
+    st, p = down_slab_fn(1, 8, 128, 4096, 1536, 1536)
+    assert st == 0 and (p.tiles_per_cta, p.groups, p.chunk_pairs, p.ctas_per_sm) == (1, 32, 8, 2)
     st, p = down_slab_fn(8, 8, 128, 4096, 1536, 1536)
     assert st == 0 and (p.tiles_per_cta, p.groups, p.chunk_pairs, p.ctas_per_sm) == (2, 16, 8, 3)
 
