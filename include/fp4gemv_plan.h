@@ -97,9 +97,13 @@ typedef struct {
  * least 256 (one token on the E = 128, top-8, H = 4096, I = SI = 1536 block:
  * a split of two).  Otherwise, up to 64 tokens, the grouped form: the whole
  * H per CTA and T of its column's tiles in turn (T = 1 up to 2 tokens, else
- * 2), many waves of CTAs; chunks of 1 pair up to 2 tokens, 2 up to 16, 4
+ * 2), many waves of CTAs; chunks of 1 pair up to 2 tokens, 2 below 32, 4
  * from 32 (halved while fewer than two stages fit); three CTAs per SM, two
- * from 32 tokens; as many weight stages as fit (2 .. 8).
+ * from 32 tokens; as many weight stages as fit (2 .. 8).  From 3 to 31
+ * tokens, with n(T, c) = (E (1 - (1 - 1/E)^(M topk)), at least
+ * ceil(M topk / c)) + ceil(M / c) expected streaming columns times
+ * ceil(tiles / T) and f = n(2, 2) / (3 sms): f < 0.7 with n(2, 4) <= 2 sms
+ * takes T = 2, chunks of 4, two CTAs per SM; 0.9 < f <= 1.35 takes T = 1.
  * Returns FP4GEMV_ERR_INVALID_ARG for a null out, sms < 1 or regs < 1;
  * FP4GEMV_ERR_UNSUPPORTED_SHAPE for shapes fp4gemv_moe_gate_up rejects and
  * for calls the slab kernel does not serve (they run on the register-fed
@@ -133,10 +137,9 @@ typedef struct {
  * memory.  Chunks of 8 pairs.  With C = (E (1 - (1 - 1/E)^(M topk)), at
  * least ceil(M topk / 8)) + ceil(M / 8) expected streaming columns and
  * n(T) = C ceil(ceil(H / 128) / T) CTAs: T = 1 at two CTAs per SM if
- * n(1) <= 2 sms, else T = 2 at two per SM if n(2) <= 2 sms, else T = 2 at
- * three per SM if n(2) <= 3 sms, else T = 1 at three per SM if
- * n(2) <= 3.3 sms, else T = 2 at three per SM; as many weight stages as fit
- * (2 .. 8, at most T stage streams of I).
+ * n(1) <= 2 sms, else T = 2 at two per SM if n(2) <= 2 sms, else T = 1 at
+ * three per SM if 0.9 < n(2) / (3 sms) <= 1.35, else T = 2 at three per SM;
+ * as many weight stages as fit (2 .. 8, at most T stage streams of I).
  * Returns FP4GEMV_ERR_INVALID_ARG for a null out, sms < 1 or regs < 1;
  * FP4GEMV_ERR_UNSUPPORTED_SHAPE for shapes fp4gemv_moe_down_combine rejects
  * and for calls the slab kernel does not serve. */

@@ -524,9 +524,10 @@ bool plan_slab(int M, int N, int K, bool silu, int sms, int inbox_bytes, const i
 //            three CTAs per SM up to 16 tokens and pairs of 4 at two CTAs
 //            per SM (a deeper ring) from 32 (255 vs 265); fewer, longer
 //            CTAs were slower at every size (each CTA's stream is bounded
-//            by its ring, so the GPU needs many of them).  The ring takes
-//            as many stages as fit (2 .. 8); a chunk that leaves room for
-//            fewer than two is halved.
+//            by its ring, so the GPU needs many of them).  Where that grid
+//            fills a wave badly (below): 3 tokens 46.3 (55.6), 5: 71.5
+//            (81.1), 6: 85.2 (97.8), 7: 90.6 (100.0).  The ring takes as many stages as fit (2 .. 8); a
+//            chunk that leaves room for fewer than two is halved.
 struct SlabMoePlan {
   int S = 1, kslab = 0, T = 0, groups = 0, chunk = fp4::kSlabChunk, slab_bytes = 0, stage_bytes = 0, nstages = 2,
       occ = kSlabOcc;
@@ -571,9 +572,25 @@ bool plan_slab_moe(int M, int topk, int E, int H, int I, int SI, int sms, int re
   // grouped form
   const int nst = (H + 255) / 256;
   if (nst > fp4::kSlabMaxStages) return false;
-  const int occ = M >= 32 ? 2 : 3;
-  const int T = M <= 2 ? 1 : 2;
-  for (int chunk = M >= 32 ? 4 : M <= 2 ? 1 : 2; chunk >= 1; chunk /= 2) {
+  int occ = M >= 32 ? 2 : 3;
+  int T = M <= 2 ? 1 : 2;
+  int chunk0 = M >= 32 ? 4 : M <= 2 ? 1 : 2;
+  if (M >= 3 && M < 32) {
+    // Two exceptions by the CTAs that stream (the expected distinct experts
+    // of P uniform draws, at least ceil(P / c) chunks of c pairs, plus the
+    // shared expert's ceil(M / c) chunks, times the tile groups): two tiles
+    // of pairs of 2 filling less than 0.7 of a wave at three per SM take
+    // pairs of 4 at two per SM (deeper rings) if those fit one wave; more
+    // than 0.9 and at most 1.35 waves take one tile per CTA.
+    const double distinct = E * (1.0 - std::pow(1.0 - 1.0 / E, static_cast<double>(P)));
+    auto ctas = [&](int T_, int c) {
+      return (std::max(distinct, static_cast<double>((P + c - 1) / c)) + (M + c - 1) / c) * ((tiles + T_ - 1) / T_);
+    };
+    const double f = ctas(2, 2) / (3.0 * sms);
+    if (f < 0.7 && ctas(2, 4) <= 2.0 * sms) T = 2, chunk0 = 4, occ = 2;
+    else if (f > 0.9 && f <= 1.35) T = 1;
+  }
+  for (int chunk = chunk0; chunk >= 1; chunk /= 2) {
     const int rows = static_cast<int>(P < chunk ? P : chunk);
     const int slab = (rows * nst * 512 + 1023) / 1024 * 1024;
     const long room = static_cast<long>(kSmemPerSm / occ - kSmemPerCta) - 1024 - slab - fp4::SlabInboxBytes;
@@ -608,14 +625,15 @@ std::atomic<int> g_slab_moe_regs[kMaxDevices];
 // expert's token chunks as the columns, times ceil(tiles / T):
 //   one tile per CTA at two CTAs per SM if those fit in one wave (deeper
 //   rings), else two tiles at two per SM if they fit, else two tiles at
-//   three per SM, except when that overflows one wave by at most 10 % (then
-//   one tile at three per SM: twice as many CTAs of half the length).
+//   three per SM, except when those fill more than 0.9 and at most 1.35
+//   waves (then one tile at three per SM: twice as many CTAs of half the
+//   length, and no nearly empty second wave of long ones).
 // Measured on the E = 128, top-8, H = 4096, I = SI = 1536 block (us per
 // call, L2-cold, 8 routings; a sweep of T = 1, 2, 3, 4, chunks of 2, 4, 8
 // and two or three CTAs per SM): 1 token 15.7 (register-fed kernel 17.9),
 // 2 tokens 25.6 (two tiles at three per SM: 32.8), 3: 33.4, 4: 44.8 (two
-// tiles: 50.0), 8: 68.8, 16: 107.7, 32: 153.1, 64: 196.8 (T = 3 or 4 within
-// 2 %).
+// tiles: 50.0), 5: 50.3 (54.8), 6: 59.6, 8: 68.8, 16: 107.7, 32: 153.1,
+// 64: 196.8 (T = 3 or 4 within 2 %).
 struct SlabDownPlan {
   int T = 2, groups = 1, chunk = 8, slab_bytes = 0, stage_bytes = 0, nstages = 2, occ = 3;
   size_t smem = 0;
@@ -634,10 +652,10 @@ bool plan_slab_down(int M, int topk, int E, int H, int I, int SI, int sms, int r
   const double cols = std::max(distinct, static_cast<double>((P + chunk - 1) / chunk)) + (M + chunk - 1) / chunk;
   auto ctas = [&](int T) { return cols * ((tiles + T - 1) / T); };
   int T = 2, occ = 3;
+  const double f = ctas(2) / (3.0 * sms);  // waves of two-tile CTAs at three per SM
   if (ctas(1) <= 2.0 * sms) T = 1, occ = 2;
   else if (ctas(2) <= 2.0 * sms) T = 2, occ = 2;
-  else if (ctas(2) <= 3.0 * sms) T = 2, occ = 3;
-  else if (ctas(2) <= 3.3 * sms) T = 1, occ = 3;
+  else if (f > 0.9 && f <= 1.35) T = 1, occ = 3;
   if (static_cast<long>(occ) * (cw + 1) * warp_regs > 65536) return false;
   const int rows = static_cast<int>(P < chunk ? P : chunk);
   const int kmax = I > SI ? I : SI;

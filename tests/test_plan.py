@@ -314,7 +314,11 @@ def moe_slab_rule(M, topk, E, H, I, SI, sms=SMS):
     form (M <= 64): the whole H, T = 1 tile per CTA up to 2 tokens else 2;
     chunks of 1 (M <= 2), 2 (M < 32) or 4 pairs, halved while fewer than two
     20 KB stages fit; three CTAs per SM, two from 32 tokens; as many stages
-    as fit (<= 8, <= T stages of H)."""
+    as fit (<= 8, <= T stages of H).  For 3 <= M < 32, with n(T, c) the
+    expected streaming CTAs (expected distinct experts of P uniform draws, at
+    least ceil(P / c), plus ceil(M / c), times ceil(tiles / T)) and
+    f = n(2, 2) / (3 sms): f < 0.7 and n(2, 4) <= 2 sms gives T = 2, pairs of
+    4, two CTAs per SM; 0.9 < f <= 1.35 gives T = 1."""
     if M > 64:
         return None
     P = M * topk
@@ -338,6 +342,14 @@ def moe_slab_rule(M, topk, E, H, I, SI, sms=SMS):
     occ = 2 if M >= 32 else 3
     T = 1 if M <= 2 else 2
     chunk = 4 if M >= 32 else 1 if M <= 2 else 2
+    if 3 <= M < 32:
+        d = E * (1.0 - (1.0 - 1.0 / E) ** P)
+        n = lambda T_, c: (max(d, float(-(-P // c))) + -(-M // c)) * -(-tiles // T_)  # noqa: E731
+        f = n(2, 2) / (3.0 * sms)
+        if f < 0.7 and n(2, 4) <= 2.0 * sms:
+            T, chunk, occ = 2, 4, 2
+        elif 0.9 < f <= 1.35:
+            T = 1
     while chunk >= 1:
         rows = min(P, chunk)
         slab = -(-(rows * nst * 512) // 1024) * 1024
@@ -416,9 +428,9 @@ def down_slab_rule(M, topk, E, H, I, SI, sms=SMS):
     expected distinct experts of P uniform draws (at least ceil(P / 8)
     chunks) plus ceil(M / 8) shared-expert chunks; n(T) = C ceil(tiles / T).
     One tile at two CTAs per SM when n(1) fits one wave of two per SM, two
-    tiles at two per SM when n(2) does, two tiles at three per SM when n(2)
-    fits one wave of three, one tile at three per SM when n(2) overflows that
-    wave by at most 10 %, else two tiles at three per SM.  As many 18 KB
+    tiles at two per SM when n(2) does, one tile at three per SM when n(2)
+    fills more than 0.9 and at most 1.35 waves of three per SM, else two
+    tiles at three per SM.  As many 18 KB
     stages as fit beside the slab within 228 KB / occ less 4 KB (2 .. 8, at
     most T stage streams of I)."""
     if M < 1 or M > 64 or E > 256:
@@ -427,13 +439,12 @@ def down_slab_rule(M, topk, E, H, I, SI, sms=SMS):
     tiles = -(-H // 128)
     cols = max(E * (1.0 - (1.0 - 1.0 / E) ** P), float(-(-P // 8))) + -(-M // 8)
     n = lambda T: cols * -(-tiles // T)  # noqa: E731
+    f = n(2) / (3.0 * sms)
     if n(1) <= 2.0 * sms:
         T, occ = 1, 2
     elif n(2) <= 2.0 * sms:
         T, occ = 2, 2
-    elif n(2) <= 3.0 * sms:
-        T, occ = 2, 3
-    elif n(2) <= 3.3 * sms:
+    elif 0.9 < f <= 1.35:
         T, occ = 1, 3
     else:
         T, occ = 2, 3
@@ -447,12 +458,23 @@ def down_slab_rule(M, topk, E, H, I, SI, sms=SMS):
                 smem_bytes=1024 + slab + ns * 18432)
 
 
+def test_moe_slab_rule_decode_block():
+    # gate_up of the E = 128, top-8, H = 4096, I = SI = 1536 block on 152
+    # SMs: the shapes the sweep found best (split form at one token)
+    c = (8, 128, 4096, 1536, 1536)
+    got = {M: (moe_slab_rule(M, *c)["split"], moe_slab_rule(M, *c)["tiles_per_cta"], moe_slab_rule(M, *c)["chunk_pairs"],
+               moe_slab_rule(M, *c)["ctas_per_sm"]) for M in (1, 2, 3, 4, 5, 6, 7, 8, 9, 32)}
+    assert got == {1: (2, 0, 4, 3), 2: (1, 1, 1, 3), 3: (1, 2, 4, 2), 4: (1, 2, 2, 3), 5: (1, 1, 2, 3), 6: (1, 1, 2, 3),
+                   7: (1, 1, 2, 3), 8: (1, 2, 2, 3), 9: (1, 2, 2, 3), 32: (1, 2, 4, 2)}
+
+
 def test_down_slab_rule_decode_block():
     # the E = 128, top-8, H = 4096, I = SI = 1536 block on 152 SMs: the
     # shapes the sweep found best at 1, 2, 4 and 8 tokens
     c = (8, 128, 4096, 1536, 1536)
-    got = {M: (down_slab_rule(M, *c)["tiles_per_cta"], down_slab_rule(M, *c)["ctas_per_sm"]) for M in (1, 2, 3, 4, 8, 64)}
-    assert got == {1: (1, 2), 2: (2, 2), 3: (2, 3), 4: (1, 3), 8: (2, 3), 64: (2, 3)}
+    got = {M: (down_slab_rule(M, *c)["tiles_per_cta"], down_slab_rule(M, *c)["ctas_per_sm"])
+           for M in (1, 2, 3, 4, 5, 6, 8, 64)}
+    assert got == {1: (1, 2), 2: (2, 2), 3: (2, 3), 4: (1, 3), 5: (1, 3), 6: (2, 3), 8: (2, 3), 64: (2, 3)}
 
 
 @pytest.mark.parametrize("M,topk,E,H,I,SI", [(1, 8, 128, 4096, 1536, 1536), (8, 8, 128, 4096, 1536, 1536),
