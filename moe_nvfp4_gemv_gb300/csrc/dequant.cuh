@@ -136,6 +136,17 @@ __device__ __forceinline__ void scale_pair_to_f16x2(uint32_t two_bytes, uint32_t
   hi = prmt(h, h, 0x3232u);
 }
 
+// The same scales times a replicated f16x2 `mul` (a power of two that keeps
+// every product exact, see the slab kernel's shifted f16 route).
+__device__ __forceinline__ void scale_pair_to_f16x2_scaled(uint32_t two_bytes, uint32_t mul, uint32_t& lo,
+                                                           uint32_t& hi) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(static_cast<unsigned short>(two_bytes & 0xFFFFu)));
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(h) : "r"(h), "r"(mul));
+  lo = prmt(h, h, 0x1010u);
+  hi = prmt(h, h, 0x3232u);
+}
+
 // bf16 pair -> f16 pair; false if either value is not exactly representable
 // in f16 (too large, too small for its bits, or NaN).
 __device__ __forceinline__ bool bf16x2_to_f16x2_exact(uint32_t v, uint32_t& out) {

@@ -48,26 +48,76 @@ struct SlabCfg {
 // Named barrier 1 over the first n threads (the consumer warps).
 __device__ __forceinline__ void cons_sync(int n) { asm volatile("bar.sync 1, %0;" ::"r"(n) : "memory"); }
 
-// Eight bf16 values -> eight f16 values; false if any is not exact in f16.
-__device__ __forceinline__ bool bf16x8_to_f16x8_exact(const uint4& v, uint4& o) {
-  bool e = bf16x2_to_f16x2_exact(v.x, o.x);
-  e &= bf16x2_to_f16x2_exact(v.y, o.y);
-  e &= bf16x2_to_f16x2_exact(v.z, o.z);
-  e &= bf16x2_to_f16x2_exact(v.w, o.w);
-  return e;
+// f16 route with a power-of-two shift.  A stage's activations x run on the
+// f16 route as x 2^s (f16) against weights e2m1 * (e4m3 2^-s) (f16), whose
+// products equal x * e2m1 * e4m3 exactly: x 2^s is exact in f16 when every
+// nonzero x 2^s lies in f16's normal range (a bf16 has 8 significant bits,
+// a normal f16 11), and e4m3 2^-s and e2m1 * e4m3 2^-s are multiples of
+// 2^-24 below 2^12 for s <= 14 (every e4m3 value is a multiple of 2^-9).
+// So the shift moves the exponent between the operands and the products,
+// and the accumulator, are those of the unshifted route.
+//
+// Largest and smallest biased exponent fields of the nonzero values among
+// eight bf16 values (zeros give 0 and 255; a bf16 subnormal gives 0).
+__device__ __forceinline__ void bf16x8_exp_range(const uint4& v, int& emax, int& emin) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  emax = 0;
+  emin = 255;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const uint32_t a = (w[q] >> (16 * half)) & 0x7FFFu;
+      const int e = static_cast<int>(a >> 7);
+      emax = max(emax, e);
+      emin = min(emin, a != 0u ? e : 255);
+    }
+  }
+}
+
+// The shift of a stage whose nonzero activations have biased exponent
+// fields in [emin, emax]: the largest s <= 14 with every x 2^s below 2^16
+// (x < 2^(emax - 126)) and at least 2^-14 (x >= 2^(emin - 127)), or -1 when
+// there is none (Inf, NaN, bf16 subnormals, or a range wider than f16's):
+// the stage takes the bf16 route.
+__device__ __forceinline__ int f16_shift(int emax, int emin) {
+  const int s = min(14, 142 - emax);
+  return (s >= 0 && s >= 113 - emin) ? s : -1;
+}
+
+// Eight bf16 values times 2^s (mul = 2^s) -> eight f16 values, exact when s
+// is the stage's f16_shift.
+__device__ __forceinline__ uint4 bf16x8_to_f16x8_scaled(const uint4& v, float mul) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float lo = __uint_as_float(w[q] << 16) * mul;
+    const float hi = __uint_as_float(w[q] & 0xFFFF0000u) * mul;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(o[q]) : "f"(hi), "f"(lo));
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Replicated f16x2 of 2^-s (0 <= s <= 14: a normal f16).
+__device__ __forceinline__ uint32_t f16x2_pow2_neg(int s) {
+  const uint32_t b = static_cast<uint32_t>(15 - s) << 10;
+  return b | (b << 16);
 }
 
 // One 128-K half h of a 256-K stage for a consumer warp of the slab
 // kernels (f16 route): thread (g, c) of the warp, its kR row blocks' code
 // rows at w_off and scale bytes at sf_off in the stage at `st`, the stage's
 // activations at `xs` (64-K atoms of M rows x 128 bytes, 16-byte chunks
-// XOR-swizzled by row % 8, f16).  `cvalid` false (a chunk past the end of a
-// ragged last stage) gives zero A registers: that chunk's scales were not
-// copied and may hold anything.
+// XOR-swizzled by row % 8, f16, times 2^s), the scales times 2^-s (sdown:
+// f16x2_pow2_neg(s)).  `cvalid` false (a chunk past the end of a ragged last
+// stage) gives zero A registers: that chunk's scales were not copied and may
+// hold anything.
 template <int kR, int kChains>
 __device__ __forceinline__ void slab_half_f16(float (&acc)[kChains][kR][4], uint32_t st, uint32_t xs, int h,
                                               bool cvalid, int M, const uint32_t (&w_off)[kR][2],
-                                              const uint32_t (&sf_off)[kR][2], uint32_t key, int g, int c) {
+                                              const uint32_t (&sf_off)[kR][2], uint32_t key, int g, int c,
+                                              uint32_t sdown) {
   const int j = 4 * h + c;
   uint4 A[kR][2];
   uint32_t slo[kR][2], shi[kR][2];
@@ -77,7 +127,7 @@ __device__ __forceinline__ void slab_half_f16(float (&acc)[kChains][kR][4], uint
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
       A[b][hr] = lds128(st + w_off[b][hr] + ((static_cast<uint32_t>(j) ^ key) * 16));
-      scale_pair_to_f16x2(lds16(st + sf_off[b][hr] + sc_off), slo[b][hr], shi[b][hr]);
+      scale_pair_to_f16x2_scaled(lds16(st + sf_off[b][hr] + sc_off), sdown, slo[b][hr], shi[b][hr]);
       if (!cvalid) slo[b][hr] = shi[b][hr] = 0u;
     }
   }
@@ -173,7 +223,8 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
   __shared__ __align__(8) uint64_t bar_empty[kMaxStages];
   __shared__ __align__(8) uint64_t bar_inbox;
   __shared__ volatile int s_abort;
-  __shared__ int s_xbad[kSlabMaxStages];  // 1: the stage's activations are not all exact in f16
+  __shared__ int s_emax[kSlabMaxStages];  // per stage: largest / smallest biased exponent field of the
+  __shared__ int s_emin[kSlabMaxStages];  // nonzero activations (the stage's f16_shift)
   __shared__ Work s_mwork;                // MoE: the CTA's work, resolved by the producer warp
 
   const int tid = threadIdx.x;
@@ -311,7 +362,10 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
     for (int s = 0; s < pre; ++s)
       if (s != p.skip_stage) issue_weights(s, s);  // (test hook: the skipped stage is never issued)
   }
-  for (int i = tid; i < nst_tile; i += blockDim.x) s_xbad[i] = 0;
+  for (int i = tid; i < nst_tile; i += blockDim.x) {
+    s_emax[i] = 0;
+    s_emin[i] = 255;
+  }
   __syncthreads();
   if (S > 1) cluster_arrive_relaxed();  // paired with a wait before the first remote access
   if (tid == 0) pdl_launch_dependents();
@@ -358,8 +412,9 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
     }
   } else {
     // ------------------------------------------------------------------ consumers
-    // The activation slab: bf16 chunks in (pass 1, with an exactness check
-    // per stage), then the exact stages to f16 in place (pass 2).
+    // The activation slab: bf16 chunks in (pass 1, with each stage's
+    // exponent range), then the stages with an f16 shift to x 2^s in f16 in
+    // place (pass 2); the others stay bf16 for the bf16 route.
     // K past the end of a ragged last stage is zero-filled (the same bits in
     // bf16 and f16), so the zero weights there meet zero activations.
     pdl_wait();
@@ -389,19 +444,26 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
         const int s = kq / 32, u = (kq % 32) / 8, ch = kq % 8;
         const uint32_t a = slab + s * slab_stage + (u * M + n) * 128 + ((ch ^ (n & 7)) * 16);
         sts128(a, v[i]);
-        uint4 o;
-        if (!bf16x8_to_f16x8_exact(v[i], o)) atomicOr(&s_xbad[s], 1);
+        // (a warp's 32 chunks share a token and a stage: M nslot and nslot
+        // are multiples of 32, and so is the first q of every warp)
+        int emx, emn;
+        bf16x8_exp_range(v[i], emx, emn);
+        emx = __reduce_max_sync(0xFFFFFFFFu, emx);
+        emn = __reduce_min_sync(0xFFFFFFFFu, emn);
+        if (lane == 0) {
+          atomicMax(&s_emax[s], emx);
+          atomicMin(&s_emin[s], emn);
+        }
       }
     }
     cons_sync(ncons);
     for (int q = tid; q < M * nchk; q += ncons) {
       const int n = q / nchk, kq = q % nchk;
       const int s = kq / 32, u = (kq % 32) / 8, ch = kq % 8;
-      if (s_xbad[s]) continue;
+      const int sh = f16_shift(s_emax[s], s_emin[s]);
+      if (sh < 0) continue;
       const uint32_t a = slab + s * slab_stage + (u * M + n) * 128 + ((ch ^ (n & 7)) * 16);
-      uint4 o;
-      bf16x8_to_f16x8_exact(lds128(a), o);
-      sts128(a, o);
+      sts128(a, bf16x8_to_f16x8_scaled(lds128(a), __int_as_float((127 + sh) << 23)));
     }
     cons_sync(ncons);
 
@@ -547,12 +609,16 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
       // valid K of the stage: 64 .. 256 in steps of 64; a chunk (32 K) is
       // wholly valid or wholly past the end
       const int kvalid = min(256, klen - ks * 256);
-      if (!s_xbad[ks]) {
+      const int sh = f16_shift(s_emax[ks], s_emin[ks]);
+      if (sh >= 0) {
+        const uint32_t sdown = f16x2_pow2_neg(sh);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           if (128 * h < kvalid) {
-            if (128 * (h + 1) <= kvalid) slab_half_f16<kR, kChains>(acc, st, xs, h, true, M, w_off, sf_off, key, g, c);
-            else slab_half_f16<kR, kChains>(acc, st, xs, h, 32 * (4 * h + c) < kvalid, M, w_off, sf_off, key, g, c);
+            if (128 * (h + 1) <= kvalid)
+              slab_half_f16<kR, kChains>(acc, st, xs, h, true, M, w_off, sf_off, key, g, c, sdown);
+            else
+              slab_half_f16<kR, kChains>(acc, st, xs, h, 32 * (4 * h + c) < kvalid, M, w_off, sf_off, key, g, c, sdown);
           }
         }
       } else {
