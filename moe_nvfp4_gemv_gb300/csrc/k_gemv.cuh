@@ -220,29 +220,46 @@ __device__ __forceinline__ float bf16_to_f32(uint16_t h) { return __uint_as_floa
 // down_combine of 8 consecutive h of token t: out[t, h .. h + 7] =
 // bf16(bf16(sum_j tw[t, j] * y[t, j, h]) + y_shared[t, h]), the sum in fp32
 // over j = 0 .. topk - 1 with fused multiply-adds (16-byte loads of y and
-// y_shared, one 16-byte store).  A token with an out-of-range id is left
-// unwritten.
+// y_shared, one 16-byte store).  The loads of up to kJ j are issued before
+// any is used (one round trip per group of kJ, not per j); the sum keeps the
+// j order, so kJ does not change the result.  A token with an out-of-range
+// id is left unwritten.
+template <int kJ = 8>
 __device__ __forceinline__ void moe_combine_item(const GemvParams& p, int t, int h) {
+  const uint4 sv = __ldcg(reinterpret_cast<const uint4*>(p.out2 + static_cast<int64_t>(t) * p.ldo2 + h));
   bool ids_ok = true;
-  for (int j = 0; j < p.topk; ++j) {
-    const int e = __ldg(p.ids + t * p.topk + j);
-    ids_ok = ids_ok && e >= 0 && e < p.E;
-  }
-  if (!ids_ok) return;
   float a[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) a[i] = 0.0f;
-  for (int j = 0; j < p.topk; ++j) {
-    const float wj = __ldg(p.tw + t * p.topk + j);
-    const uint4 yv = __ldcg(reinterpret_cast<const uint4*>(p.out + static_cast<int64_t>(t * p.topk + j) * p.ldo + h));
-    const uint32_t yw[4] = {yv.x, yv.y, yv.z, yv.w};
+  for (int j0 = 0; j0 < p.topk; j0 += kJ) {
+    int e[kJ];
+    float wj[kJ];
+    uint4 yv[kJ];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      a[2 * q] = fmaf(wj, __uint_as_float(yw[q] << 16), a[2 * q]);
-      a[2 * q + 1] = fmaf(wj, __uint_as_float(yw[q] & 0xFFFF0000u), a[2 * q + 1]);
+    for (int jj = 0; jj < kJ; ++jj) {
+      const int j = j0 + jj;
+      e[jj] = 0;
+      wj[jj] = 0.0f;
+      yv[jj] = make_uint4(0u, 0u, 0u, 0u);
+      if (j < p.topk) {
+        e[jj] = __ldg(p.ids + t * p.topk + j);
+        wj[jj] = __ldg(p.tw + t * p.topk + j);
+        yv[jj] = __ldcg(reinterpret_cast<const uint4*>(p.out + static_cast<int64_t>(t * p.topk + j) * p.ldo + h));
+      }
+    }
+#pragma unroll
+    for (int jj = 0; jj < kJ; ++jj) {
+      if (j0 + jj >= p.topk) break;
+      ids_ok = ids_ok && e[jj] >= 0 && e[jj] < p.E;
+      const uint32_t yw[4] = {yv[jj].x, yv[jj].y, yv[jj].z, yv[jj].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        a[2 * q] = fmaf(wj[jj], __uint_as_float(yw[q] << 16), a[2 * q]);
+        a[2 * q + 1] = fmaf(wj[jj], __uint_as_float(yw[q] & 0xFFFF0000u), a[2 * q + 1]);
+      }
     }
   }
-  const uint4 sv = __ldcg(reinterpret_cast<const uint4*>(p.out2 + static_cast<int64_t>(t) * p.ldo2 + h));
+  if (!ids_ok) return;
   const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
   uint32_t o[4];
 #pragma unroll
@@ -259,10 +276,11 @@ __device__ __forceinline__ void moe_combine_item(const GemvParams& p, int t, int
 // down_combine of one 128-row tile of H (rows h0 .. h0 + 127) by `nthr`
 // threads (this one is `ti`); a work item is 8 consecutive h of one token
 // (H is a multiple of 64, so an item is wholly inside or outside H).
+template <int kJ = 8>
 __device__ __forceinline__ void moe_combine_tile(const GemvParams& p, int h0, int ti, int nthr) {
   for (int it = ti; it < 16 * p.M; it += nthr) {
     const int t = it / 16, h = h0 + 8 * (it % 16);
-    if (h < p.n_out) moe_combine_item(p, t, h);
+    if (h < p.n_out) moe_combine_item<kJ>(p, t, h);
   }
 }
 

@@ -788,7 +788,7 @@ __global__ void __launch_bounds__(RfCfg<kNT>::kThreads, kOcc) gemv_rf_kernel(con
       epi_sync<kEpiThreads>();
       if (s_last) {
         pdl_wait();
-        moe_combine_tile(p, blockIdx.x * 128, tid, kEpiThreads);
+        moe_combine_tile<kOcc >= 3 ? 2 : 8>(p, blockIdx.x * 128, tid, kEpiThreads);  // (64 registers at three CTAs per SM)
       }
     }
   } else if (S > 1) {
