@@ -30,6 +30,8 @@
 // are those of the register-fed kernel.
 #pragma once
 
+#include <type_traits>
+
 #include "k_gemv_rf.cuh"
 
 namespace fp4 {
@@ -48,7 +50,17 @@ struct SlabCfg {
 // Named barrier 1 over the first n threads (the consumer warps).
 __device__ __forceinline__ void cons_sync(int n) { asm volatile("bar.sync 1, %0;" ::"r"(n) : "memory"); }
 
-// f16 route with a power-of-two shift.  A stage's activations x run on the
+// Eight bf16 values -> eight f16 values; false if any is not exact in f16.
+__device__ __forceinline__ bool bf16x8_to_f16x8_exact(const uint4& v, uint4& o) {
+  bool e = bf16x2_to_f16x2_exact(v.x, o.x);
+  e &= bf16x2_to_f16x2_exact(v.y, o.y);
+  e &= bf16x2_to_f16x2_exact(v.z, o.z);
+  e &= bf16x2_to_f16x2_exact(v.w, o.w);
+  return e;
+}
+
+// f16 route with a power-of-two shift (stages with a value that is not an
+// exact f16 as it is).  A stage's activations x run on the
 // f16 route as x 2^s (f16) against weights e2m1 * (e4m3 2^-s) (f16), whose
 // products equal x * e2m1 * e4m3 exactly: x 2^s is exact in f16 when every
 // nonzero x 2^s lies in f16's normal range (a bf16 has 8 significant bits,
@@ -109,11 +121,11 @@ __device__ __forceinline__ uint32_t f16x2_pow2_neg(int s) {
 // kernels (f16 route): thread (g, c) of the warp, its kR row blocks' code
 // rows at w_off and scale bytes at sf_off in the stage at `st`, the stage's
 // activations at `xs` (64-K atoms of M rows x 128 bytes, 16-byte chunks
-// XOR-swizzled by row % 8, f16, times 2^s), the scales times 2^-s (sdown:
-// f16x2_pow2_neg(s)).  `cvalid` false (a chunk past the end of a ragged last
+// XOR-swizzled by row % 8, f16, times 2^s), the scales times 2^-s (kScaled;
+// sdown: f16x2_pow2_neg(s)).  `cvalid` false (a chunk past the end of a ragged last
 // stage) gives zero A registers: that chunk's scales were not copied and may
 // hold anything.
-template <int kR, int kChains>
+template <int kR, int kChains, bool kScaled>
 __device__ __forceinline__ void slab_half_f16(float (&acc)[kChains][kR][4], uint32_t st, uint32_t xs, int h,
                                               bool cvalid, int M, const uint32_t (&w_off)[kR][2],
                                               const uint32_t (&sf_off)[kR][2], uint32_t key, int g, int c,
@@ -127,7 +139,8 @@ __device__ __forceinline__ void slab_half_f16(float (&acc)[kChains][kR][4], uint
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
       A[b][hr] = lds128(st + w_off[b][hr] + ((static_cast<uint32_t>(j) ^ key) * 16));
-      scale_pair_to_f16x2_scaled(lds16(st + sf_off[b][hr] + sc_off), sdown, slo[b][hr], shi[b][hr]);
+      if constexpr (kScaled) scale_pair_to_f16x2_scaled(lds16(st + sf_off[b][hr] + sc_off), sdown, slo[b][hr], shi[b][hr]);
+      else scale_pair_to_f16x2(lds16(st + sf_off[b][hr] + sc_off), slo[b][hr], shi[b][hr]);
       if (!cvalid) slo[b][hr] = shi[b][hr] = 0u;
     }
   }
@@ -223,8 +236,14 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
   __shared__ __align__(8) uint64_t bar_empty[kMaxStages];
   __shared__ __align__(8) uint64_t bar_inbox;
   __shared__ volatile int s_abort;
-  __shared__ int s_emax[kSlabMaxStages];  // per stage: largest / smallest biased exponent field of the
-  __shared__ int s_emin[kSlabMaxStages];  // nonzero activations (the stage's f16_shift)
+  // bit s: stage s has an activation that is not an exact f16 (down_combine:
+  // every stage takes the shifted route)
+  __shared__ uint32_t s_xbad[kSlabMaxStages / 32];
+  // such a stage: largest / smallest biased exponent field of its nonzero
+  // activations (its f16_shift); down_combine gathers them with atomics
+  using ExpT = std::conditional_t<kDown, int, uint8_t>;
+  __shared__ ExpT s_emax[kSlabMaxStages];
+  __shared__ ExpT s_emin[kSlabMaxStages];
   __shared__ Work s_mwork;                // MoE: the CTA's work, resolved by the producer warp
 
   const int tid = threadIdx.x;
@@ -362,9 +381,12 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
     for (int s = 0; s < pre; ++s)
       if (s != p.skip_stage) issue_weights(s, s);  // (test hook: the skipped stage is never issued)
   }
-  for (int i = tid; i < nst_tile; i += blockDim.x) {
-    s_emax[i] = 0;
-    s_emin[i] = 255;
+  for (int i = tid; i < kSlabMaxStages / 32; i += blockDim.x) s_xbad[i] = kDown ? 0xFFFFFFFFu : 0u;
+  if constexpr (kDown) {
+    for (int i = tid; i < nst_tile; i += blockDim.x) {
+      s_emax[i] = 0;
+      s_emin[i] = 255;
+    }
   }
   __syncthreads();
   if (S > 1) cluster_arrive_relaxed();  // paired with a wait before the first remote access
@@ -412,9 +434,13 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
     }
   } else {
     // ------------------------------------------------------------------ consumers
-    // The activation slab: bf16 chunks in (pass 1, with each stage's
-    // exponent range), then the stages with an f16 shift to x 2^s in f16 in
-    // place (pass 2); the others stay bf16 for the bf16 route.
+    // The activation slab: bf16 chunks in (pass 1, with an exactness check
+    // per stage); stages with an inexact value get their exponent range (pass
+    // 1b, only if there are any); then the exact stages to f16 in place and
+    // the others with an f16 shift to x 2^s (pass 2); the rest stay bf16 for
+    // the bf16 route.  down_combine, whose activations (gate_up's outputs)
+    // are often not all exact f16s, takes every stage's range in pass 1 and
+    // shifts every stage (a measured 4 % on the call).
     // K past the end of a ragged last stage is zero-filled (the same bits in
     // bf16 and f16), so the zero weights there meet zero activations.
     pdl_wait();
@@ -444,26 +470,61 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
         const int s = kq / 32, u = (kq % 32) / 8, ch = kq % 8;
         const uint32_t a = slab + s * slab_stage + (u * M + n) * 128 + ((ch ^ (n & 7)) * 16);
         sts128(a, v[i]);
-        // (a warp's 32 chunks share a token and a stage: M nslot and nslot
-        // are multiples of 32, and so is the first q of every warp)
-        int emx, emn;
-        bf16x8_exp_range(v[i], emx, emn);
-        emx = __reduce_max_sync(0xFFFFFFFFu, emx);
-        emn = __reduce_min_sync(0xFFFFFFFFu, emn);
-        if (lane == 0) {
-          atomicMax(&s_emax[s], emx);
-          atomicMin(&s_emin[s], emn);
+        if constexpr (kDown) {
+          // (a warp's 32 chunks share a token and a stage: M nslot and nslot
+          // are multiples of 32, and so is the first q of every warp)
+          int emx, emn;
+          bf16x8_exp_range(v[i], emx, emn);
+          emx = __reduce_max_sync(0xFFFFFFFFu, emx);
+          emn = __reduce_min_sync(0xFFFFFFFFu, emn);
+          if (lane == 0) {
+            atomicMax(&s_emax[s], emx);
+            atomicMin(&s_emin[s], emn);
+          }
+        } else {
+          uint4 o;
+          if (!bf16x8_to_f16x8_exact(v[i], o)) atomicOr(&s_xbad[s / 32], 1u << (s % 32));
         }
       }
     }
     cons_sync(ncons);
+    auto xbad = [&](int s) { return (s_xbad[s / 32] >> (s % 32)) & 1u; };
+    bool any_bad = false;
+    for (int i = 0; i < kSlabMaxStages / 32; ++i) any_bad |= s_xbad[i] != 0u;
+    if (!kDown && any_bad) {
+      // one warp per such stage: the exponent range of its M x 32 chunks
+      // (chunks past the end of K hold zeros)
+      for (int s = warp; s < nst_tile; s += cw) {
+        if (!xbad(s)) continue;
+        int emx = 0, emn = 255;
+        for (int q = lane; q < M * 32; q += 32) {
+          const int n = q / 32, u = (q % 32) / 8, ch = q % 8;
+          int e1, e2;
+          bf16x8_exp_range(lds128(slab + s * slab_stage + (u * M + n) * 128 + ((ch ^ (n & 7)) * 16)), e1, e2);
+          emx = max(emx, e1);
+          emn = min(emn, e2);
+        }
+        emx = __reduce_max_sync(0xFFFFFFFFu, emx);
+        emn = __reduce_min_sync(0xFFFFFFFFu, emn);
+        if (lane == 0) {
+          s_emax[s] = static_cast<uint8_t>(emx);
+          s_emin[s] = static_cast<uint8_t>(emn);
+        }
+      }
+      cons_sync(ncons);
+    }
     for (int q = tid; q < M * nchk; q += ncons) {
       const int n = q / nchk, kq = q % nchk;
       const int s = kq / 32, u = (kq % 32) / 8, ch = kq % 8;
-      const int sh = f16_shift(s_emax[s], s_emin[s]);
-      if (sh < 0) continue;
       const uint32_t a = slab + s * slab_stage + (u * M + n) * 128 + ((ch ^ (n & 7)) * 16);
-      sts128(a, bf16x8_to_f16x8_scaled(lds128(a), __int_as_float((127 + sh) << 23)));
+      if (!kDown && !xbad(s)) {
+        uint4 o;
+        bf16x8_to_f16x8_exact(lds128(a), o);
+        sts128(a, o);
+        continue;
+      }
+      const int sh = f16_shift(s_emax[s], s_emin[s]);
+      if (sh >= 0) sts128(a, bf16x8_to_f16x8_scaled(lds128(a), __int_as_float((127 + sh) << 23)));
     }
     cons_sync(ncons);
 
@@ -609,16 +670,27 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
       // valid K of the stage: 64 .. 256 in steps of 64; a chunk (32 K) is
       // wholly valid or wholly past the end
       const int kvalid = min(256, klen - ks * 256);
-      const int sh = f16_shift(s_emax[ks], s_emin[ks]);
-      if (sh >= 0) {
+      const bool bad = kDown || ((s_xbad[ks / 32] >> (ks % 32)) & 1u);
+      const int sh = bad ? f16_shift(s_emax[ks], s_emin[ks]) : 0;
+      if (!bad) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (128 * h < kvalid) {
+            if (128 * (h + 1) <= kvalid)
+              slab_half_f16<kR, kChains, false>(acc, st, xs, h, true, M, w_off, sf_off, key, g, c, 0u);
+            else
+              slab_half_f16<kR, kChains, false>(acc, st, xs, h, 32 * (4 * h + c) < kvalid, M, w_off, sf_off, key, g, c, 0u);
+          }
+        }
+      } else if (sh >= 0) {
         const uint32_t sdown = f16x2_pow2_neg(sh);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           if (128 * h < kvalid) {
             if (128 * (h + 1) <= kvalid)
-              slab_half_f16<kR, kChains>(acc, st, xs, h, true, M, w_off, sf_off, key, g, c, sdown);
+              slab_half_f16<kR, kChains, true>(acc, st, xs, h, true, M, w_off, sf_off, key, g, c, sdown);
             else
-              slab_half_f16<kR, kChains>(acc, st, xs, h, 32 * (4 * h + c) < kvalid, M, w_off, sf_off, key, g, c, sdown);
+              slab_half_f16<kR, kChains, true>(acc, st, xs, h, 32 * (4 * h + c) < kvalid, M, w_off, sf_off, key, g, c, sdown);
           }
         }
       } else {
