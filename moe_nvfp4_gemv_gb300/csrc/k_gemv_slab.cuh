@@ -409,6 +409,17 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
   }
   const int g = lane / 4, c = lane % 4;
   const int sg = (g % 2) * 4 + g / 2;  // sigma(g)
+  // Tile row of this thread's MMA row sg + 8 hr in row block b.  gate_up's
+  // grouped form pairs a feature's two rows in one thread: warp w's block 0
+  // holds rows 16 w .. 16 w + 15 and block 1 the rows 64 below them (a
+  // routed [up; gate] group's up and gate rows, a shared pair's gate and up
+  // rows), so the tile epilogue needs no exchange.  Other forms: the warp's
+  // kR consecutive 16-row blocks.
+  constexpr bool kPairRows = kMode == kMoeGateUp && kGroupedUp;
+  static_assert(!kPairRows || kR == 2, "paired rows: two 16-row blocks per warp, 128-row tiles");
+  auto tile_row = [&](int b, int hr) {
+    return kPairRows ? b * 64 + warp * 16 + sg + 8 * hr : (warp * kR + b) * 16 + sg + 8 * hr;
+  };
 
   if (warp == cw) {
     // ------------------------------------------------------------------ producer
@@ -537,7 +548,7 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
       for (int b = 0; b < kR; ++b) {
 #pragma unroll
         for (int hr = 0; hr < 2; ++hr) {
-          const int row = (warp * kR + b) * 16 + sg + 8 * hr;
+          const int row = tile_row(b, hr);
           w_off[b][hr] = (row / 8) * 1024 + (row % 8) * 128;
           const int half = trows / 2;
           const bool b1 = w.paired && row >= half;
@@ -556,12 +567,14 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
     //     the workspace, or y_shared = bf16(acc * gssd)), each warp its own
     //     rows with no barrier: the combine is a kernel of its own, after
     //     this grid.  A CTA that gave up tags its tiles instead (below).
-    //   gate_up: the tile's sums staged in shared memory (row-major per B
-    //     row), then the 64 features' outputs as in the split epilogue; the
-    //     first barrier agrees on the abort, which skips the tile's writes
-    //     (its outputs stay unwritten).
+    //   gate_up (grouped form): each thread holds both rows of its features
+    //     (tile_row) and writes their outputs, with no barrier; a warp that
+    //     saw a wait run out writes nothing (the tile's outputs stay
+    //     unwritten).  Otherwise the tile's sums are staged in shared memory
+    //     (row-major per B row), then the 64 features' outputs as in the
+    //     split epilogue; the first barrier agrees on the abort.
     auto tile_done = [&](int tt) -> bool {
-      const bool ab = kDown ? s_abort != 0 : bar_red_or<1>(ncons, s_abort != 0);
+      const bool ab = (kDown || kPairRows) ? s_abort != 0 : bar_red_or<1>(ncons, s_abort != 0);
       const int t = tile_of(tt);
       const float post = static_cast<float>(1 << kShift);
       float v[kR][2][2];  // this thread's sums: row block, row half, token
@@ -602,13 +615,37 @@ __global__ void __launch_bounds__(kSlabThreads, kSlabMinBlocks) gemv_slab_kernel
             }
           }
         }
+      } else if constexpr (kPairRows) {
+        // this thread's features 16 w + sg + 8 hr, tokens 2 c + e: block 0
+        // holds the up (routed) or gate (shared) row, block 1 the other
+        if (!ab) {
+          const float sc = wk.shared ? __ldg(p.gs) : __ldg(p.alpha + wk.expert);
+#pragma unroll
+          for (int hr = 0; hr < 2; ++hr) {
+            const int feat = t * 64 + warp * 16 + sg + 8 * hr;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int n = 2 * c + e;
+              if (n >= M) continue;
+              if (!wk.shared) {
+                if (feat < p.n_out)
+                  p.out[static_cast<int64_t>(s_mwork.orow[n]) * p.ldo + feat] =
+                      f32_to_bf16_rn(silu_fast(v[1][hr][e] * sc) * (v[0][hr][e] * sc));
+              } else if (feat < p.shared_n_out) {
+                const float G = bf16_to_f32(f32_to_bf16_rn(v[0][hr][e] * sc));
+                const float U = bf16_to_f32(f32_to_bf16_rn(v[1][hr][e] * sc));
+                p.out2[static_cast<int64_t>(s_mwork.orow[n]) * p.ldo2 + feat] = f32_to_bf16_rn(silu_exact(G) * U);
+              }
+            }
+          }
+        }
       } else {
         if (!ab) {
 #pragma unroll
           for (int b = 0; b < kR; ++b) {
 #pragma unroll
             for (int hr = 0; hr < 2; ++hr) {
-              const int row = (warp * kR + b) * 16 + sg + 8 * hr;
+              const int row = tile_row(b, hr);
 #pragma unroll
               for (int e = 0; e < 2; ++e) {
                 const int n = 2 * c + e;
