@@ -214,7 +214,7 @@ fp4gemv_status fp4gemv_set_wait_limit_ns(uint64_t ns);
 
 /* Test hook for the timeout path (no counterpart on the pages): from now on
  * the producers of the dense NVFP4 GEMV for 1 .. 16 tokens, and of
- * fp4gemv_moe_down_combine on the slab kernel (1 .. 64 tokens, E <= 256),
+ * fp4gemv_moe_down_combine on the slab kernel (1 .. 64 tokens, where its plan applies),
  * issue nothing at all -- no copy, no arrival -- for the 256-K ring stage
  * with this index of every CTA (down_combine: counted over the CTA's row
  * tiles in turn), so the consumers' bounded wait for it runs out with no

@@ -132,9 +132,9 @@ typedef struct {
  *   sms:  streaming multiprocessors of the GPU (152 on GB300).
  *   regs: registers per thread of the kernel.
  *   out:  HOST pointer, filled on success.
- * Applies to 1 <= M <= 64 and E <= 256 when up to 8 activation rows of
- * max(I, SI) and two weight stages fit the CTA's share of the SM's shared
- * memory.  Chunks of 8 pairs.  With C = (E (1 - (1 - 1/E)^(M topk)), at
+ * Applies to 1 <= M <= 64 when up to 8 activation rows of max(I, SI) and
+ * two weight stages fit the CTA's share of the SM's shared memory, and the
+ * CTA's T tiles of I hold at least two 256-K stages.  Chunks of 8 pairs.  With C = (E (1 - (1 - 1/E)^(M topk)), at
  * least ceil(M topk / 8)) + ceil(M / 8) expected streaming columns and
  * n(T) = C ceil(ceil(H / 128) / T) CTAs: T = 1 at two CTAs per SM if
  * n(1) <= 2 sms, else T = 2 at two per SM if n(2) <= 2 sms, else T = 1 at

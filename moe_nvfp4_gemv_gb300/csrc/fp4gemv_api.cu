@@ -644,7 +644,7 @@ constexpr int kSmemPerCtaDown = 4096;  // reservation + static shared memory
 bool plan_slab_down(int M, int topk, int E, int H, int I, int SI, int sms, int regs, SlabDownPlan* sp) {
   const int cw = fp4::kSlabMaxCW;
   const int warp_regs = (regs * 32 + 255) / 256 * 256;
-  if (sms < 1 || E > fp4::kSlabMaxExperts || M < 1 || M > 64) return false;
+  if (sms < 1 || M < 1 || M > 64) return false;
   const long P = static_cast<long>(M) * topk;
   const int chunk = fp4::kSlabNT;
   const int tiles = (H + 127) / 128;
@@ -1196,8 +1196,9 @@ fp4gemv_status fp4gemv_moe_down_combine(const void* act, const int32_t* ids, con
   fp4gemv_status st = device_state(&err, &sms);
   if (st != FP4GEMV_OK) return st;
   // Up to 64 tokens the slab kernel when its plan fits (plan_slab_down),
-  // then the combine kernel; otherwise (more than 256 experts, or activation
-  // rows too long for the slab) the register-fed kernel for up to 64 tokens,
+  // then the combine kernel; otherwise (CTAs that would stream fewer than
+  // two 256-K stages, or activation rows too long for the slab) the
+  // register-fed kernel for up to 64 tokens,
   // chunks of at most 8 pairs (as gate_up), the tcgen05 kernel beyond.  From
   // 8 tokens the register-fed grid holds many short CTAs (K = I is a few
   // stages): the variant budgeted for three CTAs per SM (72 KB ring) hides

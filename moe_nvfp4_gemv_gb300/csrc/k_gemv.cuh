@@ -79,7 +79,6 @@ constexpr int kSlabMaxStages = 64;  // slab kernel: K per CTA <= 64 stages of 25
 constexpr int kSlabMaxCW = 4;       // slab kernel: consumer warps (tiles of 16 kSlabR cw rows: 64 or 128)
 constexpr int kSlabChunk = 4;       // slab kernel, MoE: pairs of one expert per CTA (B rows)
 constexpr int kSlabNT = 8;          // slab kernel: MMA N (tokens / pairs 0 .. 7)
-constexpr int kSlabMaxExperts = 256;  // slab kernel, down_combine: experts counted in shared memory
 constexpr int SlabInboxBytes = 8 * (128 + 16) * 4;  // slab kernel: split-K inbox (8 tokens x 144 rows, fp32)
 
 struct GemvParams {

@@ -377,10 +377,11 @@ def test_down_combine_slab_decode_block_one_token(fp4):
     assert fp4.get_device_error() == 0
 
 
-# More than 256 experts: the slab kernel has no plan (its per-CTA expert
-# table holds 256), so down_combine runs on the register-fed kernel with its
-# in-kernel arrival counters and combine (one token: the converter-warp
-# variant; 8 tokens: the variant budgeted for three CTAs per SM).
+# I = 256, a single 256-K stage: the slab kernel has no plan (its ring would
+# hold fewer than two stages), so down_combine runs on the register-fed
+# kernel with its in-kernel arrival counters and combine (one token: the
+# converter-warp variant; 8 tokens: the variant budgeted for three CTAs per
+# SM).  Then 300 experts on the slab kernel (no per-CTA expert table).
 @pytest.mark.parametrize("M", [1, 8])
 def test_down_combine_register_fed_path(fp4, M):
     E = 300
@@ -390,6 +391,18 @@ def test_down_combine_register_fed_path(fp4, M):
     ref, bad = ref_down(d)
     assert bad == 0
     assert_close(u16(out), ref, f"down register-fed M={M} E={E}")
+    assert fp4.get_device_error() == 0
+
+
+@pytest.mark.parametrize("M", [1, 8])
+def test_down_combine_slab_many_experts(fp4, M):
+    E = 300
+    assert _down_slab_tiles(fp4, M, 2, E, 256, 512, 256) is not None
+    d = make_moe(M, E=E, H=256, I=512, SI=256, topk=2, seed=1100 + M)
+    out = run_down(fp4, d)
+    ref, bad = ref_down(d)
+    assert bad == 0
+    assert_close(u16(out), ref, f"down slab M={M} E={E}")
     assert fp4.get_device_error() == 0
 
 

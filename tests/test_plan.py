@@ -423,7 +423,7 @@ def down_slab_fn():
 
 
 def down_slab_rule(M, topk, E, H, I, SI, sms=SMS):
-    """The rule written out: 1 <= M <= 64, E <= 256; chunks of 8 pairs (rows
+    """The rule written out: 1 <= M <= 64; chunks of 8 pairs (rows
     min(P, 8) of max(I, SI) bf16).  Expected streaming columns C: the
     expected distinct experts of P uniform draws (at least ceil(P / 8)
     chunks) plus ceil(M / 8) shared-expert chunks; n(T) = C ceil(tiles / T).
@@ -433,7 +433,7 @@ def down_slab_rule(M, topk, E, H, I, SI, sms=SMS):
     tiles at three per SM.  As many 18 KB
     stages as fit beside the slab within 228 KB / occ less 4 KB (2 .. 8, at
     most T stage streams of I)."""
-    if M < 1 or M > 64 or E > 256:
+    if M < 1 or M > 64:
         return None
     P = M * topk
     tiles = -(-H // 128)
