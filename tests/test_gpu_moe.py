@@ -377,6 +377,25 @@ def test_down_combine_slab_decode_block_one_token(fp4):
     assert fp4.get_device_error() == 0
 
 
+# More experts per token than one group of the combine's loads (8), and a
+# single expert per token: gate_up and down_combine (slab kernel, then the
+# combine kernel) against the oracle.
+@pytest.mark.parametrize("M,topk", [(3, 12), (20, 12), (2, 1)])
+def test_moe_topk_beyond_one_load_group(fp4, M, topk):
+    E, H, I, SI = 32, 384, 512, 256
+    d = make_moe(M, E=E, H=H, I=I, SI=SI, topk=topk, seed=1200 + M + topk)
+    act, sact = run_gate_up(fp4, d)
+    (an, al, ah), (sn, sl, sh), bad = ref_gate_up(d)
+    assert bad == 0
+    assert_close(u16(act), (an, al, ah), f"act M={M} topk={topk}")
+    assert_close(u16(sact), (sn, sl, sh), f"sact M={M} topk={topk}")
+    out = run_down(fp4, d)
+    ref, bad = ref_down(d)
+    assert bad == 0
+    assert_close(u16(out), ref, f"down M={M} topk={topk}")
+    assert fp4.get_device_error() == 0
+
+
 # I = 256, a single 256-K stage: the slab kernel has no plan (its ring would
 # hold fewer than two stages), so down_combine runs on the register-fed
 # kernel with its in-kernel arrival counters and combine (one token: the
