@@ -150,13 +150,16 @@ fp4gemv_status fp4gemv_moe_gate_up(const void* x, const int32_t* ids, int M, int
                                    int pdl, cudaStream_t stream);
 
 /* Scratch bytes fp4gemv_moe_down_combine needs for M tokens, top-k and
- * hidden size H: per-row-tile arrival counters, then the bf16 y_j and
- * y_shared values.  The contents need no initialisation and carry nothing
+ * hidden size H: per-row-tile counters (arrival counts, or the tags of row
+ * tiles whose computation gave up), then the bf16 y_j and y_shared values.  The contents need no initialisation and carry nothing
  * between calls; one workspace serves calls of any shape that fit in it.
  * Calls that may run concurrently on the GPU must not share a workspace. */
 size_t fp4gemv_moe_down_combine_workspace_bytes(int M, int topk, int H);
 
-/* down_combine (vllm.models.flint.ops.moe_gemv, down_combine), one launch:
+/* down_combine (vllm.models.flint.ops.moe_gemv, down_combine).  When the
+ * slab kernel serves the call (fp4gemv_plan_moe_down_slab) its grid is
+ * followed by a small combine kernel on the same stream (two launches);
+ * otherwise one launch combines in its last CTAs:
  *   y_j  = bf16(fp32(act[t*topk+j] . W2[e_j] row h) * alpha2[e_j])
  *   y_sh = bf16(fp32(sact[t] . Wsd row h) * gssd[0])
  *   out[t, h] = bf16(bf16(sum_j tw[t, j] * y_j) + y_sh)   (fp32 sum, j order)

@@ -275,7 +275,8 @@ def moe_workspace(device: torch.device, nbytes: int, stream: int | None = None) 
 
 def moe_down_combine(act, ids, tw, w2, w2_sf, alpha2, sact, wsd, ssd, gssd, out, pdl: bool = True,
                      workspace: torch.Tensor | None = None) -> None:
-    """out[t] = bf16(bf16(sum_j tw[t,j] * y_j) + y_shared), one launch."""
+    """out[t] = bf16(bf16(sum_j tw[t,j] * y_j) + y_shared): the GEMV grid,
+    then (slab kernel) a small combine kernel on the same stream."""
     M, topk = ids.shape
     E, H, I = w2.shape[0], w2.shape[1], w2.shape[2] * 2
     SI = wsd.shape[1] * 2
