@@ -1,19 +1,26 @@
-// k_gemv_slab.cuh -- the dense NVFP4 GEMV for 1 .. 8 tokens with the CTA's
-// activations resident in shared memory.
+// k_gemv_slab.cuh -- the NVFP4 GEMV with the CTA's activations resident in
+// shared memory: the dense GEMV for 1 .. 4 tokens on large weights, and the
+// MoE pair (gate_up: split and grouped forms; down_combine: grouped, its
+// combine a kernel of its own after the grid).
 //
-// Same operation as the dense mode of k_gemv_rf.cuh (vllm.models.flint.ops.
-// nvfp4_gemv, nvfp4_gemv, with or without silu_mul), organised so that the
-// only per-stage traffic is the weight stream:
+// Same operations as the register-fed kernel k_gemv_rf.cuh
+// (vllm.models.flint.ops.nvfp4_gemv, nvfp4_gemv, with or without silu_mul;
+// vllm.models.flint.ops.moe_gemv, gate_up and down_combine), organised so
+// that the only per-stage traffic is the weight stream:
 //
-//   * The CTA's activation slab, x[0 .. M)[k_begin .. k_end), is read from
-//     global memory once, after griddepcontrol.wait, by all consumer threads
-//     and kept in shared memory for the whole launch (64-K atoms of M rows x
-//     128 bytes, 16-byte chunks XOR-swizzled by token).  A 256-K stage whose
-//     activations are all exactly representable in f16 is converted to f16
-//     in place (the f16 route: cvt.rn.f16x2.e2m1x2 on the weights, f16
-//     MMAs); any other stage keeps its bf16 values and runs the bf16
-//     bit-placement route (dequant.cuh).  Both routes form exact products
-//     and accumulate in fp32, separately, summed at the end.
+//   * The CTA's activation slab, x[0 .. M)[k_begin .. k_end) (MoE: the rows
+//     of its chunk of pairs of one expert), is read from global memory once,
+//     after griddepcontrol.wait, by all consumer threads and kept in shared
+//     memory for the whole launch (64-K atoms of M rows x 128 bytes, 16-byte
+//     chunks XOR-swizzled by token).  A 256-K stage whose activations are
+//     all exactly representable in f16 is converted to f16 in place (the f16
+//     route: cvt.rn.f16x2.e2m1x2 on the weights, f16 MMAs); a stage whose
+//     values fit f16's normal range after a power-of-two shift s takes the
+//     same route with x 2^s and the scales times 2^-s (exact, the same
+//     products); any other stage keeps its bf16 values and runs the bf16
+//     bit-placement route (dequant.cuh).  The routes form exact products and
+//     accumulate in fp32 (f16 route and bf16 route separately, summed at the
+//     end).
 //   * The ring holds only weights and their scale groups (TMA boxes and
 //     bulk copies).  The producer warp never waits for the previous grid:
 //     weights are not written by it, so the ring fills completely under PDL.
@@ -21,13 +28,18 @@
 //     on one full barrier per stage and releases the stage with one arrival.
 //   * The block has exactly cw consumer warps and the producer warp (the
 //     host launches (cw + 1) x 32 threads), so no warp sits idle.
+//   * Grouped MoE forms stream T row tiles per CTA in turn over the same
+//     resident rows, the ring running across the tile boundary; each tile's
+//     outputs are written from registers without a CTA barrier (gate_up
+//     pairs each feature's up and gate rows in one thread).
 //
 // Fragment mapping as in k_gemv_rf.cuh: thread (g, c) of consumer warp w
 // holds, for each of its kR 16-row blocks b, MMA rows g and g + 8 = tile rows
-// 16 (kR w + b) + sigma(g) and + 8, sigma = (0 4 1 5 2 6 3 7); in 128-K half h
-// of a stage it reads code chunk 4 h + c of both rows.  The K split over the
-// S CTAs of a cluster and its reduction through distributed shared memory
-// are those of the register-fed kernel.
+// 16 (kR w + b) + sigma(g) and + 8, sigma = (0 4 1 5 2 6 3 7) (gate_up's
+// grouped form: 64 b + 16 w + sigma(g)); in 128-K half h of a stage it reads
+// code chunk 4 h + c of both rows.  The K split over the S CTAs of a cluster
+// and its reduction through distributed shared memory are those of the
+// register-fed kernel.
 #pragma once
 
 #include <type_traits>
