@@ -1,4 +1,6 @@
-// k_gemv_rf.cuh -- the dense NVFP4 GEMV for M <= 16 with register-fed MMAs.
+// k_gemv_rf.cuh -- the NVFP4 GEMV for M <= 16 with register-fed MMAs: the
+// dense calls the slab kernel (k_gemv_slab.cuh) does not serve, and the MoE
+// calls of up to 64 tokens (chunks of up to 8 pairs) it has no plan for.
 //
 // Same operation as the dense mode of k_gemv.cuh (vllm.models.flint.ops.nvfp4_gemv
 // nvfp4_gemv, with or without silu_mul), built for the decode shapes where
@@ -32,7 +34,7 @@
 // registers of two MMAs, and the activation chunk of the same 8 K (token g,
 // permuted the same way) their B registers.
 //
-// Routes.  The bf16 route above serves 9-16 tokens (and MoE chunks of 5-8
+// Routes.  The bf16 route above serves 13-16 tokens (and MoE chunks of 5-8
 // pairs).  For M <= kF16MaxM the f16 route: a converter warp turns each
 // stage's activation rows in shared memory into f16 in place as soon as they
 // land (ahead of the consumers: its arrival is part of the stage's full
