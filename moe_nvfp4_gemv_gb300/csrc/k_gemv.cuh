@@ -1,9 +1,10 @@
 // k_gemv.cuh -- the small-M GEMV pipeline on tcgen05 tensor cores.
 //
-// One kernel template serves the dense NVFP4 GEMV (optionally with the fused
-// silu_mul epilogue), the BF16-weight GEMV, and both MoE kernels
-// (vllm.models.flint.ops.nvfp4_gemv nvfp4_gemv / bf16_gemv,
-// vllm.models.flint.ops.moe_gemv gate_up / down_combine).
+// One kernel template serves the dense NVFP4 GEMV above 16 tokens
+// (optionally with the fused silu_mul epilogue), the BF16-weight GEMV, and
+// both MoE kernels above 64 tokens (vllm.models.flint.ops.nvfp4_gemv
+// nvfp4_gemv / bf16_gemv, vllm.models.flint.ops.moe_gemv gate_up /
+// down_combine).
 //
 // Swap-AB: a CTA owns one tile of 128 weight rows (the MMA M dimension); the
 // tokens are the MMA N dimension (kNT = 16 .. 128).  A tile is either 128
@@ -14,7 +15,8 @@
 // memory in rank order (deterministic).
 //
 // Warp roles (kW dequant warpgroups, then a weight producer warp, an MMA
-// warp and, NVFP4 only, an activation producer warp and a permute warp):
+// warp and, NVFP4 only, an activation producer warp and, for tiles of up to
+// 32 tokens, a permute warp):
 //   weights   lane 0 streams weight boxes (TMA, 128-byte swizzle) and the
 //             matching 512-byte scale chunks (bulk copies) into a ring of
 //             shared-memory stages of 256 K; with PDL the first stages are
@@ -26,11 +28,13 @@
 //             the weight ring, which hides HBM latency, is not shortened by
 //             activations that come from L2.  BF16: a stage's activations
 //             travel in the weight stage, loaded by the weight producer.
-//   permute   (NVFP4) as each slice lands, its activations in place into
-//             the weight pairs' K order (dequant.cuh), then an arrival the
-//             MMA warp waits for, so the dequant warps never wait for
-//             activations (measured at 32 tokens: ~0.6 us of waiting and
-//             ~0.3 us of permuting per slice when they did).
+//   permute   (NVFP4, up to 32 tokens) as each slice lands, its activations
+//             in place into the weight pairs' K order (dequant.cuh), then an
+//             arrival the MMA warp waits for, so the dequant warps never wait
+//             for activations (measured at 32 tokens: ~0.6 us of waiting and
+//             ~0.3 us of permuting per slice when they did).  Larger tiles:
+//             the dequant warps permute their share of each slice (one warp
+//             was too slow for 64 and 128 tokens).
 //   dequant   warpgroup w takes the 128-wide K slices q = w, w + kW, ...  For
 //             each slice thread i (row i) reads its code bytes and scale
 //             bytes (then frees its warp's share of the weight stage),
