@@ -151,14 +151,16 @@ fp4gemv_status fp4gemv_moe_gate_up(const void* x, const int32_t* ids, int M, int
 
 /* Scratch bytes fp4gemv_moe_down_combine needs for M tokens, top-k and
  * hidden size H: per-row-tile counters (arrival counts, or the tags of row
- * tiles whose computation gave up), then the bf16 y_j and y_shared values.  The contents need no initialisation and carry nothing
+ * tiles whose computation gave up) and one work counter of the persistent
+ * grid, then the bf16 y_j and y_shared values.  The contents need no initialisation and carry nothing
  * between calls; one workspace serves calls of any shape that fit in it.
  * Calls that may run concurrently on the GPU must not share a workspace. */
 size_t fp4gemv_moe_down_combine_workspace_bytes(int M, int topk, int H);
 
 /* down_combine (vllm.models.flint.ops.moe_gemv, down_combine).  When the
- * slab kernel serves the call (fp4gemv_plan_moe_down_slab) its grid is
- * followed by a small combine kernel on the same stream (two launches);
+ * slab kernel serves the call (fp4gemv_plan_moe_down_slab; one CTA per item
+ * or, beyond one wave, the persistent grid) it is followed by a small
+ * combine kernel on the same stream (two launches);
  * otherwise one launch combines in its last CTAs:
  *   y_j  = bf16(fp32(act[t*topk+j] . W2[e_j] row h) * alpha2[e_j])
  *   y_sh = bf16(fp32(sact[t] . Wsd row h) * gssd[0])
@@ -220,7 +222,8 @@ fp4gemv_status fp4gemv_set_wait_limit_ns(uint64_t ns);
  * fp4gemv_moe_down_combine on the slab kernel (1 .. 64 tokens, where its plan applies),
  * issue nothing at all -- no copy, no arrival -- for the 256-K ring stage
  * with this index of every CTA (down_combine: counted over the CTA's row
- * tiles in turn), so the consumers' bounded wait for it runs out with no
+ * tiles, and on the persistent grid over its items, in turn, the item
+ * stream's end counting as one stage), so the consumers' bounded wait for it runs out with no
  * copy in flight; -1 (the default) turns it off.  A process-wide host
  * setting read at each of those launches; for tests only.
  * FP4GEMV_ERR_INVALID_ARG for stage < -1. */

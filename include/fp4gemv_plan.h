@@ -120,6 +120,7 @@ typedef struct {
   int stage_bytes;    /* one weight stage (codes of 128 rows x 256 K, one scale group) */
   int stages;         /* weight ring stages (2 .. 8) */
   int ctas_per_sm;    /* CTAs per SM the ring is sized for (2 or 3) */
+  int persistent;     /* 1: a persistent grid of ctas_per_sm x sms CTAs takes the groups x columns items in turn */
   size_t smem_bytes;  /* dynamic shared memory per CTA */
 } fp4gemv_moe_down_slab_plan;
 
@@ -138,8 +139,13 @@ typedef struct {
  * least ceil(M topk / 8)) + ceil(M / 8) expected streaming columns and
  * n(T) = C ceil(ceil(H / 128) / T) CTAs: T = 1 at two CTAs per SM if
  * n(1) <= 2 sms, else T = 2 at two per SM if n(2) <= 2 sms, else T = 1 at
- * three per SM if 0.9 < n(2) / (3 sms) <= 1.35, else T = 2 at three per SM;
- * as many weight stages as fit (2 .. 8, at most T stage streams of I).
+ * three per SM if 0.9 < n(2) / (3 sms) <= 1.35, else T = 2 at three per SM.
+ * When that grid holds more than one wave (n(T) > CTAs per SM x sms), the
+ * persistent grid (persistent = 1): three CTAs per SM that take items of T
+ * tiles of one column in turn from a counter, T = 4 if n(4) >= 1.6 x 3 sms,
+ * else 2 if n(2) is, else 1.  As many weight stages as fit (2 .. 8; on
+ * the grid of one CTA per item at most T stage streams of I).  tiles_per_cta
+ * reports the largest group, ceil(tiles / groups).
  * Returns FP4GEMV_ERR_INVALID_ARG for a null out, sms < 1 or regs < 1;
  * FP4GEMV_ERR_UNSUPPORTED_SHAPE for shapes fp4gemv_moe_down_combine rejects
  * and for calls the slab kernel does not serve. */

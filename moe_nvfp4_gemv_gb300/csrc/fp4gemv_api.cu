@@ -628,14 +628,23 @@ std::atomic<int> g_slab_moe_regs[kMaxDevices];
 //   three per SM, except when those fill more than 0.9 and at most 1.35
 //   waves (then one tile at three per SM: twice as many CTAs of half the
 //   length, and no nearly empty second wave of long ones).
+// When that grid still holds more than one wave, the persistent form
+// (k_moe_down_persist.cuh) serves the call instead: three CTAs per SM take
+// the (tile group, column) items from a counter, so no slot idles while
+// another wave finishes; its items hold 4 tiles when that still gives every
+// slot 1.6 items or more on average, else 2 tiles when that does, else 1
+// (an item's start costs a few microseconds -- the activation rows'
+// round trip and the ring's restart -- so the longest items that still
+// spread evenly).
 // Measured on the E = 128, top-8, H = 4096, I = SI = 1536 block (us per
-// call, L2-cold, 8 routings; a sweep of T = 1, 2, 3, 4, chunks of 2, 4, 8
-// and two or three CTAs per SM): 1 token 15.7 (register-fed kernel 17.9),
-// 2 tokens 25.6 (two tiles at three per SM: 32.8), 3: 33.4, 4: 44.8 (two
-// tiles: 50.0), 5: 50.3 (54.8), 6: 59.6, 8: 68.8, 16: 107.7, 32: 153.1,
-// 64: 196.8 (T = 3 or 4 within 2 %).
+// call, L2-flushed by rotation, 8 routings; sweeps of T = 1 .. 4, chunks of
+// 2, 4, 8 and two or three CTAs per SM): one CTA per item 1 token 14.9,
+// 2 tokens 24.6, 3: 30.7; persistent 4 tokens 41.3 (one CTA per item:
+// 42.3), 5: 45.0, 6: 55.0, 8: 61.2 (66.6), 16: 91.5 (103.3), 32: 131.3
+// (148.3), 64: 177.2 (196.4; persistent with 2-tile items 183.2).
 struct SlabDownPlan {
   int T = 2, groups = 1, chunk = 8, slab_bytes = 0, stage_bytes = 0, nstages = 2, occ = 3;
+  bool persist = false;
   size_t smem = 0;
 };
 
@@ -656,6 +665,15 @@ bool plan_slab_down(int M, int topk, int E, int H, int I, int SI, int sms, int r
   if (ctas(1) <= 2.0 * sms) T = 1, occ = 2;
   else if (ctas(2) <= 2.0 * sms) T = 2, occ = 2;
   else if (f > 0.9 && f <= 1.35) T = 1, occ = 3;
+  // More CTAs than one wave: the persistent grid instead, three CTAs per
+  // SM, items of the most tiles (4, 2, 1) that still give every CTA slot
+  // 1.6 items or more on average.
+  const bool persist = ctas(T) > static_cast<double>(occ) * sms;
+  if (persist) {
+    occ = 3;
+    const double slots = 3.0 * sms;
+    T = ctas(4) >= 1.6 * slots ? 4 : ctas(2) >= 1.6 * slots ? 2 : 1;
+  }
   if (static_cast<long>(occ) * (cw + 1) * warp_regs > 65536) return false;
   const int rows = static_cast<int>(P < chunk ? P : chunk);
   const int kmax = I > SI ? I : SI;
@@ -666,10 +684,11 @@ bool plan_slab_down(int M, int topk, int E, int H, int I, int SI, int sms, int r
   const long room = static_cast<long>(kSmemPerSm / occ - kSmemPerCtaDown) - 1024 - slab;
   int ns = static_cast<int>(room / stage);
   if (ns > fp4::kMaxStages) ns = fp4::kMaxStages;
-  if (ns > T * ((I + 255) / 256)) ns = T * ((I + 255) / 256);  // (no deeper than a routed CTA's stream)
+  if (!persist && ns > T * ((I + 255) / 256)) ns = T * ((I + 255) / 256);  // (no deeper than a routed CTA's stream)
   if (ns < 2) return false;
-  sp->T = T;
   sp->groups = (tiles + T - 1) / T;
+  sp->T = (tiles + sp->groups - 1) / sp->groups;
+  sp->persist = persist;
   sp->chunk = chunk;
   sp->slab_bytes = slab;
   sp->stage_bytes = stage;
@@ -921,6 +940,7 @@ fp4gemv_status fp4gemv_plan_moe_down_slab(int M, int topk, int E, int H, int I, 
   out->stage_bytes = sp.stage_bytes;
   out->stages = sp.nstages;
   out->ctas_per_sm = sp.occ;
+  out->persistent = sp.persist ? 1 : 0;
   out->smem_bytes = sp.smem;
   return FP4GEMV_OK;
 }
@@ -1169,7 +1189,7 @@ fp4gemv_status fp4gemv_moe_gate_up(const void* x, const int32_t* ids, int M, int
 
 size_t fp4gemv_moe_down_combine_workspace_bytes(int M, int topk, int H) {
   if (M < 1 || topk < 1 || H < 1) return 0;
-  const size_t counters = ((static_cast<size_t>(H) + 127) / 128 * 8 + 15) / 16 * 16;
+  const size_t counters = ((static_cast<size_t>(H) + 127) / 128 * 8 + 8 + 15) / 16 * 16;  // (+ the work counter)
   const size_t y = (static_cast<size_t>(M) * topk * H * 2 + 15) / 16 * 16;
   const size_t ysh = (static_cast<size_t>(M) * H * 2 + 15) / 16 * 16;
   return counters + y + ysh;
@@ -1236,7 +1256,7 @@ fp4gemv_status fp4gemv_moe_down_combine(const void* act, const int32_t* ids, con
   if (!encode_2d(&p.tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w2, I / 2, static_cast<uint64_t>(E) * H, I / 2, 128, 128))
     return FP4GEMV_ERR_CUDA;
   if (!encode_2d(&p.tm_w2, CU_TENSOR_MAP_DATA_TYPE_UINT8, wsd, SI / 2, H, SI / 2, 128, 128)) return FP4GEMV_ERR_CUDA;
-  const size_t counters = ((static_cast<size_t>(H) + 127) / 128 * 8 + 15) / 16 * 16;
+  const size_t counters = ((static_cast<size_t>(H) + 127) / 128 * 8 + 8 + 15) / 16 * 16;  // (+ the work counter)
   const size_t ybytes = (static_cast<size_t>(M) * topk * H * 2 + 15) / 16 * 16;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.counters = reinterpret_cast<unsigned long long*>(ws);
@@ -1292,22 +1312,25 @@ fp4gemv_status fp4gemv_moe_down_combine(const void* act, const int32_t* ids, con
     p.slab_r = 2;
     p.tiles_per_cta = sdp.T;
     p.chunk = sdp.chunk;
-    p.routed_tiles = p.shared_tiles = sdp.groups;  // (a CTA's first tile is blockIdx.x * T)
+    p.routed_tiles = p.shared_tiles = sdp.groups;  // (slab grid: a CTA's first tile is blockIdx.x * T)
+    const int ncols = p.P + (M + sdp.chunk - 1) / sdp.chunk;
+    const long items = static_cast<long>(sdp.groups) * ncols;
     LaunchCfg cfg{};
-    cfg.grid = dim3(sdp.groups, p.P + (M + sdp.chunk - 1) / sdp.chunk, 1);
+    cfg.grid = sdp.persist ? dim3(static_cast<unsigned>(std::min<long>(items, static_cast<long>(sdp.occ) * sms)), 1, 1)
+                           : dim3(sdp.groups, ncols, 1);
     cfg.cluster = 1;
     cfg.smem = sdp.smem;
     cfg.pdl = pdl;
     cfg.stream = stream;
     g_launches.fetch_add(1, std::memory_order_relaxed);
-    st = from_cuda(fp4::launch_slab_moe(fp4::kMoeDown, p, cfg));
+    st = from_cuda(sdp.persist ? fp4::launch_moe_down_persist(p, cfg) : fp4::launch_slab_moe(fp4::kMoeDown, p, cfg));
     if (st != FP4GEMV_OK) return st;
     // The combine runs as a kernel of its own, launched early (PDL) and
     // waiting for the slab grid: measured, the slab CTAs' per-tile arrival
     // (fence, counter, the last CTA's combine) cost 20 % of the call.
-    const long items = static_cast<long>(M) * (H / 8);
+    const long citems = static_cast<long>(M) * (H / 8);
     LaunchCfg ccfg{};
-    ccfg.grid = dim3(static_cast<unsigned>(std::min<long>((items + 127) / 128, 4L * sms)), 1, 1);
+    ccfg.grid = dim3(static_cast<unsigned>(std::min<long>((citems + 127) / 128, 4L * sms)), 1, 1);
     ccfg.cluster = 1;
     ccfg.smem = 0;
     ccfg.pdl = 1;

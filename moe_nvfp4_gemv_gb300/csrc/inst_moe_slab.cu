@@ -1,16 +1,18 @@
 // Instantiations of the slab kernel's MoE modes: gate_up (routed chunks of
 // pairs of one expert and the shared expert's token chunks; split form: H
 // split over a cluster; grouped form: several tiles per CTA over one
-// resident activation slab) and down_combine (grouped), and the combine
-// kernel that follows the slab kernel's down_combine.
+// resident activation slab) and down_combine (grouped, one CTA per item,
+// and its persistent form), and the combine kernel that follows either.
 #include "k_gemv_slab.cuh"
+#include "k_moe_down_persist.cuh"
 #include "launch.h"
 
 namespace fp4 {
 
 // down_combine after the slab kernel: one thread per 8 consecutive h of one
-// token, grid-strided; waits for the previous grid (the slab kernel, whose y
-// rows it reads) and skips the tiles a CTA of that grid tagged as given up.
+// token, grid-strided; waits for the previous grid (the slab kernel or its
+// persistent form, whose y rows it reads) and skips the tiles a CTA of that
+// grid tagged as given up.
 __global__ void __launch_bounds__(128) moe_combine_kernel(const __grid_constant__ GemvParams p) {
   if (threadIdx.x == 0) pdl_launch_dependents();
   pdl_wait();
@@ -51,7 +53,15 @@ cudaError_t launch_slab_moe(int mode, const GemvParams& p, const LaunchCfg& cfg)
   return cudaErrorInvalidValue;
 }
 
-// (gate_up: the larger of its two forms)
+cudaError_t launch_moe_down_persist(const GemvParams& p, const LaunchCfg& cfg) {
+  if (p.cw != kSlabMaxCW || cfg.cluster != 1) return cudaErrorInvalidValue;
+  static int configured[64];  // per device (0 = not yet)
+  cudaError_t e = configure_kernel(moe_down_persist_kernel<2>, configured, cfg.smem, 1);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(moe_down_persist_kernel<2>, (p.cw + 1) * 32, p, cfg);
+}
+
+// (gate_up, down_combine: the larger of their two forms)
 cudaError_t slab_moe_regs(int mode, int* regs) {
   cudaFuncAttributes a, b;
   cudaError_t e = cudaErrorInvalidValue;
@@ -59,8 +69,10 @@ cudaError_t slab_moe_regs(int mode, int* regs) {
     e = cudaFuncGetAttributes(&a, gemv_slab_kernel<2, kMoeGateUp>);
     if (e == cudaSuccess) e = cudaFuncGetAttributes(&b, gemv_slab_kernel<2, kMoeGateUp, true>);
     if (e == cudaSuccess && b.numRegs > a.numRegs) a.numRegs = b.numRegs;
-  } else if (mode == kMoeDown) {
+  } else if (mode == kMoeDown) {  // (the larger of the grid and the persistent form)
     e = cudaFuncGetAttributes(&a, gemv_slab_kernel<2, kMoeDown>);
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&b, moe_down_persist_kernel<2>);
+    if (e == cudaSuccess && b.numRegs > a.numRegs) a.numRegs = b.numRegs;
   }
   if (e == cudaSuccess) *regs = a.numRegs;
   return e;

@@ -330,14 +330,14 @@ __device__ __forceinline__ void set_box(Work& w, int b, int wrow, int srow, int 
   }
 }
 
-// Resolve what this CTA computes (called by all 32 lanes of the producer
-// warp, before the barriers are initialised).  gate_up routed CTAs wait for
-// the previous grid first: their expert ids come from the router.  A routed
-// CTA's chunk is found with warp-wide ballots over the ids, so resolving
-// costs O(P / 32) loads per lane however many pairs there are.
+// Resolve what a CTA computes for row tile (or tile group) `tile` of grid
+// column `col` (called by all 32 lanes of the producer warp).  gate_up
+// routed CTAs wait for the previous grid first: their expert ids come from
+// the router.  A routed CTA's chunk is found with warp-wide ballots over the
+// ids, so resolving costs O(P / 32) loads per lane however many pairs there
+// are.
 template <int kMode, int kNT, typename Work = CtaWork>
-__device__ void resolve_work(const GemvParams& p, Work& w, uint32_t split, int lane) {
-  const int tile = blockIdx.x / max(1u, cluster_nctarank());
+__device__ void resolve_work_at(const GemvParams& p, Work& w, uint32_t split, int lane, int tile, int col) {
   // pairs (tokens) per MoE chunk: p.chunk when the host set one (1 .. kNT), else kNT
   const int cn = p.chunk > 0 && p.chunk < kNT ? p.chunk : kNT;
   if (lane == 0) {
@@ -367,7 +367,6 @@ __device__ void resolve_work(const GemvParams& p, Work& w, uint32_t split, int l
     }
   } else {
     // MoE: blockIdx.y < P: routed pair column; else shared-expert token chunk.
-    const int col = blockIdx.y;
     if (lane == 0) w.k_begin = 0;
     if (col < p.P) {
       // gate_up runs right after the router: its ids are complete only after
@@ -452,6 +451,14 @@ __device__ void resolve_work(const GemvParams& p, Work& w, uint32_t split, int l
     }
   }
   __syncwarp();
+}
+
+// The work of this CTA of the grid (tile from blockIdx.x over the cluster,
+// column blockIdx.y), before the barriers are initialised.
+template <int kMode, int kNT, typename Work = CtaWork>
+__device__ void resolve_work(const GemvParams& p, Work& w, uint32_t split, int lane) {
+  resolve_work_at<kMode, kNT, Work>(p, w, split, lane, static_cast<int>(blockIdx.x / max(1u, cluster_nctarank())),
+                                    static_cast<int>(blockIdx.y));
 }
 
 template <int kMode, int kNT>

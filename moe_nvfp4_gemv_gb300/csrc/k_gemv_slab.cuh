@@ -1,7 +1,9 @@
 // k_gemv_slab.cuh -- the NVFP4 GEMV with the CTA's activations resident in
 // shared memory: the dense GEMV for 1 .. 4 tokens on large weights, and the
 // MoE pair (gate_up: split and grouped forms; down_combine: grouped, its
-// combine a kernel of its own after the grid).
+// combine a kernel of its own after the grid; beyond one wave of CTAs
+// down_combine runs on the persistent form of this kernel,
+// k_moe_down_persist.cuh).
 //
 // Same operations as the register-fed kernel k_gemv_rf.cuh
 // (vllm.models.flint.ops.nvfp4_gemv, nvfp4_gemv, with or without silu_mul;

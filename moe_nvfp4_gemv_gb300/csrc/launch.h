@@ -50,6 +50,7 @@ cudaError_t slab_moe_regs(int mode, int* regs);
 // The combine of down_combine after the slab kernel (128-thread blocks; with
 // cfg.pdl it waits for the slab kernel's grid before reading its y rows).
 cudaError_t launch_moe_combine(const GemvParams& p, const LaunchCfg& cfg);
+cudaError_t launch_moe_down_persist(const GemvParams& p, const LaunchCfg& cfg);
 // Clusters of `cluster` slab-kernel CTAs (cw consumer warps, `smem` bytes of
 // dynamic shared memory) that fit on the GPU at once.
 cudaError_t slab_max_clusters(int r, int cw, unsigned cluster, size_t smem, int* n);

@@ -55,7 +55,7 @@ def test_scale_bytes_matches_oracle(fp4, rows, K):
 
 def test_workspace_bytes(fp4):
     # counters (one u64 per 128-row tile, 16-byte padded) + y [M*topk, H] + y_shared [M, H], bf16
-    assert fp4.moe_down_combine_workspace_bytes(1, 8, 4096) == 256 + 2 * 8 * 4096 + 2 * 4096
+    assert fp4.moe_down_combine_workspace_bytes(1, 8, 4096) == 272 + 2 * 8 * 4096 + 2 * 4096
     assert fp4.moe_down_combine_workspace_bytes(0, 8, 4096) == 0
 
 

@@ -6,7 +6,8 @@ come back, the device error word must read FP4GEMV_ERR_TIMEOUT, the outputs
 must be left unwritten, and the next normal call must be correct.  Unsplit
 (one CTA per cluster) launches on both kernels that serve 1 .. 16 tokens,
 and down_combine on the slab kernel, whose CTAs that gave up tag their row
-tiles so that the combine kernel after them leaves those outputs unwritten."""
+tiles so that the combine kernel after them leaves those outputs unwritten
+(on both of its grids: one CTA per item, and the persistent one)."""
 import numpy as np
 import pytest
 import torch
@@ -78,10 +79,13 @@ def test_skip_hook_rejects_bad_stage(fp4):
 
 
 # (I = 512: two 256-K stages per row tile; SI = 256: the shared expert's
-# CTAs have one, so skipping stage 1 stops only the routed CTAs.  The last
+# CTAs have one, so skipping stage 1 stops only the routed CTAs.  The third
 # case streams two tiles per CTA and stops in the second: the CTA has
-# written the first tile's y rows, and both of its tiles are tagged.)
-@pytest.mark.parametrize("M,E,H,topk,T,skip", [(1, 16, 512, 2, 1, 1), (8, 16, 512, 2, 1, 0), (8, 128, 1024, 8, 2, 3)])
+# written the first tile's y rows, and both of its tiles are tagged.  The
+# last runs on the persistent grid (items of two tiles) and stops in a CTA's
+# second item, after its first item's y rows are written.)
+@pytest.mark.parametrize("M,E,H,topk,T,skip", [(1, 16, 512, 2, 1, 1), (8, 16, 512, 2, 1, 0), (8, 128, 1024, 8, 2, 3),
+                                               (8, 128, 4096, 8, 2, 5)])
 def test_down_combine_timeout_then_recovery(fp4, M, E, H, topk, T, skip):
     from test_gpu_moe import _down_slab_tiles, make_moe, ref_down, run_down
     I, SI = 512, 256

@@ -227,12 +227,14 @@ def test_moe_config(fp4, M):
 
 def test_workspace_reuse_across_shapes(fp4):
     # one uninitialised workspace (sized for the largest call) serves calls of
-    # different M and H in turn: nothing is carried between calls
+    # different M and H in turn, on the grid and the persistent form (E = 128):
+    # nothing is carried between calls
     c = synth.MOE
     ws = torch.full((fp4.moe_down_combine_workspace_bytes(32, c["topk"], 1024),), 0xA5, dtype=torch.uint8,
                     device=DEV)
-    for M, H in ((5, 1024), (32, 256), (1, 1024), (17, 512), (32, 1024)):
-        d = make_moe(M, 16, H, 512, 512, c["topk"], seed=M)
+    for M, H, E in ((5, 1024, 16), (32, 256, 16), (32, 1024, 128), (1, 1024, 16), (17, 512, 16), (32, 1024, 128),
+                    (32, 1024, 16)):
+        d = make_moe(M, E, H, 512, 512, c["topk"], seed=M + E)
         g = {k: v.to(DEV) for k, v in d.items() if isinstance(v, torch.Tensor)}
         out = torch.empty(M, H, dtype=torch.bfloat16, device=DEV)
         fp4.moe_down_combine(g["act"], g["ids"], g["tw"], g["w2"], g["w2_sf"], g["alpha2"], g["sact"], g["wsd"],
@@ -315,21 +317,29 @@ def test_gate_up_slab_decode_block(fp4):
     assert fp4.get_device_error() == 0
 
 
-def _down_slab_tiles(fp4, M, topk, E, H, I, SI):
-    """Row tiles per CTA of the slab kernel's plan for this down_combine call
-    on this GPU (None: another kernel serves it)."""
+def _down_slab_plan(fp4, M, topk, E, H, I, SI):
+    """The slab plan for this down_combine call on this GPU (None: another
+    kernel serves it)."""
     import ctypes
 
     class Plan(ctypes.Structure):
         _fields_ = [(n, ctypes.c_int) for n in ("tiles_per_cta", "groups", "columns", "chunk_pairs", "slab_bytes",
-                                                "stage_bytes", "stages", "ctas_per_sm")] + \
+                                                "stage_bytes", "stages", "ctas_per_sm", "persistent")] + \
             [("smem_bytes", ctypes.c_size_t)]
     f = fp4.lib().fp4gemv_plan_moe_down_slab
     f.restype = ctypes.c_int
     f.argtypes = [ctypes.c_int] * 8 + [ctypes.POINTER(Plan)]
     out = Plan()
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    return out.tiles_per_cta if f(M, topk, E, H, I, SI, sms, 128, ctypes.byref(out)) == 0 else None
+    return out if f(M, topk, E, H, I, SI, sms, 128, ctypes.byref(out)) == 0 else None
+
+
+def _down_slab_tiles(fp4, M, topk, E, H, I, SI):
+    """Row tiles per CTA (or per item of the persistent grid) of the slab
+    plan for this down_combine call on this GPU (None: another kernel serves
+    it)."""
+    p = _down_slab_plan(fp4, M, topk, E, H, I, SI)
+    return None if p is None else p.tiles_per_cta
 
 
 # down_combine on the slab kernel with two row tiles per CTA: H = 832 is
@@ -361,6 +371,34 @@ def test_down_combine_slab_decode_block(fp4):
     assert bad == 0
     assert_close(u16(out)[tokens], tuple(r[tokens] for r in ref), "down slab decode block M=8")
     assert fp4.get_device_error() == 0
+
+
+# The persistent grid (more items than one wave of CTAs): three CTAs per SM
+# take (tile group, column) items from a counter.  32 tokens of the decode
+# block: groups of 4 tiles; 64 tokens over 1024 experts with H = 832: two
+# groups of 3 and 4 tiles, one partial; 32 tokens with H = 1024: one tile per
+# item.  Each call twice on one workspace (the counter of the first call is
+# stale for the second), sampled or whole outputs against the oracle.
+@pytest.mark.parametrize("M,topk,E,H,I,SI,T", [(32, 8, 128, 4096, 1536, 1536, 4), (64, 8, 1024, 832, 256, 256, 4),
+                                               (32, 8, 128, 1024, 512, 512, 1)])
+def test_down_combine_persistent(fp4, M, topk, E, H, I, SI, T):
+    p = _down_slab_plan(fp4, M, topk, E, H, I, SI)
+    assert p is not None and p.persistent == 1 and p.tiles_per_cta == T
+    d = make_moe(M, E=E, H=H, I=I, SI=SI, topk=topk, seed=1300 + M + E)
+    g = {k: v.to(DEV) for k, v in d.items() if isinstance(v, torch.Tensor)}
+    ws = torch.full((fp4.moe_down_combine_workspace_bytes(M, topk, H),), 0xA5, dtype=torch.uint8, device=DEV)
+    outs = []
+    for _ in range(2):
+        out = torch.full((M, H), 7.0, dtype=torch.bfloat16, device=DEV)
+        fp4.moe_down_combine(g["act"], g["ids"], g["tw"], g["w2"], g["w2_sf"], g["alpha2"], g["sact"], g["wsd"],
+                             g["ssd"], g["gssd"], out, workspace=ws)
+        outs.append(out)
+    assert fp4.get_device_error() == 0
+    tokens = list(range(M)) if H * I <= 1 << 20 else [0, 5, M // 2, M - 1]
+    ref, bad = ref_down(d, tokens=tokens)
+    assert bad == 0
+    assert_close(u16(outs[0])[tokens], tuple(r[tokens] for r in ref), f"down persistent M={M} E={E} H={H}")
+    assert torch.equal(outs[0], outs[1])
 
 
 def test_down_combine_slab_decode_block_one_token(fp4):

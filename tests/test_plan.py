@@ -406,7 +406,8 @@ def test_moe_slab_plan_rejects_bad_arguments(moe_slab_fn):
 
 class MoeDownSlabPlan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in ("tiles_per_cta", "groups", "columns", "chunk_pairs", "slab_bytes",
-                                            "stage_bytes", "stages", "ctas_per_sm")] + [("smem_bytes", ctypes.c_size_t)]
+                                            "stage_bytes", "stages", "ctas_per_sm", "persistent")] + \
+        [("smem_bytes", ctypes.c_size_t)]
 
 
 @pytest.fixture(scope="module")
@@ -430,9 +431,12 @@ def down_slab_rule(M, topk, E, H, I, SI, sms=SMS):
     One tile at two CTAs per SM when n(1) fits one wave of two per SM, two
     tiles at two per SM when n(2) does, one tile at three per SM when n(2)
     fills more than 0.9 and at most 1.35 waves of three per SM, else two
-    tiles at three per SM.  As many 18 KB
-    stages as fit beside the slab within 228 KB / occ less 4 KB (2 .. 8, at
-    most T stage streams of I)."""
+    tiles at three per SM.  When that grid holds more than one wave (n(T) >
+    occ x sms): the persistent grid at three per SM, T = 4 if n(4) is at
+    least 1.6 x 3 sms, else 2 if n(2) is, else 1.  As many 18 KB stages as
+    fit beside the slab within 228 KB / occ less 4 KB (2 .. 8; on the grid
+    form at most T stage streams of I).  The reported T is the largest
+    group, ceil(tiles / groups)."""
     if M < 1 or M > 64:
         return None
     P = M * topk
@@ -448,14 +452,21 @@ def down_slab_rule(M, topk, E, H, I, SI, sms=SMS):
         T, occ = 1, 3
     else:
         T, occ = 2, 3
+    persistent = n(T) > occ * sms
+    if persistent:
+        occ = 3
+        T = 4 if n(4) >= 1.6 * 3 * sms else 2 if n(2) >= 1.6 * 3 * sms else 1
     rows = min(P, 8)
     nst = -(-max(I, SI) // 256)
     slab = -(-(rows * nst * 512) // 1024) * 1024
-    ns = min(8, (228 * 1024 // occ - 4096 - 1024 - slab) // 18432, T * -(-I // 256))
+    ns = min(8, (228 * 1024 // occ - 4096 - 1024 - slab) // 18432)
+    if not persistent:
+        ns = min(ns, T * -(-I // 256))
     if ns < 2:
         return None
-    return dict(tiles_per_cta=T, groups=-(-tiles // T), chunk_pairs=8, slab_bytes=slab, stages=ns, ctas_per_sm=occ,
-                smem_bytes=1024 + slab + ns * 18432)
+    groups = -(-tiles // T)
+    return dict(tiles_per_cta=-(-tiles // groups), groups=groups, chunk_pairs=8, slab_bytes=slab, stages=ns,
+                ctas_per_sm=occ, persistent=int(persistent), smem_bytes=1024 + slab + ns * 18432)
 
 
 def test_moe_slab_rule_decode_block():
@@ -472,9 +483,10 @@ def test_down_slab_rule_decode_block():
     # the E = 128, top-8, H = 4096, I = SI = 1536 block on 152 SMs: the
     # shapes the sweep found best at 1, 2, 4 and 8 tokens
     c = (8, 128, 4096, 1536, 1536)
-    got = {M: (down_slab_rule(M, *c)["tiles_per_cta"], down_slab_rule(M, *c)["ctas_per_sm"])
-           for M in (1, 2, 3, 4, 5, 6, 8, 64)}
-    assert got == {1: (1, 2), 2: (2, 2), 3: (2, 3), 4: (1, 3), 5: (1, 3), 6: (2, 3), 8: (2, 3), 64: (2, 3)}
+    got = {M: tuple(down_slab_rule(M, *c)[k] for k in ("tiles_per_cta", "ctas_per_sm", "persistent"))
+           for M in (1, 2, 3, 4, 5, 6, 8, 16, 32, 64)}
+    assert got == {1: (1, 2, 0), 2: (2, 2, 0), 3: (2, 3, 0), 4: (1, 3, 1), 5: (1, 3, 1), 6: (1, 3, 1), 8: (2, 3, 1),
+                   16: (2, 3, 1), 32: (4, 3, 1), 64: (4, 3, 1)}
 
 
 @pytest.mark.parametrize("M,topk,E,H,I,SI", [(1, 8, 128, 4096, 1536, 1536), (8, 8, 128, 4096, 1536, 1536),
@@ -491,7 +503,7 @@ def test_down_slab_plan_matches_rule(down_slab_fn, M, topk, E, H, I, SI):
         return
     assert st == 0
     got = dict(tiles_per_cta=p.tiles_per_cta, groups=p.groups, chunk_pairs=p.chunk_pairs, slab_bytes=p.slab_bytes,
-               stages=p.stages, ctas_per_sm=p.ctas_per_sm, smem_bytes=p.smem_bytes)
+               stages=p.stages, ctas_per_sm=p.ctas_per_sm, persistent=p.persistent, smem_bytes=p.smem_bytes)
     assert got == want
     assert p.stage_bytes == 18432 and p.columns == M * topk + -(-M // p.chunk_pairs)
     # the groups split the tiles evenly: floor or ceil of tiles / groups each
