@@ -115,7 +115,7 @@ typedef struct {
   int tiles_per_cta;  /* most 128-row tiles of H one CTA streams in turn: ceil(tiles / groups) */
   int groups;         /* grid columns along H; group g takes tiles [g tiles / groups, (g + 1) tiles / groups) */
   int columns;        /* grid rows: M * topk routed pair columns + the shared expert's token chunks */
-  int chunk_pairs;    /* most (token, expert) pairs one routed CTA computes (8) */
+  int chunk_pairs;    /* most (token, expert) pairs one routed CTA (or item) computes (8, or 4) */
   int slab_bytes;     /* shared memory holding a CTA's activation rows (the whole K) */
   int stage_bytes;    /* one weight stage (codes of 128 rows x 256 K, one scale group) */
   int stages;         /* weight ring stages (2 .. 8) */
@@ -135,15 +135,16 @@ typedef struct {
  *   out:  HOST pointer, filled on success.
  * Applies to 1 <= M <= 64 when up to 8 activation rows of max(I, SI) and
  * two weight stages fit the CTA's share of the SM's shared memory, and the
- * CTA's T tiles of I hold at least two 256-K stages.  Chunks of 8 pairs.  With C = (E (1 - (1 - 1/E)^(M topk)), at
+ * CTA's T tiles of I hold at least two 256-K stages.  Chunks of 8 pairs (but see below).  With C = (E (1 - (1 - 1/E)^(M topk)), at
  * least ceil(M topk / 8)) + ceil(M / 8) expected streaming columns and
  * n(T) = C ceil(ceil(H / 128) / T) CTAs: T = 1 at two CTAs per SM if
  * n(1) <= 2 sms, else T = 2 at two per SM if n(2) <= 2 sms, else T = 1 at
  * three per SM if 0.9 < n(2) / (3 sms) <= 1.35, else T = 2 at three per SM.
  * When that grid holds more than one wave (n(T) > CTAs per SM x sms), the
  * persistent grid (persistent = 1): three CTAs per SM that take items of T
- * tiles of one column in turn from a counter, T = 4 if n(4) >= 1.6 x 3 sms,
- * else 2 if n(2) is, else 1.  As many weight stages as fit (2 .. 8; on
+ * tiles of one column in turn from a counter; chunks of 4 pairs if
+ * M topk <= E (C and n(T) taken again with them); T = 4 if
+ * n(4) >= 1.6 x 3 sms, else 2 if n(2) is, else 1.  As many weight stages as fit (2 .. 8; on
  * the grid of one CTA per item at most T stage streams of I).  tiles_per_cta
  * reports the largest group, ceil(tiles / groups).
  * Returns FP4GEMV_ERR_INVALID_ARG for a null out, sms < 1 or regs < 1;

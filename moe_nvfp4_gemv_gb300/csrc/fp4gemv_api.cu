@@ -655,10 +655,13 @@ bool plan_slab_down(int M, int topk, int E, int H, int I, int SI, int sms, int r
   const int warp_regs = (regs * 32 + 255) / 256 * 256;
   if (sms < 1 || M < 1 || M > 64) return false;
   const long P = static_cast<long>(M) * topk;
-  const int chunk = fp4::kSlabNT;
+  int chunk = fp4::kSlabNT;
   const int tiles = (H + 127) / 128;
   const double distinct = E * (1.0 - std::pow(1.0 - 1.0 / E, static_cast<double>(P)));
-  const double cols = std::max(distinct, static_cast<double>((P + chunk - 1) / chunk)) + (M + chunk - 1) / chunk;
+  auto columns = [&](int cn) {
+    return std::max(distinct, static_cast<double>((P + cn - 1) / cn)) + static_cast<double>((M + cn - 1) / cn);
+  };
+  double cols = columns(chunk);
   auto ctas = [&](int T) { return cols * ((tiles + T - 1) / T); };
   int T = 2, occ = 3;
   const double f = ctas(2) / (3.0 * sms);  // waves of two-tile CTAs at three per SM
@@ -666,11 +669,17 @@ bool plan_slab_down(int M, int topk, int E, int H, int I, int SI, int sms, int r
   else if (ctas(2) <= 2.0 * sms) T = 2, occ = 2;
   else if (f > 0.9 && f <= 1.35) T = 1, occ = 3;
   // More CTAs than one wave: the persistent grid instead, three CTAs per
-  // SM, items of the most tiles (4, 2, 1) that still give every CTA slot
-  // 1.6 items or more on average.
+  // SM; chunks of 4 pairs when there are no more pairs than experts (few
+  // experts then take more than 4, and the half-height slab leaves room for
+  // a deeper ring); items of the most tiles (4, 2, 1) that still give every
+  // CTA slot 1.6 items or more on average.
   const bool persist = ctas(T) > static_cast<double>(occ) * sms;
   if (persist) {
     occ = 3;
+    if (P <= E) {
+      chunk = 4;
+      cols = columns(chunk);
+    }
     const double slots = 3.0 * sms;
     T = ctas(4) >= 1.6 * slots ? 4 : ctas(2) >= 1.6 * slots ? 2 : 1;
   }

@@ -432,8 +432,9 @@ def down_slab_rule(M, topk, E, H, I, SI, sms=SMS):
     tiles at two per SM when n(2) does, one tile at three per SM when n(2)
     fills more than 0.9 and at most 1.35 waves of three per SM, else two
     tiles at three per SM.  When that grid holds more than one wave (n(T) >
-    occ x sms): the persistent grid at three per SM, T = 4 if n(4) is at
-    least 1.6 x 3 sms, else 2 if n(2) is, else 1.  As many 18 KB stages as
+    occ x sms): the persistent grid at three per SM, chunks of 4 pairs if
+    P <= E (C and n recomputed with them), T = 4 if n(4) is at least
+    1.6 x 3 sms, else 2 if n(2) is, else 1.  As many 18 KB stages as
     fit beside the slab within 228 KB / occ less 4 KB (2 .. 8; on the grid
     form at most T stage streams of I).  The reported T is the largest
     group, ceil(tiles / groups)."""
@@ -453,10 +454,14 @@ def down_slab_rule(M, topk, E, H, I, SI, sms=SMS):
     else:
         T, occ = 2, 3
     persistent = n(T) > occ * sms
+    chunk = 8
     if persistent:
         occ = 3
+        if P <= E:
+            chunk = 4
+            cols = max(E * (1.0 - (1.0 - 1.0 / E) ** P), float(-(-P // 4))) + -(-M // 4)
         T = 4 if n(4) >= 1.6 * 3 * sms else 2 if n(2) >= 1.6 * 3 * sms else 1
-    rows = min(P, 8)
+    rows = min(P, chunk)
     nst = -(-max(I, SI) // 256)
     slab = -(-(rows * nst * 512) // 1024) * 1024
     ns = min(8, (228 * 1024 // occ - 4096 - 1024 - slab) // 18432)
@@ -465,7 +470,7 @@ def down_slab_rule(M, topk, E, H, I, SI, sms=SMS):
     if ns < 2:
         return None
     groups = -(-tiles // T)
-    return dict(tiles_per_cta=-(-tiles // groups), groups=groups, chunk_pairs=8, slab_bytes=slab, stages=ns,
+    return dict(tiles_per_cta=-(-tiles // groups), groups=groups, chunk_pairs=chunk, slab_bytes=slab, stages=ns,
                 ctas_per_sm=occ, persistent=int(persistent), smem_bytes=1024 + slab + ns * 18432)
 
 
@@ -514,12 +519,15 @@ def test_down_slab_plan_matches_rule(down_slab_fn, M, topk, E, H, I, SI):
 
 def test_down_slab_plan_decode_block(down_slab_fn):
     # E = 128, top-8, H = 4096, I = SI = 1536: one token, one tile per CTA at
-    # two CTAs per SM (its 288 CTAs in one wave); 8 tokens, chunks of 8 pairs
-    # and two tiles per CTA at three per SM
+    # two CTAs per SM (its 288 CTAs in one wave); 8 tokens, the persistent
+    # grid at three per SM, chunks of 4 pairs (64 pairs over 128 experts),
+    # items of two tiles; 32 tokens, chunks of 8 pairs and items of four
     st, p = down_slab_fn(1, 8, 128, 4096, 1536, 1536)
-    assert st == 0 and (p.tiles_per_cta, p.groups, p.chunk_pairs, p.ctas_per_sm) == (1, 32, 8, 2)
+    assert st == 0 and (p.tiles_per_cta, p.groups, p.chunk_pairs, p.ctas_per_sm, p.persistent) == (1, 32, 8, 2, 0)
     st, p = down_slab_fn(8, 8, 128, 4096, 1536, 1536)
-    assert st == 0 and (p.tiles_per_cta, p.groups, p.chunk_pairs, p.ctas_per_sm) == (2, 16, 8, 3)
+    assert st == 0 and (p.tiles_per_cta, p.groups, p.chunk_pairs, p.ctas_per_sm, p.persistent) == (2, 16, 4, 3, 1)
+    st, p = down_slab_fn(32, 8, 128, 4096, 1536, 1536)
+    assert st == 0 and (p.tiles_per_cta, p.groups, p.chunk_pairs, p.ctas_per_sm, p.persistent) == (4, 8, 8, 3, 1)
 
 
 def test_down_slab_plan_rejects_bad_arguments(down_slab_fn):
