@@ -22,7 +22,9 @@ have lo == hi == nominal.
 Sources (title / section): vllm.models.flint.ops.nvfp4_gemv (module docstring,
 nvfp4_gemv, bf16_gemv, dequantize_rows), vllm.models.flint.ops.linear
 (_swizzled_scale_buffer), vllm.models.flint.ops.moe_gemv (module docstring,
-gate_up, down_combine).
+gate_up, down_combine), vllm.model_executor.kernels.linear.nvfp4.flashinfer
+(the W4A4 kernels' apply_weights: scaled_fp4_quant, then the NVFP4 GEMM with
+alpha; the quantiser's arithmetic is a reading, see ``quantize_act``).
 
 Parity pins: every function here is pinned by ``tests/test_oracle_*.py``
 (value tables, closed forms, brute force, a library cross-check and
@@ -90,6 +92,9 @@ def _load():
                 "orc_moe_down_combine": (ctypes.c_int, [_vp, _vp, _vp, _i64, _vp, _vp, _vp, _i64, _i64, _i64,
                                                         _vp, _vp, _vp, _dbl, _i64, _i64, _i64, _vp, _vp, _vp,
                                                         _vp]),
+                "orc_e4m3_encode": (ctypes.c_int, [ctypes.c_float]),
+                "orc_e2m1_encode": (ctypes.c_int, [ctypes.c_float]),
+                "orc_quantize_act": (None, [_vp, _i64, _i64, _i64, ctypes.c_float, _vp, _vp]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(lib, name)
@@ -390,3 +395,42 @@ def check(gpu_bits: np.ndarray, ref, rel: float = 2.0 ** -7, rms_frac: float = 2
     nbad = int(bad.sum())
     first = int(np.argmax(bad.reshape(-1))) if nbad else -1
     return nbad == 0, float(excess.max()) if excess.size else 0.0, nbad, first
+
+
+# --------------------------------------------------------------------------
+# W4A4 (activation quantisation, then the NVFP4 x NVFP4 GEMM)
+# --------------------------------------------------------------------------
+
+def e4m3_encode(v: float) -> int:
+    """Nearest finite E4M3 code of a float v >= 0 (ties to even, saturating at 448)."""
+    return int(_load().orc_e4m3_encode(float(v)))
+
+
+def e2m1_encode(v: float) -> int:
+    """Nearest E2M1 code of a float v (ties to even, saturating at 6; zero as +0)."""
+    return int(_load().orc_e2m1_encode(float(v)))
+
+
+def quantize_act(x: np.ndarray, gsi: float) -> tuple[np.ndarray, np.ndarray]:
+    """scaled_fp4_quant(x, input_global_scale_inv) as read in the C oracle
+    (per 16-value block: s = (amax / 6) * gsi to E4M3, codes = E2M1 of
+    x * (gsi / e4m3(s)), all in float): x bf16 bits [M, K] -> (codes uint8
+    [M, K / 2], flat 128x4-swizzled scales of scale_bytes(M, K) bytes)."""
+    lib = _load()
+    x = np.ascontiguousarray(x, np.uint16)
+    M, K = x.shape
+    assert K % 16 == 0 and gsi > 0
+    q = np.empty((M, K // 2), np.uint8)
+    sf = np.empty(scale_bytes(M, K), np.uint8)
+    lib.orc_quantize_act(_p(x), K, M, K, float(np.float32(gsi)), _p(q), _p(sf))
+    return q, sf
+
+
+def w4a4_gemm(xq: np.ndarray, xsf: np.ndarray, w: np.ndarray, sf: np.ndarray, alpha: float, rows=None,
+              threads: int | None = None):
+    """The NVFP4 x NVFP4 GEMM of the W4A4 kernels: out = bf16(fp32(xd @ wd^T) *
+    alpha) with xd, wd the exact dequantisations of both NVFP4 tensors.  Every
+    product e2m1 * e4m3 has at most 5 significant bits, so xd is exact in bf16
+    and the GEMM is the dense NVFP4 GEMV of xd (nominal, lo, hi)."""
+    xd = dequantize_rows(xq, xsf, threads=threads)
+    return nvfp4_gemv(xd, w, sf, alpha, rows=rows, threads=threads)

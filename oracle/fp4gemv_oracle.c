@@ -14,6 +14,9 @@
  *                  _swizzled_scale_buffer sections.
  *   [moe_gemv]     vllm.models.flint.ops.moe_gemv, module docstring and the
  *                  gate_up / down_combine sections.
+ *   [flashinfer]   vllm.model_executor.kernels.linear.nvfp4.flashinfer, the
+ *                  W4A4 kernels' apply_weights (activation quantisation; its
+ *                  arithmetic is a reading, stated at orc_quantize_act).
  *
  * Arithmetic: products and sums in double (every product of a bf16 activation
  * and an exactly-dequantised weight has <= 14 significant bits, so products
@@ -420,4 +423,92 @@ int orc_moe_down_combine(const uint16_t* act, const int32_t* ids, const float* t
         }
     }
     return bad;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Activation quantisation (the W4A4 path)                                   */
+/* ------------------------------------------------------------------------ */
+
+/* The flashinfer page's W4A4 kernels (FlashInferB12xNvFp4LinearKernel and
+ * the other NvFp4LinearKernel backends, apply_weights) quantise x with
+ * scaled_fp4_quant(x, input_global_scale_inv) into an NVFP4 tensor of the
+ * weight's own format (E2M1 codes, 128x4-swizzled E4M3 block scales, one per
+ * 16 values) and hand both NVFP4 tensors and alpha to the NVFP4 GEMM.  The
+ * pages do not print the quantiser's arithmetic.  Reading (the plainest one
+ * the rest supports): e2m1 x e4m3 approximates x * gsi, so that
+ * out = bf16(fp32(sum_k xq_k * wq_k) * alpha) with alpha = the product of
+ * the activation's (1 / gsi) and the weight's global scales.  Per row m and
+ * block b of 16 values, in float (binary32), each operation rounded to
+ * nearest even, no fused multiply-add:
+ *   amax = max |x[m, 16b .. 16b + 15]|
+ *   s    = (amax / 6) * gsi
+ *   sf   = orc_e4m3_encode(s)
+ *   r    = gsi / e4m3(sf)             (sf = 0: every code of the block is 0)
+ *   code = orc_e2m1_encode(x * r)
+ * gsi must be positive and finite, x finite. */
+
+/* The finite E4M3 code nearest v >= 0 (ties to the even code), saturating at
+ * 448 (code 0x7E): a plain search over the 127 non-negative finite codes. */
+int orc_e4m3_encode(float v)
+{
+    int best = 0;
+    double bd = INFINITY;
+    for (int c = 0; c <= 0x7E; ++c) {
+        double d = fabs((double)v - orc_e4m3(c));
+        if (d < bd || (d == bd && (c & 1) == 0 && (best & 1) != 0)) {
+            best = c;
+            bd = d;
+        }
+    }
+    return best;
+}
+
+/* The E2M1 code nearest v (ties to the even magnitude code), saturating at
+ * magnitude 6; the sign bit is set for v < 0 unless the magnitude code is 0
+ * (a value that rounds to zero is stored as +0). */
+int orc_e2m1_encode(float v)
+{
+    double a = fabs((double)v);
+    int best = 0;
+    double bd = INFINITY;
+    for (int c = 0; c < 8; ++c) {
+        double d = fabs(a - E2M1_MAG[c]);
+        if (d < bd || (d == bd && (c & 1) == 0 && (best & 1) != 0)) {
+            best = c;
+            bd = d;
+        }
+    }
+    if (a > 6.0) best = 7;
+    return (v < 0.0f && best != 0) ? (best | 8) : best;
+}
+
+/* scaled_fp4_quant as read above: x bf16 [M, K] (row stride ldx), K % 16 ==
+ * 0; writes q [M, K / 2] (element 2j in the low nibble of byte j, as the
+ * weights) and sf, orc_scale_bytes(M, K) bytes in the 128x4 layout (bytes of
+ * padding rows and blocks are 0). */
+void orc_quantize_act(const uint16_t* x, int64_t ldx, int64_t M, int64_t K, float gsi, uint8_t* q, uint8_t* sf)
+{
+    memset(sf, 0, (size_t)orc_scale_bytes(M, K));
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t b = 0; b < K / 16; ++b) {
+            const uint16_t* xb = x + m * ldx + 16 * b;
+            float amax = 0.0f;
+            for (int i = 0; i < 16; ++i) {
+                float a = (float)fabs(bf16_to_double(xb[i]));
+                if (a > amax) amax = a;
+            }
+            float s = (amax / 6.0f) * gsi;
+            int sc = orc_e4m3_encode(s);
+            sf[orc_swz(m, b, K)] = (uint8_t)sc;
+            float e = (float)orc_e4m3(sc);
+            float r = e > 0.0f ? gsi / e : 0.0f;
+            for (int i = 0; i < 16; i += 2) {
+                float v0 = (float)bf16_to_double(xb[i]) * r;
+                float v1 = (float)bf16_to_double(xb[i + 1]) * r;
+                int c0 = e > 0.0f ? orc_e2m1_encode(v0) : 0;
+                int c1 = e > 0.0f ? orc_e2m1_encode(v1) : 0;
+                q[m * (K / 2) + 8 * b + i / 2] = (uint8_t)(c0 | (c1 << 4));
+            }
+        }
+    }
 }
