@@ -127,6 +127,56 @@ fp4gemv_status fp4gemv_dequant_gemm(const void* x, int64_t ldx, const uint8_t* w
                                     const float* global_scale, void* w_bf16, void* out, int64_t ldo, int M,
                                     int N, int K, int pdl, cudaStream_t stream);
 
+/* ---- W4A4 path (vllm.model_executor.kernels.linear.nvfp4.flashinfer, the
+ * W4A4 kernels' apply_weights: x_fp4, x_blockscale = scaled_fp4_quant(x,
+ * input_global_scale_inv); out = the NVFP4 x NVFP4 GEMM with alpha).  The
+ * pages name the quantiser but not its arithmetic; this library's reading,
+ * per row m and 16-value block, in binary32 with round-to-nearest-even:
+ *   s = (max |x| / 6) * gsi;  sf = nearest finite E4M3 of s (ties to even,
+ *   saturating at 448);  codes = nearest E2M1 of x * (gsi / e4m3(sf)) (ties
+ *   to the even code, saturating at 6, zero stored as +0; all 0 if sf = 0).
+ * The NVFP4 activation tensor has the weights' format: x_fp4 uint8
+ * [M, K / 2] (element 2j in the low nibble of byte j), x_sf the flat 128x4
+ * layout of fp4gemv_scale_bytes(M, K) bytes (padding bytes written 0).
+ * The GEMM: out[m, n] = bf16(fp32(sum_k xq[m, k] * wq[n, k]) * alpha[0]),
+ * xq = e2m1 * e4m3 of the activations, wq of the weights (alpha = the
+ * activation's and the weight's global scales multiplied).  It runs on this
+ * library's NVFP4 GEMV / GEMM kernels over the exact bf16 dequantisation of
+ * the activations (every e2m1 * e4m3 product is exact in bf16), in launches
+ * of at most FP4GEMV_MAX_M rows; the block-scaled FP4 tensor-core MMA is not
+ * used. */
+
+/* Bytes of the bf16 scratch fp4gemv_w4a4_gemm / fp4gemv_w4a4_linear need for
+ * M rows of K activations (M * K * 2, rounded up to 16). */
+size_t fp4gemv_w4a4_workspace_bytes(int M, int K);
+
+/* scaled_fp4_quant as read above.  x bf16 [M, ldx >= K] (16-byte aligned,
+ * ldx * 2 % 16 == 0); gsi fp32 [1] device (> 0, finite; x finite); x_fp4
+ * [M, K / 2] (8-byte aligned) and x_sf (fp4gemv_scale_bytes(M, K) bytes)
+ * device, written.  Shapes: M >= 1, K % 16 == 0.  One launch. */
+fp4gemv_status fp4gemv_quantize_act(const void* x, int64_t ldx, const float* gsi, uint8_t* x_fp4, uint8_t* x_sf,
+                                    int M, int K, cudaStream_t stream);
+
+/* The W4A4 GEMM on quantised activations (x_fp4, x_sf as written by
+ * fp4gemv_quantize_act) and NVFP4 weights (w, w_sf as for
+ * fp4gemv_nvfp4_gemv): the activations are dequantised into `workspace`
+ * (fp4gemv_w4a4_workspace_bytes(M, K) bytes, 16-byte aligned, device), then
+ * out bf16 [M, ldo >= N] = bf16(fp32(xq @ wq^T) * alpha[0]).  Shapes: M >= 1
+ * (any; launches of FP4GEMV_MAX_M rows), N % 16 == 0, K % 64 == 0,
+ * K >= 256.  pdl as for fp4gemv_nvfp4_gemv (the GEMM launches). */
+fp4gemv_status fp4gemv_w4a4_gemm(const uint8_t* x_fp4, const uint8_t* x_sf, const uint8_t* w, const uint8_t* w_sf,
+                                 const float* alpha, void* out, int64_t ldo, int M, int N, int K, void* workspace,
+                                 size_t workspace_bytes, int pdl, cudaStream_t stream);
+
+/* Quantisation and GEMM in one call: fp4gemv_quantize_act into x_fp4 / x_sf,
+ * whose kernel also writes the exact dequantised activations into
+ * `workspace`, then the GEMM of fp4gemv_w4a4_gemm on them (no second pass
+ * over the codes).  Arguments and shapes as those two calls. */
+fp4gemv_status fp4gemv_w4a4_linear(const void* x, int64_t ldx, const float* gsi, const uint8_t* w,
+                                   const uint8_t* w_sf, const float* alpha, void* out, int64_t ldo, int M, int N,
+                                   int K, uint8_t* x_fp4, uint8_t* x_sf, void* workspace, size_t workspace_bytes,
+                                   int pdl, cudaStream_t stream);
+
 /* gate_up (vllm.models.flint.ops.moe_gemv, gate_up), one launch:
  * routed pairs p = t * topk + j (t < M, j < topk), e = ids[p]:
  *   g, u = fp32(x[t] . W1[e] gate / up row) * alpha[e]   (fp32, not rounded)

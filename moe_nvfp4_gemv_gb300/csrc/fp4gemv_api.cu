@@ -1039,6 +1039,87 @@ fp4gemv_status fp4gemv_dequant_gemm(const void* x, int64_t ldx, const uint8_t* w
   return dense_launch(fp4::kDenseBf16, x, ldx, w_bf16, nullptr, global_scale, out, ldo, M, N, K, 0, 0, stream);
 }
 
+size_t fp4gemv_w4a4_workspace_bytes(int M, int K) {
+  if (M < 1 || K < 1) return 0;
+  return (static_cast<size_t>(M) * K * 2 + 15) / 16 * 16;
+}
+
+fp4gemv_status fp4gemv_quantize_act(const void* x, int64_t ldx, const float* gsi, uint8_t* x_fp4, uint8_t* x_sf,
+                                    int M, int K, cudaStream_t stream) {
+  if (M < 1 || K < 1 || ldx < K) return FP4GEMV_ERR_INVALID_ARG;
+  if (K % 16 != 0) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(x, 16) || (ldx * 2) % 16 != 0 || !aligned(x_fp4, 8) || !aligned(gsi, 4)) return FP4GEMV_ERR_MISALIGNED;
+  if (!x || !gsi || !x_fp4 || !x_sf) return FP4GEMV_ERR_INVALID_ARG;
+  fp4gemv_status st = device_state(nullptr, nullptr);
+  if (st != FP4GEMV_OK) return st;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return from_cuda(fp4::launch_quantize_act(x, ldx, gsi, x_fp4, x_sf, nullptr, M, K, stream));
+}
+
+namespace {
+
+// The W4A4 GEMM on the exact bf16 dequantisation of the activations (in the
+// workspace): the dense NVFP4 GEMM with alpha as its global scale, in
+// launches of at most FP4GEMV_MAX_M rows.
+fp4gemv_status w4a4_gemm_on(const uint16_t* xd, const uint8_t* w, const uint8_t* w_sf, const float* alpha,
+                            void* out, int64_t ldo, int M, int N, int K, int pdl, cudaStream_t stream) {
+  for (int m0 = 0; m0 < M; m0 += FP4GEMV_MAX_M) {
+    const int mc = std::min(FP4GEMV_MAX_M, M - m0);
+    fp4gemv_status st = dense_launch(fp4::kDenseFp4, xd + static_cast<int64_t>(m0) * K, K, w, w_sf, alpha,
+                                     static_cast<uint16_t*>(out) + static_cast<int64_t>(m0) * ldo, ldo, mc, N, K, 0,
+                                     pdl, stream);
+    if (st != FP4GEMV_OK) return st;
+  }
+  return FP4GEMV_OK;
+}
+
+fp4gemv_status w4a4_check(const uint8_t* w, const uint8_t* w_sf, const float* alpha, void* out, int64_t ldo, int M,
+                          int N, int K, void* workspace, size_t workspace_bytes, int pdl) {
+  if (pdl != 0 && pdl != 1) return FP4GEMV_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 1 || ldo < N) return FP4GEMV_ERR_INVALID_ARG;
+  if (N % 16 != 0 || K % 64 != 0 || K < 256) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
+  if (workspace_bytes < fp4gemv_w4a4_workspace_bytes(M, K)) return FP4GEMV_ERR_INVALID_ARG;
+  if (!aligned(w, 16) || !aligned(w_sf, 16) || !aligned(out, 16) || ldo % 8 != 0 || !aligned(workspace, 16) ||
+      !aligned(alpha, 4))
+    return FP4GEMV_ERR_MISALIGNED;
+  if (!w || !w_sf || !alpha || !out || !workspace) return FP4GEMV_ERR_INVALID_ARG;
+  return FP4GEMV_OK;
+}
+
+}  // namespace
+
+fp4gemv_status fp4gemv_w4a4_gemm(const uint8_t* x_fp4, const uint8_t* x_sf, const uint8_t* w, const uint8_t* w_sf,
+                                 const float* alpha, void* out, int64_t ldo, int M, int N, int K, void* workspace,
+                                 size_t workspace_bytes, int pdl, cudaStream_t stream) {
+  fp4gemv_status st = w4a4_check(w, w_sf, alpha, out, ldo, M, N, K, workspace, workspace_bytes, pdl);
+  if (st != FP4GEMV_OK) return st;
+  if (!aligned(x_fp4, 8)) return FP4GEMV_ERR_MISALIGNED;
+  if (!x_fp4 || !x_sf) return FP4GEMV_ERR_INVALID_ARG;
+  st = device_state(nullptr, nullptr);
+  if (st != FP4GEMV_OK) return st;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  st = from_cuda(fp4::launch_dequantize_act(x_fp4, x_sf, workspace, M, K, stream));
+  if (st != FP4GEMV_OK) return st;
+  return w4a4_gemm_on(static_cast<const uint16_t*>(workspace), w, w_sf, alpha, out, ldo, M, N, K, pdl, stream);
+}
+
+fp4gemv_status fp4gemv_w4a4_linear(const void* x, int64_t ldx, const float* gsi, const uint8_t* w,
+                                   const uint8_t* w_sf, const float* alpha, void* out, int64_t ldo, int M, int N,
+                                   int K, uint8_t* x_fp4, uint8_t* x_sf, void* workspace, size_t workspace_bytes,
+                                   int pdl, cudaStream_t stream) {
+  fp4gemv_status st = w4a4_check(w, w_sf, alpha, out, ldo, M, N, K, workspace, workspace_bytes, pdl);
+  if (st != FP4GEMV_OK) return st;
+  if (ldx < K) return FP4GEMV_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || (ldx * 2) % 16 != 0 || !aligned(x_fp4, 8) || !aligned(gsi, 4)) return FP4GEMV_ERR_MISALIGNED;
+  if (!x || !gsi || !x_fp4 || !x_sf) return FP4GEMV_ERR_INVALID_ARG;
+  st = device_state(nullptr, nullptr);
+  if (st != FP4GEMV_OK) return st;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  st = from_cuda(fp4::launch_quantize_act(x, ldx, gsi, x_fp4, x_sf, workspace, M, K, stream));
+  if (st != FP4GEMV_OK) return st;
+  return w4a4_gemm_on(static_cast<const uint16_t*>(workspace), w, w_sf, alpha, out, ldo, M, N, K, pdl, stream);
+}
+
 fp4gemv_status fp4gemv_moe_gate_up(const void* x, const int32_t* ids, int M, int topk, const uint8_t* w1,
                                    const uint8_t* w1_sf, const float* alpha, int E, int H, int I, void* act,
                                    const uint8_t* wsh, const uint8_t* ssh, const float* gssh, int SI, void* sact,

@@ -1,0 +1,154 @@
+// k_quantize_act.cuh -- NVFP4 quantisation of bf16 activations for the W4A4
+// path (vllm.model_executor.kernels.linear.nvfp4.flashinfer, the W4A4
+// kernels' apply_weights: scaled_fp4_quant(x, input_global_scale_inv), then
+// the NVFP4 x NVFP4 GEMM with alpha).
+//
+// The pages name the operation but not its arithmetic.  Reading: the output
+// is an NVFP4 tensor of the weights' own format (E2M1 codes, element 2j in
+// the low nibble of byte j; E4M3 block scales, one per 16 values, in the
+// 128x4 layout) whose values e2m1 x e4m3 approximate x * gsi.  Per row m and
+// 16-value block b, in binary32, each operation rounded to nearest even and
+// none fused:
+//   amax = max |x|;  s = (amax / 6) * gsi;  sf = E4M3(s) (nearest, ties to
+//   even, saturating at 448);  r = gsi / e4m3(sf) (0 if the scale is 0);
+//   code = E2M1(x * r) (nearest, ties to the even code, saturating at 6; a
+//   value that rounds to zero is stored as +0).
+//
+// HBM-bound: one thread per position (row r, block kb) of the padded scale
+// layout, roundup(M, 128) x roundup(K / 16, 4) positions, kb fastest, so a
+// warp's activation loads (32 bytes each) and code stores (8 bytes each)
+// are contiguous; positions in the padding write a zero scale byte only.
+// Optionally the exact dequantised values e2m1 x e4m3 (bf16, no global
+// scale) go to x_deq, the operand of the W4A4 GEMM.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+
+namespace fp4 {
+
+constexpr int kQuantThreads = 256;
+
+// Nearest E2M1 magnitude code of a >= 0: midpoints go to the even code
+// (0.25 -> 0, 0.75 -> 2, 1.25 -> 2, 1.75 -> 4, 2.5 -> 4, 3.5 -> 6, 5 -> 6),
+// everything above 5 to 6 (code 7).
+__device__ __forceinline__ uint32_t e2m1_mag_code(float a) {
+  return a <= 0.25f ? 0u : a < 0.75f ? 1u : a <= 1.25f ? 2u : a < 1.75f ? 3u : a <= 2.5f ? 4u
+       : a < 3.5f ? 5u : a <= 5.0f ? 6u : 7u;
+}
+
+__device__ __forceinline__ uint32_t e2m1_code(float v) {
+  const uint32_t c = e2m1_mag_code(fabsf(v));
+  return (v < 0.0f && c != 0u) ? (c | 8u) : c;
+}
+
+// E2M1 code -> value (exact in float).
+__device__ __forceinline__ float e2m1_value(uint32_t c) {
+  const uint32_t m = c & 7u;  // 0, 0.5 (subnormal), then 2^(m / 2 - 1) x (1 or 1.5)
+  const float mag = m < 2u ? 0.5f * static_cast<float>(m)
+                           : static_cast<float>(1u << (m / 2u - 1u)) * ((m & 1u) ? 1.5f : 1.0f);
+  return (c & 8u) ? -mag : mag;
+}
+
+// Nearest finite E4M3 byte of s >= 0 (round to nearest even, saturating).
+__device__ __forceinline__ uint32_t e4m3_code(float s) {
+  unsigned short d;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %1;" : "=h"(d) : "f"(s));
+  return d & 0xFFu;
+}
+
+__device__ __forceinline__ float e4m3_value(uint32_t b) {
+  unsigned int h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(static_cast<unsigned short>(b & 0xFFu)));
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(h & 0xFFFFu)));
+}
+
+__global__ void __launch_bounds__(kQuantThreads) quantize_act_kernel(const uint16_t* __restrict__ x, int64_t ldx,
+                                                                    const float* __restrict__ gsi_p,
+                                                                    uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
+                                                                    uint16_t* __restrict__ x_deq, int M, int K,
+                                                                    uint32_t kbp, uint64_t npos) {
+  const float gsi = __ldg(gsi_p);
+  const int kb_used = K / 16;
+  for (uint64_t pos = static_cast<uint64_t>(blockIdx.x) * kQuantThreads + threadIdx.x; pos < npos;
+       pos += static_cast<uint64_t>(gridDim.x) * kQuantThreads) {
+    const uint32_t r = static_cast<uint32_t>(pos / kbp), kb = static_cast<uint32_t>(pos % kbp);
+    const uint32_t soff = ((r >> 7) * (kbp >> 2) + (kb >> 2)) * 512u + (r & 31u) * 16u + ((r & 127u) >> 5) * 4u +
+                          (kb & 3u);
+    if (r >= static_cast<uint32_t>(M) || kb >= static_cast<uint32_t>(kb_used)) {
+      sf[soff] = 0;  // padding of the 128x4 layout
+      continue;
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(r) * ldx + 16 * kb);
+    const uint4 a = __ldcs(src), b = __ldcs(src + 1);
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    float v[16];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[2 * i] = __uint_as_float(w[i] << 16);
+      v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      amax = fmaxf(amax, fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1])));
+    }
+    const float s = __fmul_rn(__fdiv_rn(amax, 6.0f), gsi);
+    const uint32_t sc = e4m3_code(s);
+    const float e = e4m3_value(sc);
+    const float rcp = e > 0.0f ? __fdiv_rn(gsi, e) : 0.0f;
+    uint32_t codes[2] = {0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t c = e > 0.0f ? e2m1_code(__fmul_rn(v[i], rcp)) : 0u;
+      codes[i / 8] |= c << (4 * (i % 8));
+    }
+    *reinterpret_cast<uint2*>(q + static_cast<int64_t>(r) * (K / 2) + 8 * kb) = make_uint2(codes[0], codes[1]);
+    sf[soff] = static_cast<uint8_t>(sc);
+    if (x_deq) {
+      uint32_t o[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float d0 = e2m1_value((codes[i / 4] >> (8 * (i % 4))) & 0xFu) * e;
+        const float d1 = e2m1_value((codes[i / 4] >> (8 * (i % 4) + 4)) & 0xFu) * e;
+        o[i] = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(d0))) |
+               (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(d1))) << 16);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(x_deq + static_cast<int64_t>(r) * K + 16 * kb);
+      dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+      dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+  }
+}
+
+// x_deq [M, K] bf16 = e2m1 x e4m3 of an NVFP4 activation tensor (exact; no
+// global scale): the W4A4 GEMM's operand when its caller passes codes and
+// scales.  One thread per 16-value block, kb fastest.
+__global__ void __launch_bounds__(kQuantThreads) dequantize_act_kernel(const uint8_t* __restrict__ q,
+                                                                      const uint8_t* __restrict__ sf,
+                                                                      uint16_t* __restrict__ x_deq, int K,
+                                                                      uint32_t kbp, uint64_t nblk) {
+  const uint32_t kb_used = static_cast<uint32_t>(K / 16);
+  for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * kQuantThreads + threadIdx.x; i < nblk;
+       i += static_cast<uint64_t>(gridDim.x) * kQuantThreads) {
+    const uint32_t r = static_cast<uint32_t>(i / kb_used), kb = static_cast<uint32_t>(i % kb_used);
+    const uint32_t soff = ((r >> 7) * (kbp >> 2) + (kb >> 2)) * 512u + (r & 31u) * 16u + ((r & 127u) >> 5) * 4u +
+                          (kb & 3u);
+    const float e = e4m3_value(__ldg(sf + soff));
+    const uint2 c = __ldg(reinterpret_cast<const uint2*>(q + static_cast<int64_t>(r) * (K / 2) + 8 * kb));
+    const uint32_t codes[2] = {c.x, c.y};
+    uint32_t o[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float d0 = e2m1_value((codes[j / 4] >> (8 * (j % 4))) & 0xFu) * e;
+      const float d1 = e2m1_value((codes[j / 4] >> (8 * (j % 4) + 4)) & 0xFu) * e;
+      o[j] = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(d0))) |
+             (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(d1))) << 16);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(x_deq + static_cast<int64_t>(r) * K + 16 * kb);
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
+}  // namespace fp4

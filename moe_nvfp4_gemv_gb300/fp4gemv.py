@@ -58,6 +58,10 @@ def _load() -> ctypes.CDLL:
         "fp4gemv_moe_down_combine_workspace_bytes": (sz, [i32, i32, i32]),
         "fp4gemv_moe_down_combine": (i32, [vp, vp, vp, i32, i32, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp, i32,
                                            vp, vp, sz, i32, vp]),
+        "fp4gemv_w4a4_workspace_bytes": (sz, [i32, i32]),
+        "fp4gemv_quantize_act": (i32, [vp, i64, vp, vp, vp, i32, i32, vp]),
+        "fp4gemv_w4a4_gemm": (i32, [vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, vp, sz, i32, vp]),
+        "fp4gemv_w4a4_linear": (i32, [vp, i64, vp, vp, vp, vp, vp, i64, i32, i32, i32, vp, vp, vp, sz, i32, vp]),
         "fp4gemv_get_device_error": (i32, [vp]),
         "fp4gemv_status_string": (ctypes.c_char_p, [i32]),
         "fp4gemv_set_wait_limit_ns": (i32, [ctypes.c_uint64]),
@@ -233,6 +237,69 @@ def dequant_gemm(x: torch.Tensor, weight: torch.Tensor, weight_scale: torch.Tens
     _check(_lib.fp4gemv_dequant_gemm(_ptr(x), x.stride(0), _ptr(w), _ptr(_bytes(weight_scale)),
                                      _ptr(global_scale.reshape(1)), _ptr(w_bf16), _ptr(out), out.stride(0), M, N, K,
                                      1, _stream(x.device)), "fp4gemv_dequant_gemm")
+    return out
+
+
+def quantize_act(x: torch.Tensor, input_global_scale_inv: torch.Tensor, x_fp4: torch.Tensor | None = None,
+                 x_sf: torch.Tensor | None = None) -> tuple[torch.Tensor, torch.Tensor]:
+    """scaled_fp4_quant of the W4A4 path: bf16 [M, K] -> (uint8 codes [M, K / 2],
+    uint8 flat 128x4 block scales of scale_bytes(M, K) bytes); the arithmetic
+    is stated in include/fp4gemv.h."""
+    x = _rows_bf16(x, "x")
+    M, K = x.shape
+    if x_fp4 is None:
+        x_fp4 = torch.empty(M, K // 2, dtype=_U8, device=x.device)
+    if x_sf is None:
+        x_sf = torch.empty(scale_bytes(M, K), dtype=_U8, device=x.device)
+    _check(_lib.fp4gemv_quantize_act(_ptr(x), x.stride(0), _ptr(input_global_scale_inv.reshape(1)), _ptr(x_fp4),
+                                     _ptr(x_sf), M, K, _stream(x.device)), "fp4gemv_quantize_act")
+    return x_fp4, x_sf
+
+
+def w4a4_workspace_bytes(M: int, K: int) -> int:
+    return int(_lib.fp4gemv_w4a4_workspace_bytes(M, K))
+
+
+def w4a4_gemm(x_fp4: torch.Tensor, x_sf: torch.Tensor, weight: torch.Tensor, weight_scale: torch.Tensor,
+              alpha: torch.Tensor, out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+              pdl: bool = True) -> torch.Tensor:
+    """The W4A4 GEMM: bf16(fp32(xq @ wq.T) * alpha) of NVFP4 activations and weights."""
+    xq = _bytes(x_fp4)
+    M, K = xq.shape[0], xq.shape[1] * 2
+    w = _bytes(weight)
+    N = w.shape[0]
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=xq.device)
+    if workspace is None:
+        workspace = torch.empty(w4a4_workspace_bytes(M, K), dtype=_U8, device=xq.device)
+    _check(_lib.fp4gemv_w4a4_gemm(_ptr(xq), _ptr(_bytes(x_sf)), _ptr(w), _ptr(_bytes(weight_scale)),
+                                  _ptr(alpha.reshape(1)), _ptr(out), out.stride(0), M, N, K, _ptr(workspace),
+                                  workspace.numel(), int(pdl), _stream(xq.device)), "fp4gemv_w4a4_gemm")
+    return out
+
+
+def w4a4_linear(x: torch.Tensor, input_global_scale_inv: torch.Tensor, weight: torch.Tensor,
+                weight_scale: torch.Tensor, alpha: torch.Tensor, out: torch.Tensor | None = None,
+                x_fp4: torch.Tensor | None = None, x_sf: torch.Tensor | None = None,
+                workspace: torch.Tensor | None = None, pdl: bool = True) -> torch.Tensor:
+    """quantize_act then w4a4_gemm in one call (the quantiser also writes the
+    dequantised activations the GEMM reads)."""
+    x = _rows_bf16(x, "x")
+    M, K = x.shape
+    w = _bytes(weight)
+    N = w.shape[0]
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=x.device)
+    if x_fp4 is None:
+        x_fp4 = torch.empty(M, K // 2, dtype=_U8, device=x.device)
+    if x_sf is None:
+        x_sf = torch.empty(scale_bytes(M, K), dtype=_U8, device=x.device)
+    if workspace is None:
+        workspace = torch.empty(w4a4_workspace_bytes(M, K), dtype=_U8, device=x.device)
+    _check(_lib.fp4gemv_w4a4_linear(_ptr(x), x.stride(0), _ptr(input_global_scale_inv.reshape(1)), _ptr(w),
+                                    _ptr(_bytes(weight_scale)), _ptr(alpha.reshape(1)), _ptr(out), out.stride(0), M,
+                                    N, K, _ptr(x_fp4), _ptr(x_sf), _ptr(workspace), workspace.numel(), int(pdl),
+                                    _stream(x.device)), "fp4gemv_w4a4_linear")
     return out
 
 

@@ -131,5 +131,22 @@ def test_moe_host_validation(fp4):
                                       a[9], 1536, a[10], a[11], 1 << 24, 1, None) == 1
 
 
+def test_w4a4_host_validation(fp4):
+    vp = ctypes.c_void_p
+    L = fp4.lib()
+    z = vp(0)
+    assert fp4.w4a4_workspace_bytes(3, 512) == 3 * 512 * 2 and fp4.w4a4_workspace_bytes(0, 512) == 0
+    # quantize_act: ldx < K, then K % 16, then misaligned x, then a null pointer
+    assert L.fp4gemv_quantize_act(z, 8, z, z, z, 1, 16, None) == 1
+    assert L.fp4gemv_quantize_act(z, 24, z, z, z, 1, 24, None) == 2
+    assert L.fp4gemv_quantize_act(vp(A16 + 2), 16, z, z, z, 1, 16, None) == 3
+    assert L.fp4gemv_quantize_act(z, 16, z, z, z, 1, 16, None) == 1
+    # w4a4_gemm: K < 256, then the workspace too small, then a null pointer
+    assert L.fp4gemv_w4a4_gemm(z, z, z, z, z, z, 16, 1, 16, 128, z, 1 << 20, 1, None) == 2
+    assert L.fp4gemv_w4a4_gemm(z, z, z, z, z, z, 16, 4, 16, 256, z, 1024, 1, None) == 1
+    assert L.fp4gemv_w4a4_gemm(z, z, z, z, z, z, 16, 4, 16, 256, z, 1 << 20, 1, None) == 1
+    assert L.fp4gemv_w4a4_linear(z, 256, z, z, z, z, z, 16, 4, 16, 256, z, z, z, 1 << 20, 2, None) == 1
+
+
 def test_launch_counter_starts_at_zero_without_launches(fp4):
     assert fp4.launch_count() >= 0
