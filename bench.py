@@ -533,8 +533,9 @@ def config_results(dev, compact=True):
     """Every configuration besides the default step, L2-cold (weights rotated
     over >= 400 MB of replicas, MoE over 8 routings): the 70B layers and
     their dequantize_rows, the 8B layers with BF16 weights, the MoE block,
-    and the N = K = 8192 sweep of the GEMV against dequantize + GEMM (with
-    `compact`, the sweep at M = 1, 8, 32, 128 only)."""
+    the N = K = 8192 sweep of the GEMV against dequantize + GEMM (with
+    `compact`, the sweep at M = 1, 8, 32, 128 only) and the W4A4 path on
+    that layer."""
     from moe_nvfp4_gemv_gb300 import fp4gemv
     stream = torch.cuda.current_stream(dev)
     peak, peak_kind = read_peaks()
@@ -678,7 +679,39 @@ def config_results(dev, compact=True):
     rows_m = [int(m) for m in sw]
     cross = next((m for m in rows_m if sw[str(m)]["dequant_gemm_us"] < sw[str(m)]["gemv_us"]), None)
     res["sweep_8192"] = {"rows": sw, "crossover_M": cross}
-    del ws, wbs, wb
+    del wbs, wb
+
+    # W4A4 on the same layer: quantise the activations, then the NVFP4 x NVFP4
+    # GEMM (w4a4_linear: one quantisation launch writing codes, scales and
+    # the exact dequantised operand, then the GEMM launches), against the
+    # W4A16 GEMV of the sweep; and the quantisation alone on an 8192 x 8192
+    # activation block (HBM-bound: larger than L2, so every call is cold)
+    gsi_v = 448.0 * 6 / 4.0
+    gsi = torch.tensor([gsi_v], dtype=torch.float32, device=dev)
+    alpha = torch.tensor([GS / gsi_v], dtype=torch.float32, device=dev)
+    w4 = {}
+    for M in ((1, 32, 128) if compact else (1, 8, 32, 128, 512)):
+        x = synth.activations(M, K, seed=M, device=dev)
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        xq = torch.empty(M, K // 2, dtype=torch.uint8, device=dev)
+        xsf = torch.empty(fp4gemv.scale_bytes(M, K), dtype=torch.uint8, device=dev)
+        wsp = torch.empty(fp4gemv.w4a4_workspace_bytes(M, K), dtype=torch.uint8, device=dev)
+        fns = [lambda w=w, sf=sf: fp4gemv.w4a4_linear(x, gsi, w, sf, alpha, out=out, x_fp4=xq, x_sf=xsf,
+                                                      workspace=wsp) for w, sf in ws]
+        us_l = time_calls(fns, 20, stream)
+        us_q = time_calls([lambda: fp4gemv.quantize_act(x, gsi, x_fp4=xq, x_sf=xsf)], 20, stream)
+        w4[str(M)] = {"w4a4_linear_us": round(us_l, 2), "quantize_us": round(us_q, 2),
+                      "w4a16_gemv_us": sw[str(M)]["gemv_us"] if str(M) in sw else None}
+    Mq = 8192
+    xl = synth.activations(Mq, K, seed=3, device=dev)
+    ql = torch.empty(Mq, K // 2, dtype=torch.uint8, device=dev)
+    sfl = torch.empty(fp4gemv.scale_bytes(Mq, K), dtype=torch.uint8, device=dev)
+    us_big = time_calls([lambda: fp4gemv.quantize_act(xl, gsi, x_fp4=ql, x_sf=sfl)], 10, stream)
+    bq = Mq * K * 2 + Mq * K // 2 + fp4gemv.scale_bytes(Mq, K)
+    res["w4a4_8192"] = {"rows": w4, "quantize_8192x8192": {
+        "us": round(us_big, 2), "GB/s": round(bq / (us_big * 1e-6) / 1e9, 1),
+        "frac": round(bq / (us_big * 1e-6) / 1e9 / peak, 3), "bytes": bq}}
+    del ws, xl, ql, sfl
     assert fp4gemv.get_device_error() == 0
     return res
 
@@ -733,7 +766,8 @@ def decode_chain(dev, gs, peak, Ms=(1, 4, 8)):
 def run_profile_case(spec):
     """A few launches of one case, for ncu captures: LAYER:M[:bf16] with
     LAYER in qkv, o_proj, gate_up, down; moe:M; dequantize_rows:N (N x N);
-    sweep_gemm:M (dequantize + GEMM, N = K = 8192)."""
+    sweep_gemm:M (dequantize + GEMM, N = K = 8192); quantize:M (the W4A4
+    activation quantisation of M x 8192)."""
     from moe_nvfp4_gemv_gb300 import fp4gemv
     dev = torch.device("cuda", 0)
     parts = spec.split(":")
@@ -756,6 +790,13 @@ def run_profile_case(spec):
         out = torch.empty(N, N, dtype=torch.bfloat16, device=dev)
         for _ in range(4):
             fp4gemv.dequantize_rows(w, sf, out=out)
+    elif parts[0] == "quantize":
+        # the W4A4 activation quantisation of M x 8192 bf16 activations
+        K = synth.SWEEP_NK
+        x = synth.activations(M, K, seed=1, device=dev)
+        g = torch.tensor([448.0 * 6 / 4.0], dtype=torch.float32, device=dev)
+        for _ in range(4):
+            fp4gemv.quantize_act(x, g)
     elif parts[0] == "moe":
         c = synth.MOE
         E, H, I, SI, topk = c["E"], c["H"], c["I"], c["SI"], c["topk"]

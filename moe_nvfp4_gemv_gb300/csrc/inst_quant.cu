@@ -23,11 +23,13 @@ cudaError_t launch_quantize_act(const void* x, int64_t ldx, const float* gsi, ui
                                 int M, int K, cudaStream_t stream) {
   const uint32_t kbp = static_cast<uint32_t>(((K / 16) + 3) / 4 * 4);
   const uint64_t npos = static_cast<uint64_t>((M + 127) / 128 * 128) * kbp;
+  if (npos >= (1ull << 31)) return cudaErrorInvalidValue;  // (32-bit positions)
   unsigned ctas = 0;
   cudaError_t e = grid_for(npos, &ctas);
   if (e != cudaSuccess) return e;
   quantize_act_kernel<<<ctas, kQuantThreads, 0, stream>>>(static_cast<const uint16_t*>(x), ldx, gsi, q, sf,
-                                                         static_cast<uint16_t*>(x_deq), M, K, kbp, npos);
+                                                         static_cast<uint16_t*>(x_deq), M, K, kbp,
+                                                         static_cast<uint32_t>(npos));
   return cudaGetLastError();
 }
 
@@ -35,10 +37,12 @@ cudaError_t launch_dequantize_act(const uint8_t* q, const uint8_t* sf, void* x_d
                                   cudaStream_t stream) {
   const uint32_t kbp = static_cast<uint32_t>(((K / 16) + 3) / 4 * 4);
   const uint64_t nblk = static_cast<uint64_t>(M) * (K / 16);
+  if (nblk >= (1ull << 31)) return cudaErrorInvalidValue;  // (32-bit positions)
   unsigned ctas = 0;
   cudaError_t e = grid_for(nblk, &ctas);
   if (e != cudaSuccess) return e;
-  dequantize_act_kernel<<<ctas, kQuantThreads, 0, stream>>>(q, sf, static_cast<uint16_t*>(x_deq), K, kbp, nblk);
+  dequantize_act_kernel<<<ctas, kQuantThreads, 0, stream>>>(q, sf, static_cast<uint16_t*>(x_deq), K, kbp,
+                                                           static_cast<uint32_t>(nblk));
   return cudaGetLastError();
 }
 

@@ -18,6 +18,9 @@
 // layout, roundup(M, 128) x roundup(K / 16, 4) positions, kb fastest, so a
 // warp's activation loads (32 bytes each) and code stores (8 bytes each)
 // are contiguous; positions in the padding write a zero scale byte only.
+// The E2M1 and E4M3 roundings are the conversion instructions' (round to
+// nearest even, saturating to the largest finite value), the divisions
+// IEEE-rounded (__fdiv_rn), the products __fmul_rn (no contraction).
 // Optionally the exact dequantised values e2m1 x e4m3 (bf16, no global
 // scale) go to x_deq, the operand of the W4A4 GEMM.
 #pragma once
@@ -32,17 +35,22 @@ namespace fp4 {
 
 constexpr int kQuantThreads = 256;
 
-// Nearest E2M1 magnitude code of a >= 0: midpoints go to the even code
-// (0.25 -> 0, 0.75 -> 2, 1.25 -> 2, 1.75 -> 4, 2.5 -> 4, 3.5 -> 6, 5 -> 6),
-// everything above 5 to 6 (code 7).
-__device__ __forceinline__ uint32_t e2m1_mag_code(float a) {
-  return a <= 0.25f ? 0u : a < 0.75f ? 1u : a <= 1.25f ? 2u : a < 1.75f ? 3u : a <= 2.5f ? 4u
-       : a < 3.5f ? 5u : a <= 5.0f ? 6u : 7u;
-}
-
-__device__ __forceinline__ uint32_t e2m1_code(float v) {
-  const uint32_t c = e2m1_mag_code(fabsf(v));
-  return (v < 0.0f && c != 0u) ? (c | 8u) : c;
+// Eight floats -> eight E2M1 codes (element i in nibble i) with the
+// conversion instruction (round to nearest even, saturating at 6), then
+// every zero magnitude stored as +0: a nibble's magnitude plus 7 sets its bit
+// 3 exactly when the magnitude is not zero (no carry leaves the nibble).
+__device__ __forceinline__ uint32_t e2m1x8_codes(const float* v) {
+  uint32_t w;
+  asm("{ .reg .b8 t0, t1, t2, t3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t3, %8, %7;\n\t"
+      "mov.b32 %0, {t0, t1, t2, t3}; }"
+      : "=r"(w)
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+  const uint32_t nz = ((w & 0x77777777u) + 0x77777777u) & 0x88888888u;
+  return w & (0x77777777u | nz);
 }
 
 // E2M1 code -> value (exact in float).
@@ -70,12 +78,14 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_act_kernel(const uint1
                                                                     const float* __restrict__ gsi_p,
                                                                     uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
                                                                     uint16_t* __restrict__ x_deq, int M, int K,
-                                                                    uint32_t kbp, uint64_t npos) {
+                                                                    uint32_t kbp, uint32_t npos) {
+  // (the GEMM launched after this grid may start now and stream its weights;
+  // it reads this grid's outputs only after waiting for the grid to end)
+  if (threadIdx.x == 0) pdl_launch_dependents();
   const float gsi = __ldg(gsi_p);
   const int kb_used = K / 16;
-  for (uint64_t pos = static_cast<uint64_t>(blockIdx.x) * kQuantThreads + threadIdx.x; pos < npos;
-       pos += static_cast<uint64_t>(gridDim.x) * kQuantThreads) {
-    const uint32_t r = static_cast<uint32_t>(pos / kbp), kb = static_cast<uint32_t>(pos % kbp);
+  for (uint32_t pos = blockIdx.x * kQuantThreads + threadIdx.x; pos < npos; pos += gridDim.x * kQuantThreads) {
+    const uint32_t r = pos / kbp, kb = pos - r * kbp;
     const uint32_t soff = ((r >> 7) * (kbp >> 2) + (kb >> 2)) * 512u + (r & 31u) * 16u + ((r & 127u) >> 5) * 4u +
                           (kb & 3u);
     if (r >= static_cast<uint32_t>(M) || kb >= static_cast<uint32_t>(kb_used)) {
@@ -97,12 +107,10 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_act_kernel(const uint1
     const uint32_t sc = e4m3_code(s);
     const float e = e4m3_value(sc);
     const float rcp = e > 0.0f ? __fdiv_rn(gsi, e) : 0.0f;
-    uint32_t codes[2] = {0u, 0u};
+    float sv[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint32_t c = e > 0.0f ? e2m1_code(__fmul_rn(v[i], rcp)) : 0u;
-      codes[i / 8] |= c << (4 * (i % 8));
-    }
+    for (int i = 0; i < 16; ++i) sv[i] = __fmul_rn(v[i], rcp);  // (rcp = 0: all +-0, codes 0)
+    const uint32_t codes[2] = {e2m1x8_codes(sv), e2m1x8_codes(sv + 8)};
     *reinterpret_cast<uint2*>(q + static_cast<int64_t>(r) * (K / 2) + 8 * kb) = make_uint2(codes[0], codes[1]);
     sf[soff] = static_cast<uint8_t>(sc);
     if (x_deq) {
@@ -127,11 +135,11 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_act_kernel(const uint1
 __global__ void __launch_bounds__(kQuantThreads) dequantize_act_kernel(const uint8_t* __restrict__ q,
                                                                       const uint8_t* __restrict__ sf,
                                                                       uint16_t* __restrict__ x_deq, int K,
-                                                                      uint32_t kbp, uint64_t nblk) {
+                                                                      uint32_t kbp, uint32_t nblk) {
   const uint32_t kb_used = static_cast<uint32_t>(K / 16);
-  for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * kQuantThreads + threadIdx.x; i < nblk;
-       i += static_cast<uint64_t>(gridDim.x) * kQuantThreads) {
-    const uint32_t r = static_cast<uint32_t>(i / kb_used), kb = static_cast<uint32_t>(i % kb_used);
+  if (threadIdx.x == 0) pdl_launch_dependents();
+  for (uint32_t i = blockIdx.x * kQuantThreads + threadIdx.x; i < nblk; i += gridDim.x * kQuantThreads) {
+    const uint32_t r = i / kb_used, kb = i - r * kb_used;
     const uint32_t soff = ((r >> 7) * (kbp >> 2) + (kb >> 2)) * 512u + (r & 31u) * 16u + ((r & 127u) >> 5) * 4u +
                           (kb & 3u);
     const float e = e4m3_value(__ldg(sf + soff));
