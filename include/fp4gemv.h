@@ -153,9 +153,11 @@ size_t fp4gemv_w4a4_workspace_bytes(int M, int K);
 /* scaled_fp4_quant as read above.  x bf16 [M, ldx >= K] (16-byte aligned,
  * ldx * 2 % 16 == 0); gsi fp32 [1] device (> 0, finite; x finite); x_fp4
  * [M, K / 2] (8-byte aligned) and x_sf (fp4gemv_scale_bytes(M, K) bytes)
- * device, written.  Shapes: M >= 1, K % 16 == 0.  One launch. */
+ * device, written; x_deq: NULL, or bf16 [M, K] device (16-byte aligned)
+ * that receives the exact dequantised values e2m1 * e4m3 (no global scale).
+ * Shapes: M >= 1, K % 16 == 0.  One launch. */
 fp4gemv_status fp4gemv_quantize_act(const void* x, int64_t ldx, const float* gsi, uint8_t* x_fp4, uint8_t* x_sf,
-                                    int M, int K, cudaStream_t stream);
+                                    void* x_deq, int M, int K, cudaStream_t stream);
 
 /* The W4A4 GEMM on quantised activations (x_fp4, x_sf as written by
  * fp4gemv_quantize_act) and NVFP4 weights (w, w_sf as for

@@ -1045,15 +1045,16 @@ size_t fp4gemv_w4a4_workspace_bytes(int M, int K) {
 }
 
 fp4gemv_status fp4gemv_quantize_act(const void* x, int64_t ldx, const float* gsi, uint8_t* x_fp4, uint8_t* x_sf,
-                                    int M, int K, cudaStream_t stream) {
+                                    void* x_deq, int M, int K, cudaStream_t stream) {
   if (M < 1 || K < 1 || ldx < K) return FP4GEMV_ERR_INVALID_ARG;
   if (K % 16 != 0) return FP4GEMV_ERR_UNSUPPORTED_SHAPE;
-  if (!aligned(x, 16) || (ldx * 2) % 16 != 0 || !aligned(x_fp4, 8) || !aligned(gsi, 4)) return FP4GEMV_ERR_MISALIGNED;
+  if (!aligned(x, 16) || (ldx * 2) % 16 != 0 || !aligned(x_fp4, 8) || !aligned(gsi, 4) || !aligned(x_deq, 16))
+    return FP4GEMV_ERR_MISALIGNED;
   if (!x || !gsi || !x_fp4 || !x_sf) return FP4GEMV_ERR_INVALID_ARG;
   fp4gemv_status st = device_state(nullptr, nullptr);
   if (st != FP4GEMV_OK) return st;
   g_launches.fetch_add(1, std::memory_order_relaxed);
-  return from_cuda(fp4::launch_quantize_act(x, ldx, gsi, x_fp4, x_sf, nullptr, M, K, stream));
+  return from_cuda(fp4::launch_quantize_act(x, ldx, gsi, x_fp4, x_sf, x_deq, M, K, stream));
 }
 
 namespace {

@@ -59,7 +59,7 @@ def _load() -> ctypes.CDLL:
         "fp4gemv_moe_down_combine": (i32, [vp, vp, vp, i32, i32, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp, i32,
                                            vp, vp, sz, i32, vp]),
         "fp4gemv_w4a4_workspace_bytes": (sz, [i32, i32]),
-        "fp4gemv_quantize_act": (i32, [vp, i64, vp, vp, vp, i32, i32, vp]),
+        "fp4gemv_quantize_act": (i32, [vp, i64, vp, vp, vp, vp, i32, i32, vp]),
         "fp4gemv_w4a4_gemm": (i32, [vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, vp, sz, i32, vp]),
         "fp4gemv_w4a4_linear": (i32, [vp, i64, vp, vp, vp, vp, vp, i64, i32, i32, i32, vp, vp, vp, sz, i32, vp]),
         "fp4gemv_get_device_error": (i32, [vp]),
@@ -241,18 +241,23 @@ def dequant_gemm(x: torch.Tensor, weight: torch.Tensor, weight_scale: torch.Tens
 
 
 def quantize_act(x: torch.Tensor, input_global_scale_inv: torch.Tensor, x_fp4: torch.Tensor | None = None,
-                 x_sf: torch.Tensor | None = None) -> tuple[torch.Tensor, torch.Tensor]:
+                 x_sf: torch.Tensor | None = None,
+                 x_deq: torch.Tensor | None = None) -> tuple[torch.Tensor, torch.Tensor]:
     """scaled_fp4_quant of the W4A4 path: bf16 [M, K] -> (uint8 codes [M, K / 2],
     uint8 flat 128x4 block scales of scale_bytes(M, K) bytes); the arithmetic
-    is stated in include/fp4gemv.h."""
+    is stated in include/fp4gemv.h.  ``x_deq`` (bf16 [M, K], optional)
+    receives the exact dequantised values."""
     x = _rows_bf16(x, "x")
     M, K = x.shape
     if x_fp4 is None:
         x_fp4 = torch.empty(M, K // 2, dtype=_U8, device=x.device)
     if x_sf is None:
         x_sf = torch.empty(scale_bytes(M, K), dtype=_U8, device=x.device)
+    if x_deq is not None and (x_deq.dtype != torch.bfloat16 or not x_deq.is_contiguous() or
+                              tuple(x_deq.shape) != (M, K)):
+        raise ValueError("x_deq must be a contiguous bf16 [M, K] tensor")
     _check(_lib.fp4gemv_quantize_act(_ptr(x), x.stride(0), _ptr(input_global_scale_inv.reshape(1)), _ptr(x_fp4),
-                                     _ptr(x_sf), M, K, _stream(x.device)), "fp4gemv_quantize_act")
+                                     _ptr(x_sf), _ptr(x_deq), M, K, _stream(x.device)), "fp4gemv_quantize_act")
     return x_fp4, x_sf
 
 

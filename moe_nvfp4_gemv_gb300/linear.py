@@ -17,6 +17,13 @@ gate_up_silu_mul) over this library's kernels:
 * Fused gate/up projections (``[gate | up]`` halves of N): ``gate_up_silu_mul``
   returns ``bf16(silu(G) * U)`` from one GEMV for small M, else None (the
   caller runs the linear and its own silu_and_mul).
+* W4A4 (``NvFp4W4A4Linear``; the flashinfer page's W4A4 kernels,
+  apply_weights): the activations are quantised to NVFP4
+  (``fp4gemv.quantize_act``) and multiplied with the NVFP4 weight, alpha on
+  the fp32 accumulator -- ``fp4gemv.w4a4_linear`` up to ``MAX_M`` tokens;
+  beyond, the quantiser's exact dequantised activations times the
+  dequantized weight on cuBLAS (``torch.addmm``, alpha the host copy), one
+  weight pass instead of one per 128 tokens.
 
 The pages route by tuned tables (``pick_nt`` / ``tuned``, contents not
 printed).  Here the library accepts every valid shape and picks its launch
@@ -175,3 +182,71 @@ class Bf16Linear(torch.nn.Module):
         if x.dim() != 2 or self.out_features % 32 != 0 or self.route(x.shape[0]) != "gemv":
             return None
         return fp4gemv.bf16_gemv(x, self.weight, silu_mul=True, pdl=self.pdl)
+
+
+class NvFp4W4A4Linear(torch.nn.Module):
+    """y = bf16(fp32(quant(x) @ dequant(W)^T) * alpha): the W4A4 linear of the
+    flashinfer page's NVFP4 kernels (apply_weights: scaled_fp4_quant(x,
+    input_global_scale_inv), then the NVFP4 GEMM with alpha).
+
+    weight / weight_scale as for ``NvFp4Linear`` (flat, unpadded scales);
+    input_global_scale_inv and alpha: fp32 [1] on the weight's device (alpha
+    = the activation's 1 / input_global_scale_inv times the weight's global
+    scale).  Up to ``MAX_M`` tokens the library's W4A4 call; beyond, the
+    quantiser's exactly dequantised activations and the dequantized weight on
+    cuBLAS with alpha applied to the fp32 accumulator (the same products, so
+    the same numbers up to the order of the fp32 sums).  ``last_codes``
+    holds the latest call's NVFP4 activations (codes, scales)."""
+
+    def __init__(self, weight: torch.Tensor, weight_scale: torch.Tensor, input_global_scale_inv: torch.Tensor,
+                 alpha: torch.Tensor, pdl: bool = True):
+        super().__init__()
+        if weight.dtype != torch.uint8 or weight.dim() != 2 or not weight.is_contiguous():
+            raise ValueError("weight must be a contiguous uint8 [N, K/2] tensor")
+        N, K = weight.shape[0], weight.shape[1] * 2
+        sf = fp4gemv.flat_scale_buffer(weight_scale)
+        if sf.numel() < fp4gemv.scale_bytes(N, K):
+            raise ValueError(f"weight_scale must hold at least {fp4gemv.scale_bytes(N, K)} bytes")
+        for name, t in (("input_global_scale_inv", input_global_scale_inv), ("alpha", alpha)):
+            if t.dtype != torch.float32 or t.numel() != 1:
+                raise ValueError(f"{name} must be one float32 value")
+        self.register_buffer("weight", weight, persistent=False)
+        self.register_buffer("weight_scale", sf, persistent=False)
+        self.register_buffer("input_global_scale_inv", input_global_scale_inv.reshape(1), persistent=False)
+        self.register_buffer("alpha", alpha.reshape(1), persistent=False)
+        self.alpha_host = float(alpha.reshape(()).item())  # alpha of the cuBLAS path
+        self.out_features, self.in_features = N, K
+        self.pdl = bool(pdl)
+        self.last_codes = None
+
+    def route(self, m: int) -> str:
+        """'empty', 'w4a4' (the library's call) or 'dequant_gemm' (cuBLAS)."""
+        if m == 0:
+            return "empty"
+        return "w4a4" if m <= MAX_M else "dequant_gemm"
+
+    def forward(self, x: torch.Tensor) -> torch.Tensor:
+        x2 = x.reshape(-1, x.shape[-1])
+        m, K = x2.shape
+        route = self.route(m)
+        if route == "empty":
+            return x2.new_empty(*x.shape[:-1], self.out_features)
+        xq = torch.empty(m, K // 2, dtype=torch.uint8, device=x2.device)
+        xsf = torch.empty(fp4gemv.scale_bytes(m, K), dtype=torch.uint8, device=x2.device)
+        if route == "w4a4":
+            out = fp4gemv.w4a4_linear(x2, self.input_global_scale_inv, self.weight, self.weight_scale, self.alpha,
+                                      x_fp4=xq, x_sf=xsf, pdl=self.pdl)
+        else:
+            xd = torch.empty(m, K, dtype=torch.bfloat16, device=x2.device)
+            fp4gemv.quantize_act(x2, self.input_global_scale_inv, x_fp4=xq, x_sf=xsf, x_deq=xd)
+            w = fp4gemv.dequantize_rows(self.weight, self.weight_scale)
+            out = torch.empty(m, self.out_features, dtype=torch.bfloat16, device=x2.device)
+            matmul = torch.backends.cuda.matmul
+            prev = matmul.allow_bf16_reduced_precision_reduction
+            matmul.allow_bf16_reduced_precision_reduction = False  # fp32 split-K sums
+            try:
+                torch.addmm(out, xd, w.t(), beta=0, alpha=self.alpha_host, out=out)
+            finally:
+                matmul.allow_bf16_reduced_precision_reduction = prev
+        self.last_codes = (xq, xsf)
+        return out.view(*x.shape[:-1], self.out_features)

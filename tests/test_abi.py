@@ -137,10 +137,10 @@ def test_w4a4_host_validation(fp4):
     z = vp(0)
     assert fp4.w4a4_workspace_bytes(3, 512) == 3 * 512 * 2 and fp4.w4a4_workspace_bytes(0, 512) == 0
     # quantize_act: ldx < K, then K % 16, then misaligned x, then a null pointer
-    assert L.fp4gemv_quantize_act(z, 8, z, z, z, 1, 16, None) == 1
-    assert L.fp4gemv_quantize_act(z, 24, z, z, z, 1, 24, None) == 2
-    assert L.fp4gemv_quantize_act(vp(A16 + 2), 16, z, z, z, 1, 16, None) == 3
-    assert L.fp4gemv_quantize_act(z, 16, z, z, z, 1, 16, None) == 1
+    assert L.fp4gemv_quantize_act(z, 8, z, z, z, z, 1, 16, None) == 1
+    assert L.fp4gemv_quantize_act(z, 24, z, z, z, z, 1, 24, None) == 2
+    assert L.fp4gemv_quantize_act(vp(A16 + 2), 16, z, z, z, z, 1, 16, None) == 3
+    assert L.fp4gemv_quantize_act(z, 16, z, z, z, z, 1, 16, None) == 1
     # w4a4_gemm: K < 256, then the workspace too small, then a null pointer
     assert L.fp4gemv_w4a4_gemm(z, z, z, z, z, z, 16, 1, 16, 128, z, 1 << 20, 1, None) == 2
     assert L.fp4gemv_w4a4_gemm(z, z, z, z, z, z, 16, 4, 16, 256, z, 1024, 1, None) == 1

@@ -33,6 +33,10 @@ def test_routes():
     assert lin2.route(47) == "gemv" and lin2.route(48) == "dequant_gemm"
     b = linear.Bf16Linear(torch.zeros(64, 128, dtype=torch.bfloat16), gemv_max_m=16)
     assert (b.route(0), b.route(16), b.route(17)) == ("empty", "gemv", "cublas")
+    w4 = linear.NvFp4W4A4Linear(synth.fp4_bytes(256, 512, seed=1), synth.e4m3_bytes(oracle.scale_bytes(256, 512),
+                                                                                       seed=2),
+                                torch.tensor([30.0]), torch.tensor([0.001]))
+    assert (w4.route(0), w4.route(1), w4.route(128), w4.route(129)) == ("empty", "w4a4", "w4a4", "dequant_gemm")
 
 
 def test_argument_checks():
@@ -182,3 +186,25 @@ def test_padded_scales_dequantize_rows_and_linear():
         x = synth.activations(M, K, seed=M)
         ref = oracle.nvfp4_gemv(_u16(x), w.numpy(), sf.numpy(), 0.01)
         assert oracle.check(_u16(lin(x.cuda())), ref)[0], M
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("M", [3, 128, 300])
+def test_w4a4_linear_routes_match_oracle(M):
+    # the library's W4A4 call up to 128 tokens, cuBLAS on the dequantised
+    # operands beyond: both against the oracle's quantiser and GEMM
+    if not torch.cuda.is_available():
+        pytest.fail("GPU test run without a CUDA device")
+    N, K = 384, 1024
+    w = synth.fp4_bytes(N, K, seed=5)
+    sf = synth.e4m3_bytes(oracle.scale_bytes(N, K), seed=6)
+    gsi, wgs = 448.0 * 6 / 5.0, 0.02
+    alpha = float(np.float32(wgs / gsi))
+    lin = linear.NvFp4W4A4Linear(w.cuda(), sf.cuda(), torch.tensor([gsi]).cuda(), torch.tensor([alpha]).cuda())
+    x = synth.activations(M, K, seed=M)
+    y = lin(x.cuda())
+    xq, xsf = oracle.quantize_act(_u16(x), gsi)
+    assert np.array_equal(lin.last_codes[0].cpu().numpy(), xq)
+    assert np.array_equal(lin.last_codes[1].cpu().numpy(), xsf)
+    ok, excess, nbad, _ = oracle.check(_u16(y), oracle.w4a4_gemm(xq, xsf, w.numpy(), sf.numpy(), alpha))
+    assert ok, f"{lin.route(M)} M={M}: {nbad} outside tolerance (excess {excess})"

@@ -134,12 +134,16 @@ def test_noalloc_chained_layers_under_pdl():
     assert fp4gemv.get_device_error() == 0
 
 
-def test_back_to_back_down_combine_share_a_workspace():
+# (8 tokens over 32 experts: one CTA per item, one wave; 16 tokens over 128
+# experts: the persistent grid, whose work counter each call restarts)
+@pytest.mark.parametrize("M,E", [(8, 32), (16, 128)])
+def test_back_to_back_down_combine_share_a_workspace(M, E):
     # Consecutive down_combine launches with PDL and one workspace: each
-    # call's arrival counting must finish before the next call retags the
-    # counters.  Every output is compared with its own isolated run.
+    # call's counters (abort tags, the persistent grid's work counter) must be
+    # out of use before the next call claims them.  Every output is compared
+    # with its own isolated run.
     fp4gemv = _fp4()
-    M, E, H, I, SI, topk = 8, 32, 2048, 512, 512, 8
+    H, I, SI, topk = 2048, 512, 512, 8
     ins = [{k: v.to(DEV) for k, v in _down_inputs(M, E, H, I, SI, topk, seed).items()} for seed in (21, 22, 23, 24)]
     ws = torch.empty(fp4gemv.moe_down_combine_workspace_bytes(M, topk, H), dtype=torch.uint8, device=DEV)
     iso = []
