@@ -173,7 +173,9 @@ fp4gemv_status fp4gemv_w4a4_gemm(const uint8_t* x_fp4, const uint8_t* x_sf, cons
 /* Quantisation and GEMM in one call: fp4gemv_quantize_act into x_fp4 / x_sf,
  * whose kernel also writes the exact dequantised activations into
  * `workspace`, then the GEMM of fp4gemv_w4a4_gemm on them (no second pass
- * over the codes).  Arguments and shapes as those two calls. */
+ * over the codes).  Arguments and shapes as those two calls; with pdl = 1
+ * the quantisation launch is also early (it waits for the previous grid
+ * before reading x). */
 fp4gemv_status fp4gemv_w4a4_linear(const void* x, int64_t ldx, const float* gsi, const uint8_t* w,
                                    const uint8_t* w_sf, const float* alpha, void* out, int64_t ldo, int M, int N,
                                    int K, uint8_t* x_fp4, uint8_t* x_sf, void* workspace, size_t workspace_bytes,

@@ -1054,7 +1054,7 @@ fp4gemv_status fp4gemv_quantize_act(const void* x, int64_t ldx, const float* gsi
   fp4gemv_status st = device_state(nullptr, nullptr);
   if (st != FP4GEMV_OK) return st;
   g_launches.fetch_add(1, std::memory_order_relaxed);
-  return from_cuda(fp4::launch_quantize_act(x, ldx, gsi, x_fp4, x_sf, x_deq, M, K, stream));
+  return from_cuda(fp4::launch_quantize_act(x, ldx, gsi, x_fp4, x_sf, x_deq, M, K, 0, stream));
 }
 
 namespace {
@@ -1116,7 +1116,7 @@ fp4gemv_status fp4gemv_w4a4_linear(const void* x, int64_t ldx, const float* gsi,
   st = device_state(nullptr, nullptr);
   if (st != FP4GEMV_OK) return st;
   g_launches.fetch_add(1, std::memory_order_relaxed);
-  st = from_cuda(fp4::launch_quantize_act(x, ldx, gsi, x_fp4, x_sf, workspace, M, K, stream));
+  st = from_cuda(fp4::launch_quantize_act(x, ldx, gsi, x_fp4, x_sf, workspace, M, K, pdl, stream));
   if (st != FP4GEMV_OK) return st;
   return w4a4_gemm_on(static_cast<const uint16_t*>(workspace), w, w_sf, alpha, out, ldo, M, N, K, pdl, stream);
 }

@@ -20,17 +20,26 @@ static cudaError_t grid_for(uint64_t items, unsigned* ctas) {
 }
 
 cudaError_t launch_quantize_act(const void* x, int64_t ldx, const float* gsi, uint8_t* q, uint8_t* sf, void* x_deq,
-                                int M, int K, cudaStream_t stream) {
+                                int M, int K, int pdl, cudaStream_t stream) {
   const uint32_t kbp = static_cast<uint32_t>(((K / 16) + 3) / 4 * 4);
   const uint64_t npos = static_cast<uint64_t>((M + 127) / 128 * 128) * kbp;
   if (npos >= (1ull << 31)) return cudaErrorInvalidValue;  // (32-bit positions)
   unsigned ctas = 0;
   cudaError_t e = grid_for(npos, &ctas);
   if (e != cudaSuccess) return e;
-  quantize_act_kernel<<<ctas, kQuantThreads, 0, stream>>>(static_cast<const uint16_t*>(x), ldx, gsi, q, sf,
-                                                         static_cast<uint16_t*>(x_deq), M, K, kbp,
-                                                         static_cast<uint32_t>(npos));
-  return cudaGetLastError();
+  // with pdl, launched early (programmatic stream serialisation): the kernel
+  // waits for the previous grid before it reads anything
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(ctas, 1, 1);
+  lc.blockDim = dim3(kQuantThreads, 1, 1);
+  lc.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = &attr;
+  lc.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&lc, quantize_act_kernel, static_cast<const uint16_t*>(x), ldx, gsi, q, sf,
+                            static_cast<uint16_t*>(x_deq), M, K, kbp, static_cast<uint32_t>(npos));
 }
 
 cudaError_t launch_dequantize_act(const uint8_t* q, const uint8_t* sf, void* x_deq, int M, int K,

@@ -82,6 +82,7 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_act_kernel(const uint1
   // (the GEMM launched after this grid may start now and stream its weights;
   // it reads this grid's outputs only after waiting for the grid to end)
   if (threadIdx.x == 0) pdl_launch_dependents();
+  pdl_wait();  // x (and gsi) may come from the previous grid
   const float gsi = __ldg(gsi_p);
   const int kb_used = K / 16;
   for (uint32_t pos = blockIdx.x * kQuantThreads + threadIdx.x; pos < npos; pos += gridDim.x * kQuantThreads) {

@@ -52,7 +52,7 @@ cudaError_t slab_moe_regs(int mode, int* regs);
 cudaError_t launch_moe_combine(const GemvParams& p, const LaunchCfg& cfg);
 cudaError_t launch_moe_down_persist(const GemvParams& p, const LaunchCfg& cfg);
 cudaError_t launch_quantize_act(const void* x, int64_t ldx, const float* gsi, uint8_t* q, uint8_t* sf, void* x_deq,
-                                int M, int K, cudaStream_t stream);
+                                int M, int K, int pdl, cudaStream_t stream);
 cudaError_t launch_dequantize_act(const uint8_t* q, const uint8_t* sf, void* x_deq, int M, int K,
                                   cudaStream_t stream);
 // Clusters of `cluster` slab-kernel CTAs (cw consumer warps, `smem` bytes of
