@@ -105,3 +105,30 @@ def test_w4a4_linear_llama8b_gate_up_sampled(fp4):
     ref = oracle.w4a4_gemm(xq, xsf, w.numpy(), wsf.numpy(), alpha, rows=rows)
     assert_close(u16(out)[:, rows], ref, "w4a4 gate_up M=128 (sampled rows)")
     assert fp4.get_device_error() == 0
+
+
+def _random_shapes():
+    rng = np.random.default_rng(44)
+    return [(int(rng.integers(1, 301)), 16 * int(rng.integers(1, 65)), 64 * int(rng.integers(4, 33))) for _ in range(8)]
+
+
+@pytest.mark.parametrize("M,N,K", _random_shapes())
+def test_w4a4_random_shapes(fp4, M, N, K):
+    # seeded random shapes: codes and scales bit-exact, outputs (sampled rows
+    # past 256 features) under the tolerance, through w4a4_linear
+    x = act_inputs(M, K, seed=M * 7 + K, kind="wide" if M % 2 else "normal")
+    w = synth.fp4_bytes(N, K, seed=N + K)
+    wsf = synth.e4m3_bytes(oracle.scale_bytes(N, K), seed=N + K + 1)
+    gsi = float(2.0 ** (M % 7 - 2))
+    alpha = float(np.float32(0.01 / gsi))
+    q = torch.empty(M, K // 2, dtype=torch.uint8, device=DEV)
+    sf = torch.empty(oracle.scale_bytes(M, K), dtype=torch.uint8, device=DEV)
+    out = fp4.w4a4_linear(x.to(DEV), torch.tensor([gsi], device=DEV), w.to(DEV), wsf.to(DEV),
+                          torch.tensor([alpha], device=DEV), x_fp4=q, x_sf=sf)
+    xq, xsf = oracle.quantize_act(u16(x), gsi)
+    assert np.array_equal(q.cpu().numpy(), xq) and np.array_equal(sf.cpu().numpy(), xsf)
+    rows = None if N <= 256 else sample_rows(N, 40, seed=M)
+    ref = oracle.w4a4_gemm(xq, xsf, w.numpy(), wsf.numpy(), alpha, rows=rows)
+    got = u16(out) if rows is None else u16(out)[:, rows]
+    assert_close(got, ref, f"w4a4 random M={M} N={N} K={K}")
+    assert fp4.get_device_error() == 0
