@@ -6,14 +6,16 @@
 
 namespace fp4 {
 
-static cudaError_t grid_for(uint64_t items, unsigned* ctas) {
+// CTAs for `items` threads' work, at most `per_sm` resident CTAs per SM
+// (the grid-stride loops then start every CTA at once).
+static cudaError_t grid_for(uint64_t items, int per_sm, unsigned* ctas) {
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   uint64_t n = (items + kQuantThreads - 1) / kQuantThreads;
-  const uint64_t cap = static_cast<uint64_t>(sms) * 8;  // 8 x 256 threads per SM
+  const uint64_t cap = static_cast<uint64_t>(sms) * per_sm;
   if (n > cap) n = cap;
   *ctas = static_cast<unsigned>(n < 1 ? 1 : n);
   return cudaSuccess;
@@ -25,7 +27,7 @@ cudaError_t launch_quantize_act(const void* x, int64_t ldx, const float* gsi, ui
   const uint64_t npos = static_cast<uint64_t>((M + 127) / 128 * 128) * kbp;
   if (npos >= (1ull << 31)) return cudaErrorInvalidValue;  // (32-bit positions)
   unsigned ctas = 0;
-  cudaError_t e = grid_for(npos, &ctas);
+  cudaError_t e = grid_for((npos + 1) / 2, 4, &ctas);  // (two positions per thread; 57 registers: 4 CTAs per SM)
   if (e != cudaSuccess) return e;
   // with pdl, launched early (programmatic stream serialisation): the kernel
   // waits for the previous grid before it reads anything
@@ -48,7 +50,7 @@ cudaError_t launch_dequantize_act(const uint8_t* q, const uint8_t* sf, void* x_d
   const uint64_t nblk = static_cast<uint64_t>(M) * (K / 16);
   if (nblk >= (1ull << 31)) return cudaErrorInvalidValue;  // (32-bit positions)
   unsigned ctas = 0;
-  cudaError_t e = grid_for(nblk, &ctas);
+  cudaError_t e = grid_for(nblk, 8, &ctas);
   if (e != cudaSuccess) return e;
   dequantize_act_kernel<<<ctas, kQuantThreads, 0, stream>>>(q, sf, static_cast<uint16_t*>(x_deq), K, kbp,
                                                            static_cast<uint32_t>(nblk));

@@ -84,17 +84,8 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_act_kernel(const uint1
   if (threadIdx.x == 0) pdl_launch_dependents();
   pdl_wait();  // x (and gsi) may come from the previous grid
   const float gsi = __ldg(gsi_p);
-  const int kb_used = K / 16;
-  for (uint32_t pos = blockIdx.x * kQuantThreads + threadIdx.x; pos < npos; pos += gridDim.x * kQuantThreads) {
-    const uint32_t r = pos / kbp, kb = pos - r * kbp;
-    const uint32_t soff = ((r >> 7) * (kbp >> 2) + (kb >> 2)) * 512u + (r & 31u) * 16u + ((r & 127u) >> 5) * 4u +
-                          (kb & 3u);
-    if (r >= static_cast<uint32_t>(M) || kb >= static_cast<uint32_t>(kb_used)) {
-      sf[soff] = 0;  // padding of the 128x4 layout
-      continue;
-    }
-    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(r) * ldx + 16 * kb);
-    const uint4 a = __ldcs(src), b = __ldcs(src + 1);
+  const uint32_t kb_used = static_cast<uint32_t>(K / 16);
+  auto quant_block = [&](uint32_t r, uint32_t kb, uint32_t soff, const uint4& a, const uint4& b) {
     const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
     float v[16];
     float amax = 0.0f;
@@ -126,6 +117,34 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_act_kernel(const uint1
       uint4* dst = reinterpret_cast<uint4*>(x_deq + static_cast<int64_t>(r) * K + 16 * kb);
       dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
       dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+  };
+  // two positions per thread and iteration, both loads issued first (64
+  // bytes in flight per thread)
+  const uint32_t stride = gridDim.x * kQuantThreads;
+  for (uint32_t pos0 = blockIdx.x * kQuantThreads + threadIdx.x; pos0 < npos; pos0 += 2 * stride) {
+    uint32_t r[2], kb[2], soff[2];
+    bool live[2];
+    uint4 a[2], b[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const uint32_t pos = pos0 + u * stride;  // (< 2^31 + 2 stride: no wrap)
+      r[u] = pos / kbp;
+      kb[u] = pos - r[u] * kbp;
+      soff[u] = ((r[u] >> 7) * (kbp >> 2) + (kb[u] >> 2)) * 512u + (r[u] & 31u) * 16u + ((r[u] & 127u) >> 5) * 4u +
+                (kb[u] & 3u);
+      live[u] = pos < npos && r[u] < static_cast<uint32_t>(M) && kb[u] < kb_used;
+      if (live[u]) {
+        const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(r[u]) * ldx + 16 * kb[u]);
+        a[u] = __ldcs(src);
+        b[u] = __ldcs(src + 1);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      if (pos0 + u * stride >= npos) break;
+      if (live[u]) quant_block(r[u], kb[u], soff[u], a[u], b[u]);
+      else sf[soff[u]] = 0;  // padding of the 128x4 layout
     }
   }
 }
