@@ -27,7 +27,9 @@ cudaError_t launch_quantize_act(const void* x, int64_t ldx, const float* gsi, ui
   const uint64_t npos = static_cast<uint64_t>((M + 127) / 128 * 128) * kbp;
   if (npos >= (1ull << 31)) return cudaErrorInvalidValue;  // (32-bit positions)
   unsigned ctas = 0;
-  cudaError_t e = grid_for((npos + 1) / 2, 4, &ctas);  // (two positions per thread; 57 registers: 4 CTAs per SM)
+  // one thread per position up to four 256-thread CTAs per SM (57 registers);
+  // past that the grid-stride loop takes two positions per iteration
+  cudaError_t e = grid_for(npos, 4, &ctas);
   if (e != cudaSuccess) return e;
   // with pdl, launched early (programmatic stream serialisation): the kernel
   // waits for the previous grid before it reads anything
