@@ -401,6 +401,25 @@ def test_down_combine_persistent(fp4, M, topk, E, H, I, SI, T):
     assert torch.equal(outs[0], outs[1])
 
 
+def test_down_combine_persistent_crowded_experts(fp4):
+    # The persistent grid's plan assumes uniform routing; here 32 tokens send
+    # their 8 pairs to 12 of 128 experts (each of those gets ~21 pairs: two
+    # or three full chunks of 8), so items of 8 activation rows and experts
+    # split over several columns meet most columns being inactive duplicates.
+    M, topk, E, H, I, SI = 32, 8, 128, 1024, 512, 512
+    p = _down_slab_plan(fp4, M, topk, E, H, I, SI)
+    assert p is not None and p.persistent == 1
+    g = torch.Generator().manual_seed(5)
+    hot = torch.randperm(E, generator=g)[:12]
+    ids = torch.stack([hot[torch.randperm(12, generator=g)[:topk]] for _ in range(M)])
+    d = make_moe(M, E=E, H=H, I=I, SI=SI, topk=topk, seed=1400, ids=ids)
+    out = run_down(fp4, d)
+    ref, bad = ref_down(d)
+    assert bad == 0
+    assert_close(u16(out), ref, "down persistent crowded")
+    assert fp4.get_device_error() == 0
+
+
 def test_down_combine_slab_decode_block_one_token(fp4):
     # one token of the E = 128, top-8, H = 4096, I = SI = 1536 block: one row
     # tile per CTA at two CTAs per SM (288 CTAs, one wave), then the combine
