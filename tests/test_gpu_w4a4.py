@@ -132,3 +132,29 @@ def test_w4a4_random_shapes(fp4, M, N, K):
     got = u16(out) if rows is None else u16(out)[:, rows]
     assert_close(got, ref, f"w4a4 random M={M} N={N} K={K}")
     assert fp4.get_device_error() == 0
+
+
+def test_w4a4_linear_chained_under_pdl(fp4):
+    # w4a4_linear right after the GEMV that writes its input, both with PDL:
+    # the quantisation (launched early) must wait for that GEMV's outputs.
+    # Chained results equal the same calls run one by one, bit for bit.
+    M, K, N = 4, 1024, 512
+    x = act_inputs(M, K, seed=3, kind="normal").to(DEV)
+    w1 = synth.fp4_bytes(K, K, seed=21).to(DEV)
+    s1 = synth.e4m3_bytes(oracle.scale_bytes(K, K), seed=22).to(DEV)
+    w2 = synth.fp4_bytes(N, K, seed=23).to(DEV)
+    s2 = synth.e4m3_bytes(oracle.scale_bytes(N, K), seed=24).to(DEV)
+    gs = torch.tensor([0.05], device=DEV)
+    gsi = torch.tensor([448.0 * 6 / 8.0], device=DEV)
+    alpha = torch.tensor([0.02 / (448.0 * 6 / 8.0)], device=DEV)
+    h_iso = fp4.nvfp4_gemv(x, w1, s1, gs, pdl=False)
+    torch.cuda.synchronize()
+    y_iso = fp4.w4a4_linear(h_iso, gsi, w2, s2, alpha, pdl=False)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        h = torch.full((M, K), 9.0, dtype=torch.bfloat16, device=DEV)
+        fp4.nvfp4_gemv(x, w1, s1, gs, out=h, pdl=True)
+        y = fp4.w4a4_linear(h, gsi, w2, s2, alpha, pdl=True)
+        torch.cuda.synchronize()
+        assert torch.equal(h, h_iso) and torch.equal(y, y_iso)
+    assert fp4.get_device_error() == 0
