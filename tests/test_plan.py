@@ -517,6 +517,24 @@ def test_down_slab_plan_matches_rule(down_slab_fn, M, topk, E, H, I, SI):
     assert sum(sizes) == tiles and max(sizes) == p.tiles_per_cta and max(sizes) - min(sizes) <= 1
 
 
+@pytest.mark.parametrize("topk,E,H,I,SI", [(8, 128, 4096, 1536, 1536), (8, 256, 7168, 2048, 2048),
+                                           (2, 8, 4096, 14336, 14336), (4, 64, 2048, 768, 1536)])
+def test_down_slab_plan_matches_rule_every_m(down_slab_fn, topk, E, H, I, SI):
+    # every token count 1 .. 64 (grid form, persistent form and the switch
+    # between them, chunks of 4 or 8), and no plan past 64 tokens
+    for M in range(1, 66):
+        st, p = down_slab_fn(M, topk, E, H, I, SI)
+        want = down_slab_rule(M, topk, E, H, I, SI)
+        if want is None:
+            assert st == 2, M
+            continue
+        assert st == 0, M
+        got = dict(tiles_per_cta=p.tiles_per_cta, groups=p.groups, chunk_pairs=p.chunk_pairs,
+                   slab_bytes=p.slab_bytes, stages=p.stages, ctas_per_sm=p.ctas_per_sm, persistent=p.persistent,
+                   smem_bytes=p.smem_bytes)
+        assert got == want, M
+
+
 def test_down_slab_plan_decode_block(down_slab_fn):
     # E = 128, top-8, H = 4096, I = SI = 1536: one token, one tile per CTA at
     # two CTAs per SM (its 288 CTAs in one wave); 8 tokens, the persistent
