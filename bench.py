@@ -767,7 +767,7 @@ def run_profile_case(spec):
     """A few launches of one case, for ncu captures: LAYER:M[:bf16] with
     LAYER in qkv, o_proj, gate_up, down; moe:M; dequantize_rows:N (N x N);
     sweep_gemm:M (dequantize + GEMM, N = K = 8192); quantize:M (the W4A4
-    activation quantisation of M x 8192)."""
+    activation quantisation of M x 8192); w4a4:M (w4a4_linear, N = K = 8192)."""
     from moe_nvfp4_gemv_gb300 import fp4gemv
     dev = torch.device("cuda", 0)
     parts = spec.split(":")
@@ -797,6 +797,16 @@ def run_profile_case(spec):
         g = torch.tensor([448.0 * 6 / 4.0], dtype=torch.float32, device=dev)
         for _ in range(4):
             fp4gemv.quantize_act(x, g)
+    elif parts[0] == "w4a4":
+        # w4a4_linear on the N = K = 8192 layer at M tokens (quantisation, then the GEMM)
+        N = K = synth.SWEEP_NK
+        x = synth.activations(M, K, seed=1, device=dev)
+        w = synth.fp4_bytes(N, K, seed=1, device=dev)
+        sf = synth.e4m3_bytes(fp4gemv.scale_bytes(N, K), seed=2, device=dev)
+        g = torch.tensor([448.0 * 6 / 4.0], dtype=torch.float32, device=dev)
+        a = torch.tensor([GS / (448.0 * 6 / 4.0)], dtype=torch.float32, device=dev)
+        for _ in range(4):
+            fp4gemv.w4a4_linear(x, g, w, sf, a)
     elif parts[0] == "moe":
         c = synth.MOE
         E, H, I, SI, topk = c["E"], c["H"], c["I"], c["SI"], c["topk"]
